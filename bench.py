@@ -1,0 +1,499 @@
+#!/usr/bin/env python3
+"""Benchmark of the block-speculative-decoding hot path on GB300.
+
+Headline workload (one step = the whole path of a decode step at B=1):
+    spec_draft_block (gamma=15, V=248320, rank-256 Markov bias, T=0)
+  + spec_verify      (16 target rows, T=0)
+on seeded synthetic logits (see verify_spec_draft_gb300/synth.py, configuration 3).
+Metric: verify rows per second over the whole draft+verify step, with the step's
+microseconds alongside, and the dominant kernel's fraction of the HBM roofline.
+
+Secondary numbers measured in the same run (not separate bench lines):
+    verify T=1 at B=32, gamma=7, V=248320 (configuration 4), rows/s and HBM fraction;
+    E2E-TV over 16x64x7 rows, V=248320 (configuration 5), tokens/s and HBM fraction.
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 run it under torch.distributed.run; every rank processes its own
+independent requests (weak scaling, no collective on the data path).
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verify rows/s (V-wide) + % HBM roofline; draft+verify µs @B1 γ15 V248320"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 512 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-secondary", action="store_true", help="skip the configuration 4 and 5 numbers")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------------
+# clocks sampled while the GPU works
+# ---------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+        self.active = False
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append((self.active, parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        busy = [p for a, p in self.samples if a] or [p for _, p in self.samples]
+        if not busy:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[0]) for p in busy if num(p[0]) is not None]
+        smax = [num(p[1]) for p in busy if num(p[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in busy for i in range(4) if p[4 + i].lower().startswith("active")})
+        power = [num(p[2]) for p in busy if num(p[2]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(busy), "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------------------------
+# our implementation
+# ---------------------------------------------------------------------------------
+def capture(fn, torch):
+    """CUDA-graph capture of a call sequence; falls back to eager replay."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="thread_local"):
+            fn()
+        torch.cuda.synchronize()
+        return g.replay, True
+    except Exception as e:  # noqa: BLE001
+        print(f"[bench] graph capture failed ({e}); timing eager calls", file=sys.stderr)
+        torch.cuda.synchronize()
+        return fn, False
+
+
+def time_steps(torch, replay, steps, flush=None, parts=None):
+    """Per-step CUDA-event times (ms) on the current stream.  ``parts`` is a list of
+    callables making up the step, each timed on its own; ``flush`` runs between steps
+    outside the events."""
+    parts = parts or [replay]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(parts) + 1)] for _ in range(steps)]
+    for k in range(steps):
+        if flush is not None:
+            flush()
+        evs[k][0].record()
+        for i, p in enumerate(parts):
+            p()
+            evs[k][i + 1].record()
+    torch.cuda.synchronize()
+    per_part = [[evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(steps)] for i in range(len(parts))]
+    total = [evs[k][0].elapsed_time(evs[k][-1]) for k in range(steps)]
+    return total, per_part
+
+
+def run_ours(args, rank, world, torch, dist):
+    import verify_spec_draft_gb300 as vsd
+    from verify_spec_draft_gb300 import synth
+
+    vsd.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    hbm, hbm_kind = peaks()
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+
+    # ---- headline: configuration 3 (B=1, gamma=15, V=248320, r=256), draft + verify, T=0
+    inp = synth.config_inputs(3, device=dev)
+    c = inp["cfg"]
+    B, G, V, r = c.B, c.gamma, c.V, c.r
+    L, tgt, U, Wt, anchor = inp["draft"], inp["target"], inp["U"], inp["Wt"], inp["anchor"]
+    ws_d = vsd.workspace(vsd.OP_DRAFT, B, G, V, r, dev)
+    ws_v = vsd.workspace(vsd.OP_VERIFY, B, G, V, 0, dev)
+    out_d = dict(tokens=torch.empty((B, G), dtype=torch.int32, device=dev),
+                 conf=torch.empty((B, G), dtype=torch.float32, device=dev),
+                 qtok=torch.empty((B, G), dtype=torch.float32, device=dev),
+                 passes=torch.zeros((1,), dtype=torch.int32, device=dev))
+    out_v = dict(n=torch.empty((B,), dtype=torch.int32, device=dev),
+                 committed=torch.empty((B, G + 1), dtype=torch.int32, device=dev),
+                 bonus=torch.empty((B,), dtype=torch.int32, device=dev),
+                 near=torch.empty((B,), dtype=torch.int32, device=dev))
+
+    def do_draft():
+        vsd.draft_block(L, anchor, U, Wt, 0, None, ws=ws_d, out=out_d)
+
+    def do_verify():
+        vsd.verify(tgt, None, out_d["tokens"], 0, None, ws=ws_v, out=out_v)
+
+    flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flush():
+        flush_buf.zero_()
+
+    g_draft, graphed_d = capture(do_draft, torch)
+    g_verify, graphed_v = capture(do_verify, torch)
+    for _ in range(args.warmup):
+        flush()
+        g_draft()
+        g_verify()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.active = True
+    t_wall = time.perf_counter()
+    total, (t_draft, t_verify) = time_steps(torch, None, args.steps, flush=flush, parts=[g_draft, g_verify])
+    t_wall = time.perf_counter() - t_wall
+    sampler.active = False
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms_step = sum(total) / len(total)
+    ms_draft = sum(t_draft) / len(t_draft)
+    ms_verify = sum(t_verify) / len(t_verify)
+    if world > 1:
+        t = torch.tensor([ms_step, ms_draft, ms_verify], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step, ms_draft, ms_verify = t.tolist()
+    passes = int(out_d["passes"].item())
+    rows = B * (G + 1)
+    # algorithmic bytes of one draft launch: the draft rows and Wt read once (plus the
+    # U rows of the gamma previous tokens); verify: the 16 target rows read once
+    draft_bytes = B * G * V * 2 + V * r * 2 + B * G * r * 2
+    verify_bytes = B * (G + 1) * V * 2
+    dominant = "draft" if ms_draft >= ms_verify else "verify"
+    dom_bytes, dom_ms = (draft_bytes, ms_draft) if dominant == "draft" else (verify_bytes, ms_verify)
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    n_acc = out_v["n"].cpu().tolist()
+
+    result = {
+        "metric": METRIC,
+        "value": rows * world / (ms_step * 1e-3),
+        "unit": "rows/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "draft_verify_us": ms_step * 1e3,
+        "draft_us": ms_draft * 1e3,
+        "verify_us": ms_verify * 1e3,
+        "verify_only_rows_per_s": rows / (ms_verify * 1e-3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16 storage, f32 accumulate",
+        "data": "synthetic (seeded zipf-skewed logits and N(0,0.02^2) Markov weights, shaped like the pages' workloads)",
+        "config": {
+            "workload": "latency: draft block + verify, B=1, gamma=15 (block 16), V=248320, r=256, T=0",
+            "B": B, "gamma": G, "V": V, "r": r, "temperature": 0,
+            "fixed_point_passes": passes,
+            "accepted_n": n_acc,
+            "cuda_graphs": bool(graphed_d and graphed_v),
+            "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write), outside the timed events",
+            "parallelism": f"replicas x{world} (independent requests per GPU, no collective)",
+        },
+        "roofline": {
+            "kernel": "spec::draft_kernel" if dominant == "draft" else "spec::verify_t0_kernel",
+            "bound": "hbm",
+            "achieved": achieved,
+            "peak": hbm,
+            "peak_kind": hbm_kind,
+            "unit": "GB/s",
+            "frac": achieved / hbm,
+            "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
+            "algorithmic_bytes_per_launch": dom_bytes,
+            "traffic": None,
+        },
+        "gpu_launches": 2 * args.steps,
+        "wall_s_timed_loop": t_wall,
+    }
+
+    # ---- end to end through the public API with host buffers (pinned), copies timed
+    if not args.no_e2e:
+        h_L = L.cpu().pin_memory()
+        h_t = tgt.cpu().pin_memory()
+        h_a = anchor.cpu().pin_memory()
+        d_L, d_t, d_a = torch.empty_like(L), torch.empty_like(tgt), torch.empty_like(anchor)
+        h_out = torch.empty((B * (G + 1) + 2 * B + B * G,), dtype=torch.int32).pin_memory()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        e2e_steps = min(args.steps, 200)
+
+        def e2e_step():
+            d_L.copy_(h_L, non_blocking=True)
+            d_t.copy_(h_t, non_blocking=True)
+            d_a.copy_(h_a, non_blocking=True)
+            vsd.draft_block(d_L, d_a, U, Wt, 0, None, ws=ws_d, out=out_d)
+            vsd.verify(d_t, None, out_d["tokens"], 0, None, ws=ws_v, out=out_v)
+            packed = torch.cat([out_v["n"], out_v["committed"].flatten(), out_v["bonus"], out_d["tokens"].flatten()])
+            h_out.copy_(packed, non_blocking=True)
+
+        for _ in range(5):
+            flush()
+            e2e_step()
+        torch.cuda.synchronize()
+        times = []
+        for _ in range(e2e_steps):
+            flush()
+            ev[0].record()
+            e2e_step()
+            ev[1].record()
+            ev[1].synchronize()
+            times.append(ev[0].elapsed_time(ev[1]))
+        ms_e2e = sum(times) / len(times)
+        result["e2e"] = {"value": rows * world / (ms_e2e * 1e-3), "unit": "rows/s", "us_per_step": ms_e2e * 1e3,
+                         "h2d_bytes_per_step": h_L.numel() * 2 + h_t.numel() * 2 + h_a.numel() * 4,
+                         "d2h_bytes_per_step": h_out.numel() * 4,
+                         "path": "pinned host buffers -> cudaMemcpyAsync -> spec_draft_block -> spec_verify -> "
+                                 "results to pinned host, eager C-ABI calls (Markov weights resident)"}
+    del flush_buf
+
+    # ---- secondary: verify T=1 at B=32 (configuration 4) and E2E-TV (configuration 5)
+    if not args.no_secondary:
+        result["secondary"] = secondary(args, torch, vsd, synth, dev, hbm, hbm_kind, sampler)
+
+    sampler.stop()
+    result["clocks"] = sampler.summary()
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(inp, budget_s=20.0)
+    return result
+
+
+def secondary(args, torch, vsd, synth, dev, hbm, hbm_kind, sampler):
+    out = {}
+    steps = max(5, min(args.steps, 50))
+    # configuration 4: verify T=1, B=32, gamma=7, V=248320; inputs 238 MB > L2
+    inp = synth.config_inputs(4, device=dev)
+    c = inp["cfg"]
+    B, G, V = c.B, c.gamma, c.V
+    t, d, seeds = inp["target"], inp["draft"], inp["seeds"]
+    tok = synth.draft_tokens(d, 1, seed=c.seed)
+    ws = vsd.workspace(vsd.OP_VERIFY, B, G, V, 0, dev)
+    o = dict(n=torch.empty((B,), dtype=torch.int32, device=dev),
+             committed=torch.empty((B, G + 1), dtype=torch.int32, device=dev),
+             bonus=torch.empty((B,), dtype=torch.int32, device=dev),
+             near=torch.empty((B,), dtype=torch.int32, device=dev))
+    fn, graphed = capture(lambda: vsd.verify(t, d, tok, 1, seeds, ws=ws, out=o), torch)
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    sampler.active = True
+    total, _ = time_steps(torch, fn, steps)
+    sampler.active = False
+    ms = sum(total) / len(total)
+    rows = B * (G + 1)
+    byts = (B * (G + 1) + B * G) * V * 2
+    ach = byts / (ms * 1e-3) / 1e9
+    out["verify_t1_b32"] = {
+        "workload": "verify T=1, B=32, gamma=7, V=248320, bf16, per-request seeds",
+        "value": rows / (ms * 1e-3), "unit": "rows/s", "us_per_step": ms * 1e3, "cuda_graphs": graphed,
+        "accepted_mean_n": float(o["n"].float().mean().item()),
+        "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "peak_kind": hbm_kind, "unit": "GB/s",
+                     "frac": ach / hbm, "frac_of_nominal_8tbs": ach / NOMINAL_HBM_GBS,
+                     "algorithmic_bytes_per_launch": byts},
+        "gpu_launches": 2 * steps,
+    }
+    del t, d, inp
+    torch.cuda.empty_cache()
+
+    # configuration 5: E2E-TV, 16 x 64 x 7 rows, V=248320; 7.1 GB of inputs
+    inp = synth.config_inputs(5, device=dev)
+    c = inp["cfg"]
+    N, Wb, V = c.B, c.gamma, c.V
+    t, d = inp["target"], inp["draft"]
+    ws = vsd.workspace(vsd.OP_E2ETV, N, Wb, V, 0, dev)
+    R = N * Wb
+    o = dict(a=torch.empty((R,), dtype=torch.float32, device=dev),
+             surv=torch.empty((R,), dtype=torch.float32, device=dev),
+             loss=torch.empty((1,), dtype=torch.float32, device=dev),
+             grad=torch.empty((R, V), dtype=torch.bfloat16, device=dev))
+    fn, graphed = capture(lambda: vsd.e2etv(t, d, N, Wb, ws=ws, out=o), torch)
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    steps5 = max(5, min(args.steps, 30))
+    sampler.active = True
+    total, _ = time_steps(torch, fn, steps5)
+    sampler.active = False
+    ms = sum(total) / len(total)
+    byts = 3 * R * V * 2
+    ach = byts / (ms * 1e-3) / 1e9
+    out["e2etv_cfg5"] = {
+        "workload": "E2E-TV, 16 refs x 64 anchors x Wb=7 = 7168 rows, V=248320, bf16 in/out",
+        "value": R / (ms * 1e-3), "unit": "supervised tokens/s", "ms_per_step": ms, "cuda_graphs": graphed,
+        "loss": float(o["loss"].item()),
+        "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "peak_kind": hbm_kind, "unit": "GB/s",
+                     "frac": ach / hbm, "frac_of_nominal_8tbs": ach / NOMINAL_HBM_GBS,
+                     "algorithmic_bytes_per_launch": byts},
+        "gpu_launches": steps5,
+    }
+    del t, d, inp, o
+    torch.cuda.empty_cache()
+    return out
+
+
+# ---------------------------------------------------------------------------------
+# CPU baseline: the float64 oracle, as it stands
+# ---------------------------------------------------------------------------------
+def oracle_step(L, anchor, U, Wt, tgt):
+    from oracle import draft as od, verify as ov
+    d = od.draft_block(L, anchor, U, Wt, 0, [0])
+    ov.verify(tgt, None, d["tokens"], 0, None)
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else 1
+    except Exception:
+        return int(os.environ.get("OPENBLAS_NUM_THREADS", os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1)))
+
+
+def cpu_baseline(inp, budget_s=20.0):
+    c = inp["cfg"]
+    L = inp["draft"].double().cpu().numpy()
+    tgt = inp["target"].double().cpu().numpy()
+    U = inp["U"].double().cpu().numpy()
+    Wt = inp["Wt"].double().cpu().numpy()
+    anchor = inp["anchor"].cpu().numpy()
+    done, t0 = 0, time.perf_counter()
+    while True:
+        oracle_step(L, anchor, U, Wt, tgt)
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or done >= 20:
+            break
+    rows = done * c.B * (c.gamma + 1)
+    return {"value": rows / el, "unit": "rows/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"{done} full draft+verify steps of the headline workload (float64 numpy oracle, "
+                      f"{el:.1f} s)", "host_cpus": os.cpu_count()}
+
+
+def run_reference(args, rank, world):
+    """The oracle timed on the host cores on the headline workload (bounded sample)."""
+    import torch
+    from verify_spec_draft_gb300 import synth
+    inp = synth.config_inputs(3, device="cpu")
+    c = inp["cfg"]
+    L = inp["draft"].double().numpy()
+    tgt = inp["target"].double().numpy()
+    U = inp["U"].double().numpy()
+    Wt = inp["Wt"].double().numpy()
+    anchor = inp["anchor"].numpy()
+    w = min(args.warmup, 1)
+    for _ in range(w):
+        oracle_step(L, anchor, U, Wt, tgt)
+    budget = 90.0
+    done, t0 = 0, time.perf_counter()
+    while done < args.steps:
+        oracle_step(L, anchor, U, Wt, tgt)
+        done += 1
+        if time.perf_counter() - t0 > budget:
+            break
+    el = time.perf_counter() - t0
+    rows = done * c.B * (c.gamma + 1)
+    v = rows / el
+    cores = blas_threads()
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": "rows/s", "n_gpus": world,
+            "steps": done, "warmup": w, "ms_per_step": el / done * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "latency: draft block + verify, B=1, gamma=15, V=248320, r=256, T=0",
+                       "B": c.B, "gamma": c.gamma, "V": c.V, "r": c.r},
+            "cpu_baseline": {"value": v, "unit": "rows/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{done} of {args.steps} requested steps (capped at {budget:.0f} s)"},
+            "e2e": {"value": v, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, rank, world)))
+        return
+    import torch
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        local = int(os.environ.get("LOCAL_RANK", "0"))
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the library has no CPU path)")
+    res = run_ours(args, rank, world, torch, dist)
+    if rank == 0:
+        print(json.dumps(res))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

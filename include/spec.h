@@ -1,0 +1,221 @@
+/*
+ * spec.h - C ABI of the GB300 (sm_103a) block-speculative-decoding hot path.
+ *
+ * Three operations on vocabulary-wide logit rows, each one or two CUDA kernels:
+ *
+ *   spec_draft_block  DSpark low-rank Markov logit bias + softmax + argmax/sample
+ *                     over a parallel drafter's gamma positions.
+ *   spec_verify       target verification of gamma draft tokens against gamma+1
+ *                     target rows: accepted length, committed tokens, bonus token.
+ *   spec_e2etv        SpecOPD E2E-TV surrogate: overlap 1-TV, prefix survival,
+ *                     mean loss and its gradient w.r.t. the draft logits.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Memory.   Every array argument is a DEVICE pointer owned by the caller.  The
+ *           library allocates nothing and keeps no per-call global state.
+ *           Scratch lives in a caller-supplied workspace (see below).
+ * Layout.   Row-major, contiguous.  A "row" is V consecutive elements.
+ * Dtypes.   Logits are float32 or bfloat16 (stored as raw 16-bit words); every
+ *           reduction accumulates in float32.  Tokens are int32 in [0, V).
+ * Align.    Every logits/weights base pointer must be 16-byte aligned (rejected
+ *           with SPEC_ERR_ALIGN otherwise).  V need not be a multiple of anything:
+ *           rows whose byte length is not a multiple of 16 take a scalar path.
+ * Streams.  Calls enqueue work on `stream` (a cudaStream_t; NULL = legacy default
+ *           stream) and never synchronise the host.
+ * Errors.   Argument errors are returned synchronously before anything is
+ *           enqueued.  A failed CUDA launch returns SPEC_ERR_CUDA.  Conditions met
+ *           on the device (a non-finite row, a token out of range, a bounded wait
+ *           that ran out) are OR-ed as flags into a status word inside the
+ *           workspace; read them with spec_get_device_status.  Affected requests
+ *           also get -1 outputs (see each call).
+ * Invalid rows.  A logit of -inf is a token of probability zero.  A row that holds
+ *           NaN or +inf, or no finite entry, has no distribution: the request that
+ *           reads it is reported with -1 tokens and the SPEC_DEV_NONFINITE flag.
+ * Workspace.  Query the size with spec_workspace_bytes, allocate it on the device,
+ *           and zero it ONCE with spec_workspace_init before its first use.  Every
+ *           call leaves it zeroed again (except the status word), so it can be
+ *           reused by later calls on the same stream.  Calls that run concurrently
+ *           need separate workspaces.  After a SPEC_DEV_TIMEOUT flag, run
+ *           spec_workspace_init again before reusing it.
+ * Randomness.  T=1 draws use Philox4x64-10 (Salmon et al., SC'11) with key
+ *           (seed_b, 0) and counter (b, j, stream, 0); the uniform is
+ *           (word0 >> 40) * 2^-24.  Streams: 0 draft sample, 1 accept test,
+ *           2 residual draw, 3 bonus draw.  Any call replays bit for bit.
+ * Sampling.  Single-uniform inverse CDF in vocabulary order: the smallest v with
+ *           C_v > u * Z (C_v running sum of the weights, Z their total).  Argmax
+ *           ties go to the lowest index.
+ */
+#ifndef SPEC_GB300_SPEC_H
+#define SPEC_GB300_SPEC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t (CUDA declares it as struct CUstream_st *). */
+struct CUstream_st;
+typedef struct CUstream_st *spec_stream_t;
+
+typedef enum {
+    SPEC_OK = 0,
+    SPEC_ERR_INVALID_ARG = 1, /* null pointer, bad temperature, bad op code        */
+    SPEC_ERR_SHAPE = 2,       /* a size outside the supported range               */
+    SPEC_ERR_DTYPE = 3,       /* unknown dtype code                               */
+    SPEC_ERR_ALIGN = 4,       /* a base pointer that is not 16-byte aligned       */
+    SPEC_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed             */
+    SPEC_ERR_TIMEOUT = 6,     /* device: a bounded wait gave up                   */
+    SPEC_ERR_NONFINITE = 7,   /* device: a row with NaN/+inf or no finite entry   */
+    SPEC_ERR_TOKEN = 8,       /* device: a token outside [0, V)                   */
+    SPEC_ERR_WORKSPACE = 9    /* workspace null or smaller than required          */
+} spec_status;
+
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
+
+typedef enum { SPEC_OP_DRAFT = 0, SPEC_OP_VERIFY = 1, SPEC_OP_E2ETV = 2 } spec_op;
+
+/* Device status flags (OR-ed into the workspace status word). */
+#define SPEC_DEV_TIMEOUT 1u
+#define SPEC_DEV_NONFINITE 2u
+#define SPEC_DEV_TOKEN 4u
+
+/* Supported ranges. */
+#define SPEC_MAX_GAMMA 64      /* draft positions per request                      */
+#define SPEC_MAX_RANK 256      /* Markov rank r                                    */
+#define SPEC_MAX_V (1 << 26)   /* vocabulary size                                  */
+
+/*
+ * spec_workspace_bytes - workspace size for one operation (host only, pure).
+ *   op     SPEC_OP_DRAFT / SPEC_OP_VERIFY: B requests, gamma positions, V, r.
+ *          SPEC_OP_E2ETV: B = number of branches, gamma = branch length Wb, r unused.
+ * Returns 0 for arguments outside the supported ranges.
+ */
+size_t spec_workspace_bytes(spec_op op, int B, int gamma, int V, int r);
+
+/* spec_workspace_init - zero `bytes` of workspace on `stream` (asynchronous). */
+spec_status spec_workspace_init(void *workspace, size_t bytes, spec_stream_t stream);
+
+/*
+ * spec_get_device_status - synchronise `stream`, read the workspace status word.
+ * Writes the raw SPEC_DEV_* flags to *flags_out (nullable) and returns SPEC_OK when
+ * no flag is set, else the status of the most severe flag (TIMEOUT, then TOKEN,
+ * then NONFINITE).  Flags stay set until spec_workspace_init.
+ */
+spec_status spec_get_device_status(const void *workspace, spec_stream_t stream,
+                                   uint32_t *flags_out);
+
+/* spec_status_string - static description of a status code. */
+const char *spec_status_string(spec_status status);
+
+/*
+ * spec_draft_block - DSpark block draft with the rank-r Markov logit bias.
+ *
+ * Defines ("Speculative Decoding Part 2", VESSL AI, DSpark section, bias equation;
+ * "Solar Open2 DSpark", sionic.ai, section 2): for request b and positions
+ * j = 1..gamma, with x_0 = anchor[b],
+ *     z_j = l_j + W_1[x_{j-1}] W_2          (W_1 = U [V, r], W_2 = Wt^T)
+ *     m = max z_j,  Z = sum_v exp(z_j,v - m),  c_j = 1/Z  (the max probability)
+ *     T=0: x_j = lowest index attaining m
+ *     T=1: x_j = inverse-CDF draw from softmax(z_j), u = Philox(seed_b; b, j, 0)
+ *     q_j(x_j) = exp(z_j,x_j - m) / Z
+ * computed exactly as this sequential recurrence defines it (the library solves it
+ * by fixed-point passes over all positions at once; the result is the sequential
+ * one).
+ *
+ *   draft_logits  [B, gamma, V], dtype logits_dtype; row (b, j-1) is l_j.
+ *   anchor        [B] int32, x_0 of each request.
+ *   U, Wt         [V, r] each, dtype w_dtype (both the same).  U row x is W_1[x];
+ *                 Wt row v is column v of W_2 (the nn.Linear(r, V) weight layout).
+ *                 r = 0 means no bias; U and Wt may then be NULL.
+ *   temperature   0 (argmax) or 1 (sample at temperature 1).
+ *   seeds         [B] uint64 Philox keys; required when temperature == 1.
+ *   tokens_out    [B, gamma] int32.
+ *   conf_out      [B, gamma] float32, c_j.
+ *   qtok_out      [B, gamma] float32, q_j(x_j) (nullable).
+ *   qlogits_out   [B, gamma, V] float32, the biased logits z_j the draws used
+ *                 (nullable; pass it to spec_verify as the T=1 draft rows).
+ *   passes_out    [1] int32, fixed-point passes over W used (nullable).
+ * A request whose anchor lies outside [0, V), or whose row j is invalid, gets
+ * tokens -1 and NaN statistics from that position on (flags TOKEN / NONFINITE).
+ * Limits: 1 <= gamma <= SPEC_MAX_GAMMA, 0 <= r <= SPEC_MAX_RANK, 1 <= V <= SPEC_MAX_V,
+ * 1 <= B*gamma <= 4096.
+ */
+spec_status spec_draft_block(const void *draft_logits, spec_dtype logits_dtype,
+                             const int32_t *anchor, const void *U, const void *Wt,
+                             spec_dtype w_dtype, int r, int B, int gamma, int V,
+                             int temperature, const uint64_t *seeds, int32_t *tokens_out,
+                             float *conf_out, float *qtok_out, float *qlogits_out,
+                             int32_t *passes_out, void *workspace, size_t workspace_bytes,
+                             spec_stream_t stream);
+
+/*
+ * spec_verify - verify gamma draft tokens against gamma+1 target rows.
+ *
+ * Defines ("Solar Open2 DSpark", sionic.ai, sections 1 and 6: one target forward
+ * over gamma+1 positions checks the drafts and commits the agreeing prefix;
+ * "Speculative Decoding Part 2", VESSL AI, blockwise decoding section: the longest
+ * matching prefix is accepted).  Target row i is the distribution of position i+1.
+ *     T=0: n = largest k with x_j == argmax(target row j-1) for all j <= k;
+ *          y = argmax(target row n).
+ *     T=1: for j = 1..gamma: accept iff u_j * q_j(x_j) < p_j(x_j), u_j =
+ *          Philox(seed_b; b, j, 1); at the first rejection k, y is drawn from
+ *          max(0, p_k - q_k) normalised (from p_k if that is all zero) with
+ *          Philox(seed_b; b, k, 2); if all are accepted, y is drawn from
+ *          p_{gamma+1} with Philox(seed_b; b, gamma+1, 3).  p = softmax(target
+ *          row), q = softmax(draft row), both at temperature 1.
+ *   target_logits   [B, gamma+1, V], dtype target_dtype.
+ *   draft_logits    [B, gamma, V], dtype draft_dtype (may be the float32
+ *                   qlogits_out of spec_draft_block); ignored and nullable at T=0.
+ *   draft_tokens    [B, gamma] int32.
+ *   seeds           [B] uint64, required at T=1.
+ *   n_accepted_out  [B] int32 in [0, gamma]; the acceptance length as the pages
+ *                   count it (with the bonus) is n + 1.
+ *   committed_out   [B, gamma+1] int32: x_1..x_n, y, then -1.
+ *   bonus_out       [B] int32: y.
+ *   near_tie_out    [B] int32 (nullable): 1 when some draw of the request landed
+ *                   within 1e-6 (relative) of its decision threshold, where float32
+ *                   and exact arithmetic may legitimately decide differently.
+ * An invalid request (a token outside [0, V) or an invalid row it reads) gets
+ * n = -1, committed all -1 and bonus -1.
+ * Limits: 1 <= gamma <= SPEC_MAX_GAMMA, 1 <= V <= SPEC_MAX_V, 1 <= B <= 65535.
+ */
+spec_status spec_verify(const void *target_logits, spec_dtype target_dtype,
+                        const void *draft_logits, spec_dtype draft_dtype,
+                        const int32_t *draft_tokens, int B, int gamma, int V, int temperature,
+                        const uint64_t *seeds, int32_t *n_accepted_out, int32_t *committed_out,
+                        int32_t *bonus_out, int32_t *near_tie_out, void *workspace,
+                        size_t workspace_bytes, spec_stream_t stream);
+
+/*
+ * spec_e2etv - SpecOPD E2E-TV surrogate and its gradient.
+ *
+ * Defines ("SpecOPD" paper summary, onedev.kr, section "how to use it"; VESSL AI
+ * "Speculative Decoding Part 2", DSpark section: alpha = 1 - D_TV).  Rows are
+ * branch-major: row n*Wb + i is position i of branch n.  p = softmax(target row),
+ * q = softmax(draft row):
+ *     a_{n,i} = sum_v min(p_v, q_v),   s_{n,i} = sum_{q_v < p_v} q_v
+ *     S_{n,j} = prod_{i<=j} a_{n,i},   loss = 1 - mean_{n,j} S_{n,j}
+ *     grad_{n,i,v} = dloss/dz_{n,i,v} = -kappa_{n,i} q_v (1[q_v < p_v] - s_{n,i}),
+ *     kappa_{n,i} = (1/(N*Wb)) sum_{j>=i} prod_{k<=j, k!=i} a_{n,k}
+ * The target is held fixed (no gradient w.r.t. the target logits).
+ *   target_logits, draft_logits  bf16 [N*Wb, V].
+ *   a_out, surv_out              [N*Wb] float32: a and S.
+ *   loss_out                     [1] float32.
+ *   grad_out                     bf16 [N*Wb, V], rounded once from float32 (RNE).
+ * A branch with an invalid row gets NaN a/surv, a zero gradient, and makes the
+ * loss NaN (flag NONFINITE).
+ * Limits: 1 <= Wb <= SPEC_MAX_GAMMA, 1 <= V <= SPEC_MAX_V, 1 <= N*Wb <= 2^24.
+ */
+spec_status spec_e2etv(const uint16_t *target_logits, const uint16_t *draft_logits,
+                       int n_branches, int Wb, int V, float *a_out, float *surv_out,
+                       float *loss_out, uint16_t *grad_out, void *workspace,
+                       size_t workspace_bytes, spec_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_GB300_SPEC_H */

@@ -72,6 +72,8 @@ def branch(target_rows, draft_rows, n_total, with_grad=True):
     """E2E-TV quantities for one branch of Wb positions.
 
     Returns dict(a [Wb], s [Wb], surv [Wb], sum_surv, grad [Wb, V] or None, valid).
+    A branch with an invalid row has no distribution: NaN a, s and surv, a zero
+    gradient (nothing to descend), and it makes the loss NaN.
     ``n_total`` is N*Wb over the whole batch (the mean's denominator).
     """
     P = as_f64(target_rows)
@@ -80,7 +82,7 @@ def branch(target_rows, draft_rows, n_total, with_grad=True):
     if not all(row_valid(r) for r in P) or not all(row_valid(r) for r in Q):
         nan = np.full(Wb, np.nan)
         return dict(a=nan, s=nan, surv=nan, sum_surv=np.nan,
-                    grad=np.full((Wb, V), np.nan) if with_grad else None, valid=False)
+                    grad=np.zeros((Wb, V)) if with_grad else None, valid=False)
     a = np.zeros(Wb)
     s = np.zeros(Wb)
     ps, qs = [], []

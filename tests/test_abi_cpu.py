@@ -1,0 +1,158 @@
+"""C ABI checks that need no GPU: the library loads, exports every function that
+include/spec.h declares, and rejects bad arguments before enqueuing anything.
+
+Every call below carries at least one invalid argument, so it returns before its
+first CUDA call; fake device addresses are never dereferenced.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import verify_spec_draft_gb300 as vsd
+from verify_spec_draft_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "spec.h")
+
+A = 0x10000          # a 16-byte aligned fake device address
+MIS = 0x10008        # misaligned
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if build.needs_build():
+        build.build()
+    return vsd.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(spec_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    fns = declared_functions()
+    for name in ("spec_draft_block", "spec_verify", "spec_e2etv", "spec_workspace_bytes",
+                 "spec_workspace_init", "spec_get_device_status", "spec_status_string"):
+        assert name in fns
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(declared_functions()) >= set(vsd.SIGNATURES)
+
+
+def test_status_strings(lib):
+    for code in range(10):
+        s = lib.spec_status_string(code).decode()
+        assert s and s != "unknown status"
+    assert lib.spec_status_string(99).decode() == "unknown status"
+
+
+def test_workspace_bytes_ranges(lib):
+    wb = lib.spec_workspace_bytes
+    assert wb(vsd.OP_VERIFY, 32, 7, 248320, 0) > 0
+    assert wb(vsd.OP_DRAFT, 1, 15, 248320, 256) > 0
+    assert wb(vsd.OP_E2ETV, 1024, 7, 248320, 0) > 0
+    assert wb(vsd.OP_VERIFY, 0, 7, 100, 0) == 0
+    assert wb(vsd.OP_VERIFY, 1, 65, 100, 0) == 0
+    assert wb(vsd.OP_VERIFY, 1, 7, 0, 0) == 0
+    assert wb(vsd.OP_DRAFT, 1, 7, 100, 257) == 0
+    assert wb(vsd.OP_DRAFT, 4097, 1, 100, 8) == 0
+    assert wb(vsd.OP_E2ETV, 1 << 20, 64, 8, 0) == 0
+    assert wb(7, 1, 1, 1, 0) == 0
+    # bigger problems never need less workspace
+    assert wb(vsd.OP_VERIFY, 64, 7, 248320, 0) >= wb(vsd.OP_VERIFY, 32, 7, 248320, 0)
+
+
+def _draft(lib, **kw):
+    a = dict(logits=A, ldt=vsd.BF16, anchor=A, U=A, Wt=A, wdt=vsd.BF16, r=8, B=2, gamma=3, V=100, T=0,
+             seeds=A, tokens=A, conf=A, qtok=0, qlogits=0, passes=0, ws=A, wsb=1 << 30)
+    a.update(kw)
+    return lib.spec_draft_block(a["logits"], a["ldt"], a["anchor"], a["U"], a["Wt"], a["wdt"], a["r"], a["B"],
+                                a["gamma"], a["V"], a["T"], a["seeds"], a["tokens"], a["conf"], a["qtok"],
+                                a["qlogits"], a["passes"], a["ws"], a["wsb"], None)
+
+
+def test_draft_argument_errors(lib):
+    assert _draft(lib, logits=0) == 1
+    assert _draft(lib, T=2) == 1
+    assert _draft(lib, T=1, seeds=0) == 1
+    assert _draft(lib, U=0) == 1
+    assert _draft(lib, ldt=5) == 3
+    assert _draft(lib, wdt=9) == 3
+    assert _draft(lib, gamma=0) == 2
+    assert _draft(lib, gamma=65) == 2
+    assert _draft(lib, r=257) == 2
+    assert _draft(lib, B=4097, gamma=1) == 2
+    assert _draft(lib, V=0) == 2
+    assert _draft(lib, logits=MIS) == 4
+    assert _draft(lib, Wt=MIS) == 4
+    assert _draft(lib, qlogits=MIS) == 4
+    assert _draft(lib, ws=0) == 9
+    assert _draft(lib, wsb=100) == 9
+
+
+def _verify(lib, **kw):
+    a = dict(target=A, tdt=vsd.BF16, draft=A, ddt=vsd.BF16, tokens=A, B=2, gamma=3, V=100, T=0, seeds=A,
+             n=A, com=A, bonus=A, near=0, ws=A, wsb=1 << 30)
+    a.update(kw)
+    return lib.spec_verify(a["target"], a["tdt"], a["draft"], a["ddt"], a["tokens"], a["B"], a["gamma"], a["V"],
+                           a["T"], a["seeds"], a["n"], a["com"], a["bonus"], a["near"], a["ws"], a["wsb"], None)
+
+
+def test_verify_argument_errors(lib):
+    assert _verify(lib, target=0) == 1
+    assert _verify(lib, tokens=0) == 1
+    assert _verify(lib, n=0) == 1
+    assert _verify(lib, T=1, draft=0) == 1
+    assert _verify(lib, T=1, seeds=0) == 1
+    assert _verify(lib, T=3) == 1
+    assert _verify(lib, tdt=2) == 3
+    assert _verify(lib, T=1, ddt=2) == 3
+    assert _verify(lib, B=0) == 2
+    assert _verify(lib, B=65536) == 2
+    assert _verify(lib, gamma=65) == 2
+    assert _verify(lib, V=(1 << 26) + 1) == 2
+    assert _verify(lib, target=MIS) == 4
+    assert _verify(lib, T=1, draft=MIS) == 4
+    assert _verify(lib, ws=0) == 9
+    assert _verify(lib, wsb=10) == 9
+
+
+def _e2etv(lib, **kw):
+    a = dict(target=A, draft=A, N=4, Wb=7, V=64, a=A, s=A, loss=A, grad=A, ws=A, wsb=1 << 30)
+    a.update(kw)
+    return lib.spec_e2etv(a["target"], a["draft"], a["N"], a["Wb"], a["V"], a["a"], a["s"], a["loss"], a["grad"],
+                          a["ws"], a["wsb"], None)
+
+
+def test_e2etv_argument_errors(lib):
+    assert _e2etv(lib, target=0) == 1
+    assert _e2etv(lib, grad=0) == 1
+    assert _e2etv(lib, loss=0) == 1
+    assert _e2etv(lib, N=0) == 2
+    assert _e2etv(lib, Wb=65) == 2
+    assert _e2etv(lib, V=0) == 2
+    assert _e2etv(lib, draft=MIS) == 4
+    assert _e2etv(lib, grad=MIS) == 4
+    assert _e2etv(lib, ws=0) == 9
+    assert _e2etv(lib, wsb=100) == 9
+
+
+def test_workspace_init_rejects_missing(lib):
+    assert lib.spec_workspace_init(None, 1 << 20, None) == 9
+    assert lib.spec_workspace_init(A, 16, None) == 9
+    assert lib.spec_get_device_status(None, None, None) == 9
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    torch = pytest.importorskip("torch")
+    x = torch.zeros((1, 2, 8))
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        vsd.verify(x, None, torch.zeros((1, 1), dtype=torch.int32))

@@ -1,0 +1,162 @@
+"""spec_draft_block on the GPU against the float64 oracle.
+
+Tokens are compared bit for bit.  Where the oracle flags a near-tie (T=0: the top two
+biased logits closer than float32 can resolve; T=1: the uniform within 1e-6 of a CDF
+boundary) the GPU may take the other branch; the check is then teacher-forced: every
+GPU token must be the oracle's choice given the GPU's own previous token, or a
+flagged near-tie.  Confidences and q(x) agree to 1e-5.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import verify_spec_draft_gb300 as vsd
+from verify_spec_draft_gb300 import synth
+from oracle import draft as od, philox
+
+pytestmark = pytest.mark.gpu
+
+
+def _np(t):
+    return None if t is None else t.double().cpu().numpy()
+
+
+def _gpu(L, anchor, U, Wt, T, seeds, qlogits=False):
+    dev = torch.device("cuda")
+    out = vsd.draft_block(L.to(dev), anchor.to(dev), None if U is None else U.to(dev),
+                          None if Wt is None else Wt.to(dev), T, seeds.to(dev), qlogits=qlogits)
+    torch.cuda.synchronize()
+    return out
+
+
+def check_draft(out, L, anchor, U, Wt, T, seeds, tol=1e-5):
+    """Teacher-forced comparison; returns (exact, near) counts."""
+    tok = out["tokens"].cpu().numpy()
+    conf = out["conf"].cpu().numpy()
+    qtok = out["qtok"].cpu().numpy()
+    Ln, Un, Wn = _np(L), _np(U), _np(Wt)
+    B, gamma, V = Ln.shape
+    ref = od.draft_block(Ln, anchor.cpu().numpy(), Un, Wn, T, seeds.cpu().numpy())
+    if (tok == ref["tokens"]).all():
+        ok = np.isfinite(ref["conf"])
+        assert np.abs(conf[ok] - ref["conf"][ok]).max(initial=0) <= tol
+        assert np.abs(qtok[ok] - ref["qtok"][ok]).max(initial=0) <= tol
+        assert (np.isnan(conf) == ~ok).all()
+        return tok.size, 0
+    near = 0
+    for b in range(B):
+        prev = int(anchor[b])
+        for j in range(gamma):
+            u = philox.uniform(int(seeds[b]), b, j + 1, philox.STREAM_DRAFT) if T else 0.0
+            st = od.draft_step(Ln[b, j], prev, Un, Wn, T, u)
+            if tok[b, j] != st["x"]:
+                assert st["near"], (b, j, tok[b, j], st["x"])
+                near += 1
+            else:
+                assert abs(conf[b, j] - st["conf"]) <= tol
+            prev = int(tok[b, j])
+            if prev < 0:
+                break
+    return tok.size - near, near
+
+
+SMALL = [  # (B, gamma, V, r, dtype)
+    (3, 5, 1000, 8, torch.float32),      # 8 tiles, ragged tail
+    (2, 4, 1000, 16, torch.bfloat16),
+    (1, 7, 4099, 32, torch.float32),     # V odd
+    (4, 3, 777, 0, torch.bfloat16),      # no bias
+    (2, 6, 300, 12, torch.bfloat16),     # r*2 bytes not a multiple of 16: scalar weight path
+    (1, 64, 200, 8, torch.float32),      # maximum gamma
+]
+
+
+@pytest.mark.parametrize("B,gamma,V,r,dtype", SMALL)
+@pytest.mark.parametrize("T", [0, 1])
+def test_small(spec, B, gamma, V, r, dtype, T):
+    L, _ = synth.target_and_draft(B, gamma - 1, V, "gaussian", 0.0, dtype, seed=V * 3 + r)
+    L = L[:, :gamma].contiguous()
+    U, Wt = (None, None) if r == 0 else synth.markov_weights(V, r, dtype, seed=r, scale=0.5)
+    anchor = synth.anchors(B, V, seed=B)
+    seeds = synth.seeds_for(B, 3)
+    out = _gpu(L, anchor, U, Wt, T, seeds)
+    exact, near = check_draft(out, L, anchor, U, Wt, T, seeds)
+    assert near <= 1
+    assert 0 <= int(out["passes"].item()) <= gamma
+
+
+@pytest.mark.parametrize("T", [0, 1])
+def test_strong_bias_needs_many_passes(spec, T):
+    """A bias far larger than the logit gaps: the unbiased guess is wrong everywhere
+    and the fixed point takes several passes, yet equals the sequential chain."""
+    B, gamma, V, r = 4, 12, 600, 4
+    L, _ = synth.target_and_draft(B, gamma - 1, V, "gaussian", 0.0, torch.float32, seed=1)
+    L = (L[:, :gamma] * 0.1).contiguous()
+    U, Wt = synth.markov_weights(V, r, torch.float32, seed=2, scale=3.0)
+    anchor = synth.anchors(B, V, seed=5)
+    seeds = synth.seeds_for(B, 9)
+    out = _gpu(L, anchor, U, Wt, T, seeds)
+    check_draft(out, L, anchor, U, Wt, T, seeds)
+    assert int(out["passes"].item()) >= 3
+
+
+def test_qlogits_are_the_biased_rows(spec):
+    B, gamma, V, r = 2, 3, 2000, 16
+    L, _ = synth.target_and_draft(B, gamma - 1, V, "gaussian", 0.0, torch.bfloat16, seed=4)
+    L = L[:, :gamma].contiguous()
+    U, Wt = synth.markov_weights(V, r, torch.bfloat16, seed=4, scale=0.3)
+    anchor = synth.anchors(B, V, seed=4)
+    seeds = synth.seeds_for(B)
+    out = _gpu(L, anchor, U, Wt, 1, seeds, qlogits=True)
+    ref = od.draft_block(_np(L), anchor.numpy(), _np(U), _np(Wt), 1, seeds.numpy(), return_z=True)
+    assert (out["tokens"].cpu().numpy() == ref["tokens"]).all()
+    z = out["qlogits"].cpu().double().numpy()
+    assert np.abs(z - ref["z"]).max() <= 1e-5 * max(1.0, np.abs(ref["z"]).max())
+
+
+def test_invalid_anchor_and_rows(spec):
+    B, gamma, V, r = 3, 4, 500, 8
+    L, _ = synth.target_and_draft(B, gamma - 1, V, "gaussian", 0.0, torch.float32, seed=8)
+    L = L[:, :gamma].contiguous()
+    L[1, 2, 10] = float("nan")
+    U, Wt = synth.markov_weights(V, r, torch.float32, seed=8)
+    anchor = synth.anchors(B, V, seed=8)
+    anchor[2] = V + 5
+    seeds = synth.seeds_for(B)
+    for T in (0, 1):
+        out = _gpu(L, anchor, U, Wt, T, seeds)
+        check_draft(out, L, anchor, U, Wt, T, seeds)
+        tok = out["tokens"].cpu()
+        assert tok[1, 2:].tolist() == [-1, -1] and (tok[1, :2] >= 0).all()
+        assert (tok[2] == -1).all() and (tok[0] >= 0).all()
+        flags = vsd.device_status(out["ws"])
+        assert flags & vsd.DEV_NONFINITE and flags & vsd.DEV_TOKEN
+
+
+def test_deterministic(spec):
+    B, gamma, V, r = 8, 7, 30000, 64
+    L, _ = synth.target_and_draft(B, gamma - 1, V, "zipf", 0.0, torch.bfloat16, seed=6, device="cuda")
+    L = L[:, :gamma].contiguous()
+    U, Wt = synth.markov_weights(V, r, torch.bfloat16, seed=6, device="cuda")
+    anchor = synth.anchors(B, V, seed=6, device="cuda")
+    seeds = synth.seeds_for(B, device="cuda")
+    for T in (0, 1):
+        ws = vsd.workspace(vsd.OP_DRAFT, B, gamma, V, r)
+        outs = [vsd.draft_block(L, anchor, U, Wt, T, seeds, ws=ws) for _ in range(3)]
+        torch.cuda.synchronize()
+        for o in outs[1:]:
+            for k in ("tokens", "conf", "qtok", "passes"):
+                assert torch.equal(o[k], outs[0][k])
+
+
+@pytest.mark.parametrize("cfg_id,T", [(1, 0), (1, 1), (2, 0), (2, 1), (3, 0), (4, 1)])
+def test_configs_full_size(spec, cfg_id, T):
+    inp = synth.config_inputs(cfg_id, device="cuda")
+    c = inp["cfg"]
+    L = inp["draft"]
+    out = vsd.draft_block(L, inp["anchor"], inp["U"], inp["Wt"], T, inp["seeds"])
+    torch.cuda.synchronize()
+    exact, near = check_draft(out, L.cpu(), inp["anchor"].cpu(), inp["U"].cpu(), inp["Wt"].cpu(), T,
+                              inp["seeds"].cpu())
+    assert near <= max(1, c.B * c.gamma // 64)
+    assert vsd.device_status(out["ws"]) == 0

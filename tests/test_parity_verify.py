@@ -1,0 +1,166 @@
+"""spec_verify on the GPU against the float64 oracle.
+
+T=0 is compared bit for bit.  T=1 is bit for bit except requests whose draws the
+oracle flags as near-ties (within 1e-6 of a threshold), which are counted and must
+stay rare.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import verify_spec_draft_gb300 as vsd
+from verify_spec_draft_gb300 import synth
+from oracle import verify as ov
+
+pytestmark = pytest.mark.gpu
+
+
+def _tokens_with_mismatches(target, gamma, seed):
+    """Draft tokens equal to the target argmax up to a random first mismatch per
+    request (all n in 0..gamma occur)."""
+    g = torch.Generator().manual_seed(seed)
+    am = target.float().argmax(-1)[:, :gamma].clone()
+    B, V = target.shape[0], target.shape[2]
+    for b in range(B):
+        k = int(torch.randint(0, gamma + 1, (1,), generator=g))
+        if k < gamma:
+            am[b, k] = (am[b, k] + 1 + torch.randint(0, max(1, V - 1), (1,), generator=g)) % V
+    return am.to(torch.int32).contiguous()
+
+
+def _run_gpu(target, draft, tokens, T, seeds, ws=None):
+    dev = torch.device("cuda")
+    out = vsd.verify(target.to(dev), None if draft is None else draft.to(dev), tokens.to(dev), T,
+                     None if seeds is None else seeds.to(dev), ws=ws)
+    torch.cuda.synchronize()
+    return {k: v.cpu() for k, v in out.items() if k != "ws"}, out["ws"]
+
+
+def _oracle(target, draft, tokens, T, seeds):
+    return ov.verify(target.double().numpy(), None if draft is None else draft.double().numpy(),
+                     tokens.numpy(), T, None if seeds is None else seeds.numpy())
+
+
+def _compare(g, o, allow_near):
+    n_near = 0
+    B = g["n"].shape[0]
+    for b in range(B):
+        same = (int(g["n"][b]) == int(o["n"][b]) and int(g["bonus"][b]) == int(o["bonus"][b])
+                and g["committed"][b].tolist() == o["committed"][b].tolist())
+        if not same:
+            assert allow_near and o["near"][b], (b, g["n"][b], o["n"][b], g["committed"][b], o["committed"][b])
+            n_near += 1
+    return n_near
+
+
+SMALL = [  # (B, gamma, V, dtype)
+    (3, 4, 20000, torch.bfloat16),      # 3 chunks, ragged tail, vector path
+    (2, 7, 8192, torch.float32),         # exactly one chunk
+    (4, 3, 999, torch.bfloat16),         # V % 8 != 0: scalar path
+    (1, 1, 1, torch.float32),            # one token vocabulary
+    (5, 2, 17, torch.float32),           # tiny
+    (2, 64, 300, torch.bfloat16),        # maximum gamma
+]
+
+
+@pytest.mark.parametrize("B,gamma,V,dtype", SMALL)
+def test_t0_small(spec, B, gamma, V, dtype):
+    t, _ = synth.target_and_draft(B, gamma, V, "gaussian", 0.5, dtype, seed=V + gamma)
+    tok = _tokens_with_mismatches(t, gamma, seed=B)
+    g, _ = _run_gpu(t, None, tok, 0, None)
+    o = _oracle(t, None, tok, 0, None)
+    _compare(g, o, allow_near=False)
+    assert (g["near"] == 0).all()
+
+
+def test_t0_ties_lowest_index(spec):
+    # integer-valued bf16 logits in a small range: many exact ties per row
+    g0 = torch.Generator().manual_seed(5)
+    B, gamma, V = 6, 5, 40000
+    t = torch.randint(-3, 3, (B, gamma + 1, V), generator=g0).to(torch.bfloat16)
+    tok = _tokens_with_mismatches(t, gamma, seed=3)
+    g, _ = _run_gpu(t, None, tok, 0, None)
+    o = _oracle(t, None, tok, 0, None)
+    _compare(g, o, allow_near=False)
+    # every argmax is the first index of the row maximum
+    assert (g["bonus"] >= 0).all()
+
+
+@pytest.mark.parametrize("B,gamma,V,dtype", SMALL[:3] + [(8, 7, 5000, torch.bfloat16)])
+@pytest.mark.parametrize("ddtype", [None, torch.float32])
+def test_t1_small(spec, B, gamma, V, dtype, ddtype):
+    t, d = synth.target_and_draft(B, gamma, V, "gaussian", 0.7, dtype, seed=11 * V + gamma)
+    if ddtype is not None:
+        d = d.to(ddtype)
+    near = 0
+    for s in range(6):
+        tok = synth.draft_tokens(d, 1, seed=s)
+        seeds = synth.seeds_for(B, 100 * s)
+        g, _ = _run_gpu(t, d, tok, 1, seeds)
+        o = _oracle(t, d, tok, 1, seeds)
+        near += _compare(g, o, allow_near=True)
+    assert near <= 2
+
+
+def test_t1_acceptance_spread(spec):
+    """Noisy drafts: every n from 0 to gamma shows up, including residual draws at
+    every position and the bonus draw."""
+    B, gamma, V = 64, 4, 3000
+    t, d = synth.target_and_draft(B, gamma, V, "gaussian", (0.2, 3.0), torch.bfloat16, seed=77)
+    tok = synth.draft_tokens(d, 1, seed=1)
+    seeds = synth.seeds_for(B, 5)
+    g, _ = _run_gpu(t, d, tok, 1, seeds)
+    o = _oracle(t, d, tok, 1, seeds)
+    _compare(g, o, allow_near=True)
+    assert len(set(g["n"].tolist())) >= 4
+
+
+def test_invalid_requests(spec):
+    B, gamma, V = 5, 3, 5000
+    t, d = synth.target_and_draft(B, gamma, V, "gaussian", 0.5, torch.float32, seed=3)
+    tok = synth.draft_tokens(d, 0)
+    t[1, 2, 77] = float("nan")
+    t[2, 0, 4999] = float("inf")
+    t[3, 3, :] = float("-inf")
+    tok[4, 1] = V                      # out of range
+    for T in (0, 1):
+        seeds = synth.seeds_for(B)
+        g, ws = _run_gpu(t, d, tok, T, seeds)
+        o = _oracle(t, d, tok, T, seeds)
+        _compare(g, o, allow_near=True)
+        assert g["n"][1:5].tolist() == [-1, -1, -1, -1]
+        assert int(g["n"][0]) >= 0
+        flags = vsd.device_status(ws)
+        assert flags & vsd.DEV_NONFINITE and flags & vsd.DEV_TOKEN
+
+
+def test_deterministic_and_workspace_reuse(spec):
+    B, gamma, V = 16, 7, 50000
+    t, d = synth.target_and_draft(B, gamma, V, "zipf", (0.3, 1.5), torch.bfloat16, seed=9, device="cuda")
+    seeds = synth.seeds_for(B, device="cuda")
+    for T in (0, 1):
+        tok = synth.draft_tokens(d, T, seed=2)
+        ws = vsd.workspace(vsd.OP_VERIFY, B, gamma, V)
+        outs = [vsd.verify(t, d, tok, T, seeds, ws=ws) for _ in range(3)]
+        torch.cuda.synchronize()
+        for o in outs[1:]:
+            for k in ("n", "committed", "bonus", "near"):
+                assert torch.equal(o[k], outs[0][k])
+        assert vsd.device_status(ws) == 0
+
+
+@pytest.mark.parametrize("cfg_id,T", [(1, 0), (1, 1), (2, 0), (2, 1), (3, 0), (4, 1)])
+def test_configs_full_size(spec, cfg_id, T):
+    inp = synth.config_inputs(cfg_id, device="cuda")
+    c = inp["cfg"]
+    t, d = inp["target"], inp["draft"]
+    tok = synth.draft_tokens(d, T, seed=c.seed)
+    seeds = inp["seeds"]
+    out = vsd.verify(t, d, tok, T, seeds)
+    torch.cuda.synchronize()
+    g = {k: v.cpu() for k, v in out.items() if k != "ws"}
+    o = _oracle(t.cpu(), d.cpu() if T else None, tok.cpu(), T, seeds.cpu())
+    near = _compare(g, o, allow_near=(T == 1))
+    assert near <= max(1, c.B // 16)
+    assert vsd.device_status(out["ws"]) == 0

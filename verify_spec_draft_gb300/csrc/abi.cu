@@ -1,0 +1,196 @@
+// abi.cu - the C ABI (include/spec.h): argument checks, workspace layout, launches.
+//
+// Every check that can fail is done here, on the host, before anything is enqueued;
+// conditions only the device can see go to the workspace status word.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "spec.h"
+#include "internal.h"
+#include "spec_device.cuh"
+
+namespace spec {
+
+int device_sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    static int cache[128] = {0};
+    if (dev >= 0 && dev < 128 && cache[dev] > 0) return cache[dev];
+    int n = 1;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
+    if (dev >= 0 && dev < 128) cache[dev] = n;
+    return n;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+static bool dtype_ok(int d) { return d == SPEC_F32 || d == SPEC_BF16; }
+static size_t dtype_size(int d) { return d == SPEC_F32 ? 4 : 2; }
+
+}  // namespace spec
+
+using namespace spec;
+
+extern "C" {
+
+size_t spec_workspace_bytes(spec_op op, int B, int gamma, int V, int r) {
+    if (B < 1 || gamma < 1 || gamma > SPEC_MAX_GAMMA || V < 1 || V > SPEC_MAX_V) return 0;
+    switch (op) {
+        case SPEC_OP_DRAFT:
+            if (r < 0 || r > SPEC_MAX_RANK || (long)B * gamma > 4096) return 0;
+            return draft_workspace_bytes(B, gamma, V, r);
+        case SPEC_OP_VERIFY:
+            if (B > 65535) return 0;
+            return verify_workspace_bytes(B, gamma, V);
+        case SPEC_OP_E2ETV:
+            if ((long)B * gamma > (1L << 24)) return 0;
+            return e2etv_workspace_bytes(B, gamma, V);
+        default:
+            return 0;
+    }
+}
+
+spec_status spec_workspace_init(void* workspace, size_t bytes, spec_stream_t stream) {
+    if (!workspace || bytes < kWsHeaderBytes) return SPEC_ERR_WORKSPACE;
+    if (cudaMemsetAsync(workspace, 0, bytes, (cudaStream_t)stream) != cudaSuccess) return SPEC_ERR_CUDA;
+    return SPEC_OK;
+}
+
+spec_status spec_get_device_status(const void* workspace, spec_stream_t stream, uint32_t* flags_out) {
+    if (!workspace) return SPEC_ERR_WORKSPACE;
+    uint32_t flags = 0;
+    if (cudaMemcpyAsync(&flags, workspace, sizeof(flags), cudaMemcpyDeviceToHost, (cudaStream_t)stream) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (flags_out) *flags_out = flags;
+    if (flags & SPEC_DEV_TIMEOUT) return SPEC_ERR_TIMEOUT;
+    if (flags & SPEC_DEV_TOKEN) return SPEC_ERR_TOKEN;
+    if (flags & SPEC_DEV_NONFINITE) return SPEC_ERR_NONFINITE;
+    return SPEC_OK;
+}
+
+const char* spec_status_string(spec_status s) {
+    switch (s) {
+        case SPEC_OK: return "ok";
+        case SPEC_ERR_INVALID_ARG: return "invalid argument (null pointer, temperature, op code)";
+        case SPEC_ERR_SHAPE: return "size outside the supported range";
+        case SPEC_ERR_DTYPE: return "unknown dtype";
+        case SPEC_ERR_ALIGN: return "base pointer not 16-byte aligned";
+        case SPEC_ERR_CUDA: return "CUDA runtime error";
+        case SPEC_ERR_TIMEOUT: return "a bounded device wait ran out";
+        case SPEC_ERR_NONFINITE: return "a row holds NaN/+inf or no finite entry";
+        case SPEC_ERR_TOKEN: return "a token outside [0, V)";
+        case SPEC_ERR_WORKSPACE: return "workspace missing or too small";
+        default: return "unknown status";
+    }
+}
+
+spec_status spec_draft_block(const void* draft_logits, spec_dtype logits_dtype, const int32_t* anchor,
+                             const void* U, const void* Wt, spec_dtype w_dtype, int r, int B, int gamma, int V,
+                             int temperature, const uint64_t* seeds, int32_t* tokens_out, float* conf_out,
+                             float* qtok_out, float* qlogits_out, int32_t* passes_out, void* workspace,
+                             size_t workspace_bytes, spec_stream_t stream) {
+    if (!dtype_ok(logits_dtype) || (r > 0 && !dtype_ok(w_dtype))) return SPEC_ERR_DTYPE;
+    if (B < 1 || gamma < 1 || gamma > SPEC_MAX_GAMMA || V < 1 || V > SPEC_MAX_V || r < 0 || r > SPEC_MAX_RANK ||
+        (long)B * gamma > 4096)
+        return SPEC_ERR_SHAPE;
+    if (temperature != 0 && temperature != 1) return SPEC_ERR_INVALID_ARG;
+    if (!draft_logits || !anchor || !tokens_out || !conf_out) return SPEC_ERR_INVALID_ARG;
+    if (r > 0 && (!U || !Wt)) return SPEC_ERR_INVALID_ARG;
+    if (temperature == 1 && !seeds) return SPEC_ERR_INVALID_ARG;
+    if (!aligned16(draft_logits) || (r > 0 && (!aligned16(U) || !aligned16(Wt))) ||
+        (qlogits_out && !aligned16(qlogits_out)))
+        return SPEC_ERR_ALIGN;
+    const size_t need = draft_workspace_bytes(B, gamma, V, r);
+    if (!workspace || workspace_bytes < need) return SPEC_ERR_WORKSPACE;
+
+    DraftParams p;
+    memset(&p, 0, sizeof(p));
+    p.logits = draft_logits;
+    p.ldt = logits_dtype;
+    p.anchor = anchor;
+    p.U = U;
+    p.Wt = Wt;
+    p.wdt = r > 0 ? w_dtype : logits_dtype;
+    p.r = r;
+    p.B = B;
+    p.gamma = gamma;
+    p.V = V;
+    p.temperature = temperature;
+    p.seeds = seeds;
+    p.tokens_out = tokens_out;
+    p.conf_out = conf_out;
+    p.qtok_out = qtok_out;
+    p.qlogits_out = qlogits_out;
+    p.passes_out = passes_out;
+    p.vec_l = ((size_t)V * dtype_size(logits_dtype)) % 16 == 0;
+    p.vec_w = r > 0 && ((size_t)r * dtype_size(w_dtype)) % 16 == 0;
+    draft_bind_workspace(p, workspace);
+    return draft_launch(p, (cudaStream_t)stream) == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+spec_status spec_verify(const void* target_logits, spec_dtype target_dtype, const void* draft_logits,
+                        spec_dtype draft_dtype, const int32_t* draft_tokens, int B, int gamma, int V, int temperature,
+                        const uint64_t* seeds, int32_t* n_accepted_out, int32_t* committed_out, int32_t* bonus_out,
+                        int32_t* near_tie_out, void* workspace, size_t workspace_bytes, spec_stream_t stream) {
+    if (!dtype_ok(target_dtype) || (temperature == 1 && !dtype_ok(draft_dtype))) return SPEC_ERR_DTYPE;
+    if (B < 1 || B > 65535 || gamma < 1 || gamma > SPEC_MAX_GAMMA || V < 1 || V > SPEC_MAX_V) return SPEC_ERR_SHAPE;
+    if (temperature != 0 && temperature != 1) return SPEC_ERR_INVALID_ARG;
+    if (!target_logits || !draft_tokens || !n_accepted_out || !committed_out || !bonus_out)
+        return SPEC_ERR_INVALID_ARG;
+    if (temperature == 1 && (!draft_logits || !seeds)) return SPEC_ERR_INVALID_ARG;
+    if (!aligned16(target_logits) || (temperature == 1 && !aligned16(draft_logits))) return SPEC_ERR_ALIGN;
+    const size_t need = verify_workspace_bytes(B, gamma, V);
+    if (!workspace || workspace_bytes < need) return SPEC_ERR_WORKSPACE;
+
+    VerifyParams p;
+    memset(&p, 0, sizeof(p));
+    p.target = target_logits;
+    p.draft = temperature == 1 ? draft_logits : nullptr;
+    p.tdt = target_dtype;
+    p.ddt = temperature == 1 ? draft_dtype : target_dtype;
+    p.tokens = draft_tokens;
+    p.seeds = seeds;
+    p.B = B;
+    p.gamma = gamma;
+    p.V = V;
+    p.temperature = temperature;
+    p.nchunk = (V + kVerifyChunk - 1) / kVerifyChunk;
+    p.vec_t = ((size_t)V * dtype_size(target_dtype)) % 16 == 0;
+    p.vec_d = temperature == 1 && ((size_t)V * dtype_size(draft_dtype)) % 16 == 0;
+    p.n_out = n_accepted_out;
+    p.committed_out = committed_out;
+    p.bonus_out = bonus_out;
+    p.near_out = near_tie_out;
+    verify_bind_workspace(p, workspace);
+    return verify_launch(p, (cudaStream_t)stream) == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+spec_status spec_e2etv(const uint16_t* target_logits, const uint16_t* draft_logits, int n_branches, int Wb, int V,
+                       float* a_out, float* surv_out, float* loss_out, uint16_t* grad_out, void* workspace,
+                       size_t workspace_bytes, spec_stream_t stream) {
+    if (n_branches < 1 || Wb < 1 || Wb > SPEC_MAX_GAMMA || V < 1 || V > SPEC_MAX_V ||
+        (long)n_branches * Wb > (1L << 24))
+        return SPEC_ERR_SHAPE;
+    if (!target_logits || !draft_logits || !a_out || !surv_out || !loss_out || !grad_out)
+        return SPEC_ERR_INVALID_ARG;
+    if (!aligned16(target_logits) || !aligned16(draft_logits) || !aligned16(grad_out)) return SPEC_ERR_ALIGN;
+    const size_t need = e2etv_workspace_bytes(n_branches, Wb, V);
+    if (!workspace || workspace_bytes < need) return SPEC_ERR_WORKSPACE;
+
+    E2etvParams p;
+    memset(&p, 0, sizeof(p));
+    p.target = target_logits;
+    p.draft = draft_logits;
+    p.n_branches = n_branches;
+    p.Wb = Wb;
+    p.V = V;
+    p.vec_ok = (V % 8) == 0;
+    p.a_out = a_out;
+    p.surv_out = surv_out;
+    p.loss_out = loss_out;
+    p.grad_out = grad_out;
+    return e2etv_launch(p, workspace, (cudaStream_t)stream) == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,103 @@
+// internal.h - launch interfaces between the C ABI layer (abi.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "spec.h"
+
+namespace spec {
+
+// Streaming work granularity of the verify kernels: elements per work item and per
+// thread (256 threads x 32 contiguous elements).
+constexpr int kVerifyChunk = 8192;
+
+struct VerifyParams {
+    const void* target;        // [B, gamma+1, V]
+    const void* draft;         // [B, gamma, V] (T=1)
+    int tdt, ddt;              // spec_dtype of target / draft
+    const int32_t* tokens;     // [B, gamma]
+    const uint64_t* seeds;     // [B]
+    int B, gamma, V, temperature;
+    int nchunk;                // ceil(V / kVerifyChunk)
+    int vec_t, vec_d;          // rows 16-byte aligned (vector loads allowed)
+    int32_t* n_out;
+    int32_t* committed_out;
+    int32_t* bonus_out;
+    int32_t* near_out;         // nullable
+    // workspace regions
+    unsigned* status;
+    unsigned* done;            // header done[] counters
+    unsigned long long* keys;  // [B*(gamma+1)] argmax keys (T=0)
+    unsigned* rowbad;          // [B*(2*gamma+1)]
+    float2* stats;             // [B*(2*gamma+1)*nchunk] (m, s)
+    unsigned* done1;           // [B]
+    unsigned* done2;           // [B]
+    int4* state;               // [B*2]: mode, n, near, pad | mp, Zp, mq, Zq (as float bits)
+    float2* ksums;             // [B*nchunk] (residual sum, p sum) per chunk
+};
+
+size_t verify_workspace_bytes(int B, int gamma, int V);
+void verify_bind_workspace(VerifyParams& p, void* ws);
+cudaError_t verify_launch(const VerifyParams& p, cudaStream_t stream);
+
+struct DraftParams {
+    const void* logits;        // [B, gamma, V]
+    int ldt;                   // spec_dtype
+    const int32_t* anchor;     // [B]
+    const void* U;             // [V, r]
+    const void* Wt;            // [V, r]
+    int wdt;
+    int r, B, gamma, V, temperature;
+    const uint64_t* seeds;
+    int32_t* tokens_out;
+    float* conf_out;
+    float* qtok_out;           // nullable
+    float* qlogits_out;        // nullable
+    int32_t* passes_out;       // nullable
+    int vec_l;                 // logits rows 16-byte aligned
+    int vec_w;                 // weight rows 16-byte aligned
+    int n_tiles;               // ceil(V / kDraftTile)
+    // workspace regions
+    unsigned* status;
+    unsigned* barrier;         // one barrier slot
+    float4* tile_stats;        // [R * n_tiles]: m, s, argmax index bits, bad
+    int32_t* tokbuf;           // [2 * R] fixed-point iterates
+    unsigned* changed;         // [gamma + 2]
+};
+
+constexpr int kDraftTile = 128;   // vocabulary entries per tile
+
+size_t draft_workspace_bytes(int B, int gamma, int V, int r);
+void draft_bind_workspace(DraftParams& p, void* ws);
+cudaError_t draft_launch(const DraftParams& p, cudaStream_t stream);
+
+struct E2etvParams {
+    const uint16_t* target;    // bf16 [R, V]
+    const uint16_t* draft;     // bf16 [R, V]
+    int n_branches, Wb, V;
+    int vec_ok;                // V % 8 == 0 (rows 16-byte aligned)
+    float* a_out;
+    float* surv_out;
+    float* loss_out;
+    uint16_t* grad_out;
+    // layout chosen at launch
+    int n_groups;              // groups of CTAs, each processing one branch at a time
+    int group_size;            // CTAs per group
+    int cols;                  // columns per CTA (multiple of 8)
+    // workspace regions
+    unsigned* status;
+    unsigned* barriers;        // n_groups barrier slots (stride 64 words)
+    unsigned* done;
+    float2* partials;          // [n_groups][2][group_size][2*Wb]
+    float* branch_sum;         // [n_branches]
+    unsigned* branch_bad;      // [n_branches]
+};
+
+size_t e2etv_workspace_bytes(int n_branches, int Wb, int V);
+cudaError_t e2etv_launch(E2etvParams& p, void* ws, cudaStream_t stream);
+
+int device_sm_count();
+
+}  // namespace spec

@@ -1,0 +1,260 @@
+// spec_device.cuh - device helpers shared by the draft, verify and E2E-TV kernels.
+//
+// Row loads (128-bit, read-only, L1 no-allocate), Philox4x64-10, order-preserving
+// argmax keys, softmax statistics and their merge, warp reductions, and the bounded
+// grid/group barrier used by the persistent kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <math.h>
+
+#include "spec.h"
+
+namespace spec {
+
+constexpr int kThreads = 256;               // threads per CTA for the streaming kernels
+constexpr int kWarps = kThreads / 32;
+constexpr float kNearTie = 1e-6f;           // relative window of a near-tie draw
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // bounded waits: 1 s
+
+// ---------------------------------------------------------------------------------
+// Element loads.  bf16 is carried as raw uint16 words; widening to float32 is exact.
+// ---------------------------------------------------------------------------------
+typedef uint16_t bf16_t;
+
+__device__ __forceinline__ float to_float(float x) { return x; }
+__device__ __forceinline__ float to_float(bf16_t x) { return __uint_as_float(((uint32_t)x) << 16); }
+
+template <typename T> struct VecTraits;
+template <> struct VecTraits<float> { static constexpr int N = 4; };
+template <> struct VecTraits<bf16_t> { static constexpr int N = 8; };
+
+// One 16-byte read-only streaming load of N elements, widened to float.
+__device__ __forceinline__ void load_vec(const float* p, float (&o)[4]) {
+    float4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+    o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+}
+__device__ __forceinline__ void load_vec(const bf16_t* p, float (&o)[8]) {
+    uint32_t a, b, c, d;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "l"(p));
+    o[0] = __uint_as_float(a << 16); o[1] = __uint_as_float(a & 0xffff0000u);
+    o[2] = __uint_as_float(b << 16); o[3] = __uint_as_float(b & 0xffff0000u);
+    o[4] = __uint_as_float(c << 16); o[5] = __uint_as_float(c & 0xffff0000u);
+    o[6] = __uint_as_float(d << 16); o[7] = __uint_as_float(d & 0xffff0000u);
+}
+
+__device__ __forceinline__ float load_one(const float* p) { return __ldg(p); }
+__device__ __forceinline__ float load_one(const bf16_t* p) {
+    return to_float((bf16_t)__ldg(reinterpret_cast<const unsigned short*>(p)));
+}
+
+// Loads N consecutive elements starting at element index `v` of a row of length V,
+// with -inf past the end.  `vec_ok` says rows are 16-byte aligned (V*sizeof(T) % 16
+// == 0 and an aligned base), so whole in-range groups can use one vector load.
+template <typename T, int N>
+__device__ __forceinline__ void load_group(const T* row, long v, long V, bool vec_ok, float (&o)[N]) {
+    if (vec_ok && v + N <= V) {
+        load_vec(row + v, o);
+    } else {
+#pragma unroll
+        for (int e = 0; e < N; ++e) o[e] = (v + e < V) ? load_one(row + v + e) : -INFINITY;
+    }
+}
+
+// A valid logit is finite or -inf; NaN and +inf are not.
+__device__ __forceinline__ bool bad_logit(float x) { return !(x < INFINITY); }
+
+// ---------------------------------------------------------------------------------
+// Philox4x64-10 (Salmon, Moraes, Dror, Shaw, SC'11, section 3.2, table 2).
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ float philox_uniform(uint64_t seed, uint64_t b, uint64_t j, uint64_t stream) {
+    const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
+    const uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
+    uint64_t c0 = b, c1 = j, c2 = stream, c3 = 0;
+    uint64_t k0 = seed, k1 = 0;
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        if (r) { k0 += W0; k1 += W1; }
+        const uint64_t hi0 = __umul64hi(M0, c0), lo0 = M0 * c0;
+        const uint64_t hi1 = __umul64hi(M1, c2), lo1 = M1 * c2;
+        const uint64_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+        c0 = n0; c1 = lo1; c2 = n2; c3 = lo0;
+    }
+    return (float)(c0 >> 40) * 0x1p-24f;   // 24-bit uniform, exact in float32
+}
+
+// ---------------------------------------------------------------------------------
+// Argmax keys: a 64-bit integer whose maximum is the largest value and, among equal
+// values, the lowest index.  -0.0 is folded into +0.0 so the two compare equal.
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t float_order(float f) {
+    if (f == 0.0f) f = 0.0f;
+    const uint32_t b = __float_as_uint(f);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float order_float(uint32_t o) {
+    const uint32_t b = (o & 0x80000000u) ? (o & 0x7fffffffu) : ~o;
+    return __uint_as_float(b);
+}
+__device__ __forceinline__ unsigned long long argmax_key(float v, uint32_t idx) {
+    return ((unsigned long long)float_order(v) << 32) | (unsigned long long)(~idx);
+}
+__device__ __forceinline__ uint32_t key_index(unsigned long long k) { return ~(uint32_t)(k & 0xffffffffu); }
+__device__ __forceinline__ float key_value(unsigned long long k) { return order_float((uint32_t)(k >> 32)); }
+
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long k) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long t = __shfl_xor_sync(0xffffffffu, k, o);
+        k = t > k ? t : k;
+    }
+    return k;
+}
+
+// ---------------------------------------------------------------------------------
+// Softmax statistics: m = max, s = sum exp(x - m).  An empty set is (-inf, 0).
+// merge() is exact for m and rounds s; callers merge in a fixed order so results
+// are bit-reproducible.
+// ---------------------------------------------------------------------------------
+struct Stat { float m; float s; };
+
+__device__ __forceinline__ Stat stat_empty() { return Stat{-INFINITY, 0.0f}; }
+__device__ __forceinline__ Stat stat_merge(Stat a, Stat b) {
+    if (b.m == -INFINITY) return a;
+    if (a.m == -INFINITY) return b;
+    const float m = fmaxf(a.m, b.m);
+    return Stat{m, a.s * expf(a.m - m) + b.s * expf(b.m - m)};
+}
+__device__ __forceinline__ Stat warp_stat(Stat a) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        Stat b{__shfl_xor_sync(0xffffffffu, a.m, o), __shfl_xor_sync(0xffffffffu, a.s, o)};
+        // xor partners merge in opposite operand orders; order the pair by lane so
+        // both lanes compute the identical float result
+        const bool lower = (threadIdx.x & o) == 0;
+        a = lower ? stat_merge(a, b) : stat_merge(b, a);
+    }
+    return a;
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float y = __shfl_xor_sync(0xffffffffu, x, o);
+        x = ((threadIdx.x & o) == 0) ? x + y : y + x;
+    }
+    return x;
+}
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+__device__ __forceinline__ int warp_or(int x) { return __any_sync(0xffffffffu, x) ? 1 : 0; }
+
+// Inclusive prefix sum over the lanes of a warp (fixed association order).
+__device__ __forceinline__ float warp_inclusive_scan(float x) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x = y + x;
+    }
+    return x;
+}
+
+// ---------------------------------------------------------------------------------
+// Memory-model helpers and the bounded barrier.
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release(unsigned* p, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait until *gen differs from `seen`, for at most kWaitLimitNs.  Returns false (and
+// sets SPEC_DEV_TIMEOUT in *status) if the limit ran out.  One thread calls it.
+__device__ __forceinline__ bool wait_generation(const unsigned* gen, unsigned seen, unsigned* status,
+                                                unsigned long long limit_ns) {
+    const unsigned long long t0 = global_timer_ns();
+    unsigned spins = 0;
+    while (ld_acquire(gen) == seen) {
+        if (((++spins) & 63u) == 0 && global_timer_ns() - t0 > limit_ns) {
+            atomicOr(status, SPEC_DEV_TIMEOUT);
+            return false;
+        }
+        __nanosleep(64);
+    }
+    return true;
+}
+
+// Barrier over `nblocks` CTAs that are all resident (cooperative launch).  slot[0] is
+// the arrival count, slot[32] the generation (separate 128-byte lines).  The last
+// CTA to arrive resets the count and bumps the generation; the count is back at 0
+// when the barrier completes.  Returns false on timeout; the kernel must then exit.
+__device__ __forceinline__ bool block_barrier(unsigned* slot, unsigned nblocks, unsigned* status) {
+    __shared__ int s_ok;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned* count = slot;
+        unsigned* gen = slot + 32;
+        const unsigned seen = ld_acquire(gen);
+        const unsigned arrived = atom_add_acq_rel(count, 1u) + 1u;
+        bool ok = true;
+        if (arrived == nblocks) {
+            atomicExch(count, 0u);
+            st_release(gen, seen + 1u);
+        } else {
+            ok = wait_generation(gen, seen, status, kWaitLimitNs);
+        }
+        s_ok = ok ? 1 : 0;
+    }
+    __syncthreads();
+    return s_ok != 0;
+}
+
+// "Last CTA done" test: every CTA calls it once after its writes; exactly one CTA
+// (the last) gets true, after which it sees every other CTA's writes.  The counter
+// is left for that CTA to reset.  No waiting is involved.
+__device__ __forceinline__ bool last_block_done(unsigned* counter, unsigned expected) {
+    __shared__ int s_last;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned prev = atomicAdd(counter, 1u);
+        s_last = (prev == expected - 1u) ? 1 : 0;
+        if (s_last) __threadfence();
+    }
+    __syncthreads();
+    return s_last != 0;
+}
+
+// Workspace header (32 KiB at the start of every workspace).
+struct WsHeader {
+    unsigned status;             // SPEC_DEV_* flags, sticky
+    unsigned pad0[31];
+    unsigned done[32];           // last-CTA counters of single-kernel phases
+    unsigned barrier[64][64];    // barrier slots: [i][0] count, [i][32] generation
+};
+static_assert(sizeof(WsHeader) <= 32768, "workspace header exceeds 32 KiB");
+constexpr size_t kWsHeaderBytes = 32768;
+
+}  // namespace spec
