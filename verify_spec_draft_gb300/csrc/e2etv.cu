@@ -10,101 +10,135 @@
 // and s = sum_{q<p} q, which need (1)'s normalisers, (3) the gradient, which needs
 // kappa and so every a of the branch.  A branch (Wb row pairs) is handled by a
 // GROUP of CTAs; each CTA stages its column slice of all 2*Wb rows in shared memory
-// once, so HBM sees each logit read once and each gradient written once (6 bytes
-// per entry), and the sweeps run from shared memory.  Groups move through branches
-// independently; inside a group two bounded barriers (after sweeps 1 and 2) exchange
-// per-CTA partials through global memory.  The grid is one cooperative launch with
-// several CTAs per SM, so one CTA's barrier wait overlaps another's sweeps.
+// with TMA bulk copies, so HBM sees each logit read once and each gradient written
+// once (6 bytes per entry), and the sweeps run from shared memory.  Groups move
+// through branches independently; inside a group two bounded barriers (after sweeps 1
+// and 2) exchange per-CTA partials through global memory.  Sweep 2 keeps the q < p
+// test as one bit per entry, so the target rows are free after it: the next branch's
+// target rows are fetched while the group waits at the second barrier and sweep 3
+// runs, and its draft rows as soon as sweep 3 is done.
 //
-// Exponentials use the log-sum-exp form p_v = exp(l_v - LSE_p); the test q_v < p_v
-// is taken on logits, d_v - LSE_q < l_v - LSE_p, and min(p, q) = exp(min(...)).
+// Arithmetic is base 2 on FFMA-scaled logits: p_v = 2^(l_v log2e - LSE2_p), LSE2 the
+// log2 of the row normaliser; q_v < p_v is decided on the exponents; min(p, q) =
+// 2^(min of the exponents).  Each exponential is one FFMA and one MUFU ex2; the row
+// maximum uses packed bf16x2 max with NaN propagation, which also flags invalid rows.
+#include <cuda_bf16.h>
+
 #include "spec_device.cuh"
 #include "internal.h"
 
 namespace spec {
 
-constexpr int kE2Smem = 110 * 1024;   // staging budget per CTA (2 CTAs per SM)
+constexpr int kE2Smem = 110 * 1024;   // staging budget per CTA at two CTAs per SM
 
-// Reads the 8 elements at columns k..k+7 of a row as float: one 16-byte load from
-// shared or global memory on the vector path, else scalar loads with -inf past ncol.
-template <bool STAGED, bool VEC>
-__device__ __forceinline__ void load8(const bf16_t* row, int k, int ncol, float (&o)[8]) {
-    if (!VEC) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) o[e] = (k + e < ncol) ? load_one(row + k + e) : -INFINITY;
-        return;
-    }
-    const bf16_t* p = row + k;
+// ---------------------------------------------------------------------------------
+// 8-entry groups: one 16-byte word of bf16 from shared (staged) or global memory.
+// ---------------------------------------------------------------------------------
+template <bool STAGED>
+__device__ __forceinline__ uint4 ld16(const bf16_t* p) {
     uint4 v;
     if (STAGED) {
-        const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
-        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(smem_u32(p)));
     } else {
-        asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+        v = __ldg(reinterpret_cast<const uint4*>(p));
     }
-    o[0] = __uint_as_float(v.x << 16); o[1] = __uint_as_float(v.x & 0xffff0000u);
-    o[2] = __uint_as_float(v.y << 16); o[3] = __uint_as_float(v.y & 0xffff0000u);
-    o[4] = __uint_as_float(v.z << 16); o[5] = __uint_as_float(v.z & 0xffff0000u);
-    o[6] = __uint_as_float(v.w << 16); o[7] = __uint_as_float(v.w & 0xffff0000u);
+    return v;
+}
+__device__ __forceinline__ float lo_bf(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float hi_bf(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Scalar path (V not a multiple of 8): the same 8-entry group with -inf past ncol.
+__device__ __forceinline__ uint4 ld16_scalar(const bf16_t* row, int k, int ncol) {
+    uint32_t h[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        h[e] = (k + e < ncol) ? (uint32_t)__ldg(reinterpret_cast<const unsigned short*>(row) + k + e) : 0xff80u;
+    return make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
 }
 
+template <bool STAGED, bool VEC>
+__device__ __forceinline__ uint4 group8(const bf16_t* row, int k, int ncol) {
+    if (VEC) return ld16<STAGED>(row + k);
+    return ld16_scalar(row, k, ncol);
+}
+
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// Two floats rounded to nearest-even bf16, lo in the low half.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    const uint32_t a = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo));
-    const uint32_t b = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi));
-    return a | (b << 16);
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
 }
 
-// Row access for one branch: staged rows live in shared memory (row stride `cols`),
-// unstaged rows are read from global memory (row stride V).  Columns are relative to
-// the CTA's first column c0; `ncol` is a multiple of 8 on the vector path.
+// Rows of one branch: staged in shared memory (stride cols) or read from global.
 struct Rows {
-    const bf16_t* tgt;   // row 0 of the target slice
-    const bf16_t* drf;   // row 0 of the draft slice
+    const bf16_t* tgt;
+    const bf16_t* drf;
     size_t stride;
 };
 
+// Sweep 1 for one row slice: (m2, s) with s = sum 2^(x log2e - m2), m2 = max*log2e;
+// bad if the slice holds NaN or +inf.
 template <bool STAGED, bool VEC>
-__device__ __forceinline__ void sweep_stats(const Rows& rw, int i, bool is_draft, int ncol, Stat& out, int& bad) {
+__device__ __forceinline__ void sweep_stats(const bf16_t* row, int ncol, Stat2& out, int& bad) {
     const int lane = threadIdx.x & 31;
-    const bf16_t* row = (is_draft ? rw.drf : rw.tgt) + (size_t)i * rw.stride;
-    float m = -INFINITY;
+    uint32_t mx2 = 0xff80ff80u;   // (-inf, -inf)
     for (int k = lane * 8; k < ncol; k += 256) {
-        float x[8];
-        load8<STAGED, VEC>(row, k, ncol, x);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) { bad |= bad_logit(x[e]) ? 1 : 0; m = fmaxf(m, x[e]); }
+        const uint4 w = group8<STAGED, VEC>(row, k, ncol);
+        mx2 = bmax2(mx2, bmax2(bmax2(w.x, w.y), bmax2(w.z, w.w)));
     }
-    m = warp_max(m);
-    float s = 0.0f;
-    if (m != -INFINITY) {
-        for (int k = lane * 8; k < ncol; k += 256) {
-            float x[8];
-            load8<STAGED, VEC>(row, k, ncol, x);
+    float m = fmaxf(lo_bf(mx2), hi_bf(mx2));
+    if (isnan(lo_bf(mx2)) || isnan(hi_bf(mx2))) m = NAN;
+    // warp max with NaN propagation
 #pragma unroll
-            for (int e = 0; e < 8; ++e) s += expf(x[e] - m);
+    for (int o = 16; o > 0; o >>= 1) {
+        const float y = __shfl_xor_sync(0xffffffffu, m, o);
+        m = (isnan(m) || isnan(y)) ? NAN : fmaxf(m, y);
+    }
+    bad = (isnan(m) || m == INFINITY) ? 1 : 0;
+    float s0 = 0.0f, s1 = 0.0f;
+    const float m2 = m * kLog2e;
+    if (!bad && m != -INFINITY) {
+        for (int k = lane * 8; k < ncol; k += 256) {
+            const uint4 w = group8<STAGED, VEC>(row, k, ncol);
+            s0 += ex2(fmaf(lo_bf(w.x), kLog2e, -m2)) + ex2(fmaf(hi_bf(w.x), kLog2e, -m2));
+            s1 += ex2(fmaf(lo_bf(w.y), kLog2e, -m2)) + ex2(fmaf(hi_bf(w.y), kLog2e, -m2));
+            s0 += ex2(fmaf(lo_bf(w.z), kLog2e, -m2)) + ex2(fmaf(hi_bf(w.z), kLog2e, -m2));
+            s1 += ex2(fmaf(lo_bf(w.w), kLog2e, -m2)) + ex2(fmaf(hi_bf(w.w), kLog2e, -m2));
         }
     }
-    out = Stat{m, warp_sum(s)};
+    out = Stat2{(bad || m == -INFINITY) ? -INFINITY : m2, warp_sum(s0 + s1)};
 }
 
+// Sweep 2 for one row pair: a = sum min(p, q), s = sum_{q<p} q; the q < p bits of
+// each 8-entry group go to mask[k/8].
 template <bool STAGED, bool VEC>
-__device__ __forceinline__ void sweep_overlap(const Rows& rw, int i, int ncol, float lse_p, float lse_q,
-                                              float& a, float& s) {
+__device__ __forceinline__ void sweep_overlap(const bf16_t* tr, const bf16_t* dr, int ncol, float lse_p,
+                                              float lse_q, uint8_t* mask, float& a, float& s) {
     const int lane = threadIdx.x & 31;
-    const bf16_t* tr = rw.tgt + (size_t)i * rw.stride;
-    const bf16_t* dr = rw.drf + (size_t)i * rw.stride;
     float sa = 0.0f, ss = 0.0f;
     for (int k = lane * 8; k < ncol; k += 256) {
-        float l[8], d[8];
-        load8<STAGED, VEC>(tr, k, ncol, l);
-        load8<STAGED, VEC>(dr, k, ncol, d);
+        const uint4 wl = group8<STAGED, VEC>(tr, k, ncol);
+        const uint4 wd = group8<STAGED, VEC>(dr, k, ncol);
+        const uint32_t l4[4] = {wl.x, wl.y, wl.z, wl.w};
+        const uint32_t d4[4] = {wd.x, wd.y, wd.z, wd.w};
+        uint32_t bits = 0;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const float lp = l[e] - lse_p, lq = d[e] - lse_q;
-            const float mn = expf(fminf(lp, lq));
-            sa += mn;
-            ss += (lq < lp) ? mn : 0.0f;
+        for (int h = 0; h < 4; ++h) {
+            const float lp0 = fmaf(lo_bf(l4[h]), kLog2e, -lse_p), lq0 = fmaf(lo_bf(d4[h]), kLog2e, -lse_q);
+            const float lp1 = fmaf(hi_bf(l4[h]), kLog2e, -lse_p), lq1 = fmaf(hi_bf(d4[h]), kLog2e, -lse_q);
+            const float m0 = ex2(fminf(lp0, lq0)), m1 = ex2(fminf(lp1, lq1));
+            sa += m0 + m1;
+            if (lq0 < lp0) { ss += m0; bits |= 1u << (2 * h); }
+            if (lq1 < lp1) { ss += m1; bits |= 2u << (2 * h); }
         }
+        mask[k >> 3] = (uint8_t)bits;
     }
     a = warp_sum(sa);
     s = warp_sum(ss);
@@ -112,70 +146,93 @@ __device__ __forceinline__ void sweep_overlap(const Rows& rw, int i, int ncol, f
 
 template <bool STAGED, bool VEC>
 __global__ void __launch_bounds__(kThreads) e2etv_kernel(E2etvParams p) {
-    extern __shared__ uint4 s_dyn[];
-    bf16_t* s_rows = reinterpret_cast<bf16_t*>(s_dyn);
+    extern __shared__ __align__(128) uint8_t s_dyn[];
     const int Wb = p.Wb, nr = 2 * Wb;
     const int g = blockIdx.x / p.group_size;
     const int gi = blockIdx.x - g * p.group_size;
     const long V = p.V;
     const long c0 = (long)gi * p.cols;
     const int ncol = (int)max(0L, min(V, c0 + p.cols) - c0);
+    const int ngroups8 = (p.cols + 7) / 8;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // shared layout: [STAGED: target rows | draft rows] | q<p bits, one byte per 8 entries
+    bf16_t* s_tgt = reinterpret_cast<bf16_t*>(s_dyn);
+    bf16_t* s_drf = s_tgt + (STAGED ? (size_t)Wb * p.cols : 0);
+    uint8_t* s_mask = reinterpret_cast<uint8_t*>(s_drf + (STAGED ? (size_t)Wb * p.cols : 0));
     __shared__ float s_lse[2 * SPEC_MAX_GAMMA];
-    __shared__ float s_a[SPEC_MAX_GAMMA], s_s[SPEC_MAX_GAMMA], s_kappa[SPEC_MAX_GAMMA];
+    __shared__ float s_a[SPEC_MAX_GAMMA], s_s[SPEC_MAX_GAMMA], s_c1[SPEC_MAX_GAMMA], s_c0[SPEC_MAX_GAMMA];
     __shared__ int s_bad;
+    __shared__ __align__(8) uint64_t s_bar[2];   // [0] target rows, [1] draft rows
     unsigned* bar = p.barriers + (size_t)g * 64;
     float2* part = p.partials + (size_t)g * 2 * p.group_size * nr;
+    float2* part2 = part + (size_t)p.group_size * nr;
     const double inv_total = 1.0 / ((double)p.n_branches * Wb);
-    const bool active = g < p.n_groups;
+    const unsigned bytes = (unsigned)ncol * 2u;
+    unsigned ph_t = 0, ph_d = 0;
 
-    for (int n = g; active && n < p.n_branches; n += p.n_groups) {
-        const bf16_t* gt = p.target + (size_t)n * Wb * V + c0;
-        const bf16_t* gd = p.draft + (size_t)n * Wb * V + c0;
+    // TMA bulk loads of one half (target or draft rows) of branch n's slice
+    auto issue = [&](int n, int half) {
+        if (!STAGED || ncol == 0 || n >= p.n_branches) return;
+        const bf16_t* src = (half == 0 ? p.target : p.draft) + (size_t)n * Wb * V + c0;
+        bf16_t* dst = half == 0 ? s_tgt : s_drf;
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&s_bar[half], bytes * (unsigned)Wb);
+        for (int i = 0; i < Wb; ++i) bulk_g2s(dst + (size_t)i * p.cols, src + (size_t)i * V, bytes, &s_bar[half]);
+    };
+
+    if (STAGED) {
+        if (threadIdx.x == 0) {
+            mbar_init(&s_bar[0], 1);
+            mbar_init(&s_bar[1], 1);
+            fence_mbar_init();
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) { issue(g, 0); issue(g, 1); }
+    }
+
+    for (int n = g; n < p.n_branches; n += p.n_groups) {
         Rows rw;
         if (STAGED) {
-            // stage the slice of the 2*Wb rows (16-byte vector copies)
-            const int nv = ncol / 8;
-            for (int idx = threadIdx.x; idx < nr * nv; idx += blockDim.x) {
-                const int i = idx / nv, k = (idx - i * nv) * 8;
-                const bf16_t* src = (i < Wb ? gt : gd) + (size_t)(i % Wb) * V + k;
-                uint4 v;
-                asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                             : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(src));
-                *reinterpret_cast<uint4*>(s_rows + (size_t)i * p.cols + k) = v;
+            if (ncol > 0) {
+                if (!mbar_wait(&s_bar[0], ph_t, p.status, kWaitLimitNs) ||
+                    !mbar_wait(&s_bar[1], ph_d, p.status, kWaitLimitNs)) {
+                    mbar_wait(&s_bar[0], ph_t, p.status, kWaitLimitNs);   // let copies in flight land
+                    mbar_wait(&s_bar[1], ph_d, p.status, kWaitLimitNs);
+                    return;
+                }
+                ph_t ^= 1u;
+                ph_d ^= 1u;
             }
-            __syncthreads();
-            rw.tgt = s_rows;
-            rw.drf = s_rows + (size_t)Wb * p.cols;
+            rw.tgt = s_tgt;
+            rw.drf = s_drf;
             rw.stride = p.cols;
         } else {
-            rw.tgt = gt;
-            rw.drf = gd;
+            rw.tgt = p.target + (size_t)n * Wb * V + c0;
+            rw.drf = p.draft + (size_t)n * Wb * V + c0;
             rw.stride = V;
         }
 
         // sweep 1: per-row max and sum-exp of this CTA's slice
         for (int i = warp; i < nr; i += kWarps) {
-            Stat st;
+            Stat2 st;
             int bad = 0;
-            sweep_stats<STAGED, VEC>(rw, i % Wb, i >= Wb, ncol, st, bad);
-            bad = warp_or(bad);
+            sweep_stats<STAGED, VEC>((i < Wb ? rw.tgt : rw.drf) + (size_t)(i % Wb) * rw.stride, ncol, st, bad);
             if (lane == 0) {
-                part[(size_t)gi * nr + i] = make_float2(st.m, st.s);
+                part[(size_t)gi * nr + i] = make_float2(st.m2, st.s);
                 if (bad) atomicOr(&p.branch_bad[n], 1u);
             }
         }
         if (!block_barrier(bar, p.group_size, p.status)) return;
 
-        // merge the group's partials in CTA order: LSE of every row
+        // merge the group's partials in CTA order: LSE2 of every row
         for (int i = warp; i < nr; i += kWarps) {
-            Stat acc = stat_empty();
+            Stat2 acc = stat2_empty();
             for (int c = lane; c < p.group_size; c += 32) {
                 const float2 v = __ldcg(&part[(size_t)c * nr + i]);
-                acc = stat_merge(acc, Stat{v.x, v.y});
+                acc = stat2_merge(acc, Stat2{v.x, v.y});
             }
-            acc = warp_stat(acc);
-            if (lane == 0) s_lse[i] = (acc.m == -INFINITY) ? NAN : acc.m + logf(acc.s);
+            acc = warp_stat2(acc);
+            if (lane == 0) s_lse[i] = (acc.m2 == -INFINITY) ? NAN : stat2_lse2(acc);
         }
         if (threadIdx.x == 0) s_bad = (__ldcg(&p.branch_bad[n]) != 0u) ? 1 : 0;
         __syncthreads();
@@ -183,15 +240,17 @@ __global__ void __launch_bounds__(kThreads) e2etv_kernel(E2etvParams p) {
         __syncthreads();
         const bool bad_branch = s_bad != 0;
 
-        // sweep 2: overlap a and s of every row pair
-        float2* part2 = part + (size_t)p.group_size * nr;
+        // sweep 2: overlap a and s of every row pair, q<p bits to shared memory
         if (!bad_branch) {
             for (int i = warp; i < Wb; i += kWarps) {
                 float a, s;
-                sweep_overlap<STAGED, VEC>(rw, i, ncol, s_lse[i], s_lse[Wb + i], a, s);
+                sweep_overlap<STAGED, VEC>(rw.tgt + (size_t)i * rw.stride, rw.drf + (size_t)i * rw.stride, ncol,
+                                           s_lse[i], s_lse[Wb + i], s_mask + (size_t)i * ngroups8, a, s);
                 if (lane == 0) part2[(size_t)gi * Wb + i] = make_float2(a, s);
             }
         }
+        __syncthreads();                                   // target rows no longer read
+        if (threadIdx.x == 0) issue(n + p.n_groups, 0);
         if (!block_barrier(bar, p.group_size, p.status)) return;
 
         if (!bad_branch) {
@@ -208,15 +267,18 @@ __global__ void __launch_bounds__(kThreads) e2etv_kernel(E2etvParams p) {
             }
             __syncthreads();
             if (threadIdx.x == 0) {
-                // kappa_i = P_{i-1} * T_i / (N*Wb), T_i = 1 + a_{i+1} T_{i+1}, T_last = 1
+                // kappa_i = P_{i-1} * T_i / (N*Wb), T_i = 1 + a_{i+1} T_{i+1}, T_last = 1;
+                // grad = q * kappa (s - 1) where q < p, q * kappa s elsewhere
                 float T = 1.0f;
                 for (int i = Wb - 1; i >= 0; --i) {
-                    s_kappa[i] = T;
+                    s_c1[i] = T;
                     if (i > 0) T = 1.0f + s_a[i] * T;
                 }
                 float P = 1.0f, sum_s = 0.0f;
                 for (int i = 0; i < Wb; ++i) {
-                    s_kappa[i] = (float)((double)(P * s_kappa[i]) * inv_total);
+                    const float kap = (float)((double)(P * s_c1[i]) * inv_total);
+                    s_c1[i] = kap * (s_s[i] - 1.0f);
+                    s_c0[i] = kap * s_s[i];
                     P *= s_a[i];
                     sum_s += P;
                     if (gi == 0) {
@@ -235,40 +297,42 @@ __global__ void __launch_bounds__(kThreads) e2etv_kernel(E2etvParams p) {
             p.branch_sum[n] = NAN;
         }
 
-        // sweep 3: gradient of the loss w.r.t. the draft logits, rounded once to bf16
+        // sweep 3: gradient w.r.t. the draft logits, rounded once to bf16
         {
             const int ng = (ncol + 7) / 8;
             for (int idx = threadIdx.x; idx < Wb * ng; idx += blockDim.x) {
                 const int i = idx / ng, k = (idx - i * ng) * 8;
-                float gv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                uint4 out = make_uint4(0u, 0u, 0u, 0u);
                 if (!bad_branch) {
-                    float l[8], d[8];
-                    load8<STAGED, VEC>(rw.tgt + (size_t)i * rw.stride, k, ncol, l);
-                    load8<STAGED, VEC>(rw.drf + (size_t)i * rw.stride, k, ncol, d);
-                    const float lse_p = s_lse[i], lse_q = s_lse[Wb + i];
-                    const float kap = -s_kappa[i], si = s_s[i];
+                    const uint4 wd = group8<STAGED, VEC>(rw.drf + (size_t)i * rw.stride, k, ncol);
+                    const uint32_t bits = s_mask[(size_t)i * ngroups8 + (k >> 3)];
+                    const float lse_q = s_lse[Wb + i], c1 = s_c1[i], c0v = s_c0[i];
+                    const uint32_t d4[4] = {wd.x, wd.y, wd.z, wd.w};
+                    uint32_t o4[4];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float lq = d[e] - lse_q;
-                        const float q = expf(lq);
-                        const float ind = (lq < l[e] - lse_p) ? 1.0f : 0.0f;
-                        gv[e] = kap * q * (ind - si);
+                    for (int h = 0; h < 4; ++h) {
+                        const float q0 = ex2(fmaf(lo_bf(d4[h]), kLog2e, -lse_q));
+                        const float q1 = ex2(fmaf(hi_bf(d4[h]), kLog2e, -lse_q));
+                        const float g0 = q0 * (((bits >> (2 * h)) & 1u) ? c1 : c0v);
+                        const float g1 = q1 * (((bits >> (2 * h + 1)) & 1u) ? c1 : c0v);
+                        o4[h] = pack_bf16x2(g0, g1);
                     }
+                    out = make_uint4(o4[0], o4[1], o4[2], o4[3]);
                 }
                 uint16_t* dst = p.grad_out + ((size_t)n * Wb + i) * V + c0 + k;
                 if (VEC) {
-                    const uint4 out = make_uint4(pack_bf16x2(gv[0], gv[1]), pack_bf16x2(gv[2], gv[3]),
-                                                 pack_bf16x2(gv[4], gv[5]), pack_bf16x2(gv[6], gv[7]));
                     asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};"
                                  :: "l"(dst), "r"(out.x), "r"(out.y), "r"(out.z), "r"(out.w) : "memory");
                 } else {
+                    const uint32_t o4[4] = {out.x, out.y, out.z, out.w};
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
-                        if (k + e < ncol) dst[e] = __bfloat16_as_ushort(__float2bfloat16_rn(gv[e]));
+                        if (k + e < ncol) dst[e] = (uint16_t)((o4[e >> 1] >> (16 * (e & 1))) & 0xffffu);
                 }
             }
         }
-        __syncthreads();   // the next branch overwrites the staged rows
+        __syncthreads();                                   // draft rows no longer read
+        if (threadIdx.x == 0) issue(n + p.n_groups, 1);
     }
 
     // loss = 1 - mean S, summed over branches in order by the last CTA to finish
@@ -298,7 +362,6 @@ __global__ void __launch_bounds__(kThreads) e2etv_kernel(E2etvParams p) {
 // ----------------------------------------------------------------------------------
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Upper bound on the grid: 152 SMs x 2 CTAs plus headroom for other parts.
 constexpr int kE2MaxGrid = 1024;
 
 size_t e2etv_workspace_bytes(int n_branches, int Wb, int V) {
@@ -313,10 +376,8 @@ size_t e2etv_workspace_bytes(int n_branches, int Wb, int V) {
 template <bool STAGED, bool VEC>
 static cudaError_t launch_typed(E2etvParams& p, size_t smem, int grid, cudaStream_t stream) {
     auto kern = e2etv_kernel<STAGED, VEC>;
-    if (smem > 0) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-    }
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
     E2etvParams args = p;
     void* kargs[] = {&args};
     return cudaLaunchCooperativeKernel((const void*)kern, dim3(grid), dim3(kThreads), kargs, smem, stream);
@@ -325,8 +386,7 @@ static cudaError_t launch_typed(E2etvParams& p, size_t smem, int grid, cudaStrea
 template <bool STAGED, bool VEC>
 static int occupancy(size_t smem) {
     auto kern = e2etv_kernel<STAGED, VEC>;
-    if (smem > 0 && cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-        return 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
     int occ = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, smem) != cudaSuccess) return 0;
     return occ;
@@ -346,15 +406,15 @@ cudaError_t e2etv_launch(E2etvParams& p, void* ws, cudaStream_t stream) {
     p.branch_bad = reinterpret_cast<unsigned*>(w + off);
 
     const int sms = device_sm_count();
-    // Plan: up to four groups; a staged plan needs every CTA's slice of the 2*Wb rows
-    // within the shared-memory budget, which sets the smallest group.
+    // Plan: up to four groups.  A staged plan needs every CTA's slice of the 2*Wb rows
+    // (plus its q<p bits) within the shared-memory budget, which sets the smallest group.
     for (int per_sm = 2; per_sm >= 1; --per_sm) {
         int grid = sms * per_sm;
         if (grid > kE2MaxGrid) grid = kE2MaxGrid;
         bool staged = false;
         int n_groups = 0, group_size = 0;
         const long budget = per_sm == 2 ? kE2Smem : 2 * kE2Smem;
-        const long cols_max = (budget / (4L * p.Wb)) / 8 * 8;
+        const long cols_max = ((budget - 64) * 8 / (32L * p.Wb + p.Wb)) / 8 * 8;
         if (p.vec_ok && cols_max >= 64) {
             const long need = (p.V + cols_max - 1) / cols_max;
             if (need <= grid) {
@@ -371,19 +431,20 @@ cudaError_t e2etv_launch(E2etvParams& p, void* ws, cudaStream_t stream) {
         }
         long cols = (p.V + group_size - 1) / group_size;
         cols = (cols + 7) / 8 * 8;
-        const size_t smem = staged ? (size_t)2 * p.Wb * cols * sizeof(uint16_t) : 0;
+        const size_t mask_bytes = align_up((size_t)p.Wb * (size_t)(cols / 8), 16);
+        const size_t smem = (staged ? (size_t)2 * p.Wb * cols * sizeof(uint16_t) : 0) + mask_bytes;
         int occ;
         if (staged) occ = occupancy<true, true>(smem);
-        else if (p.vec_ok) occ = occupancy<false, true>(0);
-        else occ = occupancy<false, false>(0);
+        else if (p.vec_ok) occ = occupancy<false, true>(smem);
+        else occ = occupancy<false, false>(smem);
         if (occ < per_sm) continue;
         p.n_groups = n_groups;
         p.group_size = group_size;
         p.cols = (int)cols;
         grid = n_groups * group_size;
         if (staged) return launch_typed<true, true>(p, smem, grid, stream);
-        if (p.vec_ok) return launch_typed<false, true>(p, 0, grid, stream);
-        return launch_typed<false, false>(p, 0, grid, stream);
+        if (p.vec_ok) return launch_typed<false, true>(p, smem, grid, stream);
+        return launch_typed<false, false>(p, smem, grid, stream);
     }
     return cudaErrorInvalidConfiguration;
 }

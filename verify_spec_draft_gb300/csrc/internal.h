@@ -29,13 +29,12 @@ struct VerifyParams {
     // workspace regions
     unsigned* status;
     unsigned* done;            // header done[] counters
+    unsigned* barrier;         // grid barrier slot (T=1)
     unsigned long long* keys;  // [B*(gamma+1)] argmax keys (T=0)
-    unsigned* rowbad;          // [B*(2*gamma+1)]
-    float2* stats;             // [B*(2*gamma+1)*nchunk] (m, s)
-    unsigned* done1;           // [B]
-    unsigned* done2;           // [B]
-    int4* state;               // [B*2]: mode, n, near, pad | mp, Zp, mq, Zq (as float bits)
-    float2* ksums;             // [B*nchunk] (residual sum, p sum) per chunk
+    unsigned* rowbad;          // [B*(gamma+1)] (T=0)
+    float2* stats;             // [B*(2*gamma+1)*nchunk*8] (m2, s) per warp segment (T=1)
+    int4* state;               // [B*2]: mode, n, near, pad | m2p, sp, m2q, sq (float bits)
+    float2* ksums;             // [B*nchunk*8] (residual sum, p sum) per warp segment
 };
 
 size_t verify_workspace_bytes(int B, int gamma, int V);
@@ -62,7 +61,8 @@ struct DraftParams {
     // workspace regions
     unsigned* status;
     unsigned* barrier;         // one barrier slot
-    float4* tile_stats;        // [R * n_tiles]: m, s, argmax index bits, bad
+    float4* tile_rec;          // [R * n_tiles] per-tile records (T=1): max, sum, argmax, bad
+    float4* cta_rec;           // [R * grid] per-(row, CTA) records
     int32_t* tokbuf;           // [2 * R] fixed-point iterates
     unsigned* changed;         // [gamma + 2]
 };

@@ -169,6 +169,46 @@ __device__ __forceinline__ float warp_inclusive_scan(float x) {
 }
 
 // ---------------------------------------------------------------------------------
+// Base-2 softmax statistics for the streaming loops.  A row's weights are
+// w_v = 2^(x_v*log2e - m2) for a reference m2 (in practice fl(max*log2e)); the
+// product x*log2e is formed exactly inside one FFMA, so each weight costs one FFMA and
+// one MUFU ex2.  Merging two partials rescales by 2^(m2_a - m2) with the same m2_a
+// the partial was summed against, so the rounding of m2_a cancels; only per-operation
+// rounding remains.  Normalised quantities (p_v = w_v / sum w) equal exp(x_v - m)/Z
+// up to float32 rounding and the 1.3e-8 relative error of log2e in float32.
+// ---------------------------------------------------------------------------------
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+// 2^(x*log2e - m2)
+__device__ __forceinline__ float wexp(float x, float m2) { return ex2(fmaf(x, kLog2e, -m2)); }
+
+struct Stat2 { float m2; float s; };   // s = sum 2^(x*log2e - m2); empty: (-inf, 0)
+
+__device__ __forceinline__ Stat2 stat2_empty() { return Stat2{-INFINITY, 0.0f}; }
+__device__ __forceinline__ Stat2 stat2_merge(Stat2 a, Stat2 b) {
+    if (b.m2 == -INFINITY) return a;
+    if (a.m2 == -INFINITY) return b;
+    const float m = fmaxf(a.m2, b.m2);
+    return Stat2{m, a.s * ex2(a.m2 - m) + b.s * ex2(b.m2 - m)};
+}
+__device__ __forceinline__ Stat2 warp_stat2(Stat2 a) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const Stat2 b{__shfl_xor_sync(0xffffffffu, a.m2, o), __shfl_xor_sync(0xffffffffu, a.s, o)};
+        a = stat2_merge(a, b);   // symmetric: both lanes of a pair get the same bits
+    }
+    return a;
+}
+// log2 of the row's normaliser in the same base: LSE2 = m2 + log2(s); then the
+// probability of x is 2^(x*log2e - LSE2).
+__device__ __forceinline__ float stat2_lse2(Stat2 a) { return a.m2 + log2f(a.s); }
+
+// ---------------------------------------------------------------------------------
 // Memory-model helpers and the bounded barrier.
 // ---------------------------------------------------------------------------------
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
@@ -245,6 +285,48 @@ __device__ __forceinline__ bool last_block_done(unsigned* counter, unsigned expe
     }
     __syncthreads();
     return s_last != 0;
+}
+
+// ---------------------------------------------------------------------------------
+// mbarrier + TMA bulk copies (global -> shared), with a bounded wait.
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+// 1-D bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned).
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
+    uint32_t ok;
+    asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+                 : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+// Wait for phase `parity` of the barrier to complete, for at most `limit_ns`.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity, unsigned* status,
+                                          unsigned long long limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > limit_ns) {
+            atomicOr(status, SPEC_DEV_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
 }
 
 // Workspace header (32 KiB at the start of every workspace).

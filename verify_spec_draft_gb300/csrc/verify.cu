@@ -6,39 +6,115 @@
 // matching prefix is accepted.  T=1 is standard rejection sampling with a residual or
 // bonus draw (the pages' overlap 1 - TV is its acceptance probability).
 //
-// Design (HBM-bound; one pass over every row):
-//   T=0  one kernel.  Work items are (row, 8192-element chunk); each CTA reduces a
-//        chunk to a 64-bit argmax key (value, lowest index) and merges it with one
-//        atomicMax.  The last CTA to finish ("last CTA done" counter, no waiting)
-//        scans every request's prefix and writes the outputs.
-//   T=1  two kernels.  (1) Softmax statistics (max, sum exp) of every target and
-//        draft row per chunk; the CTA that completes a request's last chunk merges
-//        that request's rows in chunk order, runs the gamma accept tests in
-//        parallel, and records the row to sample from.  (2) For each request one
-//        row pair (residual) or one row (bonus) is re-read in chunks to get its
-//        weight per chunk in vocabulary order; the CTA completing a request finds
-//        the chunk holding u * sum and scans inside it.
+// Design (HBM-bound; every row streamed once):
+//   Work items are (row, 8192-entry chunk); a persistent grid walks them with the next
+//   item's 16-byte loads in flight while the current one is reduced (register double
+//   buffering), each thread holding 32 contiguous entries.
+//   T=0  one kernel.  Each warp folds its entries into a 64-bit argmax key (value,
+//        lowest index) and merges it with one atomicMax per row.  The last CTA to
+//        finish ("last CTA done" counter, no waiting) scans every request's prefix,
+//        one warp per request, and writes the outputs.
+//   T=1  one cooperative kernel in four phases separated by bounded grid barriers:
+//        (1) base-2 softmax statistics of every target and draft row, one partial per
+//        1024-entry warp segment; (2) per request, merge its rows in order, run the
+//        gamma accept tests in parallel, record the row to sample from; (3) re-read
+//        that row pair (residual) or row (bonus) for its weight per segment in
+//        vocabulary order; (4) per request, locate the segment holding u * sum and
+//        the entry inside it.  No counters or fences in the streaming phases.
 #include "spec_device.cuh"
 #include "internal.h"
 
 namespace spec {
 
-constexpr int kEPT = kVerifyChunk / kThreads;   // 32 contiguous elements per thread
+constexpr int kEPT = kVerifyChunk / kThreads;   // 32 contiguous entries per thread
+static_assert(kEPT == 32, "chunk layout");
 
 enum { MODE_DONE = 0, MODE_RESID = 1, MODE_BONUS = 2 };
 
-// Loads this thread's 32 contiguous elements of chunk `c` of a row (-inf past V).
-template <typename T>
-__device__ __forceinline__ void load_chunk(const T* row, long V, int c, bool vec_ok, float (&x)[kEPT]) {
-    constexpr int N = VecTraits<T>::N;
-    const long base = (long)c * kVerifyChunk + (long)threadIdx.x * kEPT;
+// ----------------------------------------------------------------------------------
+// Raw chunk loads: this thread's 32 entries as 16-byte words, -inf past the row end.
+// ----------------------------------------------------------------------------------
+template <typename T> struct Words { static constexpr int N = kEPT * (int)sizeof(T) / 16; };
+
+__device__ __forceinline__ uint4 partial_words(const float* row, long e0, long V) {
+    uint32_t w[4];
 #pragma unroll
-    for (int g = 0; g < kEPT / N; ++g) {
-        float v[N];
-        load_group<T, N>(row, base + g * N, V, vec_ok, v);
+    for (int e = 0; e < 4; ++e) w[e] = (e0 + e < V) ? __float_as_uint(__ldg(row + e0 + e)) : 0xff800000u;
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+__device__ __forceinline__ uint4 partial_words(const bf16_t* row, long e0, long V) {
+    uint32_t h[8];
 #pragma unroll
-        for (int e = 0; e < N; ++e) x[g * N + e] = v[e];
+    for (int e = 0; e < 8; ++e)
+        h[e] = (e0 + e < V) ? (uint32_t)__ldg(reinterpret_cast<const unsigned short*>(row) + e0 + e) : 0xff80u;
+    return make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
+}
+
+template <typename T, int NW>
+__device__ __forceinline__ void load_words(uint4 (&w)[NW], const T* row, long V, long base, bool vec_ok) {
+    constexpr int EPV = 16 / (int)sizeof(T);
+#pragma unroll
+    for (int i = 0; i < Words<T>::N; ++i) {
+        const long e0 = base + (long)i * EPV;
+        if (vec_ok && e0 + EPV <= V) w[i] = __ldg(reinterpret_cast<const uint4*>(row + e0));
+        else w[i] = partial_words(row, e0, V);
     }
+}
+
+template <typename T, int NW>
+__device__ __forceinline__ void decode_words(const uint4 (&w)[NW], float (&x)[kEPT]) {
+    if (sizeof(T) == 2) {
+#pragma unroll
+        for (int i = 0; i < kEPT / 8; ++i) {
+            const uint32_t a[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                x[8 * i + 2 * k] = __uint_as_float(a[k] << 16);
+                x[8 * i + 2 * k + 1] = __uint_as_float(a[k] & 0xffff0000u);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < kEPT / 4; ++i) {
+            x[4 * i] = __uint_as_float(w[i].x);
+            x[4 * i + 1] = __uint_as_float(w[i].y);
+            x[4 * i + 2] = __uint_as_float(w[i].z);
+            x[4 * i + 3] = __uint_as_float(w[i].w);
+        }
+    }
+}
+
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t bmax2_nan(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+// Max of this thread's 32 entries, NaN if any is NaN (bf16: packed pairs).
+template <typename T, int NW>
+__device__ __forceinline__ float chunk_max_nan(const uint4 (&w)[NW]) {
+    if (sizeof(T) == 2) {
+        uint32_t m = bmax2_nan(bmax2_nan(w[0].x, w[0].y), bmax2_nan(w[0].z, w[0].w));
+#pragma unroll
+        for (int i = 1; i < kEPT / 8; ++i)
+            m = bmax2_nan(m, bmax2_nan(bmax2_nan(w[i].x, w[i].y), bmax2_nan(w[i].z, w[i].w)));
+        return fmax_nan(__uint_as_float(m << 16), __uint_as_float(m & 0xffff0000u));
+    }
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kEPT / 4; ++i)
+        m = fmax_nan(fmax_nan(m, fmax_nan(__uint_as_float(w[i].x), __uint_as_float(w[i].y))),
+                     fmax_nan(__uint_as_float(w[i].z), __uint_as_float(w[i].w)));
+    return m;
+}
+__device__ __forceinline__ float warp_max_nan(float m) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmax_nan(m, __shfl_xor_sync(0xffffffffu, m, o));
+    return m;
 }
 
 __device__ __forceinline__ long thread_base(int c) {
@@ -52,145 +128,205 @@ template <typename TT>
 __global__ void __launch_bounds__(kThreads) verify_t0_kernel(VerifyParams p) {
     const TT* target = static_cast<const TT*>(p.target);
     const long V = p.V;
-    const int rows = p.B * (p.gamma + 1);
-    const long items = (long)rows * p.nchunk;
-    __shared__ unsigned long long s_key[kWarps];
-    __shared__ int s_bad[kWarps];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const long items = (long)p.B * (p.gamma + 1) * p.nchunk;
+    const bool vec = p.vec_t != 0;
+    constexpr int NW = Words<TT>::N;
+    uint4 cur[NW], nxt[NW];
 
-    for (long it = blockIdx.x; it < items; it += gridDim.x) {
-        const int row = (int)(it / p.nchunk);
-        const int c = (int)(it - (long)row * p.nchunk);
-        float x[kEPT];
-        load_chunk<TT>(target + (size_t)row * V, V, c, p.vec_t != 0, x);
-        const long base = thread_base(c);
-        unsigned long long key = 0ull;
-        int bad = 0;
+    long it = blockIdx.x;
+    if (it < items) {
+        const int row = (int)(it / p.nchunk), c = (int)(it - (long)row * p.nchunk);
+        load_words<TT, NW>(cur, target + (size_t)row * V, V, thread_base(c), vec);
+    }
+    for (; it < items; it += gridDim.x) {
+        const long nx = it + gridDim.x;
+        if (nx < items) {
+            const int row = (int)(nx / p.nchunk), c = (int)(nx - (long)row * p.nchunk);
+            load_words<TT, NW>(nxt, target + (size_t)row * V, V, thread_base(c), vec);
+        }
+        const int row = (int)(it / p.nchunk), c = (int)(it - (long)row * p.nchunk);
+        // NaN-propagating max of the 32 entries (-inf pads the row end), then the
+        // warp max; only lanes holding it look for their lowest index
+        float m = chunk_max_nan<TT, NW>(cur);
+        m = warp_max_nan(m);
+        const int bad = (isnan(m) || m == INFINITY) ? 1 : 0;
+        int idx = 0x7fffffff;
+        if (!bad) {
+            float x[kEPT];
+            decode_words<TT, NW>(cur, x);
+            const long base = thread_base(c);
 #pragma unroll
-        for (int e = 0; e < kEPT; ++e) {
-            if (base + e < V) {
-                bad |= bad_logit(x[e]) ? 1 : 0;
-                const unsigned long long k = argmax_key(x[e], (uint32_t)(base + e));
-                key = k > key ? k : key;
-            }
+            for (int e = kEPT - 1; e >= 0; --e)
+                if (x[e] == m) idx = (int)(base + e);
         }
-        key = warp_max_u64(key);
-        bad = warp_or(bad);
-        if (lane == 0) { s_key[warp] = key; s_bad[warp] = bad; }
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            unsigned long long k = s_key[0];
-            int b = s_bad[0];
-            for (int w = 1; w < kWarps; ++w) { k = s_key[w] > k ? s_key[w] : k; b |= s_bad[w]; }
-            atomicMax(&p.keys[row], k);
-            if (b) atomicOr(&p.rowbad[row], 1u);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) idx = min(idx, __shfl_xor_sync(0xffffffffu, idx, o));
+        if ((threadIdx.x & 31) == 0) {
+            if (bad) atomicOr(&p.rowbad[row], 1u);
+            else atomicMax(&p.keys[row], argmax_key(m, (uint32_t)idx));
         }
-        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < NW; ++i) cur[i] = nxt[i];
     }
 
     if (!last_block_done(&p.done[0], gridDim.x)) return;
 
-    // Prefix scan, one thread per request; resets the keys for the next call.
+    // prefix scan: one warp per request, one lane per row
     const int G = p.gamma;
-    for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
-        bool bad_row = false, bad_tok = false;
-        int n = -1, y = -1;
-        for (int i = 0; i <= G; ++i) {
-            const int row = b * (G + 1) + i;
-            const unsigned long long k = __ldcg(&p.keys[row]);
-            const unsigned rb = __ldcg(&p.rowbad[row]);
-            p.keys[row] = 0ull;
-            p.rowbad[row] = 0u;
-            if (rb || key_value(k) == -INFINITY) bad_row = true;
-            const int am = (int)key_index(k);
-            if (i < G) {
-                const int t = p.tokens[(size_t)b * G + i];
-                if (t < 0 || t >= p.V) bad_tok = true;
-                if (n < 0 && t != am) { n = i; y = am; }
-            } else if (n < 0) {
-                n = G; y = am;
+    const int lane = threadIdx.x & 31;
+    for (int b = threadIdx.x >> 5; b < p.B; b += kWarps) {
+        unsigned long long k3[3] = {0ull, 0ull, 0ull};
+        int tok3[3] = {0, 0, 0};
+        unsigned bad_row = 0, bad_tok = 0, mism[3] = {0u, 0u, 0u};
+#pragma unroll
+        for (int h = 0; h < 3; ++h) {
+            const int i = lane + 32 * h;
+            bool rb = false, tb = false, mm = false;
+            if (i <= G) {
+                const int row = b * (G + 1) + i;
+                k3[h] = __ldcg(&p.keys[row]);
+                rb = __ldcg(&p.rowbad[row]) != 0u || key_value(k3[h]) == -INFINITY;
+                p.keys[row] = 0ull;
+                p.rowbad[row] = 0u;
+                if (i < G) {
+                    tok3[h] = p.tokens[(size_t)b * G + i];
+                    tb = tok3[h] < 0 || tok3[h] >= p.V;
+                    mm = tok3[h] != (int)key_index(k3[h]);
+                }
             }
+            bad_row |= __ballot_sync(0xffffffffu, rb);
+            bad_tok |= __ballot_sync(0xffffffffu, tb);
+            mism[h] = __ballot_sync(0xffffffffu, mm);
         }
+        int n = G;
+        for (int h = 2; h >= 0; --h)
+            if (mism[h]) n = 32 * h + __ffs(mism[h]) - 1;
+        const unsigned long long kn =
+            __shfl_sync(0xffffffffu, n < 32 ? k3[0] : (n < 64 ? k3[1] : k3[2]), n & 31);
+        const int y = (int)key_index(kn);
         int32_t* com = p.committed_out + (size_t)b * (G + 1);
-        if (bad_row || bad_tok) {
-            atomicOr(p.status, (bad_tok ? SPEC_DEV_TOKEN : 0u) | (bad_row ? SPEC_DEV_NONFINITE : 0u));
-            p.n_out[b] = -1;
-            p.bonus_out[b] = -1;
-            for (int i = 0; i <= G; ++i) com[i] = -1;
-        } else {
-            p.n_out[b] = n;
-            p.bonus_out[b] = y;
-            for (int i = 0; i < n; ++i) com[i] = p.tokens[(size_t)b * G + i];
-            com[n] = y;
-            for (int i = n + 1; i <= G; ++i) com[i] = -1;
+        const bool invalid = bad_row || bad_tok;
+#pragma unroll
+        for (int h = 0; h < 3; ++h) {
+            const int i = lane + 32 * h;
+            if (i <= G) com[i] = invalid ? -1 : (i < n ? tok3[h] : (i == n ? y : -1));
         }
-        if (p.near_out) p.near_out[b] = 0;
+        if (lane == 0) {
+            if (invalid) atomicOr(p.status, (bad_tok ? SPEC_DEV_TOKEN : 0u) | (bad_row ? SPEC_DEV_NONFINITE : 0u));
+            p.n_out[b] = invalid ? -1 : n;
+            p.bonus_out[b] = invalid ? -1 : y;
+            if (p.near_out) p.near_out[b] = 0;
+        }
     }
     __syncthreads();
     if (threadIdx.x == 0) p.done[0] = 0u;
 }
 
 // ----------------------------------------------------------------------------------
-// T = 1, kernel 1: row statistics + per-request accept tests
+// T = 1: one cooperative kernel, four phases separated by bounded grid barriers
+//   1  base-2 softmax statistics of every target and draft row, one partial per
+//      (row, chunk, warp): (m2, s) with s = sum 2^(x log2e - m2), m2 = NaN if bad
+//   2  one CTA per request: merge its rows, run the gamma accept tests, record the
+//      row to draw from (residual at the first rejection, or the bonus row)
+//   3  weights of those rows per (request, chunk, warp), in vocabulary order
+//   4  one warp per request: locate the 1024-entry segment holding u * sum, then the
+//      entry inside it
 // ----------------------------------------------------------------------------------
-
-// Softmax statistics of this thread's elements (two passes over registers), then of
-// the CTA (fixed order).  Result valid in thread 0.
-__device__ __forceinline__ Stat block_stat(const float (&x)[kEPT], long base, long V, int& bad, Stat* s_stat) {
-    float m = -INFINITY;
-#pragma unroll
-    for (int e = 0; e < kEPT; ++e) {
-        if (base + e < V) { bad |= bad_logit(x[e]) ? 1 : 0; m = fmaxf(m, x[e]); }
-    }
-    float s = 0.0f;
-    if (m != -INFINITY) {
-#pragma unroll
-        for (int e = 0; e < kEPT; ++e) s += expf(x[e] - m);   // -inf past V gives 0
-    }
-    Stat st = warp_stat(Stat{m, s});
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (lane == 0) s_stat[warp] = st;
-    __syncthreads();
-    Stat r = s_stat[0];
-    if (threadIdx.x == 0) {
-        for (int w = 1; w < kWarps; ++w) r = stat_merge(r, s_stat[w]);
-    }
+struct Item1 { int b, lr, c; };   // local rows 0..G target, G+1..2G draft
+__device__ __forceinline__ Item1 item1(const VerifyParams& p, long it) {
+    const long per_req = (long)(2 * p.gamma + 1) * p.nchunk;
+    Item1 r;
+    r.b = (int)(it / per_req);
+    const long rem = it - (long)r.b * per_req;
+    r.lr = (int)(rem / p.nchunk);
+    r.c = (int)(rem - (long)r.lr * p.nchunk);
     return r;
 }
 
+template <typename TT, typename DT, int NW>
+__device__ __forceinline__ void load_item1(const VerifyParams& p, long it, uint4 (&w)[NW]) {
+    const Item1 q = item1(p, it);
+    const int G = p.gamma;
+    if (q.lr <= G)
+        load_words<TT, NW>(w, static_cast<const TT*>(p.target) + ((size_t)q.b * (G + 1) + q.lr) * p.V, p.V,
+                           thread_base(q.c), p.vec_t != 0);
+    else
+        load_words<DT, NW>(w, static_cast<const DT*>(p.draft) + ((size_t)q.b * G + (q.lr - G - 1)) * p.V, p.V,
+                           thread_base(q.c), p.vec_d != 0);
+}
+
+template <typename T, int NW>
+__device__ __forceinline__ float2 warp_partial(const uint4 (&w)[NW]) {
+    const float m = warp_max_nan(chunk_max_nan<T, NW>(w));
+    if (isnan(m) || m == INFINITY) return make_float2(NAN, 0.0f);
+    if (m == -INFINITY) return make_float2(-INFINITY, 0.0f);
+    const float m2 = m * kLog2e;
+    float x[kEPT];
+    decode_words<T, NW>(w, x);
+    float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+    for (int e = 0; e < kEPT; e += 2) { s0 += wexp(x[e], m2); s1 += wexp(x[e + 1], m2); }
+    return make_float2(m2, warp_sum(s0 + s1));
+}
+
 template <typename TT, typename DT>
-__device__ void accept_phase(const VerifyParams& p, int b) {
+__device__ __forceinline__ void phase_stats(const VerifyParams& p) {
+    const long items = (long)(2 * p.gamma + 1) * p.nchunk * p.B;
+    constexpr int NW = Words<TT>::N > Words<DT>::N ? Words<TT>::N : Words<DT>::N;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint4 cur[NW], nxt[NW];
+    long it = blockIdx.x;
+    if (it < items) load_item1<TT, DT, NW>(p, it, cur);
+    for (; it < items; it += gridDim.x) {
+        const long nx = it + gridDim.x;
+        if (nx < items) load_item1<TT, DT, NW>(p, nx, nxt);
+        const Item1 q = item1(p, it);
+        const float2 st = (q.lr <= p.gamma) ? warp_partial<TT, NW>(cur) : warp_partial<DT, NW>(cur);
+        if (lane == 0) {
+            const size_t rowid = (size_t)q.b * (2 * p.gamma + 1) + q.lr;
+            p.stats[(rowid * p.nchunk + q.c) * kWarps + warp] = st;
+        }
+#pragma unroll
+        for (int i = 0; i < NW; ++i) cur[i] = nxt[i];
+    }
+}
+
+template <typename TT, typename DT>
+__device__ __noinline__ void accept_phase(const VerifyParams& p, int b) {
     const TT* target = static_cast<const TT*>(p.target);
     const DT* draft = static_cast<const DT*>(p.draft);
     const int G = p.gamma;
-    const int nr = 2 * G + 1;                 // local rows: 0..G target, G+1..2G draft
-    __shared__ float s_m[2 * SPEC_MAX_GAMMA + 1], s_Z[2 * SPEC_MAX_GAMMA + 1];
-    __shared__ int s_badrow;
-    __shared__ int s_acc[SPEC_MAX_GAMMA], s_near[SPEC_MAX_GAMMA], s_badtok;
+    const int nr = 2 * G + 1;
+    __shared__ float s_m2[2 * SPEC_MAX_GAMMA + 1], s_s[2 * SPEC_MAX_GAMMA + 1];
+    __shared__ int s_badrow, s_badtok;
+    __shared__ int s_acc[SPEC_MAX_GAMMA], s_near[SPEC_MAX_GAMMA];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) { s_badrow = 0; s_badtok = 0; }
     __syncthreads();
 
-    // merge each row's chunk statistics in chunk order (lane-strided, fixed tree)
+    // merge each row's partials (lane-strided, fixed tree)
+    const int np = p.nchunk * kWarps;
     for (int lr = warp; lr < nr; lr += kWarps) {
         const size_t rowid = (size_t)b * nr + lr;
-        Stat acc = stat_empty();
-        for (int c = lane; c < p.nchunk; c += 32) {
-            const float2 st = __ldcg(&p.stats[rowid * p.nchunk + c]);
-            acc = stat_merge(acc, Stat{st.x, st.y});
+        Stat2 acc = stat2_empty();
+        int bad = 0;
+        for (int i = lane; i < np; i += 32) {
+            const float2 st = __ldcg(&p.stats[rowid * np + i]);
+            if (isnan(st.x)) bad = 1;
+            else acc = stat2_merge(acc, Stat2{st.x, st.y});
         }
-        acc = warp_stat(acc);
+        acc = warp_stat2(acc);
+        bad = warp_or(bad);
         if (lane == 0) {
-            s_m[lr] = acc.m;
-            s_Z[lr] = acc.s;
-            const unsigned rb = __ldcg(&p.rowbad[rowid]);
-            p.rowbad[rowid] = 0u;
-            if (rb || acc.m == -INFINITY) atomicOr(&s_badrow, 1);
+            s_m2[lr] = acc.m2;
+            s_s[lr] = acc.s;
+            if (bad || acc.m2 == -INFINITY) atomicOr(&s_badrow, 1);
         }
     }
     __syncthreads();
 
-    // the gamma accept tests, one thread each
+    // the gamma accept tests, one thread each; p and q of the drafted token with the
+    // accurate exp2 (the decision is compared against exact arithmetic)
     const uint64_t seed = p.seeds[b];
     for (int j = threadIdx.x; j < G; j += blockDim.x) {
         const int t = p.tokens[(size_t)b * G + j];
@@ -200,8 +336,8 @@ __device__ void accept_phase(const VerifyParams& p, int b) {
         } else {
             const float lp = to_float(target[((size_t)b * (G + 1) + j) * p.V + t]);
             const float lq = to_float(draft[((size_t)b * G + j) * p.V + t]);
-            const float pj = expf(lp - s_m[j]) / s_Z[j];
-            const float qj = expf(lq - s_m[G + 1 + j]) / s_Z[G + 1 + j];
+            const float pj = exp2f(fmaf(lp, kLog2e, -s_m2[j])) / s_s[j];
+            const float qj = exp2f(fmaf(lq, kLog2e, -s_m2[G + 1 + j])) / s_s[G + 1 + j];
             const float u = philox_uniform(seed, (uint64_t)b, (uint64_t)(j + 1), 1);
             acc = (u * qj < pj) ? 1 : 0;
             near = (fabsf(u * qj - pj) < kNearTie * qj) ? 1 : 0;
@@ -229,11 +365,11 @@ __device__ void accept_phase(const VerifyParams& p, int b) {
             for (int i = k + 1; i <= G; ++i) com[i] = -1;
             if (k < G) {   // rejected at position k+1: target row k and draft row k
                 st0 = make_int4(MODE_RESID, k, near, 0);
-                st1 = make_int4(__float_as_int(s_m[k]), __float_as_int(s_Z[k]),
-                                __float_as_int(s_m[G + 1 + k]), __float_as_int(s_Z[G + 1 + k]));
+                st1 = make_int4(__float_as_int(s_m2[k]), __float_as_int(s_s[k]),
+                                __float_as_int(s_m2[G + 1 + k]), __float_as_int(s_s[G + 1 + k]));
             } else {       // all accepted: bonus from target row gamma
                 st0 = make_int4(MODE_BONUS, G, near, 0);
-                st1 = make_int4(__float_as_int(s_m[G]), __float_as_int(s_Z[G]), 0, 0);
+                st1 = make_int4(__float_as_int(s_m2[G]), __float_as_int(s_s[G]), 0, 0);
             }
         }
         p.state[2 * b] = st0;
@@ -242,251 +378,225 @@ __device__ void accept_phase(const VerifyParams& p, int b) {
     __syncthreads();
 }
 
-template <typename TT, typename DT>
-__global__ void __launch_bounds__(kThreads) verify_t1_stats_kernel(VerifyParams p) {
-    const TT* target = static_cast<const TT*>(p.target);
-    const DT* draft = static_cast<const DT*>(p.draft);
-    const long V = p.V;
-    const int G = p.gamma;
-    const int nr = 2 * G + 1;
-    const long per_req = (long)nr * p.nchunk;
-    const long items = per_req * p.B;
-    __shared__ Stat s_stat[kWarps];
-    __shared__ int s_badw[kWarps];
-    __shared__ int s_last;
-
-    for (long it = blockIdx.x; it < items; it += gridDim.x) {
-        const int b = (int)(it / per_req);
-        const long rem = it - (long)b * per_req;
-        const int lr = (int)(rem / p.nchunk);
-        const int c = (int)(rem - (long)lr * p.nchunk);
-        float x[kEPT];
-        if (lr <= G) load_chunk<TT>(target + ((size_t)b * (G + 1) + lr) * V, V, c, p.vec_t != 0, x);
-        else load_chunk<DT>(draft + ((size_t)b * G + (lr - G - 1)) * V, V, c, p.vec_d != 0, x);
-        int bad = 0;
-        const Stat st = block_stat(x, thread_base(c), V, bad, s_stat);
-        bad = warp_or(bad);
-        if ((threadIdx.x & 31) == 0) s_badw[threadIdx.x >> 5] = bad;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            const size_t rowid = (size_t)b * nr + lr;
-            p.stats[rowid * p.nchunk + c] = make_float2(st.m, st.s);
-            int bb = 0;
-            for (int w = 0; w < kWarps; ++w) bb |= s_badw[w];
-            if (bb) atomicOr(&p.rowbad[rowid], 1u);
-            __threadfence();
-            const unsigned prev = atomicAdd(&p.done1[b], 1u);
-            s_last = (prev == (unsigned)per_req - 1u) ? 1 : 0;
-            if (s_last) { __threadfence(); p.done1[b] = 0u; }
-        }
-        __syncthreads();
-        if (s_last) accept_phase<TT, DT>(p, b);
-    }
+struct DrawRow {   // what the accept phase recorded for a request
+    int mode, n, near;
+    float m2p, sp, m2q, sq;
+};
+__device__ __forceinline__ DrawRow draw_row(const VerifyParams& p, int b) {
+    const int4 a = __ldcg(&p.state[2 * b]);
+    const int4 c = __ldcg(&p.state[2 * b + 1]);
+    return DrawRow{a.x, a.y, a.z, __int_as_float(c.x), __int_as_float(c.y), __int_as_float(c.z), __int_as_float(c.w)};
 }
 
-// ----------------------------------------------------------------------------------
-// T = 1, kernel 2: residual / bonus draw
-// ----------------------------------------------------------------------------------
-
-// Weights of this thread's 32 elements of chunk c: w = max(0, p - q) (residual) and
-// p, with p = exp(l - mp) / Zp, q = exp(d - mq) / Zq.  Identical arithmetic in the
-// chunk-sum pass and in the final scan, so the per-thread sums agree bit for bit.
-template <typename TT, typename DT>
-__device__ __forceinline__ void chunk_weights(const VerifyParams& p, int b, int mode, int n, int c,
-                                              float mp, float Zp, float mq, float Zq,
-                                              float (&wr)[kEPT], float (&wp)[kEPT]) {
-    const TT* target = static_cast<const TT*>(p.target);
-    const DT* draft = static_cast<const DT*>(p.draft);
-    const long V = p.V;
-    const int G = p.gamma;
+// Weights of 32 entries: wp = p, wr = max(0, p - q) in residual mode, with
+// p = 2^(l log2e - m2p) / sp and q = 2^(d log2e - m2q) / sq.  The streaming pass and
+// the final scan use this same arithmetic in the same order.
+template <typename TT, typename DT, int NW>
+__device__ __forceinline__ void weights(const DrawRow& d, const uint4 (&wt)[NW], const uint4 (&wd)[NW],
+                                        float (&wr)[kEPT], float (&wp)[kEPT]) {
     float lt[kEPT];
-    load_chunk<TT>(target + ((size_t)b * (G + 1) + n) * V, V, c, p.vec_t != 0, lt);
-    if (mode == MODE_RESID) {
+    decode_words<TT, NW>(wt, lt);
+    const float ip = 1.0f / d.sp;
+    if (d.mode == MODE_RESID) {
         float ld[kEPT];
-        load_chunk<DT>(draft + ((size_t)b * G + n) * V, V, c, p.vec_d != 0, ld);
+        decode_words<DT, NW>(wd, ld);
+        const float iq = 1.0f / d.sq;
 #pragma unroll
         for (int e = 0; e < kEPT; ++e) {
-            const float pv = expf(lt[e] - mp) / Zp;
-            const float qv = expf(ld[e] - mq) / Zq;
+            const float pv = wexp(lt[e], d.m2p) * ip;
+            const float qv = wexp(ld[e], d.m2q) * iq;
             wp[e] = pv;
             wr[e] = fmaxf(0.0f, pv - qv);
         }
     } else {
 #pragma unroll
         for (int e = 0; e < kEPT; ++e) {
-            wp[e] = expf(lt[e] - mp) / Zp;
+            wp[e] = wexp(lt[e], d.m2p) * ip;
             wr[e] = 0.0f;
         }
     }
 }
 
-// Block-wide exclusive scan of one float per thread (fixed order).  Returns the
-// exclusive prefix of this thread; *total receives the block total.
-__device__ __forceinline__ float block_exclusive_scan(float x, float* s_warp, float* total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const float incl = warp_inclusive_scan(x);
-    if (lane == 31) s_warp[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        const float w = lane < kWarps ? s_warp[lane] : 0.0f;
-        const float wi = warp_inclusive_scan(w);
-        if (lane < kWarps) s_warp[kWarps + lane] = wi - w;    // exclusive warp offsets
-        if (lane == kWarps - 1) s_warp[2 * kWarps] = wi;
+// weights() summed in the same order, without keeping the entries.
+template <typename TT, typename DT, int NW>
+__device__ __forceinline__ void weight_sums(const DrawRow& d, const uint4 (&wt)[NW], const uint4 (&wd)[NW],
+                                            float& sr, float& sp) {
+    float lt[kEPT];
+    decode_words<TT, NW>(wt, lt);
+    const float ip = 1.0f / d.sp;
+    sr = 0.0f;
+    sp = 0.0f;
+    if (d.mode == MODE_RESID) {
+        float ld[kEPT];
+        decode_words<DT, NW>(wd, ld);
+        const float iq = 1.0f / d.sq;
+#pragma unroll
+        for (int e = 0; e < kEPT; ++e) {
+            const float pv = wexp(lt[e], d.m2p) * ip;
+            const float qv = wexp(ld[e], d.m2q) * iq;
+            sp += pv;
+            sr += fmaxf(0.0f, pv - qv);
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < kEPT; ++e) sp += wexp(lt[e], d.m2p) * ip;
     }
-    __syncthreads();
-    const float ex = s_warp[kWarps + warp] + (incl - x);
-    *total = s_warp[2 * kWarps];
-    __syncthreads();
-    return ex;
+}
+
+template <typename TT, typename DT, int NW>
+__device__ __forceinline__ void load_draw(const VerifyParams& p, int b, long base, const DrawRow& d,
+                                          uint4 (&wt)[NW], uint4 (&wd)[NW]) {
+    const int G = p.gamma;
+    load_words<TT, NW>(wt, static_cast<const TT*>(p.target) + ((size_t)b * (G + 1) + d.n) * p.V, p.V, base,
+                       p.vec_t != 0);
+    if (d.mode == MODE_RESID)
+        load_words<DT, NW>(wd, static_cast<const DT*>(p.draft) + ((size_t)b * G + d.n) * p.V, p.V, base,
+                           p.vec_d != 0);
 }
 
 template <typename TT, typename DT>
-__device__ void sample_phase(const VerifyParams& p, int b, int4 st0, int4 st1) {
-    const int G = p.gamma;
-    const int mode = st0.x, n = st0.y;
-    const float mp = __int_as_float(st1.x), Zp = __int_as_float(st1.y);
-    const float mq = __int_as_float(st1.z), Zq = __int_as_float(st1.w);
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    __shared__ float s_scan[2 * kWarps + 1];
-    __shared__ int s_chunk, s_use_resid, s_tok, s_near;
-    __shared__ float s_tloc, s_W;
-
-    // totals and the chunk that holds the threshold (warp 0, contiguous segments)
-    if (warp == 0) {
-        const int K = (p.nchunk + 31) / 32;
-        const int c0 = lane * K, c1 = min(p.nchunk, c0 + K);
-        float sr = 0.0f, sp = 0.0f;
-        for (int c = c0; c < c1; ++c) {
-            const float2 ks = __ldcg(&p.ksums[(size_t)b * p.nchunk + c]);
-            sr += ks.x;
-            sp += ks.y;
-        }
-        const float ir = warp_inclusive_scan(sr), ip = warp_inclusive_scan(sp);
-        const float Wr = __shfl_sync(0xffffffffu, ir, 31), Wp = __shfl_sync(0xffffffffu, ip, 31);
-        const int use_resid = (mode == MODE_RESID) && (Wr > 0.0f);
-        const float W = use_resid ? Wr : Wp;
-        const float incl = use_resid ? ir : ip;
-        const float mine = use_resid ? sr : sp;
-        const float u = (mode == MODE_RESID) ? philox_uniform(p.seeds[b], (uint64_t)b, (uint64_t)(n + 1), 2)
-                                             : philox_uniform(p.seeds[b], (uint64_t)b, (uint64_t)(G + 1), 3);
-        const float t = u * W;
-        const unsigned cross = __ballot_sync(0xffffffffu, incl > t);
-        int chunk = -1;
-        float tloc = 0.0f;
-        if (cross) {
-            const int L = __ffs(cross) - 1;
-            if (lane == L) {
-                float run = incl - mine;
-                for (int c = c0; c < c1; ++c) {
-                    const float2 ks = __ldcg(&p.ksums[(size_t)b * p.nchunk + c]);
-                    const float w = use_resid ? ks.x : ks.y;
-                    if (run + w > t) { chunk = c; tloc = t - run; break; }
-                    run += w;
-                }
-                if (chunk < 0) {   // rounding: the segment's walk fell short
-                    chunk = c1 - 1;
-                    tloc = INFINITY;
-                }
-            }
-            chunk = __shfl_sync(0xffffffffu, chunk, L);
-            tloc = __shfl_sync(0xffffffffu, tloc, L);
-        } else {
-            // u * W rounded up to W: take the last chunk with positive weight
-            int last = -1;
-            for (int c = c0; c < c1; ++c) {
-                const float2 ks = __ldcg(&p.ksums[(size_t)b * p.nchunk + c]);
-                if ((use_resid ? ks.x : ks.y) > 0.0f) last = c;
-            }
-            const unsigned has = __ballot_sync(0xffffffffu, last >= 0);
-            chunk = has ? __shfl_sync(0xffffffffu, last, 31 - __clz(has)) : 0;
-            tloc = INFINITY;
-        }
-        chunk = max(0, min(chunk, p.nchunk - 1));
-        if (lane == 0) { s_chunk = chunk; s_tloc = tloc; s_use_resid = use_resid; s_W = W; }
+__device__ __forceinline__ void phase_weights(const VerifyParams& p) {
+    const long items = (long)p.B * p.nchunk;
+    constexpr int NW = Words<TT>::N > Words<DT>::N ? Words<TT>::N : Words<DT>::N;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint4 ct[NW], cd[NW], nt[NW], nd[NW];
+    DrawRow dc{MODE_DONE, 0, 0, 0.f, 0.f, 0.f, 0.f}, dn = dc;
+    long it = blockIdx.x;
+    if (it < items) {
+        const int b = (int)(it / p.nchunk);
+        dc = draw_row(p, b);
+        if (dc.mode != MODE_DONE) load_draw<TT, DT, NW>(p, b, thread_base((int)(it - (long)b * p.nchunk)), dc, ct, cd);
     }
-    __syncthreads();
+    for (; it < items; it += gridDim.x) {
+        const long nx = it + gridDim.x;
+        if (nx < items) {
+            const int bn = (int)(nx / p.nchunk);
+            dn = draw_row(p, bn);
+            if (dn.mode != MODE_DONE)
+                load_draw<TT, DT, NW>(p, bn, thread_base((int)(nx - (long)bn * p.nchunk)), dn, nt, nd);
+        }
+        if (dc.mode != MODE_DONE) {
+            const int b = (int)(it / p.nchunk);
+            const int c = (int)(it - (long)b * p.nchunk);
+            float sr, sp;
+            weight_sums<TT, DT, NW>(dc, ct, cd, sr, sp);
+            const float ir = warp_inclusive_scan(sr), ip = warp_inclusive_scan(sp);
+            if (lane == 31) p.ksums[((size_t)b * p.nchunk + c) * kWarps + warp] = make_float2(ir, ip);
+        }
+        dc = dn;
+#pragma unroll
+        for (int i = 0; i < NW; ++i) { ct[i] = nt[i]; cd[i] = nd[i]; }
+    }
+}
 
-    // scan inside the chunk
-    const int c = s_chunk;
+// One warp draws the token of request b (segments are 1024 entries: chunk c, warp w).
+template <typename TT, typename DT>
+__device__ __noinline__ void draw_token(const VerifyParams& p, int b) {
+    constexpr int NW = Words<TT>::N > Words<DT>::N ? Words<TT>::N : Words<DT>::N;
+    const int lane = threadIdx.x & 31;
+    const DrawRow d = draw_row(p, b);
+    if (d.mode == MODE_DONE) return;
+    const int G = p.gamma;
+    const int nseg = p.nchunk * kWarps;
+    const float2* ks = p.ksums + (size_t)b * nseg;
+    // totals and the segment holding the threshold (contiguous lane ranges)
+    const int K = (nseg + 31) / 32;
+    const int s0 = lane * K, s1 = min(nseg, s0 + K);
+    float sr = 0.0f, sp = 0.0f;
+    for (int i = s0; i < s1; ++i) { const float2 v = __ldcg(&ks[i]); sr += v.x; sp += v.y; }
+    const float ir = warp_inclusive_scan(sr), ip = warp_inclusive_scan(sp);
+    const float Wr = __shfl_sync(0xffffffffu, ir, 31), Wp = __shfl_sync(0xffffffffu, ip, 31);
+    const bool ur = (d.mode == MODE_RESID) && (Wr > 0.0f);
+    const float W = ur ? Wr : Wp;
+    const float incl = ur ? ir : ip, mine = ur ? sr : sp;
+    const float u = (d.mode == MODE_RESID) ? philox_uniform(p.seeds[b], (uint64_t)b, (uint64_t)(d.n + 1), 2)
+                                           : philox_uniform(p.seeds[b], (uint64_t)b, (uint64_t)(G + 1), 3);
+    const float t = u * W;
+    const unsigned cross = __ballot_sync(0xffffffffu, incl > t);
+    int seg = -1;
+    float tl = INFINITY;
+    if (cross) {
+        const int L = __ffs(cross) - 1;
+        if (lane == L) {
+            float run = incl - mine;
+            for (int i = s0; i < s1; ++i) {
+                const float2 v = __ldcg(&ks[i]);
+                const float w = ur ? v.x : v.y;
+                if (run + w > t) { seg = i; tl = t - run; break; }
+                run += w;
+            }
+            if (seg < 0) seg = s1 - 1;
+        }
+        seg = __shfl_sync(0xffffffffu, seg, L);
+        tl = __shfl_sync(0xffffffffu, tl, L);
+    } else {   // u * W rounded up to W: the last segment with positive weight
+        int last = -1;
+        for (int i = s0; i < s1; ++i) {
+            const float2 v = __ldcg(&ks[i]);
+            if ((ur ? v.x : v.y) > 0.0f) last = i;
+        }
+        const unsigned has = __ballot_sync(0xffffffffu, last >= 0);
+        seg = has ? __shfl_sync(0xffffffffu, last, 31 - __clz(has)) : 0;
+    }
+    seg = max(0, min(seg, nseg - 1));
+    // recompute the segment's weights (same lanes, same arithmetic) and scan them
+    const long base = (long)(seg / kWarps) * kVerifyChunk + (long)(seg % kWarps) * 1024 + (long)lane * kEPT;
+    uint4 wt[NW], wd[NW];
+    load_draw<TT, DT, NW>(p, b, base, d, wt, wd);
     float wr[kEPT], wp[kEPT];
-    chunk_weights<TT, DT>(p, b, mode, n, c, mp, Zp, mq, Zq, wr, wp);
-    const bool ur = s_use_resid != 0;
+    weights<TT, DT, NW>(d, wt, wd, wr, wp);
     float mysum = 0.0f;
 #pragma unroll
     for (int e = 0; e < kEPT; ++e) mysum += ur ? wr[e] : wp[e];
-    float total;
-    const float ex = block_exclusive_scan(mysum, s_scan, &total);
-    const float tl = s_tloc;
-    const long base = thread_base(c);
-    // the thread whose range crosses tl scans its elements
-    int tok = -1;
-    float near_lo = 0.0f, near_hi = 0.0f;
-    if (ex <= tl && ex + mysum > tl) {
-        float run = ex;
-        for (int e = 0; e < kEPT; ++e) {
-            const float w = ur ? wr[e] : wp[e];
-            if (run + w > tl && w > 0.0f) { tok = (int)(base + e); near_lo = run; near_hi = run + w; break; }
-            run += w;
+    const float inc = warp_inclusive_scan(mysum);
+    const float ex = inc - mysum;
+    const unsigned hit = __ballot_sync(0xffffffffu, ex <= tl && inc > tl);
+    int tok = -1, near = 0;
+    if (hit) {
+        const int L = __ffs(hit) - 1;
+        if (lane == L) {
+            float run = ex;
+            for (int e = 0; e < kEPT; ++e) {
+                const float w = ur ? wr[e] : wp[e];
+                if (run + w > tl && w > 0.0f) {
+                    tok = (int)(base + e);
+                    const float tol = kNearTie * W;
+                    near = ((run > 0.0f && fabsf(tl - run) < tol) || fabsf(run + w - tl) < tol) ? 1 : 0;
+                    break;
+                }
+                run += w;
+            }
         }
+        tok = __shfl_sync(0xffffffffu, tok, L);
+        near = __shfl_sync(0xffffffffu, near, L);
     }
-    if (threadIdx.x == 0) { s_tok = -1; s_near = 0; }
-    __syncthreads();
-    if (tok >= 0) atomicMax(&s_tok, tok);   // at most one thread crosses; max is safe
-    __syncthreads();
-    if (s_tok < 0) {
-        // rounding left no crossing: the last element of positive weight in the chunk
+    if (tok < 0) {   // rounding left no crossing: last entry of positive weight in the segment
         int last = -1;
         for (int e = 0; e < kEPT; ++e)
             if ((ur ? wr[e] : wp[e]) > 0.0f && base + e < p.V) last = (int)(base + e);
-        if (last >= 0) atomicMax(&s_tok, last);
-        __syncthreads();
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+        tok = last;
     }
-    if (tok >= 0) {
-        const float tol = kNearTie * s_W;
-        if ((near_lo > 0.0f && fabsf(tl - near_lo) < tol) || fabsf(near_hi - tl) < tol) s_near = 1;
+    if (lane == 0) {
+        p.committed_out[(size_t)b * (G + 1) + d.n] = tok;
+        p.bonus_out[b] = tok;
+        p.n_out[b] = d.n;
+        if (p.near_out) p.near_out[b] = d.near | near;
     }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const int y = s_tok;
-        p.committed_out[(size_t)b * (G + 1) + n] = y;
-        p.bonus_out[b] = y;
-        p.n_out[b] = n;
-        if (p.near_out) p.near_out[b] = st0.z | s_near;
-    }
-    __syncthreads();
 }
 
 template <typename TT, typename DT>
-__global__ void __launch_bounds__(kThreads) verify_t1_sample_kernel(VerifyParams p) {
-    const long items = (long)p.B * p.nchunk;
-    __shared__ float s_red[2][2 * kWarps + 1];
-    __shared__ int s_last;
-    for (long it = blockIdx.x; it < items; it += gridDim.x) {
-        const int b = (int)(it / p.nchunk);
-        const int c = (int)(it - (long)b * p.nchunk);
-        const int4 st0 = __ldcg(&p.state[2 * b]);
-        if (st0.x == MODE_DONE) continue;
-        const int4 st1 = __ldcg(&p.state[2 * b + 1]);
-        float wr[kEPT], wp[kEPT];
-        chunk_weights<TT, DT>(p, b, st0.x, st0.y, c, __int_as_float(st1.x), __int_as_float(st1.y),
-                              __int_as_float(st1.z), __int_as_float(st1.w), wr, wp);
-        float sr = 0.0f, sp = 0.0f;
-#pragma unroll
-        for (int e = 0; e < kEPT; ++e) { sr += wr[e]; sp += wp[e]; }
-        // chunk totals with exactly the association of the final in-chunk scan
-        float tr, tp;
-        block_exclusive_scan(sr, s_red[0], &tr);
-        block_exclusive_scan(sp, s_red[1], &tp);
-        if (threadIdx.x == 0) {
-            p.ksums[(size_t)b * p.nchunk + c] = make_float2(tr, tp);
-            __threadfence();
-            const unsigned prev = atomicAdd(&p.done2[b], 1u);
-            s_last = (prev == (unsigned)p.nchunk - 1u) ? 1 : 0;
-            if (s_last) { __threadfence(); p.done2[b] = 0u; }
-        }
-        __syncthreads();
-        if (s_last) sample_phase<TT, DT>(p, b, st0, st1);
-    }
+__global__ void __launch_bounds__(kThreads, 2) verify_t1_kernel(VerifyParams p) {
+    const unsigned nb = gridDim.x;
+    phase_stats<TT, DT>(p);
+    if (!block_barrier(p.barrier, nb, p.status)) return;
+    for (int b = blockIdx.x; b < p.B; b += gridDim.x) accept_phase<TT, DT>(p, b);
+    if (!block_barrier(p.barrier, nb, p.status)) return;
+    phase_weights<TT, DT>(p);
+    if (!block_barrier(p.barrier, nb, p.status)) return;
+    const int gw = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    for (int b = gw; b < p.B; b += gridDim.x * kWarps) draw_token<TT, DT>(p, b);
 }
 
 // ----------------------------------------------------------------------------------
@@ -499,12 +609,10 @@ size_t verify_workspace_bytes(int B, int gamma, int V) {
     const size_t nr = 2 * (size_t)gamma + 1;
     size_t off = kWsHeaderBytes;
     off = align_up(off + sizeof(unsigned long long) * (size_t)B * (gamma + 1), 256);
-    off = align_up(off + sizeof(unsigned) * (size_t)B * nr, 256);
-    off = align_up(off + sizeof(float2) * (size_t)B * nr * nchunk, 256);
-    off = align_up(off + sizeof(unsigned) * (size_t)B, 256);
-    off = align_up(off + sizeof(unsigned) * (size_t)B, 256);
+    off = align_up(off + sizeof(unsigned) * (size_t)B * (gamma + 1), 256);
+    off = align_up(off + sizeof(float2) * (size_t)B * nr * nchunk * kWarps, 256);
     off = align_up(off + sizeof(int4) * 2 * (size_t)B, 256);
-    off = align_up(off + sizeof(float2) * (size_t)B * nchunk, 256);
+    off = align_up(off + sizeof(float2) * (size_t)B * nchunk * kWarps, 256);
     return off;
 }
 
@@ -513,45 +621,55 @@ void verify_bind_workspace(VerifyParams& p, void* ws) {
     WsHeader* h = reinterpret_cast<WsHeader*>(w);
     p.status = &h->status;
     p.done = h->done;
+    p.barrier = &h->barrier[0][0];
     const size_t nchunk = ((size_t)p.V + kVerifyChunk - 1) / kVerifyChunk;
     const size_t nr = 2 * (size_t)p.gamma + 1;
     size_t off = kWsHeaderBytes;
     p.keys = reinterpret_cast<unsigned long long*>(w + off);
     off = align_up(off + sizeof(unsigned long long) * (size_t)p.B * (p.gamma + 1), 256);
     p.rowbad = reinterpret_cast<unsigned*>(w + off);
-    off = align_up(off + sizeof(unsigned) * (size_t)p.B * nr, 256);
+    off = align_up(off + sizeof(unsigned) * (size_t)p.B * (p.gamma + 1), 256);
     p.stats = reinterpret_cast<float2*>(w + off);
-    off = align_up(off + sizeof(float2) * (size_t)p.B * nr * nchunk, 256);
-    p.done1 = reinterpret_cast<unsigned*>(w + off);
-    off = align_up(off + sizeof(unsigned) * (size_t)p.B, 256);
-    p.done2 = reinterpret_cast<unsigned*>(w + off);
-    off = align_up(off + sizeof(unsigned) * (size_t)p.B, 256);
+    off = align_up(off + sizeof(float2) * (size_t)p.B * nr * nchunk * kWarps, 256);
     p.state = reinterpret_cast<int4*>(w + off);
     off = align_up(off + sizeof(int4) * 2 * (size_t)p.B, 256);
     p.ksums = reinterpret_cast<float2*>(w + off);
 }
 
+// Persistent grid: enough CTAs to keep every SM streaming, never more than the items.
+template <typename K>
+static int grid_for(K kern, long items) {
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, 0) != cudaSuccess || occ < 1) occ = 1;
+    const long cap = (long)device_sm_count() * occ;
+    return (int)(items < cap ? (items > 0 ? items : 1) : cap);
+}
+
 template <typename TT, typename DT>
 static cudaError_t launch_t1(const VerifyParams& p, cudaStream_t stream) {
-    const int sms = device_sm_count();
-    const long items1 = (long)p.B * (2 * p.gamma + 1) * p.nchunk;
-    const int grid1 = (int)(items1 < (long)sms * 8 ? items1 : (long)sms * 8);
-    verify_t1_stats_kernel<TT, DT><<<grid1, kThreads, 0, stream>>>(p);
-    cudaError_t e = cudaGetLastError();
+    auto kern = verify_t1_kernel<TT, DT>;
+    int occ = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, 0);
     if (e != cudaSuccess) return e;
-    const long items2 = (long)p.B * p.nchunk;
-    const int grid2 = (int)(items2 < (long)sms * 8 ? items2 : (long)sms * 8);
-    verify_t1_sample_kernel<TT, DT><<<grid2, kThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    if (occ < 1) return cudaErrorInvalidConfiguration;
+    const long items = (long)p.B * (2 * p.gamma + 1) * p.nchunk;
+    long grid = (long)device_sm_count() * occ;
+    if (grid > items) grid = items;
+    VerifyParams args = p;
+    void* kargs[] = {&args};
+    return cudaLaunchCooperativeKernel((const void*)kern, dim3((unsigned)grid), dim3(kThreads), kargs, 0, stream);
 }
 
 cudaError_t verify_launch(const VerifyParams& p, cudaStream_t stream) {
-    const int sms = device_sm_count();
     if (p.temperature == 0) {
         const long items = (long)p.B * (p.gamma + 1) * p.nchunk;
-        const int grid = (int)(items < (long)sms * 8 ? items : (long)sms * 8);
-        if (p.tdt == SPEC_BF16) verify_t0_kernel<bf16_t><<<grid, kThreads, 0, stream>>>(p);
-        else verify_t0_kernel<float><<<grid, kThreads, 0, stream>>>(p);
+        if (p.tdt == SPEC_BF16) {
+            auto k = verify_t0_kernel<bf16_t>;
+            k<<<grid_for(k, items), kThreads, 0, stream>>>(p);
+        } else {
+            auto k = verify_t0_kernel<float>;
+            k<<<grid_for(k, items), kThreads, 0, stream>>>(p);
+        }
         return cudaGetLastError();
     }
     if (p.tdt == SPEC_BF16 && p.ddt == SPEC_BF16) return launch_t1<bf16_t, bf16_t>(p, stream);
