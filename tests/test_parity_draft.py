@@ -61,13 +61,18 @@ def check_draft(out, L, anchor, U, Wt, T, seeds, tol=1e-5):
     return tok.size - near, near
 
 
-SMALL = [  # (B, gamma, V, r, dtype)
-    (3, 5, 1000, 8, torch.float32),      # 8 tiles, ragged tail
-    (2, 4, 1000, 16, torch.bfloat16),
+SMALL = [  # (B, gamma, V, r, dtype); bf16 with r % 64 == 0 and B*gamma <= 256 takes tcgen05
+    (3, 5, 1000, 8, torch.float32),      # 8 tiles, ragged tail (CUDA cores)
+    (2, 4, 1000, 16, torch.bfloat16),    # CUDA cores
     (1, 7, 4099, 32, torch.float32),     # V odd
     (4, 3, 777, 0, torch.bfloat16),      # no bias
     (2, 6, 300, 12, torch.bfloat16),     # r*2 bytes not a multiple of 16: scalar weight path
     (1, 64, 200, 8, torch.float32),      # maximum gamma
+    (3, 5, 1000, 64, torch.bfloat16),    # tensor cores, one M tile, ragged last tile
+    (2, 7, 4104, 128, torch.bfloat16),   # tensor cores, r = 128
+    (1, 15, 2048, 256, torch.bfloat16),  # tensor cores, r = 256, gamma = 15
+    (20, 7, 2000, 64, torch.bfloat16),   # tensor cores, 140 rows: two M tiles
+    (32, 8, 3000, 192, torch.bfloat16),  # tensor cores, 256 rows: two full M tiles
 ]
 
 
@@ -86,13 +91,14 @@ def test_small(spec, B, gamma, V, r, dtype, T):
 
 
 @pytest.mark.parametrize("T", [0, 1])
-def test_strong_bias_needs_many_passes(spec, T):
+@pytest.mark.parametrize("wdtype,r", [(torch.float32, 4), (torch.bfloat16, 64)])
+def test_strong_bias_needs_many_passes(spec, T, wdtype, r):
     """A bias far larger than the logit gaps: the unbiased guess is wrong everywhere
     and the fixed point takes several passes, yet equals the sequential chain."""
-    B, gamma, V, r = 4, 12, 600, 4
-    L, _ = synth.target_and_draft(B, gamma - 1, V, "gaussian", 0.0, torch.float32, seed=1)
-    L = (L[:, :gamma] * 0.1).contiguous()
-    U, Wt = synth.markov_weights(V, r, torch.float32, seed=2, scale=3.0)
+    B, gamma, V = 4, 12, 600
+    L, _ = synth.target_and_draft(B, gamma - 1, V, "gaussian", 0.0, wdtype, seed=1)
+    L = (L[:, :gamma].float() * 0.1).to(wdtype).contiguous()
+    U, Wt = synth.markov_weights(V, r, wdtype, seed=2, scale=3.0 / (r / 4) ** 0.25)
     anchor = synth.anchors(B, V, seed=5)
     seeds = synth.seeds_for(B, 9)
     out = _gpu(L, anchor, U, Wt, T, seeds)

@@ -25,42 +25,6 @@
 namespace spec {
 
 template <typename LT, typename WT>
-__device__ void tile_phase_cc(const DraftParams& p, bool use_bias, const int32_t* prev, float* s_uw) {
-    const int R = p.B * p.gamma;
-    const int lane = threadIdx.x & 31;
-    const WT* U = static_cast<const WT*>(p.U);
-    const bool write_z = p.qlogits_out != nullptr && (use_bias || p.r == 0);
-    const bool keep_tiles = p.temperature == 1;
-    const int tb = tile_begin(blockIdx.x, gridDim.x, p.n_tiles), te = tile_begin(blockIdx.x + 1, gridDim.x, p.n_tiles);
-    for (int row = threadIdx.x >> 5; row < R; row += kWarps) {
-        int prev_ok = 1;
-        if (use_bias) {
-            const int xp = prev_token(p, prev, row);
-            prev_ok = (xp >= 0 && xp < p.V) ? 1 : 0;
-            for (int k = lane; k < p.r; k += 32) s_uw[k] = prev_ok ? load_one(U + (size_t)xp * p.r + k) : 0.0f;
-            __syncwarp();
-        }
-        RowAcc acc = rowacc_empty();
-        for (int t = tb; t < te; ++t) {
-            float z[4];
-            long v[4];
-            row_tile_z<LT, WT>(p, row, t, use_bias, s_uw, z, v);
-            RowAcc tr = warp_rowacc_of(z, v, p.V);
-            if (!prev_ok) tr.bad = 2;
-            if (keep_tiles && lane == 0) p.tile_rec[(size_t)row * p.n_tiles + t] = rowacc_pack(tr);
-            acc = rowacc_merge(acc, tr);
-            if (write_z) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    if (v[i] < p.V) p.qlogits_out[(size_t)row * p.V + v[i]] = z[i];
-            }
-        }
-        if (lane == 0) p.cta_rec[(size_t)row * gridDim.x + blockIdx.x] = rowacc_pack(acc);
-        __syncwarp();
-    }
-}
-
-template <typename LT, typename WT>
 __global__ void __launch_bounds__(kThreads) draft_kernel(DraftParams p) {
     extern __shared__ float s_dyn[];
     float* s_uw = s_dyn + (size_t)(threadIdx.x >> 5) * (p.r > 0 ? p.r : 1);   // [kWarps][r]
@@ -150,7 +114,13 @@ cudaError_t draft_launch_cc(const DraftParams& p, cudaStream_t stream) {
     return launch_typed<float, float>(p, stream);
 }
 
+bool draft_tc_supported(const DraftParams& p);
+cudaError_t draft_launch_tc(const DraftParams& p, cudaStream_t stream);
+
+// bf16 weights with r a multiple of 64 (<= 256) and at most 256 rows take the tcgen05
+// kernel; everything else the CUDA-core kernel.
 cudaError_t draft_launch(const DraftParams& p, cudaStream_t stream) {
+    if (draft_tc_supported(p)) return draft_launch_tc(p, stream);
     return draft_launch_cc(p, stream);
 }
 

@@ -142,8 +142,9 @@ __device__ void finalize_rows(const DraftParams& p, int pass, bool use_bias, con
                               int nblk_tile, float* s_uw) {
     const int R = p.B * p.gamma;
     const int lane = threadIdx.x & 31;
-    const int gw = blockIdx.x * kWarps + (threadIdx.x >> 5);
-    const int TW = gridDim.x * kWarps;
+    const int nw = blockDim.x >> 5;
+    const int gw = blockIdx.x * nw + (threadIdx.x >> 5);
+    const int TW = gridDim.x * nw;
     const WT* U = static_cast<const WT*>(p.U);
     for (int row = gw; row < R; row += TW) {
         const int b = row / p.gamma, j = row % p.gamma;
@@ -269,6 +270,45 @@ __device__ void finalize_rows(const DraftParams& p, int pass, bool use_bias, con
             cur[row] = x;
             if (pass > 0 && __ldcg(&prev[row]) != x) atomicOr(&p.changed[pass], 1u);
         }
+    }
+}
+
+// CUDA-core tile phase: z = l + U[x_prev] . Wt[v] in float32, one warp per row, four
+// entries per lane per tile; the CTA's contiguous tile range folded into one record
+// per row (and one per tile at T=1).
+template <typename LT, typename WT>
+__device__ void tile_phase_cc(const DraftParams& p, bool use_bias, const int32_t* prev, float* s_uw) {
+    const int R = p.B * p.gamma;
+    const int lane = threadIdx.x & 31;
+    const WT* U = static_cast<const WT*>(p.U);
+    const bool write_z = p.qlogits_out != nullptr && (use_bias || p.r == 0);
+    const bool keep_tiles = p.temperature == 1;
+    const int tb = tile_begin(blockIdx.x, gridDim.x, p.n_tiles), te = tile_begin(blockIdx.x + 1, gridDim.x, p.n_tiles);
+    for (int row = threadIdx.x >> 5; row < R; row += (int)(blockDim.x >> 5)) {
+        int prev_ok = 1;
+        if (use_bias) {
+            const int xp = prev_token(p, prev, row);
+            prev_ok = (xp >= 0 && xp < p.V) ? 1 : 0;
+            for (int k = lane; k < p.r; k += 32) s_uw[k] = prev_ok ? load_one(U + (size_t)xp * p.r + k) : 0.0f;
+            __syncwarp();
+        }
+        RowAcc acc = rowacc_empty();
+        for (int t = tb; t < te; ++t) {
+            float z[4];
+            long v[4];
+            row_tile_z<LT, WT>(p, row, t, use_bias, s_uw, z, v);
+            RowAcc tr = warp_rowacc_of(z, v, p.V);
+            if (!prev_ok) tr.bad = 2;
+            if (keep_tiles && lane == 0) p.tile_rec[(size_t)row * p.n_tiles + t] = rowacc_pack(tr);
+            acc = rowacc_merge(acc, tr);
+            if (write_z) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (v[i] < p.V) p.qlogits_out[(size_t)row * p.V + v[i]] = z[i];
+            }
+        }
+        if (lane == 0) p.cta_rec[(size_t)row * gridDim.x + blockIdx.x] = rowacc_pack(acc);
+        __syncwarp();
     }
 }
 

@@ -1,0 +1,451 @@
+// draft_tc.cu - DSpark block draft, Markov bias on the tcgen05 tensor cores.
+//
+// Defines: "Speculative Decoding Part 2" (VESSL AI), DSpark section, bias equation
+// B(x_{k-1}, .) = W_1[x_{k-1}] W_2; the fixed-point pass loop, finalize and chain
+// semantics are those of draft_common.cuh (shared with the CUDA-core kernel).
+//
+// One biased pass computes, for every row n = (request, position) and every vocabulary
+// entry v, z[n, v] = l[n, v] + sum_k U[x_prev(n), k] Wt[v, k]: a GEMM with M = rows
+// (B*gamma <= 256, padded to 128 or 256), N = V, K = r.  W is the big operand (r*V
+// bf16, 127 MB at r = 256, V = 248,320) and is read once per pass; the rows are few,
+// so the tensor cores only keep the contraction off the critical path of the stream.
+//
+// Per CTA (one per SM, persistent, contiguous tile range):
+//   warp 0      TMA producer: Wt tiles [128 entries x 64 k] (128-byte swizzle) into a
+//               ring of 16 KB stages, completion counted on mbarriers;
+//   warp 1      allocates TMEM and issues tcgen05.mma (M=128, N=128, K=16, bf16 in,
+//               f32 accumulate) from one thread, committing to the ring's "empty"
+//               barriers and, per tile, to a "TMEM full" barrier; two TMEM buffers;
+//   warps 2..   epilogue, four warps per 128-row M tile (warp w reads TMEM lanes
+//               32*(w%4)..+31): each thread owns one row, pulls its 128 accumulators
+//               with tcgen05.ld, adds the drafter logits and folds max / sum-exp /
+//               argmax of the tile into its row's running record.
+// The A operand (the gathered rows U[x_prev(n)]) is written to shared memory in the
+// same K-major 128-byte-swizzled layout once per pass.  Pass 0 (no bias yet) and the
+// finalize run on CUDA cores with every warp.
+#include <cuda.h>
+
+#include "draft_common.cuh"
+
+namespace spec {
+
+constexpr int kTcN = 128;                    // vocabulary entries per tile (MMA N)
+constexpr int kTcK = 64;                     // k per 128-byte swizzle block
+constexpr int kTcBlock = 128 * kTcK * 2;     // 16 KB: 128 rows x 64 k of bf16
+static_assert(kTcN == kDraftTile, "tile width shared with the CUDA-core phases");
+
+// Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A and B bf16 (bits 7-9,
+// 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at 24-28.
+constexpr uint32_t kTcIdesc =
+    (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kTcN >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+
+// Shared-memory matrix descriptor for a K-major operand in the 128-byte swizzle
+// layout: rows of 128 bytes, 8-row groups 1024 bytes apart (stride byte offset),
+// leading byte offset unused, descriptor version 1, layout code 2 (128B swizzle).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+__device__ __forceinline__ void mbar_arrive1(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        :: "r"(smem_u32(dst)), "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 :: "r"(smem_u32(dst)), "r"(ncols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+        :: "r"(d), "l"(a), "l"(b), "r"(kTcIdesc), "r"(accumulate) : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 :: "r"(smem_u32(bar)) : "memory");
+}
+
+// 32 consecutive accumulator columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ float fmax_nan_f(float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+// Drafter logits of 32 consecutive entries (v0 multiple of 32, rows 16-byte aligned,
+// V a multiple of the vector width), -inf past V.
+__device__ __forceinline__ void load_l32(const bf16_t* row, long v0, long V, uint4 (&w)[8]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const long v = v0 + 8 * i;
+        w[i] = (v + 8 <= V) ? __ldg(reinterpret_cast<const uint4*>(row + v)) : make_uint4(0xff80ff80u, 0xff80ff80u,
+                                                                                          0xff80ff80u, 0xff80ff80u);
+    }
+}
+__device__ __forceinline__ void load_l32(const float* row, long v0, long V, uint4 (&w)[8]) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const long v = v0 + 4 * i;
+        w[i] = (v + 4 <= V) ? __ldg(reinterpret_cast<const uint4*>(row + v))
+                            : make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
+    }
+}
+__device__ __forceinline__ void decode_l32(const uint4 (&w)[8], float (&x)[32], bf16_t) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t a[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            x[8 * i + 2 * k] = __uint_as_float(a[k] << 16);
+            x[8 * i + 2 * k + 1] = __uint_as_float(a[k] & 0xffff0000u);
+        }
+    }
+}
+__device__ __forceinline__ void decode_l32(const uint4 (&w)[8], float (&x)[32], float) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        x[4 * i] = __uint_as_float(w[i].x);
+        x[4 * i + 1] = __uint_as_float(w[i].y);
+        x[4 * i + 2] = __uint_as_float(w[i].z);
+        x[4 * i + 3] = __uint_as_float(w[i].w);
+    }
+}
+
+// Record of 32 consecutive entries of one row held by one thread.
+__device__ __forceinline__ RowAcc record32(const float (&z)[32], int v0) {
+    float m = z[0];
+#pragma unroll
+    for (int e = 1; e < 32; ++e) m = fmax_nan_f(m, z[e]);
+    RowAcc r;
+    r.bad = (isnan(m) || m == INFINITY) ? 1 : 0;
+    r.mx = r.bad ? -INFINITY : m;
+    r.s = 0.0f;
+    r.idx = 0x7fffffff;
+    if (!r.bad && m != -INFINITY) {
+        const float m2 = m * kLog2e;
+        float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) { s0 += wexp(z[e], m2); s1 += wexp(z[e + 1], m2); }
+        r.s = s0 + s1;
+#pragma unroll
+        for (int e = 31; e >= 0; --e)
+            if (z[e] == m) r.idx = v0 + e;
+    }
+    return r;
+}
+
+struct TcShared {
+    uint8_t* a;          // MT * KB blocks (gathered U rows)
+    uint8_t* b;          // S blocks (Wt tiles)
+    uint64_t* full;      // [S]
+    uint64_t* empty;     // [S]
+    uint64_t* tfull;     // [2]
+    uint64_t* tempty;    // [2]
+    uint64_t* drain;     // [1]
+    int S;
+};
+
+// The tensor-core tile phase of one biased pass.  Pipeline counters persist across
+// passes in the registers of the thread that owns each role.
+template <int MT, typename LT>
+__device__ bool tc_tile_phase(const DraftParams& p, const CUtensorMap* tmap, const int32_t* prev, const TcShared& sh,
+                              uint32_t tmem, uint32_t& it_p, uint32_t& it_m, uint32_t& jt_m, uint32_t& jt_e) {
+    const int R = p.B * p.gamma;
+    const int KB = p.r / kTcK;
+    const int CPR = p.r / 8;                  // 16-byte chunks per U row
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bf16_t* U = static_cast<const bf16_t*>(p.U);
+    __shared__ int s_fail;
+
+    // gather A = U[x_prev(n)] for the padded rows, 128-byte swizzled, K-major
+    if (threadIdx.x == 0) s_fail = 0;
+    for (int idx = threadIdx.x; idx < MT * 128 * CPR; idx += blockDim.x) {
+        const int n = idx / CPR, kc = idx - n * CPR;
+        const int kb = kc >> 3, c = kc & 7, mt = n >> 7, nl = n & 127;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (n < R) {
+            const int x = prev_token(p, prev, n);
+            if (x >= 0 && x < p.V) v = __ldg(reinterpret_cast<const uint4*>(U + (size_t)x * p.r) + kc);
+        }
+        *reinterpret_cast<uint4*>(sh.a + (size_t)(mt * KB + kb) * kTcBlock + nl * 128 + ((c ^ (nl & 7)) << 4)) = v;
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+
+    const int tb = tile_begin(blockIdx.x, gridDim.x, p.n_tiles), te = tile_begin(blockIdx.x + 1, gridDim.x, p.n_tiles);
+    const int S = sh.S;
+    if (warp == 0) {
+        if (lane == 0) {
+            for (int t = tb; t < te && !*(volatile int*)&s_fail; ++t) {
+                for (int kb = 0; kb < KB; ++kb) {
+                    const uint32_t s = it_p % S, ph = (it_p / S) & 1u;
+                    if (!mbar_wait(&sh.empty[s], ph ^ 1u, p.status, kWaitLimitNs)) { s_fail = 1; break; }
+                    mbar_arrive_expect_tx(&sh.full[s], kTcBlock);
+                    tma_load_2d(sh.b + (size_t)s * kTcBlock, tmap, kb * kTcK, t * kTcN, &sh.full[s]);
+                    ++it_p;
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            for (int t = tb; t < te && !*(volatile int*)&s_fail; ++t) {
+                const uint32_t buf = jt_m & 1u, jph = (jt_m >> 1) & 1u;
+                if (!mbar_wait(&sh.tempty[buf], jph ^ 1u, p.status, kWaitLimitNs)) { s_fail = 1; break; }
+                tc_fence_after();
+                for (int kb = 0; kb < KB; ++kb) {
+                    const uint32_t s = it_m % S, ph = (it_m / S) & 1u;
+                    if (!mbar_wait(&sh.full[s], ph, p.status, kWaitLimitNs)) { s_fail = 1; break; }
+                    tc_fence_after();
+                    const uint32_t b0 = smem_u32(sh.b + (size_t)s * kTcBlock);
+#pragma unroll
+                    for (int kk = 0; kk < kTcK / 16; ++kk) {
+#pragma unroll
+                        for (int mt = 0; mt < MT; ++mt) {
+                            const uint32_t a0 = smem_u32(sh.a + (size_t)(mt * KB + kb) * kTcBlock);
+                            umma_bf16(tmem + (buf * MT + mt) * kTcN, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32),
+                                      (kb | kk) != 0 ? 1u : 0u);
+                        }
+                    }
+                    umma_commit(&sh.empty[s]);
+                    ++it_m;
+                }
+                umma_commit(&sh.tfull[buf]);
+                ++jt_m;
+            }
+        }
+    } else {
+        // epilogue: four warps per M tile; thread = one row
+        const int q = warp & 3, mt = (warp - 2) >> 2;
+        const int g = mt * 128 + 32 * q + lane;
+        const bool warp_rows = (mt * 128 + 32 * q) < R;
+        const bool mine = g < R;
+        int prev_ok = 1;
+        if (mine) {
+            const int x = prev_token(p, prev, g);
+            prev_ok = (x >= 0 && x < p.V) ? 1 : 0;
+        }
+        const LT* lrow = static_cast<const LT*>(p.logits) + (size_t)(mine ? g : 0) * p.V;
+        const bool write_z = p.qlogits_out != nullptr;
+        const bool keep_tiles = p.temperature == 1;
+        RowAcc cta = rowacc_empty();
+        for (int t = tb; t < te; ++t) {
+            const uint32_t buf = jt_e & 1u, jph = (jt_e >> 1) & 1u;
+            const long v0 = (long)t * kTcN;
+            uint4 lw[4][8];
+            if (mine) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) load_l32(lrow, v0 + 32 * c, p.V, lw[c]);
+            }
+            if (!mbar_wait(&sh.tfull[buf], jph, p.status, kWaitLimitNs)) { s_fail = 1; break; }
+            tc_fence_after();
+            if (warp_rows) {
+                const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (buf * MT + mt) * kTcN;
+                RowAcc tacc = rowacc_empty();
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float acc[32];
+                    tmem_ld32(taddr + 32 * c, acc);
+                    if (mine) {
+                        float z[32];
+                        decode_l32(lw[c], z, LT());
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) z[e] = (v0 + 32 * c + e < p.V) ? z[e] + acc[e] : -INFINITY;
+                        tacc = rowacc_merge(tacc, record32(z, (int)(v0 + 32 * c)));
+                        if (write_z) {
+                            float* dst = p.qlogits_out + (size_t)g * p.V + v0 + 32 * c;
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                if (v0 + 32 * c + 4 * i + 4 <= p.V)
+                                    *reinterpret_cast<float4*>(dst + 4 * i) =
+                                        make_float4(z[4 * i], z[4 * i + 1], z[4 * i + 2], z[4 * i + 3]);
+                        }
+                    }
+                }
+                if (mine) {
+                    if (!prev_ok) tacc.bad = 2;
+                    if (keep_tiles) p.tile_rec[(size_t)g * p.n_tiles + t] = rowacc_pack(tacc);
+                    cta = rowacc_merge(cta, tacc);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive1(&sh.tempty[buf]);
+            ++jt_e;
+        }
+        if (mine) {
+            if (!prev_ok) cta.bad = 2;
+            p.cta_rec[(size_t)g * gridDim.x + blockIdx.x] = rowacc_pack(cta);
+        }
+    }
+    __syncthreads();
+    return s_fail == 0;
+}
+
+template <int MT, typename LT>
+__global__ void __launch_bounds__(32 * (2 + 4 * MT), 1)
+    draft_tc_kernel(const __grid_constant__ DraftParams p, const __grid_constant__ CUtensorMap tmap) {
+    extern __shared__ uint8_t s_raw[];
+    uint8_t* base = s_raw + ((1024u - (smem_u32(s_raw) & 1023u)) & 1023u);
+    const int KB = p.r / kTcK;
+    const int nw = blockDim.x >> 5;
+    TcShared sh;
+    sh.S = MT == 1 ? 6 : 4;
+    sh.a = base;
+    sh.b = base + (size_t)MT * KB * kTcBlock;
+    float* s_uw_all = reinterpret_cast<float*>(sh.b + (size_t)sh.S * kTcBlock);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s_uw_all + (size_t)nw * p.r);
+    sh.full = bars;
+    sh.empty = bars + sh.S;
+    sh.tfull = bars + 2 * sh.S;
+    sh.tempty = bars + 2 * sh.S + 2;
+    sh.drain = bars + 2 * sh.S + 4;
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * sh.S + 5);
+    const int warp = threadIdx.x >> 5;
+    float* s_uw = s_uw_all + (size_t)warp * p.r;
+    const uint32_t tmem_cols = MT == 1 ? 256u : 512u;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < sh.S; ++s) { mbar_init(&sh.full[s], 1); mbar_init(&sh.empty[s], 1); }
+        for (int b = 0; b < 2; ++b) { mbar_init(&sh.tfull[b], 1); mbar_init(&sh.tempty[b], 4 * MT); }
+        mbar_init(sh.drain, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(s_tmem, tmem_cols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *s_tmem;
+
+    uint32_t it_p = 0, it_m = 0, jt_m = 0, jt_e = 0;
+    const int R = p.B * p.gamma;
+    const unsigned nb = gridDim.x;
+    bool ok = true;
+    int pass = 0;
+    for (;; ++pass) {
+        const bool use_bias = pass > 0;
+        const int32_t* prev = p.tokbuf + ((pass + 1) & 1) * (size_t)R;
+        int32_t* cur = p.tokbuf + (pass & 1) * (size_t)R;
+        if (blockIdx.x == 0 && threadIdx.x == 0) p.changed[pass + 1] = 0u;
+        if (use_bias) {
+            if (!tc_tile_phase<MT, LT>(p, &tmap, prev, sh, tmem, it_p, it_m, jt_m, jt_e)) { ok = false; break; }
+        } else {
+            tile_phase_cc<LT, bf16_t>(p, false, prev, s_uw);
+        }
+        if (!block_barrier(p.barrier, nb, p.status)) { ok = false; break; }
+        finalize_rows<LT, bf16_t>(p, pass, use_bias, prev, cur, gridDim.x, s_uw);
+        if (!block_barrier(p.barrier, nb, p.status)) { ok = false; break; }
+        if (pass >= 1 && __ldcg(&p.changed[pass]) == 0u) break;
+        if (pass == p.gamma) break;
+    }
+
+    // every MMA this CTA issued has completed before TMEM is released
+    __syncthreads();
+    if (threadIdx.x == 32) {
+        umma_commit(sh.drain);
+        mbar_wait(sh.drain, 0u, p.status, kWaitLimitNs);
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, tmem_cols);
+    }
+    if (!ok || blockIdx.x != 0) return;
+    chain_fixup(p);
+    if (threadIdx.x == 0 && p.passes_out) *p.passes_out = pass;
+}
+
+// ----------------------------------------------------------------------------------
+// Host side
+// ----------------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+bool draft_tc_supported(const DraftParams& p) {
+    const int R = p.B * p.gamma;
+    return p.r >= kTcK && p.r <= 256 && p.r % kTcK == 0 && p.wdt == SPEC_BF16 && R <= 256 && p.vec_l &&
+           encode_tiled() != nullptr;
+}
+
+template <int MT, typename LT>
+static cudaError_t launch_tc(const DraftParams& p, cudaStream_t stream) {
+    const int threads = 32 * (2 + 4 * MT);
+    const int S = MT == 1 ? 6 : 4;
+    const int KB = p.r / kTcK;
+    const size_t smem = 1024 + (size_t)MT * KB * kTcBlock + (size_t)S * kTcBlock + sizeof(float) * (threads / 32) * p.r +
+                        sizeof(uint64_t) * (2 * S + 5) + 16;
+    auto kern = draft_tc_kernel<MT, LT>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int occ = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem);
+    if (e != cudaSuccess) return e;
+    if (occ < 1) return cudaErrorInvalidConfiguration;
+    int grid = device_sm_count();   // one CTA per SM (TMEM and shared memory sized for it)
+    if (grid > p.n_tiles) grid = p.n_tiles;
+
+    CUtensorMap tmap;
+    const cuuint64_t dims[2] = {(cuuint64_t)p.r, (cuuint64_t)p.V};
+    const cuuint64_t strides[1] = {(cuuint64_t)p.r * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kTcK, (cuuint32_t)kTcN};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode_tiled()(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p.Wt), dims, strides, box, estr,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    DraftParams args = p;
+    void* kargs[] = {&args, &tmap};
+    return cudaLaunchCooperativeKernel((const void*)kern, dim3(grid), dim3(threads), kargs, smem, stream);
+}
+
+cudaError_t draft_launch_tc(const DraftParams& p, cudaStream_t stream) {
+    const int R = p.B * p.gamma;
+    const bool lb = p.ldt == SPEC_BF16;
+    if (R <= 128) return lb ? launch_tc<1, bf16_t>(p, stream) : launch_tc<1, float>(p, stream);
+    return lb ? launch_tc<2, bf16_t>(p, stream) : launch_tc<2, float>(p, stream);
+}
+
+}  // namespace spec
