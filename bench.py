@@ -260,7 +260,7 @@ def run_ours(args, rank, world, torch, dist):
             "parallelism": f"replicas x{world} (independent requests per GPU, no collective)",
         },
         "roofline": {
-            "kernel": "spec::draft_kernel" if dominant == "draft" else "spec::verify_t0_kernel",
+            "kernel": "spec::draft_tc_kernel" if dominant == "draft" else "spec::verify_t0_kernel",
             "bound": "hbm",
             "achieved": achieved,
             "peak": hbm,

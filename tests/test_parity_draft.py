@@ -102,7 +102,10 @@ def test_strong_bias_needs_many_passes(spec, T, wdtype, r):
     anchor = synth.anchors(B, V, seed=5)
     seeds = synth.seeds_for(B, 9)
     out = _gpu(L, anchor, U, Wt, T, seeds)
-    check_draft(out, L, anchor, U, Wt, T, seeds)
+    # |z| reaches ~50 here (the bias alone has std ~18): float32 accumulation of z carries
+    # errors near 2^-24 * sqrt(r) * sum_k |u_k w_k| ~ 4e-5, so this stress case bounds the
+    # confidence by 1e-4 instead of the 1e-5 used at the pages' scales (tokens stay exact)
+    check_draft(out, L, anchor, U, Wt, T, seeds, tol=1e-4)
     assert int(out["passes"].item()) >= 3
 
 
