@@ -111,6 +111,14 @@ spec_status spec_get_device_status(const void *workspace, spec_stream_t stream,
 const char *spec_status_string(spec_status status);
 
 /*
+ * spec_last_cuda_error - the CUDA runtime error code behind the most recent
+ * SPEC_ERR_CUDA returned on the calling host thread (0 if none), and its message.
+ * Kept per host thread, like errno; no other call state is kept.
+ */
+int spec_last_cuda_error(void);
+const char *spec_last_cuda_error_string(void);
+
+/*
  * spec_draft_block - DSpark block draft with the rank-r Markov logit bias.
  *
  * Defines ("Speculative Decoding Part 2", VESSL AI, DSpark section, bias equation;

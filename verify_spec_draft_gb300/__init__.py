@@ -35,6 +35,8 @@ SIGNATURES = {
     "spec_workspace_init": (_i32, [_vp, _sz, _vp]),
     "spec_get_device_status": (_i32, [_vp, _vp, _u32p]),
     "spec_status_string": (ctypes.c_char_p, [_i32]),
+    "spec_last_cuda_error": (_i32, []),
+    "spec_last_cuda_error_string": (ctypes.c_char_p, []),
     "spec_draft_block": (_i32, [_vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp,
                                 _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "spec_verify": (_i32, [_vp, _i32, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _vp,
@@ -47,7 +49,10 @@ _lib = None
 
 class SpecError(RuntimeError):
     def __init__(self, code, what):
-        super().__init__(f"{what}: {STATUS.get(code, code)} ({status_string(code)})")
+        msg = f"{what}: {STATUS.get(code, code)} ({status_string(code)})"
+        if code == 5 and _lib is not None:
+            msg += f" [cuda error {_lib.spec_last_cuda_error()}: {_lib.spec_last_cuda_error_string().decode()}]"
+        super().__init__(msg)
         self.code = code
 
 

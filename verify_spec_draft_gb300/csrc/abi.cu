@@ -23,6 +23,14 @@ int device_sm_count() {
     return n;
 }
 
+static thread_local int g_last_cuda_error = 0;   // per host thread, like errno
+
+static spec_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return SPEC_OK;
+    g_last_cuda_error = (int)e;
+    return SPEC_ERR_CUDA;
+}
+
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 static bool dtype_ok(int d) { return d == SPEC_F32 || d == SPEC_BF16; }
 static size_t dtype_size(int d) { return d == SPEC_F32 ? 4 : 2; }
@@ -52,16 +60,15 @@ size_t spec_workspace_bytes(spec_op op, int B, int gamma, int V, int r) {
 
 spec_status spec_workspace_init(void* workspace, size_t bytes, spec_stream_t stream) {
     if (!workspace || bytes < kWsHeaderBytes) return SPEC_ERR_WORKSPACE;
-    if (cudaMemsetAsync(workspace, 0, bytes, (cudaStream_t)stream) != cudaSuccess) return SPEC_ERR_CUDA;
-    return SPEC_OK;
+    return cuda_status(cudaMemsetAsync(workspace, 0, bytes, (cudaStream_t)stream));
 }
 
 spec_status spec_get_device_status(const void* workspace, spec_stream_t stream, uint32_t* flags_out) {
     if (!workspace) return SPEC_ERR_WORKSPACE;
     uint32_t flags = 0;
-    if (cudaMemcpyAsync(&flags, workspace, sizeof(flags), cudaMemcpyDeviceToHost, (cudaStream_t)stream) != cudaSuccess)
+    if (cuda_status(cudaMemcpyAsync(&flags, workspace, sizeof(flags), cudaMemcpyDeviceToHost, (cudaStream_t)stream)))
         return SPEC_ERR_CUDA;
-    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (cuda_status(cudaStreamSynchronize((cudaStream_t)stream))) return SPEC_ERR_CUDA;
     if (flags_out) *flags_out = flags;
     if (flags & SPEC_DEV_TIMEOUT) return SPEC_ERR_TIMEOUT;
     if (flags & SPEC_DEV_TOKEN) return SPEC_ERR_TOKEN;
@@ -83,6 +90,12 @@ const char* spec_status_string(spec_status s) {
         case SPEC_ERR_WORKSPACE: return "workspace missing or too small";
         default: return "unknown status";
     }
+}
+
+int spec_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char* spec_last_cuda_error_string(void) {
+    return g_last_cuda_error ? cudaGetErrorString((cudaError_t)g_last_cuda_error) : "no CUDA error";
 }
 
 spec_status spec_draft_block(const void* draft_logits, spec_dtype logits_dtype, const int32_t* anchor,
@@ -126,7 +139,7 @@ spec_status spec_draft_block(const void* draft_logits, spec_dtype logits_dtype, 
     p.vec_l = ((size_t)V * dtype_size(logits_dtype)) % 16 == 0;
     p.vec_w = r > 0 && ((size_t)r * dtype_size(w_dtype)) % 16 == 0;
     draft_bind_workspace(p, workspace);
-    return draft_launch(p, (cudaStream_t)stream) == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+    return cuda_status(draft_launch(p, (cudaStream_t)stream));
 }
 
 spec_status spec_verify(const void* target_logits, spec_dtype target_dtype, const void* draft_logits,
@@ -163,7 +176,7 @@ spec_status spec_verify(const void* target_logits, spec_dtype target_dtype, cons
     p.bonus_out = bonus_out;
     p.near_out = near_tie_out;
     verify_bind_workspace(p, workspace);
-    return verify_launch(p, (cudaStream_t)stream) == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+    return cuda_status(verify_launch(p, (cudaStream_t)stream));
 }
 
 spec_status spec_e2etv(const uint16_t* target_logits, const uint16_t* draft_logits, int n_branches, int Wb, int V,
@@ -190,7 +203,7 @@ spec_status spec_e2etv(const uint16_t* target_logits, const uint16_t* draft_logi
     p.surv_out = surv_out;
     p.loss_out = loss_out;
     p.grad_out = grad_out;
-    return e2etv_launch(p, workspace, (cudaStream_t)stream) == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+    return cuda_status(e2etv_launch(p, workspace, (cudaStream_t)stream));
 }
 
 }  // extern "C"

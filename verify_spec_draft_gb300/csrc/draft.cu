@@ -31,16 +31,20 @@ __global__ void __launch_bounds__(kThreads) draft_kernel(DraftParams p) {
     const bool biased = p.r > 0;
     const unsigned nb = gridDim.x;
     const int R = p.B * p.gamma;
+    pdl_launch_dependents();   // a following verify may stream its target rows meanwhile
+    GridBarrier gb = grid_barrier_init(p.barrier);
     int pass = 0;
     for (;; ++pass) {
         const bool use_bias = biased && pass > 0;
         const int32_t* prev = p.tokbuf + ((pass + 1) & 1) * (size_t)R;
         int32_t* cur = p.tokbuf + (pass & 1) * (size_t)R;
         if (blockIdx.x == 0 && threadIdx.x == 0) p.changed[pass + 1] = 0u;
-        tile_phase_cc<LT, WT>(p, use_bias, prev, s_uw);
-        if (!block_barrier(p.barrier, nb, p.status)) return;
+        if (!use_bias && p.vec_l && p.temperature == 0) tile_phase_stream0_t0<LT>(p, p.cta_rec, !biased);
+        else if (!use_bias && p.vec_l) tile_phase_stream0<LT>(p);
+        else tile_phase_cc<LT, WT>(p, use_bias, prev, s_uw);
+        if (!grid_barrier(gb, nb, p.status)) return;
         finalize_rows<LT, WT>(p, pass, use_bias, prev, cur, gridDim.x, s_uw);
-        if (!block_barrier(p.barrier, nb, p.status)) return;
+        if (!grid_barrier(gb, nb, p.status)) return;
         if (!biased) break;
         if (pass >= 1 && __ldcg(&p.changed[pass]) == 0u) break;
         if (pass == p.gamma) break;
@@ -64,6 +68,7 @@ size_t draft_workspace_bytes(int B, int gamma, int V, int r) {
     size_t off = kWsHeaderBytes;
     off = align_up(off + sizeof(float4) * R * n_tiles, 256);        // tile records
     off = align_up(off + sizeof(float4) * R * kDraftMaxGrid, 256);  // CTA records
+    off = align_up(off + sizeof(float4) * R * kDraftMaxGrid, 256);  // second buffer
     off = align_up(off + sizeof(int32_t) * 2 * R, 256);
     off = align_up(off + sizeof(unsigned) * (gamma + 2), 256);
     return off;
@@ -80,6 +85,8 @@ void draft_bind_workspace(DraftParams& p, void* ws) {
     p.tile_rec = reinterpret_cast<float4*>(w + off);
     off = align_up(off + sizeof(float4) * R * p.n_tiles, 256);
     p.cta_rec = reinterpret_cast<float4*>(w + off);
+    off = align_up(off + sizeof(float4) * R * kDraftMaxGrid, 256);
+    p.cta_rec2 = reinterpret_cast<float4*>(w + off);
     off = align_up(off + sizeof(float4) * R * kDraftMaxGrid, 256);
     p.tokbuf = reinterpret_cast<int32_t*>(w + off);
     off = align_up(off + sizeof(int32_t) * 2 * R, 256);

@@ -91,9 +91,12 @@ __device__ __forceinline__ RowAcc warp_rowacc_of(const float (&z)[4], const long
     return RowAcc{m, s, idx, bad};
 }
 
+// x_{j-1} of a row: the anchor at j = 0, else the previous pass's token of the row
+// before (in shared or global memory; read with a relaxed load so a token another CTA
+// wrote is seen).
 __device__ __forceinline__ int prev_token(const DraftParams& p, const int32_t* prev, int row) {
     const int j = row % p.gamma;
-    return j == 0 ? p.anchor[row / p.gamma] : __ldcg(&prev[row - 1]);
+    return j == 0 ? p.anchor[row / p.gamma] : ld_relaxed_i32(&prev[row - 1]);
 }
 
 // z for the four entries v = tile*128 + 32*i + lane of one row, computed on CUDA
@@ -310,6 +313,255 @@ __device__ void tile_phase_cc(const DraftParams& p, bool use_bias, const int32_t
         if (lane == 0) p.cta_rec[(size_t)row * gridDim.x + blockIdx.x] = rowacc_pack(acc);
         __syncwarp();
     }
+}
+
+// Unbiased tile phase (pass 0) on rows whose bytes are 16-byte aligned: one warp per
+// row, each lane one 16-byte word per unit of 32 words (a unit is one tile of f32 or
+// two tiles of bf16), with the next eight units' loads in flight (register ring,
+// statically indexed).  Tile records are reduced over the lanes of each tile.
+template <typename LT>
+__device__ __forceinline__ void unit_record(const uint4& w, long e0, long V, int lanes_per_tile, RowAcc& out) {
+    constexpr int EPL = 16 / (int)sizeof(LT);
+    float x[EPL];
+    if (sizeof(LT) == 2) {
+        const uint32_t a[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            x[(2 * k) % EPL] = __uint_as_float(a[k] << 16);
+            x[(2 * k + 1) % EPL] = __uint_as_float(a[k] & 0xffff0000u);
+        }
+    } else {
+        x[0] = __uint_as_float(w.x);
+        x[1 % EPL] = __uint_as_float(w.y);
+        x[2 % EPL] = __uint_as_float(w.z);
+        x[3 % EPL] = __uint_as_float(w.w);
+    }
+    float m = -INFINITY;
+    int bad = 0;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+        if (e0 + e < V) { bad |= bad_logit(x[e]) ? 1 : 0; m = fmaxf(m, x[e]); }
+    }
+    for (int o = lanes_per_tile >> 1; o > 0; o >>= 1) {
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+    }
+    float s = 0.0f;
+    int idx = 0x7fffffff;
+    if (m != -INFINITY && !bad) {
+        const float m2 = m * kLog2e;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+            if (e0 + e < V) {
+                s += wexp(x[e], m2);
+                if (x[e] == m) idx = min(idx, (int)(e0 + e));
+            }
+        }
+    }
+    for (int o = lanes_per_tile >> 1; o > 0; o >>= 1) {
+        s += __shfl_xor_sync(0xffffffffu, s, o);
+        idx = min(idx, __shfl_xor_sync(0xffffffffu, idx, o));
+    }
+    out = RowAcc{bad ? -INFINITY : m, s, idx, bad};
+}
+
+// Pass 0 at T=0: only the argmax of the unbiased rows is used when a biased pass
+// follows (need_s false), so each lane keeps a running (max, lowest index) and, if
+// need_s, a running sum rescaled when the max grows; one warp reduction per row.
+template <typename LT>
+__device__ void tile_phase_stream0_t0(const DraftParams& p, float4* rec_out, bool need_s) {
+    constexpr int EPL = 16 / (int)sizeof(LT);
+    constexpr int UNIT = 32 * EPL;
+    const int R = p.B * p.gamma;
+    const int lane = threadIdx.x & 31;
+    const int nw = blockDim.x >> 5;
+    const int tb = tile_begin(blockIdx.x, gridDim.x, p.n_tiles), te = tile_begin(blockIdx.x + 1, gridDim.x, p.n_tiles);
+    const long e_begin = (long)tb * kDraftTile, e_end = (long)te * kDraftTile;
+    const int upr = (int)((e_end - e_begin + UNIT - 1) / UNIT);
+    for (int row = threadIdx.x >> 5; row < R; row += nw) {
+        const LT* lrow = static_cast<const LT*>(p.logits) + (size_t)row * p.V;
+        float m = -INFINITY, s = 0.0f;
+        int idx = 0x7fffffff, bad = 0;
+        for (int u0 = 0; u0 < upr; u0 += 8) {
+            uint4 w[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const long e0 = e_begin + (long)(u0 + k) * UNIT + (long)lane * EPL;
+                w[k] = (u0 + k < upr && e0 < e_end && e0 + EPL <= p.V)
+                           ? __ldg(reinterpret_cast<const uint4*>(lrow + e0))
+                           : (sizeof(LT) == 2 ? make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u)
+                                              : make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u));
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const long e0 = e_begin + (long)(u0 + k) * UNIT + (long)lane * EPL;
+                float x[EPL];
+                if (sizeof(LT) == 2) {
+                    const uint32_t a[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        x[(2 * h) % EPL] = __uint_as_float(a[h] << 16);
+                        x[(2 * h + 1) % EPL] = __uint_as_float(a[h] & 0xffff0000u);
+                    }
+                } else {
+                    x[0] = __uint_as_float(w[k].x);
+                    x[1 % EPL] = __uint_as_float(w[k].y);
+                    x[2 % EPL] = __uint_as_float(w[k].z);
+                    x[3 % EPL] = __uint_as_float(w[k].w);
+                }
+                float m8 = x[0];
+#pragma unroll
+                for (int e = 1; e < EPL; ++e) m8 = fmaxf(m8, x[e]);
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) bad |= bad_logit(x[e]) ? 1 : 0;
+                if (m8 > m) {
+                    if (need_s && m != -INFINITY) s *= ex2(m * kLog2e - m8 * kLog2e);
+                    m = m8;
+#pragma unroll
+                    for (int e = EPL - 1; e >= 0; --e)
+                        if (x[e] == m8) idx = (int)(e0 + e);
+                } else if (m8 == m && m != -INFINITY) {
+#pragma unroll
+                    for (int e = EPL - 1; e >= 0; --e)
+                        if (x[e] == m8) idx = min(idx, (int)(e0 + e));
+                }
+                if (need_s && m != -INFINITY) {
+                    const float m2 = m * kLog2e;
+#pragma unroll
+                    for (int e = 0; e < EPL; ++e) s += wexp(x[e], m2);
+                }
+            }
+        }
+        RowAcc a{bad ? -INFINITY : m, need_s ? s : 0.0f, idx, bad};
+        a = warp_rowacc(a);
+        if (lane == 0) rec_out[(size_t)row * gridDim.x + blockIdx.x] = rowacc_pack(a);
+    }
+}
+
+template <typename LT>
+__device__ void tile_phase_stream0(const DraftParams& p) {
+    constexpr int EPL = 16 / (int)sizeof(LT);          // entries per lane per unit
+    constexpr int UNIT = 32 * EPL;                     // entries per unit
+    constexpr int TPU = UNIT / kDraftTile;             // tiles per unit (1 or 2)
+    constexpr int LPT = 32 / TPU;                      // lanes per tile
+    constexpr int D = 8;                               // units in flight per lane
+    const int R = p.B * p.gamma;
+    const int lane = threadIdx.x & 31;
+    const int nw = blockDim.x >> 5;
+    const int tb = tile_begin(blockIdx.x, gridDim.x, p.n_tiles), te = tile_begin(blockIdx.x + 1, gridDim.x, p.n_tiles);
+    const long e_begin = (long)tb * kDraftTile, e_end = (long)te * kDraftTile;
+    const int upr = (int)((e_end - e_begin + UNIT - 1) / UNIT);   // units per row
+    const int my_rows = (R - (int)(threadIdx.x >> 5) + nw - 1) / nw;
+    const int Nu = my_rows * upr;
+    const bool keep_tiles = p.temperature == 1;
+    auto unit_ptr = [&](int u, long& e0) -> const uint4* {
+        const int row = (int)(threadIdx.x >> 5) + (u / upr) * nw;
+        e0 = e_begin + (long)(u % upr) * UNIT + (long)lane * EPL;
+        return reinterpret_cast<const uint4*>(static_cast<const LT*>(p.logits) + (size_t)row * p.V + e0);
+    };
+    auto load_unit = [&](int u) -> uint4 {
+        long e0;
+        const uint4* ptr = unit_ptr(u, e0);
+        if (e0 + EPL <= p.V && e0 < e_end) return __ldg(ptr);
+        return sizeof(LT) == 2 ? make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u)
+                               : make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
+    };
+    uint4 ring[D];
+#pragma unroll
+    for (int s = 0; s < D; ++s)
+        if (s < Nu) ring[s] = load_unit(s);
+    RowAcc acc = rowacc_empty();
+    for (int u0 = 0; u0 < Nu; u0 += D) {
+#pragma unroll
+        for (int s = 0; s < D; ++s) {
+            const int u = u0 + s;
+            if (u < Nu) {
+                const uint4 w = ring[s];
+                if (u + D < Nu) ring[s] = load_unit(u + D);
+                long e0;
+                unit_ptr(u, e0);
+                RowAcc tr;
+                unit_record<LT>(w, e0, p.V, LPT, tr);
+                const int row = (int)(threadIdx.x >> 5) + (u / upr) * nw;
+                const int t0 = (int)((e0 - lane * EPL) / kDraftTile);   // first tile of the unit
+                // lanes 0..LPT-1 hold the first tile's record, LPT.. the second's
+                RowAcc t1;
+                t1.mx = __shfl_sync(0xffffffffu, tr.mx, LPT % 32);
+                t1.s = __shfl_sync(0xffffffffu, tr.s, LPT % 32);
+                t1.idx = __shfl_sync(0xffffffffu, tr.idx, LPT % 32);
+                t1.bad = __shfl_sync(0xffffffffu, tr.bad, LPT % 32);
+                if (lane == 0) {
+                    if (t0 < te) {
+                        if (keep_tiles) p.tile_rec[(size_t)row * p.n_tiles + t0] = rowacc_pack(tr);
+                        acc = rowacc_merge(acc, tr);
+                    }
+                    if (TPU == 2 && t0 + 1 < te) {
+                        if (keep_tiles) p.tile_rec[(size_t)row * p.n_tiles + t0 + 1] = rowacc_pack(t1);
+                        acc = rowacc_merge(acc, t1);
+                    }
+                    if ((u % upr) == upr - 1) {
+                        p.cta_rec[(size_t)row * gridDim.x + blockIdx.x] = rowacc_pack(acc);
+                        acc = rowacc_empty();
+                    }
+                }
+            }
+        }
+    }
+    // rows without units (an empty tile range) still get an empty record
+    if (upr == 0 && lane == 0)
+        for (int row = threadIdx.x >> 5; row < R; row += nw)
+            p.cta_rec[(size_t)row * gridDim.x + blockIdx.x] = rowacc_pack(rowacc_empty());
+}
+
+// T=0 finalize run by EVERY CTA over every row (so the next pass needs no second grid
+// barrier): the tokens go to this CTA's shared array `cur`; the CTA owning a row
+// (row % gridDim.x) writes its outputs, applying the chain rule (an invalid anchor or
+// position voids the rest of the request).  Returns whether any token differs from
+// `prev` (identical in every CTA, so all leave the pass loop together).
+__device__ __forceinline__ bool finalize_all_t0(const DraftParams& p, const float4* recs_all, const int32_t* prev,
+                                                int32_t* cur, bool compare) {
+    const int R = p.B * p.gamma;
+    const int lane = threadIdx.x & 31;
+    const int nw = blockDim.x >> 5;
+    const int nblk = gridDim.x;
+    for (int row = threadIdx.x >> 5; row < R; row += nw) {
+        const float4* recs = recs_all + (size_t)row * nblk;
+        RowAcc acc = rowacc_empty();
+#pragma unroll 4
+        for (int c = lane; c < nblk; c += 32) acc = rowacc_merge(acc, rowacc_unpack(__ldcg(&recs[c])));
+        acc = warp_rowacc(acc);
+        const bool valid = !acc.bad && acc.mx != -INFINITY;
+        if (lane == 0) cur[row] = valid ? acc.idx : -1;
+        if (lane == 0 && (row % nblk) == (int)blockIdx.x) {
+            // conf for the owner's output; the chain check needs every token, so the
+            // write happens after the barrier below
+            p.conf_out[row] = valid ? ex2(fmaf(acc.mx, kLog2e, -acc.mx * kLog2e)) / acc.s : NAN;
+        }
+    }
+    __syncthreads();
+    int diff = 0;
+    if (compare)
+        for (int row = threadIdx.x; row < R; row += blockDim.x) diff |= (cur[row] != prev[row]) ? 1 : 0;
+    const int changed = __syncthreads_or(diff);
+    // owners: tokens, q(x) = conf at T=0, chain validity and status flags
+    for (int row = blockIdx.x + nblk * (int)threadIdx.x; row < R; row += nblk * (int)blockDim.x) {
+        const int b = row / p.gamma, j = row % p.gamma;
+        const int a = p.anchor[b];
+        bool dead = (a < 0 || a >= p.V);
+        int first_dead = dead ? 0 : -1;
+        for (int k = 0; k <= j && !dead; ++k)
+            if (cur[b * p.gamma + k] < 0) { dead = true; first_dead = k; }
+        if (dead) {
+            p.tokens_out[row] = -1;
+            p.conf_out[row] = NAN;
+            if (p.qtok_out) p.qtok_out[row] = NAN;
+            if (first_dead == j) atomicOr(p.status, (a < 0 || a >= p.V) ? SPEC_DEV_TOKEN : SPEC_DEV_NONFINITE);
+        } else {
+            p.tokens_out[row] = cur[row];
+            if (p.qtok_out) p.qtok_out[row] = p.conf_out[row];
+        }
+    }
+    return changed != 0;
 }
 
 // Chain validity after the last pass (CTA 0): an anchor outside [0, V) or an invalid

@@ -10,16 +10,21 @@
 // bf16, 127 MB at r = 256, V = 248,320) and is read once per pass; the rows are few,
 // so the tensor cores only keep the contraction off the critical path of the stream.
 //
-// Per CTA (one per SM, persistent, contiguous tile range):
+// Per CTA (one per SM, persistent, contiguous tile range), 18 warps:
 //   warp 0      TMA producer: Wt tiles [128 entries x 64 k] (128-byte swizzle) into a
 //               ring of 16 KB stages, completion counted on mbarriers;
 //   warp 1      allocates TMEM and issues tcgen05.mma (M=128, N=128, K=16, bf16 in,
 //               f32 accumulate) from one thread, committing to the ring's "empty"
 //               barriers and, per tile, to a "TMEM full" barrier; two TMEM buffers;
-//   warps 2..   epilogue, four warps per 128-row M tile (warp w reads TMEM lanes
-//               32*(w%4)..+31): each thread owns one row, pulls its 128 accumulators
-//               with tcgen05.ld, adds the drafter logits and folds max / sum-exp /
-//               argmax of the tile into its row's running record.
+//   warps 2-17  epilogue.  Warp w may read TMEM lanes 32*(w%4)..+31 only, so the 16
+//               warps form four groups per lane quadrant, each group splitting the
+//               tile's 128 columns (32 columns per warp with one 128-row M tile, 64
+//               with two).  A thread owns one row: it pulls its columns with
+//               tcgen05.ld, adds the drafter logits (fetched one tile ahead) and folds
+//               max / sum-exp / argmax into its row's running record; the column
+//               slices are merged through shared memory.  Rows are laid out
+//               round-robin over the lane quadrants so a handful of rows still keeps
+//               every group busy.
 // The A operand (the gathered rows U[x_prev(n)]) is written to shared memory in the
 // same K-major 128-byte-swizzled layout once per pass.  Pass 0 (no bias yet) and the
 // finalize run on CUDA cores with every warp.
@@ -102,47 +107,49 @@ __device__ __forceinline__ float fmax_nan_f(float a, float b) {
     return r;
 }
 
-// Drafter logits of 32 consecutive entries (v0 multiple of 32, rows 16-byte aligned,
-// V a multiple of the vector width), -inf past V.
-__device__ __forceinline__ void load_l32(const bf16_t* row, long v0, long V, uint4 (&w)[8]) {
+// Drafter logits of 32 consecutive entries (v0 a multiple of 32, rows 16-byte aligned,
+// V a multiple of the vector width): LW 16-byte words, -inf past V.
+template <typename LT> struct LWords { static constexpr int N = 32 * (int)sizeof(LT) / 16; };
+
+template <typename LT>
+__device__ __forceinline__ void load_l32(const LT* row, long v0, long V, uint4 (&w)[LWords<LT>::N]) {
+    constexpr int N = LWords<LT>::N, EPV = 32 / N;
+    const uint32_t ninf = sizeof(LT) == 2 ? 0xff80ff80u : 0xff800000u;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const long v = v0 + 8 * i;
-        w[i] = (v + 8 <= V) ? __ldg(reinterpret_cast<const uint4*>(row + v)) : make_uint4(0xff80ff80u, 0xff80ff80u,
-                                                                                          0xff80ff80u, 0xff80ff80u);
+    for (int i = 0; i < N; ++i) {
+        const long v = v0 + EPV * i;
+        w[i] = (v + EPV <= V) ? __ldg(reinterpret_cast<const uint4*>(row + v)) : make_uint4(ninf, ninf, ninf, ninf);
     }
 }
-__device__ __forceinline__ void load_l32(const float* row, long v0, long V, uint4 (&w)[8]) {
+// z[e] += logit e, in place
+template <typename LT>
+__device__ __forceinline__ void add_l32(const uint4 (&w)[LWords<LT>::N], float (&z)[32]) {
+    if (sizeof(LT) == 2) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const long v = v0 + 4 * i;
-        w[i] = (v + 4 <= V) ? __ldg(reinterpret_cast<const uint4*>(row + v))
-                            : make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
-    }
-}
-__device__ __forceinline__ void decode_l32(const uint4 (&w)[8], float (&x)[32], bf16_t) {
+        for (int i = 0; i < LWords<LT>::N; ++i) {
+            const uint32_t a[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t a[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+            for (int k = 0; k < 4; ++k) {
+                z[(8 * i + 2 * k) & 31] += __uint_as_float(a[k] << 16);
+                z[(8 * i + 2 * k + 1) & 31] += __uint_as_float(a[k] & 0xffff0000u);
+            }
+        }
+    } else {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            x[8 * i + 2 * k] = __uint_as_float(a[k] << 16);
-            x[8 * i + 2 * k + 1] = __uint_as_float(a[k] & 0xffff0000u);
+        for (int i = 0; i < LWords<LT>::N; ++i) {
+            z[(4 * i) & 31] += __uint_as_float(w[i].x);
+            z[(4 * i + 1) & 31] += __uint_as_float(w[i].y);
+            z[(4 * i + 2) & 31] += __uint_as_float(w[i].z);
+            z[(4 * i + 3) & 31] += __uint_as_float(w[i].w);
         }
     }
 }
-__device__ __forceinline__ void decode_l32(const uint4 (&w)[8], float (&x)[32], float) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        x[4 * i] = __uint_as_float(w[i].x);
-        x[4 * i + 1] = __uint_as_float(w[i].y);
-        x[4 * i + 2] = __uint_as_float(w[i].z);
-        x[4 * i + 3] = __uint_as_float(w[i].w);
-    }
-}
 
-// Record of 32 consecutive entries of one row held by one thread.
-__device__ __forceinline__ RowAcc record32(const float (&z)[32], int v0) {
+// Record of 32 consecutive entries of one row held by one thread.  The lowest index
+// of the maximum is needed only when this chunk raises the running maximum `run_mx`
+// (entries are visited in increasing order, so on a tie the earlier index stands);
+// `want_idx` is false when no argmax is used (T=1).
+__device__ __forceinline__ RowAcc record32(const float (&z)[32], int v0, float run_mx, bool want_idx) {
     float m = z[0];
 #pragma unroll
     for (int e = 1; e < 32; ++e) m = fmax_nan_f(m, z[e]);
@@ -157,16 +164,32 @@ __device__ __forceinline__ RowAcc record32(const float (&z)[32], int v0) {
 #pragma unroll
         for (int e = 0; e < 32; e += 2) { s0 += wexp(z[e], m2); s1 += wexp(z[e + 1], m2); }
         r.s = s0 + s1;
+        if (want_idx && m > run_mx) {
 #pragma unroll
-        for (int e = 31; e >= 0; --e)
-            if (z[e] == m) r.idx = v0 + e;
+            for (int e = 31; e >= 0; --e)
+                if (z[e] == m) r.idx = v0 + e;
+        }
     }
     return r;
 }
 
+// Rows are spread over the TMEM lane quadrants so that every epilogue group has rows
+// when there are few: row n sits at MMA row 128*mt + 32*q + l with (mt, q) = the
+// quadrant slot n mod (4*MT) and lane l = n / (4*MT).
+__device__ __forceinline__ int mma_row(int n, int MT) {
+    const int slot = n % (4 * MT), l = n / (4 * MT);
+    return (slot >> 2) * 128 + (slot & 3) * 32 + l;
+}
+__device__ __forceinline__ int row_of(int mt, int q, int l, int MT) { return l * (4 * MT) + mt * 4 + q; }
+
+constexpr int kTcWarps = 18;                 // producer, MMA, 16 epilogue warps
+constexpr int kTcThreads = 32 * kTcWarps;
+
 struct TcShared {
     uint8_t* a;          // MT * KB blocks (gathered U rows)
     uint8_t* b;          // S blocks (Wt tiles)
+    float4* slice_rec;   // [4 groups][4 quadrants][32 lanes] running records
+    float4* tile_rec;    // [2][4][4][32] per-tile slice records (T=1)
     uint64_t* full;      // [S]
     uint64_t* empty;     // [S]
     uint64_t* tfull;     // [2]
@@ -175,11 +198,20 @@ struct TcShared {
     int S;
 };
 
+__device__ __forceinline__ void named_barrier(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
+}
+
 // The tensor-core tile phase of one biased pass.  Pipeline counters persist across
 // passes in the registers of the thread that owns each role.
 template <int MT, typename LT>
-__device__ bool tc_tile_phase(const DraftParams& p, const CUtensorMap* tmap, const int32_t* prev, const TcShared& sh,
-                              uint32_t tmem, uint32_t& it_p, uint32_t& it_m, uint32_t& jt_m, uint32_t& jt_e) {
+__device__ bool tc_tile_phase(const DraftParams& p, const CUtensorMap* tmap, const int32_t* prev, float4* rec_out,
+                              const TcShared& sh, uint32_t tmem, uint32_t& it_p, uint32_t& it_m, uint32_t& jt_m,
+                              uint32_t& jt_e) {
+    constexpr int EW = 4 / MT;                 // column slices per quadrant and M tile
+    constexpr int CPW = kTcN / EW;             // columns per epilogue warp (32 * MT)
+    constexpr int NCH = CPW / 32;              // 32-column chunks per warp (MT)
+    constexpr int LW = LWords<LT>::N;          // 16-byte words per chunk of logits
     const int R = p.B * p.gamma;
     const int KB = p.r / kTcK;
     const int CPR = p.r / 8;                  // 16-byte chunks per U row
@@ -191,7 +223,8 @@ __device__ bool tc_tile_phase(const DraftParams& p, const CUtensorMap* tmap, con
     if (threadIdx.x == 0) s_fail = 0;
     for (int idx = threadIdx.x; idx < MT * 128 * CPR; idx += blockDim.x) {
         const int n = idx / CPR, kc = idx - n * CPR;
-        const int kb = kc >> 3, c = kc & 7, mt = n >> 7, nl = n & 127;
+        const int pos = mma_row(n, MT);
+        const int kb = kc >> 3, c = kc & 7, mt = pos >> 7, nl = pos & 127;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (n < R) {
             const int x = prev_token(p, prev, n);
@@ -244,10 +277,12 @@ __device__ bool tc_tile_phase(const DraftParams& p, const CUtensorMap* tmap, con
             }
         }
     } else {
-        // epilogue: four warps per M tile; thread = one row
-        const int q = warp & 3, mt = (warp - 2) >> 2;
-        const int g = mt * 128 + 32 * q + lane;
-        const bool warp_rows = (mt * 128 + 32 * q) < R;
+        // epilogue: group g4 = (w-2)/4 of lane quadrant q = w%4 holds column slice cs
+        // of M tile mt; thread = one row
+        const int q = warp & 3, g4 = (warp - 2) >> 2;
+        const int mt = g4 / EW, cs = g4 % EW;
+        const int g = row_of(mt, q, lane, MT);
+        const bool group_rows = row_of(mt, q, 0, MT) < R;
         const bool mine = g < R;
         int prev_ok = 1;
         if (mine) {
@@ -257,30 +292,38 @@ __device__ bool tc_tile_phase(const DraftParams& p, const CUtensorMap* tmap, con
         const LT* lrow = static_cast<const LT*>(p.logits) + (size_t)(mine ? g : 0) * p.V;
         const bool write_z = p.qlogits_out != nullptr;
         const bool keep_tiles = p.temperature == 1;
-        RowAcc cta = rowacc_empty();
+        const bool want_idx = p.temperature == 0;
+        const int col0 = cs * CPW;
+        RowAcc run = rowacc_empty();
+        // logits of this warp's columns of tile t, chunk c of tile t+1 requested as soon
+        // as chunk c of tile t is consumed
+        uint4 lw[NCH][LW];
+        if (mine && tb < te) {
+#pragma unroll
+            for (int c = 0; c < NCH; ++c) load_l32<LT>(lrow, (long)tb * kTcN + col0 + 32 * c, p.V, lw[c]);
+        }
         for (int t = tb; t < te; ++t) {
             const uint32_t buf = jt_e & 1u, jph = (jt_e >> 1) & 1u;
-            const long v0 = (long)t * kTcN;
-            uint4 lw[4][8];
-            if (mine) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) load_l32(lrow, v0 + 32 * c, p.V, lw[c]);
-            }
+            const long v0 = (long)t * kTcN + col0;
             if (!mbar_wait(&sh.tfull[buf], jph, p.status, kWaitLimitNs)) { s_fail = 1; break; }
             tc_fence_after();
-            if (warp_rows) {
-                const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (buf * MT + mt) * kTcN;
-                RowAcc tacc = rowacc_empty();
+            RowAcc tacc = rowacc_empty();
+            if (group_rows) {
+                const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (buf * MT + mt) * kTcN + col0;
+                const bool full = v0 + CPW <= p.V;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    float acc[32];
-                    tmem_ld32(taddr + 32 * c, acc);
+                for (int c = 0; c < NCH; ++c) {
+                    float z[32];
+                    tmem_ld32(taddr + 32 * c, z);
                     if (mine) {
-                        float z[32];
-                        decode_l32(lw[c], z, LT());
+                        add_l32<LT>(lw[c], z);
+                        if (t + 1 < te) load_l32<LT>(lrow, v0 + kTcN + 32 * c, p.V, lw[c]);
+                        if (!full) {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) z[e] = (v0 + 32 * c + e < p.V) ? z[e] + acc[e] : -INFINITY;
-                        tacc = rowacc_merge(tacc, record32(z, (int)(v0 + 32 * c)));
+                            for (int e = 0; e < 32; ++e)
+                                if (v0 + 32 * c + e >= p.V) z[e] = -INFINITY;
+                        }
+                        tacc = rowacc_merge(tacc, record32(z, (int)(v0 + 32 * c), fmaxf(run.mx, tacc.mx), want_idx));
                         if (write_z) {
                             float* dst = p.qlogits_out + (size_t)g * p.V + v0 + 32 * c;
 #pragma unroll
@@ -291,38 +334,59 @@ __device__ bool tc_tile_phase(const DraftParams& p, const CUtensorMap* tmap, con
                         }
                     }
                 }
-                if (mine) {
-                    if (!prev_ok) tacc.bad = 2;
-                    if (keep_tiles) p.tile_rec[(size_t)g * p.n_tiles + t] = rowacc_pack(tacc);
-                    cta = rowacc_merge(cta, tacc);
-                }
+                if (mine && !prev_ok) tacc.bad = 2;
+                run = rowacc_merge(run, tacc);
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive1(&sh.tempty[buf]);
             ++jt_e;
+            if (keep_tiles && group_rows) {
+                // T=1: merge the column slices of the tile in slice order
+                float4* slot = sh.tile_rec + (size_t)(buf * 16 + g4 * 4 + q) * 32;
+                slot[lane] = rowacc_pack(tacc);
+                named_barrier(1 + mt * 4 + q, 32 * EW);
+                if (cs == 0 && mine) {
+                    RowAcc m = rowacc_empty();
+                    for (int k = 0; k < EW; ++k)
+                        m = rowacc_merge(m, rowacc_unpack(sh.tile_rec[(size_t)(buf * 16 + (mt * EW + k) * 4 + q) * 32 + lane]));
+                    p.tile_rec[(size_t)g * p.n_tiles + t] = rowacc_pack(m);
+                }
+            }
         }
-        if (mine) {
-            if (!prev_ok) cta.bad = 2;
-            p.cta_rec[(size_t)g * gridDim.x + blockIdx.x] = rowacc_pack(cta);
-        }
+        if (mine && !prev_ok) run.bad = 2;
+        sh.slice_rec[(size_t)(g4 * 4 + q) * 32 + lane] = rowacc_pack(run);
     }
     __syncthreads();
-    return s_fail == 0;
+    // the CTA's record per row: its column slices merged in slice order
+    if (warp >= 2) {
+        const int q = warp & 3, g4 = (warp - 2) >> 2;
+        const int mt = g4 / EW, cs = g4 % EW;
+        const int g = row_of(mt, q, lane, MT);
+        if (cs == 0 && g < R) {
+            RowAcc m = rowacc_empty();
+            for (int k = 0; k < EW; ++k)
+                m = rowacc_merge(m, rowacc_unpack(sh.slice_rec[(size_t)((mt * EW + k) * 4 + q) * 32 + lane]));
+            rec_out[(size_t)g * gridDim.x + blockIdx.x] = rowacc_pack(m);
+        }
+    }
+    return *(volatile int*)&s_fail == 0;
 }
 
 template <int MT, typename LT>
-__global__ void __launch_bounds__(32 * (2 + 4 * MT), 1)
+__global__ void __launch_bounds__(kTcThreads, 1)
     draft_tc_kernel(const __grid_constant__ DraftParams p, const __grid_constant__ CUtensorMap tmap) {
     extern __shared__ uint8_t s_raw[];
     uint8_t* base = s_raw + ((1024u - (smem_u32(s_raw) & 1023u)) & 1023u);
     const int KB = p.r / kTcK;
     const int nw = blockDim.x >> 5;
     TcShared sh;
-    sh.S = MT == 1 ? 6 : 4;
+    sh.S = MT == 1 ? 6 : 3;
     sh.a = base;
     sh.b = base + (size_t)MT * KB * kTcBlock;
-    float* s_uw_all = reinterpret_cast<float*>(sh.b + (size_t)sh.S * kTcBlock);
+    sh.slice_rec = reinterpret_cast<float4*>(sh.b + (size_t)sh.S * kTcBlock);
+    sh.tile_rec = sh.slice_rec + 16 * 32;
+    float* s_uw_all = reinterpret_cast<float*>(sh.tile_rec + 2 * 16 * 32);
     uint64_t* bars = reinterpret_cast<uint64_t*>(s_uw_all + (size_t)nw * p.r);
     sh.full = bars;
     sh.empty = bars + sh.S;
@@ -330,13 +394,15 @@ __global__ void __launch_bounds__(32 * (2 + 4 * MT), 1)
     sh.tempty = bars + 2 * sh.S + 2;
     sh.drain = bars + 2 * sh.S + 4;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * sh.S + 5);
+    int32_t* s_tok = reinterpret_cast<int32_t*>(s_tmem + 4);   // [2][B*gamma] (T=0)
     const int warp = threadIdx.x >> 5;
     float* s_uw = s_uw_all + (size_t)warp * p.r;
     const uint32_t tmem_cols = MT == 1 ? 256u : 512u;
 
+    pdl_launch_dependents();   // a following verify may stream its target rows meanwhile
     if (threadIdx.x == 0) {
         for (int s = 0; s < sh.S; ++s) { mbar_init(&sh.full[s], 1); mbar_init(&sh.empty[s], 1); }
-        for (int b = 0; b < 2; ++b) { mbar_init(&sh.tfull[b], 1); mbar_init(&sh.tempty[b], 4 * MT); }
+        for (int b = 0; b < 2; ++b) { mbar_init(&sh.tfull[b], 1); mbar_init(&sh.tempty[b], kTcWarps - 2); }
         mbar_init(sh.drain, 1);
         fence_mbar_init();
     }
@@ -349,23 +415,46 @@ __global__ void __launch_bounds__(32 * (2 + 4 * MT), 1)
     uint32_t it_p = 0, it_m = 0, jt_m = 0, jt_e = 0;
     const int R = p.B * p.gamma;
     const unsigned nb = gridDim.x;
+    GridBarrier gb = grid_barrier_init(p.barrier);
     bool ok = true;
     int pass = 0;
-    for (;; ++pass) {
-        const bool use_bias = pass > 0;
-        const int32_t* prev = p.tokbuf + ((pass + 1) & 1) * (size_t)R;
-        int32_t* cur = p.tokbuf + (pass & 1) * (size_t)R;
-        if (blockIdx.x == 0 && threadIdx.x == 0) p.changed[pass + 1] = 0u;
-        if (use_bias) {
-            if (!tc_tile_phase<MT, LT>(p, &tmap, prev, sh, tmem, it_p, it_m, jt_m, jt_e)) { ok = false; break; }
-        } else {
-            tile_phase_cc<LT, bf16_t>(p, false, prev, s_uw);
+    if (p.temperature == 0) {
+        // T=0: every CTA finalizes every row, so a pass needs one grid barrier; records
+        // alternate between two buffers so no CTA overwrites what another still reads
+        int32_t* tok[2] = {s_tok, s_tok + R};
+        tile_phase_stream0_t0<LT>(p, p.cta_rec, false);
+        if (!grid_barrier(gb, nb, p.status)) ok = false;
+        if (ok) finalize_all_t0(p, p.cta_rec, nullptr, tok[0], false);
+        for (pass = 1; ok; ++pass) {
+            float4* rec = (pass & 1) ? p.cta_rec2 : p.cta_rec;
+            if (!tc_tile_phase<MT, LT>(p, &tmap, tok[(pass + 1) & 1], rec, sh, tmem, it_p, it_m, jt_m, jt_e)) {
+                ok = false;
+                break;
+            }
+            if (!grid_barrier(gb, nb, p.status)) { ok = false; break; }
+            const bool changed = finalize_all_t0(p, rec, tok[(pass + 1) & 1], tok[pass & 1], true);
+            if (!changed || pass == p.gamma) break;
         }
-        if (!block_barrier(p.barrier, nb, p.status)) { ok = false; break; }
-        finalize_rows<LT, bf16_t>(p, pass, use_bias, prev, cur, gridDim.x, s_uw);
-        if (!block_barrier(p.barrier, nb, p.status)) { ok = false; break; }
-        if (pass >= 1 && __ldcg(&p.changed[pass]) == 0u) break;
-        if (pass == p.gamma) break;
+    } else {
+        for (;; ++pass) {
+            const bool use_bias = pass > 0;
+            const int32_t* prev = p.tokbuf + ((pass + 1) & 1) * (size_t)R;
+            int32_t* cur = p.tokbuf + (pass & 1) * (size_t)R;
+            if (blockIdx.x == 0 && threadIdx.x == 0) p.changed[pass + 1] = 0u;
+            if (use_bias) {
+                if (!tc_tile_phase<MT, LT>(p, &tmap, prev, p.cta_rec, sh, tmem, it_p, it_m, jt_m, jt_e)) {
+                    ok = false;
+                    break;
+                }
+            } else {
+                tile_phase_stream0<LT>(p);
+            }
+            if (!grid_barrier(gb, nb, p.status)) { ok = false; break; }
+            finalize_rows<LT, bf16_t>(p, pass, use_bias, prev, cur, gridDim.x, s_uw);
+            if (!grid_barrier(gb, nb, p.status)) { ok = false; break; }
+            if (pass >= 1 && __ldcg(&p.changed[pass]) == 0u) break;
+            if (pass == p.gamma) break;
+        }
     }
 
     // every MMA this CTA issued has completed before TMEM is released
@@ -380,7 +469,7 @@ __global__ void __launch_bounds__(32 * (2 + 4 * MT), 1)
         tmem_dealloc(tmem, tmem_cols);
     }
     if (!ok || blockIdx.x != 0) return;
-    chain_fixup(p);
+    if (p.temperature != 0) chain_fixup(p);   // T=0 owners applied the chain rule already
     if (threadIdx.x == 0 && p.passes_out) *p.passes_out = pass;
 }
 
@@ -412,11 +501,12 @@ bool draft_tc_supported(const DraftParams& p) {
 
 template <int MT, typename LT>
 static cudaError_t launch_tc(const DraftParams& p, cudaStream_t stream) {
-    const int threads = 32 * (2 + 4 * MT);
-    const int S = MT == 1 ? 6 : 4;
+    const int threads = kTcThreads;
+    const int S = MT == 1 ? 6 : 3;
     const int KB = p.r / kTcK;
-    const size_t smem = 1024 + (size_t)MT * KB * kTcBlock + (size_t)S * kTcBlock + sizeof(float) * (threads / 32) * p.r +
-                        sizeof(uint64_t) * (2 * S + 5) + 16;
+    const size_t smem = 1024 + (size_t)MT * KB * kTcBlock + (size_t)S * kTcBlock + sizeof(float4) * 3 * 16 * 32 +
+                        sizeof(float) * kTcWarps * p.r + sizeof(uint64_t) * (2 * S + 5) + 16 +
+                        sizeof(int32_t) * 2 * (size_t)p.B * p.gamma;
     auto kern = draft_tc_kernel<MT, LT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

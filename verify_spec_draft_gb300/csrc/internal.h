@@ -63,6 +63,7 @@ struct DraftParams {
     unsigned* barrier;         // one barrier slot
     float4* tile_rec;          // [R * n_tiles] per-tile records (T=1): max, sum, argmax, bad
     float4* cta_rec;           // [R * grid] per-(row, CTA) records
+    float4* cta_rec2;          // [R * grid] second buffer (passes alternate at T=0)
     int32_t* tokbuf;           // [2 * R] fixed-point iterates
     unsigned* changed;         // [gamma + 2]
 };

@@ -246,6 +246,48 @@ __device__ __forceinline__ bool wait_generation(const unsigned* gen, unsigned se
     return true;
 }
 
+// Grid barrier with the generation read once per kernel: at entry every CTA records
+// the slot's generation (stable: no CTA can complete a barrier before all arrive);
+// each barrier then waits for generation + k.  One atomic round trip per arrival.
+struct GridBarrier {
+    unsigned* slot;
+    unsigned target;
+};
+__device__ __forceinline__ GridBarrier grid_barrier_init(unsigned* slot) {
+    __shared__ unsigned s_gen;
+    if (threadIdx.x == 0) s_gen = ld_acquire(slot + 32);
+    __syncthreads();
+    return GridBarrier{slot, s_gen};
+}
+__device__ __forceinline__ bool grid_barrier(GridBarrier& gb, unsigned nblocks, unsigned* status) {
+    __shared__ int s_ok;
+    __syncthreads();
+    gb.target += 1u;
+    if (threadIdx.x == 0) {
+        unsigned* count = gb.slot;
+        unsigned* gen = gb.slot + 32;
+        const unsigned arrived = atom_add_acq_rel(count, 1u) + 1u;
+        bool ok = true;
+        if (arrived == nblocks) {
+            atomicExch(count, 0u);
+            st_release(gen, gb.target);
+        } else {
+            const unsigned long long t0 = global_timer_ns();
+            unsigned spins = 0;
+            while (ld_acquire(gen) != gb.target) {
+                if (((++spins) & 255u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) {
+                    atomicOr(status, SPEC_DEV_TIMEOUT);
+                    ok = false;
+                    break;
+                }
+            }
+        }
+        s_ok = ok ? 1 : 0;
+    }
+    __syncthreads();
+    return s_ok != 0;
+}
+
 // Barrier over `nblocks` CTAs that are all resident (cooperative launch).  slot[0] is
 // the arrival count, slot[32] the generation (separate 128-byte lines).  The last
 // CTA to arrive resets the count and bumps the generation; the count is back at 0
@@ -269,6 +311,12 @@ __device__ __forceinline__ bool block_barrier(unsigned* slot, unsigned nblocks, 
     }
     __syncthreads();
     return s_ok != 0;
+}
+
+__device__ __forceinline__ int ld_relaxed_i32(const int32_t* p) {
+    int v;
+    asm volatile("ld.relaxed.gpu.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
 }
 
 // "Last CTA done" test: every CTA calls it once after its writes; exactly one CTA
@@ -328,6 +376,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity, unsign
     }
     return true;
 }
+
+// ---------------------------------------------------------------------------------
+// Programmatic dependent launch.  A kernel that produces what the next one reads last
+// lets the next one start early; the dependent waits only where it needs the data.
+// Both are no-ops for launches without the programmatic-serialization attribute.
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait_primary() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // Workspace header (32 KiB at the start of every workspace).
 struct WsHeader {

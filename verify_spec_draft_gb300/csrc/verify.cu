@@ -132,6 +132,8 @@ __global__ void __launch_bounds__(kThreads) verify_t0_kernel(VerifyParams p) {
     const bool vec = p.vec_t != 0;
     constexpr int NW = Words<TT>::N;
     uint4 cur[NW], nxt[NW];
+    __shared__ unsigned long long s_key[2][kWarps];
+    int par = 0;
 
     long it = blockIdx.x;
     if (it < items) {
@@ -161,15 +163,29 @@ __global__ void __launch_bounds__(kThreads) verify_t0_kernel(VerifyParams p) {
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) idx = min(idx, __shfl_xor_sync(0xffffffffu, idx, o));
-        if ((threadIdx.x & 31) == 0) {
-            if (bad) atomicOr(&p.rowbad[row], 1u);
-            else atomicMax(&p.keys[row], argmax_key(m, (uint32_t)idx));
+        // one atomic per CTA and item: warps post their keys, thread 0 folds them
+        // (slots alternate with the item parity, so one barrier per item suffices)
+        if ((threadIdx.x & 31) == 0)
+            s_key[par][threadIdx.x >> 5] = bad ? ~0ull : argmax_key(m, (uint32_t)idx);
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            unsigned long long k = 0ull;
+            int anybad = 0;
+            for (int w = 0; w < kWarps; ++w) {
+                const unsigned long long kw = s_key[par][w];
+                if (kw == ~0ull) anybad = 1;
+                else k = kw > k ? kw : k;
+            }
+            if (anybad) atomicOr(&p.rowbad[row], 1u);
+            else atomicMax(&p.keys[row], k);
         }
+        par ^= 1;
 #pragma unroll
         for (int i = 0; i < NW; ++i) cur[i] = nxt[i];
     }
 
     if (!last_block_done(&p.done[0], gridDim.x)) return;
+    pdl_wait_primary();   // the draft tokens come from the kernel this one may overlap
 
     // prefix scan: one warp per request, one lane per row
     const int G = p.gamma;
@@ -663,14 +679,21 @@ static cudaError_t launch_t1(const VerifyParams& p, cudaStream_t stream) {
 cudaError_t verify_launch(const VerifyParams& p, cudaStream_t stream) {
     if (p.temperature == 0) {
         const long items = (long)p.B * (p.gamma + 1) * p.nchunk;
-        if (p.tdt == SPEC_BF16) {
-            auto k = verify_t0_kernel<bf16_t>;
-            k<<<grid_for(k, items), kThreads, 0, stream>>>(p);
-        } else {
-            auto k = verify_t0_kernel<float>;
-            k<<<grid_for(k, items), kThreads, 0, stream>>>(p);
-        }
-        return cudaGetLastError();
+        // launched as a programmatic dependent: its target-row pass may overlap the
+        // kernel before it (the draft), the final scan waits for that kernel first
+        void (*k)(VerifyParams) = p.tdt == SPEC_BF16 ? verify_t0_kernel<bf16_t> : verify_t0_kernel<float>;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid_for(k, items));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        VerifyParams args = p;
+        return cudaLaunchKernelEx(&cfg, k, args);
     }
     if (p.tdt == SPEC_BF16 && p.ddt == SPEC_BF16) return launch_t1<bf16_t, bf16_t>(p, stream);
     if (p.tdt == SPEC_BF16 && p.ddt == SPEC_F32) return launch_t1<bf16_t, float>(p, stream);
