@@ -198,6 +198,44 @@ spec_status spec_verify(const void *target_logits, spec_dtype target_dtype,
                         size_t workspace_bytes, spec_stream_t stream);
 
 /*
+ * spec_verify_noalloc - spec_verify without a caller-supplied workspace.
+ *
+ * No counterpart in the pages: it exists for callers that cannot allocate device
+ * memory, such as a plugin running inside a host program whose own allocator owns
+ * the GPU's memory and lends none of it out, or a serving process that has given
+ * nearly all device memory to a caching pool (where one more cudaMalloc fails, and
+ * synchronises the device on a latency-critical path even when it succeeds).  It
+ * computes exactly what spec_verify computes, with the same arguments and outputs
+ * minus `workspace` and `workspace_bytes`, and calls no cudaMalloc, cudaFree or other
+ * allocating routine.
+ *
+ * Scratch.  The workspace lives in a static device array of
+ * SPEC_NOALLOC_SCRATCH_BYTES that the library holds on every GPU that loads it, until
+ * the process exits.  A problem whose spec_workspace_bytes(SPEC_OP_VERIFY, B, gamma,
+ * V, 0) exceeds that size is rejected with SPEC_ERR_SHAPE before anything is
+ * enqueued (B = 32, gamma = 7, V = 248,320 needs about 1.05 MB).
+ * Sharing.  Every call on a device uses the same array, which keeps the previous
+ * call's contents: each call first clears the bytes it needs (an asynchronous memset
+ * on `stream`).  Calls whose work overlaps on the GPU (issued on different streams,
+ * or from several host threads without ordering) race on the array and give wrong
+ * results; order them on one stream.
+ * Set-up.  The first call made with a given device current looks up the array's
+ * device address (cudaGetSymbolAddress) and keeps it; make that first call before
+ * any stream capture begins.
+ * Device conditions (a non-finite row, a token out of range, a bounded wait that
+ * ran out) show only as the -1 outputs of the requests concerned: the status word
+ * is inside the array and is cleared by the next call.
+ */
+#define SPEC_NOALLOC_SCRATCH_BYTES (4u << 20)   /* 4 MiB */
+spec_status spec_verify_noalloc(const void *target_logits, spec_dtype target_dtype,
+                                const void *draft_logits, spec_dtype draft_dtype,
+                                const int32_t *draft_tokens, int B, int gamma, int V,
+                                int temperature, const uint64_t *seeds,
+                                int32_t *n_accepted_out, int32_t *committed_out,
+                                int32_t *bonus_out, int32_t *near_tie_out,
+                                spec_stream_t stream);
+
+/*
  * spec_e2etv - SpecOPD E2E-TV surrogate and its gradient.
  *
  * Defines ("SpecOPD" paper summary, onedev.kr, section "how to use it"; VESSL AI

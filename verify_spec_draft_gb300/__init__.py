@@ -42,6 +42,8 @@ SIGNATURES = {
     "spec_verify": (_i32, [_vp, _i32, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _vp,
                            _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "spec_e2etv": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "spec_verify_noalloc": (_i32, [_vp, _i32, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _vp,
+                                   _vp, _vp, _vp, _vp, _vp]),
 }
 
 _lib = None

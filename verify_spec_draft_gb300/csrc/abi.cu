@@ -31,6 +31,8 @@ static spec_status cuda_status(cudaError_t e) {
     return SPEC_ERR_CUDA;
 }
 
+spec_status record_cuda_error(cudaError_t e) { return cuda_status(e); }
+
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 static bool dtype_ok(int d) { return d == SPEC_F32 || d == SPEC_BF16; }
 static size_t dtype_size(int d) { return d == SPEC_F32 ? 4 : 2; }

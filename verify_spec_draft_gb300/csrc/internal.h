@@ -101,4 +101,8 @@ cudaError_t e2etv_launch(E2etvParams& p, void* ws, cudaStream_t stream);
 
 int device_sm_count();
 
+// Keeps e as the calling thread's last CUDA error (spec_last_cuda_error) and
+// returns SPEC_ERR_CUDA, or SPEC_OK for cudaSuccess.
+spec_status record_cuda_error(cudaError_t e);
+
 }  // namespace spec
