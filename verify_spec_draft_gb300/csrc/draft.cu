@@ -49,6 +49,7 @@ __global__ void __launch_bounds__(kThreads) draft_kernel(DraftParams p) {
         if (pass >= 1 && __ldcg(&p.changed[pass]) == 0u) break;
         if (pass == p.gamma) break;
     }
+    grid_barrier_exit(gb, nb);
     if (blockIdx.x != 0) return;
     chain_fixup(p);
     if (threadIdx.x == 0 && p.passes_out) *p.passes_out = biased ? pass : 0;

@@ -94,9 +94,12 @@ __device__ __forceinline__ RowAcc warp_rowacc_of(const float (&z)[4], const long
 // x_{j-1} of a row: the anchor at j = 0, else the previous pass's token of the row
 // before (in shared or global memory; read with a relaxed load so a token another CTA
 // wrote is seen).
-__device__ __forceinline__ int prev_token(const DraftParams& p, const int32_t* prev, int row) {
+__device__ __forceinline__ int prev_token(const DraftParams& p, const int32_t* prev, int row, const int32_t* anc) {
     const int j = row % p.gamma;
-    return j == 0 ? p.anchor[row / p.gamma] : ld_relaxed_i32(&prev[row - 1]);
+    return j == 0 ? anc[row / p.gamma] : ld_relaxed_i32(&prev[row - 1]);
+}
+__device__ __forceinline__ int prev_token(const DraftParams& p, const int32_t* prev, int row) {
+    return prev_token(p, prev, row, p.anchor);
 }
 
 // z for the four entries v = tile*128 + 32*i + lane of one row, computed on CUDA
@@ -380,7 +383,7 @@ __device__ void tile_phase_stream0_t0(const DraftParams& p, float4* rec_out, boo
     const int upr = (int)((e_end - e_begin + UNIT - 1) / UNIT);
     for (int row = threadIdx.x >> 5; row < R; row += nw) {
         const LT* lrow = static_cast<const LT*>(p.logits) + (size_t)row * p.V;
-        float m = -INFINITY, s = 0.0f;
+        float m = -INFINITY, s = 0.0f, mall = -INFINITY;
         int idx = 0x7fffffff, bad = 0;
         for (int u0 = 0; u0 < upr; u0 += 8) {
             uint4 w[8];
@@ -395,6 +398,31 @@ __device__ void tile_phase_stream0_t0(const DraftParams& p, float4* rec_out, boo
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const long e0 = e_begin + (long)(u0 + k) * UNIT + (long)lane * EPL;
+                if (!need_s) {
+                    // argmax only: one packed NaN-propagating maximum per word; the
+                    // entries are looked at only when the word raises the lane's maximum
+                    // (a lane visits its words in increasing index order, so on a tie
+                    // the earlier index stands)
+                    const float m8 = u4_max_nan<(int)sizeof(LT)>(w[k]);
+                    mall = f_max_nan(mall, m8);
+                    if (m8 > m) {
+                        m = m8;
+                        if (sizeof(LT) == 2) {
+                            const uint32_t a[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
+#pragma unroll
+                            for (int h = 3; h >= 0; --h) {
+                                if (__uint_as_float(a[h] & 0xffff0000u) == m8) idx = (int)(e0 + 2 * h + 1);
+                                if (__uint_as_float(a[h] << 16) == m8) idx = (int)(e0 + 2 * h);
+                            }
+                        } else {
+                            const uint32_t a[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
+#pragma unroll
+                            for (int h = 3; h >= 0; --h)
+                                if (__uint_as_float(a[h]) == m8) idx = (int)(e0 + h);
+                        }
+                    }
+                    continue;
+                }
                 float x[EPL];
                 if (sizeof(LT) == 2) {
                     const uint32_t a[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
@@ -432,6 +460,7 @@ __device__ void tile_phase_stream0_t0(const DraftParams& p, float4* rec_out, boo
                 }
             }
         }
+        if (!need_s) bad = (isnan(mall) || mall == INFINITY) ? 1 : 0;
         RowAcc a{bad ? -INFINITY : m, need_s ? s : 0.0f, idx, bad};
         a = warp_rowacc(a);
         if (lane == 0) rec_out[(size_t)row * gridDim.x + blockIdx.x] = rowacc_pack(a);
@@ -519,16 +548,25 @@ __device__ void tile_phase_stream0(const DraftParams& p) {
 // position voids the rest of the request).  Returns whether any token differs from
 // `prev` (identical in every CTA, so all leave the pass loop together).
 __device__ __forceinline__ bool finalize_all_t0(const DraftParams& p, const float4* recs_all, const int32_t* prev,
-                                                int32_t* cur, bool compare) {
+                                                int32_t* cur, bool compare, const int32_t* anc) {
     const int R = p.B * p.gamma;
     const int lane = threadIdx.x & 31;
     const int nw = blockDim.x >> 5;
     const int nblk = gridDim.x;
     for (int row = threadIdx.x >> 5; row < R; row += nw) {
         const float4* recs = recs_all + (size_t)row * nblk;
+        // every record load of the lane in flight at once (up to 256 CTAs), then merged
+        // in CTA order
+        float4 rv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int c = lane + 32 * i;
+            rv[i] = c < nblk ? __ldcg(&recs[c]) : rowacc_pack(rowacc_empty());
+        }
         RowAcc acc = rowacc_empty();
-#pragma unroll 4
-        for (int c = lane; c < nblk; c += 32) acc = rowacc_merge(acc, rowacc_unpack(__ldcg(&recs[c])));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc = rowacc_merge(acc, rowacc_unpack(rv[i]));
+        for (int c = lane + 256; c < nblk; c += 32) acc = rowacc_merge(acc, rowacc_unpack(__ldcg(&recs[c])));
         acc = warp_rowacc(acc);
         const bool valid = !acc.bad && acc.mx != -INFINITY;
         if (lane == 0) cur[row] = valid ? acc.idx : -1;
@@ -546,7 +584,7 @@ __device__ __forceinline__ bool finalize_all_t0(const DraftParams& p, const floa
     // owners: tokens, q(x) = conf at T=0, chain validity and status flags
     for (int row = blockIdx.x + nblk * (int)threadIdx.x; row < R; row += nblk * (int)blockDim.x) {
         const int b = row / p.gamma, j = row % p.gamma;
-        const int a = p.anchor[b];
+        const int a = anc[b];
         bool dead = (a < 0 || a >= p.V);
         int first_dead = dead ? 0 : -1;
         for (int k = 0; k <= j && !dead; ++k)

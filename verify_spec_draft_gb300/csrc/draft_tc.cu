@@ -51,9 +51,6 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
     return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-__device__ __forceinline__ void mbar_arrive1(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_u32(bar)) : "memory");
-}
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
     asm volatile(
@@ -183,6 +180,9 @@ __device__ __forceinline__ int mma_row(int n, int MT) {
 __device__ __forceinline__ int row_of(int mt, int q, int l, int MT) { return l * (4 * MT) + mt * 4 + q; }
 
 constexpr int kTcWarps = 18;                 // producer, MMA, 16 epilogue warps
+// TMEM accumulator buffers: all 512 columns, so the MMA runs up to NB-1 tiles ahead
+// of the epilogue (4 with one 128-row M tile, 2 with two)
+template <int MT> struct TcBufs { static constexpr int N = MT == 1 ? 4 : 2; };
 constexpr int kTcThreads = 32 * kTcWarps;
 
 struct TcShared {
@@ -192,8 +192,8 @@ struct TcShared {
     float4* tile_rec;    // [2][4][4][32] per-tile slice records (T=1)
     uint64_t* full;      // [S]
     uint64_t* empty;     // [S]
-    uint64_t* tfull;     // [2]
-    uint64_t* tempty;    // [2]
+    uint64_t* tfull;     // [NB]
+    uint64_t* tempty;    // [NB]
     uint64_t* drain;     // [1]
     int S;
 };
@@ -205,9 +205,10 @@ __device__ __forceinline__ void named_barrier(int id, int nthreads) {
 // The tensor-core tile phase of one biased pass.  Pipeline counters persist across
 // passes in the registers of the thread that owns each role.
 template <int MT, typename LT>
-__device__ bool tc_tile_phase(const DraftParams& p, const CUtensorMap* tmap, const int32_t* prev, float4* rec_out,
-                              const TcShared& sh, uint32_t tmem, uint32_t& it_p, uint32_t& it_m, uint32_t& jt_m,
-                              uint32_t& jt_e) {
+__device__ bool tc_tile_phase(const DraftParams& p, const CUtensorMap* tmap, const int32_t* prev, const int32_t* anc,
+                              float4* rec_out, const TcShared& sh, uint32_t tmem, uint32_t& it_p, uint32_t& it_m,
+                              uint32_t& jt_m, uint32_t& jt_e, uint32_t& pre_issued) {
+    constexpr int NB = TcBufs<MT>::N;
     constexpr int EW = 4 / MT;                 // column slices per quadrant and M tile
     constexpr int CPW = kTcN / EW;             // columns per epilogue warp (32 * MT)
     constexpr int NCH = CPW / 32;              // 32-column chunks per warp (MT)
@@ -227,7 +228,7 @@ __device__ bool tc_tile_phase(const DraftParams& p, const CUtensorMap* tmap, con
         const int kb = kc >> 3, c = kc & 7, mt = pos >> 7, nl = pos & 127;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (n < R) {
-            const int x = prev_token(p, prev, n);
+            const int x = prev_token(p, prev, n, anc);
             if (x >= 0 && x < p.V) v = __ldg(reinterpret_cast<const uint4*>(U + (size_t)x * p.r) + kc);
         }
         *reinterpret_cast<uint4*>(sh.a + (size_t)(mt * KB + kb) * kTcBlock + nl * 128 + ((c ^ (nl & 7)) << 4)) = v;
@@ -239,8 +240,11 @@ __device__ bool tc_tile_phase(const DraftParams& p, const CUtensorMap* tmap, con
     const int S = sh.S;
     if (warp == 0) {
         if (lane == 0) {
+            uint32_t skip = pre_issued;   // stages of this pass already in flight
+            pre_issued = 0;
             for (int t = tb; t < te && !*(volatile int*)&s_fail; ++t) {
                 for (int kb = 0; kb < KB; ++kb) {
+                    if (skip > 0) { --skip; continue; }
                     const uint32_t s = it_p % S, ph = (it_p / S) & 1u;
                     if (!mbar_wait(&sh.empty[s], ph ^ 1u, p.status, kWaitLimitNs)) { s_fail = 1; break; }
                     mbar_arrive_expect_tx(&sh.full[s], kTcBlock);
@@ -252,7 +256,7 @@ __device__ bool tc_tile_phase(const DraftParams& p, const CUtensorMap* tmap, con
     } else if (warp == 1) {
         if (lane == 0) {
             for (int t = tb; t < te && !*(volatile int*)&s_fail; ++t) {
-                const uint32_t buf = jt_m & 1u, jph = (jt_m >> 1) & 1u;
+                const uint32_t buf = jt_m % NB, jph = (jt_m / NB) & 1u;
                 if (!mbar_wait(&sh.tempty[buf], jph ^ 1u, p.status, kWaitLimitNs)) { s_fail = 1; break; }
                 tc_fence_after();
                 for (int kb = 0; kb < KB; ++kb) {
@@ -286,7 +290,7 @@ __device__ bool tc_tile_phase(const DraftParams& p, const CUtensorMap* tmap, con
         const bool mine = g < R;
         int prev_ok = 1;
         if (mine) {
-            const int x = prev_token(p, prev, g);
+            const int x = prev_token(p, prev, g, anc);
             prev_ok = (x >= 0 && x < p.V) ? 1 : 0;
         }
         const LT* lrow = static_cast<const LT*>(p.logits) + (size_t)(mine ? g : 0) * p.V;
@@ -303,7 +307,7 @@ __device__ bool tc_tile_phase(const DraftParams& p, const CUtensorMap* tmap, con
             for (int c = 0; c < NCH; ++c) load_l32<LT>(lrow, (long)tb * kTcN + col0 + 32 * c, p.V, lw[c]);
         }
         for (int t = tb; t < te; ++t) {
-            const uint32_t buf = jt_e & 1u, jph = (jt_e >> 1) & 1u;
+            const uint32_t buf = jt_e % NB, jph = (jt_e / NB) & 1u;
             const long v0 = (long)t * kTcN + col0;
             if (!mbar_wait(&sh.tfull[buf], jph, p.status, kWaitLimitNs)) { s_fail = 1; break; }
             tc_fence_after();
@@ -340,16 +344,17 @@ __device__ bool tc_tile_phase(const DraftParams& p, const CUtensorMap* tmap, con
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive1(&sh.tempty[buf]);
+            const uint32_t tsl = jt_e & 1u;   // two record slots suffice: a named barrier per tile
             ++jt_e;
             if (keep_tiles && group_rows) {
                 // T=1: merge the column slices of the tile in slice order
-                float4* slot = sh.tile_rec + (size_t)(buf * 16 + g4 * 4 + q) * 32;
+                float4* slot = sh.tile_rec + (size_t)(tsl * 16 + g4 * 4 + q) * 32;
                 slot[lane] = rowacc_pack(tacc);
                 named_barrier(1 + mt * 4 + q, 32 * EW);
                 if (cs == 0 && mine) {
                     RowAcc m = rowacc_empty();
                     for (int k = 0; k < EW; ++k)
-                        m = rowacc_merge(m, rowacc_unpack(sh.tile_rec[(size_t)(buf * 16 + (mt * EW + k) * 4 + q) * 32 + lane]));
+                        m = rowacc_merge(m, rowacc_unpack(sh.tile_rec[(size_t)(tsl * 16 + (mt * EW + k) * 4 + q) * 32 + lane]));
                     p.tile_rec[(size_t)g * p.n_tiles + t] = rowacc_pack(m);
                 }
             }
@@ -390,19 +395,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(s_uw_all + (size_t)nw * p.r);
     sh.full = bars;
     sh.empty = bars + sh.S;
+    constexpr int NB = TcBufs<MT>::N;
     sh.tfull = bars + 2 * sh.S;
-    sh.tempty = bars + 2 * sh.S + 2;
-    sh.drain = bars + 2 * sh.S + 4;
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * sh.S + 5);
+    sh.tempty = bars + 2 * sh.S + NB;
+    sh.drain = bars + 2 * sh.S + 2 * NB;
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * sh.S + 2 * NB + 1);
+    const int R = p.B * p.gamma;
     int32_t* s_tok = reinterpret_cast<int32_t*>(s_tmem + 4);   // [2][B*gamma] (T=0)
+    int32_t* s_anc = s_tok + 2 * R;                             // [B] anchors
     const int warp = threadIdx.x >> 5;
     float* s_uw = s_uw_all + (size_t)warp * p.r;
-    const uint32_t tmem_cols = MT == 1 ? 256u : 512u;
+    constexpr uint32_t tmem_cols = 512u;
 
     pdl_launch_dependents();   // a following verify may stream its target rows meanwhile
     if (threadIdx.x == 0) {
         for (int s = 0; s < sh.S; ++s) { mbar_init(&sh.full[s], 1); mbar_init(&sh.empty[s], 1); }
-        for (int b = 0; b < 2; ++b) { mbar_init(&sh.tfull[b], 1); mbar_init(&sh.tempty[b], kTcWarps - 2); }
+        for (int b = 0; b < NB; ++b) { mbar_init(&sh.tfull[b], 1); mbar_init(&sh.tempty[b], kTcWarps - 2); }
         mbar_init(sh.drain, 1);
         fence_mbar_init();
     }
@@ -412,8 +420,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
 
-    uint32_t it_p = 0, it_m = 0, jt_m = 0, jt_e = 0;
-    const int R = p.B * p.gamma;
+    uint32_t it_p = 0, it_m = 0, jt_m = 0, jt_e = 0, pre_issued = 0;
+    if (threadIdx.x == 0) {
+        // the first biased pass's first Wt stages depend on no token: they are requested
+        // now and land while pass 0 streams the logits
+        const int tb = tile_begin(blockIdx.x, gridDim.x, p.n_tiles);
+        const int te = tile_begin(blockIdx.x + 1, gridDim.x, p.n_tiles);
+        const uint32_t total = (uint32_t)(te - tb) * (uint32_t)KB;
+        pre_issued = total < (uint32_t)sh.S ? total : (uint32_t)sh.S;
+        for (uint32_t i = 0; i < pre_issued; ++i) {
+            mbar_arrive_expect_tx(&sh.full[i], kTcBlock);
+            tma_load_2d(sh.b + (size_t)i * kTcBlock, &tmap, (int)(i % KB) * kTcK, (tb + (int)(i / KB)) * kTcN,
+                        &sh.full[i]);
+        }
+        it_p = pre_issued;
+    }
+    // anchors, first needed after pass 0 and its barrier; loaded by the last warp, which
+    // has no pass-0 row unless there are more rows than warps
+    if (warp == nw - 1)
+        for (int b = threadIdx.x & 31; b < p.B; b += 32) s_anc[b] = p.anchor[b];
     const unsigned nb = gridDim.x;
     GridBarrier gb = grid_barrier_init(p.barrier);
     bool ok = true;
@@ -424,15 +449,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         int32_t* tok[2] = {s_tok, s_tok + R};
         tile_phase_stream0_t0<LT>(p, p.cta_rec, false);
         if (!grid_barrier(gb, nb, p.status)) ok = false;
-        if (ok) finalize_all_t0(p, p.cta_rec, nullptr, tok[0], false);
+        if (ok) finalize_all_t0(p, p.cta_rec, nullptr, tok[0], false, s_anc);
         for (pass = 1; ok; ++pass) {
             float4* rec = (pass & 1) ? p.cta_rec2 : p.cta_rec;
-            if (!tc_tile_phase<MT, LT>(p, &tmap, tok[(pass + 1) & 1], rec, sh, tmem, it_p, it_m, jt_m, jt_e)) {
+            if (!tc_tile_phase<MT, LT>(p, &tmap, tok[(pass + 1) & 1], s_anc, rec, sh, tmem, it_p, it_m, jt_m, jt_e,
+                                       pre_issued)) {
                 ok = false;
                 break;
             }
             if (!grid_barrier(gb, nb, p.status)) { ok = false; break; }
-            const bool changed = finalize_all_t0(p, rec, tok[(pass + 1) & 1], tok[pass & 1], true);
+            const bool changed = finalize_all_t0(p, rec, tok[(pass + 1) & 1], tok[pass & 1], true, s_anc);
             if (!changed || pass == p.gamma) break;
         }
     } else {
@@ -442,7 +468,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             int32_t* cur = p.tokbuf + (pass & 1) * (size_t)R;
             if (blockIdx.x == 0 && threadIdx.x == 0) p.changed[pass + 1] = 0u;
             if (use_bias) {
-                if (!tc_tile_phase<MT, LT>(p, &tmap, prev, p.cta_rec, sh, tmem, it_p, it_m, jt_m, jt_e)) {
+                if (!tc_tile_phase<MT, LT>(p, &tmap, prev, s_anc, p.cta_rec, sh, tmem, it_p, it_m, jt_m, jt_e,
+                                           pre_issued)) {
                     ok = false;
                     break;
                 }
@@ -457,17 +484,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     }
 
-    // every MMA this CTA issued has completed before TMEM is released
+    // every MMA this CTA issued has completed before TMEM is released, and no TMA copy
+    // still writes this CTA's shared memory when it exits (stages requested ahead and
+    // never consumed, after an error)
     __syncthreads();
     if (threadIdx.x == 32) {
         umma_commit(sh.drain);
         mbar_wait(sh.drain, 0u, p.status, kWaitLimitNs);
+    }
+    if (threadIdx.x == 0) {
+        const uint32_t n = it_p < (uint32_t)sh.S ? it_p : (uint32_t)sh.S;
+        for (uint32_t i = it_p - n; i < it_p; ++i)
+            mbar_wait(&sh.full[i % sh.S], (i / sh.S) & 1u, p.status, kWaitLimitNs);
     }
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, tmem_cols);
     }
+    if (ok) grid_barrier_exit(gb, nb);
     if (!ok || blockIdx.x != 0) return;
     if (p.temperature != 0) chain_fixup(p);   // T=0 owners applied the chain rule already
     if (threadIdx.x == 0 && p.passes_out) *p.passes_out = pass;
@@ -505,8 +540,8 @@ static cudaError_t launch_tc(const DraftParams& p, cudaStream_t stream) {
     const int S = MT == 1 ? 6 : 3;
     const int KB = p.r / kTcK;
     const size_t smem = 1024 + (size_t)MT * KB * kTcBlock + (size_t)S * kTcBlock + sizeof(float4) * 3 * 16 * 32 +
-                        sizeof(float) * kTcWarps * p.r + sizeof(uint64_t) * (2 * S + 5) + 16 +
-                        sizeof(int32_t) * 2 * (size_t)p.B * p.gamma;
+                        sizeof(float) * kTcWarps * p.r + sizeof(uint64_t) * (2 * S + 2 * TcBufs<MT>::N + 1) + 16 +
+                        sizeof(int32_t) * (2 * (size_t)p.B * p.gamma + p.B);
     auto kern = draft_tc_kernel<MT, LT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

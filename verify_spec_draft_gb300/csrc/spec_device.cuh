@@ -69,6 +69,28 @@ __device__ __forceinline__ void load_group(const T* row, long v, long V, bool ve
 // A valid logit is finite or -inf; NaN and +inf are not.
 __device__ __forceinline__ bool bad_logit(float x) { return !(x < INFINITY); }
 
+// Larger of two floats, NaN when either is NaN.
+__device__ __forceinline__ float f_max_nan(float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+// Maximum of the entries of one 16-byte word of logits (8 bf16 or 4 float32), NaN
+// when any entry is NaN: one reduction both finds the maximum and flags a NaN, and a
+// +inf entry shows as a maximum of +inf.
+template <int ELT_BYTES>
+__device__ __forceinline__ float u4_max_nan(const uint4& w) {
+    if (ELT_BYTES == 2) {
+        uint32_t a, b, c;
+        asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(a) : "r"(w.x), "r"(w.y));
+        asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(b) : "r"(w.z), "r"(w.w));
+        asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(c) : "r"(a), "r"(b));
+        return f_max_nan(__uint_as_float(c << 16), __uint_as_float(c & 0xffff0000u));
+    }
+    return f_max_nan(f_max_nan(__uint_as_float(w.x), __uint_as_float(w.y)),
+                     f_max_nan(__uint_as_float(w.z), __uint_as_float(w.w)));
+}
+
 // ---------------------------------------------------------------------------------
 // Philox4x64-10 (Salmon, Moraes, Dror, Shaw, SC'11, section 3.2, table 2).
 // ---------------------------------------------------------------------------------
@@ -246,46 +268,51 @@ __device__ __forceinline__ bool wait_generation(const unsigned* gen, unsigned se
     return true;
 }
 
-// Grid barrier with the generation read once per kernel: at entry every CTA records
-// the slot's generation (stable: no CTA can complete a barrier before all arrive);
-// each barrier then waits for generation + k.  One atomic round trip per arrival.
+__device__ __forceinline__ void red_add_release(unsigned* p, unsigned v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+
+// Grid barrier on a monotonic arrival counter (slot[0]): barrier k of a launch is
+// complete once the counter reaches k * nblocks.  An arrival is a fire-and-forget
+// release reduction, so a barrier costs one poll round trip after the last arrival,
+// and nothing is read at kernel entry.  The counter must be 0 at launch: every CTA
+// calls grid_barrier_exit after its last barrier, and the last one to do so resets
+// the counter and the exit count (slot[32]); by then no CTA is still waiting.  After
+// a timeout the counters are left as they are (the workspace must be re-zeroed).
 struct GridBarrier {
-    unsigned* slot;
+    unsigned* count;
+    unsigned* exits;
     unsigned target;
 };
 __device__ __forceinline__ GridBarrier grid_barrier_init(unsigned* slot) {
-    __shared__ unsigned s_gen;
-    if (threadIdx.x == 0) s_gen = ld_acquire(slot + 32);
-    __syncthreads();
-    return GridBarrier{slot, s_gen};
+    return GridBarrier{slot, slot + 32, 0u};
 }
 __device__ __forceinline__ bool grid_barrier(GridBarrier& gb, unsigned nblocks, unsigned* status) {
     __shared__ int s_ok;
     __syncthreads();
-    gb.target += 1u;
+    gb.target += nblocks;
     if (threadIdx.x == 0) {
-        unsigned* count = gb.slot;
-        unsigned* gen = gb.slot + 32;
-        const unsigned arrived = atom_add_acq_rel(count, 1u) + 1u;
+        red_add_release(gb.count, 1u);
         bool ok = true;
-        if (arrived == nblocks) {
-            atomicExch(count, 0u);
-            st_release(gen, gb.target);
-        } else {
-            const unsigned long long t0 = global_timer_ns();
-            unsigned spins = 0;
-            while (ld_acquire(gen) != gb.target) {
-                if (((++spins) & 255u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) {
-                    atomicOr(status, SPEC_DEV_TIMEOUT);
-                    ok = false;
-                    break;
-                }
+        const unsigned long long t0 = global_timer_ns();
+        unsigned spins = 0;
+        while ((int)(ld_acquire(gb.count) - gb.target) < 0) {
+            if (((++spins) & 255u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) {
+                atomicOr(status, SPEC_DEV_TIMEOUT);
+                ok = false;
+                break;
             }
         }
         s_ok = ok ? 1 : 0;
     }
     __syncthreads();
     return s_ok != 0;
+}
+__device__ __forceinline__ void grid_barrier_exit(const GridBarrier& gb, unsigned nblocks) {
+    if (threadIdx.x == 0 && atom_add_acq_rel(gb.exits, 1u) == nblocks - 1u) {
+        atomicExch(gb.count, 0u);
+        atomicExch(gb.exits, 0u);
+    }
 }
 
 // Barrier over `nblocks` CTAs that are all resident (cooperative launch).  slot[0] is
@@ -349,6 +376,9 @@ __device__ __forceinline__ void fence_mbar_init() {
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+__device__ __forceinline__ void mbar_arrive1(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_u32(bar)) : "memory");
+}
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, unsigned bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
@@ -390,7 +420,7 @@ struct WsHeader {
     unsigned status;             // SPEC_DEV_* flags, sticky
     unsigned pad0[31];
     unsigned done[32];           // last-CTA counters of single-kernel phases
-    unsigned barrier[64][64];    // barrier slots: [i][0] count, [i][32] generation
+    unsigned barrier[64][64];    // barrier slots: [i][0] count, [i][32] generation or exit count
 };
 static_assert(sizeof(WsHeader) <= 32768, "workspace header exceeds 32 KiB");
 constexpr size_t kWsHeaderBytes = 32768;

@@ -124,29 +124,44 @@ __device__ __forceinline__ long thread_base(int c) {
 // ----------------------------------------------------------------------------------
 // T = 0
 // ----------------------------------------------------------------------------------
+// T=0 runs 256-thread CTAs on 8192-entry items, as many CTAs as fit.
+constexpr int kT0Threads = 256;
+constexpr int kT0Warps = kT0Threads / 32;
+constexpr int kT0Chunk = kT0Threads * kEPT;
+
+__device__ __forceinline__ long t0_base(int c) { return (long)c * kT0Chunk + (long)threadIdx.x * kEPT; }
+
 template <typename TT>
-__global__ void __launch_bounds__(kThreads) verify_t0_kernel(VerifyParams p) {
+__global__ void __launch_bounds__(kT0Threads) verify_t0_kernel(VerifyParams p) {
     const TT* target = static_cast<const TT*>(p.target);
     const long V = p.V;
-    const long items = (long)p.B * (p.gamma + 1) * p.nchunk;
+    const unsigned nch = (unsigned)((V + kT0Chunk - 1) / kT0Chunk);
+    const long items = (long)p.B * (p.gamma + 1) * nch;
     const bool vec = p.vec_t != 0;
     constexpr int NW = Words<TT>::N;
     uint4 cur[NW], nxt[NW];
-    __shared__ unsigned long long s_key[2][kWarps];
+    __shared__ unsigned long long s_key[2][kT0Warps];
     int par = 0;
 
     long it = blockIdx.x;
+    auto split = [&](long i, int& row, int& c) {   // 32-bit division where the index fits
+        if (i <= 0xffffffffL) { row = (int)((unsigned)i / nch); c = (int)((unsigned)i - (unsigned)row * nch); }
+        else { row = (int)(i / nch); c = (int)(i - (long)row * nch); }
+    };
     if (it < items) {
-        const int row = (int)(it / p.nchunk), c = (int)(it - (long)row * p.nchunk);
-        load_words<TT, NW>(cur, target + (size_t)row * V, V, thread_base(c), vec);
+        int row, c;
+        split(it, row, c);
+        load_words<TT, NW>(cur, target + (size_t)row * V, V, t0_base(c), vec);
     }
     for (; it < items; it += gridDim.x) {
         const long nx = it + gridDim.x;
         if (nx < items) {
-            const int row = (int)(nx / p.nchunk), c = (int)(nx - (long)row * p.nchunk);
-            load_words<TT, NW>(nxt, target + (size_t)row * V, V, thread_base(c), vec);
+            int rn, cn;
+            split(nx, rn, cn);
+            load_words<TT, NW>(nxt, target + (size_t)rn * V, V, t0_base(cn), vec);
         }
-        const int row = (int)(it / p.nchunk), c = (int)(it - (long)row * p.nchunk);
+        int row, c;
+        split(it, row, c);
         // NaN-propagating max of the 32 entries (-inf pads the row end), then the
         // warp max; only lanes holding it look for their lowest index
         float m = chunk_max_nan<TT, NW>(cur);
@@ -156,7 +171,7 @@ __global__ void __launch_bounds__(kThreads) verify_t0_kernel(VerifyParams p) {
         if (!bad) {
             float x[kEPT];
             decode_words<TT, NW>(cur, x);
-            const long base = thread_base(c);
+            const long base = t0_base(c);
 #pragma unroll
             for (int e = kEPT - 1; e >= 0; --e)
                 if (x[e] == m) idx = (int)(base + e);
@@ -171,7 +186,7 @@ __global__ void __launch_bounds__(kThreads) verify_t0_kernel(VerifyParams p) {
         if (threadIdx.x == 0) {
             unsigned long long k = 0ull;
             int anybad = 0;
-            for (int w = 0; w < kWarps; ++w) {
+            for (int w = 0; w < kT0Warps; ++w) {
                 const unsigned long long kw = s_key[par][w];
                 if (kw == ~0ull) anybad = 1;
                 else k = kw > k ? kw : k;
@@ -190,7 +205,7 @@ __global__ void __launch_bounds__(kThreads) verify_t0_kernel(VerifyParams p) {
     // prefix scan: one warp per request, one lane per row
     const int G = p.gamma;
     const int lane = threadIdx.x & 31;
-    for (int b = threadIdx.x >> 5; b < p.B; b += kWarps) {
+    for (int b = threadIdx.x >> 5; b < p.B; b += kT0Warps) {
         unsigned long long k3[3] = {0ull, 0ull, 0ull};
         int tok3[3] = {0, 0, 0};
         unsigned bad_row = 0, bad_tok = 0, mism[3] = {0u, 0u, 0u};
@@ -250,12 +265,19 @@ __global__ void __launch_bounds__(kThreads) verify_t0_kernel(VerifyParams p) {
 // ----------------------------------------------------------------------------------
 struct Item1 { int b, lr, c; };   // local rows 0..G target, G+1..2G draft
 __device__ __forceinline__ Item1 item1(const VerifyParams& p, long it) {
-    const long per_req = (long)(2 * p.gamma + 1) * p.nchunk;
+    const unsigned per_req = (unsigned)(2 * p.gamma + 1) * (unsigned)p.nchunk;   // < 2^21
     Item1 r;
-    r.b = (int)(it / per_req);
-    const long rem = it - (long)r.b * per_req;
-    r.lr = (int)(rem / p.nchunk);
-    r.c = (int)(rem - (long)r.lr * p.nchunk);
+    unsigned rem;
+    if (it <= 0xffffffffL) {   // 32-bit division where the index fits
+        const unsigned u = (unsigned)it;
+        r.b = (int)(u / per_req);
+        rem = u - (unsigned)r.b * per_req;
+    } else {
+        r.b = (int)(it / (long)per_req);
+        rem = (unsigned)(it - (long)r.b * per_req);
+    }
+    r.lr = (int)(rem / (unsigned)p.nchunk);
+    r.c = (int)(rem - (unsigned)r.lr * (unsigned)p.nchunk);
     return r;
 }
 
@@ -307,6 +329,99 @@ __device__ __forceinline__ void phase_stats(const VerifyParams& p) {
     }
 }
 
+// Phase 1 with the rows staged by bulk copies (rows 16-byte aligned): each CTA keeps
+// S chunk copies in flight in a shared-memory ring, one mbarrier per stage; the 8
+// warps reduce their 1024-entry segments of a stage into the same per-(row, chunk,
+// warp) partials as phase_stats, then thread 0 refills the stage with the CTA's item
+// S further on.  Bytes in flight per SM no longer depend on registers.
+constexpr int kV1StagesBf16 = 6;   // 16 KB stages; with float32 rows, 3 stages of 32 KB
+constexpr unsigned long long kV1WaitNs = kWaitLimitNs;
+// ring layout: full and empty mbarriers, the staged items' (b, row, chunk, entries),
+// then the stages (128-byte aligned)
+constexpr int kV1RingOffset = 256;
+static_assert(2 * 8 * kV1StagesBf16 + 16 * kV1StagesBf16 <= kV1RingOffset, "ring header");
+
+
+template <typename TT, typename DT>
+__device__ __forceinline__ void issue_item1(const VerifyParams& p, long it, uint8_t* dst, uint64_t* bar,
+                                            int4* slot) {
+    const Item1 q = item1(p, it);
+    const int G = p.gamma;
+    const long e0 = (long)q.c * kVerifyChunk;
+    const long n = (long)p.V - e0 < kVerifyChunk ? (long)p.V - e0 : kVerifyChunk;
+    const void* src;
+    unsigned bytes;
+    if (q.lr <= G) {
+        src = static_cast<const TT*>(p.target) + ((size_t)q.b * (G + 1) + q.lr) * p.V + e0;
+        bytes = (unsigned)(n * (long)sizeof(TT));
+    } else {
+        src = static_cast<const DT*>(p.draft) + ((size_t)q.b * G + (q.lr - G - 1)) * p.V + e0;
+        bytes = (unsigned)(n * (long)sizeof(DT));
+    }
+    *slot = make_int4(q.b, q.lr, q.c, (int)n);   // published to the consumers by the barrier phase
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_g2s(dst, src, bytes, bar);
+}
+
+// This warp's 1024-entry segment of a staged chunk as 32 entries per lane (lane-
+// interleaved 16-byte words, so a warp's shared loads hit distinct banks), -inf past
+// the `nvalid` entries the chunk holds.
+template <typename T, int NW>
+__device__ __forceinline__ void stage_words(const uint8_t* stage, int warp, int lane, int nvalid, uint4 (&w)[NW]) {
+    constexpr int EPV = 16 / (int)sizeof(T);
+    constexpr int WPS = 1024 / EPV;   // 16-byte words per warp segment
+    const uint4* seg = reinterpret_cast<const uint4*>(stage) + (size_t)warp * WPS;
+    const uint32_t ninf = sizeof(T) == 2 ? 0xff80ff80u : 0xff800000u;
+#pragma unroll
+    for (int j = 0; j < Words<T>::N; ++j) {
+        const int u = j * 32 + lane;
+        w[j] = (warp * 1024 + u * EPV + EPV <= nvalid) ? seg[u] : make_uint4(ninf, ninf, ninf, ninf);
+    }
+}
+
+template <typename TT, typename DT>
+__device__ __forceinline__ void phase_stats_staged(const VerifyParams& p, uint8_t* ring, uint64_t* full,
+                                                   uint64_t* empty, int4* s_item, int S, size_t stage_bytes) {
+    const long items = (long)(2 * p.gamma + 1) * p.nchunk * p.B;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long mine = items > (long)blockIdx.x ? (items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    if (threadIdx.x == 0)
+        for (long k = 0; k < S && k < mine; ++k)
+            issue_item1<TT, DT>(p, blockIdx.x + k * gridDim.x, ring + (size_t)k * stage_bytes, &full[k], &s_item[k]);
+    for (long k = 0; k < mine; ++k) {
+        const int s = (int)(k % S);
+        if (threadIdx.x == 0 && k >= 1 && k - 1 + S < mine) {
+            // refill the stage of item k-1 with item k-1+S once every warp has left it
+            const int sp = (int)((k - 1) % S);
+            mbar_wait(&empty[sp], (unsigned)(((k - 1) / S) & 1), p.status, kV1WaitNs);
+            fence_proxy_async_smem();
+            issue_item1<TT, DT>(p, blockIdx.x + (k - 1 + S) * gridDim.x, ring + (size_t)sp * stage_bytes, &full[sp],
+                                &s_item[sp]);
+        }
+        const uint8_t* stage = ring + (size_t)s * stage_bytes;
+        mbar_wait(&full[s], (unsigned)((k / S) & 1), p.status, kV1WaitNs);
+        const int4 qi = s_item[s];
+        const Item1 q{qi.x, qi.y, qi.z};
+        const int nvalid = qi.w;
+        float2 st;
+        if (q.lr <= p.gamma) {
+            uint4 w[Words<TT>::N];
+            stage_words<TT>(stage, warp, lane, nvalid, w);
+            st = warp_partial<TT, Words<TT>::N>(w);
+        } else {
+            uint4 w[Words<DT>::N];
+            stage_words<DT>(stage, warp, lane, nvalid, w);
+            st = warp_partial<DT, Words<DT>::N>(w);
+        }
+        __syncwarp();
+        if (lane == 0) {
+            const size_t rowid = (size_t)q.b * (2 * p.gamma + 1) + q.lr;
+            p.stats[(rowid * p.nchunk + q.c) * kWarps + warp] = st;
+            mbar_arrive1(&empty[s]);   // this warp is done with stage s
+        }
+    }
+}
+
 template <typename TT, typename DT>
 __device__ __noinline__ void accept_phase(const VerifyParams& p, int b) {
     const TT* target = static_cast<const TT*>(p.target);
@@ -326,7 +441,19 @@ __device__ __noinline__ void accept_phase(const VerifyParams& p, int b) {
         const size_t rowid = (size_t)b * nr + lr;
         Stat2 acc = stat2_empty();
         int bad = 0;
-        for (int i = lane; i < np; i += 32) {
+        // the lane's first 8 partials are requested together, then merged in order
+        float2 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = lane + 32 * u;
+            v[u] = i < np ? __ldcg(&p.stats[rowid * np + i]) : make_float2(-INFINITY, 0.0f);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            if (isnan(v[u].x)) bad = 1;
+            else acc = stat2_merge(acc, Stat2{v[u].x, v[u].y});
+        }
+        for (int i = lane + 256; i < np; i += 32) {
             const float2 st = __ldcg(&p.stats[rowid * np + i]);
             if (isnan(st.x)) bad = 1;
             else acc = stat2_merge(acc, Stat2{st.x, st.y});
@@ -477,23 +604,25 @@ __device__ __forceinline__ void phase_weights(const VerifyParams& p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint4 ct[NW], cd[NW], nt[NW], nd[NW];
     DrawRow dc{MODE_DONE, 0, 0, 0.f, 0.f, 0.f, 0.f}, dn = dc;
-    long it = blockIdx.x;
-    if (it < items) {
-        const int b = (int)(it / p.nchunk);
+    // items = B * nchunk < 2^31 (B <= 65535, nchunk <= 8192): 32-bit index math
+    const unsigned nch = (unsigned)p.nchunk;
+    unsigned it = blockIdx.x;
+    if ((long)it < items) {
+        const int b = (int)(it / nch);
         dc = draw_row(p, b);
-        if (dc.mode != MODE_DONE) load_draw<TT, DT, NW>(p, b, thread_base((int)(it - (long)b * p.nchunk)), dc, ct, cd);
+        if (dc.mode != MODE_DONE) load_draw<TT, DT, NW>(p, b, thread_base((int)(it - (unsigned)b * nch)), dc, ct, cd);
     }
-    for (; it < items; it += gridDim.x) {
-        const long nx = it + gridDim.x;
-        if (nx < items) {
-            const int bn = (int)(nx / p.nchunk);
+    for (; (long)it < items; it += gridDim.x) {
+        const unsigned nx = it + gridDim.x;
+        if ((long)nx < items) {
+            const int bn = (int)(nx / nch);
             dn = draw_row(p, bn);
             if (dn.mode != MODE_DONE)
-                load_draw<TT, DT, NW>(p, bn, thread_base((int)(nx - (long)bn * p.nchunk)), dn, nt, nd);
+                load_draw<TT, DT, NW>(p, bn, thread_base((int)(nx - (unsigned)bn * nch)), dn, nt, nd);
         }
         if (dc.mode != MODE_DONE) {
-            const int b = (int)(it / p.nchunk);
-            const int c = (int)(it - (long)b * p.nchunk);
+            const int b = (int)(it / nch);
+            const int c = (int)(it - (unsigned)b * nch);
             float sr, sp;
             weight_sums<TT, DT, NW>(dc, ct, cd, sr, sp);
             const float ir = warp_inclusive_scan(sr), ip = warp_inclusive_scan(sp);
@@ -518,8 +647,17 @@ __device__ __noinline__ void draw_token(const VerifyParams& p, int b) {
     // totals and the segment holding the threshold (contiguous lane ranges)
     const int K = (nseg + 31) / 32;
     const int s0 = lane * K, s1 = min(nseg, s0 + K);
+    // the lane's segment sums, requested together and kept for the search below
+    // (up to 8 in registers: V <= 8192 * 32; longer ranges reload the rest)
+    constexpr int KR = 8;
+    float2 kv[KR];
+#pragma unroll
+    for (int u = 0; u < KR; ++u) kv[u] = (s0 + u < s1) ? __ldcg(&ks[s0 + u]) : make_float2(0.0f, 0.0f);
+    auto ksum = [&](int i) -> float2 { return i - s0 < KR ? kv[i - s0] : __ldcg(&ks[i]); };
     float sr = 0.0f, sp = 0.0f;
-    for (int i = s0; i < s1; ++i) { const float2 v = __ldcg(&ks[i]); sr += v.x; sp += v.y; }
+#pragma unroll
+    for (int u = 0; u < KR; ++u) { sr += kv[u].x; sp += kv[u].y; }
+    for (int i = s0 + KR; i < s1; ++i) { const float2 v = __ldcg(&ks[i]); sr += v.x; sp += v.y; }
     const float ir = warp_inclusive_scan(sr), ip = warp_inclusive_scan(sp);
     const float Wr = __shfl_sync(0xffffffffu, ir, 31), Wp = __shfl_sync(0xffffffffu, ip, 31);
     const bool ur = (d.mode == MODE_RESID) && (Wr > 0.0f);
@@ -536,7 +674,7 @@ __device__ __noinline__ void draw_token(const VerifyParams& p, int b) {
         if (lane == L) {
             float run = incl - mine;
             for (int i = s0; i < s1; ++i) {
-                const float2 v = __ldcg(&ks[i]);
+                const float2 v = ksum(i);
                 const float w = ur ? v.x : v.y;
                 if (run + w > t) { seg = i; tl = t - run; break; }
                 run += w;
@@ -548,7 +686,7 @@ __device__ __noinline__ void draw_token(const VerifyParams& p, int b) {
     } else {   // u * W rounded up to W: the last segment with positive weight
         int last = -1;
         for (int i = s0; i < s1; ++i) {
-            const float2 v = __ldcg(&ks[i]);
+            const float2 v = ksum(i);
             if ((ur ? v.x : v.y) > 0.0f) last = i;
         }
         const unsigned has = __ballot_sync(0xffffffffu, last >= 0);
@@ -605,7 +743,24 @@ __device__ __noinline__ void draw_token(const VerifyParams& p, int b) {
 template <typename TT, typename DT>
 __global__ void __launch_bounds__(kThreads, 2) verify_t1_kernel(VerifyParams p) {
     const unsigned nb = gridDim.x;
-    phase_stats<TT, DT>(p);
+    if (p.vec_t && p.vec_d) {
+        extern __shared__ __align__(128) uint8_t v1_smem[];
+        constexpr bool wide = sizeof(TT) == 4 || sizeof(DT) == 4;
+        constexpr int S = wide ? kV1StagesBf16 / 2 : kV1StagesBf16;
+        constexpr size_t stage_bytes = (size_t)kVerifyChunk * (wide ? 4 : 2);
+        uint64_t* full = reinterpret_cast<uint64_t*>(v1_smem);
+        uint64_t* empty = full + kV1StagesBf16;
+        int4* s_item = reinterpret_cast<int4*>(v1_smem + 2 * 8 * kV1StagesBf16);
+        uint8_t* ring = v1_smem + kV1RingOffset;
+        if (threadIdx.x == 0) {
+            for (int i = 0; i < S; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], kWarps); }
+            fence_mbar_init();
+        }
+        __syncthreads();
+        phase_stats_staged<TT, DT>(p, ring, full, empty, s_item, S, stage_bytes);
+    } else {
+        phase_stats<TT, DT>(p);
+    }
     if (!block_barrier(p.barrier, nb, p.status)) return;
     for (int b = blockIdx.x; b < p.B; b += gridDim.x) accept_phase<TT, DT>(p, b);
     if (!block_barrier(p.barrier, nb, p.status)) return;
@@ -652,20 +807,15 @@ void verify_bind_workspace(VerifyParams& p, void* ws) {
     p.ksums = reinterpret_cast<float2*>(w + off);
 }
 
-// Persistent grid: enough CTAs to keep every SM streaming, never more than the items.
-template <typename K>
-static int grid_for(K kern, long items) {
-    int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, 0) != cudaSuccess || occ < 1) occ = 1;
-    const long cap = (long)device_sm_count() * occ;
-    return (int)(items < cap ? (items > 0 ? items : 1) : cap);
-}
-
 template <typename TT, typename DT>
 static cudaError_t launch_t1(const VerifyParams& p, cudaStream_t stream) {
     auto kern = verify_t1_kernel<TT, DT>;
+    // the bulk-copy ring of phase 1 (rows 16-byte aligned): 96 KB per CTA, two per SM
+    const size_t smem = (p.vec_t && p.vec_d) ? kV1RingOffset + (size_t)kV1StagesBf16 * kVerifyChunk * 2 : 0;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
     int occ = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, 0);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, smem);
     if (e != cudaSuccess) return e;
     if (occ < 1) return cudaErrorInvalidConfiguration;
     const long items = (long)p.B * (2 * p.gamma + 1) * p.nchunk;
@@ -673,18 +823,21 @@ static cudaError_t launch_t1(const VerifyParams& p, cudaStream_t stream) {
     if (grid > items) grid = items;
     VerifyParams args = p;
     void* kargs[] = {&args};
-    return cudaLaunchCooperativeKernel((const void*)kern, dim3((unsigned)grid), dim3(kThreads), kargs, 0, stream);
+    return cudaLaunchCooperativeKernel((const void*)kern, dim3((unsigned)grid), dim3(kThreads), kargs, smem, stream);
 }
 
 cudaError_t verify_launch(const VerifyParams& p, cudaStream_t stream) {
     if (p.temperature == 0) {
-        const long items = (long)p.B * (p.gamma + 1) * p.nchunk;
+        const long items = (long)p.B * (p.gamma + 1) * (((long)p.V + kT0Chunk - 1) / kT0Chunk);
         // launched as a programmatic dependent: its target-row pass may overlap the
         // kernel before it (the draft), the final scan waits for that kernel first
         void (*k)(VerifyParams) = p.tdt == SPEC_BF16 ? verify_t0_kernel<bf16_t> : verify_t0_kernel<float>;
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(grid_for(k, items));
-        cfg.blockDim = dim3(kThreads);
+        int occ = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, kT0Threads, 0) != cudaSuccess || occ < 1) occ = 1;
+        const long cap = (long)device_sm_count() * occ;
+        cfg.gridDim = dim3((unsigned)(items < cap ? (items > 0 ? items : 1) : cap));
+        cfg.blockDim = dim3(kT0Threads);
         cfg.dynamicSmemBytes = 0;
         cfg.stream = stream;
         cudaLaunchAttribute attr[1];

@@ -1,0 +1,58 @@
+"""Launch one operation a few times on a synthetic workload, for profiler captures.
+
+    python -m verify_spec_draft_gb300.profile_cases {draft,verify_t0,verify_t1,e2etv} [--launches N]
+
+Nothing is timed here; the point is a short process with a handful of launches of one
+kernel, on inputs larger than L2 (129 MB) but only a few hundred MB on the device:
+
+  draft      spec_draft_block, B=1, gamma=15, V=248320, r=256, T=0 (151 MB: logits, U, Wt)
+  verify_t0  spec_verify T=0 on the 16 target rows of the same workload (8 MB; below L2)
+  verify_t1  spec_verify T=1, B=32, gamma=7, V=248320 (238 MB of target and draft rows)
+  e2etv      spec_e2etv on 64 branches x Wb=7 = 448 rows, V=248320 (445 MB in, 222 MB out):
+             a 64-anchor slice of the 16 x 64 x 7 layout
+"""
+
+import argparse
+
+import torch
+
+from . import draft_block, e2etv, load, synth, verify
+
+CASES = ("draft", "verify_t0", "verify_t1", "e2etv")
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("case", choices=CASES)
+    ap.add_argument("--launches", type=int, default=3)
+    args = ap.parse_args(argv)
+    load()
+    dev = torch.device("cuda")
+    if args.case in ("draft", "verify_t0"):
+        inp = synth.config_inputs(3, device=dev)
+        out = draft_block(inp["draft"], inp["anchor"], inp["U"], inp["Wt"], 0)
+        if args.case == "draft":
+            run = lambda: draft_block(inp["draft"], inp["anchor"], inp["U"], inp["Wt"], 0, ws=out["ws"], out=out)
+        else:
+            ref = verify(inp["target"], None, out["tokens"], 0)
+            run = lambda: verify(inp["target"], None, out["tokens"], 0, ws=ref["ws"], out=ref)
+    elif args.case == "verify_t1":
+        inp = synth.config_inputs(4, device=dev)
+        tok = synth.draft_tokens(inp["draft"], 1, seed=inp["cfg"].seed)
+        ref = verify(inp["target"], inp["draft"], tok, 1, inp["seeds"])
+        run = lambda: verify(inp["target"], inp["draft"], tok, 1, inp["seeds"], ws=ref["ws"], out=ref)
+    else:
+        c = synth.CONFIGS[5]
+        n_branches = 64
+        t, d = synth.e2etv_rows(n_branches, c.gamma, c.V, c.draft_sigma, c.dtype, c.seed, dev)
+        ref = e2etv(t, d, n_branches, c.gamma)
+        run = lambda: e2etv(t, d, n_branches, c.gamma, ws=ref["ws"], out=ref)
+    torch.cuda.synchronize()
+    for _ in range(args.launches):
+        run()
+    torch.cuda.synchronize()
+    print(f"{args.case}: {args.launches} launches done")
+
+
+if __name__ == "__main__":
+    main()
