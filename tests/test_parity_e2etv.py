@@ -43,7 +43,7 @@ def _check_rows(out, t, d, N, Wb, rows_of_branches, total_branches):
             assert _grad_relerr(g[i], ref["grad"][i]) <= 1e-3, (n, i)
 
 
-@pytest.mark.parametrize("N,Wb,V", [(3, 4, 1000), (2, 7, 999), (5, 1, 64), (1, 64, 300), (4, 7, 33000)])
+@pytest.mark.parametrize("N,Wb,V", [(3, 4, 1000), (2, 7, 999), (5, 1, 64), (1, 64, 300), (4, 7, 33000), (9, 3, 20000)])
 def test_small(spec, N, Wb, V):
     t, d = synth.e2etv_rows(N, Wb, V, 1.0, seed=N * 100 + V)
     out = vsd.e2etv(t.cuda(), d.cuda(), N, Wb)

@@ -144,6 +144,96 @@ __device__ __forceinline__ void sweep_overlap(const bf16_t* tr, const bf16_t* dr
     s = warp_sum(ss);
 }
 
+// Batched variants of the two reductions for staged slices: each lane keeps B of its
+// 16-byte words in flight at once (instead of one load, then its arithmetic, then the
+// next load), and sums go to independent accumulators.  Same results up to the order
+// of float additions.
+template <int B>
+__device__ __forceinline__ void slice_stats(const bf16_t* row, int ncol, Stat2& out, int& bad) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t ninf = 0xff80ff80u;
+    uint32_t mx2 = ninf;
+    for (int k0 = lane * 8; k0 < ncol; k0 += 256 * B) {
+        uint4 w[B];
+#pragma unroll
+        for (int g = 0; g < B; ++g) {
+            const int k = k0 + 256 * g;
+            w[g] = k < ncol ? ld16<true>(row + k) : make_uint4(ninf, ninf, ninf, ninf);
+        }
+#pragma unroll
+        for (int g = 0; g < B; ++g) mx2 = bmax2(mx2, bmax2(bmax2(w[g].x, w[g].y), bmax2(w[g].z, w[g].w)));
+    }
+    float m = fmaxf(lo_bf(mx2), hi_bf(mx2));
+    if (isnan(lo_bf(mx2)) || isnan(hi_bf(mx2))) m = NAN;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float y = __shfl_xor_sync(0xffffffffu, m, o);
+        m = (isnan(m) || isnan(y)) ? NAN : fmaxf(m, y);
+    }
+    bad = (isnan(m) || m == INFINITY) ? 1 : 0;
+    float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+    const float m2 = m * kLog2e;
+    if (!bad && m != -INFINITY) {
+        for (int k0 = lane * 8; k0 < ncol; k0 += 256 * B) {
+            uint4 w[B];
+#pragma unroll
+            for (int g = 0; g < B; ++g) {
+                const int k = k0 + 256 * g;
+                w[g] = k < ncol ? ld16<true>(row + k) : make_uint4(ninf, ninf, ninf, ninf);
+            }
+#pragma unroll
+            for (int g = 0; g < B; ++g) {   // -inf padding contributes 2^-inf = 0
+                s0 += ex2(fmaf(lo_bf(w[g].x), kLog2e, -m2)) + ex2(fmaf(hi_bf(w[g].x), kLog2e, -m2));
+                s1 += ex2(fmaf(lo_bf(w[g].y), kLog2e, -m2)) + ex2(fmaf(hi_bf(w[g].y), kLog2e, -m2));
+                s2 += ex2(fmaf(lo_bf(w[g].z), kLog2e, -m2)) + ex2(fmaf(hi_bf(w[g].z), kLog2e, -m2));
+                s3 += ex2(fmaf(lo_bf(w[g].w), kLog2e, -m2)) + ex2(fmaf(hi_bf(w[g].w), kLog2e, -m2));
+            }
+        }
+    }
+    out = Stat2{(bad || m == -INFINITY) ? -INFINITY : m2, warp_sum((s0 + s1) + (s2 + s3))};
+}
+
+template <int B>
+__device__ __forceinline__ void slice_overlap(const bf16_t* tr, const bf16_t* dr, int ncol, float lse_p, float lse_q,
+                                              uint8_t* mask, float& a, float& s) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t ninf = 0xff80ff80u;
+    float sa0 = 0.0f, sa1 = 0.0f, ss0 = 0.0f, ss1 = 0.0f;
+    for (int k0 = lane * 8; k0 < ncol; k0 += 256 * B) {
+        uint4 wl[B], wd[B];
+#pragma unroll
+        for (int g = 0; g < B; ++g) {
+            const int k = k0 + 256 * g;
+            const bool in = k < ncol;
+            wl[g] = in ? ld16<true>(tr + k) : make_uint4(ninf, ninf, ninf, ninf);
+            wd[g] = in ? ld16<true>(dr + k) : make_uint4(ninf, ninf, ninf, ninf);
+        }
+#pragma unroll
+        for (int g = 0; g < B; ++g) {
+            const uint32_t l4[4] = {wl[g].x, wl[g].y, wl[g].z, wl[g].w};
+            const uint32_t d4[4] = {wd[g].x, wd[g].y, wd[g].z, wd[g].w};
+            uint32_t bits = 0;
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const float lp0 = fmaf(lo_bf(l4[h]), kLog2e, -lse_p), lq0 = fmaf(lo_bf(d4[h]), kLog2e, -lse_q);
+                const float lp1 = fmaf(hi_bf(l4[h]), kLog2e, -lse_p), lq1 = fmaf(hi_bf(d4[h]), kLog2e, -lse_q);
+                const float m0 = ex2(fminf(lp0, lq0)), m1 = ex2(fminf(lp1, lq1));
+                const bool b0 = lq0 < lp0, b1 = lq1 < lp1;
+                sa0 += m0;
+                sa1 += m1;
+                ss0 += b0 ? m0 : 0.0f;
+                ss1 += b1 ? m1 : 0.0f;
+                bits |= (b0 ? 1u : 0u) << (2 * h);
+                bits |= (b1 ? 2u : 0u) << (2 * h);
+            }
+            const int k = k0 + 256 * g;
+            if (k < ncol) mask[k >> 3] = (uint8_t)bits;
+        }
+    }
+    a = warp_sum(sa0 + sa1);
+    s = warp_sum(ss0 + ss1);
+}
+
 template <bool STAGED, bool VEC>
 __global__ void __launch_bounds__(kThreads) e2etv_kernel(E2etvParams p) {
     extern __shared__ __align__(128) uint8_t s_dyn[];
@@ -216,7 +306,8 @@ __global__ void __launch_bounds__(kThreads) e2etv_kernel(E2etvParams p) {
         for (int i = warp; i < nr; i += kWarps) {
             Stat2 st;
             int bad = 0;
-            sweep_stats<STAGED, VEC>((i < Wb ? rw.tgt : rw.drf) + (size_t)(i % Wb) * rw.stride, ncol, st, bad);
+            if (STAGED) slice_stats<8>((i < Wb ? rw.tgt : rw.drf) + (size_t)(i % Wb) * rw.stride, ncol, st, bad);
+            else sweep_stats<STAGED, VEC>((i < Wb ? rw.tgt : rw.drf) + (size_t)(i % Wb) * rw.stride, ncol, st, bad);
             if (lane == 0) {
                 part[(size_t)gi * nr + i] = make_float2(st.m2, st.s);
                 if (bad) atomicOr(&p.branch_bad[n], 1u);
@@ -244,8 +335,12 @@ __global__ void __launch_bounds__(kThreads) e2etv_kernel(E2etvParams p) {
         if (!bad_branch) {
             for (int i = warp; i < Wb; i += kWarps) {
                 float a, s;
-                sweep_overlap<STAGED, VEC>(rw.tgt + (size_t)i * rw.stride, rw.drf + (size_t)i * rw.stride, ncol,
-                                           s_lse[i], s_lse[Wb + i], s_mask + (size_t)i * ngroups8, a, s);
+                if (STAGED)
+                    slice_overlap<4>(rw.tgt + (size_t)i * rw.stride, rw.drf + (size_t)i * rw.stride, ncol, s_lse[i],
+                                     s_lse[Wb + i], s_mask + (size_t)i * ngroups8, a, s);
+                else
+                    sweep_overlap<STAGED, VEC>(rw.tgt + (size_t)i * rw.stride, rw.drf + (size_t)i * rw.stride, ncol,
+                                               s_lse[i], s_lse[Wb + i], s_mask + (size_t)i * ngroups8, a, s);
                 if (lane == 0) part2[(size_t)gi * Wb + i] = make_float2(a, s);
             }
         }
