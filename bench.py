@@ -4,7 +4,9 @@
 Headline workload (one step = the whole path of a decode step at B=1):
     spec_draft_block (gamma=15, V=248320, rank-256 Markov bias, T=0)
   + spec_verify      (16 target rows, T=0)
-on seeded synthetic logits (see verify_spec_draft_gb300/synth.py, configuration 3).
+timed as the two calls in one CUDA graph (the headline), and also as
+spec_draft_verify, the one-call form of the two (same outputs, one launch); on seeded
+synthetic logits (verify_spec_draft_gb300/synth.py, configuration 3).
 Metric: verify rows per second over the whole draft+verify step, with the step's
 microseconds alongside, and the dominant kernel's fraction of the HBM roofline.
 
@@ -177,6 +179,7 @@ def run_ours(args, rank, world, torch, dist):
     L, tgt, U, Wt, anchor = inp["draft"], inp["target"], inp["U"], inp["Wt"], inp["anchor"]
     ws_d = vsd.workspace(vsd.OP_DRAFT, B, G, V, r, dev)
     ws_v = vsd.workspace(vsd.OP_VERIFY, B, G, V, 0, dev)
+    ws_f = vsd.workspace(vsd.OP_DRAFT_VERIFY, B, G, V, r, dev)
     out_d = dict(tokens=torch.empty((B, G), dtype=torch.int32, device=dev),
                  conf=torch.empty((B, G), dtype=torch.float32, device=dev),
                  qtok=torch.empty((B, G), dtype=torch.float32, device=dev),
@@ -185,6 +188,13 @@ def run_ours(args, rank, world, torch, dist):
                  committed=torch.empty((B, G + 1), dtype=torch.int32, device=dev),
                  bonus=torch.empty((B,), dtype=torch.int32, device=dev),
                  near=torch.empty((B,), dtype=torch.int32, device=dev))
+
+    out_f = dict(out_d)
+    out_f.update({k: torch.empty_like(v) for k, v in out_d.items()})
+    out_f.update({k: torch.empty_like(v) for k, v in out_v.items() if k != "near"})
+
+    def do_fused():
+        vsd.draft_verify(L, tgt, anchor, U, Wt, ws=ws_f, out=out_f)
 
     def do_draft():
         vsd.draft_block(L, anchor, U, Wt, 0, None, ws=ws_d, out=out_d)
@@ -201,8 +211,9 @@ def run_ours(args, rank, world, torch, dist):
         do_draft()
         do_verify()
 
-    # one graph per step (the verify launch may overlap the draft kernel inside it),
-    # plus each call on its own for the per-kernel numbers
+    # the headline step: the two calls in one graph (the verify launch may overlap the
+    # draft kernel inside it); then the one-call form and each call alone
+    g_fused, graphed_f = capture(do_fused, torch)
     g_step, graphed_s = capture(do_step, torch)
     g_draft, graphed_d = capture(do_draft, torch)
     g_verify, graphed_v = capture(do_verify, torch)
@@ -222,25 +233,27 @@ def run_ours(args, rank, world, torch, dist):
     if world > 1:
         dist.barrier()
     n_part = max(20, min(args.steps, 200))
+    t_one, _ = time_steps(torch, g_fused, n_part, flush=flush)
     t_draft, _ = time_steps(torch, g_draft, n_part, flush=flush)
     t_verify, _ = time_steps(torch, g_verify, n_part, flush=flush)
     ms_step = sum(total) / len(total)
+    ms_one = sum(t_one) / len(t_one)
     ms_draft = sum(t_draft) / len(t_draft)
     ms_verify = sum(t_verify) / len(t_verify)
     if world > 1:
-        t = torch.tensor([ms_step, ms_draft, ms_verify], dtype=torch.float64, device=dev)
+        t = torch.tensor([ms_step, ms_one, ms_draft, ms_verify], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step, ms_draft, ms_verify = t.tolist()
-    passes = int(out_d["passes"].item())
+        ms_step, ms_one, ms_draft, ms_verify = t.tolist()
+    passes = int(out_f["passes"].item())
     rows = B * (G + 1)
-    # algorithmic bytes of one draft launch: the draft rows and Wt read once (plus the
-    # U rows of the gamma previous tokens); verify: the 16 target rows read once
+    # algorithmic bytes of one draft launch (the dominant kernel): the draft rows and Wt
+    # read once, plus the U rows of the gamma previous tokens; verify: the 16 target rows
     draft_bytes = B * G * V * 2 + V * r * 2 + B * G * r * 2
     verify_bytes = B * (G + 1) * V * 2
-    dominant = "draft" if ms_draft >= ms_verify else "verify"
-    dom_bytes, dom_ms = (draft_bytes, ms_draft) if dominant == "draft" else (verify_bytes, ms_verify)
+    dom_bytes, dom_ms = draft_bytes, ms_draft
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
-    n_acc = out_v["n"].cpu().tolist()
+    n_acc = out_f["n"].cpu().tolist()
+    assert torch.equal(out_f["tokens"], out_d["tokens"]) and torch.equal(out_f["n"], out_v["n"])
 
     result = {
         "metric": METRIC,
@@ -251,9 +264,11 @@ def run_ours(args, rank, world, torch, dist):
         "warmup": args.warmup,
         "ms_per_step": ms_step,
         "draft_verify_us": ms_step * 1e3,
+        "one_call_step_us": ms_one * 1e3,
         "draft_us": ms_draft * 1e3,
         "verify_us": ms_verify * 1e3,
-        "note_parts": "draft_us and verify_us time each call alone; their sum exceeds the step when they overlap",
+        "note_parts": "draft_verify_us: spec_draft_block + spec_verify in one graph; one_call_step_us: "
+                      "spec_draft_verify (one launch, same outputs); draft_us and verify_us time each call alone",
         "verify_only_rows_per_s": rows / (ms_verify * 1e-3),
         "higher_is_better": True,
         "scaling": "weak",
@@ -265,14 +280,14 @@ def run_ours(args, rank, world, torch, dist):
             "B": B, "gamma": G, "V": V, "r": r, "temperature": 0,
             "fixed_point_passes": passes,
             "accepted_n": n_acc,
-            "cuda_graphs": bool(graphed_s and graphed_d and graphed_v),
+            "cuda_graphs": bool(graphed_f and graphed_s and graphed_d and graphed_v),
             "step": "one CUDA graph: spec_draft_block then spec_verify; verify's target-row pass may overlap the "
                     "draft kernel (programmatic dependent launch) and waits for it before reading the tokens",
             "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write), outside the timed events",
             "parallelism": f"replicas x{world} (independent requests per GPU, no collective)",
         },
         "roofline": {
-            "kernel": "spec::draft_tc_kernel" if dominant == "draft" else "spec::verify_t0_kernel",
+            "kernel": "spec::draft_tc_kernel",
             "bound": "hbm",
             "achieved": achieved,
             "peak": hbm,
@@ -301,9 +316,8 @@ def run_ours(args, rank, world, torch, dist):
             d_L.copy_(h_L, non_blocking=True)
             d_t.copy_(h_t, non_blocking=True)
             d_a.copy_(h_a, non_blocking=True)
-            vsd.draft_block(d_L, d_a, U, Wt, 0, None, ws=ws_d, out=out_d)
-            vsd.verify(d_t, None, out_d["tokens"], 0, None, ws=ws_v, out=out_v)
-            packed = torch.cat([out_v["n"], out_v["committed"].flatten(), out_v["bonus"], out_d["tokens"].flatten()])
+            vsd.draft_verify(d_L, d_t, d_a, U, Wt, ws=ws_f, out=out_f)
+            packed = torch.cat([out_f["n"], out_f["committed"].flatten(), out_f["bonus"], out_f["tokens"].flatten()])
             h_out.copy_(packed, non_blocking=True)
 
         for _ in range(5):
@@ -322,8 +336,8 @@ def run_ours(args, rank, world, torch, dist):
         result["e2e"] = {"value": rows * world / (ms_e2e * 1e-3), "unit": "rows/s", "us_per_step": ms_e2e * 1e3,
                          "h2d_bytes_per_step": h_L.numel() * 2 + h_t.numel() * 2 + h_a.numel() * 4,
                          "d2h_bytes_per_step": h_out.numel() * 4,
-                         "path": "pinned host buffers -> cudaMemcpyAsync -> spec_draft_block -> spec_verify -> "
-                                 "results to pinned host, eager C-ABI calls (Markov weights resident)"}
+                         "path": "pinned host buffers -> cudaMemcpyAsync -> spec_draft_verify -> results to pinned "
+                                 "host, eager C-ABI calls (Markov weights resident)"}
     del flush_buf
 
     # ---- secondary: verify T=1 at B=32 (configuration 4) and E2E-TV (configuration 5)

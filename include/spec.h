@@ -75,7 +75,7 @@ typedef enum {
 
 typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
 
-typedef enum { SPEC_OP_DRAFT = 0, SPEC_OP_VERIFY = 1, SPEC_OP_E2ETV = 2 } spec_op;
+typedef enum { SPEC_OP_DRAFT = 0, SPEC_OP_VERIFY = 1, SPEC_OP_E2ETV = 2, SPEC_OP_DRAFT_VERIFY = 3 } spec_op;
 
 /* Device status flags (OR-ed into the workspace status word). */
 #define SPEC_DEV_TIMEOUT 1u
@@ -89,7 +89,8 @@ typedef enum { SPEC_OP_DRAFT = 0, SPEC_OP_VERIFY = 1, SPEC_OP_E2ETV = 2 } spec_o
 
 /*
  * spec_workspace_bytes - workspace size for one operation (host only, pure).
- *   op     SPEC_OP_DRAFT / SPEC_OP_VERIFY: B requests, gamma positions, V, r.
+ *   op     SPEC_OP_DRAFT / SPEC_OP_VERIFY / SPEC_OP_DRAFT_VERIFY: B requests, gamma
+ *          positions, V, r.
  *          SPEC_OP_E2ETV: B = number of branches, gamma = branch length Wb, r unused.
  * Returns 0 for arguments outside the supported ranges.
  */
@@ -196,6 +197,40 @@ spec_status spec_verify(const void *target_logits, spec_dtype target_dtype,
                         const uint64_t *seeds, int32_t *n_accepted_out, int32_t *committed_out,
                         int32_t *bonus_out, int32_t *near_tie_out, void *workspace,
                         size_t workspace_bytes, spec_stream_t stream);
+
+/*
+ * spec_draft_verify - one greedy (T=0) block step: spec_draft_block followed by
+ * spec_verify of its tokens against the target rows, in one call.
+ *
+ * Defines: the draft-then-verify cycle ("Solar Open2 DSpark", sionic.ai, sections 1
+ * and 6: the drafter proposes a block, one target forward over gamma+1 positions
+ * commits the agreeing prefix and the target's next token), with each half defined
+ * as in spec_draft_block (temperature 0) and spec_verify (temperature 0).  The
+ * outputs equal those of the two calls made in sequence, bit for bit: tokens_out,
+ * conf_out, qtok_out and passes_out as spec_draft_block writes them; n_accepted_out,
+ * committed_out and bonus_out as spec_verify writes them for those tokens.
+ *
+ * It runs the draft kernel and, as its programmatic dependent, the verify kernel:
+ * one workspace and one call for the common greedy step.
+ *
+ *   draft_logits .. V   as spec_draft_block.
+ *   target_logits       [B, gamma+1, V], dtype target_dtype; target row i is the
+ *                       distribution of position i+1.
+ *   tokens_out, conf_out  [B, gamma]; qtok_out [B, gamma] (nullable); passes_out [1]
+ *                       (nullable).
+ *   n_accepted_out [B], committed_out [B, gamma+1], bonus_out [B]  as spec_verify.
+ *   workspace           spec_workspace_bytes(SPEC_OP_DRAFT_VERIFY, B, gamma, V, r).
+ * Limits: those of spec_draft_block.  Device conditions of either half set the same
+ * status flags in this one workspace.
+ */
+spec_status spec_draft_verify(const void *draft_logits, spec_dtype logits_dtype,
+                              const int32_t *anchor, const void *U, const void *Wt,
+                              spec_dtype w_dtype, int r, int B, int gamma, int V,
+                              const void *target_logits, spec_dtype target_dtype,
+                              int32_t *tokens_out, float *conf_out, float *qtok_out,
+                              int32_t *passes_out, int32_t *n_accepted_out,
+                              int32_t *committed_out, int32_t *bonus_out, void *workspace,
+                              size_t workspace_bytes, spec_stream_t stream);
 
 /*
  * spec_verify_noalloc - spec_verify without a caller-supplied workspace.

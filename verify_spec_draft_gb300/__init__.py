@@ -25,7 +25,7 @@ STATUS = {
     8: "SPEC_ERR_TOKEN", 9: "SPEC_ERR_WORKSPACE",
 }
 F32, BF16 = 0, 1
-OP_DRAFT, OP_VERIFY, OP_E2ETV = 0, 1, 2
+OP_DRAFT, OP_VERIFY, OP_E2ETV, OP_DRAFT_VERIFY = 0, 1, 2, 3
 DEV_TIMEOUT, DEV_NONFINITE, DEV_TOKEN = 1, 2, 4
 
 # C signatures of include/spec.h, as ctypes types
@@ -44,6 +44,8 @@ SIGNATURES = {
     "spec_e2etv": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "spec_verify_noalloc": (_i32, [_vp, _i32, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _vp,
                                    _vp, _vp, _vp, _vp, _vp]),
+    "spec_draft_verify": (_i32, [_vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _i32,
+                                 _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
 }
 
 _lib = None
@@ -231,6 +233,47 @@ def verify(target, draft, tokens, temperature=0, seeds=None, ws=None, out=None, 
         B, gamma, V, int(temperature), _ptr(seeds), _ptr(out["n"]), _ptr(out["committed"]), _ptr(out["bonus"]),
         _ptr(out.get("near")), _ptr(ws), ws.numel(), _stream(stream))
     _check(code, "spec_verify")
+    out["ws"] = ws
+    return out
+
+
+def draft_verify(logits, target, anchor, U=None, Wt=None, ws=None, out=None, stream=None):
+    """spec_draft_verify (T=0).  logits [B, gamma, V]; target [B, gamma+1, V]; anchor [B]
+    int32; U, Wt [V, r] or None.  Returns a dict of device tensors: the draft's tokens,
+    conf, qtok, passes and verify's n, committed, bonus."""
+    torch = _torch()
+    lib = load()
+    _need(logits, "logits")
+    dev = logits.device
+    B, gamma, V = logits.shape
+    _need(target, "target", dev, None, (B, gamma + 1, V))
+    _need(anchor, "anchor", dev, torch.int32, (B,))
+    r = 0
+    if U is not None:
+        _need(U, "U", dev)
+        _need(Wt, "Wt", dev, U.dtype, tuple(U.shape))
+        if U.shape[0] != V:
+            raise ValueError("U and Wt must have V rows")
+        r = U.shape[1]
+    wdt = _dtype_code(U) if U is not None else F32
+    if out is None:
+        out = dict(
+            tokens=torch.empty((B, gamma), dtype=torch.int32, device=dev),
+            conf=torch.empty((B, gamma), dtype=torch.float32, device=dev),
+            qtok=torch.empty((B, gamma), dtype=torch.float32, device=dev),
+            passes=torch.zeros((1,), dtype=torch.int32, device=dev),
+            n=torch.empty((B,), dtype=torch.int32, device=dev),
+            committed=torch.empty((B, gamma + 1), dtype=torch.int32, device=dev),
+            bonus=torch.empty((B,), dtype=torch.int32, device=dev),
+        )
+    if ws is None:
+        ws = workspace(OP_DRAFT_VERIFY, B, gamma, V, r, dev, stream)
+    code = lib.spec_draft_verify(
+        _ptr(logits), _dtype_code(logits), _ptr(anchor), _ptr(U), _ptr(Wt), wdt, r, B, gamma, V,
+        _ptr(target), _dtype_code(target), _ptr(out["tokens"]), _ptr(out["conf"]), _ptr(out.get("qtok")),
+        _ptr(out.get("passes")), _ptr(out["n"]), _ptr(out["committed"]), _ptr(out["bonus"]), _ptr(ws),
+        ws.numel(), _stream(stream))
+    _check(code, "spec_draft_verify")
     out["ws"] = ws
     return out
 

@@ -52,6 +52,9 @@ size_t spec_workspace_bytes(spec_op op, int B, int gamma, int V, int r) {
         case SPEC_OP_VERIFY:
             if (B > 65535) return 0;
             return verify_workspace_bytes(B, gamma, V);
+        case SPEC_OP_DRAFT_VERIFY:
+            if (r < 0 || r > SPEC_MAX_RANK || (long)B * gamma > 4096) return 0;
+            return draft_verify_workspace_bytes(B, gamma, V, r);
         case SPEC_OP_E2ETV:
             if ((long)B * gamma > (1L << 24)) return 0;
             return e2etv_workspace_bytes(B, gamma, V);
@@ -179,6 +182,71 @@ spec_status spec_verify(const void* target_logits, spec_dtype target_dtype, cons
     p.near_out = near_tie_out;
     verify_bind_workspace(p, workspace);
     return cuda_status(verify_launch(p, (cudaStream_t)stream));
+}
+
+spec_status spec_draft_verify(const void* draft_logits, spec_dtype logits_dtype, const int32_t* anchor,
+                              const void* U, const void* Wt, spec_dtype w_dtype, int r, int B, int gamma, int V,
+                              const void* target_logits, spec_dtype target_dtype, int32_t* tokens_out,
+                              float* conf_out, float* qtok_out, int32_t* passes_out, int32_t* n_accepted_out,
+                              int32_t* committed_out, int32_t* bonus_out, void* workspace, size_t workspace_bytes,
+                              spec_stream_t stream) {
+    if (!dtype_ok(logits_dtype) || !dtype_ok(target_dtype) || (r > 0 && !dtype_ok(w_dtype))) return SPEC_ERR_DTYPE;
+    if (B < 1 || gamma < 1 || gamma > SPEC_MAX_GAMMA || V < 1 || V > SPEC_MAX_V || r < 0 || r > SPEC_MAX_RANK ||
+        (long)B * gamma > 4096)
+        return SPEC_ERR_SHAPE;
+    if (!draft_logits || !anchor || !tokens_out || !conf_out || !target_logits || !n_accepted_out || !committed_out ||
+        !bonus_out)
+        return SPEC_ERR_INVALID_ARG;
+    if (r > 0 && (!U || !Wt)) return SPEC_ERR_INVALID_ARG;
+    if (!aligned16(draft_logits) || !aligned16(target_logits) || (r > 0 && (!aligned16(U) || !aligned16(Wt))))
+        return SPEC_ERR_ALIGN;
+    const size_t need = draft_verify_workspace_bytes(B, gamma, V, r);
+    if (!workspace || workspace_bytes < need) return SPEC_ERR_WORKSPACE;
+
+    DraftParams p;
+    memset(&p, 0, sizeof(p));
+    p.logits = draft_logits;
+    p.ldt = logits_dtype;
+    p.anchor = anchor;
+    p.U = U;
+    p.Wt = Wt;
+    p.wdt = r > 0 ? w_dtype : logits_dtype;
+    p.r = r;
+    p.B = B;
+    p.gamma = gamma;
+    p.V = V;
+    p.temperature = 0;
+    p.tokens_out = tokens_out;
+    p.conf_out = conf_out;
+    p.qtok_out = qtok_out;
+    p.passes_out = passes_out;
+    p.vec_l = ((size_t)V * dtype_size(logits_dtype)) % 16 == 0;
+    p.vec_w = r > 0 && ((size_t)r * dtype_size(w_dtype)) % 16 == 0;
+    draft_bind_workspace(p, workspace);
+    const bool vec_t = ((size_t)V * dtype_size(target_dtype)) % 16 == 0;
+    // the draft kernel, then verify T=0 as its programmatic dependent (its target-row
+    // pass may start while the draft finishes); verify writes its flags into this
+    // workspace's status word
+    spec_status st = cuda_status(draft_launch(p, (cudaStream_t)stream));
+    if (st != SPEC_OK) return st;
+    VerifyParams v;
+    memset(&v, 0, sizeof(v));
+    v.target = target_logits;
+    v.tdt = target_dtype;
+    v.ddt = target_dtype;
+    v.tokens = tokens_out;
+    v.B = B;
+    v.gamma = gamma;
+    v.V = V;
+    v.temperature = 0;
+    v.nchunk = (V + kVerifyChunk - 1) / kVerifyChunk;
+    v.vec_t = vec_t;
+    v.n_out = n_accepted_out;
+    v.committed_out = committed_out;
+    v.bonus_out = bonus_out;
+    verify_bind_workspace(v, draft_verify_verify_ws(workspace, B, gamma, V, r));
+    v.status = p.status;
+    return cuda_status(verify_launch(v, (cudaStream_t)stream));
 }
 
 spec_status spec_e2etv(const uint16_t* target_logits, const uint16_t* draft_logits, int n_branches, int Wb, int V,

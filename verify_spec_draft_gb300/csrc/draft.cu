@@ -75,6 +75,17 @@ size_t draft_workspace_bytes(int B, int gamma, int V, int r) {
     return off;
 }
 
+// spec_draft_verify's workspace: the draft's, then a verify workspace.
+static size_t dv_verify_offset(int B, int gamma, int V, int r) {
+    return align_up(draft_workspace_bytes(B, gamma, V, r), 256);
+}
+size_t draft_verify_workspace_bytes(int B, int gamma, int V, int r) {
+    return dv_verify_offset(B, gamma, V, r) + verify_workspace_bytes(B, gamma, V);
+}
+void* draft_verify_verify_ws(void* ws, int B, int gamma, int V, int r) {
+    return static_cast<char*>(ws) + dv_verify_offset(B, gamma, V, r);
+}
+
 void draft_bind_workspace(DraftParams& p, void* ws) {
     char* w = static_cast<char*>(ws);
     WsHeader* h = reinterpret_cast<WsHeader*>(w);

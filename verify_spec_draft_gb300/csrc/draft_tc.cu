@@ -183,6 +183,10 @@ constexpr int kTcWarps = 18;                 // producer, MMA, 16 epilogue warps
 // TMEM accumulator buffers: all 512 columns, so the MMA runs up to NB-1 tiles ahead
 // of the epilogue (4 with one 128-row M tile, 2 with two)
 template <int MT> struct TcBufs { static constexpr int N = MT == 1 ? 4 : 2; };
+// Wt ring stages of 16 KB: a compile-time count, so the single-thread producer and MMA
+// loops index the ring without integer division (deeper rings did not stream faster:
+// the extra copies only queue behind the first ones)
+template <int MT> struct TcStages { static constexpr int N = MT == 1 ? 6 : 3; };
 constexpr int kTcThreads = 32 * kTcWarps;
 
 struct TcShared {
@@ -195,7 +199,6 @@ struct TcShared {
     uint64_t* tfull;     // [NB]
     uint64_t* tempty;    // [NB]
     uint64_t* drain;     // [1]
-    int S;
 };
 
 __device__ __forceinline__ void named_barrier(int id, int nthreads) {
@@ -237,7 +240,7 @@ __device__ bool tc_tile_phase(const DraftParams& p, const CUtensorMap* tmap, con
     __syncthreads();
 
     const int tb = tile_begin(blockIdx.x, gridDim.x, p.n_tiles), te = tile_begin(blockIdx.x + 1, gridDim.x, p.n_tiles);
-    const int S = sh.S;
+    constexpr int S = TcStages<MT>::N;
     if (warp == 0) {
         if (lane == 0) {
             uint32_t skip = pre_issued;   // stages of this pass already in flight
@@ -385,21 +388,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint8_t* base = s_raw + ((1024u - (smem_u32(s_raw) & 1023u)) & 1023u);
     const int KB = p.r / kTcK;
     const int nw = blockDim.x >> 5;
+    // shared layout: A | Wt ring (S stages) | slice records | [T=1: tile records |
+    // per-warp U rows] | mbarriers | TMEM address | tokens | anchors.  T=0 needs neither
+    // T=1 region, so the launch gives its room to more ring stages.
     TcShared sh;
-    sh.S = MT == 1 ? 6 : 3;
+    constexpr int S = TcStages<MT>::N;
     sh.a = base;
     sh.b = base + (size_t)MT * KB * kTcBlock;
-    sh.slice_rec = reinterpret_cast<float4*>(sh.b + (size_t)sh.S * kTcBlock);
-    sh.tile_rec = sh.slice_rec + 16 * 32;
-    float* s_uw_all = reinterpret_cast<float*>(sh.tile_rec + 2 * 16 * 32);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(s_uw_all + (size_t)nw * p.r);
+    sh.slice_rec = reinterpret_cast<float4*>(sh.b + (size_t)S * kTcBlock);
+    const bool t1 = p.temperature == 1;
+    sh.tile_rec = t1 ? sh.slice_rec + 16 * 32 : nullptr;
+    float* s_uw_all = reinterpret_cast<float*>(sh.slice_rec + (t1 ? 3 : 1) * 16 * 32);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s_uw_all + (t1 ? (size_t)nw * p.r : 0));
     sh.full = bars;
-    sh.empty = bars + sh.S;
+    sh.empty = bars + S;
     constexpr int NB = TcBufs<MT>::N;
-    sh.tfull = bars + 2 * sh.S;
-    sh.tempty = bars + 2 * sh.S + NB;
-    sh.drain = bars + 2 * sh.S + 2 * NB;
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * sh.S + 2 * NB + 1);
+    sh.tfull = bars + 2 * S;
+    sh.tempty = bars + 2 * S + NB;
+    sh.drain = bars + 2 * S + 2 * NB;
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * S + 2 * NB + 1);
     const int R = p.B * p.gamma;
     int32_t* s_tok = reinterpret_cast<int32_t*>(s_tmem + 4);   // [2][B*gamma] (T=0)
     int32_t* s_anc = s_tok + 2 * R;                             // [B] anchors
@@ -409,7 +416,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     pdl_launch_dependents();   // a following verify may stream its target rows meanwhile
     if (threadIdx.x == 0) {
-        for (int s = 0; s < sh.S; ++s) { mbar_init(&sh.full[s], 1); mbar_init(&sh.empty[s], 1); }
+        for (int s = 0; s < S; ++s) { mbar_init(&sh.full[s], 1); mbar_init(&sh.empty[s], 1); }
         for (int b = 0; b < NB; ++b) { mbar_init(&sh.tfull[b], 1); mbar_init(&sh.tempty[b], kTcWarps - 2); }
         mbar_init(sh.drain, 1);
         fence_mbar_init();
@@ -421,24 +428,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t tmem = *s_tmem;
 
     uint32_t it_p = 0, it_m = 0, jt_m = 0, jt_e = 0, pre_issued = 0;
-    if (threadIdx.x == 0) {
-        // the first biased pass's first Wt stages depend on no token: they are requested
-        // now and land while pass 0 streams the logits
-        const int tb = tile_begin(blockIdx.x, gridDim.x, p.n_tiles);
-        const int te = tile_begin(blockIdx.x + 1, gridDim.x, p.n_tiles);
-        const uint32_t total = (uint32_t)(te - tb) * (uint32_t)KB;
-        pre_issued = total < (uint32_t)sh.S ? total : (uint32_t)sh.S;
-        for (uint32_t i = 0; i < pre_issued; ++i) {
-            mbar_arrive_expect_tx(&sh.full[i], kTcBlock);
-            tma_load_2d(sh.b + (size_t)i * kTcBlock, &tmap, (int)(i % KB) * kTcK, (tb + (int)(i / KB)) * kTcN,
-                        &sh.full[i]);
+    __shared__ uint32_t s_pre;
+    if (warp == nw - 1) {
+        // the last warp has no pass-0 row unless there are more rows than warps.  It
+        // requests the first biased pass's first Wt stages, which depend on no token, so
+        // they land while pass 0 streams the logits; the producer (thread 0) takes the
+        // count over after the next barrier.  It also loads the anchors, first needed
+        // after pass 0 and its barrier.
+        if ((threadIdx.x & 31) == 0) {
+            const int tb = tile_begin(blockIdx.x, gridDim.x, p.n_tiles);
+            const int te = tile_begin(blockIdx.x + 1, gridDim.x, p.n_tiles);
+            const uint32_t total = (uint32_t)(te - tb) * (uint32_t)KB;
+            const uint32_t n = total < (uint32_t)S ? total : (uint32_t)S;
+            for (uint32_t i = 0; i < n; ++i) {
+                mbar_arrive_expect_tx(&sh.full[i], kTcBlock);
+                tma_load_2d(sh.b + (size_t)i * kTcBlock, &tmap, (int)(i % KB) * kTcK, (tb + (int)(i / KB)) * kTcN,
+                            &sh.full[i]);
+            }
+            s_pre = n;
         }
-        it_p = pre_issued;
-    }
-    // anchors, first needed after pass 0 and its barrier; loaded by the last warp, which
-    // has no pass-0 row unless there are more rows than warps
-    if (warp == nw - 1)
         for (int b = threadIdx.x & 31; b < p.B; b += 32) s_anc[b] = p.anchor[b];
+    }
     const unsigned nb = gridDim.x;
     GridBarrier gb = grid_barrier_init(p.barrier);
     bool ok = true;
@@ -449,6 +459,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         int32_t* tok[2] = {s_tok, s_tok + R};
         tile_phase_stream0_t0<LT>(p, p.cta_rec, false);
         if (!grid_barrier(gb, nb, p.status)) ok = false;
+        if (threadIdx.x == 0) { pre_issued = s_pre; it_p = s_pre; }
         if (ok) finalize_all_t0(p, p.cta_rec, nullptr, tok[0], false, s_anc);
         for (pass = 1; ok; ++pass) {
             float4* rec = (pass & 1) ? p.cta_rec2 : p.cta_rec;
@@ -477,6 +488,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tile_phase_stream0<LT>(p);
             }
             if (!grid_barrier(gb, nb, p.status)) { ok = false; break; }
+            if (pass == 0 && threadIdx.x == 0) { pre_issued = s_pre; it_p = s_pre; }
             finalize_rows<LT, bf16_t>(p, pass, use_bias, prev, cur, gridDim.x, s_uw);
             if (!grid_barrier(gb, nb, p.status)) { ok = false; break; }
             if (pass >= 1 && __ldcg(&p.changed[pass]) == 0u) break;
@@ -493,9 +505,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_wait(sh.drain, 0u, p.status, kWaitLimitNs);
     }
     if (threadIdx.x == 0) {
-        const uint32_t n = it_p < (uint32_t)sh.S ? it_p : (uint32_t)sh.S;
+        if (it_p == 0) it_p = s_pre;   // stopped before taking the requested stages over
+        const uint32_t n = it_p < (uint32_t)S ? it_p : (uint32_t)S;
         for (uint32_t i = it_p - n; i < it_p; ++i)
-            mbar_wait(&sh.full[i % sh.S], (i / sh.S) & 1u, p.status, kWaitLimitNs);
+            mbar_wait(&sh.full[i % S], (i / S) & 1u, p.status, kWaitLimitNs);
     }
     __syncthreads();
     if (warp == 1) {
@@ -534,14 +547,19 @@ bool draft_tc_supported(const DraftParams& p) {
            encode_tiled() != nullptr;
 }
 
+constexpr size_t kTcSmemBudget = 227 * 1024;   // dynamic shared memory per CTA
+
 template <int MT, typename LT>
 static cudaError_t launch_tc(const DraftParams& p, cudaStream_t stream) {
     const int threads = kTcThreads;
-    const int S = MT == 1 ? 6 : 3;
     const int KB = p.r / kTcK;
-    const size_t smem = 1024 + (size_t)MT * KB * kTcBlock + (size_t)S * kTcBlock + sizeof(float4) * 3 * 16 * 32 +
-                        sizeof(float) * kTcWarps * p.r + sizeof(uint64_t) * (2 * S + 2 * TcBufs<MT>::N + 1) + 16 +
+    const bool t1 = p.temperature == 1;
+    constexpr int S = TcStages<MT>::N;
+    const size_t smem = 1024 + (size_t)MT * KB * kTcBlock + (size_t)S * kTcBlock +
+                        sizeof(float4) * (t1 ? 3 : 1) * 16 * 32 + (t1 ? sizeof(float) * kTcWarps * p.r : 0) +
+                        sizeof(uint64_t) * (2 * S + 2 * TcBufs<MT>::N + 1) + 16 +
                         sizeof(int32_t) * (2 * (size_t)p.B * p.gamma + p.B);
+    if (smem > kTcSmemBudget) return cudaErrorInvalidConfiguration;
     auto kern = draft_tc_kernel<MT, LT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

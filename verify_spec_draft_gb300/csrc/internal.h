@@ -74,6 +74,11 @@ size_t draft_workspace_bytes(int B, int gamma, int V, int r);
 void draft_bind_workspace(DraftParams& p, void* ws);
 cudaError_t draft_launch(const DraftParams& p, cudaStream_t stream);
 
+// spec_draft_verify: [draft workspace | verify workspace]
+size_t draft_verify_workspace_bytes(int B, int gamma, int V, int r);
+void* draft_verify_verify_ws(void* ws, int B, int gamma, int V, int r);
+bool draft_tc_supported(const DraftParams& p);
+
 struct E2etvParams {
     const uint16_t* target;    // bf16 [R, V]
     const uint16_t* draft;     // bf16 [R, V]
