@@ -32,7 +32,8 @@ struct VerifyParams {
     unsigned* barrier;         // grid barrier slot (T=1)
     unsigned long long* keys;  // [B*(gamma+1)] argmax keys (T=0)
     unsigned* rowbad;          // [B*(gamma+1)] (T=0)
-    float2* stats;             // [B*(2*gamma+1)*nchunk*8] (m2, s) per warp segment (T=1)
+    float2* stats;             // [B*(2*gamma+1)*nchunk*parts] (m2, s) partials (T=1)
+    int parts;                 // partials per (row, chunk): 8 warp segments, or 1 merged
     int4* state;               // [B*2]: mode, n, near, pad | m2p, sp, m2q, sq (float bits)
     float2* ksums;             // [B*nchunk*8] (residual sum, p sum) per warp segment
 };

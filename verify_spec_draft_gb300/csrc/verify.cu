@@ -382,6 +382,7 @@ __device__ __forceinline__ void stage_words(const uint8_t* stage, int warp, int 
 template <typename TT, typename DT>
 __device__ __forceinline__ void phase_stats_staged(const VerifyParams& p, uint8_t* ring, uint64_t* full,
                                                    uint64_t* empty, int4* s_item, int S, size_t stage_bytes) {
+
     const long items = (long)(2 * p.gamma + 1) * p.nchunk * p.B;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long mine = items > (long)blockIdx.x ? (items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
@@ -422,8 +423,31 @@ __device__ __forceinline__ void phase_stats_staged(const VerifyParams& p, uint8_
     }
 }
 
+// What the accept test of request b reads besides the row statistics: its draft tokens
+// and the target and draft logits at them.  Loaded by the CTA that tests request b
+// right after its streaming phase, so the two dependent round trips overlap the wait
+// at the grid barrier (threads 64.., one per position).
+struct AcceptInputs {
+    int tok[SPEC_MAX_GAMMA];
+    float lt[SPEC_MAX_GAMMA], ld[SPEC_MAX_GAMMA];
+    uint64_t seed;
+};
 template <typename TT, typename DT>
-__device__ __noinline__ void accept_phase(const VerifyParams& p, int b) {
+__device__ __forceinline__ void load_accept_inputs(const VerifyParams& p, int b, AcceptInputs& ai) {
+    const int G = p.gamma;
+    const int j = (int)threadIdx.x - 64;
+    if (j == 0) ai.seed = p.seeds[b];
+    if (j < 0 || j >= G) return;
+    const int t = p.tokens[(size_t)b * G + j];
+    ai.tok[j] = t;
+    if (t >= 0 && t < p.V) {
+        ai.lt[j] = to_float(static_cast<const TT*>(p.target)[((size_t)b * (G + 1) + j) * p.V + t]);
+        ai.ld[j] = to_float(static_cast<const DT*>(p.draft)[((size_t)b * G + j) * p.V + t]);
+    }
+}
+
+template <typename TT, typename DT>
+__device__ __noinline__ void accept_phase(const VerifyParams& p, int b, const AcceptInputs* pre) {
     const TT* target = static_cast<const TT*>(p.target);
     const DT* draft = static_cast<const DT*>(p.draft);
     const int G = p.gamma;
@@ -435,50 +459,72 @@ __device__ __noinline__ void accept_phase(const VerifyParams& p, int b) {
     if (threadIdx.x == 0) { s_badrow = 0; s_badtok = 0; }
     __syncthreads();
 
-    // merge each row's partials (lane-strided, fixed tree)
-    const int np = p.nchunk * kWarps;
-    for (int lr = warp; lr < nr; lr += kWarps) {
-        const size_t rowid = (size_t)b * nr + lr;
-        Stat2 acc = stat2_empty();
-        int bad = 0;
-        // the lane's first 8 partials are requested together, then merged in order
-        float2 v[8];
+    // each row's partials: the maximum first, then every partial's sum rescaled to it
+    // (independent exponentials, no chain of pairwise merges); a warp takes two rows
+    // with all their loads in flight.  NaN in a partial marks a row without a
+    // distribution.
+    const int np = p.nchunk * p.parts;
+    for (int lr0 = warp; lr0 < nr; lr0 += 2 * kWarps) {
+        float2 v[2][8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int i = lane + 32 * u;
-            v[u] = i < np ? __ldcg(&p.stats[rowid * np + i]) : make_float2(-INFINITY, 0.0f);
+        for (int h = 0; h < 2; ++h) {
+            const int lr = lr0 + h * kWarps;
+            const size_t rowid = (size_t)b * nr + (lr < nr ? lr : 0);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int i = lane + 32 * u;
+                v[h][u] = (lr < nr && i < np) ? __ldcg(&p.stats[rowid * np + i]) : make_float2(-INFINITY, 0.0f);
+            }
         }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            if (isnan(v[u].x)) bad = 1;
-            else acc = stat2_merge(acc, Stat2{v[u].x, v[u].y});
-        }
-        for (int i = lane + 256; i < np; i += 32) {
-            const float2 st = __ldcg(&p.stats[rowid * np + i]);
-            if (isnan(st.x)) bad = 1;
-            else acc = stat2_merge(acc, Stat2{st.x, st.y});
-        }
-        acc = warp_stat2(acc);
-        bad = warp_or(bad);
-        if (lane == 0) {
-            s_m2[lr] = acc.m2;
-            s_s[lr] = acc.s;
-            if (bad || acc.m2 == -INFINITY) atomicOr(&s_badrow, 1);
+        for (int h = 0; h < 2; ++h) {
+            const int lr = lr0 + h * kWarps;
+            const size_t rowid = (size_t)b * nr + (lr < nr ? lr : 0);
+            float M = -INFINITY;
+            int bad = 0;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (isnan(v[h][u].x)) bad = 1;
+                else M = fmaxf(M, v[h][u].x);
+            }
+            for (int i = lane + 256; i < np; i += 32) {
+                const float2 w = __ldcg(&p.stats[rowid * np + i]);
+                if (isnan(w.x)) bad = 1;
+                else M = fmaxf(M, w.x);
+            }
+            M = warp_max(M);
+            float sum = 0.0f;
+            if (M != -INFINITY) {
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (!isnan(v[h][u].x) && v[h][u].x != -INFINITY) sum += v[h][u].y * ex2(v[h][u].x - M);
+                for (int i = lane + 256; i < np; i += 32) {
+                    const float2 w = __ldcg(&p.stats[rowid * np + i]);
+                    if (!isnan(w.x) && w.x != -INFINITY) sum += w.y * ex2(w.x - M);
+                }
+            }
+            sum = warp_sum(sum);
+            bad = warp_or(bad);
+            if (lane == 0 && lr < nr) {
+                s_m2[lr] = M;
+                s_s[lr] = sum;
+                if (bad || M == -INFINITY) atomicOr(&s_badrow, 1);
+            }
         }
     }
     __syncthreads();
 
     // the gamma accept tests, one thread each; p and q of the drafted token with the
     // accurate exp2 (the decision is compared against exact arithmetic)
-    const uint64_t seed = p.seeds[b];
+    const uint64_t seed = pre ? pre->seed : p.seeds[b];
     for (int j = threadIdx.x; j < G; j += blockDim.x) {
-        const int t = p.tokens[(size_t)b * G + j];
+        const int t = pre ? pre->tok[j] : p.tokens[(size_t)b * G + j];
         int acc = 0, near = 0;
         if (t < 0 || t >= p.V) {
             atomicOr(&s_badtok, 1);
         } else {
-            const float lp = to_float(target[((size_t)b * (G + 1) + j) * p.V + t]);
-            const float lq = to_float(draft[((size_t)b * G + j) * p.V + t]);
+            const float lp = pre ? pre->lt[j] : to_float(target[((size_t)b * (G + 1) + j) * p.V + t]);
+            const float lq = pre ? pre->ld[j] : to_float(draft[((size_t)b * G + j) * p.V + t]);
             const float pj = exp2f(fmaf(lp, kLog2e, -s_m2[j])) / s_s[j];
             const float qj = exp2f(fmaf(lq, kLog2e, -s_m2[G + 1 + j])) / s_s[G + 1 + j];
             const float u = philox_uniform(seed, (uint64_t)b, (uint64_t)(j + 1), 1);
@@ -761,8 +807,10 @@ __global__ void __launch_bounds__(kThreads, 2) verify_t1_kernel(VerifyParams p) 
     } else {
         phase_stats<TT, DT>(p);
     }
+    __shared__ AcceptInputs s_ai;
+    if ((int)blockIdx.x < p.B) load_accept_inputs<TT, DT>(p, blockIdx.x, s_ai);
     if (!block_barrier(p.barrier, nb, p.status)) return;
-    for (int b = blockIdx.x; b < p.B; b += gridDim.x) accept_phase<TT, DT>(p, b);
+    for (int b = blockIdx.x; b < p.B; b += gridDim.x) accept_phase<TT, DT>(p, b, b == (int)blockIdx.x ? &s_ai : nullptr);
     if (!block_barrier(p.barrier, nb, p.status)) return;
     phase_weights<TT, DT>(p);
     if (!block_barrier(p.barrier, nb, p.status)) return;
@@ -822,6 +870,7 @@ static cudaError_t launch_t1(const VerifyParams& p, cudaStream_t stream) {
     long grid = (long)device_sm_count() * occ;
     if (grid > items) grid = items;
     VerifyParams args = p;
+    args.parts = kWarps;
     void* kargs[] = {&args};
     return cudaLaunchCooperativeKernel((const void*)kern, dim3((unsigned)grid), dim3(kThreads), kargs, smem, stream);
 }
