@@ -253,7 +253,9 @@ __global__ void __launch_bounds__(kThreads) e2etv_kernel(E2etvParams p) {
     __shared__ float s_a[SPEC_MAX_GAMMA], s_s[SPEC_MAX_GAMMA], s_c1[SPEC_MAX_GAMMA], s_c0[SPEC_MAX_GAMMA];
     __shared__ int s_bad;
     __shared__ __align__(8) uint64_t s_bar[2];   // [0] target rows, [1] draft rows
-    unsigned* bar = p.barriers + (size_t)g * 64;
+    // the group's barrier: a monotonic arrival count (slot word 0), as for the draft's
+    // grid barrier; the last CTA of the launch resets every group's count
+    GridBarrier gbar = grid_barrier_init(p.barriers + (size_t)g * 64);
     float2* part = p.partials + (size_t)g * 2 * p.group_size * nr;
     float2* part2 = part + (size_t)p.group_size * nr;
     const double inv_total = 1.0 / ((double)p.n_branches * Wb);
@@ -313,17 +315,44 @@ __global__ void __launch_bounds__(kThreads) e2etv_kernel(E2etvParams p) {
                 if (bad) atomicOr(&p.branch_bad[n], 1u);
             }
         }
-        if (!block_barrier(bar, p.group_size, p.status)) return;
+        if (!grid_barrier(gbar, p.group_size, p.status)) return;
 
-        // merge the group's partials in CTA order: LSE2 of every row
-        for (int i = warp; i < nr; i += kWarps) {
-            Stat2 acc = stat2_empty();
-            for (int c = lane; c < p.group_size; c += 32) {
-                const float2 v = __ldcg(&part[(size_t)c * nr + i]);
-                acc = stat2_merge(acc, Stat2{v.x, v.y});
+        // the group's partials of every row: LSE2 = log2 of the sum over CTAs of
+        // s * 2^(m2 - M) with M the largest m2, plus M.  A warp takes two rows with all
+        // their loads in flight (up to 128 CTAs per group; more are read in a loop).
+        for (int i0 = warp; i0 < nr; i0 += 2 * kWarps) {
+            float2 v[2][4];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int i = i0 + h * kWarps;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int c = lane + 32 * u;
+                    v[h][u] = (i < nr && c < p.group_size) ? __ldcg(&part[(size_t)c * nr + i])
+                                                            : make_float2(-INFINITY, 0.0f);
+                }
             }
-            acc = warp_stat2(acc);
-            if (lane == 0) s_lse[i] = (acc.m2 == -INFINITY) ? NAN : stat2_lse2(acc);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int i = i0 + h * kWarps;
+                float M = -INFINITY;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) M = fmaxf(M, v[h][u].x);
+                for (int c = lane + 128; c < p.group_size && i < nr; c += 32) M = fmaxf(M, __ldcg(&part[(size_t)c * nr + i]).x);
+                M = warp_max(M);
+                float sum = 0.0f;
+                if (M != -INFINITY) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        if (v[h][u].x != -INFINITY) sum += v[h][u].y * ex2(v[h][u].x - M);
+                    for (int c = lane + 128; c < p.group_size && i < nr; c += 32) {
+                        const float2 w = __ldcg(&part[(size_t)c * nr + i]);
+                        if (w.x != -INFINITY) sum += w.y * ex2(w.x - M);
+                    }
+                }
+                sum = warp_sum(sum);
+                if (lane == 0 && i < nr) s_lse[i] = (M == -INFINITY) ? NAN : M + log2f(sum);
+            }
         }
         if (threadIdx.x == 0) s_bad = (__ldcg(&p.branch_bad[n]) != 0u) ? 1 : 0;
         __syncthreads();
@@ -346,15 +375,23 @@ __global__ void __launch_bounds__(kThreads) e2etv_kernel(E2etvParams p) {
         }
         __syncthreads();                                   // target rows no longer read
         if (threadIdx.x == 0) issue(n + p.n_groups, 0);
-        if (!block_barrier(bar, p.group_size, p.status)) return;
+        if (!grid_barrier(gbar, p.group_size, p.status)) return;
 
         if (!bad_branch) {
             for (int i = warp; i < Wb; i += kWarps) {
                 float a = 0.0f, s = 0.0f;
-                for (int c = lane; c < p.group_size; c += 32) {
-                    const float2 v = __ldcg(&part2[(size_t)c * Wb + i]);
-                    a += v.x;
-                    s += v.y;
+                float2 v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int c = lane + 32 * u;
+                    v[u] = c < p.group_size ? __ldcg(&part2[(size_t)c * Wb + i]) : make_float2(0.0f, 0.0f);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) { a += v[u].x; s += v[u].y; }
+                for (int c = lane + 128; c < p.group_size; c += 32) {
+                    const float2 w = __ldcg(&part2[(size_t)c * Wb + i]);
+                    a += w.x;
+                    s += w.y;
                 }
                 a = warp_sum(a);
                 s = warp_sum(s);
@@ -432,6 +469,7 @@ __global__ void __launch_bounds__(kThreads) e2etv_kernel(E2etvParams p) {
 
     // loss = 1 - mean S, summed over branches in order by the last CTA to finish
     if (!last_block_done(p.done, gridDim.x)) return;
+    for (int i = threadIdx.x; i < p.n_groups; i += blockDim.x) p.barriers[(size_t)i * 64] = 0u;
     if (warp == 0) {
         const int N = p.n_branches;
         const int K = (N + 31) / 32;
