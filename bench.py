@@ -35,6 +35,10 @@ METRIC = "verify rows/s (V-wide) + % HBM roofline; draft+verify µs @B1 γ15 V24
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 512 << 20
+# DRAM bytes (read + written) per launch of draft_tc_kernel<1, bf16> on the headline
+# workload, from an ncu capture (ncu --set full, one launch); None once the kernel
+# changes, until it is captured again
+DRAFT_TC_TRAFFIC_BYTES = 142_696_960
 
 
 def parse():
@@ -296,7 +300,9 @@ def run_ours(args, rank, world, torch, dist):
             "frac": achieved / hbm,
             "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
             "algorithmic_bytes_per_launch": dom_bytes,
-            "traffic": None,
+            # dram__bytes_read.sum + dram__bytes_write.sum of this kernel on this workload,
+            # from one ncu capture
+            "traffic": DRAFT_TC_TRAFFIC_BYTES,
         },
         "gpu_launches": 2 * args.steps,
         "wall_s_timed_loop": t_wall,
