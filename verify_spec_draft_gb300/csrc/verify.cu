@@ -550,7 +550,7 @@ __device__ __noinline__ void accept_phase(const VerifyParams& p, int b, const Ac
             int k = 0, near = 0;
             while (k < G && s_acc[k]) { near |= s_near[k]; ++k; }
             if (k < G) near |= s_near[k];
-            for (int i = 0; i < k; ++i) com[i] = p.tokens[(size_t)b * G + i];
+            for (int i = 0; i < k; ++i) com[i] = pre ? pre->tok[i] : p.tokens[(size_t)b * G + i];
             for (int i = k + 1; i <= G; ++i) com[i] = -1;
             if (k < G) {   // rejected at position k+1: target row k and draft row k
                 st0 = make_int4(MODE_RESID, k, near, 0);
