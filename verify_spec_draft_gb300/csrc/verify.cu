@@ -16,11 +16,12 @@
 //        one warp per request, and writes the outputs.
 //   T=1  one cooperative kernel in four phases separated by bounded grid barriers:
 //        (1) base-2 softmax statistics of every target and draft row, one partial per
-//        1024-entry warp segment; (2) per request, merge its rows in order, run the
-//        gamma accept tests in parallel, record the row to sample from; (3) re-read
-//        that row pair (residual) or row (bonus) for its weight per segment in
-//        vocabulary order; (4) per request, locate the segment holding u * sum and
-//        the entry inside it.  No counters or fences in the streaming phases.
+//        1024-entry warp segment; (2) per request, merge its rows in order while the
+//        request's uniforms are drawn, run the gamma accept tests in parallel, record
+//        the row to sample from; (3) re-read that row pair (residual) or row (bonus)
+//        for its weight per segment in vocabulary order; (4) one CTA per request
+//        locates the segment holding u * sum and the entry inside it.  No counters or
+//        fences in the streaming phase.
 #include "spec_device.cuh"
 #include "internal.h"
 
@@ -260,7 +261,7 @@ __global__ void __launch_bounds__(kT0Threads) verify_t0_kernel(VerifyParams p) {
 //   2  one CTA per request: merge its rows, run the gamma accept tests, record the
 //      row to draw from (residual at the first rejection, or the bonus row)
 //   3  weights of those rows per (request, chunk, warp), in vocabulary order
-//   4  one warp per request: locate the 1024-entry segment holding u * sum, then the
+//   4  one CTA per request: locate the 1024-entry segment holding u * sum, then the
 //      entry inside it
 // ----------------------------------------------------------------------------------
 struct Item1 { int b, lr, c; };   // local rows 0..G target, G+1..2G draft
@@ -455,7 +456,11 @@ __device__ __noinline__ void accept_phase(const VerifyParams& p, int b, const Ac
     __shared__ float s_m2[2 * SPEC_MAX_GAMMA + 1], s_s[2 * SPEC_MAX_GAMMA + 1];
     __shared__ int s_badrow, s_badtok;
     __shared__ int s_acc[SPEC_MAX_GAMMA], s_near[SPEC_MAX_GAMMA];
+    // the request's uniforms: accept tests (stream 1) for positions 1..G, residual
+    // draws (stream 2) for positions 1..G, the bonus draw (stream 3)
+    __shared__ float s_u[2 * SPEC_MAX_GAMMA + 1];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint64_t seed = pre ? pre->seed : p.seeds[b];
     if (threadIdx.x == 0) { s_badrow = 0; s_badtok = 0; }
     __syncthreads();
 
@@ -475,6 +480,14 @@ __device__ __noinline__ void accept_phase(const VerifyParams& p, int b, const Ac
                 const int i = lane + 32 * u;
                 v[h][u] = (lr < nr && i < np) ? __ldcg(&p.stats[rowid * np + i]) : make_float2(-INFINITY, 0.0f);
             }
+        }
+        // the Philox draws depend on no data: computed while the loads are in flight
+        // (threads 0..2G lie in warps below nr, which all run this first iteration)
+        if (lr0 == warp && (int)threadIdx.x < nr) {
+            const int t = threadIdx.x;
+            const int pos = t < G ? t + 1 : (t < 2 * G ? t - G + 1 : G + 1);
+            const int stream = t < G ? 1 : (t < 2 * G ? 2 : 3);
+            s_u[t] = philox_uniform(seed, (uint64_t)b, (uint64_t)pos, (uint64_t)stream);
         }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -516,7 +529,6 @@ __device__ __noinline__ void accept_phase(const VerifyParams& p, int b, const Ac
 
     // the gamma accept tests, one thread each; p and q of the drafted token with the
     // accurate exp2 (the decision is compared against exact arithmetic)
-    const uint64_t seed = pre ? pre->seed : p.seeds[b];
     for (int j = threadIdx.x; j < G; j += blockDim.x) {
         const int t = pre ? pre->tok[j] : p.tokens[(size_t)b * G + j];
         int acc = 0, near = 0;
@@ -527,7 +539,7 @@ __device__ __noinline__ void accept_phase(const VerifyParams& p, int b, const Ac
             const float lq = pre ? pre->ld[j] : to_float(draft[((size_t)b * G + j) * p.V + t]);
             const float pj = exp2f(fmaf(lp, kLog2e, -s_m2[j])) / s_s[j];
             const float qj = exp2f(fmaf(lq, kLog2e, -s_m2[G + 1 + j])) / s_s[G + 1 + j];
-            const float u = philox_uniform(seed, (uint64_t)b, (uint64_t)(j + 1), 1);
+            const float u = s_u[j];
             acc = (u * qj < pj) ? 1 : 0;
             near = (fabsf(u * qj - pj) < kNearTie * qj) ? 1 : 0;
         }
@@ -553,11 +565,11 @@ __device__ __noinline__ void accept_phase(const VerifyParams& p, int b, const Ac
             for (int i = 0; i < k; ++i) com[i] = pre ? pre->tok[i] : p.tokens[(size_t)b * G + i];
             for (int i = k + 1; i <= G; ++i) com[i] = -1;
             if (k < G) {   // rejected at position k+1: target row k and draft row k
-                st0 = make_int4(MODE_RESID, k, near, 0);
+                st0 = make_int4(MODE_RESID, k, near, __float_as_int(s_u[G + k]));
                 st1 = make_int4(__float_as_int(s_m2[k]), __float_as_int(s_s[k]),
                                 __float_as_int(s_m2[G + 1 + k]), __float_as_int(s_s[G + 1 + k]));
             } else {       // all accepted: bonus from target row gamma
-                st0 = make_int4(MODE_BONUS, G, near, 0);
+                st0 = make_int4(MODE_BONUS, G, near, __float_as_int(s_u[2 * G]));
                 st1 = make_int4(__float_as_int(s_m2[G]), __float_as_int(s_s[G]), 0, 0);
             }
         }
@@ -569,44 +581,19 @@ __device__ __noinline__ void accept_phase(const VerifyParams& p, int b, const Ac
 
 struct DrawRow {   // what the accept phase recorded for a request
     int mode, n, near;
+    float u;       // the draw's uniform
     float m2p, sp, m2q, sq;
 };
 __device__ __forceinline__ DrawRow draw_row(const VerifyParams& p, int b) {
     const int4 a = __ldcg(&p.state[2 * b]);
     const int4 c = __ldcg(&p.state[2 * b + 1]);
-    return DrawRow{a.x, a.y, a.z, __int_as_float(c.x), __int_as_float(c.y), __int_as_float(c.z), __int_as_float(c.w)};
+    return DrawRow{a.x, a.y, a.z, __int_as_float(a.w),
+                   __int_as_float(c.x), __int_as_float(c.y), __int_as_float(c.z), __int_as_float(c.w)};
 }
 
-// Weights of 32 entries: wp = p, wr = max(0, p - q) in residual mode, with
-// p = 2^(l log2e - m2p) / sp and q = 2^(d log2e - m2q) / sq.  The streaming pass and
-// the final scan use this same arithmetic in the same order.
-template <typename TT, typename DT, int NW>
-__device__ __forceinline__ void weights(const DrawRow& d, const uint4 (&wt)[NW], const uint4 (&wd)[NW],
-                                        float (&wr)[kEPT], float (&wp)[kEPT]) {
-    float lt[kEPT];
-    decode_words<TT, NW>(wt, lt);
-    const float ip = 1.0f / d.sp;
-    if (d.mode == MODE_RESID) {
-        float ld[kEPT];
-        decode_words<DT, NW>(wd, ld);
-        const float iq = 1.0f / d.sq;
-#pragma unroll
-        for (int e = 0; e < kEPT; ++e) {
-            const float pv = wexp(lt[e], d.m2p) * ip;
-            const float qv = wexp(ld[e], d.m2q) * iq;
-            wp[e] = pv;
-            wr[e] = fmaxf(0.0f, pv - qv);
-        }
-    } else {
-#pragma unroll
-        for (int e = 0; e < kEPT; ++e) {
-            wp[e] = wexp(lt[e], d.m2p) * ip;
-            wr[e] = 0.0f;
-        }
-    }
-}
-
-// weights() summed in the same order, without keeping the entries.
+// Weights of 32 entries, summed in order: wr = max(0, p - q) (residual mode only) and
+// wp = p, with p = 2^(l log2e - m2p) / sp and q = 2^(d log2e - m2q) / sq.  The draw
+// recomputes the entries of one segment with this same per-entry arithmetic.
 template <typename TT, typename DT, int NW>
 __device__ __forceinline__ void weight_sums(const DrawRow& d, const uint4 (&wt)[NW], const uint4 (&wd)[NW],
                                             float& sr, float& sp) {
@@ -649,7 +636,7 @@ __device__ __forceinline__ void phase_weights(const VerifyParams& p) {
     constexpr int NW = Words<TT>::N > Words<DT>::N ? Words<TT>::N : Words<DT>::N;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint4 ct[NW], cd[NW], nt[NW], nd[NW];
-    DrawRow dc{MODE_DONE, 0, 0, 0.f, 0.f, 0.f, 0.f}, dn = dc;
+    DrawRow dc{MODE_DONE, 0, 0, 0.f, 0.f, 0.f, 0.f, 0.f}, dn = dc;
     // items = B * nchunk < 2^31 (B <= 65535, nchunk <= 8192): 32-bit index math
     const unsigned nch = (unsigned)p.nchunk;
     unsigned it = blockIdx.x;
@@ -680,110 +667,174 @@ __device__ __forceinline__ void phase_weights(const VerifyParams& p) {
     }
 }
 
-// One warp draws the token of request b (segments are 1024 entries: chunk c, warp w).
+// Inclusive prefix over the CTA's threads, in thread order, and the total.  `buf`
+// holds one float per warp.
+__device__ __forceinline__ float block_inclusive_scan(float x, float* buf, float& total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const float wi = warp_inclusive_scan(x);
+    if (lane == 31) buf[warp] = wi;
+    __syncthreads();
+    float off = 0.0f, tot = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        const float v = buf[w];
+        if (w < warp) off += v;
+        tot += v;
+    }
+    __syncthreads();   // buf is reused by the next scan
+    total = tot;
+    return off + wi;
+}
+
+// Four consecutive entries of a row from element v, -inf past its end.
+__device__ __forceinline__ void load4(const bf16_t* row, long v, long V, bool vec_ok, float (&o)[4]) {
+    if (vec_ok && v + 4 <= V) {
+        const uint2 w = __ldg(reinterpret_cast<const uint2*>(row + v));
+        o[0] = __uint_as_float(w.x << 16); o[1] = __uint_as_float(w.x & 0xffff0000u);
+        o[2] = __uint_as_float(w.y << 16); o[3] = __uint_as_float(w.y & 0xffff0000u);
+    } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[e] = (v + e < V) ? load_one(row + v + e) : -INFINITY;
+    }
+}
+__device__ __forceinline__ void load4(const float* row, long v, long V, bool vec_ok, float (&o)[4]) {
+    if (vec_ok && v + 4 <= V) {
+        const float4 w = __ldg(reinterpret_cast<const float4*>(row + v));
+        o[0] = w.x; o[1] = w.y; o[2] = w.z; o[3] = w.w;
+    } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[e] = (v + e < V) ? load_one(row + v + e) : -INFINITY;
+    }
+}
+
+// One CTA draws the token of request b.  Segments are the weights pass's 1024-entry
+// (chunk c, warp w) sums; thread t holds segments [t K, t K + K) in order, so the
+// prefix over threads is the prefix over segments.  The thread whose range passes
+// t = u * W finds the segment and the remainder tl; the segment's entries (four per
+// thread) get the weights pass's arithmetic again, and the first entry whose running
+// sum passes tl is drawn.
 template <typename TT, typename DT>
-__device__ __noinline__ void draw_token(const VerifyParams& p, int b) {
-    constexpr int NW = Words<TT>::N > Words<DT>::N ? Words<TT>::N : Words<DT>::N;
-    const int lane = threadIdx.x & 31;
-    const DrawRow d = draw_row(p, b);
-    if (d.mode == MODE_DONE) return;
+__device__ __noinline__ void draw_block(const VerifyParams& p, int b) {
+    __shared__ float s_scan[kWarps];
+    __shared__ int s_sel, s_seg, s_tok, s_near;
+    __shared__ float s_tl;
+    const int tid = threadIdx.x;
     const int G = p.gamma;
     const int nseg = p.nchunk * kWarps;
     const float2* ks = p.ksums + (size_t)b * nseg;
-    // totals and the segment holding the threshold (contiguous lane ranges)
-    const int K = (nseg + 31) / 32;
-    const int s0 = lane * K, s1 = min(nseg, s0 + K);
-    // the lane's segment sums, requested together and kept for the search below
-    // (up to 8 in registers: V <= 8192 * 32; longer ranges reload the rest)
-    constexpr int KR = 8;
+    const int K = (nseg + kThreads - 1) / kThreads;
+    const int s0 = min(nseg, tid * K), s1 = min(nseg, s0 + K);
+    // the thread's first segment sums, requested together with the request's state
+    constexpr int KR = 4;
     float2 kv[KR];
 #pragma unroll
     for (int u = 0; u < KR; ++u) kv[u] = (s0 + u < s1) ? __ldcg(&ks[s0 + u]) : make_float2(0.0f, 0.0f);
-    auto ksum = [&](int i) -> float2 { return i - s0 < KR ? kv[i - s0] : __ldcg(&ks[i]); };
+    auto kseg = [&](int i) -> float2 {
+        const int u = i - s0;
+        return u == 0 ? kv[0] : (u == 1 ? kv[1] : (u == 2 ? kv[2] : (u == 3 ? kv[3] : __ldcg(&ks[i]))));
+    };
+    const DrawRow d = draw_row(p, b);
+    if (d.mode == MODE_DONE) return;   // the same for every thread
     float sr = 0.0f, sp = 0.0f;
 #pragma unroll
     for (int u = 0; u < KR; ++u) { sr += kv[u].x; sp += kv[u].y; }
     for (int i = s0 + KR; i < s1; ++i) { const float2 v = __ldcg(&ks[i]); sr += v.x; sp += v.y; }
-    const float ir = warp_inclusive_scan(sr), ip = warp_inclusive_scan(sp);
-    const float Wr = __shfl_sync(0xffffffffu, ir, 31), Wp = __shfl_sync(0xffffffffu, ip, 31);
+    float Wr, Wp;
+    const float ir = block_inclusive_scan(sr, s_scan, Wr);
+    const float ip = block_inclusive_scan(sp, s_scan, Wp);
     const bool ur = (d.mode == MODE_RESID) && (Wr > 0.0f);
     const float W = ur ? Wr : Wp;
     const float incl = ur ? ir : ip, mine = ur ? sr : sp;
-    const float u = (d.mode == MODE_RESID) ? philox_uniform(p.seeds[b], (uint64_t)b, (uint64_t)(d.n + 1), 2)
-                                           : philox_uniform(p.seeds[b], (uint64_t)b, (uint64_t)(G + 1), 3);
-    const float t = u * W;
-    const unsigned cross = __ballot_sync(0xffffffffu, incl > t);
-    int seg = -1;
-    float tl = INFINITY;
-    if (cross) {
-        const int L = __ffs(cross) - 1;
-        if (lane == L) {
+    const float t = d.u * W;
+
+    // the segment: first thread whose inclusive prefix passes t
+    if (tid == 0) { s_sel = kThreads; s_seg = -1; s_tl = INFINITY; }
+    __syncthreads();
+    if (incl > t) atomicMin(&s_sel, tid);
+    __syncthreads();
+    const int T = s_sel;
+    if (T < kThreads) {
+        if (tid == T) {
             float run = incl - mine;
+            int sg = -1;
+            float tt = INFINITY;
             for (int i = s0; i < s1; ++i) {
-                const float2 v = ksum(i);
+                const float2 v = kseg(i);
                 const float w = ur ? v.x : v.y;
-                if (run + w > t) { seg = i; tl = t - run; break; }
+                if (run + w > t) { sg = i; tt = t - run; break; }
                 run += w;
             }
-            if (seg < 0) seg = s1 - 1;
+            s_seg = sg < 0 ? s1 - 1 : sg;
+            s_tl = tt;
         }
-        seg = __shfl_sync(0xffffffffu, seg, L);
-        tl = __shfl_sync(0xffffffffu, tl, L);
     } else {   // u * W rounded up to W: the last segment with positive weight
         int last = -1;
         for (int i = s0; i < s1; ++i) {
-            const float2 v = ksum(i);
+            const float2 v = kseg(i);
             if ((ur ? v.x : v.y) > 0.0f) last = i;
         }
-        const unsigned has = __ballot_sync(0xffffffffu, last >= 0);
-        seg = has ? __shfl_sync(0xffffffffu, last, 31 - __clz(has)) : 0;
+        if (last >= 0) atomicMax(&s_seg, last);
     }
-    seg = max(0, min(seg, nseg - 1));
-    // recompute the segment's weights (same lanes, same arithmetic) and scan them
-    const long base = (long)(seg / kWarps) * kVerifyChunk + (long)(seg % kWarps) * 1024 + (long)lane * kEPT;
-    uint4 wt[NW], wd[NW];
-    load_draw<TT, DT, NW>(p, b, base, d, wt, wd);
-    float wr[kEPT], wp[kEPT];
-    weights<TT, DT, NW>(d, wt, wd, wr, wp);
-    float mysum = 0.0f;
+    __syncthreads();
+    const int seg = max(0, min(s_seg, nseg - 1));
+    const float tl = s_tl;
+
+    // the entry: four per thread, in vocabulary order
+    const long base = (long)(seg / kWarps) * kVerifyChunk + (long)(seg % kWarps) * 1024 + (long)tid * 4;
+    float lt[4], w[4];
+    load4(static_cast<const TT*>(p.target) + ((size_t)b * (G + 1) + d.n) * p.V, base, p.V, p.vec_t != 0, lt);
+    const float ipv = 1.0f / d.sp;
+    if (ur) {
+        float ld[4];
+        load4(static_cast<const DT*>(p.draft) + ((size_t)b * G + d.n) * p.V, base, p.V, p.vec_d != 0, ld);
+        const float iq = 1.0f / d.sq;
 #pragma unroll
-    for (int e = 0; e < kEPT; ++e) mysum += ur ? wr[e] : wp[e];
-    const float inc = warp_inclusive_scan(mysum);
-    const float ex = inc - mysum;
-    const unsigned hit = __ballot_sync(0xffffffffu, ex <= tl && inc > tl);
-    int tok = -1, near = 0;
-    if (hit) {
-        const int L = __ffs(hit) - 1;
-        if (lane == L) {
-            float run = ex;
-            for (int e = 0; e < kEPT; ++e) {
-                const float w = ur ? wr[e] : wp[e];
-                if (run + w > tl && w > 0.0f) {
-                    tok = (int)(base + e);
-                    const float tol = kNearTie * W;
-                    near = ((run > 0.0f && fabsf(tl - run) < tol) || fabsf(run + w - tl) < tol) ? 1 : 0;
-                    break;
-                }
-                run += w;
-            }
+        for (int e = 0; e < 4; ++e) {
+            const float pv = wexp(lt[e], d.m2p) * ipv;
+            const float qv = wexp(ld[e], d.m2q) * iq;
+            w[e] = fmaxf(0.0f, pv - qv);
         }
-        tok = __shfl_sync(0xffffffffu, tok, L);
-        near = __shfl_sync(0xffffffffu, near, L);
-    }
-    if (tok < 0) {   // rounding left no crossing: last entry of positive weight in the segment
-        int last = -1;
-        for (int e = 0; e < kEPT; ++e)
-            if ((ur ? wr[e] : wp[e]) > 0.0f && base + e < p.V) last = (int)(base + e);
+    } else {
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
-        tok = last;
+        for (int e = 0; e < 4; ++e) w[e] = wexp(lt[e], d.m2p) * ipv;
     }
-    if (lane == 0) {
-        p.committed_out[(size_t)b * (G + 1) + d.n] = tok;
-        p.bonus_out[b] = tok;
+    const float mysum = (w[0] + w[1]) + (w[2] + w[3]);
+    float segtot;
+    const float inc = block_inclusive_scan(mysum, s_scan, segtot);
+    const float ex = inc - mysum;
+    if (tid == 0) { s_sel = kThreads; s_tok = -1; s_near = 0; }
+    __syncthreads();
+    if (ex <= tl && inc > tl) atomicMin(&s_sel, tid);
+    __syncthreads();
+    if (tid == s_sel) {
+        float run = ex;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if (run + w[e] > tl && w[e] > 0.0f) {
+                s_tok = (int)(base + e);
+                const float tol = kNearTie * W;
+                s_near = ((run > 0.0f && fabsf(tl - run) < tol) || fabsf(run + w[e] - tl) < tol) ? 1 : 0;
+                break;
+            }
+            run += w[e];
+        }
+    }
+    __syncthreads();
+    if (s_tok < 0) {   // rounding left no crossing: last entry of positive weight in the segment
+        int last = -1;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (w[e] > 0.0f && base + e < p.V) last = (int)(base + e);
+        if (last >= 0) atomicMax(&s_tok, last);
+        __syncthreads();
+    }
+    if (tid == 0) {
+        p.committed_out[(size_t)b * (G + 1) + d.n] = s_tok;
+        p.bonus_out[b] = s_tok;
         p.n_out[b] = d.n;
-        if (p.near_out) p.near_out[b] = d.near | near;
+        if (p.near_out) p.near_out[b] = d.near | s_near;
     }
+    __syncthreads();   // shared state is reused by the CTA's next request
 }
 
 template <typename TT, typename DT>
@@ -809,13 +860,14 @@ __global__ void __launch_bounds__(kThreads, 2) verify_t1_kernel(VerifyParams p) 
     }
     __shared__ AcceptInputs s_ai;
     if ((int)blockIdx.x < p.B) load_accept_inputs<TT, DT>(p, blockIdx.x, s_ai);
-    if (!block_barrier(p.barrier, nb, p.status)) return;
+    GridBarrier gb = grid_barrier_init(p.barrier);
+    if (!grid_barrier(gb, nb, p.status)) return;
     for (int b = blockIdx.x; b < p.B; b += gridDim.x) accept_phase<TT, DT>(p, b, b == (int)blockIdx.x ? &s_ai : nullptr);
-    if (!block_barrier(p.barrier, nb, p.status)) return;
+    if (!grid_barrier(gb, nb, p.status)) return;
     phase_weights<TT, DT>(p);
-    if (!block_barrier(p.barrier, nb, p.status)) return;
-    const int gw = blockIdx.x * kWarps + (threadIdx.x >> 5);
-    for (int b = gw; b < p.B; b += gridDim.x * kWarps) draw_token<TT, DT>(p, b);
+    if (!grid_barrier(gb, nb, p.status)) return;
+    grid_barrier_exit(gb, nb);
+    for (int b = blockIdx.x; b < p.B; b += gridDim.x) draw_block<TT, DT>(p, b);
 }
 
 // ----------------------------------------------------------------------------------
