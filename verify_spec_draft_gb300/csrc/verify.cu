@@ -425,19 +425,29 @@ __device__ __forceinline__ void phase_stats_staged(const VerifyParams& p, uint8_
 }
 
 // What the accept test of request b reads besides the row statistics: its draft tokens
-// and the target and draft logits at them.  Loaded by the CTA that tests request b
+// and the target and draft logits at them, loaded by the CTA that tests request b
 // right after its streaming phase, so the two dependent round trips overlap the wait
-// at the grid barrier (threads 64.., one per position).
+// at the grid barrier (threads 64.., one per position); and the request's uniforms,
+// which depend on no data: drawn at kernel start (threads 32..32+2G) while the first
+// copies are in flight.  u[j] is the accept test of position j+1 (stream 1), u[G+j]
+// the residual draw at position j+1 (stream 2), u[2G] the bonus draw (stream 3).
 struct AcceptInputs {
     int tok[SPEC_MAX_GAMMA];
     float lt[SPEC_MAX_GAMMA], ld[SPEC_MAX_GAMMA];
-    uint64_t seed;
+    float u[2 * SPEC_MAX_GAMMA + 1];
 };
+__device__ __forceinline__ void accept_uniforms(const VerifyParams& p, int b, AcceptInputs& ai) {
+    const int G = p.gamma;
+    const int t = (int)threadIdx.x - 32;
+    if (t < 0 || t > 2 * G) return;
+    const int pos = t < G ? t + 1 : (t < 2 * G ? t - G + 1 : G + 1);
+    const int stream = t < G ? 1 : (t < 2 * G ? 2 : 3);
+    ai.u[t] = philox_uniform(p.seeds[b], (uint64_t)b, (uint64_t)pos, (uint64_t)stream);
+}
 template <typename TT, typename DT>
 __device__ __forceinline__ void load_accept_inputs(const VerifyParams& p, int b, AcceptInputs& ai) {
     const int G = p.gamma;
     const int j = (int)threadIdx.x - 64;
-    if (j == 0) ai.seed = p.seeds[b];
     if (j < 0 || j >= G) return;
     const int t = p.tokens[(size_t)b * G + j];
     ai.tok[j] = t;
@@ -456,11 +466,11 @@ __device__ __noinline__ void accept_phase(const VerifyParams& p, int b, const Ac
     __shared__ float s_m2[2 * SPEC_MAX_GAMMA + 1], s_s[2 * SPEC_MAX_GAMMA + 1];
     __shared__ int s_badrow, s_badtok;
     __shared__ int s_acc[SPEC_MAX_GAMMA], s_near[SPEC_MAX_GAMMA];
-    // the request's uniforms: accept tests (stream 1) for positions 1..G, residual
-    // draws (stream 2) for positions 1..G, the bonus draw (stream 3)
+    // the request's uniforms (as AcceptInputs::u), drawn here unless `pre` has them
     __shared__ float s_u[2 * SPEC_MAX_GAMMA + 1];
+    __shared__ int s_k;
+    const float* U = pre ? pre->u : s_u;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const uint64_t seed = pre ? pre->seed : p.seeds[b];
     if (threadIdx.x == 0) { s_badrow = 0; s_badtok = 0; }
     __syncthreads();
 
@@ -481,13 +491,13 @@ __device__ __noinline__ void accept_phase(const VerifyParams& p, int b, const Ac
                 v[h][u] = (lr < nr && i < np) ? __ldcg(&p.stats[rowid * np + i]) : make_float2(-INFINITY, 0.0f);
             }
         }
-        // the Philox draws depend on no data: computed while the loads are in flight
+        // without `pre`, the Philox draws are computed while the loads are in flight
         // (threads 0..2G lie in warps below nr, which all run this first iteration)
-        if (lr0 == warp && (int)threadIdx.x < nr) {
+        if (!pre && lr0 == warp && (int)threadIdx.x < nr) {
             const int t = threadIdx.x;
             const int pos = t < G ? t + 1 : (t < 2 * G ? t - G + 1 : G + 1);
             const int stream = t < G ? 1 : (t < 2 * G ? 2 : 3);
-            s_u[t] = philox_uniform(seed, (uint64_t)b, (uint64_t)pos, (uint64_t)stream);
+            s_u[t] = philox_uniform(p.seeds[b], (uint64_t)b, (uint64_t)pos, (uint64_t)stream);
         }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -539,7 +549,7 @@ __device__ __noinline__ void accept_phase(const VerifyParams& p, int b, const Ac
             const float lq = pre ? pre->ld[j] : to_float(draft[((size_t)b * G + j) * p.V + t]);
             const float pj = exp2f(fmaf(lp, kLog2e, -s_m2[j])) / s_s[j];
             const float qj = exp2f(fmaf(lq, kLog2e, -s_m2[G + 1 + j])) / s_s[G + 1 + j];
-            const float u = s_u[j];
+            const float u = U[j];
             acc = (u * qj < pj) ? 1 : 0;
             near = (fabsf(u * qj - pj) < kNearTie * qj) ? 1 : 0;
         }
@@ -548,33 +558,42 @@ __device__ __noinline__ void accept_phase(const VerifyParams& p, int b, const Ac
     }
     __syncthreads();
 
+    // the outcome (thread 0): k accepted, or -1 for a request without a valid row or
+    // token; then the committed tokens, one thread per position (position k gets the
+    // draw later)
     if (threadIdx.x == 0) {
-        int32_t* com = p.committed_out + (size_t)b * (G + 1);
         int4 st0 = make_int4(MODE_DONE, -1, 0, 0);
         int4 st1 = make_int4(0, 0, 0, 0);
+        int k = -1;
         if (s_badrow || s_badtok) {
             atomicOr(p.status, (s_badtok ? SPEC_DEV_TOKEN : 0u) | (s_badrow ? SPEC_DEV_NONFINITE : 0u));
             p.n_out[b] = -1;
             p.bonus_out[b] = -1;
-            for (int i = 0; i <= G; ++i) com[i] = -1;
             if (p.near_out) p.near_out[b] = 0;
         } else {
-            int k = 0, near = 0;
+            int near = 0;
+            k = 0;
             while (k < G && s_acc[k]) { near |= s_near[k]; ++k; }
             if (k < G) near |= s_near[k];
-            for (int i = 0; i < k; ++i) com[i] = pre ? pre->tok[i] : p.tokens[(size_t)b * G + i];
-            for (int i = k + 1; i <= G; ++i) com[i] = -1;
             if (k < G) {   // rejected at position k+1: target row k and draft row k
-                st0 = make_int4(MODE_RESID, k, near, __float_as_int(s_u[G + k]));
+                st0 = make_int4(MODE_RESID, k, near, __float_as_int(U[G + k]));
                 st1 = make_int4(__float_as_int(s_m2[k]), __float_as_int(s_s[k]),
                                 __float_as_int(s_m2[G + 1 + k]), __float_as_int(s_s[G + 1 + k]));
             } else {       // all accepted: bonus from target row gamma
-                st0 = make_int4(MODE_BONUS, G, near, __float_as_int(s_u[2 * G]));
+                st0 = make_int4(MODE_BONUS, G, near, __float_as_int(U[2 * G]));
                 st1 = make_int4(__float_as_int(s_m2[G]), __float_as_int(s_s[G]), 0, 0);
             }
         }
         p.state[2 * b] = st0;
         p.state[2 * b + 1] = st1;
+        s_k = k;
+    }
+    __syncthreads();
+    const int k = s_k;
+    int32_t* com = p.committed_out + (size_t)b * (G + 1);
+    for (int i = threadIdx.x; i <= G; i += blockDim.x) {
+        if (k < 0 || i > k) com[i] = -1;
+        else if (i < k) com[i] = pre ? pre->tok[i] : p.tokens[(size_t)b * G + i];
     }
     __syncthreads();
 }
@@ -840,6 +859,8 @@ __device__ __noinline__ void draw_block(const VerifyParams& p, int b) {
 template <typename TT, typename DT>
 __global__ void __launch_bounds__(kThreads, 2) verify_t1_kernel(VerifyParams p) {
     const unsigned nb = gridDim.x;
+    __shared__ AcceptInputs s_ai;
+    if ((int)blockIdx.x < p.B) accept_uniforms(p, blockIdx.x, s_ai);
     if (p.vec_t && p.vec_d) {
         extern __shared__ __align__(128) uint8_t v1_smem[];
         constexpr bool wide = sizeof(TT) == 4 || sizeof(DT) == 4;
@@ -858,7 +879,6 @@ __global__ void __launch_bounds__(kThreads, 2) verify_t1_kernel(VerifyParams p) 
     } else {
         phase_stats<TT, DT>(p);
     }
-    __shared__ AcceptInputs s_ai;
     if ((int)blockIdx.x < p.B) load_accept_inputs<TT, DT>(p, blockIdx.x, s_ai);
     GridBarrier gb = grid_barrier_init(p.barrier);
     if (!grid_barrier(gb, nb, p.status)) return;
