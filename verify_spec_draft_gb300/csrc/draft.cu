@@ -39,7 +39,7 @@ __global__ void __launch_bounds__(kThreads) draft_kernel(DraftParams p) {
         const int32_t* prev = p.tokbuf + ((pass + 1) & 1) * (size_t)R;
         int32_t* cur = p.tokbuf + (pass & 1) * (size_t)R;
         if (blockIdx.x == 0 && threadIdx.x == 0) p.changed[pass + 1] = 0u;
-        if (!use_bias && p.vec_l && p.temperature == 0) tile_phase_stream0_t0<LT>(p, p.cta_rec, !biased);
+        if (!use_bias && p.vec_l && p.temperature == 0) tile_phase_stream0_t0<LT>(p, p.cta_rec, !biased, nullptr);
         else if (!use_bias && p.vec_l) tile_phase_stream0<LT>(p);
         else tile_phase_cc<LT, WT>(p, use_bias, prev, s_uw);
         if (!grid_barrier(gb, nb, p.status)) return;
@@ -72,6 +72,7 @@ size_t draft_workspace_bytes(int B, int gamma, int V, int r) {
     off = align_up(off + sizeof(float4) * R * kDraftMaxGrid, 256);  // second buffer
     off = align_up(off + sizeof(int32_t) * 2 * R, 256);
     off = align_up(off + sizeof(unsigned) * (gamma + 2), 256);
+    off = align_up(off + sizeof(unsigned long long) * 3 * R * kKeyStride, 256);   // argmax keys
     return off;
 }
 
@@ -103,6 +104,8 @@ void draft_bind_workspace(DraftParams& p, void* ws) {
     p.tokbuf = reinterpret_cast<int32_t*>(w + off);
     off = align_up(off + sizeof(int32_t) * 2 * R, 256);
     p.changed = reinterpret_cast<unsigned*>(w + off);
+    off = align_up(off + sizeof(unsigned) * (p.gamma + 2), 256);
+    p.keys = reinterpret_cast<unsigned long long*>(w + off);
 }
 
 template <typename LT, typename WT>

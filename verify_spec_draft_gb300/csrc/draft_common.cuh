@@ -44,6 +44,19 @@ __device__ __forceinline__ RowAcc rowacc_merge(RowAcc a, RowAcc b) {
     return r;
 }
 
+// 64-bit argmax key of a row record: the ordered maximum in the high word, the
+// inverted index in the low word, so the largest key is the largest value at its
+// lowest index, as rowacc_merge decides; all ones for a row without a distribution.
+// The CTAs' keys of a row are folded with a relaxed red.max (the grid barrier that
+// follows orders them), one key per 128-byte line.
+constexpr int kKeyStride = 16;
+__device__ __forceinline__ unsigned long long rec_key(const RowAcc& a) {
+    return a.bad ? ~0ull : argmax_key(a.mx, (uint32_t)a.idx);
+}
+__device__ __forceinline__ void red_max_u64(unsigned long long* p, unsigned long long v) {
+    asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
+}
+
 __device__ __forceinline__ float4 rowacc_pack(RowAcc a) {
     return make_float4(a.mx, a.s, __int_as_float(a.idx), __int_as_float(a.bad));
 }
@@ -372,7 +385,7 @@ __device__ __forceinline__ void unit_record(const uint4& w, long e0, long V, int
 // follows (need_s false), so each lane keeps a running (max, lowest index) and, if
 // need_s, a running sum rescaled when the max grows; one warp reduction per row.
 template <typename LT>
-__device__ void tile_phase_stream0_t0(const DraftParams& p, float4* rec_out, bool need_s) {
+__device__ void tile_phase_stream0_t0(const DraftParams& p, float4* rec_out, bool need_s, unsigned long long* keys) {
     constexpr int EPL = 16 / (int)sizeof(LT);
     constexpr int UNIT = 32 * EPL;
     const int R = p.B * p.gamma;
@@ -463,7 +476,10 @@ __device__ void tile_phase_stream0_t0(const DraftParams& p, float4* rec_out, boo
         if (!need_s) bad = (isnan(mall) || mall == INFINITY) ? 1 : 0;
         RowAcc a{bad ? -INFINITY : m, need_s ? s : 0.0f, idx, bad};
         a = warp_rowacc(a);
-        if (lane == 0) rec_out[(size_t)row * gridDim.x + blockIdx.x] = rowacc_pack(a);
+        if (lane == 0) {
+            rec_out[(size_t)row * gridDim.x + blockIdx.x] = rowacc_pack(a);
+            if (keys) red_max_u64(&keys[(size_t)row * kKeyStride], rec_key(a));
+        }
     }
 }
 
@@ -600,6 +616,72 @@ __device__ __forceinline__ bool finalize_all_t0(const DraftParams& p, const floa
         }
     }
     return changed != 0;
+}
+
+// T=0 tokens from the folded argmax keys, in every CTA (one load per row): into the
+// shared array `cur`; returns whether any differs from `prev` (the same in every CTA).
+__device__ __forceinline__ bool finalize_keys_t0(const DraftParams& p, const unsigned long long* keys,
+                                                 const int32_t* prev, int32_t* cur, bool compare) {
+    const int R = p.B * p.gamma;
+    for (int row = threadIdx.x; row < R; row += blockDim.x) {
+        const unsigned long long k = __ldcg(&keys[(size_t)row * kKeyStride]);
+        const bool valid = k != ~0ull && key_value(k) != -INFINITY;
+        cur[row] = valid ? (int32_t)key_index(k) : -1;
+    }
+    __syncthreads();
+    int diff = 0;
+    if (compare)
+        for (int row = threadIdx.x; row < R; row += blockDim.x) diff |= (cur[row] != prev[row]) ? 1 : 0;
+    return __syncthreads_or(diff) != 0;
+}
+
+// After the last T=0 pass: the CTA owning a row (row % gridDim.x) merges its CTA
+// records (a warp per row, all loads in flight, CTA order) for the confidence
+// 1 / sum 2^(z log2e - m2), then writes the outputs, applying the chain rule (an
+// invalid anchor or position voids the rest of the request).  `cur` holds every row's
+// token.
+__device__ __forceinline__ void owner_outputs_t0(const DraftParams& p, const float4* recs_all, const int32_t* cur,
+                                                 const int32_t* anc) {
+    const int R = p.B * p.gamma;
+    const int lane = threadIdx.x & 31;
+    const int nw = blockDim.x >> 5;
+    const int nblk = gridDim.x;
+    const int nown = R > (int)blockIdx.x ? (R - 1 - (int)blockIdx.x) / nblk + 1 : 0;
+    for (int k = threadIdx.x >> 5; k < nown; k += nw) {
+        const int row = blockIdx.x + k * nblk;
+        const float4* recs = recs_all + (size_t)row * nblk;
+        float4 rv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int c = lane + 32 * i;
+            rv[i] = c < nblk ? __ldcg(&recs[c]) : rowacc_pack(rowacc_empty());
+        }
+        RowAcc acc = rowacc_empty();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc = rowacc_merge(acc, rowacc_unpack(rv[i]));
+        for (int c = lane + 256; c < nblk; c += 32) acc = rowacc_merge(acc, rowacc_unpack(__ldcg(&recs[c])));
+        acc = warp_rowacc(acc);
+        if (lane == 0)
+            p.conf_out[row] = cur[row] >= 0 ? ex2(fmaf(acc.mx, kLog2e, -acc.mx * kLog2e)) / acc.s : NAN;
+    }
+    __syncthreads();
+    for (int row = blockIdx.x + nblk * (int)threadIdx.x; row < R; row += nblk * (int)blockDim.x) {
+        const int b = row / p.gamma, j = row % p.gamma;
+        const int a = anc[b];
+        bool dead = (a < 0 || a >= p.V);
+        int first_dead = dead ? 0 : -1;
+        for (int k = 0; k <= j && !dead; ++k)
+            if (cur[b * p.gamma + k] < 0) { dead = true; first_dead = k; }
+        if (dead) {
+            p.tokens_out[row] = -1;
+            p.conf_out[row] = NAN;
+            if (p.qtok_out) p.qtok_out[row] = NAN;
+            if (first_dead == j) atomicOr(p.status, (a < 0 || a >= p.V) ? SPEC_DEV_TOKEN : SPEC_DEV_NONFINITE);
+        } else {
+            p.tokens_out[row] = cur[row];
+            if (p.qtok_out) p.qtok_out[row] = p.conf_out[row];
+        }
+    }
 }
 
 // Chain validity after the last pass (CTA 0): an anchor outside [0, V) or an invalid

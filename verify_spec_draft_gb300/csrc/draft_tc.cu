@@ -210,7 +210,7 @@ __device__ __forceinline__ void named_barrier(int id, int nthreads) {
 template <int MT, typename LT>
 __device__ bool tc_tile_phase(const DraftParams& p, const CUtensorMap* tmap, const int32_t* prev, const int32_t* anc,
                               float4* rec_out, const TcShared& sh, uint32_t tmem, uint32_t& it_p, uint32_t& it_m,
-                              uint32_t& jt_m, uint32_t& jt_e, uint32_t& pre_issued) {
+                              uint32_t& jt_m, uint32_t& jt_e, uint32_t& pre_issued, unsigned long long* keys) {
     constexpr int NB = TcBufs<MT>::N;
     constexpr int EW = 4 / MT;                 // column slices per quadrant and M tile
     constexpr int CPW = kTcN / EW;             // columns per epilogue warp (32 * MT)
@@ -376,6 +376,7 @@ __device__ bool tc_tile_phase(const DraftParams& p, const CUtensorMap* tmap, con
             for (int k = 0; k < EW; ++k)
                 m = rowacc_merge(m, rowacc_unpack(sh.slice_rec[(size_t)((mt * EW + k) * 4 + q) * 32 + lane]));
             rec_out[(size_t)g * gridDim.x + blockIdx.x] = rowacc_pack(m);
+            if (keys) red_max_u64(&keys[(size_t)g * kKeyStride], rec_key(m));
         }
     }
     return *(volatile int*)&s_fail == 0;
@@ -453,24 +454,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     GridBarrier gb = grid_barrier_init(p.barrier);
     bool ok = true;
     int pass = 0;
+    // T=0 argmax keys: pass j folds into buffer j % 3, read after its barrier; the buffer
+    // of pass j + 1 was last read before barrier j - 1, so CTA 0 clears it at the start
+    // of pass j (j >= 2; all three are zero at launch, and the last CTA to leave
+    // clears them again)
+    auto key_buf = [&](int pass_) { return p.keys + (size_t)(pass_ % 3) * R * kKeyStride; };
     if (p.temperature == 0) {
-        // T=0: every CTA finalizes every row, so a pass needs one grid barrier; records
-        // alternate between two buffers so no CTA overwrites what another still reads
+        // T=0: every CTA takes every row's token from the folded keys, so a pass needs
+        // one grid barrier; only the last pass's confidences are merged, by the row
+        // owners.  Records alternate between two buffers so no CTA overwrites what an
+        // owner still reads.
         int32_t* tok[2] = {s_tok, s_tok + R};
-        tile_phase_stream0_t0<LT>(p, p.cta_rec, false);
+        tile_phase_stream0_t0<LT>(p, p.cta_rec, false, key_buf(0));
         if (!grid_barrier(gb, nb, p.status)) ok = false;
         if (threadIdx.x == 0) { pre_issued = s_pre; it_p = s_pre; }
-        if (ok) finalize_all_t0(p, p.cta_rec, nullptr, tok[0], false, s_anc);
+        if (ok) finalize_keys_t0(p, key_buf(0), nullptr, tok[0], false);
         for (pass = 1; ok; ++pass) {
+            if (pass >= 2 && blockIdx.x == 0)
+                for (int r = threadIdx.x; r < R; r += blockDim.x) key_buf(pass + 1)[(size_t)r * kKeyStride] = 0ull;
             float4* rec = (pass & 1) ? p.cta_rec2 : p.cta_rec;
             if (!tc_tile_phase<MT, LT>(p, &tmap, tok[(pass + 1) & 1], s_anc, rec, sh, tmem, it_p, it_m, jt_m, jt_e,
-                                       pre_issued)) {
+                                       pre_issued, key_buf(pass))) {
                 ok = false;
                 break;
             }
             if (!grid_barrier(gb, nb, p.status)) { ok = false; break; }
-            const bool changed = finalize_all_t0(p, rec, tok[(pass + 1) & 1], tok[pass & 1], true, s_anc);
-            if (!changed || pass == p.gamma) break;
+            const bool changed = finalize_keys_t0(p, key_buf(pass), tok[(pass + 1) & 1], tok[pass & 1], true);
+            if (!changed || pass == p.gamma) {
+                owner_outputs_t0(p, rec, tok[pass & 1], s_anc);
+                break;
+            }
         }
     } else {
         for (;; ++pass) {
@@ -480,7 +493,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (blockIdx.x == 0 && threadIdx.x == 0) p.changed[pass + 1] = 0u;
             if (use_bias) {
                 if (!tc_tile_phase<MT, LT>(p, &tmap, prev, s_anc, p.cta_rec, sh, tmem, it_p, it_m, jt_m, jt_e,
-                                           pre_issued)) {
+                                           pre_issued, nullptr)) {
                     ok = false;
                     break;
                 }
@@ -515,7 +528,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, tmem_cols);
     }
-    if (ok) grid_barrier_exit(gb, nb);
+    __shared__ int s_last_out;
+    if (threadIdx.x == 0) s_last_out = (ok && grid_barrier_exit(gb, nb)) ? 1 : 0;
+    __syncthreads();
+    if (s_last_out && p.temperature == 0)
+        for (int i = threadIdx.x; i < 3 * R; i += blockDim.x) p.keys[(size_t)i * kKeyStride] = 0ull;
     if (!ok || blockIdx.x != 0) return;
     if (p.temperature != 0) chain_fixup(p);   // T=0 owners applied the chain rule already
     if (threadIdx.x == 0 && p.passes_out) *p.passes_out = pass;

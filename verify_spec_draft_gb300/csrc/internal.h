@@ -67,6 +67,7 @@ struct DraftParams {
     float4* cta_rec2;          // [R * grid] second buffer (passes alternate at T=0)
     int32_t* tokbuf;           // [2 * R] fixed-point iterates
     unsigned* changed;         // [gamma + 2]
+    unsigned long long* keys;  // [3][R] argmax keys, one per 128-byte line (T=0, tcgen05); zero between launches
 };
 
 constexpr int kDraftTile = 128;   // vocabulary entries per tile

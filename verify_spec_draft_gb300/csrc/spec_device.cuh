@@ -308,11 +308,14 @@ __device__ __forceinline__ bool grid_barrier(GridBarrier& gb, unsigned nblocks, 
     __syncthreads();
     return s_ok != 0;
 }
-__device__ __forceinline__ void grid_barrier_exit(const GridBarrier& gb, unsigned nblocks) {
+// Returns true in thread 0 of the last CTA to leave.
+__device__ __forceinline__ bool grid_barrier_exit(const GridBarrier& gb, unsigned nblocks) {
     if (threadIdx.x == 0 && atom_add_acq_rel(gb.exits, 1u) == nblocks - 1u) {
         atomicExch(gb.count, 0u);
         atomicExch(gb.exits, 0u);
+        return true;
     }
+    return false;
 }
 
 // Barrier over `nblocks` CTAs that are all resident (cooperative launch).  slot[0] is
