@@ -619,14 +619,16 @@ __device__ __forceinline__ bool finalize_all_t0(const DraftParams& p, const floa
 }
 
 // T=0 tokens from the folded argmax keys, in every CTA (one load per row): into the
-// shared array `cur`; returns whether any differs from `prev` (the same in every CTA).
+// shared array `cur`, and the row maxima into `cur_mx`; returns whether any token
+// differs from `prev` (the same in every CTA).
 __device__ __forceinline__ bool finalize_keys_t0(const DraftParams& p, const unsigned long long* keys,
-                                                 const int32_t* prev, int32_t* cur, bool compare) {
+                                                 const int32_t* prev, int32_t* cur, float* cur_mx, bool compare) {
     const int R = p.B * p.gamma;
     for (int row = threadIdx.x; row < R; row += blockDim.x) {
         const unsigned long long k = __ldcg(&keys[(size_t)row * kKeyStride]);
         const bool valid = k != ~0ull && key_value(k) != -INFINITY;
         cur[row] = valid ? (int32_t)key_index(k) : -1;
+        cur_mx[row] = valid ? key_value(k) : -INFINITY;
     }
     __syncthreads();
     int diff = 0;
@@ -635,36 +637,49 @@ __device__ __forceinline__ bool finalize_keys_t0(const DraftParams& p, const uns
     return __syncthreads_or(diff) != 0;
 }
 
-// After the last T=0 pass: the CTA owning a row (row % gridDim.x) merges its CTA
-// records (a warp per row, all loads in flight, CTA order) for the confidence
-// 1 / sum 2^(z log2e - m2), then writes the outputs, applying the chain rule (an
-// invalid anchor or position voids the rest of the request).  `cur` holds every row's
-// token.
+// After the last T=0 pass: the CTA owning a row (row % gridDim.x) computes its
+// confidence 1 / sum 2^(z log2e - m2) from the CTA records, each record's sum rescaled
+// to the row maximum from the keys (m2 = max log2e), independent exponentials summed
+// per warp and then over warps in order; the whole CTA takes the owned rows two at a
+// time with all records requested at once.  Then it writes the outputs, applying the
+// chain rule (an invalid anchor or position voids the rest of the request).  `cur` and
+// `cur_mx` hold every row's token and maximum.
 __device__ __forceinline__ void owner_outputs_t0(const DraftParams& p, const float4* recs_all, const int32_t* cur,
-                                                 const int32_t* anc) {
+                                                 const float* cur_mx, const int32_t* anc) {
     const int R = p.B * p.gamma;
-    const int lane = threadIdx.x & 31;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nw = blockDim.x >> 5;
     const int nblk = gridDim.x;
     const int nown = R > (int)blockIdx.x ? (R - 1 - (int)blockIdx.x) / nblk + 1 : 0;
-    for (int k = threadIdx.x >> 5; k < nown; k += nw) {
-        const int row = blockIdx.x + k * nblk;
-        const float4* recs = recs_all + (size_t)row * nblk;
-        float4 rv[8];
+    __shared__ float s_part[2][32];
+    for (int k0 = 0; k0 < nown; k0 += 2) {
+        float part[2] = {0.0f, 0.0f};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int c = lane + 32 * i;
-            rv[i] = c < nblk ? __ldcg(&recs[c]) : rowacc_pack(rowacc_empty());
+        for (int h = 0; h < 2; ++h) {
+            if (k0 + h >= nown) continue;
+            const int row = blockIdx.x + (k0 + h) * nblk;
+            if (cur[row] < 0) continue;
+            const float m2 = cur_mx[row] * kLog2e;
+            for (int c = threadIdx.x; c < nblk; c += blockDim.x) {
+                const RowAcc a = rowacc_unpack(__ldcg(&recs_all[(size_t)row * nblk + c]));
+                if (a.mx != -INFINITY) part[h] += a.s * ex2(a.mx * kLog2e - m2);
+            }
         }
-        RowAcc acc = rowacc_empty();
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc = rowacc_merge(acc, rowacc_unpack(rv[i]));
-        for (int c = lane + 256; c < nblk; c += 32) acc = rowacc_merge(acc, rowacc_unpack(__ldcg(&recs[c])));
-        acc = warp_rowacc(acc);
-        if (lane == 0)
-            p.conf_out[row] = cur[row] >= 0 ? ex2(fmaf(acc.mx, kLog2e, -acc.mx * kLog2e)) / acc.s : NAN;
+        for (int h = 0; h < 2; ++h) {
+            const float w = warp_sum(part[h]);
+            if (lane == 0) s_part[h][warp] = w;
+        }
+        __syncthreads();
+        if (threadIdx.x < 2 && k0 + (int)threadIdx.x < nown) {
+            const int row = blockIdx.x + (k0 + (int)threadIdx.x) * nblk;
+            float S = 0.0f;
+            for (int w = 0; w < nw; ++w) S += s_part[threadIdx.x][w];
+            const float mx = cur_mx[row];
+            p.conf_out[row] = cur[row] >= 0 ? ex2(fmaf(mx, kLog2e, -mx * kLog2e)) / S : NAN;
+        }
+        __syncthreads();
     }
-    __syncthreads();
     for (int row = blockIdx.x + nblk * (int)threadIdx.x; row < R; row += nblk * (int)blockDim.x) {
         const int b = row / p.gamma, j = row % p.gamma;
         const int a = anc[b];

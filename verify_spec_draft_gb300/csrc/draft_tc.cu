@@ -411,6 +411,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int R = p.B * p.gamma;
     int32_t* s_tok = reinterpret_cast<int32_t*>(s_tmem + 4);   // [2][B*gamma] (T=0)
     int32_t* s_anc = s_tok + 2 * R;                             // [B] anchors
+    float* s_mx = reinterpret_cast<float*>(s_anc + p.B);        // [B*gamma] row maxima (T=0)
     const int warp = threadIdx.x >> 5;
     float* s_uw = s_uw_all + (size_t)warp * p.r;
     constexpr uint32_t tmem_cols = 512u;
@@ -452,6 +453,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     const unsigned nb = gridDim.x;
     GridBarrier gb = grid_barrier_init(p.barrier);
+    __shared__ int s_last_out;   // this CTA was the last to leave (thread 0 sets it)
+    bool exited = false;         // the exit count is taken
     bool ok = true;
     int pass = 0;
     // T=0 argmax keys: pass j folds into buffer j % 3, read after its barrier; the buffer
@@ -468,7 +471,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tile_phase_stream0_t0<LT>(p, p.cta_rec, false, key_buf(0));
         if (!grid_barrier(gb, nb, p.status)) ok = false;
         if (threadIdx.x == 0) { pre_issued = s_pre; it_p = s_pre; }
-        if (ok) finalize_keys_t0(p, key_buf(0), nullptr, tok[0], false);
+        if (ok) finalize_keys_t0(p, key_buf(0), nullptr, tok[0], s_mx, false);
         for (pass = 1; ok; ++pass) {
             if (pass >= 2 && blockIdx.x == 0)
                 for (int r = threadIdx.x; r < R; r += blockDim.x) key_buf(pass + 1)[(size_t)r * kKeyStride] = 0ull;
@@ -479,9 +482,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 break;
             }
             if (!grid_barrier(gb, nb, p.status)) { ok = false; break; }
-            const bool changed = finalize_keys_t0(p, key_buf(pass), tok[(pass + 1) & 1], tok[pass & 1], true);
+            const bool changed = finalize_keys_t0(p, key_buf(pass), tok[(pass + 1) & 1], tok[pass & 1], s_mx, true);
             if (!changed || pass == p.gamma) {
-                owner_outputs_t0(p, rec, tok[pass & 1], s_anc);
+                // no barrier and no key read follow: count this CTA out now, so the
+                // count's round trip overlaps the owners' work
+                if (threadIdx.x == 0) s_last_out = grid_barrier_exit(gb, nb) ? 1 : 0;
+                exited = true;
+                owner_outputs_t0(p, rec, tok[pass & 1], s_mx, s_anc);
                 break;
             }
         }
@@ -528,8 +535,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, tmem_cols);
     }
-    __shared__ int s_last_out;
-    if (threadIdx.x == 0) s_last_out = (ok && grid_barrier_exit(gb, nb)) ? 1 : 0;
+    if (!exited && threadIdx.x == 0) s_last_out = (ok && grid_barrier_exit(gb, nb)) ? 1 : 0;
     __syncthreads();
     if (s_last_out && p.temperature == 0)
         for (int i = threadIdx.x; i < 3 * R; i += blockDim.x) p.keys[(size_t)i * kKeyStride] = 0ull;
@@ -575,7 +581,7 @@ static cudaError_t launch_tc(const DraftParams& p, cudaStream_t stream) {
     const size_t smem = 1024 + (size_t)MT * KB * kTcBlock + (size_t)S * kTcBlock +
                         sizeof(float4) * (t1 ? 3 : 1) * 16 * 32 + (t1 ? sizeof(float) * kTcWarps * p.r : 0) +
                         sizeof(uint64_t) * (2 * S + 2 * TcBufs<MT>::N + 1) + 16 +
-                        sizeof(int32_t) * (2 * (size_t)p.B * p.gamma + p.B);
+                        sizeof(int32_t) * (2 * (size_t)p.B * p.gamma + p.B) + sizeof(float) * (size_t)p.B * p.gamma;
     if (smem > kTcSmemBudget) return cudaErrorInvalidConfiguration;
     auto kern = draft_tc_kernel<MT, LT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
