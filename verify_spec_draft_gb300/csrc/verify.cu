@@ -686,6 +686,104 @@ __device__ __forceinline__ void phase_weights(const VerifyParams& p) {
     }
 }
 
+// Phase 3 with the rows staged by bulk copies (rows 16-byte aligned): CTA c's items
+// c, c + G, ... (request b, chunk c) go through slots of the phase-1 ring, one chunk
+// of the target row and one of the draft row per slot (three slots of bf16 rows), all
+// slots requested at once; the request states of the first items are loaded together.
+// The barriers are initialised again for this phase (phase 1 has no copy or arrival
+// pending on them).  Same per-entry arithmetic as phase_weights; each lane sums its
+// segment's 8-entry groups lane-interleaved (stage_groups).
+// This warp's 1024-entry segment of a staged chunk in 8-entry groups: lane L holds
+// groups j * 32 + L (j < 4), one 16-byte word each in bf16, two in float32, so that
+// entry e of decode_words is the same vocabulary entry for either type (target and
+// draft words pair up entry by entry).  -inf past the `nvalid` entries.
+template <typename T, int NW>
+__device__ __forceinline__ void stage_groups(const uint8_t* stage, int warp, int lane, int nvalid, uint4 (&w)[NW]) {
+    constexpr int WPG = (int)sizeof(T) / 2;   // 16-byte words per 8-entry group
+    const uint4* seg = reinterpret_cast<const uint4*>(stage) + (size_t)warp * (1024 / 8) * WPG;
+    const uint32_t ninf = sizeof(T) == 2 ? 0xff80ff80u : 0xff800000u;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int g = j * 32 + lane;
+        const bool in = warp * 1024 + g * 8 + 8 <= nvalid;
+#pragma unroll
+        for (int h = 0; h < WPG; ++h) w[j * WPG + h] = in ? seg[g * WPG + h] : make_uint4(ninf, ninf, ninf, ninf);
+    }
+}
+
+template <typename TT, typename DT>
+__device__ __forceinline__ void phase_weights_staged(const VerifyParams& p, uint8_t* ring, uint64_t* full,
+                                                     uint64_t* empty, int4* s_info) {
+    constexpr size_t kT = (size_t)kVerifyChunk * sizeof(TT), kD = (size_t)kVerifyChunk * sizeof(DT);
+    constexpr int NS = (int)(((size_t)kV1StagesBf16 * kVerifyChunk * 2) / (kT + kD));   // slots, >= 1
+    constexpr int NW = Words<TT>::N > Words<DT>::N ? Words<TT>::N : Words<DT>::N;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = p.gamma;
+    const unsigned nch = (unsigned)p.nchunk;
+    const unsigned items = (unsigned)p.B * nch;   // < 2^31 (B <= 65535, nchunk <= 8192)
+    const unsigned mine = items > blockIdx.x ? (items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NS; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], kWarps); }
+        fence_mbar_init();
+    }
+    __syncthreads();
+    // item k of this CTA into slot s (thread 0)
+    auto issue = [&](unsigned k, int s, const DrawRow& d) {
+        const unsigned it = blockIdx.x + k * gridDim.x;
+        const int b = (int)(it / nch), c = (int)(it - (unsigned)b * nch);
+        const long e0 = (long)c * kVerifyChunk;
+        const int nvalid = (int)((long)p.V - e0 < kVerifyChunk ? (long)p.V - e0 : kVerifyChunk);
+        s_info[2 * s] = make_int4(b, c, d.mode, nvalid);
+        s_info[2 * s + 1] = make_int4(__float_as_int(d.m2p), __float_as_int(d.sp), __float_as_int(d.m2q),
+                                      __float_as_int(d.sq));
+        uint64_t* bar = &full[s];
+        if (d.mode == MODE_DONE) { mbar_arrive1(bar); return; }
+        uint8_t* dst = ring + (size_t)s * (kT + kD);
+        const unsigned bt = (unsigned)nvalid * (unsigned)sizeof(TT);
+        const unsigned bd = d.mode == MODE_RESID ? (unsigned)nvalid * (unsigned)sizeof(DT) : 0u;
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(bar, bt + bd);
+        bulk_g2s(dst, static_cast<const TT*>(p.target) + ((size_t)b * (G + 1) + d.n) * p.V + e0, bt, bar);
+        if (bd) bulk_g2s(dst + kT, static_cast<const DT*>(p.draft) + ((size_t)b * G + d.n) * p.V + e0, bd, bar);
+    };
+    if (threadIdx.x == 0) {
+        DrawRow d0[NS];
+#pragma unroll
+        for (int j = 0; j < NS; ++j)
+            if ((unsigned)j < mine) d0[j] = draw_row(p, (int)((blockIdx.x + j * gridDim.x) / nch));
+#pragma unroll
+        for (int j = 0; j < NS; ++j)
+            if ((unsigned)j < mine) issue((unsigned)j, j, d0[j]);
+    }
+    for (unsigned k = 0; k < mine; ++k) {
+        const int s = (int)(k % NS);
+        if (threadIdx.x == 0 && k >= 1 && k - 1 + NS < mine) {
+            // refill the slot of item k-1 once every warp has left it
+            const int sp = (int)((k - 1) % NS);
+            const unsigned kn = k - 1 + NS;
+            const DrawRow dn = draw_row(p, (int)((blockIdx.x + kn * gridDim.x) / nch));
+            mbar_wait(&empty[sp], ((k - 1) / NS) & 1u, p.status, kV1WaitNs);
+            issue(kn, sp, dn);
+        }
+        if (!mbar_wait(&full[s], (k / NS) & 1u, p.status, kV1WaitNs)) return;
+        const int4 i0 = s_info[2 * s], i1 = s_info[2 * s + 1];
+        if (i0.z != MODE_DONE) {
+            DrawRow d{i0.z, 0, 0, 0.0f, __int_as_float(i1.x), __int_as_float(i1.y), __int_as_float(i1.z),
+                      __int_as_float(i1.w)};
+            const uint8_t* st = ring + (size_t)s * (kT + kD);
+            uint4 wt[NW], wd[NW];
+            stage_groups<TT>(st, warp, lane, i0.w, wt);
+            if (d.mode == MODE_RESID) stage_groups<DT>(st + kT, warp, lane, i0.w, wd);
+            float sr, sp;
+            weight_sums<TT, DT, NW>(d, wt, wd, sr, sp);
+            const float ir = warp_inclusive_scan(sr), ip = warp_inclusive_scan(sp);
+            if (lane == 31) p.ksums[((size_t)i0.x * p.nchunk + i0.y) * kWarps + warp] = make_float2(ir, ip);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive1(&empty[s]);
+    }
+}
+
 // Inclusive prefix over the CTA's threads, in thread order, and the total.  `buf`
 // holds one float per warp.
 __device__ __forceinline__ float block_inclusive_scan(float x, float* buf, float& total) {
@@ -884,7 +982,14 @@ __global__ void __launch_bounds__(kThreads, 2) verify_t1_kernel(VerifyParams p) 
     if (!grid_barrier(gb, nb, p.status)) return;
     for (int b = blockIdx.x; b < p.B; b += gridDim.x) accept_phase<TT, DT>(p, b, b == (int)blockIdx.x ? &s_ai : nullptr);
     if (!grid_barrier(gb, nb, p.status)) return;
-    phase_weights<TT, DT>(p);
+    if (p.vec_t && p.vec_d) {
+        extern __shared__ __align__(128) uint8_t v3_smem[];
+        phase_weights_staged<TT, DT>(p, v3_smem + kV1RingOffset, reinterpret_cast<uint64_t*>(v3_smem),
+                                     reinterpret_cast<uint64_t*>(v3_smem) + kV1StagesBf16,
+                                     reinterpret_cast<int4*>(v3_smem + 2 * 8 * kV1StagesBf16));
+    } else {
+        phase_weights<TT, DT>(p);
+    }
     if (!grid_barrier(gb, nb, p.status)) return;
     grid_barrier_exit(gb, nb);
     for (int b = blockIdx.x; b < p.B; b += gridDim.x) draw_block<TT, DT>(p, b);
