@@ -9,14 +9,20 @@
 // Every row needs three sweeps: (1) max / sum-exp of p and q, (2) a = sum min(p, q)
 // and s = sum_{q<p} q, which need (1)'s normalisers, (3) the gradient, which needs
 // kappa and so every a of the branch.  A branch (Wb row pairs) is handled by a
-// GROUP of CTAs; each CTA stages its column slice of all 2*Wb rows in shared memory
-// with TMA bulk copies, so HBM sees each logit read once and each gradient written
-// once (6 bytes per entry), and the sweeps run from shared memory.  Groups move
-// through branches independently; inside a group two bounded barriers (after sweeps 1
-// and 2) exchange per-CTA partials through global memory.  Sweep 2 keeps the q < p
-// test as one bit per entry, so the target rows are free after it: the next branch's
-// target rows are fetched while the group waits at the second barrier and sweep 3
-// runs, and its draft rows as soon as sweep 3 is done.
+// GROUP of CTAs, each on a column slice of its 2*Wb rows.  Groups move through
+// branches independently; inside a group two bounded barriers (after sweeps 1 and 2)
+// exchange per-CTA partials through global memory.  Sweep 2 keeps the q < p test as
+// one bit per entry, so the target rows are free after it.
+//
+// Two plans.  Rows 16-byte aligned, many branches: the sweeps read the rows from
+// global memory, sweep 1 from DRAM and sweeps 2 and 3 mostly from L2, each lane
+// keeping several 16-byte words in flight; about 18 groups of a few dozen CTAs (four
+// per SM) keep that many branches in flight, so one group's barrier waits overlap
+// other groups' sweeps.  Otherwise: each CTA stages its slice of all 2*Wb rows in
+// shared memory with TMA bulk copies (the next branch's target rows are fetched while
+// the group waits at the second barrier, its draft rows once sweep 3 is done), at most
+// four groups.  Either way HBM sees each logit read once and each gradient written
+// once (6 bytes per entry).
 //
 // Arithmetic is base 2 on FFMA-scaled logits: p_v = 2^(l_v log2e - LSE2_p), LSE2 the
 // log2 of the row normaliser; q_v < p_v is decided on the exponents; min(p, q) =
@@ -144,11 +150,11 @@ __device__ __forceinline__ void sweep_overlap(const bf16_t* tr, const bf16_t* dr
     s = warp_sum(ss);
 }
 
-// Batched variants of the two reductions for staged slices: each lane keeps B of its
-// 16-byte words in flight at once (instead of one load, then its arithmetic, then the
-// next load), and sums go to independent accumulators.  Same results up to the order
-// of float additions.
-template <int B>
+// Batched variants of the two reductions for 16-byte aligned slices, staged or in
+// global memory: each lane keeps B of its 16-byte words in flight at once (instead of
+// one load, then its arithmetic, then the next load), and sums go to independent
+// accumulators.  Same results up to the order of float additions.
+template <int B, bool STAGED>
 __device__ __forceinline__ void slice_stats(const bf16_t* row, int ncol, Stat2& out, int& bad) {
     const int lane = threadIdx.x & 31;
     const uint32_t ninf = 0xff80ff80u;
@@ -158,7 +164,7 @@ __device__ __forceinline__ void slice_stats(const bf16_t* row, int ncol, Stat2& 
 #pragma unroll
         for (int g = 0; g < B; ++g) {
             const int k = k0 + 256 * g;
-            w[g] = k < ncol ? ld16<true>(row + k) : make_uint4(ninf, ninf, ninf, ninf);
+            w[g] = k < ncol ? ld16<STAGED>(row + k) : make_uint4(ninf, ninf, ninf, ninf);
         }
 #pragma unroll
         for (int g = 0; g < B; ++g) mx2 = bmax2(mx2, bmax2(bmax2(w[g].x, w[g].y), bmax2(w[g].z, w[g].w)));
@@ -179,7 +185,7 @@ __device__ __forceinline__ void slice_stats(const bf16_t* row, int ncol, Stat2& 
 #pragma unroll
             for (int g = 0; g < B; ++g) {
                 const int k = k0 + 256 * g;
-                w[g] = k < ncol ? ld16<true>(row + k) : make_uint4(ninf, ninf, ninf, ninf);
+                w[g] = k < ncol ? ld16<STAGED>(row + k) : make_uint4(ninf, ninf, ninf, ninf);
             }
 #pragma unroll
             for (int g = 0; g < B; ++g) {   // -inf padding contributes 2^-inf = 0
@@ -193,7 +199,7 @@ __device__ __forceinline__ void slice_stats(const bf16_t* row, int ncol, Stat2& 
     out = Stat2{(bad || m == -INFINITY) ? -INFINITY : m2, warp_sum((s0 + s1) + (s2 + s3))};
 }
 
-template <int B>
+template <int B, bool STAGED>
 __device__ __forceinline__ void slice_overlap(const bf16_t* tr, const bf16_t* dr, int ncol, float lse_p, float lse_q,
                                               uint8_t* mask, float& a, float& s) {
     const int lane = threadIdx.x & 31;
@@ -205,8 +211,8 @@ __device__ __forceinline__ void slice_overlap(const bf16_t* tr, const bf16_t* dr
         for (int g = 0; g < B; ++g) {
             const int k = k0 + 256 * g;
             const bool in = k < ncol;
-            wl[g] = in ? ld16<true>(tr + k) : make_uint4(ninf, ninf, ninf, ninf);
-            wd[g] = in ? ld16<true>(dr + k) : make_uint4(ninf, ninf, ninf, ninf);
+            wl[g] = in ? ld16<STAGED>(tr + k) : make_uint4(ninf, ninf, ninf, ninf);
+            wd[g] = in ? ld16<STAGED>(dr + k) : make_uint4(ninf, ninf, ninf, ninf);
         }
 #pragma unroll
         for (int g = 0; g < B; ++g) {
@@ -235,7 +241,7 @@ __device__ __forceinline__ void slice_overlap(const bf16_t* tr, const bf16_t* dr
 }
 
 template <bool STAGED, bool VEC>
-__global__ void __launch_bounds__(kThreads) e2etv_kernel(E2etvParams p) {
+__global__ void __launch_bounds__(kThreads, STAGED ? 2 : 4) e2etv_kernel(E2etvParams p) {
     extern __shared__ __align__(128) uint8_t s_dyn[];
     const int Wb = p.Wb, nr = 2 * Wb;
     const int g = blockIdx.x / p.group_size;
@@ -308,7 +314,7 @@ __global__ void __launch_bounds__(kThreads) e2etv_kernel(E2etvParams p) {
         for (int i = warp; i < nr; i += kWarps) {
             Stat2 st;
             int bad = 0;
-            if (STAGED) slice_stats<8>((i < Wb ? rw.tgt : rw.drf) + (size_t)(i % Wb) * rw.stride, ncol, st, bad);
+            if (VEC) slice_stats<8, STAGED>((i < Wb ? rw.tgt : rw.drf) + (size_t)(i % Wb) * rw.stride, ncol, st, bad);
             else sweep_stats<STAGED, VEC>((i < Wb ? rw.tgt : rw.drf) + (size_t)(i % Wb) * rw.stride, ncol, st, bad);
             if (lane == 0) {
                 part[(size_t)gi * nr + i] = make_float2(st.m2, st.s);
@@ -364,8 +370,8 @@ __global__ void __launch_bounds__(kThreads) e2etv_kernel(E2etvParams p) {
         if (!bad_branch) {
             for (int i = warp; i < Wb; i += kWarps) {
                 float a, s;
-                if (STAGED)
-                    slice_overlap<4>(rw.tgt + (size_t)i * rw.stride, rw.drf + (size_t)i * rw.stride, ncol, s_lse[i],
+                if (VEC)
+                    slice_overlap<4, STAGED>(rw.tgt + (size_t)i * rw.stride, rw.drf + (size_t)i * rw.stride, ncol, s_lse[i],
                                      s_lse[Wb + i], s_mask + (size_t)i * ngroups8, a, s);
                 else
                     sweep_overlap<STAGED, VEC>(rw.tgt + (size_t)i * rw.stride, rw.drf + (size_t)i * rw.stride, ncol,
@@ -429,14 +435,31 @@ __global__ void __launch_bounds__(kThreads) e2etv_kernel(E2etvParams p) {
             p.branch_sum[n] = NAN;
         }
 
-        // sweep 3: gradient w.r.t. the draft logits, rounded once to bf16
+        // sweep 3: gradient w.r.t. the draft logits, rounded once to bf16; rows read from
+        // global memory keep U of a thread's 16-byte words in flight
         {
             const int ng = (ncol + 7) / 8;
-            for (int idx = threadIdx.x; idx < Wb * ng; idx += blockDim.x) {
+            const int total = Wb * ng;
+            constexpr int U = (!STAGED && VEC) ? 4 : 1;
+            for (int idx0 = threadIdx.x; idx0 < total; idx0 += (int)blockDim.x * U) {
+                uint4 wdu[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int idx = idx0 + u * (int)blockDim.x;
+                    wdu[u] = make_uint4(0u, 0u, 0u, 0u);
+                    if (idx < total && !bad_branch) {
+                        const int i = idx / ng, k = (idx - i * ng) * 8;
+                        wdu[u] = group8<STAGED, VEC>(rw.drf + (size_t)i * rw.stride, k, ncol);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                const int idx = idx0 + u * (int)blockDim.x;
+                if (idx >= total) continue;
                 const int i = idx / ng, k = (idx - i * ng) * 8;
                 uint4 out = make_uint4(0u, 0u, 0u, 0u);
                 if (!bad_branch) {
-                    const uint4 wd = group8<STAGED, VEC>(rw.drf + (size_t)i * rw.stride, k, ncol);
+                    const uint4 wd = wdu[u];
                     const uint32_t bits = s_mask[(size_t)i * ngroups8 + (k >> 3)];
                     const float lse_q = s_lse[Wb + i], c1 = s_c1[i], c0v = s_c0[i];
                     const uint32_t d4[4] = {wd.x, wd.y, wd.z, wd.w};
@@ -460,6 +483,7 @@ __global__ void __launch_bounds__(kThreads) e2etv_kernel(E2etvParams p) {
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
                         if (k + e < ncol) dst[e] = (uint16_t)((o4[e >> 1] >> (16 * (e & 1))) & 0xffffu);
+                }
                 }
             }
         }
@@ -496,6 +520,12 @@ __global__ void __launch_bounds__(kThreads) e2etv_kernel(E2etvParams p) {
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 constexpr int kE2MaxGrid = 1024;
+constexpr int kE2MaxPerSm = 6;                         // CTAs per SM of the unstaged plan
+// Branch bytes in flight of the unstaged plan: 18 groups for 7-row branches at
+// V = 248,320, the fastest of 12 to 25 groups measured.  A branch's target rows are
+// dead after its sweep 2, so L2 (129 MB) holds less than this at any moment.
+constexpr size_t kE2InFlightBytes = (size_t)130 << 20;
+constexpr int kE2MaxGroups = 64;                       // one barrier slot per group
 
 size_t e2etv_workspace_bytes(int n_branches, int Wb, int V) {
     (void)V;
@@ -539,6 +569,33 @@ cudaError_t e2etv_launch(E2etvParams& p, void* ws, cudaStream_t stream) {
     p.branch_bad = reinterpret_cast<unsigned*>(w + off);
 
     const int sms = device_sm_count();
+    // Rows 16-byte aligned: rows read from global memory (sweep 1 from DRAM, sweeps 2
+    // and 3 mostly from L2), kE2InFlightBytes of branches in flight (a branch is 2*Wb
+    // rows of V bf16 values), each on a group of CTAs, as many CTAs per SM as fit (up
+    // to kE2MaxPerSm).  With fewer than eight such groups the plan below is used.
+    if (p.vec_ok) {
+        int per_sm = occupancy<false, true>(16384);
+        if (per_sm > kE2MaxPerSm) per_sm = kE2MaxPerSm;
+        int grid = sms * per_sm;
+        if (grid > kE2MaxGrid) grid = kE2MaxGrid;
+        const size_t branch_bytes = (size_t)2 * p.Wb * (size_t)p.V * sizeof(uint16_t);
+        long n_groups = (long)(kE2InFlightBytes / branch_bytes);
+        n_groups = n_groups < p.n_branches ? n_groups : p.n_branches;
+        n_groups = n_groups < kE2MaxGroups ? n_groups : kE2MaxGroups;
+        n_groups = n_groups < grid ? n_groups : grid;
+        if (per_sm >= 1 && n_groups >= 8) {
+            const int group_size = grid / (int)n_groups;
+            long cols = (p.V + group_size - 1) / group_size;
+            cols = (cols + 7) / 8 * 8;
+            const size_t mask_bytes = align_up((size_t)p.Wb * (size_t)(cols / 8), 16);
+            if (occupancy<false, true>(mask_bytes) >= per_sm) {
+                p.n_groups = (int)n_groups;
+                p.group_size = group_size;
+                p.cols = (int)cols;
+                return launch_typed<false, true>(p, mask_bytes, (int)n_groups * group_size, stream);
+            }
+        }
+    }
     // Plan: up to four groups.  A staged plan needs every CTA's slice of the 2*Wb rows
     // (plus its q<p bits) within the shared-memory budget, which sets the smallest group.
     for (int per_sm = 2; per_sm >= 1; --per_sm) {
