@@ -51,6 +51,27 @@ __device__ __forceinline__ uint4 ld16(const bf16_t* p) {
     }
     return v;
 }
+// Global rows with an L2 eviction policy: a row read again by a later sweep is kept
+// (evict_last), a row at its last read goes first (evict_first), so that the rows of
+// the branches in flight stay in L2 while finished rows leave it.
+__device__ __forceinline__ uint64_t l2_policy_keep() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ uint64_t l2_policy_last_use() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+template <bool STAGED>
+__device__ __forceinline__ uint4 ld16p(const bf16_t* p, uint64_t pol) {
+    if (STAGED) return ld16<true>(p);
+    uint4 v;
+    asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p), "l"(pol));
+    return v;
+}
 __device__ __forceinline__ float lo_bf(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float hi_bf(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
@@ -155,7 +176,7 @@ __device__ __forceinline__ void sweep_overlap(const bf16_t* tr, const bf16_t* dr
 // one load, then its arithmetic, then the next load), and sums go to independent
 // accumulators.  Same results up to the order of float additions.
 template <int B, bool STAGED>
-__device__ __forceinline__ void slice_stats(const bf16_t* row, int ncol, Stat2& out, int& bad) {
+__device__ __forceinline__ void slice_stats(const bf16_t* row, int ncol, Stat2& out, int& bad, uint64_t pol) {
     const int lane = threadIdx.x & 31;
     const uint32_t ninf = 0xff80ff80u;
     uint32_t mx2 = ninf;
@@ -164,7 +185,7 @@ __device__ __forceinline__ void slice_stats(const bf16_t* row, int ncol, Stat2& 
 #pragma unroll
         for (int g = 0; g < B; ++g) {
             const int k = k0 + 256 * g;
-            w[g] = k < ncol ? ld16<STAGED>(row + k) : make_uint4(ninf, ninf, ninf, ninf);
+            w[g] = k < ncol ? ld16p<STAGED>(row + k, pol) : make_uint4(ninf, ninf, ninf, ninf);
         }
 #pragma unroll
         for (int g = 0; g < B; ++g) mx2 = bmax2(mx2, bmax2(bmax2(w[g].x, w[g].y), bmax2(w[g].z, w[g].w)));
@@ -185,7 +206,7 @@ __device__ __forceinline__ void slice_stats(const bf16_t* row, int ncol, Stat2& 
 #pragma unroll
             for (int g = 0; g < B; ++g) {
                 const int k = k0 + 256 * g;
-                w[g] = k < ncol ? ld16<STAGED>(row + k) : make_uint4(ninf, ninf, ninf, ninf);
+                w[g] = k < ncol ? ld16p<STAGED>(row + k, pol) : make_uint4(ninf, ninf, ninf, ninf);
             }
 #pragma unroll
             for (int g = 0; g < B; ++g) {   // -inf padding contributes 2^-inf = 0
@@ -201,7 +222,7 @@ __device__ __forceinline__ void slice_stats(const bf16_t* row, int ncol, Stat2& 
 
 template <int B, bool STAGED>
 __device__ __forceinline__ void slice_overlap(const bf16_t* tr, const bf16_t* dr, int ncol, float lse_p, float lse_q,
-                                              uint8_t* mask, float& a, float& s) {
+                                              uint8_t* mask, float& a, float& s, uint64_t pol_t, uint64_t pol_d) {
     const int lane = threadIdx.x & 31;
     const uint32_t ninf = 0xff80ff80u;
     float sa0 = 0.0f, sa1 = 0.0f, ss0 = 0.0f, ss1 = 0.0f;
@@ -211,8 +232,8 @@ __device__ __forceinline__ void slice_overlap(const bf16_t* tr, const bf16_t* dr
         for (int g = 0; g < B; ++g) {
             const int k = k0 + 256 * g;
             const bool in = k < ncol;
-            wl[g] = in ? ld16<STAGED>(tr + k) : make_uint4(ninf, ninf, ninf, ninf);
-            wd[g] = in ? ld16<STAGED>(dr + k) : make_uint4(ninf, ninf, ninf, ninf);
+            wl[g] = in ? ld16p<STAGED>(tr + k, pol_t) : make_uint4(ninf, ninf, ninf, ninf);
+            wd[g] = in ? ld16p<STAGED>(dr + k, pol_d) : make_uint4(ninf, ninf, ninf, ninf);
         }
 #pragma unroll
         for (int g = 0; g < B; ++g) {
@@ -267,6 +288,8 @@ __global__ void __launch_bounds__(kThreads, STAGED ? 2 : 4) e2etv_kernel(E2etvPa
     const double inv_total = 1.0 / ((double)p.n_branches * Wb);
     const unsigned bytes = (unsigned)ncol * 2u;
     unsigned ph_t = 0, ph_d = 0;
+    const uint64_t pol_keep = STAGED ? 0ull : l2_policy_keep();
+    const uint64_t pol_last = STAGED ? 0ull : l2_policy_last_use();
 
     // TMA bulk loads of one half (target or draft rows) of branch n's slice
     auto issue = [&](int n, int half) {
@@ -314,7 +337,8 @@ __global__ void __launch_bounds__(kThreads, STAGED ? 2 : 4) e2etv_kernel(E2etvPa
         for (int i = warp; i < nr; i += kWarps) {
             Stat2 st;
             int bad = 0;
-            if (VEC) slice_stats<8, STAGED>((i < Wb ? rw.tgt : rw.drf) + (size_t)(i % Wb) * rw.stride, ncol, st, bad);
+            if (VEC)
+                slice_stats<8, STAGED>((i < Wb ? rw.tgt : rw.drf) + (size_t)(i % Wb) * rw.stride, ncol, st, bad, pol_keep);
             else sweep_stats<STAGED, VEC>((i < Wb ? rw.tgt : rw.drf) + (size_t)(i % Wb) * rw.stride, ncol, st, bad);
             if (lane == 0) {
                 part[(size_t)gi * nr + i] = make_float2(st.m2, st.s);
@@ -372,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, STAGED ? 2 : 4) e2etv_kernel(E2etvPa
                 float a, s;
                 if (VEC)
                     slice_overlap<4, STAGED>(rw.tgt + (size_t)i * rw.stride, rw.drf + (size_t)i * rw.stride, ncol, s_lse[i],
-                                     s_lse[Wb + i], s_mask + (size_t)i * ngroups8, a, s);
+                                     s_lse[Wb + i], s_mask + (size_t)i * ngroups8, a, s, pol_last, pol_keep);
                 else
                     sweep_overlap<STAGED, VEC>(rw.tgt + (size_t)i * rw.stride, rw.drf + (size_t)i * rw.stride, ncol,
                                                s_lse[i], s_lse[Wb + i], s_mask + (size_t)i * ngroups8, a, s);
@@ -449,7 +473,8 @@ __global__ void __launch_bounds__(kThreads, STAGED ? 2 : 4) e2etv_kernel(E2etvPa
                     wdu[u] = make_uint4(0u, 0u, 0u, 0u);
                     if (idx < total && !bad_branch) {
                         const int i = idx / ng, k = (idx - i * ng) * 8;
-                        wdu[u] = group8<STAGED, VEC>(rw.drf + (size_t)i * rw.stride, k, ncol);
+                        wdu[u] = VEC ? ld16p<STAGED>(rw.drf + (size_t)i * rw.stride + k, pol_last)
+                                     : group8<STAGED, VEC>(rw.drf + (size_t)i * rw.stride, k, ncol);
                     }
                 }
 #pragma unroll
@@ -521,10 +546,12 @@ static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 constexpr int kE2MaxGrid = 1024;
 constexpr int kE2MaxPerSm = 6;                         // CTAs per SM of the unstaged plan
-// Branch bytes in flight of the unstaged plan: 18 groups for 7-row branches at
-// V = 248,320, the fastest of 12 to 25 groups measured.  A branch's target rows are
-// dead after its sweep 2, so L2 (129 MB) holds less than this at any moment.
-constexpr size_t kE2InFlightBytes = (size_t)130 << 20;
+// Branch bytes in flight of the unstaged plan: 23 groups for 7-row branches at
+// V = 248,320; of 12 to 25 groups measured, 18 to 25 ran within 3 % of each other and
+// fewer ran slower.  A branch's target rows are dead after its sweep 2 and its draft
+// rows after sweep 3 (both then read evict-first), so the live rows in L2 (129 MB)
+// are fewer than this.
+constexpr size_t kE2InFlightBytes = (size_t)160 << 20;
 constexpr int kE2MaxGroups = 64;                       // one barrier slot per group
 
 size_t e2etv_workspace_bytes(int n_branches, int Wb, int V) {
