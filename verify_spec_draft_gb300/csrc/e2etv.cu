@@ -546,9 +546,9 @@ static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 constexpr int kE2MaxGrid = 1024;
 constexpr int kE2MaxPerSm = 6;                         // CTAs per SM of the unstaged plan
-// Branch bytes in flight of the unstaged plan: 23 groups for 7-row branches at
-// V = 248,320; of 12 to 25 groups measured, 18 to 25 ran within 3 % of each other and
-// fewer ran slower.  A branch's target rows are dead after its sweep 2 and its draft
+// Branch bytes in flight of the unstaged plan: 24 groups for 7-row branches at
+// V = 248,320 (6.95 MB each); of 15 to 27 groups measured, 19 to 27 ran within 4 % of
+// each other and fewer ran slower.  A branch's target rows are dead after its sweep 2 and its draft
 // rows after sweep 3 (both then read evict-first), so the live rows in L2 (129 MB)
 // are fewer than this.
 constexpr size_t kE2InFlightBytes = (size_t)160 << 20;
