@@ -34,8 +34,12 @@
  *           reads it is reported with -1 tokens and the SPEC_DEV_NONFINITE flag.
  * Workspace.  Query the size with spec_workspace_bytes, allocate it on the device,
  *           and zero it ONCE with spec_workspace_init before its first use.  Every
- *           call leaves it zeroed again (except the status word), so it can be
- *           reused by later calls on the same stream.  Calls that run concurrently
+ *           call returns the counters, keys and flags it relies on to zero (its
+ *           other contents are scratch that the call writes before it reads them),
+ *           so later calls of the SAME operation and shape reuse it as it is, on
+ *           the same stream.  Before a call with another operation or shape, run
+ *           spec_workspace_init again (or use a separate workspace): its counters
+ *           sit where the earlier call left scratch.  Calls that run concurrently
  *           need separate workspaces.  After a SPEC_DEV_TIMEOUT flag, run
  *           spec_workspace_init again before reusing it.
  * Randomness.  T=1 draws use Philox4x64-10 (Salmon et al., SC'11) with key

@@ -144,7 +144,10 @@ def workspace_bytes(op, B, gamma, V, r=0):
 
 
 def workspace(op, B, gamma, V, r=0, device=None, stream=None):
-    """Allocate a device workspace for one operation and zero it (spec_workspace_init)."""
+    """Allocate a device workspace for one operation and zero it (spec_workspace_init).
+
+    Calls of that operation and shape can reuse it as it is; zero it again (or take a
+    new one) before a call with another operation or shape."""
     torch = _torch()
     n = workspace_bytes(op, B, gamma, V, r)
     ws = torch.empty(n, dtype=torch.uint8, device=device or torch.device("cuda"))
