@@ -335,7 +335,7 @@ __device__ __forceinline__ void phase_stats(const VerifyParams& p) {
 // warps reduce their 1024-entry segments of a stage into the same per-(row, chunk,
 // warp) partials as phase_stats, then thread 0 refills the stage with the CTA's item
 // S further on.  Bytes in flight per SM no longer depend on registers.
-constexpr int kV1StagesBf16 = 6;   // 16 KB stages; with float32 rows, 3 stages of 32 KB
+constexpr int kV1StagesBf16 = 4;   // 16 KB stages; with float32 rows, 2 stages of 32 KB
 constexpr unsigned long long kV1WaitNs = kWaitLimitNs;
 // ring layout: full and empty mbarriers, the staged items' (b, row, chunk, entries),
 // then the stages (128-byte aligned)
@@ -688,7 +688,7 @@ __device__ __forceinline__ void phase_weights(const VerifyParams& p) {
 
 // Phase 3 with the rows staged by bulk copies (rows 16-byte aligned): CTA c's items
 // c, c + G, ... (request b, chunk c) go through slots of the phase-1 ring, one chunk
-// of the target row and one of the draft row per slot (three slots of bf16 rows), all
+// of the target row and one of the draft row per slot (two slots of bf16 rows), all
 // slots requested at once; the request states of the first items are loaded together.
 // The barriers are initialised again for this phase (phase 1 has no copy or arrival
 // pending on them).  Same per-entry arithmetic as phase_weights; each lane sums its
@@ -1035,7 +1035,8 @@ void verify_bind_workspace(VerifyParams& p, void* ws) {
 template <typename TT, typename DT>
 static cudaError_t launch_t1(const VerifyParams& p, cudaStream_t stream) {
     auto kern = verify_t1_kernel<TT, DT>;
-    // the bulk-copy ring of phase 1 (rows 16-byte aligned): 96 KB per CTA, two per SM
+    // the bulk-copy ring of phases 1 and 3 (rows 16-byte aligned): 64 KB per CTA, two per
+    // SM (128 KB in flight per SM streamed faster than 192 KB)
     const size_t smem = (p.vec_t && p.vec_d) ? kV1RingOffset + (size_t)kV1StagesBf16 * kVerifyChunk * 2 : 0;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
