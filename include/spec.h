@@ -275,6 +275,40 @@ spec_status spec_verify_noalloc(const void *target_logits, spec_dtype target_dty
                                 spec_stream_t stream);
 
 /*
+ * spec_verify_budget - how many draft positions of each request to verify.
+ *
+ * Defines: "Speculative Decoding Part 2: the evolution of drafter architectures" (VESSL
+ * AI), DSpark section, the paragraphs after the bias equation.  The confidence of a
+ * position (spec_draft_block's conf_out) is the probability that it passes given that
+ * every earlier position passed; the scheduler multiplies these into expected lengths
+ * and gives the verification budget to the most likely positions across the batch,
+ * maximising throughput against a measured cost curve.  The pages give no formula;
+ * the reading is:
+ *   P[b][j] = prod_{i <= j} c[b][i], each c clamped to [0, 1] and NaN read as 0,
+ *   computed in float64 in position order;
+ *   candidates (b, j) ordered by P descending, ties by b * gamma + j ascending (the
+ *   first k candidates hold a prefix of every request's positions);
+ *   E(k) = B + sum of the first k P: expected committed tokens with k positions
+ *   verified in all (each request commits its accepted drafts plus one token);
+ *   k* = the k in 0..budget with the largest E(k) / cost_us[k], the smallest on ties,
+ *   an entry that is not positive and finite left out (no usable entry: k* = 0); with
+ *   cost_us NULL, k* = budget;
+ *   gamma_out[b] = request b's positions among the first k*.
+ *
+ *   conf          float32 device [B, gamma].
+ *   budget        0 <= budget <= B * gamma: most positions verified in all.
+ *   cost_us       float32 device [budget + 1] or NULL: time to verify k positions.
+ *   gamma_out     int32 device [B].
+ *   expected_out  float32 device [1] or NULL: E(k*).
+ * Limits: 1 <= gamma <= SPEC_MAX_GAMMA, 1 <= B * gamma <= SPEC_MAX_BUDGET_CANDIDATES.
+ * Arguments are checked before anything is enqueued; one CTA does the work (no
+ * workspace, nothing allocated).
+ */
+#define SPEC_MAX_BUDGET_CANDIDATES 8192
+spec_status spec_verify_budget(const float *conf, int B, int gamma, int budget, const float *cost_us,
+                               int32_t *gamma_out, float *expected_out, spec_stream_t stream);
+
+/*
  * spec_e2etv - SpecOPD E2E-TV surrogate and its gradient.
  *
  * Defines ("SpecOPD" paper summary, onedev.kr, section "how to use it"; VESSL AI

@@ -145,6 +145,19 @@ def test_e2etv_argument_errors(lib):
     assert _e2etv(lib, wsb=100) == 9
 
 
+def test_verify_budget_argument_errors(lib):
+    def call(conf=A, B=4, gamma=7, budget=10, cost=A, gamma_out=A, expected=A):
+        return lib.spec_verify_budget(conf, B, gamma, budget, cost, gamma_out, expected, None)
+    assert call(conf=0) == 1
+    assert call(gamma_out=0) == 1
+    assert call(B=0) == 2
+    assert call(gamma=0) == 2
+    assert call(gamma=65) == 2
+    assert call(B=8193, gamma=1) == 2      # more than SPEC_MAX_BUDGET_CANDIDATES
+    assert call(budget=-1) == 2
+    assert call(budget=29) == 2            # more than B * gamma
+
+
 def test_workspace_init_rejects_missing(lib):
     assert lib.spec_workspace_init(None, 1 << 20, None) == 9
     assert lib.spec_workspace_init(A, 16, None) == 9

@@ -46,6 +46,7 @@ SIGNATURES = {
                                    _vp, _vp, _vp, _vp, _vp]),
     "spec_draft_verify": (_i32, [_vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _i32,
                                  _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "spec_verify_budget": (_i32, [_vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp]),
 }
 
 _lib = None
@@ -278,6 +279,28 @@ def draft_verify(logits, target, anchor, U=None, Wt=None, ws=None, out=None, str
         ws.numel(), _stream(stream))
     _check(code, "spec_draft_verify")
     out["ws"] = ws
+    return out
+
+
+def verify_budget(conf, budget, cost=None, out=None, stream=None):
+    """spec_verify_budget.  conf [B, gamma] float32 (spec_draft_block's conf); budget:
+    most draft positions verified in all; cost: float32 [budget + 1] time per total, or
+    None.  Returns a dict of device tensors: gamma [B] int32, expected [1] float32."""
+    torch = _torch()
+    lib = load()
+    _need(conf, "conf", None, torch.float32)
+    if conf.dim() != 2:
+        raise ValueError("conf must be [B, gamma]")
+    dev = conf.device
+    B, gamma = conf.shape
+    if cost is not None:
+        _need(cost, "cost", dev, torch.float32, (int(budget) + 1,))
+    if out is None:
+        out = dict(gamma=torch.empty((B,), dtype=torch.int32, device=dev),
+                   expected=torch.empty((1,), dtype=torch.float32, device=dev))
+    code = lib.spec_verify_budget(_ptr(conf), B, gamma, int(budget), _ptr(cost), _ptr(out["gamma"]),
+                                  _ptr(out.get("expected")), _stream(stream))
+    _check(code, "spec_verify_budget")
     return out
 
 

@@ -276,4 +276,14 @@ spec_status spec_e2etv(const uint16_t* target_logits, const uint16_t* draft_logi
     return cuda_status(e2etv_launch(p, workspace, (cudaStream_t)stream));
 }
 
+spec_status spec_verify_budget(const float* conf, int B, int gamma, int budget, const float* cost_us,
+                               int32_t* gamma_out, float* expected_out, spec_stream_t stream) {
+    if (!conf || !gamma_out) return SPEC_ERR_INVALID_ARG;
+    if (B < 1 || gamma < 1 || gamma > SPEC_MAX_GAMMA || (long)B * gamma > SPEC_MAX_BUDGET_CANDIDATES)
+        return SPEC_ERR_SHAPE;
+    if (budget < 0 || (long)budget > (long)B * gamma) return SPEC_ERR_SHAPE;
+    return cuda_status(verify_budget_launch(conf, B, gamma, budget, cost_us, gamma_out, expected_out,
+                                            (cudaStream_t)stream));
+}
+
 }  // extern "C"

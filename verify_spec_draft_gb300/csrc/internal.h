@@ -108,6 +108,9 @@ cudaError_t e2etv_launch(E2etvParams& p, void* ws, cudaStream_t stream);
 
 int device_sm_count();
 
+cudaError_t verify_budget_launch(const float* conf, int B, int gamma, int budget, const float* cost,
+                                 int32_t* gamma_out, float* expected_out, cudaStream_t stream);
+
 // Keeps e as the calling thread's last CUDA error (spec_last_cuda_error) and
 // returns SPEC_ERR_CUDA, or SPEC_OK for cudaSuccess.
 spec_status record_cuda_error(cudaError_t e);
