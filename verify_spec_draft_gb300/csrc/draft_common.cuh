@@ -558,66 +558,6 @@ __device__ void tile_phase_stream0(const DraftParams& p) {
             p.cta_rec[(size_t)row * gridDim.x + blockIdx.x] = rowacc_pack(rowacc_empty());
 }
 
-// T=0 finalize run by EVERY CTA over every row (so the next pass needs no second grid
-// barrier): the tokens go to this CTA's shared array `cur`; the CTA owning a row
-// (row % gridDim.x) writes its outputs, applying the chain rule (an invalid anchor or
-// position voids the rest of the request).  Returns whether any token differs from
-// `prev` (identical in every CTA, so all leave the pass loop together).
-__device__ __forceinline__ bool finalize_all_t0(const DraftParams& p, const float4* recs_all, const int32_t* prev,
-                                                int32_t* cur, bool compare, const int32_t* anc) {
-    const int R = p.B * p.gamma;
-    const int lane = threadIdx.x & 31;
-    const int nw = blockDim.x >> 5;
-    const int nblk = gridDim.x;
-    for (int row = threadIdx.x >> 5; row < R; row += nw) {
-        const float4* recs = recs_all + (size_t)row * nblk;
-        // every record load of the lane in flight at once (up to 256 CTAs), then merged
-        // in CTA order
-        float4 rv[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int c = lane + 32 * i;
-            rv[i] = c < nblk ? __ldcg(&recs[c]) : rowacc_pack(rowacc_empty());
-        }
-        RowAcc acc = rowacc_empty();
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc = rowacc_merge(acc, rowacc_unpack(rv[i]));
-        for (int c = lane + 256; c < nblk; c += 32) acc = rowacc_merge(acc, rowacc_unpack(__ldcg(&recs[c])));
-        acc = warp_rowacc(acc);
-        const bool valid = !acc.bad && acc.mx != -INFINITY;
-        if (lane == 0) cur[row] = valid ? acc.idx : -1;
-        if (lane == 0 && (row % nblk) == (int)blockIdx.x) {
-            // conf for the owner's output; the chain check needs every token, so the
-            // write happens after the barrier below
-            p.conf_out[row] = valid ? ex2(fmaf(acc.mx, kLog2e, -acc.mx * kLog2e)) / acc.s : NAN;
-        }
-    }
-    __syncthreads();
-    int diff = 0;
-    if (compare)
-        for (int row = threadIdx.x; row < R; row += blockDim.x) diff |= (cur[row] != prev[row]) ? 1 : 0;
-    const int changed = __syncthreads_or(diff);
-    // owners: tokens, q(x) = conf at T=0, chain validity and status flags
-    for (int row = blockIdx.x + nblk * (int)threadIdx.x; row < R; row += nblk * (int)blockDim.x) {
-        const int b = row / p.gamma, j = row % p.gamma;
-        const int a = anc[b];
-        bool dead = (a < 0 || a >= p.V);
-        int first_dead = dead ? 0 : -1;
-        for (int k = 0; k <= j && !dead; ++k)
-            if (cur[b * p.gamma + k] < 0) { dead = true; first_dead = k; }
-        if (dead) {
-            p.tokens_out[row] = -1;
-            p.conf_out[row] = NAN;
-            if (p.qtok_out) p.qtok_out[row] = NAN;
-            if (first_dead == j) atomicOr(p.status, (a < 0 || a >= p.V) ? SPEC_DEV_TOKEN : SPEC_DEV_NONFINITE);
-        } else {
-            p.tokens_out[row] = cur[row];
-            if (p.qtok_out) p.qtok_out[row] = p.conf_out[row];
-        }
-    }
-    return changed != 0;
-}
-
 // T=0 tokens from the folded argmax keys, in every CTA (one load per row): into the
 // shared array `cur`, and the row maxima into `cur_mx`; returns whether any token
 // differs from `prev` (the same in every CTA).

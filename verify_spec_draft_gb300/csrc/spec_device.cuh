@@ -53,19 +53,6 @@ __device__ __forceinline__ float load_one(const bf16_t* p) {
     return to_float((bf16_t)__ldg(reinterpret_cast<const unsigned short*>(p)));
 }
 
-// Loads N consecutive elements starting at element index `v` of a row of length V,
-// with -inf past the end.  `vec_ok` says rows are 16-byte aligned (V*sizeof(T) % 16
-// == 0 and an aligned base), so whole in-range groups can use one vector load.
-template <typename T, int N>
-__device__ __forceinline__ void load_group(const T* row, long v, long V, bool vec_ok, float (&o)[N]) {
-    if (vec_ok && v + N <= V) {
-        load_vec(row + v, o);
-    } else {
-#pragma unroll
-        for (int e = 0; e < N; ++e) o[e] = (v + e < V) ? load_one(row + v + e) : -INFINITY;
-    }
-}
-
 // A valid logit is finite or -inf; NaN and +inf are not.
 __device__ __forceinline__ bool bad_logit(float x) { return !(x < INFINITY); }
 
@@ -129,41 +116,6 @@ __device__ __forceinline__ unsigned long long argmax_key(float v, uint32_t idx) 
 __device__ __forceinline__ uint32_t key_index(unsigned long long k) { return ~(uint32_t)(k & 0xffffffffu); }
 __device__ __forceinline__ float key_value(unsigned long long k) { return order_float((uint32_t)(k >> 32)); }
 
-__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long k) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const unsigned long long t = __shfl_xor_sync(0xffffffffu, k, o);
-        k = t > k ? t : k;
-    }
-    return k;
-}
-
-// ---------------------------------------------------------------------------------
-// Softmax statistics: m = max, s = sum exp(x - m).  An empty set is (-inf, 0).
-// merge() is exact for m and rounds s; callers merge in a fixed order so results
-// are bit-reproducible.
-// ---------------------------------------------------------------------------------
-struct Stat { float m; float s; };
-
-__device__ __forceinline__ Stat stat_empty() { return Stat{-INFINITY, 0.0f}; }
-__device__ __forceinline__ Stat stat_merge(Stat a, Stat b) {
-    if (b.m == -INFINITY) return a;
-    if (a.m == -INFINITY) return b;
-    const float m = fmaxf(a.m, b.m);
-    return Stat{m, a.s * expf(a.m - m) + b.s * expf(b.m - m)};
-}
-__device__ __forceinline__ Stat warp_stat(Stat a) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        Stat b{__shfl_xor_sync(0xffffffffu, a.m, o), __shfl_xor_sync(0xffffffffu, a.s, o)};
-        // xor partners merge in opposite operand orders; order the pair by lane so
-        // both lanes compute the identical float result
-        const bool lower = (threadIdx.x & o) == 0;
-        a = lower ? stat_merge(a, b) : stat_merge(b, a);
-    }
-    return a;
-}
-
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -211,25 +163,6 @@ __device__ __forceinline__ float wexp(float x, float m2) { return ex2(fmaf(x, kL
 
 struct Stat2 { float m2; float s; };   // s = sum 2^(x*log2e - m2); empty: (-inf, 0)
 
-__device__ __forceinline__ Stat2 stat2_empty() { return Stat2{-INFINITY, 0.0f}; }
-__device__ __forceinline__ Stat2 stat2_merge(Stat2 a, Stat2 b) {
-    if (b.m2 == -INFINITY) return a;
-    if (a.m2 == -INFINITY) return b;
-    const float m = fmaxf(a.m2, b.m2);
-    return Stat2{m, a.s * ex2(a.m2 - m) + b.s * ex2(b.m2 - m)};
-}
-__device__ __forceinline__ Stat2 warp_stat2(Stat2 a) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const Stat2 b{__shfl_xor_sync(0xffffffffu, a.m2, o), __shfl_xor_sync(0xffffffffu, a.s, o)};
-        a = stat2_merge(a, b);   // symmetric: both lanes of a pair get the same bits
-    }
-    return a;
-}
-// log2 of the row's normaliser in the same base: LSE2 = m2 + log2(s); then the
-// probability of x is 2^(x*log2e - LSE2).
-__device__ __forceinline__ float stat2_lse2(Stat2 a) { return a.m2 + log2f(a.s); }
-
 // ---------------------------------------------------------------------------------
 // Memory-model helpers and the bounded barrier.
 // ---------------------------------------------------------------------------------
@@ -237,9 +170,6 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
     unsigned v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
-}
-__device__ __forceinline__ void st_release(unsigned* p, unsigned v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
 }
 __device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
     unsigned old;
@@ -250,22 +180,6 @@ __device__ __forceinline__ unsigned long long global_timer_ns() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
-}
-
-// Wait until *gen differs from `seen`, for at most kWaitLimitNs.  Returns false (and
-// sets SPEC_DEV_TIMEOUT in *status) if the limit ran out.  One thread calls it.
-__device__ __forceinline__ bool wait_generation(const unsigned* gen, unsigned seen, unsigned* status,
-                                                unsigned long long limit_ns) {
-    const unsigned long long t0 = global_timer_ns();
-    unsigned spins = 0;
-    while (ld_acquire(gen) == seen) {
-        if (((++spins) & 63u) == 0 && global_timer_ns() - t0 > limit_ns) {
-            atomicOr(status, SPEC_DEV_TIMEOUT);
-            return false;
-        }
-        __nanosleep(64);
-    }
-    return true;
 }
 
 __device__ __forceinline__ void red_add_release(unsigned* p, unsigned v) {
@@ -316,31 +230,6 @@ __device__ __forceinline__ bool grid_barrier_exit(const GridBarrier& gb, unsigne
         return true;
     }
     return false;
-}
-
-// Barrier over `nblocks` CTAs that are all resident (cooperative launch).  slot[0] is
-// the arrival count, slot[32] the generation (separate 128-byte lines).  The last
-// CTA to arrive resets the count and bumps the generation; the count is back at 0
-// when the barrier completes.  Returns false on timeout; the kernel must then exit.
-__device__ __forceinline__ bool block_barrier(unsigned* slot, unsigned nblocks, unsigned* status) {
-    __shared__ int s_ok;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        unsigned* count = slot;
-        unsigned* gen = slot + 32;
-        const unsigned seen = ld_acquire(gen);
-        const unsigned arrived = atom_add_acq_rel(count, 1u) + 1u;
-        bool ok = true;
-        if (arrived == nblocks) {
-            atomicExch(count, 0u);
-            st_release(gen, seen + 1u);
-        } else {
-            ok = wait_generation(gen, seen, status, kWaitLimitNs);
-        }
-        s_ok = ok ? 1 : 0;
-    }
-    __syncthreads();
-    return s_ok != 0;
 }
 
 __device__ __forceinline__ int ld_relaxed_i32(const int32_t* p) {
