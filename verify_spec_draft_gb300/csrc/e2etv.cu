@@ -177,9 +177,13 @@ __device__ __forceinline__ void sweep_overlap(const bf16_t* tr, const bf16_t* dr
 // accumulators.  Same results up to the order of float additions.
 template <int B, bool STAGED>
 __device__ __forceinline__ void slice_stats(const bf16_t* row, int ncol, Stat2& out, int& bad, uint64_t pol) {
+    // one pass: each lane keeps a running maximum m2 (base 2) and rescales its sums
+    // when a batch raises it; the lanes' (m2, s) are merged at the end
     const int lane = threadIdx.x & 31;
     const uint32_t ninf = 0xff80ff80u;
-    uint32_t mx2 = ninf;
+    float m2 = -INFINITY;
+    float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+    int lbad = 0;
     for (int k0 = lane * 8; k0 < ncol; k0 += 256 * B) {
         uint4 w[B];
 #pragma unroll
@@ -187,37 +191,33 @@ __device__ __forceinline__ void slice_stats(const bf16_t* row, int ncol, Stat2& 
             const int k = k0 + 256 * g;
             w[g] = k < ncol ? ld16p<STAGED>(row + k, pol) : make_uint4(ninf, ninf, ninf, ninf);
         }
+        uint32_t mx2 = ninf;
 #pragma unroll
         for (int g = 0; g < B; ++g) mx2 = bmax2(mx2, bmax2(bmax2(w[g].x, w[g].y), bmax2(w[g].z, w[g].w)));
-    }
-    float m = fmaxf(lo_bf(mx2), hi_bf(mx2));
-    if (isnan(lo_bf(mx2)) || isnan(hi_bf(mx2))) m = NAN;
+        const float bl = lo_bf(mx2), bh = hi_bf(mx2);
+        const float bm = fmaxf(bl, bh);
+        if (isnan(bl) || isnan(bh) || bm == INFINITY) lbad = 1;
+        if (lbad || bm == -INFINITY) continue;   // a batch of -inf adds nothing
+        const float bm2 = bm * kLog2e;
+        if (bm2 > m2) {
+            const float r = ex2(m2 - bm2);          // 0 when m2 was -inf
+            s0 *= r; s1 *= r; s2 *= r; s3 *= r;
+            m2 = bm2;
+        }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float y = __shfl_xor_sync(0xffffffffu, m, o);
-        m = (isnan(m) || isnan(y)) ? NAN : fmaxf(m, y);
-    }
-    bad = (isnan(m) || m == INFINITY) ? 1 : 0;
-    float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
-    const float m2 = m * kLog2e;
-    if (!bad && m != -INFINITY) {
-        for (int k0 = lane * 8; k0 < ncol; k0 += 256 * B) {
-            uint4 w[B];
-#pragma unroll
-            for (int g = 0; g < B; ++g) {
-                const int k = k0 + 256 * g;
-                w[g] = k < ncol ? ld16p<STAGED>(row + k, pol) : make_uint4(ninf, ninf, ninf, ninf);
-            }
-#pragma unroll
-            for (int g = 0; g < B; ++g) {   // -inf padding contributes 2^-inf = 0
-                s0 += ex2(fmaf(lo_bf(w[g].x), kLog2e, -m2)) + ex2(fmaf(hi_bf(w[g].x), kLog2e, -m2));
-                s1 += ex2(fmaf(lo_bf(w[g].y), kLog2e, -m2)) + ex2(fmaf(hi_bf(w[g].y), kLog2e, -m2));
-                s2 += ex2(fmaf(lo_bf(w[g].z), kLog2e, -m2)) + ex2(fmaf(hi_bf(w[g].z), kLog2e, -m2));
-                s3 += ex2(fmaf(lo_bf(w[g].w), kLog2e, -m2)) + ex2(fmaf(hi_bf(w[g].w), kLog2e, -m2));
-            }
+        for (int g = 0; g < B; ++g) {   // -inf entries contribute 2^-inf = 0
+            s0 += ex2(fmaf(lo_bf(w[g].x), kLog2e, -m2)) + ex2(fmaf(hi_bf(w[g].x), kLog2e, -m2));
+            s1 += ex2(fmaf(lo_bf(w[g].y), kLog2e, -m2)) + ex2(fmaf(hi_bf(w[g].y), kLog2e, -m2));
+            s2 += ex2(fmaf(lo_bf(w[g].z), kLog2e, -m2)) + ex2(fmaf(hi_bf(w[g].z), kLog2e, -m2));
+            s3 += ex2(fmaf(lo_bf(w[g].w), kLog2e, -m2)) + ex2(fmaf(hi_bf(w[g].w), kLog2e, -m2));
         }
     }
-    out = Stat2{(bad || m == -INFINITY) ? -INFINITY : m2, warp_sum((s0 + s1) + (s2 + s3))};
+    bad = warp_or(lbad);
+    const float M = warp_max(m2);
+    float s = 0.0f;
+    if (!bad && M != -INFINITY && m2 != -INFINITY) s = ((s0 + s1) + (s2 + s3)) * ex2(m2 - M);
+    s = warp_sum(s);
+    out = Stat2{(bad || M == -INFINITY) ? -INFINITY : M, s};
 }
 
 template <int B, bool STAGED>
