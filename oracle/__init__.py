@@ -18,6 +18,9 @@ the pages step by step, in their order and notation:
   (T=0) or rejection sampling with a residual/bonus draw (T=1).
 * ``e2etv``   - the SpecOPD E2E-TV surrogate: overlap 1-TV, prefix survival products,
   their mean, and the gradient with respect to the draft logits.
+* ``anchors`` - the SpecOPD anchor-branch plan: distinct random anchors on each
+  reference response, the anchor tokens, and the parent map and semantic positions
+  that pack the drafted branches into one proposal tree.
 * ``schedule`` - the DSpark verify budget: per-request pass products of the confidences,
   the budget given to the most likely positions across the batch, the throughput
   against a cost curve.
@@ -26,4 +29,4 @@ Pins (tests that tie each function to the pages or to mathematics rather than to
 itself) live in ``tests/test_oracle_*.py``; each function's docstring names them.
 """
 
-from . import philox, draft, verify, e2etv, schedule  # noqa: F401
+from . import philox, draft, verify, e2etv, schedule, anchors  # noqa: F401

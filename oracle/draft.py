@@ -64,10 +64,12 @@ def draft_step(l_row, x_prev, U, Wt, temperature, u):
     return dict(x=x, conf=1.0 / Z, qtok=float(p[x]), near=bool(near), z=z)
 
 
-def draft_block(logits, anchor, U, Wt, temperature, seeds, return_z=False):
+def draft_block(logits, anchor, U, Wt, temperature, seeds, return_z=False, first_b=0):
     """Run the sequential chain for every request.
 
     logits [B, gamma, V]; anchor [B]; U, Wt [V, r] (or None); seeds [B] uint64.
+    ``first_b`` is the index of request 0 in the whole batch (the Philox counter's
+    request index), so that a slice of a batch can be replayed on its own.
     Returns dict with tokens [B, gamma] (int64), conf, qtok [B, gamma] (float64),
     near [B, gamma] (bool), valid [B] (bool) and, if ``return_z``, z [B, gamma, V].
     A request whose row j is invalid (see ``_rows``), or whose anchor lies outside
@@ -87,7 +89,7 @@ def draft_block(logits, anchor, U, Wt, temperature, seeds, return_z=False):
     for b in range(B):
         x_prev = int(anchor[b])
         for j in range(1, gamma + 1):
-            u = philox.uniform(int(seeds[b]), b, j, philox.STREAM_DRAFT) if temperature else 0.0
+            u = philox.uniform(int(seeds[b]), first_b + b, j, philox.STREAM_DRAFT) if temperature else 0.0
             step = draft_step(L[b, j - 1], x_prev, U, Wt, temperature, u)
             if return_z:
                 zs[b, j - 1] = step["z"]
