@@ -428,6 +428,51 @@ def secondary(args, torch, vsd, synth, dev, hbm, hbm_kind, sampler):
     del t, d, inp, o
     torch.cuda.empty_cache()
 
+    # the SpecOPD anchor-branch sampler: 16 references x 64 anchors, W = 7, V = 248320,
+    # r = 256, T = 1: the plan, then the draft block over the 1024 branches (3.56 GB of
+    # drafter rows, more than L2), several tcgen05 launches of 36 branches each
+    c = synth.BRANCH_CONFIG
+    x = c.extra
+    inp = synth.branch_inputs(x["n_refs"], x["n_anchors"], c.gamma, c.V, c.r, x["Lmax"], c.dtype, c.seed, dev)
+    nb = x["n_refs"] * x["n_anchors"]
+    op = vsd.branch_plan(inp["trunk"], inp["lengths"], x["n_anchors"], c.gamma, c.seed)
+    anchor = op["anchor_tok"].view(-1)
+    wsd = vsd.workspace(vsd.OP_DRAFT, nb, c.gamma, c.V, c.r, dev)
+    ob = vsd.draft_block(inp["logits"], anchor, inp["U"], inp["Wt"], 1, inp["seeds"], ws=wsd)
+
+    def sampler_step():
+        vsd.branch_plan(inp["trunk"], inp["lengths"], x["n_anchors"], c.gamma, c.seed, ws=op["ws"], out=op)
+        vsd.draft_block(inp["logits"], anchor, inp["U"], inp["Wt"], 1, inp["seeds"], ws=wsd, out=ob)
+
+    fn, graphed = capture(sampler_step, torch)
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    steps6 = max(5, min(args.steps, 30))
+    sampler.active = True
+    total, _ = time_steps(torch, fn, steps6)
+    sampler.active = False
+    ms = sum(total) / len(total)
+    passes = int(ob["passes"].item())
+    per_launch = 256 // c.gamma
+    launches = 1 + (nb + per_launch - 1) // per_launch
+    # algorithmic: the drafter rows once, W once per biased pass, the outputs
+    byts = nb * c.gamma * c.V * 2 + passes * c.V * c.r * 2
+    ach = byts / (ms * 1e-3) / 1e9
+    out["anchor_branches"] = {
+        "workload": "SpecOPD anchor-branch sampler: 16 refs x 4096 tokens, 64 anchors each, W=7, V=248320, "
+                    "r=256 bf16, T=1 (plan + draft block over 1024 branches)",
+        "value": nb / (ms * 1e-3), "unit": "branches/s", "ms_per_step": ms, "cuda_graphs": graphed,
+        "passes": passes, "draft_launches_per_step": launches - 1,
+        "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "peak_kind": hbm_kind, "unit": "GB/s",
+                     "frac": ach / hbm, "frac_of_nominal_8tbs": ach / NOMINAL_HBM_GBS,
+                     "algorithmic_bytes_per_launch": byts,
+                     "note": "per step; W is read by each of the draft launches, counted once per pass"},
+        "gpu_launches": launches * steps6,
+    }
+    del inp, ob, wsd
+    torch.cuda.empty_cache()
+
     # the verify budget across a batch: B=32 requests, gamma=16 confidences in [0.4, 1),
     # budget 256 positions, a linear cost curve; a few KB of input, L2 flushed between
     # steps

@@ -79,7 +79,13 @@ typedef enum {
 
 typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
 
-typedef enum { SPEC_OP_DRAFT = 0, SPEC_OP_VERIFY = 1, SPEC_OP_E2ETV = 2, SPEC_OP_DRAFT_VERIFY = 3 } spec_op;
+typedef enum {
+    SPEC_OP_DRAFT = 0,
+    SPEC_OP_VERIFY = 1,
+    SPEC_OP_E2ETV = 2,
+    SPEC_OP_DRAFT_VERIFY = 3,
+    SPEC_OP_BRANCH_PLAN = 4
+} spec_op;
 
 /* Device status flags (OR-ed into the workspace status word). */
 #define SPEC_DEV_TIMEOUT 1u
@@ -90,12 +96,18 @@ typedef enum { SPEC_OP_DRAFT = 0, SPEC_OP_VERIFY = 1, SPEC_OP_E2ETV = 2, SPEC_OP
 #define SPEC_MAX_GAMMA 64      /* draft positions per request                      */
 #define SPEC_MAX_RANK 256      /* Markov rank r                                    */
 #define SPEC_MAX_V (1 << 26)   /* vocabulary size                                  */
+#define SPEC_MAX_DRAFT_ROWS (1 << 20)   /* spec_draft_block: B * gamma             */
+#define SPEC_MAX_TRUNK 16384   /* spec_branch_plan: tokens of one reference        */
 
 /*
  * spec_workspace_bytes - workspace size for one operation (host only, pure).
  *   op     SPEC_OP_DRAFT / SPEC_OP_VERIFY / SPEC_OP_DRAFT_VERIFY: B requests, gamma
  *          positions, V, r.
  *          SPEC_OP_E2ETV: B = number of branches, gamma = branch length Wb, r unused.
+ *          SPEC_OP_BRANCH_PLAN: the status word only (pass B = references, gamma =
+ *          W, V = Lmax, r = 0).
+ *          For SPEC_OP_DRAFT the size covers one launch's slice of requests, which
+ *          spec_draft_block reuses across the slices of a larger batch.
  * Returns 0 for arguments outside the supported ranges.
  */
 size_t spec_workspace_bytes(spec_op op, int B, int gamma, int V, int r);
@@ -153,8 +165,13 @@ const char *spec_last_cuda_error_string(void);
  *   passes_out    [1] int32, fixed-point passes over W used (nullable).
  * A request whose anchor lies outside [0, V), or whose row j is invalid, gets
  * tokens -1 and NaN statistics from that position on (flags TOKEN / NONFINITE).
+ * A batch larger than one launch takes (256 rows on the tensor-core path: bf16
+ * weights with r a multiple of 64; 4096 rows otherwise) runs as consecutive launches
+ * over slices of requests on `stream`; results are those of one call (the Philox
+ * request index b is the request's index in the whole batch), and passes_out is the
+ * largest over the slices.
  * Limits: 1 <= gamma <= SPEC_MAX_GAMMA, 0 <= r <= SPEC_MAX_RANK, 1 <= V <= SPEC_MAX_V,
- * 1 <= B*gamma <= 4096.
+ * 1 <= B*gamma <= SPEC_MAX_DRAFT_ROWS.
  */
 spec_status spec_draft_block(const void *draft_logits, spec_dtype logits_dtype,
                              const int32_t *anchor, const void *U, const void *Wt,
@@ -332,6 +349,43 @@ spec_status spec_e2etv(const uint16_t *target_logits, const uint16_t *draft_logi
                        int n_branches, int Wb, int V, float *a_out, float *surv_out,
                        float *loss_out, uint16_t *grad_out, void *workspace,
                        size_t workspace_bytes, spec_stream_t stream);
+
+/*
+ * spec_branch_plan - SpecOPD anchor-branch plan: anchors on each reference response,
+ * and the metadata that packs the branches drafted from them into one proposal tree.
+ *
+ * Defines ("SpecOPD" paper summary, onedev.kr, section "how it works": n anchors
+ * picked at random on the reference, a branch of W tokens drafted from each,
+ * independently; section "how it differs": the branches packed into a proposal tree,
+ * each node seeing its own reference prefix and branch history through a parent map,
+ * with rotary positions from semantic positions).  The pages give no formula; the
+ * reading is:
+ *   anchors of reference r (length L_r): the n distinct positions of 0..L_r-1 with
+ *   the smallest (key, position), key = word0 >> 40 of Philox4x64-10 with key
+ *   (seed, 0) and counter (r, i, 4, 0); every n-subset is equally likely; listed in
+ *   ascending position;
+ *   packing of reference r: trunk tokens are nodes 0..L_r-1 (node i's parent is
+ *   i-1); branch k, step t = 1..W is node L_r + k*W + t-1, its parent a_k when t = 1
+ *   and the node before otherwise, its semantic position a_k + t.
+ * The branch tokens come from spec_draft_block with B = n_refs * n_anchors,
+ * gamma = W, anchor = anchor_tok_out and the drafter's logits for each anchor.
+ *
+ *   trunk_tokens    int32 device [n_refs, Lmax].
+ *   lengths         int32 device [n_refs], L_r.
+ *   anchors_out     int32 device [n_refs, n_anchors]: a_k.
+ *   anchor_tok_out  int32 device [n_refs, n_anchors]: trunk token at a_k (x_0).
+ *   parent_out      int32 device [n_refs, n_anchors * W]: parent node of each branch
+ *                   node, (k, t) at k*W + t-1.
+ *   position_out    int32 device [n_refs, n_anchors * W]: semantic positions.
+ *   workspace       spec_workspace_bytes(SPEC_OP_BRANCH_PLAN, ...) (the status word).
+ * A reference with L_r < n_anchors or L_r > Lmax gets -1 everywhere (flag TOKEN).
+ * Limits: 1 <= n_refs <= 65535, 1 <= n_anchors <= Lmax <= SPEC_MAX_TRUNK,
+ * 1 <= W <= SPEC_MAX_GAMMA.
+ */
+spec_status spec_branch_plan(const int32_t *trunk_tokens, const int32_t *lengths, int n_refs,
+                             int Lmax, int n_anchors, int W, uint64_t seed, int32_t *anchors_out,
+                             int32_t *anchor_tok_out, int32_t *parent_out, int32_t *position_out,
+                             void *workspace, size_t workspace_bytes, spec_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -63,7 +63,10 @@ def test_workspace_bytes_ranges(lib):
     assert wb(vsd.OP_VERIFY, 1, 65, 100, 0) == 0
     assert wb(vsd.OP_VERIFY, 1, 7, 0, 0) == 0
     assert wb(vsd.OP_DRAFT, 1, 7, 100, 257) == 0
-    assert wb(vsd.OP_DRAFT, 4097, 1, 100, 8) == 0
+    assert wb(vsd.OP_DRAFT, (1 << 20) + 1, 1, 100, 8) == 0
+    # a batch beyond one launch needs one slice's workspace (4096 rows at most)
+    assert wb(vsd.OP_DRAFT, 1024, 7, 248320, 256) == wb(vsd.OP_DRAFT, 4096 // 7, 7, 248320, 256)
+    assert wb(vsd.OP_BRANCH_PLAN, 16, 7, 4096, 0) > 0
     assert wb(vsd.OP_E2ETV, 1 << 20, 64, 8, 0) == 0
     assert wb(7, 1, 1, 1, 0) == 0
     # bigger problems never need less workspace
@@ -89,7 +92,7 @@ def test_draft_argument_errors(lib):
     assert _draft(lib, gamma=0) == 2
     assert _draft(lib, gamma=65) == 2
     assert _draft(lib, r=257) == 2
-    assert _draft(lib, B=4097, gamma=1) == 2
+    assert _draft(lib, B=(1 << 20) + 1, gamma=1) == 2
     assert _draft(lib, V=0) == 2
     assert _draft(lib, logits=MIS) == 4
     assert _draft(lib, Wt=MIS) == 4
@@ -156,6 +159,21 @@ def test_verify_budget_argument_errors(lib):
     assert call(B=8193, gamma=1) == 2      # more than SPEC_MAX_BUDGET_CANDIDATES
     assert call(budget=-1) == 2
     assert call(budget=29) == 2            # more than B * gamma
+
+
+def test_branch_plan_argument_errors(lib):
+    def call(trunk=A, lengths=A, R=4, Lmax=100, n=8, W=7, anchors=A, tok=A, parent=A, pos=A, ws=A, wsb=1 << 20):
+        return lib.spec_branch_plan(trunk, lengths, R, Lmax, n, W, 5, anchors, tok, parent, pos, ws, wsb, None)
+    assert call(trunk=0) == 1
+    assert call(parent=0) == 1
+    assert call(R=0) == 2
+    assert call(Lmax=16385) == 2           # more than SPEC_MAX_TRUNK
+    assert call(n=0) == 2
+    assert call(n=101) == 2                # more anchors than positions
+    assert call(W=0) == 2
+    assert call(W=65) == 2
+    assert call(ws=0) == 9
+    assert call(wsb=16) == 9
 
 
 def test_workspace_init_rejects_missing(lib):

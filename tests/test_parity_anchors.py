@@ -1,0 +1,120 @@
+"""spec_branch_plan and spec_draft_block over many branches, on the GPU, against the
+oracle (oracle/anchors.py, oracle/draft.py).
+
+The plan is integer work: anchors, anchor tokens, parents and positions must be
+identical.  A draft batch larger than one launch runs as several launches; its tokens
+must be the oracle's for the whole batch (the Philox request index is the index in the
+batch), bit for bit except at a flagged near-tie, after which that request is not
+compared further; confidences agree to 1e-5.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import verify_spec_draft_gb300 as vsd
+from verify_spec_draft_gb300 import synth
+from oracle import anchors as oa, draft as od
+
+pytestmark = pytest.mark.gpu
+
+
+def _plan_check(trunk, lengths, n, W, seed):
+    dev = torch.device("cuda")
+    out = vsd.branch_plan(trunk.to(dev), lengths.to(dev), n, W, seed)
+    torch.cuda.synchronize()
+    ref = oa.plan(trunk.numpy(), lengths.numpy(), n, W, seed)
+    for k in ("anchors", "anchor_tok", "parent", "position"):
+        assert (out[k].cpu().numpy() == ref[k]).all(), k
+    return out
+
+
+@pytest.mark.parametrize("R,Lmax,n,W", [(1, 1, 1, 1), (3, 1000, 1000, 2), (4, 300, 17, 7), (2, 16384, 64, 7),
+                                        (5, 777, 64, 64)])
+def test_plan_matches_oracle(spec, R, Lmax, n, W):
+    g = torch.Generator().manual_seed(R * 7 + n)
+    trunk = torch.randint(0, 248320, (R, Lmax), generator=g, dtype=torch.int32)
+    lengths = torch.full((R,), Lmax, dtype=torch.int32)
+    out = _plan_check(trunk, lengths, n, W, seed=R + Lmax)
+    assert vsd.device_status(out["ws"]) == 0
+
+
+def test_plan_ragged_and_short_references(spec):
+    g = torch.Generator().manual_seed(3)
+    trunk = torch.randint(0, 1000, (5, 500), generator=g, dtype=torch.int32)
+    lengths = torch.tensor([500, 40, 12, 501, 233], dtype=torch.int32)   # 12 < n; 501 > Lmax
+    out = _plan_check(trunk, lengths, 16, 3, seed=11)
+    a = out["anchors"].cpu()
+    assert (a[2] == -1).all() and (a[3] == -1).all()
+    assert (a[1] < 40).all() and (a[4] < 233).all()
+    assert vsd.device_status(out["ws"]) & vsd.DEV_TOKEN
+
+
+def _draft_check(out, L, anchor, U, Wt, T, seeds, rows, first=None):
+    """Compare the requests `rows` (indices in the batch) with the oracle."""
+    tok = out["tokens"].cpu().numpy()
+    conf = out["conf"].cpu().numpy()
+    Un = None if U is None else U.double().cpu().numpy()
+    Wn = None if Wt is None else Wt.double().cpu().numpy()
+    compared = 0
+    for b in rows:
+        ref = od.draft_block(L[b:b + 1].double().cpu().numpy(), anchor[b:b + 1].cpu().numpy(), Un, Wn, T,
+                             seeds[b:b + 1].cpu().numpy(), first_b=b)
+        for j in range(tok.shape[1]):
+            if tok[b, j] != ref["tokens"][0, j]:
+                assert ref["near"][0, j], (b, j, tok[b, j], ref["tokens"][0, j])
+                break   # the chain diverges legitimately from here
+            assert abs(conf[b, j] - ref["conf"][0, j]) <= 1e-5, (b, j)
+            compared += 1
+    return compared
+
+
+@pytest.mark.parametrize("T", [0, 1])
+def test_batched_draft_tensor_cores(spec, T):
+    """40 requests x 7 = 280 rows: two launches of the tcgen05 kernel (36 + 4 requests)."""
+    B, G, V, r = 40, 7, 2000, 64
+    L, _ = synth.target_and_draft(B, G - 1, V, "zipf", 0.0, torch.bfloat16, seed=21)
+    L = L[:, :G].contiguous()
+    U, Wt = synth.markov_weights(V, r, torch.bfloat16, seed=21, scale=0.5)
+    anchor = synth.anchors(B, V, seed=21)
+    seeds = synth.seeds_for(B, 5)
+    dev = torch.device("cuda")
+    out = vsd.draft_block(L.to(dev), anchor.to(dev), U.to(dev), Wt.to(dev), T, seeds.to(dev))
+    torch.cuda.synchronize()
+    assert _draft_check(out, L, anchor, U, Wt, T, seeds, range(B)) >= B * G - 2 * G
+    assert 1 <= int(out["passes"].item()) <= G
+    assert vsd.device_status(out["ws"]) == 0
+
+
+def test_batched_draft_cuda_cores(spec):
+    """float32 weights, 600 requests x 7 = 4200 rows: two launches of the CUDA-core
+    kernel (585 + 15 requests); sampled requests on both sides of the cut."""
+    B, G, V, r = 600, 7, 300, 4
+    L, _ = synth.target_and_draft(B, G - 1, V, "gaussian", 0.0, torch.float32, seed=22)
+    L = L[:, :G].contiguous()
+    U, Wt = synth.markov_weights(V, r, torch.float32, seed=22, scale=0.5)
+    anchor = synth.anchors(B, V, seed=22)
+    seeds = synth.seeds_for(B, 9)
+    dev = torch.device("cuda")
+    out = vsd.draft_block(L.to(dev), anchor.to(dev), U.to(dev), Wt.to(dev), 1, seeds.to(dev))
+    torch.cuda.synchronize()
+    rows = [0, 1, 300, 583, 584, 585, 586, 599]
+    assert _draft_check(out, L, anchor, U, Wt, 1, seeds, rows) >= len(rows) * G - 2 * G
+
+
+def test_sampler_full_size_sampled(spec):
+    """16 references x 64 anchors, W = 7, V = 248320, r = 256, T = 1, as the benchmark
+    times it: the plan in full, sampled branches of the draft against the oracle."""
+    c = synth.BRANCH_CONFIG
+    x = c.extra
+    dev = torch.device("cuda")
+    inp = synth.branch_inputs(x["n_refs"], x["n_anchors"], c.gamma, c.V, c.r, x["Lmax"], c.dtype, c.seed, dev)
+    plan = _plan_check(inp["trunk"].cpu(), inp["lengths"].cpu(), x["n_anchors"], c.gamma, c.seed)
+    anchor = plan["anchor_tok"].reshape(-1)
+    out = vsd.draft_block(inp["logits"], anchor, inp["U"], inp["Wt"], 1, inp["seeds"])
+    torch.cuda.synchronize()
+    assert vsd.device_status(out["ws"]) == 0
+    tok = out["tokens"]
+    assert bool(((tok >= 0) & (tok < c.V)).all())
+    rows = [0, 35, 36, 511, 1000, 1023]   # both sides of a launch boundary
+    assert _draft_check(out, inp["logits"], anchor.cpu(), inp["U"], inp["Wt"], 1, inp["seeds"], rows) >= 30

@@ -25,7 +25,7 @@ STATUS = {
     8: "SPEC_ERR_TOKEN", 9: "SPEC_ERR_WORKSPACE",
 }
 F32, BF16 = 0, 1
-OP_DRAFT, OP_VERIFY, OP_E2ETV, OP_DRAFT_VERIFY = 0, 1, 2, 3
+OP_DRAFT, OP_VERIFY, OP_E2ETV, OP_DRAFT_VERIFY, OP_BRANCH_PLAN = 0, 1, 2, 3, 4
 DEV_TIMEOUT, DEV_NONFINITE, DEV_TOKEN = 1, 2, 4
 
 # C signatures of include/spec.h, as ctypes types
@@ -47,6 +47,8 @@ SIGNATURES = {
     "spec_draft_verify": (_i32, [_vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _i32,
                                  _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "spec_verify_budget": (_i32, [_vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp]),
+    "spec_branch_plan": (_i32, [_vp, _vp, _i32, _i32, _i32, _i32, ctypes.c_uint64, _vp, _vp, _vp, _vp,
+                                _vp, _sz, _vp]),
 }
 
 _lib = None
@@ -301,6 +303,33 @@ def verify_budget(conf, budget, cost=None, out=None, stream=None):
     code = lib.spec_verify_budget(_ptr(conf), B, gamma, int(budget), _ptr(cost), _ptr(out["gamma"]),
                                   _ptr(out.get("expected")), _stream(stream))
     _check(code, "spec_verify_budget")
+    return out
+
+
+def branch_plan(trunk, lengths, n_anchors, W, seed, ws=None, out=None, stream=None):
+    """spec_branch_plan.  trunk int32 [n_refs, Lmax] reference tokens; lengths int32
+    [n_refs].  Returns a dict of device tensors: anchors, anchor_tok [n_refs, n_anchors]
+    and parent, position [n_refs, n_anchors * W] (int32)."""
+    torch = _torch()
+    lib = load()
+    _need(trunk, "trunk", None, torch.int32)
+    if trunk.dim() != 2:
+        raise ValueError("trunk must be [n_refs, Lmax]")
+    dev = trunk.device
+    R, Lmax = trunk.shape
+    _need(lengths, "lengths", dev, torch.int32, (R,))
+    if out is None:
+        out = dict(anchors=torch.empty((R, n_anchors), dtype=torch.int32, device=dev),
+                   anchor_tok=torch.empty((R, n_anchors), dtype=torch.int32, device=dev),
+                   parent=torch.empty((R, n_anchors * W), dtype=torch.int32, device=dev),
+                   position=torch.empty((R, n_anchors * W), dtype=torch.int32, device=dev))
+    if ws is None:
+        ws = workspace(OP_BRANCH_PLAN, R, W, Lmax, 0, dev, stream)
+    code = lib.spec_branch_plan(_ptr(trunk), _ptr(lengths), R, Lmax, int(n_anchors), int(W), int(seed),
+                                _ptr(out["anchors"]), _ptr(out["anchor_tok"]), _ptr(out["parent"]),
+                                _ptr(out["position"]), _ptr(ws), ws.numel(), _stream(stream))
+    _check(code, "spec_branch_plan")
+    out["ws"] = ws
     return out
 
 

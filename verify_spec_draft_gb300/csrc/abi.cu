@@ -47,14 +47,17 @@ size_t spec_workspace_bytes(spec_op op, int B, int gamma, int V, int r) {
     if (B < 1 || gamma < 1 || gamma > SPEC_MAX_GAMMA || V < 1 || V > SPEC_MAX_V) return 0;
     switch (op) {
         case SPEC_OP_DRAFT:
-            if (r < 0 || r > SPEC_MAX_RANK || (long)B * gamma > 4096) return 0;
-            return draft_workspace_bytes(B, gamma, V, r);
+            // one launch's slice of requests at most (see spec_draft_block)
+            if (r < 0 || r > SPEC_MAX_RANK || (long)B * gamma > SPEC_MAX_DRAFT_ROWS) return 0;
+            return draft_workspace_bytes(B < kDraftMaxRows / gamma ? B : kDraftMaxRows / gamma, gamma, V, r);
         case SPEC_OP_VERIFY:
             if (B > 65535) return 0;
             return verify_workspace_bytes(B, gamma, V);
         case SPEC_OP_DRAFT_VERIFY:
             if (r < 0 || r > SPEC_MAX_RANK || (long)B * gamma > 4096) return 0;
             return draft_verify_workspace_bytes(B, gamma, V, r);
+        case SPEC_OP_BRANCH_PLAN:
+            return kWsHeaderBytes;   // the status word only
         case SPEC_OP_E2ETV:
             if ((long)B * gamma > (1L << 24)) return 0;
             return e2etv_workspace_bytes(B, gamma, V);
@@ -110,7 +113,7 @@ spec_status spec_draft_block(const void* draft_logits, spec_dtype logits_dtype, 
                              size_t workspace_bytes, spec_stream_t stream) {
     if (!dtype_ok(logits_dtype) || (r > 0 && !dtype_ok(w_dtype))) return SPEC_ERR_DTYPE;
     if (B < 1 || gamma < 1 || gamma > SPEC_MAX_GAMMA || V < 1 || V > SPEC_MAX_V || r < 0 || r > SPEC_MAX_RANK ||
-        (long)B * gamma > 4096)
+        (long)B * gamma > SPEC_MAX_DRAFT_ROWS)
         return SPEC_ERR_SHAPE;
     if (temperature != 0 && temperature != 1) return SPEC_ERR_INVALID_ARG;
     if (!draft_logits || !anchor || !tokens_out || !conf_out) return SPEC_ERR_INVALID_ARG;
@@ -119,8 +122,6 @@ spec_status spec_draft_block(const void* draft_logits, spec_dtype logits_dtype, 
     if (!aligned16(draft_logits) || (r > 0 && (!aligned16(U) || !aligned16(Wt))) ||
         (qlogits_out && !aligned16(qlogits_out)))
         return SPEC_ERR_ALIGN;
-    const size_t need = draft_workspace_bytes(B, gamma, V, r);
-    if (!workspace || workspace_bytes < need) return SPEC_ERR_WORKSPACE;
 
     DraftParams p;
     memset(&p, 0, sizeof(p));
@@ -143,8 +144,16 @@ spec_status spec_draft_block(const void* draft_logits, spec_dtype logits_dtype, 
     p.passes_out = passes_out;
     p.vec_l = ((size_t)V * dtype_size(logits_dtype)) % 16 == 0;
     p.vec_w = r > 0 && ((size_t)r * dtype_size(w_dtype)) % 16 == 0;
-    draft_bind_workspace(p, workspace);
-    return cuda_status(draft_launch(p, (cudaStream_t)stream));
+    // a batch larger than one launch runs as consecutive launches over slices of
+    // requests, each with the workspace of one slice
+    const int per = draft_requests_per_launch(p);
+    const size_t need = draft_workspace_bytes(per, gamma, V, r);
+    if (!workspace || workspace_bytes < need) return SPEC_ERR_WORKSPACE;
+    DraftParams bound = p;
+    bound.B = per;
+    draft_bind_workspace(bound, workspace);
+    bound.B = B;
+    return cuda_status(draft_launch_batched(bound, (cudaStream_t)stream));
 }
 
 spec_status spec_verify(const void* target_logits, spec_dtype target_dtype, const void* draft_logits,
@@ -284,6 +293,33 @@ spec_status spec_verify_budget(const float* conf, int B, int gamma, int budget, 
     if (budget < 0 || (long)budget > (long)B * gamma) return SPEC_ERR_SHAPE;
     return cuda_status(verify_budget_launch(conf, B, gamma, budget, cost_us, gamma_out, expected_out,
                                             (cudaStream_t)stream));
+}
+
+spec_status spec_branch_plan(const int32_t* trunk_tokens, const int32_t* lengths, int n_refs, int Lmax,
+                             int n_anchors, int W, uint64_t seed, int32_t* anchors_out, int32_t* anchor_tok_out,
+                             int32_t* parent_out, int32_t* position_out, void* workspace, size_t workspace_bytes,
+                             spec_stream_t stream) {
+    if (!trunk_tokens || !lengths || !anchors_out || !anchor_tok_out || !parent_out || !position_out)
+        return SPEC_ERR_INVALID_ARG;
+    if (n_refs < 1 || n_refs > 65535 || Lmax < 1 || Lmax > SPEC_MAX_TRUNK || n_anchors < 1 || n_anchors > Lmax ||
+        W < 1 || W > SPEC_MAX_GAMMA)
+        return SPEC_ERR_SHAPE;
+    if (!workspace || workspace_bytes < kWsHeaderBytes) return SPEC_ERR_WORKSPACE;
+    BranchPlanParams p;
+    memset(&p, 0, sizeof(p));
+    p.trunk = trunk_tokens;
+    p.lengths = lengths;
+    p.n_refs = n_refs;
+    p.Lmax = Lmax;
+    p.n_anchors = n_anchors;
+    p.W = W;
+    p.seed = seed;
+    p.anchors_out = anchors_out;
+    p.anchor_tok_out = anchor_tok_out;
+    p.parent_out = parent_out;
+    p.position_out = position_out;
+    p.status = &reinterpret_cast<WsHeader*>(workspace)->status;
+    return cuda_status(branch_plan_launch(p, (cudaStream_t)stream));
 }
 
 }  // extern "C"

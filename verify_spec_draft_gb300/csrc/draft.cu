@@ -52,7 +52,10 @@ __global__ void __launch_bounds__(kThreads) draft_kernel(DraftParams p) {
     grid_barrier_exit(gb, nb);
     if (blockIdx.x != 0) return;
     chain_fixup(p);
-    if (threadIdx.x == 0 && p.passes_out) *p.passes_out = biased ? pass : 0;
+    if (threadIdx.x == 0 && p.passes_out) {
+        if (p.passes_max) atomicMax(p.passes_out, biased ? pass : 0);
+        else *p.passes_out = biased ? pass : 0;
+    }
 }
 
 // ----------------------------------------------------------------------------------
@@ -144,6 +147,44 @@ cudaError_t draft_launch_tc(const DraftParams& p, cudaStream_t stream);
 cudaError_t draft_launch(const DraftParams& p, cudaStream_t stream) {
     if (draft_tc_supported(p)) return draft_launch_tc(p, stream);
     return draft_launch_cc(p, stream);
+}
+
+// A batch larger than one launch takes (256 rows on the tcgen05 kernel, kDraftMaxRows
+// on the CUDA-core kernel) runs as consecutive launches over slices of whole requests
+// on the same stream, reusing one slice's workspace: the requests are independent,
+// and b_base keeps each draw's Philox request index the one of the whole batch.
+int draft_requests_per_launch(const DraftParams& p) {
+    DraftParams q = p;
+    q.B = 256 / p.gamma > 0 ? 256 / p.gamma : 1;
+    const int per = draft_tc_supported(q) ? q.B : (kDraftMaxRows / p.gamma > 0 ? kDraftMaxRows / p.gamma : 1);
+    return p.B < per ? p.B : per;
+}
+
+cudaError_t draft_launch_batched(const DraftParams& p, cudaStream_t stream) {
+    const int per = draft_requests_per_launch(p);
+    if (per >= p.B) return draft_launch(p, stream);
+    DraftParams q = p;
+    if (p.passes_out) {
+        cudaError_t e = cudaMemsetAsync(p.passes_out, 0, sizeof(int32_t), stream);
+        if (e != cudaSuccess) return e;
+        q.passes_max = 1;
+    }
+    const size_t lsize = p.ldt == SPEC_BF16 ? 2 : 4;
+    for (int b0 = 0; b0 < p.B; b0 += per) {
+        const size_t rows = (size_t)b0 * p.gamma;
+        q.B = p.B - b0 < per ? p.B - b0 : per;
+        q.b_base = p.b_base + b0;
+        q.logits = static_cast<const char*>(p.logits) + rows * p.V * lsize;
+        q.anchor = p.anchor + b0;
+        q.seeds = p.seeds ? p.seeds + b0 : nullptr;
+        q.tokens_out = p.tokens_out + rows;
+        q.conf_out = p.conf_out + rows;
+        q.qtok_out = p.qtok_out ? p.qtok_out + rows : nullptr;
+        q.qlogits_out = p.qlogits_out ? p.qlogits_out + rows * p.V : nullptr;
+        cudaError_t e = draft_launch(q, stream);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace spec

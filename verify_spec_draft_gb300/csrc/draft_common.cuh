@@ -184,7 +184,7 @@ __device__ void finalize_rows(const DraftParams& p, int pass, bool use_bias, con
                 x = acc.idx;
                 qx = conf;
             } else {
-                const float u = philox_uniform(p.seeds[b], (uint64_t)b, (uint64_t)(j + 1), 0);
+                const float u = philox_uniform(p.seeds[b], (uint64_t)(p.b_base + b), (uint64_t)(j + 1), 0);
                 const float thr = u * S;
                 // level 1: CTA ranges, contiguous segments per lane
                 const int Kc = (nblk_tile + 31) / 32;

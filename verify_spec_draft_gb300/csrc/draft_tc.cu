@@ -541,7 +541,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int i = threadIdx.x; i < 3 * R; i += blockDim.x) p.keys[(size_t)i * kKeyStride] = 0ull;
     if (!ok || blockIdx.x != 0) return;
     if (p.temperature != 0) chain_fixup(p);   // T=0 owners applied the chain rule already
-    if (threadIdx.x == 0 && p.passes_out) *p.passes_out = pass;
+    if (threadIdx.x == 0 && p.passes_out) {
+        if (p.passes_max) atomicMax(p.passes_out, pass);
+        else *p.passes_out = pass;
+    }
 }
 
 // ----------------------------------------------------------------------------------

@@ -56,6 +56,8 @@ struct DraftParams {
     float* qtok_out;           // nullable
     float* qlogits_out;        // nullable
     int32_t* passes_out;       // nullable
+    int passes_max;            // 1: fold passes_out with atomicMax (a batch run as several launches)
+    int b_base;                // batch index of request 0 (the Philox counter's request index)
     int vec_l;                 // logits rows 16-byte aligned
     int vec_w;                 // weight rows 16-byte aligned
     int n_tiles;               // ceil(V / kDraftTile)
@@ -75,6 +77,11 @@ constexpr int kDraftTile = 128;   // vocabulary entries per tile
 size_t draft_workspace_bytes(int B, int gamma, int V, int r);
 void draft_bind_workspace(DraftParams& p, void* ws);
 cudaError_t draft_launch(const DraftParams& p, cudaStream_t stream);
+// spec_draft_block: requests per launch, and the batch as consecutive launches over
+// slices of that many requests (workspace bound for one slice)
+int draft_requests_per_launch(const DraftParams& p);
+cudaError_t draft_launch_batched(const DraftParams& p, cudaStream_t stream);
+constexpr int kDraftMaxRows = 4096;   // rows (requests x gamma) of one launch
 
 // spec_draft_verify: [draft workspace | verify workspace]
 size_t draft_verify_workspace_bytes(int B, int gamma, int V, int r);
@@ -105,6 +112,19 @@ struct E2etvParams {
 
 size_t e2etv_workspace_bytes(int n_branches, int Wb, int V);
 cudaError_t e2etv_launch(E2etvParams& p, void* ws, cudaStream_t stream);
+
+struct BranchPlanParams {
+    const int32_t* trunk;      // [n_refs, Lmax] token ids
+    const int32_t* lengths;    // [n_refs]
+    int n_refs, Lmax, n_anchors, W;
+    uint64_t seed;
+    int32_t* anchors_out;      // [n_refs, n_anchors]
+    int32_t* anchor_tok_out;   // [n_refs, n_anchors]
+    int32_t* parent_out;       // [n_refs, n_anchors * W]
+    int32_t* position_out;     // [n_refs, n_anchors * W]
+    unsigned* status;
+};
+cudaError_t branch_plan_launch(const BranchPlanParams& p, cudaStream_t stream);
 
 int device_sm_count();
 

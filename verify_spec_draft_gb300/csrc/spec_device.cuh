@@ -81,7 +81,8 @@ __device__ __forceinline__ float u4_max_nan(const uint4& w) {
 // ---------------------------------------------------------------------------------
 // Philox4x64-10 (Salmon, Moraes, Dror, Shaw, SC'11, section 3.2, table 2).
 // ---------------------------------------------------------------------------------
-__device__ __forceinline__ float philox_uniform(uint64_t seed, uint64_t b, uint64_t j, uint64_t stream) {
+// First output word for key (seed, 0) and counter (b, j, stream, 0).
+__device__ __forceinline__ uint64_t philox_word0(uint64_t seed, uint64_t b, uint64_t j, uint64_t stream) {
     const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
     const uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
     uint64_t c0 = b, c1 = j, c2 = stream, c3 = 0;
@@ -94,7 +95,10 @@ __device__ __forceinline__ float philox_uniform(uint64_t seed, uint64_t b, uint6
         const uint64_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
         c0 = n0; c1 = lo1; c2 = n2; c3 = lo0;
     }
-    return (float)(c0 >> 40) * 0x1p-24f;   // 24-bit uniform, exact in float32
+    return c0;
+}
+__device__ __forceinline__ float philox_uniform(uint64_t seed, uint64_t b, uint64_t j, uint64_t stream) {
+    return (float)(philox_word0(seed, b, j, stream) >> 40) * 0x1p-24f;   // 24-bit uniform, exact in float32
 }
 
 // ---------------------------------------------------------------------------------

@@ -134,6 +134,33 @@ def e2etv_rows(n_branches, Wb, V, sigma=1.0, dtype=torch.bfloat16, seed=0, devic
     return tgt.to(dtype).contiguous(), drf.to(dtype).contiguous()
 
 
+# The SpecOPD anchor-branch sampler (beyond the numbered configurations): 16 reference
+# responses of 4096 tokens (the pages give no length; 4096 is this workload's choice),
+# 64 anchors each, branches of W = 7 (the SpecOPD summary's 7 draft tokens), drafted at
+# T=1 with the rank-256 bias over V = 248,320; drafter rows from the zipf distribution.
+BRANCH_CONFIG = Config("anchor branches 16 refs x 64 anchors x W7 V248320 r256 bf16", 1024, 7, 248320, 256,
+                       torch.bfloat16, (1,), "zipf", 0.0, 1006,
+                       extra=dict(n_refs=16, n_anchors=64, Lmax=4096))
+
+
+def branch_inputs(n_refs, n_anchors, W, V, r, Lmax, dtype=torch.bfloat16, seed=0, device="cpu", dist="zipf",
+                  lengths=None):
+    """Inputs of the anchor-branch sampler: reference tokens [n_refs, Lmax] uniform in
+    [0, V), lengths [n_refs] (all Lmax unless given), drafter logits
+    [n_refs * n_anchors, W, V], Markov weights U, Wt [V, r] and per-branch seeds."""
+    g = generator(seed, device)
+    trunk = torch.randint(0, V, (n_refs, Lmax), generator=g, device=device, dtype=torch.int32)
+    if lengths is None:
+        lengths = torch.full((n_refs,), Lmax, dtype=torch.int32, device=device)
+    else:
+        lengths = torch.as_tensor(lengths, dtype=torch.int32).to(device)
+    B = n_refs * n_anchors
+    logits = _base_logits(B * W, V, dist, g, device).view(B, W, V).to(dtype).contiguous()
+    U, Wt = markov_weights(V, r, dtype, seed, device)
+    return dict(trunk=trunk.contiguous(), lengths=lengths.contiguous(), logits=logits, U=U, Wt=Wt,
+                seeds=seeds_for(B, seed, device))
+
+
 def config_inputs(cfg_id, device="cpu"):
     """All inputs of a numbered configuration (see CONFIGS)."""
     c = CONFIGS[cfg_id]
