@@ -135,12 +135,67 @@ __device__ __forceinline__ float bias_dot(const float* __restrict__ u, const WT*
     return acc;
 }
 
+// The bias of one tile's 128 entries for bf16 weight rows of r <= 256 values in whole
+// 16-byte words: lane l takes the rank slice [8l, 8l + 8) of every entry, so each
+// entry's Wt row is one coalesced warp load, kZBatch rows are in flight at once, and
+// the lanes' partial dot products are summed across the warp (the same bits in every
+// lane).  Lane l ends with the bias of entries 32i + l.
+constexpr int kZBatch = 8;
+__device__ __forceinline__ void tile_bias_bf16(const DraftParams& p, int tile, const float* u, float (&zb)[4]) {
+    const bf16_t* Wt = static_cast<const bf16_t*>(p.Wt);
+    const int lane = threadIdx.x & 31;
+    const bool has = lane < (p.r >> 3);
+    float uu[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) uu[e] = has ? u[lane * 8 + e] : 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float mine = 0.0f;
+#pragma unroll 1
+        for (int h = 0; h < 32 / kZBatch; ++h) {
+            const long base = (long)tile * kDraftTile + 32 * i + h * kZBatch;
+            uint4 w[kZBatch];
+#pragma unroll
+            for (int q = 0; q < kZBatch; ++q) {
+                w[q] = make_uint4(0u, 0u, 0u, 0u);
+                if (has && base + q < p.V)
+                    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                                 : "=r"(w[q].x), "=r"(w[q].y), "=r"(w[q].z), "=r"(w[q].w)
+                                 : "l"(Wt + (size_t)(base + q) * p.r + lane * 8));
+            }
+#pragma unroll
+            for (int q = 0; q < kZBatch; ++q) {
+                const uint32_t a[4] = {w[q].x, w[q].y, w[q].z, w[q].w};
+                float part = 0.0f;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    part = fmaf(uu[2 * k], __uint_as_float(a[k] << 16), part);
+                    part = fmaf(uu[2 * k + 1], __uint_as_float(a[k] & 0xffff0000u), part);
+                }
+                part = warp_sum(part);
+                if (lane == h * kZBatch + q) mine = part;
+            }
+        }
+        zb[i] = mine;
+    }
+}
+
 template <typename LT, typename WT>
 __device__ __forceinline__ void row_tile_z(const DraftParams& p, int row, int tile, bool use_bias,
                                            const float* u, float (&z)[4], long (&v)[4]) {
     const LT* lrow = static_cast<const LT*>(p.logits) + (size_t)row * p.V;
     const WT* Wt = static_cast<const WT*>(p.Wt);
     const int lane = threadIdx.x & 31;
+    if (sizeof(WT) == 2 && use_bias && p.vec_w && (p.r & 7) == 0 && p.r <= 256) {
+        float zb[4];
+        tile_bias_bf16(p, tile, u, zb);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[i] = (long)tile * kDraftTile + 32 * i + lane;
+            z[i] = v[i] < p.V ? load_one(lrow + v[i]) + zb[i] : -INFINITY;
+        }
+        return;
+    }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         v[i] = (long)tile * kDraftTile + 32 * i + lane;
@@ -481,6 +536,100 @@ __device__ void tile_phase_stream0_t0(const DraftParams& p, float4* rec_out, boo
             if (keys) red_max_u64(&keys[(size_t)row * kKeyStride], rec_key(a));
         }
     }
+}
+
+// Pass 0 at T=1 (unbiased rows): the per-(row, tile) records of the draw and one
+// record per (row, CTA).  A warp holds one row's slice of this CTA's tile range in
+// registers (at most kS1Units units of 32 x EPL entries), takes the slice maximum
+// with one warp reduction, then each tile's sum against it, so a tile costs only a
+// sum reduction over its lanes.  Records carry the slice maximum as their reference
+// (s = sum 2^(z log2e - fl(mx log2e))); no argmax is kept, since T=1 draws.  Returns
+// false (nothing done) when the slice is longer than kS1Units units.
+template <typename LT>
+__device__ __forceinline__ void unpack_word(const uint4& w, float (&x)[16 / sizeof(LT)]) {
+    if constexpr (sizeof(LT) == 2) {
+        const uint32_t a[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            x[2 * k] = __uint_as_float(a[k] << 16);
+            x[2 * k + 1] = __uint_as_float(a[k] & 0xffff0000u);
+        }
+    } else {
+        x[0] = __uint_as_float(w.x);
+        x[1] = __uint_as_float(w.y);
+        x[2] = __uint_as_float(w.z);
+        x[3] = __uint_as_float(w.w);
+    }
+}
+
+constexpr int kS1Units = 8;
+template <typename LT>
+__device__ bool tile_phase_stream0_t1(const DraftParams& p) {
+    constexpr int EPL = 16 / (int)sizeof(LT);          // entries per lane per unit
+    constexpr int UNIT = 32 * EPL;                     // entries per unit
+    constexpr int TPU = UNIT / kDraftTile;             // tiles per unit (1 or 2)
+    constexpr int LPT = 32 / TPU;                      // lanes per tile
+    const int R = p.B * p.gamma;
+    const int lane = threadIdx.x & 31;
+    const int nw = blockDim.x >> 5;
+    const int tb = tile_begin(blockIdx.x, gridDim.x, p.n_tiles), te = tile_begin(blockIdx.x + 1, gridDim.x, p.n_tiles);
+    const long e_begin = (long)tb * kDraftTile, e_end = (long)te * kDraftTile;
+    const int upr = (int)((e_end - e_begin + UNIT - 1) / UNIT);
+    if (upr > kS1Units) return false;
+    const uint4 ninf = sizeof(LT) == 2 ? make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u)
+                                       : make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
+    for (int row = (int)(threadIdx.x >> 5); row < R; row += nw) {
+        const LT* lrow = static_cast<const LT*>(p.logits) + (size_t)row * p.V;
+        uint4 w[kS1Units];
+#pragma unroll
+        for (int u = 0; u < kS1Units; ++u) {
+            const long e0 = e_begin + (long)u * UNIT + (long)lane * EPL;
+            w[u] = ninf;
+            if (u < upr && e0 < e_end && e0 + EPL <= p.V) w[u] = __ldg(reinterpret_cast<const uint4*>(lrow + e0));
+        }
+        float m = -INFINITY;
+        int bad = 0;
+#pragma unroll
+        for (int u = 0; u < kS1Units; ++u) {
+            float x[EPL];
+            unpack_word<LT>(w[u], x);
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) {
+                bad |= bad_logit(x[e]) ? 1 : 0;
+                m = fmaxf(m, x[e]);
+            }
+        }
+        m = warp_max(m);
+        bad = warp_or(bad);
+        const bool live = !bad && m != -INFINITY;
+        const float m2 = m * kLog2e;
+        float tot = 0.0f;
+#pragma unroll
+        for (int u = 0; u < kS1Units; ++u) {
+            if (u >= upr) break;
+            float sum = 0.0f;
+            if (live) {
+                float x[EPL];
+                unpack_word<LT>(w[u], x);
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) sum += wexp(x[e], m2);   // -inf entries add 0
+            }
+#pragma unroll
+            for (int o = LPT >> 1; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            tot += sum;
+            if ((lane & (LPT - 1)) == 0) {
+                const int t = (int)((e_begin + (long)u * UNIT) / kDraftTile) + lane / LPT;
+                if (t < te)
+                    p.tile_rec[(size_t)row * p.n_tiles + t] =
+                        rowacc_pack(RowAcc{live ? m : -INFINITY, live ? sum : 0.0f, 0x7fffffff, bad});
+            }
+        }
+        if (TPU == 2) tot += __shfl_xor_sync(0xffffffffu, tot, 16);
+        if (lane == 0)
+            p.cta_rec[(size_t)row * gridDim.x + blockIdx.x] =
+                rowacc_pack(RowAcc{live ? m : -INFINITY, live ? tot : 0.0f, 0x7fffffff, bad});
+    }
+    return true;
 }
 
 template <typename LT>

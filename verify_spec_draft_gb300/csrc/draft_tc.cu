@@ -207,7 +207,7 @@ __device__ __forceinline__ void named_barrier(int id, int nthreads) {
 
 // The tensor-core tile phase of one biased pass.  Pipeline counters persist across
 // passes in the registers of the thread that owns each role.
-template <int MT, typename LT>
+template <int MT, typename LT, int TT>
 __device__ bool tc_tile_phase(const DraftParams& p, const CUtensorMap* tmap, const int32_t* prev, const int32_t* anc,
                               float4* rec_out, const TcShared& sh, uint32_t tmem, uint32_t& it_p, uint32_t& it_m,
                               uint32_t& jt_m, uint32_t& jt_e, uint32_t& pre_issued, unsigned long long* keys) {
@@ -298,8 +298,8 @@ __device__ bool tc_tile_phase(const DraftParams& p, const CUtensorMap* tmap, con
         }
         const LT* lrow = static_cast<const LT*>(p.logits) + (size_t)(mine ? g : 0) * p.V;
         const bool write_z = p.qlogits_out != nullptr;
-        const bool keep_tiles = p.temperature == 1;
-        const bool want_idx = p.temperature == 0;
+        constexpr bool keep_tiles = TT == 1;
+        constexpr bool want_idx = TT == 0;
         const int col0 = cs * CPW;
         RowAcc run = rowacc_empty();
         // logits of this warp's columns of tile t, chunk c of tile t+1 requested as soon
@@ -382,7 +382,8 @@ __device__ bool tc_tile_phase(const DraftParams& p, const CUtensorMap* tmap, con
     return *(volatile int*)&s_fail == 0;
 }
 
-template <int MT, typename LT>
+// TT = the temperature (0 or 1): each kernel holds only its own temperature's code.
+template <int MT, typename LT, int TT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     draft_tc_kernel(const __grid_constant__ DraftParams p, const __grid_constant__ CUtensorMap tmap) {
     extern __shared__ uint8_t s_raw[];
@@ -397,7 +398,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     sh.a = base;
     sh.b = base + (size_t)MT * KB * kTcBlock;
     sh.slice_rec = reinterpret_cast<float4*>(sh.b + (size_t)S * kTcBlock);
-    const bool t1 = p.temperature == 1;
+    constexpr bool t1 = TT == 1;
     sh.tile_rec = t1 ? sh.slice_rec + 16 * 32 : nullptr;
     float* s_uw_all = reinterpret_cast<float*>(sh.slice_rec + (t1 ? 3 : 1) * 16 * 32);
     uint64_t* bars = reinterpret_cast<uint64_t*>(s_uw_all + (t1 ? (size_t)nw * p.r : 0));
@@ -462,7 +463,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // of pass j (j >= 2; all three are zero at launch, and the last CTA to leave
     // clears them again)
     auto key_buf = [&](int pass_) { return p.keys + (size_t)(pass_ % 3) * R * kKeyStride; };
-    if (p.temperature == 0) {
+    if constexpr (TT == 0) {
         // T=0: every CTA takes every row's token from the folded keys, so a pass needs
         // one grid barrier; only the last pass's confidences are merged, by the row
         // owners.  Records alternate between two buffers so no CTA overwrites what an
@@ -476,7 +477,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (pass >= 2 && blockIdx.x == 0)
                 for (int r = threadIdx.x; r < R; r += blockDim.x) key_buf(pass + 1)[(size_t)r * kKeyStride] = 0ull;
             float4* rec = (pass & 1) ? p.cta_rec2 : p.cta_rec;
-            if (!tc_tile_phase<MT, LT>(p, &tmap, tok[(pass + 1) & 1], s_anc, rec, sh, tmem, it_p, it_m, jt_m, jt_e,
+            if (!tc_tile_phase<MT, LT, TT>(p, &tmap, tok[(pass + 1) & 1], s_anc, rec, sh, tmem, it_p, it_m, jt_m, jt_e,
                                        pre_issued, key_buf(pass))) {
                 ok = false;
                 break;
@@ -499,12 +500,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             int32_t* cur = p.tokbuf + (pass & 1) * (size_t)R;
             if (blockIdx.x == 0 && threadIdx.x == 0) p.changed[pass + 1] = 0u;
             if (use_bias) {
-                if (!tc_tile_phase<MT, LT>(p, &tmap, prev, s_anc, p.cta_rec, sh, tmem, it_p, it_m, jt_m, jt_e,
+                if (!tc_tile_phase<MT, LT, TT>(p, &tmap, prev, s_anc, p.cta_rec, sh, tmem, it_p, it_m, jt_m, jt_e,
                                            pre_issued, nullptr)) {
                     ok = false;
                     break;
                 }
-            } else {
+            } else if (!tile_phase_stream0_t1<LT>(p)) {
                 tile_phase_stream0<LT>(p);
             }
             if (!grid_barrier(gb, nb, p.status)) { ok = false; break; }
@@ -537,10 +538,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     if (!exited && threadIdx.x == 0) s_last_out = (ok && grid_barrier_exit(gb, nb)) ? 1 : 0;
     __syncthreads();
-    if (s_last_out && p.temperature == 0)
+    if (s_last_out && TT == 0)
         for (int i = threadIdx.x; i < 3 * R; i += blockDim.x) p.keys[(size_t)i * kKeyStride] = 0ull;
     if (!ok || blockIdx.x != 0) return;
-    if (p.temperature != 0) chain_fixup(p);   // T=0 owners applied the chain rule already
+    if (TT != 0) chain_fixup(p);   // T=0 owners applied the chain rule already
     if (threadIdx.x == 0 && p.passes_out) {
         if (p.passes_max) atomicMax(p.passes_out, pass);
         else *p.passes_out = pass;
@@ -575,18 +576,18 @@ bool draft_tc_supported(const DraftParams& p) {
 
 constexpr size_t kTcSmemBudget = 227 * 1024;   // dynamic shared memory per CTA
 
-template <int MT, typename LT>
+template <int MT, typename LT, int TT>
 static cudaError_t launch_tc(const DraftParams& p, cudaStream_t stream) {
     const int threads = kTcThreads;
     const int KB = p.r / kTcK;
-    const bool t1 = p.temperature == 1;
+    constexpr bool t1 = TT == 1;
     constexpr int S = TcStages<MT>::N;
     const size_t smem = 1024 + (size_t)MT * KB * kTcBlock + (size_t)S * kTcBlock +
                         sizeof(float4) * (t1 ? 3 : 1) * 16 * 32 + (t1 ? sizeof(float) * kTcWarps * p.r : 0) +
                         sizeof(uint64_t) * (2 * S + 2 * TcBufs<MT>::N + 1) + 16 +
                         sizeof(int32_t) * (2 * (size_t)p.B * p.gamma + p.B) + sizeof(float) * (size_t)p.B * p.gamma;
     if (smem > kTcSmemBudget) return cudaErrorInvalidConfiguration;
-    auto kern = draft_tc_kernel<MT, LT>;
+    auto kern = draft_tc_kernel<MT, LT, TT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int occ = 0;
@@ -613,8 +614,12 @@ static cudaError_t launch_tc(const DraftParams& p, cudaStream_t stream) {
 cudaError_t draft_launch_tc(const DraftParams& p, cudaStream_t stream) {
     const int R = p.B * p.gamma;
     const bool lb = p.ldt == SPEC_BF16;
-    if (R <= 128) return lb ? launch_tc<1, bf16_t>(p, stream) : launch_tc<1, float>(p, stream);
-    return lb ? launch_tc<2, bf16_t>(p, stream) : launch_tc<2, float>(p, stream);
+    if (p.temperature == 0) {
+        if (R <= 128) return lb ? launch_tc<1, bf16_t, 0>(p, stream) : launch_tc<1, float, 0>(p, stream);
+        return lb ? launch_tc<2, bf16_t, 0>(p, stream) : launch_tc<2, float, 0>(p, stream);
+    }
+    if (R <= 128) return lb ? launch_tc<1, bf16_t, 1>(p, stream) : launch_tc<1, float, 1>(p, stream);
+    return lb ? launch_tc<2, bf16_t, 1>(p, stream) : launch_tc<2, float, 1>(p, stream);
 }
 
 }  // namespace spec
