@@ -145,6 +145,11 @@ __device__ __forceinline__ void tile_bias_bf16(const DraftParams& p, int tile, c
     const bf16_t* Wt = static_cast<const bf16_t*>(p.Wt);
     const int lane = threadIdx.x & 31;
     const bool has = lane < (p.r >> 3);
+    {   // the tile's Wt rows are contiguous: one bulk request into L2 ahead of the loads
+        const long v0 = (long)tile * kDraftTile;
+        const long v1 = v0 + kDraftTile < p.V ? v0 + kDraftTile : p.V;
+        if (lane == 0 && v1 > v0) bulk_prefetch_l2(Wt + (size_t)v0 * p.r, (unsigned)((v1 - v0) * p.r * 2));
+    }
     float uu[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) uu[e] = has ? u[lane * 8 + e] : 0.0f;
@@ -563,6 +568,7 @@ __device__ __forceinline__ void unpack_word(const uint4& w, float (&x)[16 / size
 }
 
 constexpr int kS1Units = 8;
+constexpr int kS1Ahead = 3;
 template <typename LT>
 __device__ bool tile_phase_stream0_t1(const DraftParams& p) {
     constexpr int EPL = 16 / (int)sizeof(LT);          // entries per lane per unit
@@ -578,7 +584,19 @@ __device__ bool tile_phase_stream0_t1(const DraftParams& p) {
     if (upr > kS1Units) return false;
     const uint4 ninf = sizeof(LT) == 2 ? make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u)
                                        : make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
+    // each warp's row slices are requested into L2 kS1Ahead rows ahead of their loads,
+    // so a warp's rows stream from DRAM while it works through them one round trip at a
+    // time (a slice is contiguous: 16-byte aligned, whole 16-byte words)
+    const long e_stop = e_end < p.V ? e_end : p.V;
+    const unsigned slice_bytes = e_stop > e_begin ? (unsigned)((e_stop - e_begin) * (long)sizeof(LT)) : 0u;
+    auto prefetch_row = [&](int r) {
+        if (lane == 0 && r < R && slice_bytes > 0)
+            bulk_prefetch_l2(static_cast<const LT*>(p.logits) + (size_t)r * p.V + e_begin, slice_bytes);
+    };
+#pragma unroll
+    for (int a = 0; a < kS1Ahead; ++a) prefetch_row((int)(threadIdx.x >> 5) + a * nw);
     for (int row = (int)(threadIdx.x >> 5); row < R; row += nw) {
+        prefetch_row(row + kS1Ahead * nw);
         const LT* lrow = static_cast<const LT*>(p.logits) + (size_t)row * p.V;
         uint4 w[kS1Units];
 #pragma unroll
