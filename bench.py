@@ -38,7 +38,7 @@ L2_FLUSH_BYTES = 512 << 20
 # DRAM bytes (read + written) per launch of draft_tc_kernel<1, bf16> on the headline
 # workload, from an ncu capture (ncu --set full, one launch); None once the kernel
 # changes, until it is captured again
-DRAFT_TC_TRAFFIC_BYTES = 142_637_824
+DRAFT_TC_TRAFFIC_BYTES = 142_743_040
 
 
 def parse():
@@ -426,6 +426,39 @@ def secondary(args, torch, vsd, synth, dev, hbm, hbm_kind, sampler):
         "gpu_launches": steps5,
     }
     del t, d, inp, o
+    torch.cuda.empty_cache()
+
+    # configuration 4's draft: B=32, gamma=7, V=248320, r=256 bf16, T=1 (224 rows, the
+    # tcgen05 kernel with two M tiles); 111 MB of drafter rows and 127 MB of Wt
+    inp = synth.config_inputs(4, device=dev)
+    c = inp["cfg"]
+    B, G, V = c.B, c.gamma, c.V
+    L4, U4, Wt4, a4, s4 = inp["draft"], inp["U"], inp["Wt"], inp["anchor"], inp["seeds"]
+    ws4 = vsd.workspace(vsd.OP_DRAFT, B, G, V, c.r, dev)
+    o4 = vsd.draft_block(L4, a4, U4, Wt4, 1, s4, ws=ws4)
+    fn, graphed = capture(lambda: vsd.draft_block(L4, a4, U4, Wt4, 1, s4, ws=ws4, out=o4), torch)
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    sampler.active = True
+    total, _ = time_steps(torch, fn, steps, flush=lambda: flush_buf.zero_())
+    sampler.active = False
+    ms = sum(total) / len(total)
+    passes = int(o4["passes"].item())
+    byts = B * G * V * 2 + passes * V * c.r * 2 + B * G * c.r * 2
+    ach = byts / (ms * 1e-3) / 1e9
+    out["draft_t1_b32"] = {
+        "workload": "draft block T=1, B=32, gamma=7, V=248320, r=256 bf16, per-request seeds (L2 flushed)",
+        "value": B * G / (ms * 1e-3), "unit": "rows/s", "us_per_step": ms * 1e3, "cuda_graphs": graphed,
+        "passes": passes,
+        "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "peak_kind": hbm_kind, "unit": "GB/s",
+                     "frac": ach / hbm, "frac_of_nominal_8tbs": ach / NOMINAL_HBM_GBS,
+                     "algorithmic_bytes_per_launch": byts,
+                     "note": "drafter rows once, W once per biased pass; pass 0 and the biased pass both read the rows"},
+        "gpu_launches": steps,
+    }
+    del inp, L4, U4, Wt4, o4, ws4, flush_buf
     torch.cuda.empty_cache()
 
     # the SpecOPD anchor-branch sampler: 16 references x 64 anchors, W = 7, V = 248320,
