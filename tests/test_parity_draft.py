@@ -169,3 +169,18 @@ def test_configs_full_size(spec, cfg_id, T):
                               inp["seeds"].cpu())
     assert near <= max(1, c.B * c.gamma // 64)
     assert vsd.device_status(out["ws"]) == 0
+
+
+@pytest.mark.parametrize("V,r,wdtype", [(400000, 64, torch.bfloat16), (700000, 4, torch.float32)])
+def test_t1_long_tile_ranges(spec, V, r, wdtype):
+    """T=1 with more than 8 units of 256 (bf16) or 128 (fp32) entries per CTA and row:
+    pass 0 takes the general record path instead of the register-resident slice."""
+    B, gamma = 2, 3
+    L, _ = synth.target_and_draft(B, gamma - 1, V, "zipf", 0.0, wdtype, seed=V % 997)
+    L = L[:, :gamma].contiguous()
+    U, Wt = synth.markov_weights(V, r, wdtype, seed=r, scale=0.3)
+    anchor = synth.anchors(B, V, seed=7)
+    seeds = synth.seeds_for(B, 11)
+    out = _gpu(L, anchor, U, Wt, 1, seeds)
+    exact, near = check_draft(out, L, anchor, U, Wt, 1, seeds)
+    assert near <= 1
