@@ -167,6 +167,7 @@ def time_steps(torch, replay, steps, flush=None, parts=None):
 
 
 def run_ours(args, rank, world, torch, dist):
+    from verify_spec_draft_gb300 import shard
     import verify_spec_draft_gb300 as vsd
     from verify_spec_draft_gb300 import synth
 
@@ -245,9 +246,8 @@ def run_ours(args, rank, world, torch, dist):
     ms_draft = sum(t_draft) / len(t_draft)
     ms_verify = sum(t_verify) / len(t_verify)
     if world > 1:
-        t = torch.tensor([ms_step, ms_one, ms_draft, ms_verify], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step, ms_one, ms_draft, ms_verify = t.tolist()
+        ms_step, ms_one, ms_draft, ms_verify = (shard.max_over_ranks(x, dev) for x in (ms_step, ms_one, ms_draft,
+                                                                                      ms_verify))
     passes = int(out_f["passes"].item())
     rows = B * (G + 1)
     # algorithmic bytes of one draft launch (the dominant kernel): the draft rows and Wt
@@ -348,7 +348,7 @@ def run_ours(args, rank, world, torch, dist):
 
     # ---- secondary: verify T=1 at B=32 (configuration 4) and E2E-TV (configuration 5)
     if not args.no_secondary:
-        result["secondary"] = secondary(args, torch, vsd, synth, dev, hbm, hbm_kind, sampler)
+        result["secondary"] = secondary(args, torch, vsd, synth, dev, hbm, hbm_kind, sampler, rank, world)
 
     sampler.stop()
     result["clocks"] = sampler.summary()
@@ -357,7 +357,8 @@ def run_ours(args, rank, world, torch, dist):
     return result
 
 
-def secondary(args, torch, vsd, synth, dev, hbm, hbm_kind, sampler):
+def secondary(args, torch, vsd, synth, dev, hbm, hbm_kind, sampler, rank=0, world=1):
+    from verify_spec_draft_gb300 import shard
     out = {}
     steps = max(5, min(args.steps, 50))
     # configuration 4: verify T=1, B=32, gamma=7, V=248320; inputs 238 MB > L2
@@ -394,18 +395,31 @@ def secondary(args, torch, vsd, synth, dev, hbm, hbm_kind, sampler):
     del t, d, inp
     torch.cuda.empty_cache()
 
-    # configuration 5: E2E-TV, 16 x 64 x 7 rows, V=248320; 7.1 GB of inputs
+    # configuration 5: E2E-TV, 16 x 64 x 7 rows, V=248320; 7.1 GB of inputs.  With N > 1
+    # ranks the 1024 branches are split across them (strong scaling for this line): each
+    # rank runs its shard and the loss takes one scalar all-reduce per step
     inp = synth.config_inputs(5, device=dev)
     c = inp["cfg"]
-    N, Wb, V = c.B, c.gamma, c.V
-    t, d = inp["target"], inp["draft"]
+    N_all, Wb, V = c.B, c.gamma, c.V
+    b0, N = shard.shard_range(N_all, rank, world)
+    t = inp["target"][b0 * Wb:(b0 + N) * Wb]
+    d = inp["draft"][b0 * Wb:(b0 + N) * Wb]
     ws = vsd.workspace(vsd.OP_E2ETV, N, Wb, V, 0, dev)
     R = N * Wb
     o = dict(a=torch.empty((R,), dtype=torch.float32, device=dev),
              surv=torch.empty((R,), dtype=torch.float32, device=dev),
              loss=torch.empty((1,), dtype=torch.float32, device=dev),
              grad=torch.empty((R, V), dtype=torch.bfloat16, device=dev))
-    fn, graphed = capture(lambda: vsd.e2etv(t, d, N, Wb, ws=ws, out=o), torch)
+    if world == 1:
+        fn, graphed = capture(lambda: vsd.e2etv(t, d, N, Wb, ws=ws, out=o), torch)
+    else:
+        o["msum"] = o["loss"]
+
+        def sharded():
+            r = shard.e2etv_rank(t, d, N, Wb, N_all, ws=ws, out=o)
+            o["loss_all"] = r["loss"]
+
+        fn, graphed = sharded, False
     for _ in range(3):
         fn()
     torch.cuda.synchronize()
@@ -414,12 +428,16 @@ def secondary(args, torch, vsd, synth, dev, hbm, hbm_kind, sampler):
     total, _ = time_steps(torch, fn, steps5)
     sampler.active = False
     ms = sum(total) / len(total)
+    if world > 1:
+        ms = shard.max_over_ranks(ms, dev)
     byts = 3 * R * V * 2
     ach = byts / (ms * 1e-3) / 1e9
     out["e2etv_cfg5"] = {
         "workload": "E2E-TV, 16 refs x 64 anchors x Wb=7 = 7168 rows, V=248320, bf16 in/out",
-        "value": R / (ms * 1e-3), "unit": "supervised tokens/s", "ms_per_step": ms, "cuda_graphs": graphed,
-        "loss": float(o["loss"].item()),
+        "value": N_all * Wb / (ms * 1e-3), "unit": "supervised tokens/s", "ms_per_step": ms, "cuda_graphs": graphed,
+        "loss": float((o["loss_all"] if world > 1 else o["loss"]).item()),
+        "scaling": "strong" if world > 1 else None,
+        "branches_per_rank": N,
         "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "peak_kind": hbm_kind, "unit": "GB/s",
                      "frac": ach / hbm, "frac_of_nominal_8tbs": ach / NOMINAL_HBM_GBS,
                      "algorithmic_bytes_per_launch": byts},

@@ -351,6 +351,24 @@ spec_status spec_e2etv(const uint16_t *target_logits, const uint16_t *draft_logi
                        size_t workspace_bytes, spec_stream_t stream);
 
 /*
+ * spec_e2etv_shard - spec_e2etv on one shard of a batch split across processes (one
+ * per GPU), for the same definitions over the whole batch of total_branches branches.
+ * The rows are this shard's n_branches branches; every branch is independent, so a
+ * shard needs nothing from the others except the loss's count: kappa and the gradient
+ * use 1/(total_branches*Wb), and
+ *   msum_out  [1] float32: this shard's part of the mean survival,
+ *             sum over its branches and positions of S / (total_branches * Wb).
+ * The loss of the whole batch is 1 - (the sum of msum_out over the shards): one scalar
+ * all-reduce, left to the caller.  A shard with an invalid branch writes NaN.
+ * Limits: those of spec_e2etv, and n_branches <= total_branches.  The workspace is
+ * spec_workspace_bytes(SPEC_OP_E2ETV, n_branches, Wb, V, 0).
+ */
+spec_status spec_e2etv_shard(const uint16_t *target_logits, const uint16_t *draft_logits,
+                             int n_branches, int Wb, int V, int total_branches, float *a_out,
+                             float *surv_out, float *msum_out, uint16_t *grad_out,
+                             void *workspace, size_t workspace_bytes, spec_stream_t stream);
+
+/*
  * spec_branch_plan - SpecOPD anchor-branch plan: anchors on each reference response,
  * and the metadata that packs the branches drafted from them into one proposal tree.
  *

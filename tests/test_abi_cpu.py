@@ -148,6 +148,18 @@ def test_e2etv_argument_errors(lib):
     assert _e2etv(lib, wsb=100) == 9
 
 
+def test_e2etv_shard_argument_errors(lib):
+    def call(target=A, draft=A, N=2, Wb=3, V=100, total=4, a=A, surv=A, msum=A, grad=A, ws=A, wsb=1 << 30):
+        return lib.spec_e2etv_shard(target, draft, N, Wb, V, total, a, surv, msum, grad, ws, wsb, None)
+    assert call(msum=0) == 1
+    assert call(target=0) == 1
+    assert call(total=1) == 2              # fewer branches in the batch than in the shard
+    assert call(N=0) == 2
+    assert call(Wb=65) == 2
+    assert call(grad=MIS) == 4
+    assert call(wsb=100) == 9
+
+
 def test_verify_budget_argument_errors(lib):
     def call(conf=A, B=4, gamma=7, budget=10, cost=A, gamma_out=A, expected=A):
         return lib.spec_verify_budget(conf, B, gamma, budget, cost, gamma_out, expected, None)

@@ -107,3 +107,26 @@ def test_config5_full_size_sampled(spec):
     scale = g.abs().sum(dim=1)
     assert (g.sum(dim=1).abs() <= 1e-2 * scale + 1e-30).all()
     assert vsd.device_status(out["ws"]) == 0
+
+
+def test_shards_match_one_call(spec):
+    """spec_e2etv_shard on two halves of a batch (as two ranks would run it) equals one
+    spec_e2etv call over the whole batch: the same a, S and gradient, and shares that add
+    up to 1 - loss."""
+    from verify_spec_draft_gb300 import shard
+    N, Wb, V = 6, 4, 5000
+    t, d = synth.e2etv_rows(N, Wb, V, 1.0, seed=12, device="cuda")
+    whole = vsd.e2etv(t, d, N, Wb)
+    shares = 0.0
+    for rank in range(2):
+        b0, n = shard.shard_range(N, rank, 2)
+        rows = slice(b0 * Wb, (b0 + n) * Wb)
+        part = vsd.e2etv_shard(t[rows].contiguous(), d[rows].contiguous(), n, Wb, N)
+        torch.cuda.synchronize()
+        assert torch.allclose(part["a"], whole["a"][rows], atol=1e-6, rtol=0)
+        assert torch.allclose(part["surv"], whole["surv"][rows], atol=1e-6, rtol=0)
+        g0 = whole["grad"][rows].double()
+        assert ((part["grad"].double() - g0).norm() / g0.norm()).item() <= 1e-3
+        shares += float(part["msum"].item())
+        assert vsd.device_status(part["ws"]) == 0
+    assert abs((1.0 - shares) - float(whole["loss"].item())) <= 1e-6

@@ -47,6 +47,7 @@ SIGNATURES = {
     "spec_draft_verify": (_i32, [_vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _i32,
                                  _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "spec_verify_budget": (_i32, [_vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp]),
+    "spec_e2etv_shard": (_i32, [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "spec_branch_plan": (_i32, [_vp, _vp, _i32, _i32, _i32, _i32, ctypes.c_uint64, _vp, _vp, _vp, _vp,
                                 _vp, _sz, _vp]),
 }
@@ -329,6 +330,35 @@ def branch_plan(trunk, lengths, n_anchors, W, seed, ws=None, out=None, stream=No
                                 _ptr(out["anchors"]), _ptr(out["anchor_tok"]), _ptr(out["parent"]),
                                 _ptr(out["position"]), _ptr(ws), ws.numel(), _stream(stream))
     _check(code, "spec_branch_plan")
+    out["ws"] = ws
+    return out
+
+
+def e2etv_shard(target, draft, n_branches, Wb, total_branches, ws=None, out=None, stream=None):
+    """spec_e2etv_shard: one shard of a batch of ``total_branches`` branches.  target, draft
+    bf16 [n_branches*Wb, V].  Returns a dict of device tensors: a, surv [R] float32,
+    msum [1] float32 (this shard's part of the mean survival), grad bf16 [R, V]."""
+    torch = _torch()
+    lib = load()
+    _need(target, "target", None, torch.bfloat16)
+    dev = target.device
+    R, V = target.shape
+    if R != n_branches * Wb:
+        raise ValueError("target must have n_branches * Wb rows")
+    _need(draft, "draft", dev, torch.bfloat16, (R, V))
+    if out is None:
+        out = dict(
+            a=torch.empty((R,), dtype=torch.float32, device=dev),
+            surv=torch.empty((R,), dtype=torch.float32, device=dev),
+            msum=torch.empty((1,), dtype=torch.float32, device=dev),
+            grad=torch.empty((R, V), dtype=torch.bfloat16, device=dev),
+        )
+    if ws is None:
+        ws = workspace(OP_E2ETV, n_branches, Wb, V, 0, dev, stream)
+    code = lib.spec_e2etv_shard(_ptr(target), _ptr(draft), n_branches, Wb, V, int(total_branches), _ptr(out["a"]),
+                                _ptr(out["surv"]), _ptr(out["msum"]), _ptr(out["grad"]), _ptr(ws), ws.numel(),
+                                _stream(stream))
+    _check(code, "spec_e2etv_shard")
     out["ws"] = ws
     return out
 

@@ -282,6 +282,37 @@ spec_status spec_e2etv(const uint16_t* target_logits, const uint16_t* draft_logi
     p.surv_out = surv_out;
     p.loss_out = loss_out;
     p.grad_out = grad_out;
+    p.total_branches = n_branches;
+    p.share_out = 0;
+    return cuda_status(e2etv_launch(p, workspace, (cudaStream_t)stream));
+}
+
+spec_status spec_e2etv_shard(const uint16_t* target_logits, const uint16_t* draft_logits, int n_branches, int Wb,
+                             int V, int total_branches, float* a_out, float* surv_out, float* msum_out,
+                             uint16_t* grad_out, void* workspace, size_t workspace_bytes, spec_stream_t stream) {
+    if (n_branches < 1 || Wb < 1 || Wb > SPEC_MAX_GAMMA || V < 1 || V > SPEC_MAX_V ||
+        (long)n_branches * Wb > (1L << 24) || total_branches < n_branches)
+        return SPEC_ERR_SHAPE;
+    if (!target_logits || !draft_logits || !a_out || !surv_out || !msum_out || !grad_out)
+        return SPEC_ERR_INVALID_ARG;
+    if (!aligned16(target_logits) || !aligned16(draft_logits) || !aligned16(grad_out)) return SPEC_ERR_ALIGN;
+    const size_t need = e2etv_workspace_bytes(n_branches, Wb, V);
+    if (!workspace || workspace_bytes < need) return SPEC_ERR_WORKSPACE;
+
+    E2etvParams p;
+    memset(&p, 0, sizeof(p));
+    p.target = target_logits;
+    p.draft = draft_logits;
+    p.n_branches = n_branches;
+    p.Wb = Wb;
+    p.V = V;
+    p.vec_ok = (V % 8) == 0;
+    p.a_out = a_out;
+    p.surv_out = surv_out;
+    p.loss_out = msum_out;
+    p.grad_out = grad_out;
+    p.total_branches = total_branches;
+    p.share_out = 1;
     return cuda_status(e2etv_launch(p, workspace, (cudaStream_t)stream));
 }
 

@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, STAGED ? 2 : 4) e2etv_kernel(E2etvPa
     GridBarrier gbar = grid_barrier_init(p.barriers + (size_t)g * 64);
     float2* part = p.partials + (size_t)g * 2 * p.group_size * nr;
     float2* part2 = part + (size_t)p.group_size * nr;
-    const double inv_total = 1.0 / ((double)p.n_branches * Wb);
+    const double inv_total = 1.0 / ((double)p.total_branches * Wb);
     const unsigned bytes = (unsigned)ncol * 2u;
     unsigned ph_t = 0, ph_d = 0;
     const uint64_t pol_keep = STAGED ? 0ull : l2_policy_keep();
@@ -532,7 +532,8 @@ __global__ void __launch_bounds__(kThreads, STAGED ? 2 : 4) e2etv_kernel(E2etvPa
         const float tot = __shfl_sync(0xffffffffu, warp_inclusive_scan(sum), 31);
         bad = warp_or(bad);
         if (lane == 0) {
-            *p.loss_out = (float)(1.0 - (double)tot * inv_total);
+            const double M = (double)tot * inv_total;   // this call's part of the mean survival
+            *p.loss_out = (float)(p.share_out ? M : 1.0 - M);
             if (bad || isnan(tot)) { *p.loss_out = NAN; atomicOr(p.status, SPEC_DEV_NONFINITE); }
             *p.done = 0u;
         }

@@ -95,8 +95,10 @@ struct E2etvParams {
     int vec_ok;                // V % 8 == 0 (rows 16-byte aligned)
     float* a_out;
     float* surv_out;
-    float* loss_out;
+    float* loss_out;           // 1 - M, or M alone (share_out) for one shard of a batch
     uint16_t* grad_out;
+    int total_branches;        // branches of the whole batch (the mean's count)
+    int share_out;
     // layout chosen at launch
     int n_groups;              // groups of CTAs, each processing one branch at a time
     int group_size;            // CTAs per group
