@@ -61,6 +61,10 @@ def _draft_check(out, L, anchor, U, Wt, T, seeds, rows, first=None):
         ref = od.draft_block(L[b:b + 1].double().cpu().numpy(), anchor[b:b + 1].cpu().numpy(), Un, Wn, T,
                              seeds[b:b + 1].cpu().numpy(), first_b=b)
         for j in range(tok.shape[1]):
+            if ref["tokens"][0, j] < 0:   # invalid from here on: -1 and NaN on both sides
+                assert tok[b, j] == -1 and np.isnan(conf[b, j]), (b, j)
+                compared += 1
+                continue
             if tok[b, j] != ref["tokens"][0, j]:
                 assert ref["near"][0, j], (b, j, tok[b, j], ref["tokens"][0, j])
                 break   # the chain diverges legitimately from here
@@ -118,3 +122,36 @@ def test_sampler_full_size_sampled(spec):
     assert bool(((tok >= 0) & (tok < c.V)).all())
     rows = [0, 35, 36, 511, 1000, 1023]   # both sides of a launch boundary
     assert _draft_check(out, inp["logits"], anchor.cpu(), inp["U"], inp["Wt"], 1, inp["seeds"], rows) >= 30
+
+
+def test_plan_every_position_at_the_largest_reference(spec):
+    """n = L = 16384 (SPEC_MAX_TRUNK): every position is an anchor, in order."""
+    L = 16384
+    trunk = torch.arange(L, dtype=torch.int32).view(1, L) % 1000
+    out = _plan_check(trunk, torch.tensor([L], dtype=torch.int32), L, 1, seed=5)
+    assert out["anchors"].cpu().view(-1).tolist() == list(range(L))
+
+
+def test_batched_draft_invalid_requests_across_slices(spec):
+    """A NaN row in the first launch's slice and an invalid anchor in the second: those
+    requests get -1 from the bad position on, the flags of both launches are kept, and
+    every other request matches the oracle."""
+    B, G, V, r = 40, 7, 2000, 64
+    L, _ = synth.target_and_draft(B, G - 1, V, "zipf", 0.0, torch.bfloat16, seed=23)
+    L = L[:, :G].contiguous()
+    L[3, 4, 17] = float("nan")
+    U, Wt = synth.markov_weights(V, r, torch.bfloat16, seed=23, scale=0.5)
+    anchor = synth.anchors(B, V, seed=23)
+    anchor[38] = -2
+    seeds = synth.seeds_for(B, 2)
+    dev = torch.device("cuda")
+    for T in (0, 1):
+        out = vsd.draft_block(L.to(dev), anchor.to(dev), U.to(dev), Wt.to(dev), T, seeds.to(dev))
+        torch.cuda.synchronize()
+        tok = out["tokens"].cpu()
+        assert tok[3, 4:].tolist() == [-1, -1, -1] and (tok[3, :4] >= 0).all()
+        assert (tok[38] == -1).all()
+        flags = vsd.device_status(out["ws"])
+        assert flags & vsd.DEV_NONFINITE and flags & vsd.DEV_TOKEN
+        rows = [0, 3, 35, 36, 38, 39]
+        assert _draft_check(out, L, anchor, U, Wt, T, seeds, rows) >= 4 * G - 2 * G

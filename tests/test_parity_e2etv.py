@@ -130,3 +130,20 @@ def test_shards_match_one_call(spec):
         shares += float(part["msum"].item())
         assert vsd.device_status(part["ws"]) == 0
     assert abs((1.0 - shares) - float(whole["loss"].item())) <= 1e-6
+
+
+def test_shard_with_an_invalid_branch(spec):
+    """A NaN in one branch of a shard makes that shard's share NaN (so the all-reduced
+    loss is NaN) and flags NONFINITE; the other branches are unaffected."""
+    N, Wb, V = 4, 3, 2048
+    t, d = synth.e2etv_rows(N, Wb, V, seed=31)
+    d[4, 7] = float("nan")   # branch 1
+    out = vsd.e2etv_shard(t.cuda(), d.cuda(), N, Wb, 10)
+    torch.cuda.synchronize()
+    assert torch.isnan(out["msum"].cpu()).all()
+    a = out["a"].cpu()
+    assert torch.isnan(a[3:6]).all() and torch.isfinite(a[:3]).all() and torch.isfinite(a[6:]).all()
+    assert out["grad"][3:6].float().abs().max().item() == 0.0
+    assert vsd.device_status(out["ws"]) & vsd.DEV_NONFINITE
+    # the valid branches, normalised by the batch of 10 branches
+    _check_rows(out, t, d, N, Wb, [0, 2, 3], 10)

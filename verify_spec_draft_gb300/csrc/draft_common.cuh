@@ -214,6 +214,109 @@ __device__ __forceinline__ void row_tile_z(const DraftParams& p, int row, int ti
     }
 }
 
+// The T=1 draw's first two levels for one row (one warp; every lane gets the result):
+// the CTA range in which the row's CDF (the CTA records' weights, in index order)
+// crosses thr, then the tile of that range, and what is left of thr at that tile's
+// start (INFINITY when rounding leaves no crossing, with the last tile of weight).
+__device__ __forceinline__ void draw_locate(const DraftParams& p, const float4* recs, int row, int nblk_tile,
+                                            float M2, float thr, int& tile_out, float& tl_out) {
+    const int lane = threadIdx.x & 31;
+    // level 1: CTA ranges, contiguous segments per lane
+    const int Kc = (nblk_tile + 31) / 32;
+    const int c0 = lane * Kc, c1 = min(nblk_tile, c0 + Kc);
+    float seg = 0.0f;
+    for (int c = c0; c < c1; ++c) {
+        const RowAcc r = rowacc_unpack(__ldcg(&recs[c]));
+        if (r.mx != -INFINITY) seg += r.s * ex2(r.mx * kLog2e - M2);
+    }
+    const float incl = warp_inclusive_scan(seg);
+    unsigned cross = __ballot_sync(0xffffffffu, incl > thr);
+    int cta = -1;
+    float tl = INFINITY;
+    if (cross) {
+        const int L = __ffs(cross) - 1;
+        if (lane == L) {
+            float run = incl - seg;
+            for (int c = c0; c < c1; ++c) {
+                const RowAcc r = rowacc_unpack(__ldcg(&recs[c]));
+                const float w = (r.mx == -INFINITY) ? 0.0f : r.s * ex2(r.mx * kLog2e - M2);
+                if (run + w > thr) { cta = c; tl = thr - run; break; }
+                run += w;
+            }
+            if (cta < 0) cta = c1 - 1;
+        }
+        cta = __shfl_sync(0xffffffffu, cta, L);
+        tl = __shfl_sync(0xffffffffu, tl, L);
+    } else {
+        int last = -1;
+        for (int c = c0; c < c1; ++c) {
+            const RowAcc r = rowacc_unpack(__ldcg(&recs[c]));
+            if (r.mx != -INFINITY && r.s > 0.0f) last = c;
+        }
+        const unsigned has = __ballot_sync(0xffffffffu, last >= 0);
+        cta = has ? __shfl_sync(0xffffffffu, last, 31 - __clz(has)) : 0;
+    }
+    cta = max(0, min(cta, nblk_tile - 1));
+    // level 2: the tiles of that CTA (at most 32 per pass of the warp)
+    const int tb = tile_begin(cta, nblk_tile, p.n_tiles), te = tile_begin(cta + 1, nblk_tile, p.n_tiles);
+    int tile = -1, last_tile = te - 1;
+    float carry = 0.0f;
+    for (int t0 = tb; t0 < te && tile < 0; t0 += 32) {
+        const int t = t0 + lane;
+        float w = 0.0f;
+        if (t < te) {
+            const RowAcc r = rowacc_unpack(__ldcg(&p.tile_rec[(size_t)row * p.n_tiles + t]));
+            w = (r.mx == -INFINITY) ? 0.0f : r.s * ex2(r.mx * kLog2e - M2);
+        }
+        const float inc = warp_inclusive_scan(w) + carry;
+        const unsigned hit = __ballot_sync(0xffffffffu, t < te && inc > tl);
+        if (hit) {
+            const int L = __ffs(hit) - 1;
+            tile = t0 + L;
+            const float before = __shfl_sync(0xffffffffu, inc - w, L);
+            tl -= before;
+        }
+        const unsigned pos = __ballot_sync(0xffffffffu, t < te && w > 0.0f);
+        if (pos) last_tile = t0 + 31 - __clz(pos);
+        carry = __shfl_sync(0xffffffffu, inc, 31);
+    }
+    if (tile < 0) { tile = last_tile; tl = INFINITY; }
+    tile = max(0, min(tile, p.n_tiles - 1));
+    tile_out = tile;
+    tl_out = tl;
+}
+
+// The draw's last level: the tile's entries in index order (lane l holds entries
+// 32i + l as z[i]); returns the entry where the running weight passes tl, or the last
+// entry of positive weight, and its z.
+__device__ __forceinline__ void draw_scan_tile(const float (&z)[4], const long (&v)[4], long V, float M2, float tl,
+                                               int tile, int& found_out, float& zf_out) {
+    const int lane = threadIdx.x & 31;
+    float car = 0.0f, zf = 0.0f, zl = 0.0f;
+    int found = -1, last_pos = -1;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float w = (v[i] < V) ? wexp(z[i], M2) : 0.0f;
+        const float inc = warp_inclusive_scan(w) + car;
+        const unsigned hit = __ballot_sync(0xffffffffu, w > 0.0f && inc > tl);
+        if (found < 0 && hit) {
+            const int L = __ffs(hit) - 1;
+            found = tile * kDraftTile + 32 * i + L;
+            zf = __shfl_sync(0xffffffffu, z[i], L);
+        }
+        const unsigned pos = __ballot_sync(0xffffffffu, w > 0.0f);
+        if (pos) {
+            const int L = 31 - __clz(pos);
+            last_pos = tile * kDraftTile + 32 * i + L;
+            zl = __shfl_sync(0xffffffffu, z[i], L);
+        }
+        car = __shfl_sync(0xffffffffu, inc, 31);
+    }
+    if (found < 0) { found = last_pos; zf = zl; }
+    found_out = found;
+    zf_out = zf;
+}
+
 // One warp per row: merge the CTA records, choose x_j, write the outputs, flag a
 // change against the previous pass.  `s_uw` is this warp's r-float scratch.
 template <typename LT, typename WT>
@@ -246,67 +349,9 @@ __device__ void finalize_rows(const DraftParams& p, int pass, bool use_bias, con
             } else {
                 const float u = philox_uniform(p.seeds[b], (uint64_t)(p.b_base + b), (uint64_t)(j + 1), 0);
                 const float thr = u * S;
-                // level 1: CTA ranges, contiguous segments per lane
-                const int Kc = (nblk_tile + 31) / 32;
-                const int c0 = lane * Kc, c1 = min(nblk_tile, c0 + Kc);
-                float seg = 0.0f;
-                for (int c = c0; c < c1; ++c) {
-                    const RowAcc r = rowacc_unpack(__ldcg(&recs[c]));
-                    if (r.mx != -INFINITY) seg += r.s * ex2(r.mx * kLog2e - M2);
-                }
-                const float incl = warp_inclusive_scan(seg);
-                unsigned cross = __ballot_sync(0xffffffffu, incl > thr);
-                int cta = -1;
+                int tile = 0;
                 float tl = INFINITY;
-                if (cross) {
-                    const int L = __ffs(cross) - 1;
-                    if (lane == L) {
-                        float run = incl - seg;
-                        for (int c = c0; c < c1; ++c) {
-                            const RowAcc r = rowacc_unpack(__ldcg(&recs[c]));
-                            const float w = (r.mx == -INFINITY) ? 0.0f : r.s * ex2(r.mx * kLog2e - M2);
-                            if (run + w > thr) { cta = c; tl = thr - run; break; }
-                            run += w;
-                        }
-                        if (cta < 0) cta = c1 - 1;
-                    }
-                    cta = __shfl_sync(0xffffffffu, cta, L);
-                    tl = __shfl_sync(0xffffffffu, tl, L);
-                } else {
-                    int last = -1;
-                    for (int c = c0; c < c1; ++c) {
-                        const RowAcc r = rowacc_unpack(__ldcg(&recs[c]));
-                        if (r.mx != -INFINITY && r.s > 0.0f) last = c;
-                    }
-                    const unsigned has = __ballot_sync(0xffffffffu, last >= 0);
-                    cta = has ? __shfl_sync(0xffffffffu, last, 31 - __clz(has)) : 0;
-                }
-                cta = max(0, min(cta, nblk_tile - 1));
-                // level 2: the tiles of that CTA (at most 32 per pass of the warp)
-                const int tb = tile_begin(cta, nblk_tile, p.n_tiles), te = tile_begin(cta + 1, nblk_tile, p.n_tiles);
-                int tile = -1, last_tile = te - 1;
-                float carry = 0.0f;
-                for (int t0 = tb; t0 < te && tile < 0; t0 += 32) {
-                    const int t = t0 + lane;
-                    float w = 0.0f;
-                    if (t < te) {
-                        const RowAcc r = rowacc_unpack(__ldcg(&p.tile_rec[(size_t)row * p.n_tiles + t]));
-                        w = (r.mx == -INFINITY) ? 0.0f : r.s * ex2(r.mx * kLog2e - M2);
-                    }
-                    const float inc = warp_inclusive_scan(w) + carry;
-                    const unsigned hit = __ballot_sync(0xffffffffu, t < te && inc > tl);
-                    if (hit) {
-                        const int L = __ffs(hit) - 1;
-                        tile = t0 + L;
-                        const float before = __shfl_sync(0xffffffffu, inc - w, L);
-                        tl -= before;
-                    }
-                    const unsigned pos = __ballot_sync(0xffffffffu, t < te && w > 0.0f);
-                    if (pos) last_tile = t0 + 31 - __clz(pos);
-                    carry = __shfl_sync(0xffffffffu, inc, 31);
-                }
-                if (tile < 0) { tile = last_tile; tl = INFINITY; }
-                tile = max(0, min(tile, p.n_tiles - 1));
+                draw_locate(p, recs, row, nblk_tile, M2, thr, tile, tl);
                 // level 3: recompute the tile's z on CUDA cores and scan it
                 if (use_bias) {
                     const int xp = prev_token(p, prev, row);
@@ -316,27 +361,9 @@ __device__ void finalize_rows(const DraftParams& p, int pass, bool use_bias, con
                 float z[4];
                 long v[4];
                 row_tile_z<LT, WT>(p, row, tile, use_bias, s_uw, z, v);
-                float car = 0.0f, zf = 0.0f, zl = 0.0f;
-                int found = -1, last_pos = -1;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float w = (v[i] < p.V) ? wexp(z[i], M2) : 0.0f;
-                    const float inc = warp_inclusive_scan(w) + car;
-                    const unsigned hit = __ballot_sync(0xffffffffu, w > 0.0f && inc > tl);
-                    if (found < 0 && hit) {
-                        const int L = __ffs(hit) - 1;
-                        found = tile * kDraftTile + 32 * i + L;
-                        zf = __shfl_sync(0xffffffffu, z[i], L);
-                    }
-                    const unsigned pos = __ballot_sync(0xffffffffu, w > 0.0f);
-                    if (pos) {
-                        const int L = 31 - __clz(pos);
-                        last_pos = tile * kDraftTile + 32 * i + L;
-                        zl = __shfl_sync(0xffffffffu, z[i], L);
-                    }
-                    car = __shfl_sync(0xffffffffu, inc, 31);
-                }
-                if (found < 0) { found = last_pos; zf = zl; }
+                int found = -1;
+                float zf = 0.0f;
+                draw_scan_tile(z, v, p.V, M2, tl, tile, found, zf);
                 x = found;
                 qx = wexp(zf, M2) / S;
                 __syncwarp();
@@ -349,6 +376,126 @@ __device__ void finalize_rows(const DraftParams& p, int pass, bool use_bias, con
             cur[row] = x;
             if (pass > 0 && __ldcg(&prev[row]) != x) atomicOr(&p.changed[pass], 1u);
         }
+    }
+}
+
+// T=1 draws after a biased pass with bf16 weight rows of whole 16-byte words (r <= 256):
+// a group of kDrawWarps warps per row.  Every warp of the group merges the row's
+// records and locates the tile itself (the same loads, so the same decisions); each
+// then computes kDraftTile / kDrawWarps of the tile's biased logits (the rank split
+// over its lanes) into the group's kDraftTile floats of `s_z`, and after a named
+// barrier the group's first warp scans them.  Rows go to CTAs first (row r to CTA
+// r % gridDim.x), so every SM takes a share of the rows.  Warps beyond the last whole
+// group take no part.
+constexpr int kDrawWarps = 8;
+constexpr int kDrawBarrier = 9;   // named barrier of group g: kDrawBarrier + g
+__device__ __forceinline__ void draw_group_sync(int grp) {
+    asm volatile("bar.sync %0, %1;" :: "r"(kDrawBarrier + grp), "r"(32 * kDrawWarps) : "memory");
+}
+
+template <typename LT>
+__device__ void finalize_rows_t1g(const DraftParams& p, int pass, const int32_t* prev, int32_t* cur, int nblk_tile,
+                                  float* s_z) {
+    constexpr int EPW = kDraftTile / kDrawWarps;   // entries of the tile per warp
+    const int R = p.B * p.gamma;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ngrp = (blockDim.x >> 5) / kDrawWarps;
+    const int grp = warp / kDrawWarps, gw = warp % kDrawWarps;
+    if (grp >= ngrp) return;
+    float* z_s = s_z + (size_t)grp * kDraftTile;
+    const bf16_t* U = static_cast<const bf16_t*>(p.U);
+    const bf16_t* Wt = static_cast<const bf16_t*>(p.Wt);
+    const bool has = lane < (p.r >> 3);
+    for (int row = grp * gridDim.x + blockIdx.x; row < R; row += gridDim.x * ngrp) {
+        const int b = row / p.gamma, j = row % p.gamma;
+        const float4* recs = p.cta_rec + (size_t)row * nblk_tile;
+        const LT* lrow = static_cast<const LT*>(p.logits) + (size_t)row * p.V;
+        RowAcc acc = rowacc_empty();
+#pragma unroll 4
+        for (int c = lane; c < nblk_tile; c += 32) acc = rowacc_merge(acc, rowacc_unpack(__ldcg(&recs[c])));
+        acc = warp_rowacc(acc);
+        const bool valid = !acc.bad && acc.mx != -INFINITY;
+        const float M2 = acc.mx * kLog2e;
+        const float S = acc.s;
+        int tile = 0;
+        float tl = INFINITY;
+        if (valid) {
+            const float u = philox_uniform(p.seeds[b], (uint64_t)(p.b_base + b), (uint64_t)(j + 1), 0);
+            draw_locate(p, recs, row, nblk_tile, M2, u * S, tile, tl);
+            const long e0 = (long)tile * kDraftTile + gw * EPW;
+            const long e1 = e0 + EPW < p.V ? e0 + EPW : p.V;
+            if (lane == 0 && e1 > e0) bulk_prefetch_l2(Wt + (size_t)e0 * p.r, (unsigned)((e1 - e0) * p.r * 2));
+            const int xp = prev_token(p, prev, row);
+            float uu[8];
+            {
+                uint4 uw = make_uint4(0u, 0u, 0u, 0u);
+                if (has && xp >= 0 && xp < p.V)   // a valid row always has a valid previous token
+                    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                                 : "=r"(uw.x), "=r"(uw.y), "=r"(uw.z), "=r"(uw.w)
+                                 : "l"(U + (size_t)xp * p.r + lane * 8));
+                const uint32_t a[4] = {uw.x, uw.y, uw.z, uw.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    uu[2 * k] = __uint_as_float(a[k] << 16);
+                    uu[2 * k + 1] = __uint_as_float(a[k] & 0xffff0000u);
+                }
+            }
+#pragma unroll 1
+            for (int h = 0; h < EPW / kZBatch; ++h) {
+                const long base = e0 + h * kZBatch;
+                uint4 w[kZBatch];
+#pragma unroll
+                for (int q = 0; q < kZBatch; ++q) {
+                    w[q] = make_uint4(0u, 0u, 0u, 0u);
+                    if (has && base + q < p.V)
+                        asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                                     : "=r"(w[q].x), "=r"(w[q].y), "=r"(w[q].z), "=r"(w[q].w)
+                                     : "l"(Wt + (size_t)(base + q) * p.r + lane * 8));
+                }
+                float zl = 0.0f;
+                if (lane < kZBatch && base + lane < p.V) zl = load_one(lrow + base + lane);
+#pragma unroll
+                for (int q = 0; q < kZBatch; ++q) {
+                    const uint32_t a[4] = {w[q].x, w[q].y, w[q].z, w[q].w};
+                    float part = 0.0f;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        part = fmaf(uu[2 * k], __uint_as_float(a[k] << 16), part);
+                        part = fmaf(uu[2 * k + 1], __uint_as_float(a[k] & 0xffff0000u), part);
+                    }
+                    part = warp_sum(part);
+                    if (lane == q) z_s[gw * EPW + h * kZBatch + q] = base + q < p.V ? zl + part : -INFINITY;
+                }
+            }
+        }
+        draw_group_sync(grp);
+        if (gw == 0) {
+            int x = -1;
+            float qx = NAN, conf = NAN;
+            if (valid) {
+                conf = ex2(fmaf(acc.mx, kLog2e, -M2)) / S;
+                float z[4];
+                long v[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    v[i] = (long)tile * kDraftTile + 32 * i + lane;
+                    z[i] = v[i] < p.V ? z_s[32 * i + lane] : -INFINITY;
+                }
+                int found = -1;
+                float zf = 0.0f;
+                draw_scan_tile(z, v, p.V, M2, tl, tile, found, zf);
+                x = found;
+                qx = wexp(zf, M2) / S;
+            }
+            if (lane == 0) {
+                p.tokens_out[row] = x;
+                p.conf_out[row] = conf;
+                if (p.qtok_out) p.qtok_out[row] = qx;
+                cur[row] = x;
+                if (pass > 0 && __ldcg(&prev[row]) != x) atomicOr(&p.changed[pass], 1u);
+            }
+        }
+        draw_group_sync(grp);   // the group's z_s is free for its next row
     }
 }
 

@@ -510,7 +510,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             if (!grid_barrier(gb, nb, p.status)) { ok = false; break; }
             if (pass == 0 && threadIdx.x == 0) { pre_issued = s_pre; it_p = s_pre; }
-            finalize_rows<LT, bf16_t>(p, pass, use_bias, prev, cur, gridDim.x, s_uw);
+            if (use_bias) finalize_rows_t1g<LT>(p, pass, prev, cur, gridDim.x, s_uw_all);
+            else finalize_rows<LT, bf16_t>(p, pass, use_bias, prev, cur, gridDim.x, s_uw);
             if (!grid_barrier(gb, nb, p.status)) { ok = false; break; }
             if (pass >= 1 && __ldcg(&p.changed[pass]) == 0u) break;
             if (pass == p.gamma) break;
