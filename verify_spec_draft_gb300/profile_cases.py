@@ -1,11 +1,12 @@
 """Launch one operation a few times on a synthetic workload, for profiler captures.
 
-    python -m verify_spec_draft_gb300.profile_cases {draft,verify_t0,verify_t1,e2etv} [--launches N]
+    python -m verify_spec_draft_gb300.profile_cases {draft,draft_t1,verify_t0,verify_t1,e2etv} [--launches N]
 
 Nothing is timed here; the point is a short process with a handful of launches of one
 kernel, on inputs larger than L2 (129 MB) but only a few hundred MB on the device:
 
   draft      spec_draft_block, B=1, gamma=15, V=248320, r=256, T=0 (151 MB: logits, U, Wt)
+  draft_t1   spec_draft_block, B=32, gamma=7, V=248320, r=256, T=1 (365 MB: logits, U, Wt)
   verify_t0  spec_verify T=0 on the 16 target rows of the same workload (8 MB; below L2)
   verify_t1  spec_verify T=1, B=32, gamma=7, V=248320 (238 MB of target and draft rows)
   e2etv      spec_e2etv on 64 branches x Wb=7 = 448 rows, V=248320 (445 MB in, 222 MB out):
@@ -18,7 +19,7 @@ import torch
 
 from . import draft_block, e2etv, load, synth, verify
 
-CASES = ("draft", "verify_t0", "verify_t1", "e2etv")
+CASES = ("draft", "draft_t1", "verify_t0", "verify_t1", "e2etv")
 
 
 def main(argv=None):
@@ -36,6 +37,11 @@ def main(argv=None):
         else:
             ref = verify(inp["target"], None, out["tokens"], 0)
             run = lambda: verify(inp["target"], None, out["tokens"], 0, ws=ref["ws"], out=ref)
+    elif args.case == "draft_t1":
+        inp = synth.config_inputs(4, device=dev)
+        out = draft_block(inp["draft"], inp["anchor"], inp["U"], inp["Wt"], 1, inp["seeds"])
+        run = lambda: draft_block(inp["draft"], inp["anchor"], inp["U"], inp["Wt"], 1, inp["seeds"], ws=out["ws"],
+                                  out=out)
     elif args.case == "verify_t1":
         inp = synth.config_inputs(4, device=dev)
         tok = synth.draft_tokens(inp["draft"], 1, seed=inp["cfg"].seed)
