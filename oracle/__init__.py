@@ -21,6 +21,8 @@ the pages step by step, in their order and notation:
 * ``anchors`` - the SpecOPD anchor-branch plan: distinct random anchors on each
   reference response, the anchor tokens, and the parent map and semantic positions
   that pack the drafted branches into one proposal tree.
+* ``topk``    - top-k / top-p filtered sampling at T=1 (the DSpine card's setting) for
+  the draft's draws and the target's verification.
 * ``schedule`` - the DSpark verify budget: per-request pass products of the confidences,
   the budget given to the most likely positions across the batch, the throughput
   against a cost curve.
@@ -29,4 +31,4 @@ Pins (tests that tie each function to the pages or to mathematics rather than to
 itself) live in ``tests/test_oracle_*.py``; each function's docstring names them.
 """
 
-from . import philox, draft, verify, e2etv, schedule, anchors  # noqa: F401
+from . import philox, draft, verify, e2etv, schedule, anchors, topk  # noqa: F401
