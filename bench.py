@@ -392,6 +392,28 @@ def secondary(args, torch, vsd, synth, dev, hbm, hbm_kind, sampler, rank=0, worl
                      "algorithmic_bytes_per_launch": byts},
         "gpu_launches": 2 * steps,
     }
+    # the same rows verified against top-k / top-p filtered distributions (the DSpine
+    # card's sampling setting: top_k 20, top_p 0.95)
+    k, top_p = 20, 0.95
+    otk = vsd.verify_topk(t, d, tok, k, top_p, seeds)
+    fn, graphed = capture(lambda: vsd.verify_topk(t, d, tok, k, top_p, seeds, ws=otk["ws"], out=otk), torch)
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    sampler.active = True
+    total, _ = time_steps(torch, fn, steps)
+    sampler.active = False
+    ms = sum(total) / len(total)
+    ach = byts / (ms * 1e-3) / 1e9
+    out["verify_t1_topk_b32"] = {
+        "workload": "verify T=1 with top_k 20, top_p 0.95, B=32, gamma=7, V=248320, bf16, per-request seeds",
+        "value": rows / (ms * 1e-3), "unit": "rows/s", "us_per_step": ms * 1e3, "cuda_graphs": graphed,
+        "accepted_mean_n": float(otk["n"].float().mean().item()),
+        "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "peak_kind": hbm_kind, "unit": "GB/s",
+                     "frac": ach / hbm, "frac_of_nominal_8tbs": ach / NOMINAL_HBM_GBS,
+                     "algorithmic_bytes_per_launch": byts},
+        "gpu_launches": 3 * steps,
+    }
     del t, d, inp
     torch.cuda.empty_cache()
 

@@ -84,7 +84,8 @@ typedef enum {
     SPEC_OP_VERIFY = 1,
     SPEC_OP_E2ETV = 2,
     SPEC_OP_DRAFT_VERIFY = 3,
-    SPEC_OP_BRANCH_PLAN = 4
+    SPEC_OP_BRANCH_PLAN = 4,
+    SPEC_OP_VERIFY_TOPK = 5
 } spec_op;
 
 /* Device status flags (OR-ed into the workspace status word). */
@@ -98,6 +99,7 @@ typedef enum {
 #define SPEC_MAX_V (1 << 26)   /* vocabulary size                                  */
 #define SPEC_MAX_DRAFT_ROWS (1 << 20)   /* spec_draft_block: B * gamma             */
 #define SPEC_MAX_TRUNK 16384   /* spec_branch_plan: tokens of one reference        */
+#define SPEC_MAX_TOP_K 32      /* spec_verify_topk: largest top_k                  */
 
 /*
  * spec_workspace_bytes - workspace size for one operation (host only, pure).
@@ -106,6 +108,7 @@ typedef enum {
  *          SPEC_OP_E2ETV: B = number of branches, gamma = branch length Wb, r unused.
  *          SPEC_OP_BRANCH_PLAN: the status word only (pass B = references, gamma =
  *          W, V = Lmax, r = 0).
+ *          SPEC_OP_VERIFY_TOPK: B requests, gamma positions (V and r unused).
  *          For SPEC_OP_DRAFT the size covers one launch's slice of requests, which
  *          spec_draft_block reuses across the slices of a larger batch.
  * Returns 0 for arguments outside the supported ranges.
@@ -366,6 +369,36 @@ spec_status spec_e2etv(const uint16_t *target_logits, const uint16_t *draft_logi
 spec_status spec_e2etv_shard(const uint16_t *target_logits, const uint16_t *draft_logits,
                              int n_branches, int Wb, int V, int total_branches, float *a_out,
                              float *surv_out, float *msum_out, uint16_t *grad_out,
+                             void *workspace, size_t workspace_bytes, spec_stream_t stream);
+
+/*
+ * spec_verify_topk - spec_verify at T=1 against top-k / top-p filtered rows.
+ *
+ * Defines ("DSpine card numbers and public file headers", aiwithghost.com, section on
+ * raising the temperature: sampling at T=1 with top_p 0.95 and top_k 20; the rejection
+ * rule as for spec_verify).  The page names only the setting; the reading is:
+ *   filter(row): the top_k largest logits (ties to the lowest index), renormalised over
+ *   them; the kept set is the shortest prefix, in descending order, whose running sum
+ *   reaches top_p (at least one entry); p_f is p on the kept set, renormalised.
+ *   For j = 1..gamma: accept iff u_j * q_f(x_j) < p_f(x_j), u_j = Philox(seed_b; b, j, 1),
+ *   with p_f from target row j-1 and q_f from draft row j-1; at the first rejection k,
+ *   y is drawn from max(0, p_f - q_f) normalised (from p_f if that is all zero) with
+ *   Philox(seed_b; b, k, 2); if all are accepted, y is drawn from the filtered target
+ *   row gamma with Philox(seed_b; b, gamma+1, 3).  Draws are the inverse CDF in
+ *   vocabulary-index order.
+ *   target_logits, draft_logits, draft_tokens, seeds, outputs: as spec_verify at T=1.
+ *   top_k   1 <= top_k <= SPEC_MAX_TOP_K.
+ *   top_p   0 < top_p <= 1 (a double, so the cut-off is the caller's exact value).
+ *   workspace  spec_workspace_bytes(SPEC_OP_VERIFY_TOPK, B, gamma, V, 0).
+ * A request with a token outside [0, V) or a row without a distribution (NaN, +inf or
+ * no finite entry) among its 2*gamma+1 rows gets n = -1, committed and bonus -1 (flag
+ * TOKEN).  Limits: 1 <= B <= 65535, 1 <= gamma <= SPEC_MAX_GAMMA, 1 <= V <= SPEC_MAX_V.
+ */
+spec_status spec_verify_topk(const void *target_logits, spec_dtype target_dtype,
+                             const void *draft_logits, spec_dtype draft_dtype,
+                             const int32_t *draft_tokens, int B, int gamma, int V, int top_k,
+                             double top_p, const uint64_t *seeds, int32_t *n_accepted_out,
+                             int32_t *committed_out, int32_t *bonus_out, int32_t *near_tie_out,
                              void *workspace, size_t workspace_bytes, spec_stream_t stream);
 
 /*

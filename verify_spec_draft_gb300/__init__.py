@@ -25,7 +25,7 @@ STATUS = {
     8: "SPEC_ERR_TOKEN", 9: "SPEC_ERR_WORKSPACE",
 }
 F32, BF16 = 0, 1
-OP_DRAFT, OP_VERIFY, OP_E2ETV, OP_DRAFT_VERIFY, OP_BRANCH_PLAN = 0, 1, 2, 3, 4
+OP_DRAFT, OP_VERIFY, OP_E2ETV, OP_DRAFT_VERIFY, OP_BRANCH_PLAN, OP_VERIFY_TOPK = 0, 1, 2, 3, 4, 5
 DEV_TIMEOUT, DEV_NONFINITE, DEV_TOKEN = 1, 2, 4
 
 # C signatures of include/spec.h, as ctypes types
@@ -47,6 +47,8 @@ SIGNATURES = {
     "spec_draft_verify": (_i32, [_vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _i32,
                                  _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "spec_verify_budget": (_i32, [_vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp]),
+    "spec_verify_topk": (_i32, [_vp, _i32, _vp, _i32, _vp, _i32, _i32, _i32, _i32, ctypes.c_double, _vp, _vp, _vp,
+                                _vp, _vp, _vp, _sz, _vp]),
     "spec_e2etv_shard": (_i32, [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "spec_branch_plan": (_i32, [_vp, _vp, _i32, _i32, _i32, _i32, ctypes.c_uint64, _vp, _vp, _vp, _vp,
                                 _vp, _sz, _vp]),
@@ -330,6 +332,34 @@ def branch_plan(trunk, lengths, n_anchors, W, seed, ws=None, out=None, stream=No
                                 _ptr(out["anchors"]), _ptr(out["anchor_tok"]), _ptr(out["parent"]),
                                 _ptr(out["position"]), _ptr(ws), ws.numel(), _stream(stream))
     _check(code, "spec_branch_plan")
+    out["ws"] = ws
+    return out
+
+
+def verify_topk(target, draft, tokens, top_k, top_p, seeds, ws=None, out=None, stream=None):
+    """spec_verify_topk (T=1 against top-k / top-p filtered rows).  target [B, gamma+1, V]
+    and draft [B, gamma, V] f32/bf16; tokens [B, gamma] int32; seeds [B] int64.  Returns
+    a dict of device tensors: n [B], committed [B, gamma+1], bonus [B], near [B]."""
+    torch = _torch()
+    lib = load()
+    _need(target, "target")
+    dev = target.device
+    B, G1, V = target.shape
+    G = G1 - 1
+    _need(draft, "draft", dev, None, (B, G, V))
+    _need(tokens, "tokens", dev, torch.int32, (B, G))
+    _need(seeds, "seeds", dev, torch.int64, (B,))
+    if out is None:
+        out = dict(n=torch.empty((B,), dtype=torch.int32, device=dev),
+                   committed=torch.empty((B, G1), dtype=torch.int32, device=dev),
+                   bonus=torch.empty((B,), dtype=torch.int32, device=dev),
+                   near=torch.empty((B,), dtype=torch.int32, device=dev))
+    if ws is None:
+        ws = workspace(OP_VERIFY_TOPK, B, G, V, 0, dev, stream)
+    code = lib.spec_verify_topk(_ptr(target), _dtype_code(target), _ptr(draft), _dtype_code(draft), _ptr(tokens), B, G,
+                                V, int(top_k), float(top_p), _ptr(seeds), _ptr(out["n"]), _ptr(out["committed"]),
+                                _ptr(out["bonus"]), _ptr(out.get("near")), _ptr(ws), ws.numel(), _stream(stream))
+    _check(code, "spec_verify_topk")
     out["ws"] = ws
     return out
 

@@ -56,6 +56,9 @@ size_t spec_workspace_bytes(spec_op op, int B, int gamma, int V, int r) {
         case SPEC_OP_DRAFT_VERIFY:
             if (r < 0 || r > SPEC_MAX_RANK || (long)B * gamma > 4096) return 0;
             return draft_verify_workspace_bytes(B, gamma, V, r);
+        case SPEC_OP_VERIFY_TOPK:
+            if (B > 65535) return 0;
+            return verify_topk_workspace_bytes(B, gamma);
         case SPEC_OP_BRANCH_PLAN:
             return kWsHeaderBytes;   // the status word only
         case SPEC_OP_E2ETV:
@@ -351,6 +354,41 @@ spec_status spec_branch_plan(const int32_t* trunk_tokens, const int32_t* lengths
     p.position_out = position_out;
     p.status = &reinterpret_cast<WsHeader*>(workspace)->status;
     return cuda_status(branch_plan_launch(p, (cudaStream_t)stream));
+}
+
+spec_status spec_verify_topk(const void* target_logits, spec_dtype target_dtype, const void* draft_logits,
+                             spec_dtype draft_dtype, const int32_t* draft_tokens, int B, int gamma, int V, int top_k,
+                             double top_p, const uint64_t* seeds, int32_t* n_accepted_out, int32_t* committed_out,
+                             int32_t* bonus_out, int32_t* near_tie_out, void* workspace, size_t workspace_bytes,
+                             spec_stream_t stream) {
+    if (!dtype_ok(target_dtype) || !dtype_ok(draft_dtype)) return SPEC_ERR_DTYPE;
+    if (B < 1 || B > 65535 || gamma < 1 || gamma > SPEC_MAX_GAMMA || V < 1 || V > SPEC_MAX_V || top_k < 1 ||
+        top_k > SPEC_MAX_TOP_K)
+        return SPEC_ERR_SHAPE;
+    if (!(top_p > 0.0 && top_p <= 1.0)) return SPEC_ERR_INVALID_ARG;
+    if (!target_logits || !draft_logits || !draft_tokens || !seeds || !n_accepted_out || !committed_out ||
+        !bonus_out)
+        return SPEC_ERR_INVALID_ARG;
+    if (!aligned16(target_logits) || !aligned16(draft_logits)) return SPEC_ERR_ALIGN;
+    if (!workspace || workspace_bytes < verify_topk_workspace_bytes(B, gamma)) return SPEC_ERR_WORKSPACE;
+    TopkParams p;
+    memset(&p, 0, sizeof(p));
+    p.target = target_logits;
+    p.draft = draft_logits;
+    p.tdt = target_dtype;
+    p.ddt = draft_dtype;
+    p.tokens = draft_tokens;
+    p.seeds = seeds;
+    p.B = B;
+    p.gamma = gamma;
+    p.V = V;
+    p.k = top_k;
+    p.top_p = top_p;
+    p.n_out = n_accepted_out;
+    p.committed_out = committed_out;
+    p.bonus_out = bonus_out;
+    p.near_out = near_tie_out;
+    return cuda_status(verify_topk_launch(p, workspace, (cudaStream_t)stream));
 }
 
 }  // extern "C"

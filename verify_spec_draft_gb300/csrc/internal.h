@@ -115,6 +115,26 @@ struct E2etvParams {
 size_t e2etv_workspace_bytes(int n_branches, int Wb, int V);
 cudaError_t e2etv_launch(E2etvParams& p, void* ws, cudaStream_t stream);
 
+constexpr int kTopkMax = 32;   // largest top_k of spec_verify_topk
+struct TopkParams {
+    const void* target;        // [B, gamma+1, V]
+    const void* draft;         // [B, gamma, V]
+    int tdt, ddt;
+    const int32_t* tokens;     // [B, gamma]
+    const uint64_t* seeds;     // [B]
+    int B, gamma, V, k;
+    double top_p;
+    int32_t* n_out;
+    int32_t* committed_out;
+    int32_t* bonus_out;
+    int32_t* near_out;         // nullable
+    unsigned* status;
+    unsigned long long* keys;  // [B*(2*gamma+1)][kTopkMax] each row's largest keys
+    unsigned* bad;             // [B*(2*gamma+1)] NaN or +inf in the row
+};
+size_t verify_topk_workspace_bytes(int B, int gamma);
+cudaError_t verify_topk_launch(TopkParams& p, void* ws, cudaStream_t stream);
+
 struct BranchPlanParams {
     const int32_t* trunk;      // [n_refs, Lmax] token ids
     const int32_t* lengths;    // [n_refs]

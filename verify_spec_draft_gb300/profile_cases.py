@@ -1,6 +1,6 @@
 """Launch one operation a few times on a synthetic workload, for profiler captures.
 
-    python -m verify_spec_draft_gb300.profile_cases {draft,draft_t1,verify_t0,verify_t1,e2etv} [--launches N]
+    python -m verify_spec_draft_gb300.profile_cases {draft,draft_t1,verify_t0,verify_t1,verify_topk,e2etv} [--launches N]
 
 Nothing is timed here; the point is a short process with a handful of launches of one
 kernel, on inputs larger than L2 (129 MB) but only a few hundred MB on the device:
@@ -9,6 +9,7 @@ kernel, on inputs larger than L2 (129 MB) but only a few hundred MB on the devic
   draft_t1   spec_draft_block, B=32, gamma=7, V=248320, r=256, T=1 (365 MB: logits, U, Wt)
   verify_t0  spec_verify T=0 on the 16 target rows of the same workload (8 MB; below L2)
   verify_t1  spec_verify T=1, B=32, gamma=7, V=248320 (238 MB of target and draft rows)
+  verify_topk spec_verify_topk on the same rows, top_k 20, top_p 0.95
   e2etv      spec_e2etv on 64 branches x Wb=7 = 448 rows, V=248320 (445 MB in, 222 MB out):
              a 64-anchor slice of the 16 x 64 x 7 layout
 """
@@ -17,9 +18,9 @@ import argparse
 
 import torch
 
-from . import draft_block, e2etv, load, synth, verify
+from . import draft_block, e2etv, load, synth, verify, verify_topk
 
-CASES = ("draft", "draft_t1", "verify_t0", "verify_t1", "e2etv")
+CASES = ("draft", "draft_t1", "verify_t0", "verify_t1", "verify_topk", "e2etv")
 
 
 def main(argv=None):
@@ -42,6 +43,11 @@ def main(argv=None):
         out = draft_block(inp["draft"], inp["anchor"], inp["U"], inp["Wt"], 1, inp["seeds"])
         run = lambda: draft_block(inp["draft"], inp["anchor"], inp["U"], inp["Wt"], 1, inp["seeds"], ws=out["ws"],
                                   out=out)
+    elif args.case == "verify_topk":
+        inp = synth.config_inputs(4, device=dev)
+        tok = synth.draft_tokens(inp["draft"], 1, seed=inp["cfg"].seed)
+        ref = verify_topk(inp["target"], inp["draft"], tok, 20, 0.95, inp["seeds"])
+        run = lambda: verify_topk(inp["target"], inp["draft"], tok, 20, 0.95, inp["seeds"], ws=ref["ws"], out=ref)
     elif args.case == "verify_t1":
         inp = synth.config_inputs(4, device=dev)
         tok = synth.draft_tokens(inp["draft"], 1, seed=inp["cfg"].seed)
