@@ -148,6 +148,27 @@ def test_e2etv_argument_errors(lib):
     assert _e2etv(lib, wsb=100) == 9
 
 
+def test_verify_topk_argument_errors(lib):
+    def call(target=A, tdt=vsd.BF16, draft=A, ddt=vsd.BF16, tokens=A, B=2, G=3, V=100, k=20, top_p=0.95, seeds=A,
+             n=A, com=A, bonus=A, near=0, ws=A, wsb=1 << 30):
+        return lib.spec_verify_topk(target, tdt, draft, ddt, tokens, B, G, V, k, top_p, seeds, n, com, bonus, near,
+                                    ws, wsb, None)
+    assert call(tdt=7) == 3
+    assert call(ddt=7) == 3
+    assert call(k=0) == 2
+    assert call(k=33) == 2                 # more than SPEC_MAX_TOP_K
+    assert call(G=65) == 2
+    assert call(B=0) == 2
+    assert call(top_p=0.0) == 1
+    assert call(top_p=1.5) == 1
+    assert call(top_p=float("nan")) == 1
+    assert call(seeds=0) == 1
+    assert call(draft=0) == 1
+    assert call(target=MIS) == 4
+    assert call(wsb=100) == 9
+    assert lib.spec_workspace_bytes(vsd.OP_VERIFY_TOPK, 32, 7, 248320, 0) > 0
+
+
 def test_e2etv_shard_argument_errors(lib):
     def call(target=A, draft=A, N=2, Wb=3, V=100, total=4, a=A, surv=A, msum=A, grad=A, ws=A, wsb=1 << 30):
         return lib.spec_e2etv_shard(target, draft, N, Wb, V, total, a, surv, msum, grad, ws, wsb, None)
