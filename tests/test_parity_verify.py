@@ -164,3 +164,34 @@ def test_configs_full_size(spec, cfg_id, T):
     near = _compare(g, o, allow_near=(T == 1))
     assert near <= max(1, c.B // 16)
     assert vsd.device_status(out["ws"]) == 0
+
+
+def test_t1_expected_accepts_monte_carlo(spec):
+    """Prefix-independent rows (every request has the same target and draft rows, no
+    Markov bias): E[n] = sum_j prod_{i<=j} a_i exactly, with a_i = sum_v min(p_i, q_i)
+    (the SpecOPD summary's survival product).  1e5 requests, each with its own Philox
+    seed and draft tokens drawn from q on the host, agree within 4 standard errors."""
+    from oracle import e2etv as oe
+    from oracle._rows import softmax
+    G, V, per_call, calls = 3, 16, 50000, 2
+    rng = np.random.default_rng(123)
+    tgt = rng.normal(0, 1.5, size=(G + 1, V)).astype(np.float32)
+    drf = (tgt[:G] + rng.normal(0, 1.0, size=(G, V))).astype(np.float32)
+    p = [softmax(tgt[i].astype(np.float64))[0] for i in range(G)]
+    q = [softmax(drf[i].astype(np.float64))[0] for i in range(G)]
+    a = np.array([oe.overlap(p[i], q[i])[0] for i in range(G)])
+    expected = float(np.cumprod(a).sum())
+    ns = []
+    for c in range(calls):
+        B = per_call
+        x = np.stack([rng.choice(V, size=B, p=q[i] / q[i].sum()) for i in range(G)], axis=1)
+        target = torch.from_numpy(np.ascontiguousarray(np.broadcast_to(tgt, (B, G + 1, V))))
+        draft = torch.from_numpy(np.ascontiguousarray(np.broadcast_to(drf, (B, G, V))))
+        tokens = torch.from_numpy(x.astype(np.int32))
+        seeds = torch.arange(B, dtype=torch.int64) + c * B + 1
+        g, _ = _run_gpu(target, draft, tokens, 1, seeds)
+        ns.append(g["n"].numpy())
+    n = np.concatenate(ns).astype(np.float64)
+    assert (n >= 0).all() and (n <= G).all()
+    se = n.std() / np.sqrt(n.size)
+    assert abs(n.mean() - expected) <= 4 * se, (n.mean(), expected, se)
