@@ -173,20 +173,22 @@ def test_t1_expected_accepts_monte_carlo(spec):
     seed and draft tokens drawn from q on the host, agree within 4 standard errors."""
     from oracle import e2etv as oe
     from oracle._rows import softmax
-    G, V, per_call, calls = 3, 16, 50000, 2
+    G, V, per_call, calls = 3, 1000, 50000, 2
     rng = np.random.default_rng(123)
-    tgt = rng.normal(0, 1.5, size=(G + 1, V)).astype(np.float32)
-    drf = (tgt[:G] + rng.normal(0, 1.0, size=(G, V))).astype(np.float32)
-    p = [softmax(tgt[i].astype(np.float64))[0] for i in range(G)]
-    q = [softmax(drf[i].astype(np.float64))[0] for i in range(G)]
+    t0 = rng.normal(0, 1.5, size=(G + 1, V))
+    tgt_t = torch.from_numpy(t0).to(torch.bfloat16)
+    drf_t = torch.from_numpy(t0[:G] + rng.normal(0, 1.0, size=(G, V))).to(torch.bfloat16)
+    tgt, drf = tgt_t.double().numpy(), drf_t.double().numpy()   # the rounded rows both sides use
+    p = [softmax(tgt[i])[0] for i in range(G)]
+    q = [softmax(drf[i])[0] for i in range(G)]
     a = np.array([oe.overlap(p[i], q[i])[0] for i in range(G)])
     expected = float(np.cumprod(a).sum())
     ns = []
     for c in range(calls):
         B = per_call
         x = np.stack([rng.choice(V, size=B, p=q[i] / q[i].sum()) for i in range(G)], axis=1)
-        target = torch.from_numpy(np.ascontiguousarray(np.broadcast_to(tgt, (B, G + 1, V))))
-        draft = torch.from_numpy(np.ascontiguousarray(np.broadcast_to(drf, (B, G, V))))
+        target = tgt_t.unsqueeze(0).expand(B, G + 1, V).contiguous()
+        draft = drf_t.unsqueeze(0).expand(B, G, V).contiguous()
         tokens = torch.from_numpy(x.astype(np.int32))
         seeds = torch.arange(B, dtype=torch.int64) + c * B + 1
         g, _ = _run_gpu(target, draft, tokens, 1, seeds)
