@@ -5,7 +5,6 @@ Every call below carries at least one invalid argument, so it returns before its
 first CUDA call; fake device addresses are never dereferenced.
 """
 
-import ctypes
 import os
 import re
 

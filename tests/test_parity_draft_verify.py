@@ -6,7 +6,6 @@ verification results are also checked against the float64 oracle run on the draf
 own tokens.
 """
 
-import numpy as np
 import pytest
 import torch
 
