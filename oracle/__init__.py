@@ -23,6 +23,8 @@ the pages step by step, in their order and notation:
   that pack the drafted branches into one proposal tree.
 * ``topk``    - top-k / top-p filtered sampling at T=1 (the DSpine card's setting) for
   the draft's draws and the target's verification.
+* ``tree``    - EAGLE-2 draft trees: path-product scores, the prefix-closed top-m
+  selection, and T=0 verification along the tree's paths.
 * ``schedule`` - the DSpark verify budget: per-request pass products of the confidences,
   the budget given to the most likely positions across the batch, the throughput
   against a cost curve.
@@ -31,4 +33,4 @@ Pins (tests that tie each function to the pages or to mathematics rather than to
 itself) live in ``tests/test_oracle_*.py``; each function's docstring names them.
 """
 
-from . import philox, draft, verify, e2etv, schedule, anchors, topk  # noqa: F401
+from . import philox, draft, verify, e2etv, schedule, anchors, topk, tree  # noqa: F401
