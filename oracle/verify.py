@@ -35,10 +35,13 @@ A request with a draft token outside [0, V) or an invalid row (see ``_rows``) am
 the rows it reads gets n = -1, committed all -1 and bonus -1.
 
 Pins (``tests/test_oracle_verify.py``): constructed drafts with a known first
-mismatch; committed tokens equal the greedy chain read off the target rows; the T=1
-output marginals equal p_1 and p_{k+1} given k acceptances (Monte Carlo, 4 sigma);
-with prefix-independent rows E[n] = sum_j prod_{i<=j} a_i, tying this module to
-``e2etv``'s survival products.
+mismatch; committed tokens equal the greedy chain read off the target rows; at T=1,
+by exhaustive enumeration of every draft path at V <= 8, gamma <= 3 with a
+prefix-dependent Markov draft (each decision integrated exactly over its uniform),
+the first committed token is distributed as p_1, the token after k accepted drafts as
+p_{k+1}, and each acceptance has probability sum_v min(p, q) = 1 - TV; the same
+marginals by Monte Carlo; with prefix-independent rows E[n] = sum_j prod_{i<=j} a_i,
+tying this module to ``e2etv``'s survival products.
 """
 
 import numpy as np
@@ -47,11 +50,16 @@ from . import philox
 from ._rows import NEAR_TIE, as_f64, row_valid, softmax, argmax_lowest, inverse_cdf
 
 
-def verify_request(target, draft, tokens, temperature, seed, b):
+def verify_request(target, draft, tokens, temperature, seed, b, uniform=None):
     """Verify one request.  target [gamma+1, V], draft [gamma, V] or None, tokens [gamma].
 
-    Returns dict(n, committed [gamma+1], bonus, near).
+    ``uniform`` (optional) is a callable (j, stream) -> u in [0, 1) that replaces the
+    Philox draw u = Philox(seed; b, j, stream); the exhaustive pin integrates the rule
+    over it.  Returns dict(n, committed [gamma+1], bonus, near).
     """
+    if uniform is None:
+        def uniform(j, stream):
+            return philox.uniform(seed, b, j, stream)
     P = as_f64(target)
     gamma = P.shape[0] - 1
     V = P.shape[1]
@@ -82,7 +90,7 @@ def verify_request(target, draft, tokens, temperature, seed, b):
         p, _, _ = softmax(P[j - 1])
         q, _, _ = softmax(Q[j - 1])
         xj = x[j - 1]
-        u = philox.uniform(seed, b, j, philox.STREAM_ACCEPT)
+        u = uniform(j, philox.STREAM_ACCEPT)
         if abs(u * q[xj] - p[xj]) < NEAR_TIE * q[xj]:
             near = True
         if u * q[xj] < p[xj]:
@@ -90,13 +98,13 @@ def verify_request(target, draft, tokens, temperature, seed, b):
         resid = np.maximum(0.0, p - q)
         if not resid.sum() > 0:
             resid = p
-        y, nr = inverse_cdf(resid, philox.uniform(seed, b, j, philox.STREAM_RESIDUAL))
+        y, nr = inverse_cdf(resid, uniform(j, philox.STREAM_RESIDUAL))
         n = j - 1
         committed[:n] = x[:n]
         committed[n] = y
         return dict(n=n, committed=committed, bonus=y, near=near or nr)
     p_last, _, _ = softmax(P[gamma])
-    y, nr = inverse_cdf(p_last, philox.uniform(seed, b, gamma + 1, philox.STREAM_BONUS))
+    y, nr = inverse_cdf(p_last, uniform(gamma + 1, philox.STREAM_BONUS))
     committed[:gamma] = x
     committed[gamma] = y
     return dict(n=gamma, committed=committed, bonus=y, near=near or nr)
