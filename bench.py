@@ -4,9 +4,11 @@
 Headline workload (one step = the whole path of a decode step at B=1):
     spec_draft_block (gamma=15, V=248320, rank-256 Markov bias, T=0)
   + spec_verify      (16 target rows, T=0)
-timed as the two calls in one CUDA graph (the headline), and also as
-spec_draft_verify, the one-call form of the two (same outputs, one launch); on seeded
-synthetic logits (verify_spec_draft_gb300/synth.py, configuration 3).
+timed as spec_draft_verify, the one-call form of the two (the verify kernel is the
+programmatic dependent of the draft kernel, so its target-row pass overlaps the
+draft), in one CUDA graph; the two calls made separately are timed too (same
+outputs); on seeded synthetic logits (verify_spec_draft_gb300/synth.py,
+configuration 3).
 Metric: verify rows per second over the whole draft+verify step, with the step's
 microseconds alongside, and the dominant kernel's fraction of the HBM roofline.
 
@@ -216,37 +218,37 @@ def run_ours(args, rank, world, torch, dist):
         do_draft()
         do_verify()
 
-    # the headline step: the two calls in one graph (the verify launch may overlap the
-    # draft kernel inside it); then the one-call form and each call alone
+    # the headline step: spec_draft_verify in one graph (its verify kernel overlaps the
+    # draft kernel); then the two calls made separately, and each call alone
     g_fused, graphed_f = capture(do_fused, torch)
     g_step, graphed_s = capture(do_step, torch)
     g_draft, graphed_d = capture(do_draft, torch)
     g_verify, graphed_v = capture(do_verify, torch)
     for _ in range(args.warmup):
         flush()
-        g_step()
+        g_fused()
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     sampler.active = True
     t_wall = time.perf_counter()
-    total, _ = time_steps(torch, g_step, args.steps, flush=flush)
+    total, _ = time_steps(torch, g_fused, args.steps, flush=flush)
     t_wall = time.perf_counter() - t_wall
     sampler.active = False
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     n_part = max(20, min(args.steps, 200))
-    t_one, _ = time_steps(torch, g_fused, n_part, flush=flush)
+    t_two, _ = time_steps(torch, g_step, n_part, flush=flush)
     t_draft, _ = time_steps(torch, g_draft, n_part, flush=flush)
     t_verify, _ = time_steps(torch, g_verify, n_part, flush=flush)
     ms_step = sum(total) / len(total)
-    ms_one = sum(t_one) / len(t_one)
+    ms_two = sum(t_two) / len(t_two)
     ms_draft = sum(t_draft) / len(t_draft)
     ms_verify = sum(t_verify) / len(t_verify)
     if world > 1:
-        ms_step, ms_one, ms_draft, ms_verify = (shard.max_over_ranks(x, dev) for x in (ms_step, ms_one, ms_draft,
+        ms_step, ms_two, ms_draft, ms_verify = (shard.max_over_ranks(x, dev) for x in (ms_step, ms_two, ms_draft,
                                                                                       ms_verify))
     passes = int(out_f["passes"].item())
     rows = B * (G + 1)
@@ -268,11 +270,11 @@ def run_ours(args, rank, world, torch, dist):
         "warmup": args.warmup,
         "ms_per_step": ms_step,
         "draft_verify_us": ms_step * 1e3,
-        "one_call_step_us": ms_one * 1e3,
+        "two_call_step_us": ms_two * 1e3,
         "draft_us": ms_draft * 1e3,
         "verify_us": ms_verify * 1e3,
-        "note_parts": "draft_verify_us: spec_draft_block + spec_verify in one graph; one_call_step_us: "
-                      "spec_draft_verify (one launch, same outputs); draft_us and verify_us time each call alone",
+        "note_parts": "draft_verify_us: spec_draft_verify (the headline step); two_call_step_us: spec_draft_block "
+                      "then spec_verify in one graph (same outputs); draft_us and verify_us time each call alone",
         "verify_only_rows_per_s": rows / (ms_verify * 1e-3),
         "higher_is_better": True,
         "scaling": "weak",
@@ -285,8 +287,9 @@ def run_ours(args, rank, world, torch, dist):
             "fixed_point_passes": passes,
             "accepted_n": n_acc,
             "cuda_graphs": bool(graphed_f and graphed_s and graphed_d and graphed_v),
-            "step": "one CUDA graph: spec_draft_block then spec_verify; verify's target-row pass may overlap the "
-                    "draft kernel (programmatic dependent launch) and waits for it before reading the tokens",
+            "step": "one CUDA graph of spec_draft_verify: the draft kernel, then the verify kernel as its "
+                    "programmatic dependent (its target-row pass overlaps the draft; it waits for the draft "
+                    "before reading the tokens)",
             "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write), outside the timed events",
             "parallelism": f"replicas x{world} (independent requests per GPU, no collective)",
         },
@@ -354,7 +357,34 @@ def run_ours(args, rank, world, torch, dist):
     result["clocks"] = sampler.summary()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(inp, budget_s=20.0)
+    result["summary"] = summary(result)
     return result
+
+
+def summary(result):
+    """The numbers of every workload in a few hundred characters, last on the line (so
+    that a tail of the output still holds all of them)."""
+    r3 = lambda x: None if x is None else float(f"{x:.4g}")
+    out = {"draft_verify_us": r3(result["draft_verify_us"]), "draft_us": r3(result["draft_us"]),
+           "draft_frac": r3(result["roofline"]["frac"])}
+    sec = result.get("secondary", {})
+    for key, name, scale, unit in (("verify_t1_b32", "verify_t1_b32", 1e-6, "Mrows_s"),
+                                   ("verify_t1_topk_b32", "verify_topk_b32", 1e-6, "Mrows_s"),
+                                   ("e2etv_cfg5", "e2etv", 1e-6, "Mtok_s"),
+                                   ("tree_verify_t0", "tree_verify", 1e-6, "Mrows_s"),
+                                   ("draft_t1_b32", "draft_t1_b32", 1e-6, "Mrows_s"),
+                                   ("anchor_branches", "sampler", 1e-3, "kbranch_s")):
+        v = sec.get(key)
+        if not v:
+            continue
+        t = v.get("us_per_step")
+        out[name + ("_us" if t is not None else "_ms")] = r3(t if t is not None else v.get("ms_per_step"))
+        out[f"{name}_{unit}"] = r3(v["value"] * scale)
+        out[name + "_frac"] = r3(v["roofline"].get("frac"))
+    cb = result.get("cpu_baseline", {})
+    for k, v in cb.get("configs", {}).items():
+        out["oracle_" + k] = [r3(v.get("value_1core")), r3(v.get("value_all")), v.get("unit")]
+    return out
 
 
 def secondary(args, torch, vsd, synth, dev, hbm, hbm_kind, sampler, rank=0, world=1):
@@ -593,6 +623,83 @@ def blas_threads():
         return int(os.environ.get("OPENBLAS_NUM_THREADS", os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1)))
 
 
+def cpu_model():
+    """The host CPU as /proc/cpuinfo names it (Arm cores list implementer and part)."""
+    arm_parts = {"0xd4f": "Arm Neoverse-V2", "0xd40": "Arm Neoverse-V1", "0xd0c": "Arm Neoverse-N1"}
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+    except OSError:
+        return None
+    for line in info.splitlines():
+        if line.lower().startswith("model name"):
+            return line.split(":", 1)[1].strip()
+    for line in info.splitlines():
+        if line.startswith("CPU part"):
+            part = line.split(":", 1)[1].strip()
+            return arm_parts.get(part, f"Arm CPU part {part}")
+    return None
+
+
+# Oracle work units for the CPU baseline, run in worker processes started with "spawn"
+# (the parent has initialised CUDA) and BLAS limited to one thread per process.  Inputs
+# are generated on the host with the same recipe as the GPU run (synthetic, seeded;
+# the host generator draws other numbers than the CUDA one, with the same shapes and
+# distributions).  Returns (seconds spent in the oracle, units done).
+def _oracle_work(kind, units, seed):
+    import numpy as np
+    import torch
+    from verify_spec_draft_gb300 import synth
+    if kind == "cfg3":       # draft + verify steps, B=1, gamma=15, V=248320, r=256
+        inp = synth.config_inputs(3, device="cpu")
+        L = inp["draft"].double().numpy()
+        tgt = inp["target"].double().numpy()
+        U = inp["U"].double().numpy()
+        Wt = inp["Wt"].double().numpy()
+        anchor = inp["anchor"].numpy()
+        t0 = time.perf_counter()
+        for _ in range(units):
+            oracle_step(L, anchor, U, Wt, tgt)
+        return time.perf_counter() - t0, units * 16
+    if kind == "cfg4":       # verify T=1 of `units` requests, gamma=7, V=248320, Zipf rows
+        from oracle import verify as ov
+        t, d = synth.target_and_draft(units, 7, 248320, "zipf", 0.9, torch.bfloat16, seed=seed)
+        tok = synth.draft_tokens(d, 1, seed=seed)
+        T, D, X = t.double().numpy(), d.double().numpy(), tok.numpy()
+        seeds = np.arange(units, dtype=np.uint64)
+        t0 = time.perf_counter()
+        ov.verify(T, D, X, 1, seeds)
+        return time.perf_counter() - t0, units * 8
+    if kind == "cfg5":       # E2E-TV with the gradient over `units` branches of 7 rows
+        from oracle import e2etv as oe
+        t, d = synth.e2etv_rows(units, 7, 248320, 1.0, seed=seed)
+        T, D = t.double().numpy(), d.double().numpy()
+        t0 = time.perf_counter()
+        oe.e2etv(T, D, units, 7)
+        return time.perf_counter() - t0, units * 7
+    raise ValueError(kind)
+
+
+def _timed_pool(kind, units, workers):
+    """Wall time of `workers` spawn processes doing `units` each, all in parallel; the
+    oracle time is the slowest worker's (set-up excluded)."""
+    import multiprocessing as mp
+    from concurrent.futures import ProcessPoolExecutor
+    saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+    for k in saved:
+        os.environ[k] = "1"
+    try:
+        with ProcessPoolExecutor(max_workers=workers, mp_context=mp.get_context("spawn")) as ex:
+            res = list(ex.map(_oracle_work, [kind] * workers, [units] * workers, range(workers)))
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    return max(r[0] for r in res), sum(r[1] for r in res)
+
+
 def cpu_baseline(inp, budget_s=20.0):
     c = inp["cfg"]
     L = inp["draft"].double().cpu().numpy()
@@ -608,9 +715,29 @@ def cpu_baseline(inp, budget_s=20.0):
         if el >= budget_s or done >= 20:
             break
     rows = done * c.B * (c.gamma + 1)
-    return {"value": rows / el, "unit": "rows/s", "cores": blas_threads(), "kind": "oracle",
-            "sample": f"{done} full draft+verify steps of the headline workload (float64 numpy oracle, "
-                      f"{el:.1f} s)", "host_cpus": os.cpu_count()}
+    out = {"value": rows / el, "unit": "rows/s", "cores": blas_threads(), "kind": "oracle",
+           "sample": f"{done} full draft+verify steps of the headline workload (float64 numpy oracle, "
+                     f"{el:.1f} s)", "host_cpus": os.cpu_count(), "nproc": os.cpu_count(), "cpu_model": cpu_model()}
+    # every configuration's oracle on one core and on all cores (one process per core,
+    # independent requests / branches / steps in parallel), units as the GPU's
+    nproc = os.cpu_count() or 1
+    # (name, work, units on one core, units per process on all cores, process cap, unit);
+    # configuration 3 holds 1 GB of float64 weights per process, hence its cap
+    plan = (("cfg3_draft_verify", "cfg3", 6, 3, 8, "rows/s"), ("cfg4_verify_t1", "cfg4", 256, 32, nproc, "rows/s"),
+            ("cfg5_e2etv", "cfg5", 96, 24, nproc, "tokens/s"))
+    configs = {}
+    try:
+        for name, kind, n1, nall, cap, unit in plan:
+            procs = max(1, min(nproc, cap))
+            t1, u1 = _timed_pool(kind, n1, 1)
+            ta, ua = _timed_pool(kind, nall, procs)
+            configs[name] = {"value_1core": u1 / t1, "value_all": ua / ta, "unit": unit, "cores_all": procs,
+                             "sample": f"1 core: {u1} units in {t1:.1f} s; {procs} processes x {nall} work items "
+                                       f"each in {ta:.1f} s (BLAS 1 thread per process)"}
+    except Exception as e:  # noqa: BLE001
+        configs["error"] = {"unit": None, "note": f"{type(e).__name__}: {e}"[:200]}
+    out["configs"] = configs
+    return out
 
 
 def run_reference(args, rank, world):

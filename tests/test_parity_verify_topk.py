@@ -77,24 +77,22 @@ def test_invalid_requests(spec):
     assert vsd.device_status(out["ws"]) & vsd.DEV_TOKEN
 
 
-def test_config4_full_size_sampled(spec):
+def test_config4_full_size(spec):
     """B=32, gamma=7, V=248320 bf16 rows with the DSpine setting (top_k 20, top_p 0.95),
-    tokens drawn by a filtered drafter: sampled requests against the oracle."""
+    draft tokens sampled from the unfiltered draft rows (so some fall outside the
+    filtered set and must be rejected): every request against the oracle.  Requests the
+    oracle flags as near-ties may differ; they are counted and must stay rare (at most
+    B*gamma/64, as in the other full-size T=1 comparisons)."""
     inp = synth.config_inputs(4, device="cuda")
     c = inp["cfg"]
     k, top_p = 20, 0.95
     d = inp["draft"]
-    rows = [0, 5, 17, 31]
     tok = synth.draft_tokens(d, 1, seed=c.seed)
     out = vsd.verify_topk(inp["target"], d, tok, k, top_p, inp["seeds"])
     torch.cuda.synchronize()
-    t_np = inp["target"][rows].double().cpu().numpy()
-    d_np = d[rows].double().cpu().numpy()
-    seeds = inp["seeds"].cpu().numpy()
-    n = out["n"].cpu().numpy()
-    com = out["committed"].cpu().numpy()
-    for i, b in enumerate(rows):
-        r = ot.verify_request_filtered(t_np[i], d_np[i], tok[b].cpu().numpy(), int(seeds[b]), b, k, top_p)
-        if not r["near"]:
-            assert n[b] == r["n"] and (com[b] == r["committed"]).all(), b
+    ref = ot.verify_filtered(inp["target"].double().cpu().numpy(), d.double().cpu().numpy(), tok.cpu().numpy(),
+                             inp["seeds"].cpu().numpy(), k, top_p)
+    B, G = c.B, c.gamma
+    same = _compare(out, ref, max_near=B * G // 64)
+    assert same >= B - B * G // 64
     assert vsd.device_status(out["ws"]) == 0

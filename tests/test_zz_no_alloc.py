@@ -101,3 +101,30 @@ def test_noalloc_rejects_problems_beyond_the_scratch():
     a = ctypes.c_void_p(A)
     code = lib.spec_verify_noalloc(a, vsd.BF16, a, vsd.BF16, a, B, gamma, V, 1, a, a, a, a, None, None)
     assert code == 2   # SPEC_ERR_SHAPE
+
+
+@pytest.mark.gpu
+def test_noalloc_reports_an_invalid_request(spec):
+    """The status word lives in the shared array, so this entry point reports a device
+    condition only through the outputs: a request whose draft row holds a NaN comes back
+    with n = -1 and bonus -1, the others as spec_verify gives them, and the next call
+    (on clean rows) is not affected by what the first left in the array."""
+    lib = spec.load()
+    dev = torch.device("cuda")
+    B, gamma, V = 4, 5, 3000
+    t, d = synth.target_and_draft(B, gamma, V, "zipf", 0.7, torch.float32, seed=91, device=dev)
+    tokens = synth.draft_tokens(d, 1, seed=91)
+    seeds = synth.seeds_for(B, 9, dev)
+    bad = d.clone()
+    bad[2, 1, 17] = float("nan")          # request 2 has no distribution at position 2
+    ref = vsd.verify(t, d, tokens, 1, seeds)
+    first, second = _outputs(B, gamma, dev), _outputs(B, gamma, dev)
+    _noalloc(lib, t, bad, tokens, 1, seeds, first)
+    _noalloc(lib, t, d, tokens, 1, seeds, second)
+    torch.cuda.synchronize()
+    assert int(first["n"][2]) == -1 and int(first["bonus"][2]) == -1
+    assert (first["committed"][2] == -1).all()
+    keep = [0, 1, 3]
+    for k in ("n", "committed", "bonus", "near"):
+        assert torch.equal(first[k][keep], ref[k][keep]), k
+        assert torch.equal(second[k], ref[k]), k

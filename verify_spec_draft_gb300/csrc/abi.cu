@@ -256,6 +256,7 @@ spec_status spec_draft_verify(const void* draft_logits, spec_dtype logits_dtype,
     v.n_out = n_accepted_out;
     v.committed_out = committed_out;
     v.bonus_out = bonus_out;
+    v.after_own_draft = 1;
     verify_bind_workspace(v, draft_verify_verify_ws(workspace, B, gamma, V, r));
     v.status = p.status;
     return cuda_status(verify_launch(v, (cudaStream_t)stream));

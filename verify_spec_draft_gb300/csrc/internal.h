@@ -22,6 +22,11 @@ struct VerifyParams {
     int B, gamma, V, temperature;
     int nchunk;                // ceil(V / kVerifyChunk)
     int vec_t, vec_d;          // rows 16-byte aligned (vector loads allowed)
+    int after_own_draft;       // T=0: launched as the programmatic dependent of the
+                               // library's own draft kernel (spec_draft_verify), whose
+                               // start already followed every producer of the target
+                               // rows; otherwise the kernel waits for the previous
+                               // kernel on the stream before it reads anything
     int32_t* n_out;
     int32_t* committed_out;
     int32_t* bonus_out;
