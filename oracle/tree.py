@@ -14,7 +14,9 @@ The pages give no formula; the readings taken here:
 
   A tree has nodes 0..n-1 in topological order: parent[i] is -1 (the root, the last
   committed token) or a node before i; token[i] is node i's drafted token and conf[i] its
-  confidence (the probability that it passes given that its parent passed).
+  confidence (the probability that it passes given that its parent passed).  A tree
+  with a parent outside [-1, i) is not a tree in this order: it has no scores (NaN), no
+  selection, and its verification is invalid (n = -1).
   score[i] = conf[i] * score[parent[i]], the root's score being 1.
   select(m): the m nodes with the largest scores, ties to the lower index, listed in
   index order.  Scores never grow along a path and a parent has the lower index, so the
@@ -29,7 +31,8 @@ The pages give no formula; the readings taken here:
 Pins (``tests/test_oracle_tree.py``): a chain reduces to the block verification of
 ``verify`` at T=0; the accepted path is the longest one found by enumerating every
 root-to-node path; the selection is prefix-closed and keeps the m largest scores; the
-scores never grow along a path.
+scores never grow along a path; the scores are products of the confidences along the
+path, found by walking up from each node; parents out of order make the tree invalid.
 """
 
 import numpy as np
@@ -37,8 +40,16 @@ import numpy as np
 from ._rows import as_f64, argmax_lowest, row_valid
 
 
+def valid_parents(parent):
+    """True when every parent[i] is -1 or an earlier node (topological order)."""
+    return all(-1 <= int(par) < i for i, par in enumerate(parent))
+
+
 def scores(parent, conf):
-    """Path products score[i] = conf[i] * score[parent[i]] (root 1)."""
+    """Path products score[i] = conf[i] * score[parent[i]] (root 1); NaN for every node
+    of a tree whose parents are not in topological order."""
+    if not valid_parents(parent):
+        return np.full(len(parent), np.nan)
     conf = np.clip(np.nan_to_num(as_f64(conf), nan=0.0), 0.0, 1.0)
     s = np.empty(len(parent))
     for i, par in enumerate(parent):
@@ -47,7 +58,10 @@ def scores(parent, conf):
 
 
 def select(parent, conf, m):
-    """Indices (ascending) of the m nodes with the largest scores, ties to the lower index."""
+    """Indices (ascending) of the m nodes with the largest scores, ties to the lower index
+    (none for a tree whose parents are not in topological order)."""
+    if not valid_parents(parent):
+        return np.array([], dtype=np.int64)
     s = scores(parent, conf)
     order = np.lexsort((np.arange(len(s)), -s))
     return np.sort(order[:int(m)])
@@ -60,6 +74,8 @@ def verify_t0(parent, token, rows, keep=None):
     empty outputs when a row on the walk has no distribution."""
     rows = as_f64(rows)
     n_nodes = len(parent)
+    if not valid_parents(parent):
+        return dict(n=-1, path=[], committed=[], bonus=-1)
     keep = set(range(n_nodes)) if keep is None else set(int(i) for i in keep)
     children = {}
     for i in range(n_nodes):

@@ -113,3 +113,33 @@ def test_pruned_walk_and_degenerate_trees():
     bad = rows.copy()
     bad[1, 2] = np.nan
     assert otr.verify_t0(parent, token, bad)["n"] == -1
+
+
+def test_scores_are_path_products():
+    """Each score is the product of the confidences from the root to the node, found
+    here by walking up the parent map (independent of the oracle's forward recurrence,
+    up to the order of the float64 products)."""
+    rng = np.random.default_rng(7)
+    parent, _ = _random_tree(rng, 40, 100)
+    conf = rng.uniform(0, 1, size=40)
+    conf[3] = np.nan     # read as 0: it and its subtree score 0
+    conf[5] = 1.7        # clamped to 1
+    s = otr.scores(parent, conf)
+    c = np.clip(np.nan_to_num(conf, nan=0.0), 0, 1)
+    for i in range(40):
+        prod, cur = 1.0, i
+        while cur >= 0:
+            prod *= c[cur]
+            cur = int(parent[cur])
+        assert abs(s[i] - prod) <= 1e-15
+
+
+def test_parents_out_of_order_make_the_tree_invalid():
+    rows = np.zeros((4, 3))
+    token = np.array([0, 0, 0])
+    for parent in (np.array([-1, 1, 0]), np.array([-1, 0, 5]), np.array([-2, 0, 1]), np.array([0, 0, 1])):
+        assert not otr.valid_parents(parent)
+        assert np.isnan(otr.scores(parent, [0.5, 0.5, 0.5])).all()
+        assert otr.select(parent, [0.5, 0.5, 0.5], 2).size == 0
+        assert otr.verify_t0(parent, token, rows)["n"] == -1
+    assert otr.valid_parents(np.array([-1, 0, 0, 2, -1]))
