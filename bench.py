@@ -447,6 +447,68 @@ def secondary(args, torch, vsd, synth, dev, hbm, hbm_kind, sampler, rank=0, worl
     del t, d, inp
     torch.cuda.empty_cache()
 
+    # draft trees: 32 trees x 64 nodes over V = 248320 bf16 rows (2080 rows, 1.03 GB > L2):
+    # T=0 verification of every node, then the EAGLE-2 step of keeping the top 24 nodes
+    # by path product and verifying only those
+    tc = synth.TREE_CONFIG
+    x = synth.tree_inputs(tc.B, tc.gamma, tc.V, tc.dtype, seed=tc.seed, device=dev, p_match=0.75)
+    T_, n_ = tc.B, tc.gamma
+    ws_t = vsd.workspace(vsd.OP_TREE_VERIFY, T_, n_, tc.V, 0, dev)
+    ot_ = vsd.tree_verify(x["target"], x["parent"], x["token"], ws=ws_t)
+    fn, graphed = capture(lambda: vsd.tree_verify(x["target"], x["parent"], x["token"], ws=ws_t, out=ot_), torch)
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    sampler.active = True
+    total, _ = time_steps(torch, fn, steps)
+    sampler.active = False
+    ms = sum(total) / len(total)
+    rows = T_ * (n_ + 1)
+    byts = rows * tc.V * 2
+    ach = byts / (ms * 1e-3) / 1e9
+    out["tree_verify_t0"] = {
+        "workload": "tree verify T=0: 32 trees x 64 nodes, V=248320 bf16 (root + 64 node rows per tree)",
+        "value": rows / (ms * 1e-3), "unit": "rows/s", "us_per_step": ms * 1e3, "cuda_graphs": graphed,
+        "accepted_mean_n": float(ot_["n"].float().mean().item()),
+        "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "peak_kind": hbm_kind, "unit": "GB/s",
+                     "frac": ach / hbm, "frac_of_nominal_8tbs": ach / NOMINAL_HBM_GBS,
+                     "algorithmic_bytes_per_launch": byts},
+        "gpu_launches": steps,
+    }
+    m_ = 24
+    os_ = vsd.tree_select(x["parent"], x["conf"], m_)
+    op_ = vsd.tree_verify(x["target"], x["parent"], x["token"], keep=os_["keep"], ws=ws_t)
+
+    def select_verify():
+        vsd.tree_select(x["parent"], x["conf"], m_, out=os_)
+        vsd.tree_verify(x["target"], x["parent"], x["token"], keep=os_["keep"], ws=ws_t, out=op_)
+
+    fn, graphed = capture(select_verify, torch)
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    sampler.active = True
+    total, _ = time_steps(torch, fn, steps, flush=lambda: flush_buf.zero_())
+    sampler.active = False
+    del flush_buf
+    ms = sum(total) / len(total)
+    rows = T_ * (m_ + 1)
+    byts = rows * tc.V * 2
+    ach = byts / (ms * 1e-3) / 1e9
+    out["tree_select_verify_m24"] = {
+        "workload": "EAGLE-2 step: top-24 of 64 nodes by path product (32 trees), then T=0 verification of the "
+                    "kept nodes, V=248320 bf16 (L2 flushed)",
+        "value": rows / (ms * 1e-3), "unit": "rows/s", "us_per_step": ms * 1e3, "cuda_graphs": graphed,
+        "accepted_mean_n": float(op_["n"].float().mean().item()),
+        "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "peak_kind": hbm_kind, "unit": "GB/s",
+                     "frac": ach / hbm, "frac_of_nominal_8tbs": ach / NOMINAL_HBM_GBS,
+                     "algorithmic_bytes_per_launch": byts},
+        "gpu_launches": 2 * steps,
+    }
+    del x, ws_t, ot_, os_, op_
+    torch.cuda.empty_cache()
+
     # configuration 5: E2E-TV, 16 x 64 x 7 rows, V=248320; 7.1 GB of inputs.  With N > 1
     # ranks the 1024 branches are split across them (strong scaling for this line): each
     # rank runs its shard and the loss takes one scalar all-reduce per step

@@ -85,7 +85,8 @@ typedef enum {
     SPEC_OP_E2ETV = 2,
     SPEC_OP_DRAFT_VERIFY = 3,
     SPEC_OP_BRANCH_PLAN = 4,
-    SPEC_OP_VERIFY_TOPK = 5
+    SPEC_OP_VERIFY_TOPK = 5,
+    SPEC_OP_TREE_VERIFY = 6
 } spec_op;
 
 /* Device status flags (OR-ed into the workspace status word). */
@@ -100,6 +101,7 @@ typedef enum {
 #define SPEC_MAX_DRAFT_ROWS (1 << 20)   /* spec_draft_block: B * gamma             */
 #define SPEC_MAX_TRUNK 16384   /* spec_branch_plan: tokens of one reference        */
 #define SPEC_MAX_TOP_K 32      /* spec_verify_topk: largest top_k                  */
+#define SPEC_MAX_TREE_NODES 1024  /* spec_tree_select / spec_tree_verify: nodes per tree */
 
 /*
  * spec_workspace_bytes - workspace size for one operation (host only, pure).
@@ -109,6 +111,8 @@ typedef enum {
  *          SPEC_OP_BRANCH_PLAN: the status word only (pass B = references, gamma =
  *          W, V = Lmax, r = 0).
  *          SPEC_OP_VERIFY_TOPK: B requests, gamma positions (V and r unused).
+ *          SPEC_OP_TREE_VERIFY: B = trees, gamma = nodes per tree (0 allowed, up to
+ *          SPEC_MAX_TREE_NODES), V, r unused.
  *          For SPEC_OP_DRAFT the size covers one launch's slice of requests, which
  *          spec_draft_block reuses across the slices of a larger batch.
  * Returns 0 for arguments outside the supported ranges.
@@ -437,6 +441,74 @@ spec_status spec_branch_plan(const int32_t *trunk_tokens, const int32_t *lengths
                              int Lmax, int n_anchors, int W, uint64_t seed, int32_t *anchors_out,
                              int32_t *anchor_tok_out, int32_t *parent_out, int32_t *position_out,
                              void *workspace, size_t workspace_bytes, spec_stream_t stream);
+
+/*
+ * spec_tree_select - EAGLE-2 top-m selection of draft-tree nodes by path product.
+ *
+ * Defines ("Speculative Decoding Part 2: the evolution of drafter architectures", VESSL
+ * AI, EAGLE section: EAGLE-2 scores each branch of a dynamic draft tree by the product
+ * of the confidences from the root and keeps the highest-scored nodes; a parent scores
+ * at least as high as its children, so the kept set holds every kept node's parent).
+ * The page gives no formula; the reading is:
+ *   nodes 0..n-1 of a tree in topological order: parent[i] is -1 (the root, the last
+ *   committed token) or an earlier node;
+ *   score[i] = c[i] * score[parent[i]] (1 at the root), c = conf clamped to [0, 1] with
+ *   NaN read as 0, in float64;
+ *   the m nodes with the largest scores are kept, ties to the lower index.
+ *
+ *   parent        int32 device [n_trees, n_nodes].
+ *   conf          float32 device [n_trees, n_nodes]: the drafter's confidence of each
+ *                 node given its parent (e.g. spec_draft_block's conf_out).
+ *   m             nodes kept per tree, 0 <= m (all nodes when m >= n_nodes).
+ *   score_out     float64 device [n_trees, n_nodes] (nullable): the scores.
+ *   keep_out      int32 device [n_trees, n_nodes]: 1 for a kept node, else 0.
+ *   selected_out  int32 device [n_trees, m] (nullable): the kept nodes in ascending
+ *                 index order, then -1.
+ * A tree with a parent outside [-1, i) gets NaN scores, no kept node and -1 in
+ * selected_out (there is no workspace and no status word).
+ * Limits: 1 <= n_trees <= 65535, 1 <= n_nodes <= SPEC_MAX_TREE_NODES.  One CTA per
+ * tree; nothing is allocated.
+ */
+spec_status spec_tree_select(const int32_t *parent, const float *conf, int n_trees, int n_nodes, int m,
+                             double *score_out, int32_t *keep_out, int32_t *selected_out,
+                             spec_stream_t stream);
+
+/*
+ * spec_tree_verify - T=0 verification of draft trees.
+ *
+ * Defines ("Speculative Decoding Part 2", VESSL AI, EAGLE section: verification of an
+ * EAGLE-2 draft tree; "Solar Open2 DSpark", sionic.ai, sections 1 and 6: the target
+ * commits the longest agreeing prefix and its next token).  The reading is:
+ *   the target row of the root is row 0 of the tree and that of node i is row 1 + i
+ *   (the distribution of the position after the node's token);
+ *   from the root, move to the kept child whose token is the argmax of the current
+ *   node's row (the lowest index among such children; argmax ties to the lowest
+ *   vocabulary index), and stop when there is none;
+ *   n = nodes passed; committed = their tokens in path order, then y = argmax of the
+ *   last node's row (the bonus).
+ * A chain (parent[i] = i - 1) is exactly spec_verify at T=0.
+ *
+ *   target_logits   [n_trees, n_nodes + 1, V], dtype target_dtype; the rows of nodes
+ *                   that are not kept are never read.
+ *   parent, token   int32 device [n_trees, n_nodes] (NULL allowed when n_nodes == 0).
+ *   keep            int32 device [n_trees, n_nodes] (nullable: every node kept); e.g.
+ *                   spec_tree_select's keep_out.
+ *   n_accepted_out  int32 device [n_trees].
+ *   path_out        int32 device [n_trees, n_nodes]: the accepted nodes, then -1.
+ *   committed_out   int32 device [n_trees, n_nodes + 1]: their tokens, y, then -1.
+ *   bonus_out       int32 device [n_trees]: y.
+ *   workspace       spec_workspace_bytes(SPEC_OP_TREE_VERIFY, n_trees, n_nodes, V, 0).
+ * A tree with a parent outside [-1, i) (flag TOKEN), or whose walk reaches a row without
+ * a distribution (NaN, +inf or no finite entry; flag NONFINITE), gets n = -1 and -1
+ * everywhere.  A token outside [0, V) never matches.
+ * Limits: 1 <= n_trees <= 65535, 0 <= n_nodes <= SPEC_MAX_TREE_NODES,
+ * 1 <= V <= SPEC_MAX_V.
+ */
+spec_status spec_tree_verify(const void *target_logits, spec_dtype target_dtype, const int32_t *parent,
+                             const int32_t *token, const int32_t *keep, int n_trees, int n_nodes, int V,
+                             int32_t *n_accepted_out, int32_t *path_out, int32_t *committed_out,
+                             int32_t *bonus_out, void *workspace, size_t workspace_bytes,
+                             spec_stream_t stream);
 
 #ifdef __cplusplus
 }

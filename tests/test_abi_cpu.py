@@ -219,3 +219,31 @@ def test_binding_refuses_cpu_tensors(lib):
     x = torch.zeros((1, 2, 8))
     with pytest.raises(ValueError, match="CUDA tensor"):
         vsd.verify(x, None, torch.zeros((1, 1), dtype=torch.int32))
+
+
+def test_tree_calls_reject_bad_arguments(lib):
+    wb = lib.spec_workspace_bytes
+    assert wb(vsd.OP_TREE_VERIFY, 32, 64, 248320, 0) > 0
+    assert wb(vsd.OP_TREE_VERIFY, 32, 0, 100, 0) > 0            # trees without draft nodes
+    assert wb(vsd.OP_TREE_VERIFY, 32, 1025, 100, 0) == 0
+    assert wb(vsd.OP_TREE_VERIFY, 0, 8, 100, 0) == 0
+    assert wb(vsd.OP_TREE_VERIFY, 4, 1000, 100, 0) > wb(vsd.OP_TREE_VERIFY, 4, 64, 100, 0)
+    a = A
+    sel = lib.spec_tree_select
+    assert sel(a, a, 4, 0, 2, a, a, a, None) == 2                  # no nodes
+    assert sel(a, a, 4, 1025, 2, a, a, a, None) == 2               # too many nodes
+    assert sel(a, a, 4, 8, -1, a, a, a, None) == 2                 # m < 0
+    assert sel(a, a, 0, 8, 2, a, a, a, None) == 2
+    assert sel(None, a, 4, 8, 2, a, a, a, None) == 1
+    assert sel(a, a, 4, 8, 2, a, None, a, None) == 1               # keep_out required
+    tv = lib.spec_tree_verify
+    big = 1 << 30
+    assert tv(a, 7, a, a, a, 4, 8, 100, a, a, a, a, a, big, None) == 3        # dtype
+    assert tv(a, vsd.BF16, a, a, a, 4, 1025, 100, a, a, a, a, a, big, None) == 2
+    assert tv(a, vsd.BF16, a, a, a, 4, 8, 0, a, a, a, a, a, big, None) == 2
+    assert tv(a, vsd.BF16, None, a, a, 4, 8, 100, a, a, a, a, a, big, None) == 1   # parent needed (n > 0)
+    assert tv(a, vsd.BF16, a, a, a, 4, 8, 100, a, None, a, a, a, big, None) == 1   # path_out needed
+    assert tv(MIS, vsd.BF16, a, a, a, 4, 8, 100, a, a, a, a, a, big, None) == 4
+    need = wb(vsd.OP_TREE_VERIFY, 4, 8, 100, 0)
+    assert tv(a, vsd.BF16, a, a, a, 4, 8, 100, a, a, a, a, a, need - 1, None) == 9
+    assert tv(a, vsd.BF16, a, a, a, 4, 8, 100, a, a, a, a, None, big, None) == 9

@@ -25,7 +25,7 @@ STATUS = {
     8: "SPEC_ERR_TOKEN", 9: "SPEC_ERR_WORKSPACE",
 }
 F32, BF16 = 0, 1
-OP_DRAFT, OP_VERIFY, OP_E2ETV, OP_DRAFT_VERIFY, OP_BRANCH_PLAN, OP_VERIFY_TOPK = 0, 1, 2, 3, 4, 5
+OP_DRAFT, OP_VERIFY, OP_E2ETV, OP_DRAFT_VERIFY, OP_BRANCH_PLAN, OP_VERIFY_TOPK, OP_TREE_VERIFY = 0, 1, 2, 3, 4, 5, 6
 DEV_TIMEOUT, DEV_NONFINITE, DEV_TOKEN = 1, 2, 4
 
 # C signatures of include/spec.h, as ctypes types
@@ -52,6 +52,8 @@ SIGNATURES = {
     "spec_e2etv_shard": (_i32, [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "spec_branch_plan": (_i32, [_vp, _vp, _i32, _i32, _i32, _i32, ctypes.c_uint64, _vp, _vp, _vp, _vp,
                                 _vp, _sz, _vp]),
+    "spec_tree_select": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp]),
+    "spec_tree_verify": (_i32, [_vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
 }
 
 _lib = None
@@ -416,5 +418,62 @@ def e2etv(target, draft, n_branches, Wb, ws=None, out=None, stream=None):
     code = lib.spec_e2etv(_ptr(target), _ptr(draft), n_branches, Wb, V, _ptr(out["a"]), _ptr(out["surv"]),
                           _ptr(out["loss"]), _ptr(out["grad"]), _ptr(ws), ws.numel(), _stream(stream))
     _check(code, "spec_e2etv")
+    out["ws"] = ws
+    return out
+
+
+def tree_select(parent, conf, m, out=None, stream=None):
+    """spec_tree_select.  parent int32 [n_trees, n_nodes], conf float32 [n_trees, n_nodes].
+    Returns a dict of device tensors: score float64 [n_trees, n_nodes], keep int32
+    [n_trees, n_nodes] (1 = kept), selected int32 [n_trees, m] (ascending, then -1)."""
+    torch = _torch()
+    lib = load()
+    _need(parent, "parent", None, torch.int32)
+    if parent.dim() != 2:
+        raise ValueError("parent must be [n_trees, n_nodes]")
+    dev = parent.device
+    T, n = parent.shape
+    _need(conf, "conf", dev, torch.float32, (T, n))
+    m = int(m)
+    if out is None:
+        out = dict(score=torch.empty((T, n), dtype=torch.float64, device=dev),
+                   keep=torch.empty((T, n), dtype=torch.int32, device=dev),
+                   selected=torch.empty((T, max(m, 0)), dtype=torch.int32, device=dev))
+    code = lib.spec_tree_select(_ptr(parent), _ptr(conf), T, n, m, _ptr(out.get("score")), _ptr(out["keep"]),
+                                _ptr(out.get("selected")) if m > 0 else _ptr(None), _stream(stream))
+    _check(code, "spec_tree_select")
+    return out
+
+
+def tree_verify(target, parent, token, keep=None, ws=None, out=None, stream=None):
+    """spec_tree_verify (T=0).  target f32/bf16 [n_trees, n_nodes + 1, V] (root row first);
+    parent, token int32 [n_trees, n_nodes]; keep int32 [n_trees, n_nodes] or None (all).
+    Returns a dict of device tensors: n [n_trees], path [n_trees, n_nodes], committed
+    [n_trees, n_nodes + 1], bonus [n_trees]."""
+    torch = _torch()
+    lib = load()
+    _need(target, "target")
+    if target.dim() != 3:
+        raise ValueError("target must be [n_trees, n_nodes + 1, V]")
+    dev = target.device
+    T, R, V = target.shape
+    n = R - 1
+    if n > 0:
+        _need(parent, "parent", dev, torch.int32, (T, n))
+        _need(token, "token", dev, torch.int32, (T, n))
+        if keep is not None:
+            _need(keep, "keep", dev, torch.int32, (T, n))
+    if out is None:
+        out = dict(n=torch.empty((T,), dtype=torch.int32, device=dev),
+                   path=torch.empty((T, n), dtype=torch.int32, device=dev),
+                   committed=torch.empty((T, R), dtype=torch.int32, device=dev),
+                   bonus=torch.empty((T,), dtype=torch.int32, device=dev))
+    if ws is None:
+        ws = workspace(OP_TREE_VERIFY, T, n, V, 0, dev, stream)
+    code = lib.spec_tree_verify(_ptr(target), _dtype_code(target), _ptr(parent if n > 0 else None),
+                                _ptr(token if n > 0 else None), _ptr(keep if n > 0 else None), T, n, V,
+                                _ptr(out["n"]), _ptr(out["path"]) if n > 0 else _ptr(None), _ptr(out["committed"]),
+                                _ptr(out["bonus"]), _ptr(ws), ws.numel(), _stream(stream))
+    _check(code, "spec_tree_verify")
     out["ws"] = ws
     return out

@@ -44,6 +44,10 @@ using namespace spec;
 extern "C" {
 
 size_t spec_workspace_bytes(spec_op op, int B, int gamma, int V, int r) {
+    if (op == SPEC_OP_TREE_VERIFY) {   // gamma is the number of nodes per tree
+        if (B < 1 || B > 65535 || gamma < 0 || gamma > SPEC_MAX_TREE_NODES || V < 1 || V > SPEC_MAX_V) return 0;
+        return tree_verify_workspace_bytes(B, gamma);
+    }
     if (B < 1 || gamma < 1 || gamma > SPEC_MAX_GAMMA || V < 1 || V > SPEC_MAX_V) return 0;
     switch (op) {
         case SPEC_OP_DRAFT:
@@ -260,6 +264,54 @@ spec_status spec_draft_verify(const void* draft_logits, spec_dtype logits_dtype,
     verify_bind_workspace(v, draft_verify_verify_ws(workspace, B, gamma, V, r));
     v.status = p.status;
     return cuda_status(verify_launch(v, (cudaStream_t)stream));
+}
+
+spec_status spec_tree_select(const int32_t* parent, const float* conf, int n_trees, int n_nodes, int m,
+                             double* score_out, int32_t* keep_out, int32_t* selected_out, spec_stream_t stream) {
+    if (n_trees < 1 || n_trees > 65535 || n_nodes < 1 || n_nodes > SPEC_MAX_TREE_NODES || m < 0)
+        return SPEC_ERR_SHAPE;
+    if (!parent || !conf || !keep_out) return SPEC_ERR_INVALID_ARG;
+    TreeSelectParams p;
+    memset(&p, 0, sizeof(p));
+    p.parent = parent;
+    p.conf = conf;
+    p.n_trees = n_trees;
+    p.n_nodes = n_nodes;
+    p.m = m;
+    p.score_out = score_out;
+    p.keep_out = keep_out;
+    p.selected_out = selected_out;
+    return cuda_status(tree_select_launch(p, (cudaStream_t)stream));
+}
+
+spec_status spec_tree_verify(const void* target_logits, spec_dtype target_dtype, const int32_t* parent,
+                             const int32_t* token, const int32_t* keep, int n_trees, int n_nodes, int V,
+                             int32_t* n_accepted_out, int32_t* path_out, int32_t* committed_out, int32_t* bonus_out,
+                             void* workspace, size_t workspace_bytes, spec_stream_t stream) {
+    if (!dtype_ok(target_dtype)) return SPEC_ERR_DTYPE;
+    if (n_trees < 1 || n_trees > 65535 || n_nodes < 0 || n_nodes > SPEC_MAX_TREE_NODES || V < 1 || V > SPEC_MAX_V)
+        return SPEC_ERR_SHAPE;
+    if (!target_logits || !n_accepted_out || !committed_out || !bonus_out) return SPEC_ERR_INVALID_ARG;
+    if (n_nodes > 0 && (!parent || !token || !path_out)) return SPEC_ERR_INVALID_ARG;
+    if (!aligned16(target_logits)) return SPEC_ERR_ALIGN;
+    const size_t need = tree_verify_workspace_bytes(n_trees, n_nodes);
+    if (!workspace || workspace_bytes < need) return SPEC_ERR_WORKSPACE;
+    TreeVerifyParams p;
+    memset(&p, 0, sizeof(p));
+    p.target = target_logits;
+    p.tdt = target_dtype;
+    p.parent = parent;
+    p.token = token;
+    p.keep = n_nodes > 0 ? keep : nullptr;
+    p.n_trees = n_trees;
+    p.n_nodes = n_nodes;
+    p.V = V;
+    p.vec_t = ((size_t)V * dtype_size(target_dtype)) % 16 == 0;
+    p.n_out = n_accepted_out;
+    p.path_out = path_out;
+    p.committed_out = committed_out;
+    p.bonus_out = bonus_out;
+    return cuda_status(tree_verify_launch(p, workspace, (cudaStream_t)stream));
 }
 
 spec_status spec_e2etv(const uint16_t* target_logits, const uint16_t* draft_logits, int n_branches, int Wb, int V,

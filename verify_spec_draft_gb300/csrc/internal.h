@@ -153,6 +153,39 @@ struct BranchPlanParams {
 };
 cudaError_t branch_plan_launch(const BranchPlanParams& p, cudaStream_t stream);
 
+struct TreeSelectParams {
+    const int32_t* parent;     // [n_trees, n_nodes]
+    const float* conf;         // [n_trees, n_nodes]
+    int n_trees, n_nodes, m;
+    double* score_out;         // [n_trees, n_nodes] (nullable)
+    int32_t* keep_out;         // [n_trees, n_nodes]
+    int32_t* selected_out;     // [n_trees, m] (nullable)
+};
+cudaError_t tree_select_launch(const TreeSelectParams& p, cudaStream_t stream);
+
+struct TreeVerifyParams {
+    const void* target;        // [n_trees, n_nodes + 1, V]: root row, then node rows
+    int tdt;
+    const int32_t* parent;     // [n_trees, n_nodes]
+    const int32_t* token;      // [n_trees, n_nodes]
+    const int32_t* keep;       // [n_trees, n_nodes] (nullable: every node kept)
+    int n_trees, n_nodes, V;
+    int vec_t;                 // rows 16-byte aligned
+    int32_t* n_out;            // [n_trees]
+    int32_t* path_out;         // [n_trees, n_nodes]
+    int32_t* committed_out;    // [n_trees, n_nodes + 1]
+    int32_t* bonus_out;        // [n_trees]
+    // workspace regions
+    unsigned* status;
+    unsigned* done;
+    unsigned long long* keys;  // [n_trees * (n_nodes + 1)] argmax keys
+    unsigned* rowbad;          // [n_trees * (n_nodes + 1)]
+    unsigned* first;           // [n_trees * (n_nodes + 1)] n - (lowest matching child) per parent
+    unsigned* treebad;         // [n_trees] parents out of order
+};
+size_t tree_verify_workspace_bytes(int n_trees, int n_nodes);
+cudaError_t tree_verify_launch(TreeVerifyParams& p, void* ws, cudaStream_t stream);
+
 int device_sm_count();
 
 cudaError_t verify_budget_launch(const float* conf, int B, int gamma, int budget, const float* cost,

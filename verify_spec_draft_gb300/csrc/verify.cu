@@ -24,99 +24,11 @@
 //        fences in the streaming phase.
 #include "spec_device.cuh"
 #include "internal.h"
+#include "chunk_rows.cuh"
 
 namespace spec {
 
-constexpr int kEPT = kVerifyChunk / kThreads;   // 32 contiguous entries per thread
-static_assert(kEPT == 32, "chunk layout");
-
 enum { MODE_DONE = 0, MODE_RESID = 1, MODE_BONUS = 2 };
-
-// ----------------------------------------------------------------------------------
-// Raw chunk loads: this thread's 32 entries as 16-byte words, -inf past the row end.
-// ----------------------------------------------------------------------------------
-template <typename T> struct Words { static constexpr int N = kEPT * (int)sizeof(T) / 16; };
-
-__device__ __forceinline__ uint4 partial_words(const float* row, long e0, long V) {
-    uint32_t w[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) w[e] = (e0 + e < V) ? __float_as_uint(__ldg(row + e0 + e)) : 0xff800000u;
-    return make_uint4(w[0], w[1], w[2], w[3]);
-}
-__device__ __forceinline__ uint4 partial_words(const bf16_t* row, long e0, long V) {
-    uint32_t h[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e)
-        h[e] = (e0 + e < V) ? (uint32_t)__ldg(reinterpret_cast<const unsigned short*>(row) + e0 + e) : 0xff80u;
-    return make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
-}
-
-template <typename T, int NW>
-__device__ __forceinline__ void load_words(uint4 (&w)[NW], const T* row, long V, long base, bool vec_ok) {
-    constexpr int EPV = 16 / (int)sizeof(T);
-#pragma unroll
-    for (int i = 0; i < Words<T>::N; ++i) {
-        const long e0 = base + (long)i * EPV;
-        if (vec_ok && e0 + EPV <= V) w[i] = __ldg(reinterpret_cast<const uint4*>(row + e0));
-        else w[i] = partial_words(row, e0, V);
-    }
-}
-
-template <typename T, int NW>
-__device__ __forceinline__ void decode_words(const uint4 (&w)[NW], float (&x)[kEPT]) {
-    if (sizeof(T) == 2) {
-#pragma unroll
-        for (int i = 0; i < kEPT / 8; ++i) {
-            const uint32_t a[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                x[8 * i + 2 * k] = __uint_as_float(a[k] << 16);
-                x[8 * i + 2 * k + 1] = __uint_as_float(a[k] & 0xffff0000u);
-            }
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < kEPT / 4; ++i) {
-            x[4 * i] = __uint_as_float(w[i].x);
-            x[4 * i + 1] = __uint_as_float(w[i].y);
-            x[4 * i + 2] = __uint_as_float(w[i].z);
-            x[4 * i + 3] = __uint_as_float(w[i].w);
-        }
-    }
-}
-
-__device__ __forceinline__ float fmax_nan(float a, float b) {
-    float r;
-    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
-    return r;
-}
-__device__ __forceinline__ uint32_t bmax2_nan(uint32_t a, uint32_t b) {
-    uint32_t r;
-    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-    return r;
-}
-// Max of this thread's 32 entries, NaN if any is NaN (bf16: packed pairs).
-template <typename T, int NW>
-__device__ __forceinline__ float chunk_max_nan(const uint4 (&w)[NW]) {
-    if (sizeof(T) == 2) {
-        uint32_t m = bmax2_nan(bmax2_nan(w[0].x, w[0].y), bmax2_nan(w[0].z, w[0].w));
-#pragma unroll
-        for (int i = 1; i < kEPT / 8; ++i)
-            m = bmax2_nan(m, bmax2_nan(bmax2_nan(w[i].x, w[i].y), bmax2_nan(w[i].z, w[i].w)));
-        return fmax_nan(__uint_as_float(m << 16), __uint_as_float(m & 0xffff0000u));
-    }
-    float m = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < kEPT / 4; ++i)
-        m = fmax_nan(fmax_nan(m, fmax_nan(__uint_as_float(w[i].x), __uint_as_float(w[i].y))),
-                     fmax_nan(__uint_as_float(w[i].z), __uint_as_float(w[i].w)));
-    return m;
-}
-__device__ __forceinline__ float warp_max_nan(float m) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmax_nan(m, __shfl_xor_sync(0xffffffffu, m, o));
-    return m;
-}
 
 __device__ __forceinline__ long thread_base(int c) {
     return (long)c * kVerifyChunk + (long)threadIdx.x * kEPT;

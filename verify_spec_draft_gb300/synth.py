@@ -21,7 +21,11 @@ Distributions (generated in float32, rounded once to bf16 where the config says 
 * anchors uniform in [0, V);
 * standalone-verify draft tokens: argmax of the draft row (T=0, a greedy drafter) or
   the Gumbel-max draw argmax(d + G), G standard Gumbel (T=1, a sample from the draft
-  row's softmax without computing one).
+  row's softmax without computing one);
+* draft trees: node i's parent uniform among the root (-1) and the nodes before it (or
+  node i-1 for a chain); its token the argmax of its parent's target row with a given
+  probability (a drafter that often agrees), else uniform in [0, V); confidences
+  uniform in [0.05, 1).
 """
 
 from dataclasses import dataclass, field
@@ -171,3 +175,34 @@ def config_inputs(cfg_id, device="cpu"):
     U, Wt = markov_weights(c.V, c.r, c.dtype, c.seed, device)
     return dict(cfg=c, target=t, draft=d, U=U, Wt=Wt, anchor=anchors(c.B, c.V, c.seed, device),
                 seeds=seeds_for(c.B, 0, device))
+
+
+# Draft trees (beyond the numbered configurations): the pages give no tree sizes; this
+# workload verifies 32 trees of 64 nodes over V = 248,320 (zipf rows, bf16), i.e. 2080
+# target rows, about the size of an EAGLE-2 tree per request in a batch of 32.
+TREE_CONFIG = Config("draft trees 32 x 64 nodes V248320 bf16", 32, 64, 248320, 0, torch.bfloat16, (0,), "zipf",
+                     0.0, 1007)
+
+
+def tree_inputs(n_trees, n_nodes, V, dtype=torch.bfloat16, seed=0, device="cpu", dist="zipf", p_match=0.7,
+                shape="bushy"):
+    """Draft trees and their target rows: parent, token int32 [n_trees, n_nodes], conf
+    float32 [n_trees, n_nodes] and target [n_trees, n_nodes + 1, V] (the root's row
+    first, then node i's at 1 + i)."""
+    g = generator(seed, device)
+    T, n = n_trees, n_nodes
+    rows = _base_logits(T * (n + 1), V, dist, g, device).view(T, n + 1, V).to(dtype).contiguous()
+    i = torch.arange(n, device=device, dtype=torch.float32)
+    if shape == "chain":
+        parent = (torch.arange(n, device=device, dtype=torch.int64) - 1).expand(T, n)
+    else:
+        u = torch.rand((T, n), generator=g, device=device, dtype=torch.float32)
+        parent = torch.floor(u * (i + 1)).to(torch.int64) - 1      # uniform in [-1, i)
+    am = rows.float().argmax(-1)                                   # [T, n + 1]
+    parent_am = torch.gather(am, 1, parent + 1)
+    rand_tok = torch.randint(0, V, (T, n), generator=g, device=device, dtype=torch.int64)
+    match = torch.rand((T, n), generator=g, device=device, dtype=torch.float32) < p_match
+    token = torch.where(match, parent_am, rand_tok)
+    conf = 0.05 + 0.95 * torch.rand((T, n), generator=g, device=device, dtype=torch.float32)
+    return dict(parent=parent.to(torch.int32).contiguous(), token=token.to(torch.int32).contiguous(),
+                conf=conf.contiguous(), target=rows)
