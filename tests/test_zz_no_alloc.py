@@ -96,7 +96,7 @@ def test_noalloc_rejects_problems_beyond_the_scratch():
     if build.needs_build():
         build.build()
     lib = vsd.load()
-    B, gamma, V = 200, 7, 248320
+    B, gamma, V = 1000, 7, 248320
     assert lib.spec_workspace_bytes(vsd.OP_VERIFY, B, gamma, V, 0) > (4 << 20)
     a = ctypes.c_void_p(A)
     code = lib.spec_verify_noalloc(a, vsd.BF16, a, vsd.BF16, a, B, gamma, V, 1, a, a, a, a, None, None)

@@ -44,6 +44,34 @@ __device__ __forceinline__ void load_words(uint4 (&w)[NW], const T* row, long V,
     }
 }
 
+// The same 32 entries per thread in the group-interleaved layout: lane l of warp w holds
+// the 8-entry groups j * 32 + l (j < 4) of the warp's 1024-entry segment of chunk c,
+// seg = c * 8192 + w * 1024; a group is one 16-byte word of bf16 or two of float32.
+// Decoded entry k (decode_words) is entry seg + ((k / 8) * 32 + l) * 8 + k % 8 for either
+// type, so rows of different types pair up entry by entry, and each load instruction
+// of a warp reads 512 contiguous bytes (bf16; float32 rows take two instructions per
+// 1 KB).
+__device__ __forceinline__ long il_seg(int c) {
+    return (long)c * kVerifyChunk + (long)(threadIdx.x >> 5) * 1024;
+}
+__device__ __forceinline__ long il_entry(long seg, int k) {
+    return seg + (long)((k >> 3) * 32 + (int)(threadIdx.x & 31)) * 8 + (k & 7);
+}
+template <typename T, int NW>
+__device__ __forceinline__ void load_words_il(uint4 (&w)[NW], const T* row, long V, long seg, bool vec_ok) {
+    constexpr int EPV = 16 / (int)sizeof(T);
+    constexpr int WPG = 8 / EPV;   // 16-byte words per 8-entry group
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+#pragma unroll
+        for (int h = 0; h < WPG; ++h) {
+            const long e0 = il_entry(seg, 8 * j) + h * EPV;
+            if (vec_ok && e0 + EPV <= V) w[j * WPG + h] = __ldg(reinterpret_cast<const uint4*>(row + e0));
+            else w[j * WPG + h] = partial_words(row, e0, V);
+        }
+    }
+}
+
 template <typename T, int NW>
 __device__ __forceinline__ void decode_words(const uint4 (&w)[NW], float (&x)[kEPT]) {
     if (sizeof(T) == 2) {

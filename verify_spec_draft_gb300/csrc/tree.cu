@@ -115,8 +115,9 @@ cudaError_t tree_select_launch(const TreeSelectParams& p, cudaStream_t stream) {
 constexpr int kTvThreads = 256;
 constexpr int kTvWarps = kTvThreads / 32;
 constexpr int kTvChunk = kTvThreads * kEPT;   // 8192 entries per item
-
-__device__ __forceinline__ long tv_base(int c) { return (long)c * kTvChunk + (long)threadIdx.x * kEPT; }
+#ifndef TV_DEPTH_BF16
+#define TV_DEPTH_BF16 2
+#endif
 
 // The row of item `it` (rows are tree-major: tree t, then its root row and node rows)
 // and its chunk; false when the row belongs to a node that is not kept.
@@ -129,6 +130,34 @@ __device__ __forceinline__ bool tv_item(const TreeVerifyParams& p, long it, unsi
     return node < 0 || !p.keep || p.keep[(size_t)t * p.n_nodes + node] != 0;
 }
 
+// One warp's 1024 entries of an item (group-interleaved): fold them into the row's
+// argmax key (or its bad flag) with one atomic per warp, so warps never wait for one
+// another.  Only the lanes holding the maximum look for its lowest index.
+template <typename TT, int NW>
+__device__ __forceinline__ void tv_fold(const TreeVerifyParams& p, const uint4 (&w)[NW], long row, int c) {
+    const float lm = chunk_max_nan<TT, NW>(w);
+    const float m = warp_max_nan(lm);
+    const int bad = (isnan(m) || m == INFINITY) ? 1 : 0;
+    int idx = 0x7fffffff;
+    if (!bad && lm == m) {
+        float x[kEPT];
+        decode_words<TT, NW>(w, x);
+        const long seg = il_seg(c);
+#pragma unroll
+        for (int k = kEPT - 1; k >= 0; --k)
+            if (x[k] == m) idx = (int)il_entry(seg, k);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) idx = min(idx, __shfl_xor_sync(0xffffffffu, idx, o));
+    if ((threadIdx.x & 31) == 0) {
+        if (bad) atomicOr(&p.rowbad[row], 1u);
+        else atomicMax(&p.keys[row], argmax_key(m, (uint32_t)idx));
+    }
+}
+
+// D items of loads in flight per thread (the one being reduced included).
+template <typename TT> struct TvDepth { static constexpr int D = sizeof(TT) == 2 ? TV_DEPTH_BF16 : 2; };
+
 template <typename TT>
 __global__ void __launch_bounds__(kTvThreads) tree_verify_kernel(TreeVerifyParams p) {
     const TT* target = static_cast<const TT*>(p.target);
@@ -138,56 +167,63 @@ __global__ void __launch_bounds__(kTvThreads) tree_verify_kernel(TreeVerifyParam
     const long items = (long)p.n_trees * rpt * nch;
     const bool vec = p.vec_t != 0;
     constexpr int NW = Words<TT>::N;
-    uint4 cur[NW], nxt[NW];
-    __shared__ unsigned long long s_key[2][kTvWarps];
-    int par = 0;
+    constexpr int D = TvDepth<TT>::D;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __shared__ long s_it[kTvThreads];   // the CTA's kept items of the current batch
+    __shared__ int s_wc[kTvWarps];
+    const long mine = items > (long)blockIdx.x ? (items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
 
-    // the next kept item of this CTA at or after `it` (items of skipped rows are passed over)
-    auto next_kept = [&](long it, long& row, int& c) -> long {
-        for (; it < items; it += gridDim.x)
-            if (tv_item(p, it, nch, row, c)) return it;
-        return items;
-    };
-    long row, nrow;
-    int c, nc;
-    long it = next_kept(blockIdx.x, row, c);
-    if (it < items) load_words<TT, NW>(cur, target + (size_t)row * V, V, tv_base(c), vec);
-    while (it < items) {
-        const long nx = next_kept(it + gridDim.x, nrow, nc);
-        if (nx < items) load_words<TT, NW>(nxt, target + (size_t)nrow * V, V, tv_base(nc), vec);
-        float m = warp_max_nan(chunk_max_nan<TT, NW>(cur));
-        const int bad = (isnan(m) || m == INFINITY) ? 1 : 0;
-        int idx = 0x7fffffff;
-        if (!bad) {
-            float x[kEPT];
-            decode_words<TT, NW>(cur, x);
-            const long base = tv_base(c);
+    for (long k0 = 0; k0 < mine; k0 += kTvThreads) {
+        // the next 256 items of this CTA, with those of dropped rows removed: each thread
+        // resolves one item, then a block compaction keeps their order
+        int cnt;
+        {
+            const long k = k0 + threadIdx.x;
+            const long it = (long)blockIdx.x + k * (long)gridDim.x;
+            long row;
+            int c;
+            const bool kept = k < mine && tv_item(p, it, nch, row, c);
+            const unsigned bal = __ballot_sync(0xffffffffu, kept);
+            if (lane == 0) s_wc[warp] = __popc(bal);
+            __syncthreads();
+            int off = 0;
+            cnt = 0;
 #pragma unroll
-            for (int e = kEPT - 1; e >= 0; --e)
-                if (x[e] == m) idx = (int)(base + e);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) idx = min(idx, __shfl_xor_sync(0xffffffffu, idx, o));
-        // one atomic per CTA and item (slots alternate with the item parity)
-        if ((threadIdx.x & 31) == 0) s_key[par][threadIdx.x >> 5] = bad ? ~0ull : argmax_key(m, (uint32_t)idx);
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            unsigned long long k = 0ull;
-            int anybad = 0;
             for (int w = 0; w < kTvWarps; ++w) {
-                const unsigned long long kw = s_key[par][w];
-                if (kw == ~0ull) anybad = 1;
-                else k = kw > k ? kw : k;
+                const int v = s_wc[w];
+                off += w < warp ? v : 0;
+                cnt += v;
             }
-            if (anybad) atomicOr(&p.rowbad[row], 1u);
-            else atomicMax(&p.keys[row], k);
+            if (kept) s_it[off + __popc(bal & ((1u << lane) - 1u))] = it;
+            __syncthreads();
         }
-        par ^= 1;
+        // stream the batch with D items of loads in flight per thread
+        uint4 buf[D][NW];
+        long rows[D];
+        int cs[D];
 #pragma unroll
-        for (int i = 0; i < NW; ++i) cur[i] = nxt[i];
-        it = nx;
-        row = nrow;
-        c = nc;
+        for (int d = 0; d < D - 1; ++d)
+            if (d < cnt) {
+                const long it = s_it[d];
+                rows[d] = it / (long)nch;
+                cs[d] = (int)(it - rows[d] * (long)nch);
+                load_words_il<TT, NW>(buf[d], target + (size_t)rows[d] * V, V, il_seg(cs[d]), vec);
+            }
+        for (int j0 = 0; j0 < cnt; j0 += D) {
+#pragma unroll
+            for (int d = 0; d < D; ++d) {
+                const int j = j0 + d;
+                const int jn = j + D - 1, dn = (d + D - 1) % D;
+                if (jn < cnt) {
+                    const long it = s_it[jn];
+                    rows[dn] = it / (long)nch;
+                    cs[dn] = (int)(it - rows[dn] * (long)nch);
+                    load_words_il<TT, NW>(buf[dn], target + (size_t)rows[dn] * V, V, il_seg(cs[dn]), vec);
+                }
+                if (j < cnt) tv_fold<TT, NW>(p, buf[d], rows[d], cs[d]);
+            }
+        }
+        __syncthreads();   // s_it is rewritten by the next batch
     }
 
     if (!last_block_done(&p.done[0], gridDim.x)) return;

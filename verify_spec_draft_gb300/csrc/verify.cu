@@ -298,54 +298,28 @@ __device__ __forceinline__ void stage_words(const uint8_t* stage, int warp, int 
     }
 }
 
-// After a bounded wait of the ring ran out: thread 0 waits (bounded again) for the copies
-// it issued to land, so that no copy into this CTA's shared memory is still in flight
-// when the CTA leaves the phase.  `last[s]` is the last item issued into stage s (-1 for
-// none); waiting on its phase returns at once when it was consumed already.
-__device__ __forceinline__ void drain_ring(uint64_t* full, const long* last, int S, unsigned* status) {
-    for (int s = 0; s < S; ++s)
-        if (last[s] >= 0) mbar_wait(&full[s], (unsigned)((last[s] / S) & 1), status, kV1WaitNs);
-}
-
-// Returns false when a bounded wait ran out (the status word has the TIMEOUT flag): the
-// producer then stops issuing copies, the consumers stop reading stages, and the copies
-// already issued are waited for before the CTA leaves.
 template <typename TT, typename DT>
-__device__ __forceinline__ bool phase_stats_staged(const VerifyParams& p, uint8_t* ring, uint64_t* full,
+__device__ __forceinline__ void phase_stats_staged(const VerifyParams& p, uint8_t* ring, uint64_t* full,
                                                    uint64_t* empty, int4* s_item, int S, size_t stage_bytes) {
-    __shared__ volatile int s_abort;
-    __shared__ long s_last[kV1StagesBf16];
+
     const long items = (long)(2 * p.gamma + 1) * p.nchunk * p.B;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long mine = items > (long)blockIdx.x ? (items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-    if (threadIdx.x == 0) {
-        s_abort = 0;
-        for (int k = 0; k < kV1StagesBf16; ++k) s_last[k] = -1;
-        for (long k = 0; k < S && k < mine; ++k) {
+    if (threadIdx.x == 0)
+        for (long k = 0; k < S && k < mine; ++k)
             issue_item1<TT, DT>(p, blockIdx.x + k * gridDim.x, ring + (size_t)k * stage_bytes, &full[k], &s_item[k]);
-            s_last[k] = k;
-        }
-    }
-    __syncthreads();
     for (long k = 0; k < mine; ++k) {
         const int s = (int)(k % S);
-        if (threadIdx.x == 0 && k >= 1 && k - 1 + S < mine && !s_abort) {
+        if (threadIdx.x == 0 && k >= 1 && k - 1 + S < mine) {
             // refill the stage of item k-1 with item k-1+S once every warp has left it
             const int sp = (int)((k - 1) % S);
-            if (mbar_wait(&empty[sp], (unsigned)(((k - 1) / S) & 1), p.status, kV1WaitNs)) {
-                fence_proxy_async_smem();
-                issue_item1<TT, DT>(p, blockIdx.x + (k - 1 + S) * gridDim.x, ring + (size_t)sp * stage_bytes,
-                                    &full[sp], &s_item[sp]);
-                s_last[sp] = k - 1 + S;
-            } else {
-                s_abort = 1;
-            }
-        }
-        if (s_abort || !mbar_wait(&full[s], (unsigned)((k / S) & 1), p.status, kV1WaitNs)) {
-            s_abort = 1;
-            break;
+            mbar_wait(&empty[sp], (unsigned)(((k - 1) / S) & 1), p.status, kV1WaitNs);
+            fence_proxy_async_smem();
+            issue_item1<TT, DT>(p, blockIdx.x + (k - 1 + S) * gridDim.x, ring + (size_t)sp * stage_bytes, &full[sp],
+                                &s_item[sp]);
         }
         const uint8_t* stage = ring + (size_t)s * stage_bytes;
+        mbar_wait(&full[s], (unsigned)((k / S) & 1), p.status, kV1WaitNs);
         const int4 qi = s_item[s];
         const Item1 q{qi.x, qi.y, qi.z};
         const int nvalid = qi.w;
@@ -366,11 +340,14 @@ __device__ __forceinline__ bool phase_stats_staged(const VerifyParams& p, uint8_
             mbar_arrive1(&empty[s]);   // this warp is done with stage s
         }
     }
-    __syncthreads();
-    if (!s_abort) return true;
-    if (threadIdx.x == 0) drain_ring(full, s_last, S, p.status);
-    __syncthreads();
-    return false;
+    // no copy may still be landing in this CTA's shared memory when it leaves the phase:
+    // thread 0 waits (bounded) on the phase of the last item issued into each stage
+    // (already complete, unless a wait above ran out)
+    if (threadIdx.x == 0)
+        for (int s = 0; s < S && s < mine; ++s) {
+            const long last = s + (mine - 1 - s) / S * S;
+            mbar_wait(&full[s], (unsigned)((last / S) & 1), p.status, kV1WaitNs);
+        }
 }
 
 // What the accept test of request b reads besides the row statistics: its draft tokens
@@ -661,21 +638,18 @@ __device__ __forceinline__ void stage_groups(const uint8_t* stage, int warp, int
 }
 
 template <typename TT, typename DT>
-__device__ __forceinline__ bool phase_weights_staged(const VerifyParams& p, uint8_t* ring, uint64_t* full,
+__device__ __forceinline__ void phase_weights_staged(const VerifyParams& p, uint8_t* ring, uint64_t* full,
                                                      uint64_t* empty, int4* s_info) {
     constexpr size_t kT = (size_t)kVerifyChunk * sizeof(TT), kD = (size_t)kVerifyChunk * sizeof(DT);
     constexpr int NS = (int)(((size_t)kV1StagesBf16 * kVerifyChunk * 2) / (kT + kD));   // slots, >= 1
     constexpr int NW = Words<TT>::N > Words<DT>::N ? Words<TT>::N : Words<DT>::N;
-    __shared__ volatile int s_abort;
-    __shared__ long s_last[NS];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.gamma;
     const unsigned nch = (unsigned)p.nchunk;
     const unsigned items = (unsigned)p.B * nch;   // < 2^31 (B <= 65535, nchunk <= 8192)
     const unsigned mine = items > blockIdx.x ? (items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
     if (threadIdx.x == 0) {
-        for (int i = 0; i < NS; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], kWarps); s_last[i] = -1; }
-        s_abort = 0;
+        for (int i = 0; i < NS; ++i) { mbar_init(&full[i], 1); mbar_init(&empty[i], kWarps); }
         fence_mbar_init();
     }
     __syncthreads();
@@ -688,7 +662,6 @@ __device__ __forceinline__ bool phase_weights_staged(const VerifyParams& p, uint
         s_info[2 * s] = make_int4(b, c, d.mode, nvalid);
         s_info[2 * s + 1] = make_int4(__float_as_int(d.m2p), __float_as_int(d.sp), __float_as_int(d.m2q),
                                       __float_as_int(d.sq));
-        s_last[s] = (long)k;
         uint64_t* bar = &full[s];
         if (d.mode == MODE_DONE) { mbar_arrive1(bar); return; }
         uint8_t* dst = ring + (size_t)s * (kT + kD);
@@ -708,21 +681,17 @@ __device__ __forceinline__ bool phase_weights_staged(const VerifyParams& p, uint
         for (int j = 0; j < NS; ++j)
             if ((unsigned)j < mine) issue((unsigned)j, j, d0[j]);
     }
-    __syncthreads();
     for (unsigned k = 0; k < mine; ++k) {
         const int s = (int)(k % NS);
-        if (threadIdx.x == 0 && k >= 1 && k - 1 + NS < mine && !s_abort) {
+        if (threadIdx.x == 0 && k >= 1 && k - 1 + NS < mine) {
             // refill the slot of item k-1 once every warp has left it
             const int sp = (int)((k - 1) % NS);
             const unsigned kn = k - 1 + NS;
             const DrawRow dn = draw_row(p, (int)((blockIdx.x + kn * gridDim.x) / nch));
-            if (mbar_wait(&empty[sp], ((k - 1) / NS) & 1u, p.status, kV1WaitNs)) issue(kn, sp, dn);
-            else s_abort = 1;
+            mbar_wait(&empty[sp], ((k - 1) / NS) & 1u, p.status, kV1WaitNs);
+            issue(kn, sp, dn);
         }
-        if (s_abort || !mbar_wait(&full[s], (k / NS) & 1u, p.status, kV1WaitNs)) {
-            s_abort = 1;
-            break;
-        }
+        if (!mbar_wait(&full[s], (k / NS) & 1u, p.status, kV1WaitNs)) break;
         const int4 i0 = s_info[2 * s], i1 = s_info[2 * s + 1];
         if (i0.z != MODE_DONE) {
             DrawRow d{i0.z, 0, 0, 0.0f, __int_as_float(i1.x), __int_as_float(i1.y), __int_as_float(i1.z),
@@ -739,11 +708,11 @@ __device__ __forceinline__ bool phase_weights_staged(const VerifyParams& p, uint
         __syncwarp();
         if (lane == 0) mbar_arrive1(&empty[s]);
     }
-    __syncthreads();
-    if (!s_abort) return true;
-    if (threadIdx.x == 0) drain_ring(full, s_last, NS, p.status);
-    __syncthreads();
-    return false;
+    if (threadIdx.x == 0)   // as in phase 1: no copy in flight when the CTA leaves
+        for (int s = 0; s < NS && (unsigned)s < mine; ++s) {
+            const unsigned last = s + (mine - 1 - s) / NS * NS;
+            mbar_wait(&full[s], (last / NS) & 1u, p.status, kV1WaitNs);
+        }
 }
 
 // Inclusive prefix over the CTA's threads, in thread order, and the total.  `buf`
@@ -935,9 +904,7 @@ __global__ void __launch_bounds__(kThreads, 2) verify_t1_kernel(VerifyParams p) 
             fence_mbar_init();
         }
         __syncthreads();
-        // after a timed-out wait the CTA skips the later phases; the others then give up
-        // at the next grid barrier (bounded too), and the TIMEOUT flag is set
-        if (!phase_stats_staged<TT, DT>(p, ring, full, empty, s_item, S, stage_bytes)) return;
+        phase_stats_staged<TT, DT>(p, ring, full, empty, s_item, S, stage_bytes);
     } else {
         phase_stats<TT, DT>(p);
     }
@@ -948,10 +915,9 @@ __global__ void __launch_bounds__(kThreads, 2) verify_t1_kernel(VerifyParams p) 
     if (!grid_barrier(gb, nb, p.status)) return;
     if (p.vec_t && p.vec_d) {
         extern __shared__ __align__(128) uint8_t v3_smem[];
-        if (!phase_weights_staged<TT, DT>(p, v3_smem + kV1RingOffset, reinterpret_cast<uint64_t*>(v3_smem),
-                                          reinterpret_cast<uint64_t*>(v3_smem) + kV1StagesBf16,
-                                          reinterpret_cast<int4*>(v3_smem + 2 * 8 * kV1StagesBf16)))
-            return;
+        phase_weights_staged<TT, DT>(p, v3_smem + kV1RingOffset, reinterpret_cast<uint64_t*>(v3_smem),
+                                     reinterpret_cast<uint64_t*>(v3_smem) + kV1StagesBf16,
+                                     reinterpret_cast<int4*>(v3_smem + 2 * 8 * kV1StagesBf16));
     } else {
         phase_weights<TT, DT>(p);
     }
