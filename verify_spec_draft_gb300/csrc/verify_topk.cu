@@ -11,242 +11,355 @@
 // prefix, in descending order, whose running sum reaches top_p; renormalised again.  Only
 // a row's top k entries matter, so no row-wide softmax is needed:
 //
-//   topk_rows_kernel   one CTA per row streams it; every thread keeps its k largest
-//                      64-bit keys (ordered value high, inverted index low, so a larger
-//                      key is a larger value or, on a tie, a lower index) in registers,
-//                      inserting only keys above its current k-th; the CTA then takes its
-//                      k largest by k rounds of a block maximum over the threads' heads.
-//                      NaN or +inf in the row flags it.
-//   topk_accept_kernel one thread per request: the filtered rows from the key lists in
-//                      float64, the accept tests (Philox stream 1), and the residual or
-//                      bonus draw over at most k candidates in index order (streams 2, 3).
+//   topk_rows_kernel   one CTA per row streams it (HBM-bound).  Each warp keeps the 32
+//                      largest 64-bit keys it has seen (ordered value high, inverted
+//                      index low: a larger key is a larger value or, on a tie, a lower
+//                      index) as a sorted list spread over its lanes.  An 8-entry group
+//                      is looked at only when its packed maximum reaches the threshold,
+//                      the larger of the warp's k-th key and the CTA's best published
+//                      k-th key (any entry below it cannot be among the row's k largest);
+//                      the threshold starts at the k-th largest lane maximum of the first
+//                      item.  A NaN or +inf ends the row: it has no distribution.  The
+//                      CTA's k largest keys are then ranked out of the warps' lists.
+//   topk_accept_kernel one CTA per request.  Each warp filters rows from their key lists
+//                      (one candidate per lane, float32; the cut-off is taken again in
+//                      float64 when a running sum lies within 1e-5 of top_p), then warp 0
+//                      runs the accept tests (Philox stream 1) and the residual or bonus
+//                      draw over at most k candidates in index order (streams 2, 3).
 #include "spec_device.cuh"
 #include "internal.h"
+#include "chunk_rows.cuh"
 
 namespace spec {
 
 constexpr int kTopkThreads = 256;
+constexpr int kTopkWarps = kTopkThreads / 32;
 
-__device__ __forceinline__ void topk_insert(unsigned long long (&L)[kTopkMax], unsigned long long key, int k,
-                                            unsigned long long& thr) {
-#pragma unroll
-    for (int i = 0; i < kTopkMax; ++i) {
-        if (key > L[i]) {
-            const unsigned long long t = L[i];
-            L[i] = key;
-            key = t;
-        }
-    }
-#pragma unroll
-    for (int i = 0; i < kTopkMax; ++i)
-        if (i == k - 1) thr = L[i];
+__device__ __forceinline__ unsigned long long shfl_u64(unsigned long long v, int src) {
+    const unsigned lo = __shfl_sync(0xffffffffu, (unsigned)v, src);
+    const unsigned hi = __shfl_sync(0xffffffffu, (unsigned)(v >> 32), src);
+    return ((unsigned long long)hi << 32) | lo;
+}
+__device__ __forceinline__ unsigned long long shfl_up_u64(unsigned long long v) {
+    const unsigned lo = __shfl_up_sync(0xffffffffu, (unsigned)v, 1);
+    const unsigned hi = __shfl_up_sync(0xffffffffu, (unsigned)(v >> 32), 1);
+    return ((unsigned long long)hi << 32) | lo;
 }
 
-template <typename T>
-__device__ __forceinline__ void topk_take(float x, long idx, unsigned long long (&L)[kTopkMax], int k,
-                                          unsigned long long& thr, int& bad) {
-    bad |= bad_logit(x) ? 1 : 0;
-    const unsigned long long key = argmax_key(x, (uint32_t)idx);
-    if (key > thr) topk_insert(L, key, k, thr);
+// The warp's list: lane i holds its (i+1)-th largest key (0 = empty).  Inserts `key`
+// (warp-uniform, smaller than at most k - 1 list keys) and updates `kth`, the list's
+// k-th key.
+__device__ __forceinline__ void list_insert(unsigned long long& mine, unsigned long long key, int k,
+                                            unsigned long long& kth) {
+    const int lane = threadIdx.x & 31;
+    const int pos = __popc(__ballot_sync(0xffffffffu, mine > key));   // list keys above it: a prefix
+    const unsigned long long up = shfl_up_u64(mine);
+    if (lane == pos) mine = key;
+    else if (lane > pos) mine = up;
+    kth = shfl_u64(mine, k - 1);
 }
 
-// Rows row0 .. row0 + gridDim.x - 1 of `src` ([rows, V]); the CTA's k keys go to
-// keys[(out0 + blockIdx.x) * kTopkMax + i] (0 where the row has fewer entries).
+// Rows row0 .. row0 + gridDim.x - 1 of `src` ([rows, V]); the CTA's k largest keys go to
+// keys[(out0 + blockIdx.x) * kTopkMax + i] in descending order (0 where the row has fewer
+// entries), its bad flag to bad_out[out0 + blockIdx.x].
 template <typename T>
 __global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(const T* src, long V, int k, bool vec,
                                                                  unsigned long long* keys, unsigned* bad_out,
                                                                  int out0) {
-    extern __shared__ __align__(16) unsigned long long s_list[];   // [threads][k]
-    __shared__ unsigned long long s_wmax[kTopkThreads / 32];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int NW = Words<T>::N;
+    constexpr int EPV = 16 / (int)sizeof(T);
+    constexpr int WPG = 8 / EPV;   // 16-byte words per 8-entry group
+    __shared__ unsigned long long s_thr;                   // the best k-th key a warp has published
+    __shared__ unsigned long long s_all[kTopkThreads];     // the warps' lists, for the final ranking
+    const int lane = threadIdx.x & 31;
     const T* row = src + (size_t)blockIdx.x * V;
-    unsigned long long L[kTopkMax];
-#pragma unroll
-    for (int i = 0; i < kTopkMax; ++i) L[i] = 0ull;
-    unsigned long long thr = 0ull;
+    const int nch = (int)((V + kVerifyChunk - 1) / kVerifyChunk);
+    if (threadIdx.x == 0) s_thr = 0ull;
+    __syncthreads();
+
+    unsigned long long mine = 0ull;   // this lane's slot of the warp's sorted list
+    unsigned long long kth = 0ull;    // the warp's k-th key (0 while the list is short)
+    unsigned long long thr = 0ull;    // the key to beat: the larger of kth and the CTA's best
+    float thr_v = -INFINITY;          // value threshold: groups below it are skipped
     int bad = 0;
-    if (vec) {
-        constexpr int N = VecTraits<T>::N;
-        const long nw = V / N;
-        for (long w = tid; w < nw; w += blockDim.x) {
-            float x[N];
-            load_vec(row + w * N, x);
+    uint4 cur[NW], nxt[NW];
+    load_words_il<T, NW>(cur, row, V, il_seg(0), vec);
+    for (int c = 0; c < nch; ++c) {
+        if (c + 1 < nch) load_words_il<T, NW>(nxt, row, V, il_seg(c + 1), vec);
+        if (c == 0) {
+            // seed: the k-th largest of the 32 lane maxima (each an entry of this item)
+            float lm = chunk_max_nan<T, NW>(cur);
+            if (isnan(lm) || lm == INFINITY) bad = 1;
 #pragma unroll
-            for (int e = 0; e < N; ++e) topk_take<T>(x[e], w * N + e, L, k, thr, bad);
+            for (int kk = 2; kk <= 32; kk <<= 1)   // bitonic sort of the lane maxima, ascending
+#pragma unroll
+                for (int j = kk >> 1; j > 0; j >>= 1) {
+                    const float o = __shfl_xor_sync(0xffffffffu, lm, j);
+                    const bool take_max = ((lane & kk) == 0) != ((lane & j) == 0);
+                    lm = take_max ? fmaxf(lm, o) : fminf(lm, o);
+                }
+            const float seed = __shfl_sync(0xffffffffu, lm, 32 - k);   // the k-th largest
+            thr_v = isnan(seed) ? -INFINITY : seed;
         }
-    } else {
-        for (long v = tid; v < V; v += blockDim.x) topk_take<T>(load_one(row + v), v, L, k, thr, bad);
-    }
-    for (int i = 0; i < k; ++i) {
-        unsigned long long w = 0ull;
+        const unsigned long long shared_thr = s_thr;
+        if (shared_thr > thr) {
+            thr = shared_thr;
+            thr_v = fmaxf(thr_v, key_value(shared_thr));
+        }
+        const long seg = il_seg(c);
 #pragma unroll
-        for (int q = 0; q < kTopkMax; ++q)
-            if (q == i) w = L[q];
-        s_list[(size_t)tid * k + i] = w;
+        for (int j = 0; j < 4; ++j) {
+            // the group's maximum, NaN if it holds a NaN
+            float gm;
+            if constexpr (sizeof(T) == 2) gm = u4_max_nan<2>(cur[j]);
+            else gm = f_max_nan(u4_max_nan<4>(cur[2 * j]), u4_max_nan<4>(cur[2 * j + 1]));
+            if (isnan(gm) || gm == INFINITY) bad = 1;
+            unsigned hot = __ballot_sync(0xffffffffu, !bad && gm >= thr_v);
+            while (hot) {
+                const int src_lane = __ffs(hot) - 1;
+                hot &= hot - 1;
+                float x[8];
+                {
+                    uint4 g0 = cur[j * WPG];
+                    g0.x = __shfl_sync(0xffffffffu, g0.x, src_lane);
+                    g0.y = __shfl_sync(0xffffffffu, g0.y, src_lane);
+                    g0.z = __shfl_sync(0xffffffffu, g0.z, src_lane);
+                    g0.w = __shfl_sync(0xffffffffu, g0.w, src_lane);
+                    if constexpr (sizeof(T) == 2) {
+                        const uint32_t a[4] = {g0.x, g0.y, g0.z, g0.w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            x[2 * q] = __uint_as_float(a[q] << 16);
+                            x[2 * q + 1] = __uint_as_float(a[q] & 0xffff0000u);
+                        }
+                    } else {
+                        uint4 g1 = cur[j * WPG + (WPG - 1)];
+                        g1.x = __shfl_sync(0xffffffffu, g1.x, src_lane);
+                        g1.y = __shfl_sync(0xffffffffu, g1.y, src_lane);
+                        g1.z = __shfl_sync(0xffffffffu, g1.z, src_lane);
+                        g1.w = __shfl_sync(0xffffffffu, g1.w, src_lane);
+                        x[0] = __uint_as_float(g0.x); x[1] = __uint_as_float(g0.y);
+                        x[2] = __uint_as_float(g0.z); x[3] = __uint_as_float(g0.w);
+                        x[4] = __uint_as_float(g1.x); x[5] = __uint_as_float(g1.y);
+                        x[6] = __uint_as_float(g1.z); x[7] = __uint_as_float(g1.w);
+                    }
+                }
+                const long e0 = seg + (long)(j * 32 + src_lane) * 8;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    if (e0 + e < V && x[e] >= thr_v) {   // warp-uniform
+                        const unsigned long long key = argmax_key(x[e], (uint32_t)(e0 + e));
+                        if (key > thr) {
+                            list_insert(mine, key, k, kth);
+                            if (kth > thr) {
+                                thr = kth;
+                                thr_v = fmaxf(thr_v, key_value(kth));
+                            }
+                        }
+                    }
+                }
+            }
+        }
+        // publish the warp's k-th key; a row with a NaN or +inf ends here (no distribution)
+        if (lane == 0 && kth > s_thr) atomicMax(&s_thr, kth);
+        if (__syncthreads_or(bad)) break;
+#pragma unroll
+        for (int i = 0; i < NW; ++i) cur[i] = nxt[i];
     }
     bad = __syncthreads_or(bad);
-    // k rounds: the largest remaining head over the block; its thread moves on (keys
-    // are distinct, the index being part of them, except the empty key 0)
-    int pos = 0;
+    // the CTA's k largest: rank every list key among all 256 (keys are distinct, the index
+    // being part of them, except the empty key 0)
+    s_all[threadIdx.x] = mine;
+    __syncthreads();
     unsigned long long* out = keys + (size_t)(out0 + blockIdx.x) * kTopkMax;
-    for (int r = 0; r < k; ++r) {
-        const unsigned long long head = pos < k ? s_list[(size_t)tid * k + pos] : 0ull;
-        unsigned long long m = head;
+    if (threadIdx.x < kTopkMax) out[threadIdx.x] = 0ull;
+    __syncthreads();
+    if (!bad && mine != 0ull) {
+        int rank = 0;
+        for (int i = 0; i < kTopkThreads; ++i) rank += s_all[i] > mine ? 1 : 0;
+        if (rank < k) out[rank] = mine;
+    }
+    if (threadIdx.x == 0) bad_out[out0 + blockIdx.x] = bad ? 1u : 0u;
+}
+
+// ----------------------------------------------------------------------------------
+// Accept and draw: one CTA per request
+// ----------------------------------------------------------------------------------
+struct FRow {                 // a filtered row: candidates in descending order of value
+    int idx[kTopkMax];
+    float pf[kTopkMax];       // filtered probability (0 past n)
+    int n;                    // kept candidates; 0 for a row without a distribution
+};
+
+// Warp: filter the row whose key list is `kl` (k keys, descending, 0 = none).
+__device__ void filter_row(const unsigned long long* kl, int k, double top_p, FRow& r) {
+    const int lane = threadIdx.x & 31;
+    const unsigned long long key = lane < k ? kl[lane] : 0ull;
+    const bool valid = key != 0ull;
+    const float v = valid ? key_value(key) : -INFINITY;
+    const float m = __shfl_sync(0xffffffffu, v, 0);
+    if (!(m > -INFINITY)) {   // no finite entry
+        if (lane == 0) r.n = 0;
+        return;
+    }
+    const float w = valid ? ex2(fmaf(v, kLog2e, -m * kLog2e)) : 0.0f;
+    const float S = warp_sum(w);
+    const float cw = warp_inclusive_scan(w);
+    const float run = cw / S;
+    const unsigned reach = __ballot_sync(0xffffffffu, valid && (double)run >= top_p);
+    const unsigned close = __ballot_sync(0xffffffffu, valid && fabs((double)run - top_p) < 1e-5);
+    const int nvalid = __popc(__ballot_sync(0xffffffffu, valid));
+    int n_keep = reach ? __ffs(reach) : nvalid;
+    if (close) {   // the cut-off is close: take it again in float64
+        const double w64 = valid ? exp((double)v - (double)m) : 0.0;
+        double S64 = w64, run64 = w64;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const unsigned long long t = __shfl_xor_sync(0xffffffffu, m, o);
-            m = t > m ? t : m;
+        for (int o = 16; o > 0; o >>= 1) S64 += __shfl_xor_sync(0xffffffffu, S64, o);
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const double y = __shfl_up_sync(0xffffffffu, run64, o);
+            if (lane >= o) run64 += y;
         }
-        if (lane == 0) s_wmax[warp] = m;
-        __syncthreads();
-        unsigned long long best = 0ull;
-        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) best = s_wmax[w] > best ? s_wmax[w] : best;
-        if (best != 0ull && head == best) ++pos;
-        if (tid == 0) out[r] = best;
-        __syncthreads();
+        const unsigned reach64 = __ballot_sync(0xffffffffu, valid && run64 / S64 >= top_p);
+        n_keep = reach64 ? __ffs(reach64) : nvalid;
     }
-    if (tid == 0) bad_out[out0 + blockIdx.x] = bad ? 1u : 0u;
+    const float Z = __shfl_sync(0xffffffffu, cw, n_keep - 1);
+    r.idx[lane] = valid ? (int)key_index(key) : -1;
+    r.pf[lane] = lane < n_keep ? w / Z : 0.0f;
+    if (lane == 0) r.n = n_keep;
 }
 
-// A filtered row from its key list: kept entries (index, weight) in descending order of
-// value, weights normalised to sum 1.  Returns the number kept, 0 for no distribution.
-__device__ int topk_filter(const unsigned long long* keys, int k, double top_p, int (&idx)[kTopkMax],
-                           double (&w)[kTopkMax]) {
-    int n = 0;
-    double m = 0.0, S = 0.0;
-    for (int i = 0; i < k; ++i) {
-        const unsigned long long key = keys[i];
-        if (key == 0ull) break;
-        const float v = key_value(key);
-        if (i == 0) {
-            if (!(v > -INFINITY)) return 0;   // no finite entry
-            m = (double)v;
-        }
-        idx[n] = (int)key_index(key);
-        w[n] = exp((double)v - m);
-        S += w[n];
-        ++n;
-    }
-    double run = 0.0, Z = 0.0;
-    int kept = 0;
-    for (int i = 0; i < n; ++i) {
-        run += w[i] / S;
-        Z += w[i];
-        ++kept;
-        if (run >= top_p) break;
-    }
-    for (int i = 0; i < kept; ++i) w[i] /= Z;
-    return kept;
+// Warp: the filtered probability of token x in row r (0 if not kept).
+__device__ __forceinline__ float frow_prob(const FRow& r, int x) {
+    const int lane = threadIdx.x & 31;
+    const unsigned hit = __ballot_sync(0xffffffffu, lane < r.n && r.idx[lane] == x);
+    return hit ? r.pf[__ffs(hit) - 1] : 0.0f;
 }
 
-__device__ __forceinline__ double topk_prob(const int (&idx)[kTopkMax], const double (&w)[kTopkMax], int n, int x) {
-    for (int i = 0; i < n; ++i)
-        if (idx[i] == x) return w[i];
-    return 0.0;
+// Per lane: the filtered probability of this lane's token x in row r (0 if not kept).
+__device__ __forceinline__ float frow_prob_lane(const FRow& r, int x) {
+    float v = 0.0f;
+    for (int i = 0; i < r.n; ++i)
+        if (r.idx[i] == x) v = r.pf[i];
+    return v;
 }
 
-// Inverse-CDF draw over (index, weight) candidates in index order: the smallest index
-// whose running weight passes u * total, else the last of positive weight; `near` when
-// the threshold lies within 1e-6 of the total from a boundary between two positive
-// entries.
-__device__ int topk_draw(int (&idx)[kTopkMax], double (&w)[kTopkMax], int n, double u, int& near) {
-    for (int i = 1; i < n; ++i) {   // insertion sort by index
-        const int ki = idx[i];
-        const double kw = w[i];
-        int j = i - 1;
-        while (j >= 0 && idx[j] > ki) { idx[j + 1] = idx[j]; w[j + 1] = w[j]; --j; }
-        idx[j + 1] = ki;
-        w[j + 1] = kw;
+// Warp: inverse-CDF draw over lane weights wl (candidate index il, -1 for none) in
+// vocabulary-index order: the smallest index whose running weight passes u * total, else
+// the last of positive weight; `near` as in the other draws (1e-6 of the total).
+__device__ int warp_draw(int il, float wl, float u, int& near) {
+    const int lane = threadIdx.x & 31;
+    // order of each candidate by index (candidates are distinct; none sort last)
+    const int key = il < 0 ? 0x7fffffff : il;
+    int rank = 0;
+    for (int j = 0; j < 32; ++j) {
+        const int o = __shfl_sync(0xffffffffu, key, j);
+        rank += (o < key || (o == key && j < lane)) ? 1 : 0;
     }
-    double Z = 0.0;
-    for (int i = 0; i < n; ++i) Z += w[i];
-    const double t = u * Z;
-    double C = 0.0, Cprev = 0.0;
-    int v = -1, last = -1;
-    for (int i = 0; i < n; ++i) {
-        if (w[i] > 0.0) last = i;
-        Cprev = C;
-        C += w[i];
-        if (v < 0 && C > t) {
-            v = i;
-            bool later = false;
-            for (int q = i + 1; q < n; ++q) later |= w[q] > 0.0;
-            if (fabs(C - t) < 1e-6 * Z && later) near = 1;
-            if (Cprev > 0.0 && fabs(Cprev - t) < 1e-6 * Z) near = 1;
-        }
+    __shared__ float s_w[kTopkWarps][32];
+    __shared__ int s_i[kTopkWarps][32];
+    const int warp = threadIdx.x >> 5;
+    s_w[warp][rank] = il < 0 ? 0.0f : wl;
+    s_i[warp][rank] = il;
+    __syncwarp();
+    const float ow = s_w[warp][lane];
+    const int oi = s_i[warp][lane];
+    const float C = warp_inclusive_scan(ow);
+    const float Z = __shfl_sync(0xffffffffu, C, 31);
+    const float t = u * Z;
+    const float Cprev = C - ow;
+    const unsigned cross = __ballot_sync(0xffffffffu, oi >= 0 && C > t);
+    const unsigned pos = __ballot_sync(0xffffffffu, oi >= 0 && ow > 0.0f);
+    int v;
+    if (cross) v = __ffs(cross) - 1;
+    else v = pos ? 31 - __clz(pos) : -1;
+    if (v >= 0 && cross) {
+        const float Cv = __shfl_sync(0xffffffffu, C, v);
+        const float Cp = __shfl_sync(0xffffffffu, Cprev, v);
+        const bool later = (pos >> v) > 1u;
+        if ((fabsf(Cv - t) < 1e-6f * Z && later) || (Cp > 0.0f && fabsf(Cp - t) < 1e-6f * Z)) near = 1;
     }
-    if (v < 0) v = last;
-    return v < 0 ? -1 : idx[v];
+    const int y = v < 0 ? -1 : __shfl_sync(0xffffffffu, oi, v);
+    __syncwarp();
+    return y;
 }
 
-__global__ void topk_accept_kernel(TopkParams p) {
-    const int b = blockIdx.x * blockDim.x + threadIdx.x;
-    if (b >= p.B) return;
+__global__ void __launch_bounds__(kTopkThreads) topk_accept_kernel(TopkParams p) {
+    const int b = blockIdx.x;
     const int G = p.gamma;
     const int nT = p.B * (G + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    extern __shared__ __align__(16) unsigned char s_dyn[];
+    FRow* rows = reinterpret_cast<FRow*>(s_dyn);   // [2G+1]: target rows 0..G, then draft rows
+    __shared__ int s_ok;
+    if (threadIdx.x == 0) s_ok = 1;
+    __syncthreads();
+    for (int i = threadIdx.x; i < G; i += blockDim.x) {
+        const int x = p.tokens[(size_t)b * G + i];
+        if (x < 0 || x >= p.V) s_ok = 0;
+    }
+    for (int r = warp; r < 2 * G + 1; r += kTopkWarps) {
+        const size_t gr = r <= G ? (size_t)b * (G + 1) + r : (size_t)nT + (size_t)b * G + (r - G - 1);
+        if (p.bad[gr]) {
+            if (lane == 0) { rows[r].n = 0; s_ok = 0; }
+            continue;
+        }
+        filter_row(p.keys + gr * kTopkMax, p.k, p.top_p, rows[r]);
+        __syncwarp();
+        if (lane == 0 && rows[r].n == 0) s_ok = 0;
+    }
+    __syncthreads();
+    if (warp != 0) return;
     int32_t* com = p.committed_out + (size_t)b * (G + 1);
-    bool ok = true;
-    for (int j = 0; j < G; ++j) {
-        const int x = p.tokens[(size_t)b * G + j];
-        ok &= x >= 0 && x < p.V;
-    }
-    for (int i = 0; i <= G; ++i) ok &= p.bad[b * (G + 1) + i] == 0u;
-    for (int i = 0; i < G; ++i) ok &= p.bad[nT + b * G + i] == 0u;
-    int idx_p[kTopkMax], idx_q[kTopkMax];
-    double wp[kTopkMax], wq[kTopkMax];
-    if (ok) {   // every row the request reads has a distribution
-        for (int i = 0; i <= G && ok; ++i)
-            ok = topk_filter(p.keys + (size_t)(b * (G + 1) + i) * kTopkMax, p.k, p.top_p, idx_p, wp) > 0;
-        for (int i = 0; i < G && ok; ++i)
-            ok = topk_filter(p.keys + (size_t)(nT + b * G + i) * kTopkMax, p.k, p.top_p, idx_q, wq) > 0;
-    }
-    if (!ok) {
-        p.n_out[b] = -1;
-        p.bonus_out[b] = -1;
-        for (int i = 0; i <= G; ++i) com[i] = -1;
-        if (p.near_out) p.near_out[b] = 0;
-        atomicOr(p.status, SPEC_DEV_TOKEN);
+    if (!s_ok) {
+        for (int i = lane; i <= G; i += 32) com[i] = -1;
+        if (lane == 0) {
+            p.n_out[b] = -1;
+            p.bonus_out[b] = -1;
+            if (p.near_out) p.near_out[b] = 0;
+            atomicOr(p.status, SPEC_DEV_TOKEN);
+        }
         return;
     }
     const uint64_t seed = p.seeds[b];
     int near = 0;
     for (int j = 1; j <= G; ++j) {
-        const int np = topk_filter(p.keys + (size_t)(b * (G + 1) + j - 1) * kTopkMax, p.k, p.top_p, idx_p, wp);
-        const int nq = topk_filter(p.keys + (size_t)(nT + b * G + j - 1) * kTopkMax, p.k, p.top_p, idx_q, wq);
+        const FRow& P = rows[j - 1];
+        const FRow& Q = rows[G + j];
         const int x = p.tokens[(size_t)b * G + j - 1];
-        const double px = topk_prob(idx_p, wp, np, x), qx = topk_prob(idx_q, wq, nq, x);
-        const double u = (double)philox_uniform(seed, (uint64_t)b, (uint64_t)j, 1);
-        if (fabs(u * qx - px) < 1e-6 * qx) near = 1;
+        const float px = frow_prob(P, x), qx = frow_prob(Q, x);
+        const float u = philox_uniform(seed, (uint64_t)b, (uint64_t)j, 1);
+        if (fabsf(u * qx - px) < 1e-6f * qx) near = 1;
         if (u * qx < px) {   // accepted (q = 0 accepts iff p > 0)
-            com[j - 1] = x;
+            if (lane == 0) com[j - 1] = x;
             continue;
         }
-        // residual max(0, p - q): positive only on the filtered p's entries
-        double r[kTopkMax];
-        double rs = 0.0;
-        for (int i = 0; i < np; ++i) {
-            r[i] = wp[i] - topk_prob(idx_q, wq, nq, idx_p[i]);
-            r[i] = r[i] > 0.0 ? r[i] : 0.0;
-            rs += r[i];
+        // the residual max(0, p - q) on the filtered p's candidates (from p if all zero)
+        const int il = lane < P.n ? P.idx[lane] : -1;
+        const float pl = lane < P.n ? P.pf[lane] : 0.0f;
+        const float ql = il >= 0 ? frow_prob_lane(Q, il) : 0.0f;
+        float rl = fmaxf(0.0f, pl - ql);
+        if (!(warp_sum(rl) > 0.0f)) rl = pl;
+        const float u2 = philox_uniform(seed, (uint64_t)b, (uint64_t)j, 2);
+        const int y = warp_draw(il, rl, u2, near);
+        for (int i = j - 1 + lane; i <= G; i += 32) com[i] = i == j - 1 ? y : -1;
+        if (lane == 0) {
+            p.n_out[b] = j - 1;
+            p.bonus_out[b] = y;
+            if (p.near_out) p.near_out[b] = near;
         }
-        if (!(rs > 0.0))
-            for (int i = 0; i < np; ++i) r[i] = wp[i];
-        const double u2 = (double)philox_uniform(seed, (uint64_t)b, (uint64_t)j, 2);
-        const int y = topk_draw(idx_p, r, np, u2, near);
-        com[j - 1] = y;
-        for (int i = j; i <= G; ++i) com[i] = -1;
-        p.n_out[b] = j - 1;
-        p.bonus_out[b] = y;
-        if (p.near_out) p.near_out[b] = near;
         return;
     }
-    const int np = topk_filter(p.keys + (size_t)(b * (G + 1) + G) * kTopkMax, p.k, p.top_p, idx_p, wp);
-    const double u3 = (double)philox_uniform(seed, (uint64_t)b, (uint64_t)(G + 1), 3);
-    const int y = topk_draw(idx_p, wp, np, u3, near);
-    com[G] = y;
-    p.n_out[b] = G;
-    p.bonus_out[b] = y;
-    if (p.near_out) p.near_out[b] = near;
+    const FRow& P = rows[G];
+    const int il = lane < P.n ? P.idx[lane] : -1;
+    const float u3 = philox_uniform(seed, (uint64_t)b, (uint64_t)(G + 1), 3);
+    const int y = warp_draw(il, lane < P.n ? P.pf[lane] : 0.0f, u3, near);
+    if (lane == 0) {
+        com[G] = y;
+        p.n_out[b] = G;
+        p.bonus_out[b] = y;
+        if (p.near_out) p.near_out[b] = near;
+    }
 }
 
 size_t verify_topk_workspace_bytes(int B, int gamma) {
@@ -257,10 +370,7 @@ size_t verify_topk_workspace_bytes(int B, int gamma) {
 template <typename T>
 static cudaError_t launch_rows(const void* src, int rows, long V, int k, bool vec, unsigned long long* keys,
                                unsigned* bad, int out0, cudaStream_t stream) {
-    const size_t smem = (size_t)kTopkThreads * k * sizeof(unsigned long long);
-    cudaError_t e = cudaFuncSetAttribute(topk_rows_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    topk_rows_kernel<T><<<rows, kTopkThreads, smem, stream>>>(static_cast<const T*>(src), V, k, vec, keys, bad, out0);
+    topk_rows_kernel<T><<<rows, kTopkThreads, 0, stream>>>(static_cast<const T*>(src), V, k, vec, keys, bad, out0);
     return cudaGetLastError();
 }
 
@@ -280,7 +390,10 @@ cudaError_t verify_topk_launch(TopkParams& p, void* ws, cudaStream_t stream) {
     e = p.ddt == SPEC_BF16 ? launch_rows<bf16_t>(p.draft, nD, p.V, p.k, vd, p.keys, p.bad, nT, stream)
                            : launch_rows<float>(p.draft, nD, p.V, p.k, vd, p.keys, p.bad, nT, stream);
     if (e != cudaSuccess) return e;
-    topk_accept_kernel<<<(p.B + 63) / 64, 64, 0, stream>>>(p);
+    const size_t smem = (size_t)(2 * p.gamma + 1) * sizeof(FRow);
+    e = cudaFuncSetAttribute(topk_accept_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    topk_accept_kernel<<<p.B, kTopkThreads, smem, stream>>>(p);
     return cudaGetLastError();
 }
 
