@@ -103,6 +103,27 @@ def test_t1_small(spec, B, gamma, V, dtype, ddtype):
     assert near <= 2
 
 
+def test_t1_float32_rows_ending_mid_group(spec):
+    """Float32 rows with V % 8 == 4 are 16-byte aligned, so their weights are staged by
+    bulk copies, and the last 8-entry group of a row is half full.  The target puts most
+    of its mass on those last four entries and the draft does not, so rejections draw
+    residuals there: the draws must reach them."""
+    B, gamma, V = 8, 3, 8196
+    t, d = synth.target_and_draft(B, gamma, V, "gaussian", 0.5, torch.float32, seed=41)
+    t[:, :, V - 4:] += 12.0
+    near = 0
+    tail = 0
+    for s in range(3):
+        tok = synth.draft_tokens(d, 1, seed=s)
+        seeds = synth.seeds_for(B, 10 * s)
+        g, _ = _run_gpu(t, d, tok, 1, seeds)
+        o = _oracle(t, d, tok, 1, seeds)
+        near += _compare(g, o, allow_near=True)
+        tail += int((g["bonus"] >= V - 4).sum())
+    assert near <= 1
+    assert tail >= B   # most draws land in the half-full last group
+
+
 def test_t1_acceptance_spread(spec):
     """Noisy drafts: every n from 0 to gamma shows up, including residual draws at
     every position and the bonus draw."""

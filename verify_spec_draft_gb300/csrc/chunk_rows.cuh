@@ -72,6 +72,27 @@ __device__ __forceinline__ void load_words_il(uint4 (&w)[NW], const T* row, long
     }
 }
 
+// This warp's 1024-entry segment of a chunk staged in shared memory, in the
+// group-interleaved layout: lane L holds groups j * 32 + L (j < 4), one 16-byte word each
+// in bf16, two in float32, so that entry k of decode_words is the same vocabulary entry
+// for either type.  -inf past the `nvalid` entries the chunk holds (checked per word).
+template <typename T, int NW>
+__device__ __forceinline__ void stage_groups(const uint8_t* stage, int warp, int lane, int nvalid, uint4 (&w)[NW]) {
+    constexpr int WPG = (int)sizeof(T) / 2;   // 16-byte words per 8-entry group
+    constexpr int EPV = 16 / (int)sizeof(T);
+    const uint4* seg = reinterpret_cast<const uint4*>(stage) + (size_t)warp * (1024 / 8) * WPG;
+    const uint32_t ninf = sizeof(T) == 2 ? 0xff80ff80u : 0xff800000u;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int g = j * 32 + lane;
+#pragma unroll
+        for (int h = 0; h < WPG; ++h) {
+            const bool in = warp * 1024 + g * 8 + h * EPV + EPV <= nvalid;
+            w[j * WPG + h] = in ? seg[g * WPG + h] : make_uint4(ninf, ninf, ninf, ninf);
+        }
+    }
+}
+
 template <typename T, int NW>
 __device__ __forceinline__ void decode_words(const uint4 (&w)[NW], float (&x)[kEPT]) {
     if (sizeof(T) == 2) {

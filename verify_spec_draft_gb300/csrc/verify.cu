@@ -619,24 +619,6 @@ __device__ __forceinline__ void phase_weights(const VerifyParams& p) {
 // The barriers are initialised again for this phase (phase 1 has no copy or arrival
 // pending on them).  Same per-entry arithmetic as phase_weights; each lane sums its
 // segment's 8-entry groups lane-interleaved (stage_groups).
-// This warp's 1024-entry segment of a staged chunk in 8-entry groups: lane L holds
-// groups j * 32 + L (j < 4), one 16-byte word each in bf16, two in float32, so that
-// entry e of decode_words is the same vocabulary entry for either type (target and
-// draft words pair up entry by entry).  -inf past the `nvalid` entries.
-template <typename T, int NW>
-__device__ __forceinline__ void stage_groups(const uint8_t* stage, int warp, int lane, int nvalid, uint4 (&w)[NW]) {
-    constexpr int WPG = (int)sizeof(T) / 2;   // 16-byte words per 8-entry group
-    const uint4* seg = reinterpret_cast<const uint4*>(stage) + (size_t)warp * (1024 / 8) * WPG;
-    const uint32_t ninf = sizeof(T) == 2 ? 0xff80ff80u : 0xff800000u;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int g = j * 32 + lane;
-        const bool in = warp * 1024 + g * 8 + 8 <= nvalid;
-#pragma unroll
-        for (int h = 0; h < WPG; ++h) w[j * WPG + h] = in ? seg[g * WPG + h] : make_uint4(ninf, ninf, ninf, ninf);
-    }
-}
-
 template <typename TT, typename DT>
 __device__ __forceinline__ void phase_weights_staged(const VerifyParams& p, uint8_t* ring, uint64_t* full,
                                                      uint64_t* empty, int4* s_info) {

@@ -11,16 +11,18 @@
 // prefix, in descending order, whose running sum reaches top_p; renormalised again.  Only
 // a row's top k entries matter, so no row-wide softmax is needed:
 //
-//   topk_rows_kernel   one CTA per row streams it (HBM-bound).  Each warp keeps the 32
-//                      largest 64-bit keys it has seen (ordered value high, inverted
-//                      index low: a larger key is a larger value or, on a tie, a lower
-//                      index) as a sorted list spread over its lanes.  An 8-entry group
-//                      is looked at only when its packed maximum reaches the threshold,
-//                      the larger of the warp's k-th key and the CTA's best published
-//                      k-th key (any entry below it cannot be among the row's k largest);
-//                      the threshold starts at the k-th largest lane maximum of the first
-//                      item.  A NaN or +inf ends the row: it has no distribution.  The
-//                      CTA's k largest keys are then ranked out of the warps' lists.
+//   topk_rows_kernel   one CTA per row (target and draft rows in one grid) streams it
+//                      (HBM-bound).  Each warp keeps the 32 largest 64-bit keys it has
+//                      seen (ordered value high, inverted index low: a larger key is a
+//                      larger value or, on a tie, a lower index) as a sorted list spread
+//                      over its lanes.  A lane looks inside its 8-entry groups only when a
+//                      group's packed maximum reaches the threshold, the larger of the
+//                      warp's k-th key and the CTA's best published k-th key (no entry
+//                      below it can be among the row's k largest); the threshold starts
+//                      at the k-th largest lane maximum of the first item.  The entries
+//                      above it go to a per-warp buffer (one prefix over the lanes) and are
+//                      inserted one by one.  NaN or +inf marks the row bad (it has no
+//                      distribution).  The CTA's k largest are ranked out of the lists.
 //   topk_accept_kernel one CTA per request.  Each warp filters rows from their key lists
 //                      (one candidate per lane, float32; the cut-off is taken again in
 //                      float64 when a running sum lies within 1e-5 of top_p), then warp 0
@@ -59,33 +61,48 @@ __device__ __forceinline__ void list_insert(unsigned long long& mine, unsigned l
     kth = shfl_u64(mine, k - 1);
 }
 
-// Rows row0 .. row0 + gridDim.x - 1 of `src` ([rows, V]); the CTA's k largest keys go to
-// keys[(out0 + blockIdx.x) * kTopkMax + i] in descending order (0 where the row has fewer
-// entries), its bad flag to bad_out[out0 + blockIdx.x].
+// Candidates a warp found in one item, waiting for insertion into its list.
+constexpr int kCandCap = 128;
+
+// Entry q (in decode_words order) of a thread's words, decoded on its own.
+template <typename T, int NW>
+__device__ __forceinline__ float word_entry(const uint4 (&w)[NW], int q) {
+    if constexpr (sizeof(T) == 2) {
+        const uint4 v = w[q >> 3];
+        const int h = (q & 7) >> 1;
+        const uint32_t a = h == 0 ? v.x : (h == 1 ? v.y : (h == 2 ? v.z : v.w));
+        return (q & 1) ? __uint_as_float(a & 0xffff0000u) : __uint_as_float(a << 16);
+    } else {
+        const uint4 v = w[q >> 2];
+        const int h = q & 3;
+        return __uint_as_float(h == 0 ? v.x : (h == 1 ? v.y : (h == 2 ? v.z : v.w)));
+    }
+}
+
+// The row at `rowp` (V entries); its k largest keys go to keys[row * kTopkMax + i] in
+// descending order (0 where the row has fewer entries), its bad flag to bad_out[row].
 template <typename T>
-__global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(const T* src, long V, int k, bool vec,
-                                                                 unsigned long long* keys, unsigned* bad_out,
-                                                                 int out0) {
+__device__ __forceinline__ void topk_row(const T* rowp, long V, int k, bool vec, int row, unsigned long long* keys,
+                                         unsigned* bad_out) {
     constexpr int NW = Words<T>::N;
-    constexpr int EPV = 16 / (int)sizeof(T);
-    constexpr int WPG = 8 / EPV;   // 16-byte words per 8-entry group
-    __shared__ unsigned long long s_thr;                   // the best k-th key a warp has published
-    __shared__ unsigned long long s_all[kTopkThreads];     // the warps' lists, for the final ranking
-    const int lane = threadIdx.x & 31;
-    const T* row = src + (size_t)blockIdx.x * V;
+    __shared__ unsigned long long s_thr;                       // best k-th key a warp has published
+    __shared__ unsigned long long s_all[kTopkThreads];         // the warps' lists, for the final ranking
+    __shared__ unsigned long long s_cand[kTopkWarps][kCandCap];
+    __shared__ int s_bad;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nch = (int)((V + kVerifyChunk - 1) / kVerifyChunk);
-    if (threadIdx.x == 0) s_thr = 0ull;
+    if (threadIdx.x == 0) { s_thr = 0ull; s_bad = 0; }
     __syncthreads();
 
     unsigned long long mine = 0ull;   // this lane's slot of the warp's sorted list
     unsigned long long kth = 0ull;    // the warp's k-th key (0 while the list is short)
     unsigned long long thr = 0ull;    // the key to beat: the larger of kth and the CTA's best
-    float thr_v = -INFINITY;          // value threshold: groups below it are skipped
+    float thr_v = -INFINITY;          // value threshold: entries below it are skipped
     int bad = 0;
     uint4 cur[NW], nxt[NW];
-    load_words_il<T, NW>(cur, row, V, il_seg(0), vec);
+    load_words_il<T, NW>(cur, rowp, V, il_seg(0), vec);
     for (int c = 0; c < nch; ++c) {
-        if (c + 1 < nch) load_words_il<T, NW>(nxt, row, V, il_seg(c + 1), vec);
+        if (c + 1 < nch) load_words_il<T, NW>(nxt, rowp, V, il_seg(c + 1), vec);
         if (c == 0) {
             // seed: the k-th largest of the 32 lane maxima (each an entry of this item)
             float lm = chunk_max_nan<T, NW>(cur);
@@ -101,85 +118,112 @@ __global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(const T* src, l
             const float seed = __shfl_sync(0xffffffffu, lm, 32 - k);   // the k-th largest
             thr_v = isnan(seed) ? -INFINITY : seed;
         }
-        const unsigned long long shared_thr = s_thr;
+        // the CTA's best k-th key, read once and broadcast: every lane of the warp must see
+        // the same threshold (the insertions below are warp-collective), and other warps
+        // raise s_thr concurrently
+        unsigned long long st_l = 0ull;
+        if (lane == 0) st_l = *(volatile unsigned long long*)&s_thr;
+        const unsigned long long shared_thr = shfl_u64(st_l, 0);
         if (shared_thr > thr) {
             thr = shared_thr;
             thr_v = fmaxf(thr_v, key_value(shared_thr));
         }
-        const long seg = il_seg(c);
+        // this lane's entries at or above the threshold (their keys), counted first; entry
+        // q of the lane is vocabulary index ebase + (q / 8) * 256 + q % 8 (V < 2^31)
+        const int ebase = (int)il_seg(c) + lane * 8;
+        const int vi = (int)V;
+        int ncand = 0;
+        float gmax[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            // the group's maximum, NaN if it holds a NaN
-            float gm;
-            if constexpr (sizeof(T) == 2) gm = u4_max_nan<2>(cur[j]);
-            else gm = f_max_nan(u4_max_nan<4>(cur[2 * j]), u4_max_nan<4>(cur[2 * j + 1]));
-            if (isnan(gm) || gm == INFINITY) bad = 1;
-            unsigned hot = __ballot_sync(0xffffffffu, !bad && gm >= thr_v);
-            while (hot) {
-                const int src_lane = __ffs(hot) - 1;
-                hot &= hot - 1;
-                float x[8];
-                {
-                    uint4 g0 = cur[j * WPG];
-                    g0.x = __shfl_sync(0xffffffffu, g0.x, src_lane);
-                    g0.y = __shfl_sync(0xffffffffu, g0.y, src_lane);
-                    g0.z = __shfl_sync(0xffffffffu, g0.z, src_lane);
-                    g0.w = __shfl_sync(0xffffffffu, g0.w, src_lane);
-                    if constexpr (sizeof(T) == 2) {
-                        const uint32_t a[4] = {g0.x, g0.y, g0.z, g0.w};
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            x[2 * q] = __uint_as_float(a[q] << 16);
-                            x[2 * q + 1] = __uint_as_float(a[q] & 0xffff0000u);
-                        }
-                    } else {
-                        uint4 g1 = cur[j * WPG + (WPG - 1)];
-                        g1.x = __shfl_sync(0xffffffffu, g1.x, src_lane);
-                        g1.y = __shfl_sync(0xffffffffu, g1.y, src_lane);
-                        g1.z = __shfl_sync(0xffffffffu, g1.z, src_lane);
-                        g1.w = __shfl_sync(0xffffffffu, g1.w, src_lane);
-                        x[0] = __uint_as_float(g0.x); x[1] = __uint_as_float(g0.y);
-                        x[2] = __uint_as_float(g0.z); x[3] = __uint_as_float(g0.w);
-                        x[4] = __uint_as_float(g1.x); x[5] = __uint_as_float(g1.y);
-                        x[6] = __uint_as_float(g1.z); x[7] = __uint_as_float(g1.w);
-                    }
-                }
-                const long e0 = seg + (long)(j * 32 + src_lane) * 8;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    if (e0 + e < V && x[e] >= thr_v) {   // warp-uniform
-                        const unsigned long long key = argmax_key(x[e], (uint32_t)(e0 + e));
-                        if (key > thr) {
-                            list_insert(mine, key, k, kth);
-                            if (kth > thr) {
-                                thr = kth;
-                                thr_v = fmaxf(thr_v, key_value(kth));
-                            }
-                        }
-                    }
-                }
-            }
+            if constexpr (sizeof(T) == 2) gmax[j] = u4_max_nan<2>(cur[j]);
+            else gmax[j] = f_max_nan(u4_max_nan<4>(cur[2 * j]), u4_max_nan<4>(cur[2 * j + 1]));
+            if (isnan(gmax[j]) || gmax[j] == INFINITY) bad = 1;
         }
-        // publish the warp's k-th key; a row with a NaN or +inf ends here (no distribution)
-        if (lane == 0 && kth > s_thr) atomicMax(&s_thr, kth);
-        if (__syncthreads_or(bad)) break;
+        const bool any_hot = !bad && (gmax[0] >= thr_v || gmax[1] >= thr_v || gmax[2] >= thr_v || gmax[3] >= thr_v);
+        if (__any_sync(0xffffffffu, any_hot)) {
+            const float cut = thr_v;   // the entries taken this item: fixed while they are buffered
+            if (any_hot) {
+#pragma unroll
+                for (int q = 0; q < kEPT; ++q)
+                    ncand += (word_entry<T, NW>(cur, q) >= cut && ebase + (q >> 3) * 256 + (q & 7) < vi) ? 1 : 0;
+            }
+            // write them to the warp's buffer (an exclusive prefix over lanes); rounds of at
+            // most kCandCap, each followed by the insertions
+            int before = 0, total = 0;
+            {
+                int incl = ncand;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                before = incl - ncand;
+                total = __shfl_sync(0xffffffffu, incl, 31);
+            }
+            for (int r0 = 0; r0 < total; r0 += kCandCap) {
+                int pos = before - r0;
+                if (any_hot && ncand > 0) {
+#pragma unroll
+                    for (int q = 0; q < kEPT; ++q) {
+                        const int e = ebase + (q >> 3) * 256 + (q & 7);
+                        const float xq = word_entry<T, NW>(cur, q);
+                        if (xq >= cut && e < vi) {
+                            if (pos >= 0 && pos < kCandCap) s_cand[warp][pos] = argmax_key(xq, (uint32_t)e);
+                            ++pos;
+                        }
+                    }
+                }
+                __syncwarp();
+                const int nr = min(kCandCap, total - r0);
+                for (int i = 0; i < nr; ++i) {   // warp-uniform
+                    const unsigned long long key = s_cand[warp][i];
+                    if (key > thr) {
+                        list_insert(mine, key, k, kth);
+                        if (kth > thr) {
+                            thr = kth;
+                            thr_v = fmaxf(thr_v, key_value(kth));
+                        }
+                    }
+                }
+                __syncwarp();
+            }
+            // publish the warp's k-th key
+            if (lane == 0 && kth > *(volatile unsigned long long*)&s_thr) atomicMax(&s_thr, kth);
+        }
 #pragma unroll
         for (int i = 0; i < NW; ++i) cur[i] = nxt[i];
     }
-    bad = __syncthreads_or(bad);
-    // the CTA's k largest: rank every list key among all 256 (keys are distinct, the index
-    // being part of them, except the empty key 0)
-    s_all[threadIdx.x] = mine;
+    if (bad) s_bad = 1;
     __syncthreads();
-    unsigned long long* out = keys + (size_t)(out0 + blockIdx.x) * kTopkMax;
+    bad = s_bad;
+    // the row's k largest: only a warp's first k keys can be among them; rank each of
+    // those among all of them (keys are distinct, the index being part of them, except
+    // the empty key 0)
+    const bool lane_k = lane < k;
+    s_all[threadIdx.x] = lane_k ? mine : 0ull;
+    __syncthreads();
+    unsigned long long* out = keys + (size_t)row * kTopkMax;
     if (threadIdx.x < kTopkMax) out[threadIdx.x] = 0ull;
     __syncthreads();
-    if (!bad && mine != 0ull) {
+    if (!bad && lane_k && mine != 0ull) {
         int rank = 0;
-        for (int i = 0; i < kTopkThreads; ++i) rank += s_all[i] > mine ? 1 : 0;
+        for (int w = 0; w < kTopkWarps; ++w)
+            for (int i = 0; i < k; ++i) rank += s_all[w * 32 + i] > mine ? 1 : 0;
         if (rank < k) out[rank] = mine;
     }
-    if (threadIdx.x == 0) bad_out[out0 + blockIdx.x] = bad ? 1u : 0u;
+    if (threadIdx.x == 0) bad_out[row] = bad ? 1u : 0u;
+}
+
+// All rows of a request batch in one grid: target rows 0 .. nT-1, then draft rows.
+template <typename TT, typename DT>
+__global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(TopkParams p, bool vt, bool vd) {
+    const int row = blockIdx.x;
+    const int nT = p.B * (p.gamma + 1);
+    if (row < nT)
+        topk_row<TT>(static_cast<const TT*>(p.target) + (size_t)row * p.V, p.V, p.k, vt, row, p.keys, p.bad);
+    else
+        topk_row<DT>(static_cast<const DT*>(p.draft) + (size_t)(row - nT) * p.V, p.V, p.k, vd, row, p.keys, p.bad);
 }
 
 // ----------------------------------------------------------------------------------
@@ -367,10 +411,10 @@ size_t verify_topk_workspace_bytes(int B, int gamma) {
     return kWsHeaderBytes + rows * kTopkMax * sizeof(unsigned long long) + rows * sizeof(unsigned);
 }
 
-template <typename T>
-static cudaError_t launch_rows(const void* src, int rows, long V, int k, bool vec, unsigned long long* keys,
-                               unsigned* bad, int out0, cudaStream_t stream) {
-    topk_rows_kernel<T><<<rows, kTopkThreads, 0, stream>>>(static_cast<const T*>(src), V, k, vec, keys, bad, out0);
+template <typename TT, typename DT>
+static cudaError_t launch_rows(const TopkParams& p, bool vt, bool vd, cudaStream_t stream) {
+    const long rows = (long)p.B * (2 * p.gamma + 1);
+    topk_rows_kernel<TT, DT><<<(unsigned)rows, kTopkThreads, 0, stream>>>(p, vt, vd);
     return cudaGetLastError();
 }
 
@@ -380,15 +424,13 @@ cudaError_t verify_topk_launch(TopkParams& p, void* ws, cudaStream_t stream) {
     const size_t rows = (size_t)p.B * (2 * p.gamma + 1);
     p.keys = reinterpret_cast<unsigned long long*>(w + kWsHeaderBytes);
     p.bad = reinterpret_cast<unsigned*>(w + kWsHeaderBytes + rows * kTopkMax * sizeof(unsigned long long));
-    const int nT = p.B * (p.gamma + 1), nD = p.B * p.gamma;
     const bool vt = ((size_t)p.V * (p.tdt == SPEC_BF16 ? 2 : 4)) % 16 == 0;
     const bool vd = ((size_t)p.V * (p.ddt == SPEC_BF16 ? 2 : 4)) % 16 == 0;
-    cudaError_t e = p.tdt == SPEC_BF16
-                        ? launch_rows<bf16_t>(p.target, nT, p.V, p.k, vt, p.keys, p.bad, 0, stream)
-                        : launch_rows<float>(p.target, nT, p.V, p.k, vt, p.keys, p.bad, 0, stream);
-    if (e != cudaSuccess) return e;
-    e = p.ddt == SPEC_BF16 ? launch_rows<bf16_t>(p.draft, nD, p.V, p.k, vd, p.keys, p.bad, nT, stream)
-                           : launch_rows<float>(p.draft, nD, p.V, p.k, vd, p.keys, p.bad, nT, stream);
+    cudaError_t e;
+    if (p.tdt == SPEC_BF16 && p.ddt == SPEC_BF16) e = launch_rows<bf16_t, bf16_t>(p, vt, vd, stream);
+    else if (p.tdt == SPEC_BF16) e = launch_rows<bf16_t, float>(p, vt, vd, stream);
+    else if (p.ddt == SPEC_BF16) e = launch_rows<float, bf16_t>(p, vt, vd, stream);
+    else e = launch_rows<float, float>(p, vt, vd, stream);
     if (e != cudaSuccess) return e;
     const size_t smem = (size_t)(2 * p.gamma + 1) * sizeof(FRow);
     e = cudaFuncSetAttribute(topk_accept_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
