@@ -103,6 +103,44 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return r;
 }
 
+// Pairs of floats held as one 64-bit register pair, and this architecture's float32x2
+// arithmetic: one instruction rounds both halves exactly as the scalar instruction would.
+typedef unsigned long long f2x;
+__device__ __forceinline__ f2x f2_pack(float lo, float hi) {
+    f2x r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float2 f2_unpack(f2x v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+__device__ __forceinline__ f2x f2_fma(f2x a, f2x b, f2x c) {
+    f2x r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ f2x f2_add(f2x a, f2x b) {
+    f2x r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f2x f2_mul(f2x a, f2x b) {
+    f2x r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+// The two bf16 values of a 32-bit word, widened (exactly) into a pair.
+__device__ __forceinline__ f2x bf2_widen(uint32_t w) {
+    return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+// (2^x, 2^y) of a pair
+__device__ __forceinline__ f2x f2_ex2(f2x v) {
+    const float2 a = f2_unpack(v);
+    return f2_pack(ex2(a.x), ex2(a.y));
+}
+
 // Rows of one branch: staged in shared memory (stride cols) or read from global.
 struct Rows {
     const bf16_t* tgt;
@@ -182,7 +220,7 @@ __device__ __forceinline__ void slice_stats(const bf16_t* row, int ncol, Stat2& 
     const int lane = threadIdx.x & 31;
     const uint32_t ninf = 0xff80ff80u;
     float m2 = -INFINITY;
-    float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+    f2x acc0 = f2_pack(0.0f, 0.0f), acc1 = acc0;
     int lbad = 0;
     for (int k0 = lane * 8; k0 < ncol; k0 += 256 * B) {
         uint4 w[B];
@@ -201,21 +239,26 @@ __device__ __forceinline__ void slice_stats(const bf16_t* row, int ncol, Stat2& 
         const float bm2 = bm * kLog2e;
         if (bm2 > m2) {
             const float r = ex2(m2 - bm2);          // 0 when m2 was -inf
-            s0 *= r; s1 *= r; s2 *= r; s3 *= r;
+            const f2x rr = f2_pack(r, r);
+            acc0 = f2_mul(acc0, rr);
+            acc1 = f2_mul(acc1, rr);
             m2 = bm2;
         }
+        // -inf entries contribute 2^-inf = 0; both halves of a word in one packed FMA
+        const f2x cl = f2_pack(kLog2e, kLog2e), cm = f2_pack(-m2, -m2);
 #pragma unroll
-        for (int g = 0; g < B; ++g) {   // -inf entries contribute 2^-inf = 0
-            s0 += ex2(fmaf(lo_bf(w[g].x), kLog2e, -m2)) + ex2(fmaf(hi_bf(w[g].x), kLog2e, -m2));
-            s1 += ex2(fmaf(lo_bf(w[g].y), kLog2e, -m2)) + ex2(fmaf(hi_bf(w[g].y), kLog2e, -m2));
-            s2 += ex2(fmaf(lo_bf(w[g].z), kLog2e, -m2)) + ex2(fmaf(hi_bf(w[g].z), kLog2e, -m2));
-            s3 += ex2(fmaf(lo_bf(w[g].w), kLog2e, -m2)) + ex2(fmaf(hi_bf(w[g].w), kLog2e, -m2));
+        for (int g = 0; g < B; ++g) {
+            acc0 = f2_add(acc0, f2_ex2(f2_fma(bf2_widen(w[g].x), cl, cm)));
+            acc1 = f2_add(acc1, f2_ex2(f2_fma(bf2_widen(w[g].y), cl, cm)));
+            acc0 = f2_add(acc0, f2_ex2(f2_fma(bf2_widen(w[g].z), cl, cm)));
+            acc1 = f2_add(acc1, f2_ex2(f2_fma(bf2_widen(w[g].w), cl, cm)));
         }
     }
     bad = warp_or(lbad);
     const float M = warp_max(m2);
     float s = 0.0f;
-    if (!bad && M != -INFINITY && m2 != -INFINITY) s = ((s0 + s1) + (s2 + s3)) * ex2(m2 - M);
+    const float2 a0 = f2_unpack(acc0), a1 = f2_unpack(acc1);
+    if (!bad && M != -INFINITY && m2 != -INFINITY) s = ((a0.x + a0.y) + (a1.x + a1.y)) * ex2(m2 - M);
     s = warp_sum(s);
     out = Stat2{(bad || M == -INFINITY) ? -INFINITY : M, s};
 }
@@ -225,7 +268,8 @@ __device__ __forceinline__ void slice_overlap(const bf16_t* tr, const bf16_t* dr
                                               uint8_t* mask, float& a, float& s, uint64_t pol_t, uint64_t pol_d) {
     const int lane = threadIdx.x & 31;
     const uint32_t ninf = 0xff80ff80u;
-    float sa0 = 0.0f, sa1 = 0.0f, ss0 = 0.0f, ss1 = 0.0f;
+    f2x sa = f2_pack(0.0f, 0.0f), ss = sa;
+    const f2x cl = f2_pack(kLog2e, kLog2e), cp = f2_pack(-lse_p, -lse_p), cq = f2_pack(-lse_q, -lse_q);
     for (int k0 = lane * 8; k0 < ncol; k0 += 256 * B) {
         uint4 wl[B], wd[B];
 #pragma unroll
@@ -241,15 +285,13 @@ __device__ __forceinline__ void slice_overlap(const bf16_t* tr, const bf16_t* dr
             const uint32_t d4[4] = {wd[g].x, wd[g].y, wd[g].z, wd[g].w};
             uint32_t bits = 0;
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                const float lp0 = fmaf(lo_bf(l4[h]), kLog2e, -lse_p), lq0 = fmaf(lo_bf(d4[h]), kLog2e, -lse_q);
-                const float lp1 = fmaf(hi_bf(l4[h]), kLog2e, -lse_p), lq1 = fmaf(hi_bf(d4[h]), kLog2e, -lse_q);
-                const float m0 = ex2(fminf(lp0, lq0)), m1 = ex2(fminf(lp1, lq1));
-                const bool b0 = lq0 < lp0, b1 = lq1 < lp1;
-                sa0 += m0;
-                sa1 += m1;
-                ss0 += b0 ? m0 : 0.0f;
-                ss1 += b1 ? m1 : 0.0f;
+            for (int h = 0; h < 4; ++h) {   // exponents of both halves of a word in one packed FMA
+                const float2 P = f2_unpack(f2_fma(bf2_widen(l4[h]), cl, cp));
+                const float2 Q = f2_unpack(f2_fma(bf2_widen(d4[h]), cl, cq));
+                const float m0 = ex2(fminf(P.x, Q.x)), m1 = ex2(fminf(P.y, Q.y));
+                const bool b0 = Q.x < P.x, b1 = Q.y < P.y;
+                sa = f2_add(sa, f2_pack(m0, m1));
+                ss = f2_add(ss, f2_pack(b0 ? m0 : 0.0f, b1 ? m1 : 0.0f));
                 bits |= (b0 ? 1u : 0u) << (2 * h);
                 bits |= (b1 ? 2u : 0u) << (2 * h);
             }
@@ -257,8 +299,9 @@ __device__ __forceinline__ void slice_overlap(const bf16_t* tr, const bf16_t* dr
             if (k < ncol) mask[k >> 3] = (uint8_t)bits;
         }
     }
-    a = warp_sum(sa0 + sa1);
-    s = warp_sum(ss0 + ss1);
+    const float2 A = f2_unpack(sa), Sx = f2_unpack(ss);
+    a = warp_sum(A.x + A.y);
+    s = warp_sum(Sx.x + Sx.y);
 }
 
 template <bool STAGED, bool VEC>
@@ -460,55 +503,71 @@ __global__ void __launch_bounds__(kThreads, STAGED ? 2 : 4) e2etv_kernel(E2etvPa
         }
 
         // sweep 3: gradient w.r.t. the draft logits, rounded once to bf16; rows read from
-        // global memory keep U of a thread's 16-byte words in flight
+        // global memory keep U of a thread's 16-byte words in flight.  Item idx is group
+        // gi of row i (idx = i * ng + gi); each of a thread's U items advances by a fixed
+        // stride, so its (row, group) is stepped forward instead of divided out.
         {
             const int ng = (ncol + 7) / 8;
             const int total = Wb * ng;
             constexpr int U = (!STAGED && VEC) ? 4 : 1;
-            for (int idx0 = threadIdx.x; idx0 < total; idx0 += (int)blockDim.x * U) {
+            const int step = (int)blockDim.x * U;
+            int ri[U], gi[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int idx = (int)threadIdx.x + u * (int)blockDim.x;
+                ri[u] = ng > 0 ? idx / ng : 0;
+                gi[u] = idx - ri[u] * ng;
+            }
+            const f2x cl = f2_pack(kLog2e, kLog2e);
+            for (int idx0 = threadIdx.x; idx0 < total; idx0 += step) {
                 uint4 wdu[U];
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int idx = idx0 + u * (int)blockDim.x;
                     wdu[u] = make_uint4(0u, 0u, 0u, 0u);
                     if (idx < total && !bad_branch) {
-                        const int i = idx / ng, k = (idx - i * ng) * 8;
+                        const int i = ri[u], k = gi[u] * 8;
                         wdu[u] = VEC ? ld16p<STAGED>(rw.drf + (size_t)i * rw.stride + k, pol_last)
                                      : group8<STAGED, VEC>(rw.drf + (size_t)i * rw.stride, k, ncol);
                     }
                 }
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
-                const int idx = idx0 + u * (int)blockDim.x;
-                if (idx >= total) continue;
-                const int i = idx / ng, k = (idx - i * ng) * 8;
-                uint4 out = make_uint4(0u, 0u, 0u, 0u);
-                if (!bad_branch) {
-                    const uint4 wd = wdu[u];
-                    const uint32_t bits = s_mask[(size_t)i * ngroups8 + (k >> 3)];
-                    const float lse_q = s_lse[Wb + i], c1 = s_c1[i], c0v = s_c0[i];
-                    const uint32_t d4[4] = {wd.x, wd.y, wd.z, wd.w};
-                    uint32_t o4[4];
+                    const int idx = idx0 + u * (int)blockDim.x;
+                    if (idx < total) {
+                        const int i = ri[u], k = gi[u] * 8;
+                        uint4 out = make_uint4(0u, 0u, 0u, 0u);
+                        if (!bad_branch) {
+                            const uint4 wd = wdu[u];
+                            const uint32_t bits = s_mask[(size_t)i * ngroups8 + (k >> 3)];
+                            const float c1 = s_c1[i], c0v = s_c0[i];
+                            const f2x cq = f2_pack(-s_lse[Wb + i], -s_lse[Wb + i]);
+                            const uint32_t d4[4] = {wd.x, wd.y, wd.z, wd.w};
+                            uint32_t o4[4];
 #pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        const float q0 = ex2(fmaf(lo_bf(d4[h]), kLog2e, -lse_q));
-                        const float q1 = ex2(fmaf(hi_bf(d4[h]), kLog2e, -lse_q));
-                        const float g0 = q0 * (((bits >> (2 * h)) & 1u) ? c1 : c0v);
-                        const float g1 = q1 * (((bits >> (2 * h + 1)) & 1u) ? c1 : c0v);
-                        o4[h] = pack_bf16x2(g0, g1);
+                            for (int h = 0; h < 4; ++h) {   // both halves of a word in packed FMA/MUL
+                                const f2x q = f2_ex2(f2_fma(bf2_widen(d4[h]), cl, cq));
+                                const f2x c = f2_pack(((bits >> (2 * h)) & 1u) ? c1 : c0v,
+                                                      ((bits >> (2 * h + 1)) & 1u) ? c1 : c0v);
+                                const float2 g = f2_unpack(f2_mul(q, c));
+                                o4[h] = pack_bf16x2(g.x, g.y);
+                            }
+                            out = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+                        }
+                        uint16_t* dst = p.grad_out + ((size_t)n * Wb + i) * V + c0 + k;
+                        if (VEC) {
+                            asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};"
+                                         :: "l"(dst), "r"(out.x), "r"(out.y), "r"(out.z), "r"(out.w) : "memory");
+                        } else {
+                            const uint32_t o4[4] = {out.x, out.y, out.z, out.w};
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                if (k + e < ncol) dst[e] = (uint16_t)((o4[e >> 1] >> (16 * (e & 1))) & 0xffffu);
+                        }
                     }
-                    out = make_uint4(o4[0], o4[1], o4[2], o4[3]);
-                }
-                uint16_t* dst = p.grad_out + ((size_t)n * Wb + i) * V + c0 + k;
-                if (VEC) {
-                    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};"
-                                 :: "l"(dst), "r"(out.x), "r"(out.y), "r"(out.z), "r"(out.w) : "memory");
-                } else {
-                    const uint32_t o4[4] = {out.x, out.y, out.z, out.w};
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        if (k + e < ncol) dst[e] = (uint16_t)((o4[e >> 1] >> (16 * (e & 1))) & 0xffffu);
-                }
+                    // the next item of slot u: step groups forward, wrapping into later rows
+                    gi[u] += step;
+                    while (gi[u] >= ng) { gi[u] -= ng; ++ri[u]; }
                 }
             }
         }
