@@ -321,6 +321,9 @@ __global__ void __launch_bounds__(kThreads, STAGED ? 2 : 4) e2etv_kernel(E2etvPa
     uint8_t* s_mask = reinterpret_cast<uint8_t*>(s_drf + (STAGED ? (size_t)Wb * p.cols : 0));
     __shared__ float s_lse[2 * SPEC_MAX_GAMMA];
     __shared__ float s_a[SPEC_MAX_GAMMA], s_s[SPEC_MAX_GAMMA], s_c1[SPEC_MAX_GAMMA], s_c0[SPEC_MAX_GAMMA];
+    // per row, the gradient coefficients of a word's two entries for each pair of their
+    // q<p bits: entry (lo, hi) takes kappa (s - 1) where its bit is set, kappa s elsewhere
+    __shared__ f2x s_ctab[SPEC_MAX_GAMMA][4];
     __shared__ int s_bad;
     __shared__ __align__(8) uint64_t s_bar[2];   // [0] target rows, [1] draft rows
     // the group's barrier: a monotonic arrival count (slot word 0), as for the draft's
@@ -494,6 +497,11 @@ __global__ void __launch_bounds__(kThreads, STAGED ? 2 : 4) e2etv_kernel(E2etvPa
                 if (gi == 0) p.branch_sum[n] = sum_s;
             }
             __syncthreads();
+            if ((int)threadIdx.x < 4 * Wb) {
+                const int i = threadIdx.x >> 2, m = threadIdx.x & 3;
+                s_ctab[i][m] = f2_pack((m & 1) ? s_c1[i] : s_c0[i], (m & 2) ? s_c1[i] : s_c0[i]);
+            }
+            __syncthreads();
         } else if (threadIdx.x == 0 && gi == 0) {
             for (int i = 0; i < Wb; ++i) {
                 p.a_out[(size_t)n * Wb + i] = NAN;
@@ -540,15 +548,14 @@ __global__ void __launch_bounds__(kThreads, STAGED ? 2 : 4) e2etv_kernel(E2etvPa
                         if (!bad_branch) {
                             const uint4 wd = wdu[u];
                             const uint32_t bits = s_mask[(size_t)i * ngroups8 + (k >> 3)];
-                            const float c1 = s_c1[i], c0v = s_c0[i];
                             const f2x cq = f2_pack(-s_lse[Wb + i], -s_lse[Wb + i]);
+                            const f2x* ctab = s_ctab[i];
                             const uint32_t d4[4] = {wd.x, wd.y, wd.z, wd.w};
                             uint32_t o4[4];
 #pragma unroll
                             for (int h = 0; h < 4; ++h) {   // both halves of a word in packed FMA/MUL
                                 const f2x q = f2_ex2(f2_fma(bf2_widen(d4[h]), cl, cq));
-                                const f2x c = f2_pack(((bits >> (2 * h)) & 1u) ? c1 : c0v,
-                                                      ((bits >> (2 * h + 1)) & 1u) ? c1 : c0v);
+                                const f2x c = ctab[(bits >> (2 * h)) & 3u];
                                 const float2 g = f2_unpack(f2_mul(q, c));
                                 o4[h] = pack_bf16x2(g.x, g.y);
                             }
