@@ -373,6 +373,7 @@ def summary(result):
                                    ("e2etv_cfg5", "e2etv", 1e-6, "Mtok_s"),
                                    ("tree_verify_t0", "tree_verify", 1e-6, "Mrows_s"),
                                    ("draft_t1_b32", "draft_t1_b32", 1e-6, "Mrows_s"),
+                                   ("draft_t1_topk_b32", "draft_topk_b32", 1e-6, "Mrows_s"),
                                    ("anchor_branches", "sampler", 1e-3, "kbranch_s")):
         v = sec.get(key)
         if not v:
@@ -590,7 +591,30 @@ def secondary(args, torch, vsd, synth, dev, hbm, hbm_kind, sampler, rank=0, worl
                      "note": "drafter rows once, W once per biased pass; pass 0 and the biased pass both read the rows"},
         "gpu_launches": steps,
     }
-    del inp, L4, U4, Wt4, o4, ws4, flush_buf
+    # the same draft with the DSpine card's filtered draws (top_k 20, top_p 0.95): the chain
+    # position by position, the weights read once per position
+    wsk = vsd.workspace(vsd.OP_DRAFT_TOPK, B, G, V, c.r, dev)
+    ok_ = vsd.draft_block_topk(L4, a4, U4, Wt4, 20, 0.95, s4, ws=wsk)
+    fn, graphed = capture(lambda: vsd.draft_block_topk(L4, a4, U4, Wt4, 20, 0.95, s4, ws=wsk, out=ok_), torch)
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    sampler.active = True
+    total, _ = time_steps(torch, fn, steps, flush=lambda: flush_buf.zero_())
+    sampler.active = False
+    ms = sum(total) / len(total)
+    byts = B * G * V * 2 + G * V * c.r * 2
+    ach = byts / (ms * 1e-3) / 1e9
+    out["draft_t1_topk_b32"] = {
+        "workload": "draft block T=1 with top_k 20, top_p 0.95, B=32, gamma=7, V=248320, r=256 bf16 (L2 flushed)",
+        "value": B * G / (ms * 1e-3), "unit": "rows/s", "us_per_step": ms * 1e3, "cuda_graphs": graphed,
+        "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "peak_kind": hbm_kind, "unit": "GB/s",
+                     "frac": ach / hbm, "frac_of_nominal_8tbs": ach / NOMINAL_HBM_GBS,
+                     "algorithmic_bytes_per_launch": byts,
+                     "note": "drafter rows once and W once per position (the chain is walked position by position)"},
+        "gpu_launches": 2 * G * steps,
+    }
+    del inp, L4, U4, Wt4, o4, ws4, flush_buf, wsk, ok_
     torch.cuda.empty_cache()
 
     # the SpecOPD anchor-branch sampler: 16 references x 64 anchors, W = 7, V = 248320,

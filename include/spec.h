@@ -86,7 +86,8 @@ typedef enum {
     SPEC_OP_DRAFT_VERIFY = 3,
     SPEC_OP_BRANCH_PLAN = 4,
     SPEC_OP_VERIFY_TOPK = 5,
-    SPEC_OP_TREE_VERIFY = 6
+    SPEC_OP_TREE_VERIFY = 6,
+    SPEC_OP_DRAFT_TOPK = 7
 } spec_op;
 
 /* Device status flags (OR-ed into the workspace status word). */
@@ -113,6 +114,7 @@ typedef enum {
  *          SPEC_OP_VERIFY_TOPK: B requests, gamma positions (V and r unused).
  *          SPEC_OP_TREE_VERIFY: B = trees, gamma = nodes per tree (0 allowed, up to
  *          SPEC_MAX_TREE_NODES), V, r unused.
+ *          SPEC_OP_DRAFT_TOPK: B requests (gamma, V, r unused).
  *          For SPEC_OP_DRAFT the size covers one launch's slice of requests, which
  *          spec_draft_block reuses across the slices of a larger batch.
  * Returns 0 for arguments outside the supported ranges.
@@ -374,6 +376,41 @@ spec_status spec_e2etv_shard(const uint16_t *target_logits, const uint16_t *draf
                              int n_branches, int Wb, int V, int total_branches, float *a_out,
                              float *surv_out, float *msum_out, uint16_t *grad_out,
                              void *workspace, size_t workspace_bytes, spec_stream_t stream);
+
+/*
+ * spec_draft_block_topk - spec_draft_block at T=1 with top-k / top-p filtered draws.
+ *
+ * Defines ("Speculative Decoding Part 2", VESSL AI, DSpark section, bias equation; "DSpine
+ * card numbers and public file headers", aiwithghost.com, section on raising the
+ * temperature: sampling at T=1 with top_p 0.95 and top_k 20).  For request b and
+ * j = 1..gamma, with x_0 = anchor[b]:
+ *     z_j = l_j + W_1[x_{j-1}] W_2                     (as spec_draft_block)
+ *     filter(z_j): spec_verify_topk's reading (the top_k largest logits renormalised,
+ *     the shortest prefix in descending order reaching top_p, renormalised again)
+ *     x_j = inverse-CDF draw from filter(z_j) in vocabulary-index order,
+ *           u = Philox(seed_b; b, j, 0)
+ *     c_j = 1/Z of the unfiltered softmax(z_j) (its largest probability)
+ *     q_j(x_j) = filter(z_j)(x_j)
+ *   draft_logits  [B, gamma, V], dtype logits_dtype.
+ *   anchor        [B] int32.
+ *   U, Wt         bf16 [V, r] (the layout of spec_draft_block), r a multiple of 16 up to
+ *                 SPEC_MAX_RANK; r = 0 means no bias (U, Wt may then be NULL).
+ *   top_k, top_p  1 <= top_k <= SPEC_MAX_TOP_K, 0 < top_p <= 1.
+ *   seeds         [B] uint64.
+ *   tokens_out    [B, gamma] int32; conf_out [B, gamma] float32; qtok_out [B, gamma]
+ *                 float32 (nullable).
+ *   workspace     spec_workspace_bytes(SPEC_OP_DRAFT_TOPK, B, gamma, V, r).
+ * A request whose anchor lies outside [0, V) (flag TOKEN), or whose row j holds NaN or
+ * +inf or no finite entry (flag NONFINITE), gets tokens -1 and NaN statistics from that
+ * position on.  The chain is walked position by position (2 * gamma launches); the
+ * weights are read once per position for every 32 requests.
+ * Limits: 1 <= gamma <= SPEC_MAX_GAMMA, 1 <= V <= SPEC_MAX_V, 1 <= B <= 65535.
+ */
+spec_status spec_draft_block_topk(const void *draft_logits, spec_dtype logits_dtype, const int32_t *anchor,
+                                  const void *U, const void *Wt, spec_dtype w_dtype, int r, int B, int gamma,
+                                  int V, int top_k, double top_p, const uint64_t *seeds, int32_t *tokens_out,
+                                  float *conf_out, float *qtok_out, void *workspace, size_t workspace_bytes,
+                                  spec_stream_t stream);
 
 /*
  * spec_verify_topk - spec_verify at T=1 against top-k / top-p filtered rows.

@@ -67,7 +67,7 @@ def test_workspace_bytes_ranges(lib):
     assert wb(vsd.OP_DRAFT, 1024, 7, 248320, 256) == wb(vsd.OP_DRAFT, 4096 // 7, 7, 248320, 256)
     assert wb(vsd.OP_BRANCH_PLAN, 16, 7, 4096, 0) > 0
     assert wb(vsd.OP_E2ETV, 1 << 20, 64, 8, 0) == 0
-    assert wb(7, 1, 1, 1, 0) == 0
+    assert wb(8, 1, 1, 1, 0) == 0
     # bigger problems never need less workspace
     assert wb(vsd.OP_VERIFY, 64, 7, 248320, 0) >= wb(vsd.OP_VERIFY, 32, 7, 248320, 0)
 
@@ -247,3 +247,24 @@ def test_tree_calls_reject_bad_arguments(lib):
     need = wb(vsd.OP_TREE_VERIFY, 4, 8, 100, 0)
     assert tv(a, vsd.BF16, a, a, a, 4, 8, 100, a, a, a, a, a, need - 1, None) == 9
     assert tv(a, vsd.BF16, a, a, a, 4, 8, 100, a, a, a, a, None, big, None) == 9
+
+
+def test_draft_block_topk_rejects_bad_arguments(lib):
+    wb = lib.spec_workspace_bytes
+    assert wb(vsd.OP_DRAFT_TOPK, 32, 7, 248320, 256) > 0
+    assert wb(vsd.OP_DRAFT_TOPK, 0, 7, 100, 0) == 0
+    a, big = A, 1 << 30
+    f = lib.spec_draft_block_topk
+    args = lambda **kw: dict(dict(l=a, ldt=vsd.BF16, anc=a, U=a, Wt=a, wdt=vsd.BF16, r=16, B=2, G=3, V=100, k=20,
+                                  tp=0.95, seeds=a, tok=a, conf=a, q=a, ws=a, wsb=big), **kw)
+    call = lambda d: f(d["l"], d["ldt"], d["anc"], d["U"], d["Wt"], d["wdt"], d["r"], d["B"], d["G"], d["V"], d["k"],
+                       d["tp"], d["seeds"], d["tok"], d["conf"], d["q"], d["ws"], d["wsb"], None)
+    assert call(args(r=24)) == 2                  # r not a multiple of 16
+    assert call(args(r=272)) == 2                 # r beyond SPEC_MAX_RANK
+    assert call(args(k=0)) == 2 and call(args(k=33)) == 2
+    assert call(args(tp=0.0)) == 1 and call(args(tp=1.5)) == 1
+    assert call(args(wdt=vsd.F32)) == 3           # weights must be bf16
+    assert call(args(seeds=None)) == 1
+    assert call(args(l=MIS)) == 4
+    assert call(args(wsb=wb(vsd.OP_DRAFT_TOPK, 2, 3, 100, 16) - 1)) == 9
+    assert call(args(G=65)) == 2

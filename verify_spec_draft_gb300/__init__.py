@@ -25,7 +25,8 @@ STATUS = {
     8: "SPEC_ERR_TOKEN", 9: "SPEC_ERR_WORKSPACE",
 }
 F32, BF16 = 0, 1
-OP_DRAFT, OP_VERIFY, OP_E2ETV, OP_DRAFT_VERIFY, OP_BRANCH_PLAN, OP_VERIFY_TOPK, OP_TREE_VERIFY = 0, 1, 2, 3, 4, 5, 6
+OP_DRAFT, OP_VERIFY, OP_E2ETV, OP_DRAFT_VERIFY, OP_BRANCH_PLAN, OP_VERIFY_TOPK, OP_TREE_VERIFY, OP_DRAFT_TOPK = (
+    0, 1, 2, 3, 4, 5, 6, 7)
 DEV_TIMEOUT, DEV_NONFINITE, DEV_TOKEN = 1, 2, 4
 
 # C signatures of include/spec.h, as ctypes types
@@ -53,6 +54,8 @@ SIGNATURES = {
     "spec_branch_plan": (_i32, [_vp, _vp, _i32, _i32, _i32, _i32, ctypes.c_uint64, _vp, _vp, _vp, _vp,
                                 _vp, _sz, _vp]),
     "spec_tree_select": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp]),
+    "spec_draft_block_topk": (_i32, [_vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, ctypes.c_double,
+                                     _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "spec_tree_verify": (_i32, [_vp, _i32, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
 }
 
@@ -475,5 +478,35 @@ def tree_verify(target, parent, token, keep=None, ws=None, out=None, stream=None
                                 _ptr(out["n"]), _ptr(out["path"]) if n > 0 else _ptr(None), _ptr(out["committed"]),
                                 _ptr(out["bonus"]), _ptr(ws), ws.numel(), _stream(stream))
     _check(code, "spec_tree_verify")
+    out["ws"] = ws
+    return out
+
+
+def draft_block_topk(logits, anchor, U, Wt, top_k, top_p, seeds, ws=None, out=None, stream=None):
+    """spec_draft_block_topk (T=1, filtered draws).  logits [B, gamma, V] f32/bf16; anchor
+    [B] int32; U, Wt bf16 [V, r] or None; seeds [B] int64.  Returns a dict of device
+    tensors: tokens [B, gamma] int32, conf and qtok [B, gamma] float32."""
+    torch = _torch()
+    lib = load()
+    _need(logits, "logits")
+    dev = logits.device
+    B, G, V = logits.shape
+    _need(anchor, "anchor", dev, torch.int32, (B,))
+    _need(seeds, "seeds", dev, torch.int64, (B,))
+    r = 0
+    if U is not None:
+        r = U.shape[1]
+        _need(U, "U", dev, torch.bfloat16, (V, r))
+        _need(Wt, "Wt", dev, torch.bfloat16, (V, r))
+    if out is None:
+        out = dict(tokens=torch.empty((B, G), dtype=torch.int32, device=dev),
+                   conf=torch.empty((B, G), dtype=torch.float32, device=dev),
+                   qtok=torch.empty((B, G), dtype=torch.float32, device=dev))
+    if ws is None:
+        ws = workspace(OP_DRAFT_TOPK, B, G, V, r, dev, stream)
+    code = lib.spec_draft_block_topk(_ptr(logits), _dtype_code(logits), _ptr(anchor), _ptr(U), _ptr(Wt), BF16, r, B, G,
+                                     V, int(top_k), float(top_p), _ptr(seeds), _ptr(out["tokens"]), _ptr(out["conf"]),
+                                     _ptr(out.get("qtok")), _ptr(ws), ws.numel(), _stream(stream))
+    _check(code, "spec_draft_block_topk")
     out["ws"] = ws
     return out

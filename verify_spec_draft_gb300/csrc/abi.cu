@@ -44,6 +44,10 @@ using namespace spec;
 extern "C" {
 
 size_t spec_workspace_bytes(spec_op op, int B, int gamma, int V, int r) {
+    if (op == SPEC_OP_DRAFT_TOPK) {
+        if (B < 1 || B > 65535) return 0;
+        return draft_topk_workspace_bytes(B);
+    }
     if (op == SPEC_OP_TREE_VERIFY) {   // gamma is the number of nodes per tree
         if (B < 1 || B > 65535 || gamma < 0 || gamma > SPEC_MAX_TREE_NODES || V < 1 || V > SPEC_MAX_V) return 0;
         return tree_verify_workspace_bytes(B, gamma);
@@ -264,6 +268,40 @@ spec_status spec_draft_verify(const void* draft_logits, spec_dtype logits_dtype,
     verify_bind_workspace(v, draft_verify_verify_ws(workspace, B, gamma, V, r));
     v.status = p.status;
     return cuda_status(verify_launch(v, (cudaStream_t)stream));
+}
+
+spec_status spec_draft_block_topk(const void* draft_logits, spec_dtype logits_dtype, const int32_t* anchor,
+                                  const void* U, const void* Wt, spec_dtype w_dtype, int r, int B, int gamma, int V,
+                                  int top_k, double top_p, const uint64_t* seeds, int32_t* tokens_out,
+                                  float* conf_out, float* qtok_out, void* workspace, size_t workspace_bytes,
+                                  spec_stream_t stream) {
+    if (!dtype_ok(logits_dtype) || (r > 0 && w_dtype != SPEC_BF16)) return SPEC_ERR_DTYPE;
+    if (B < 1 || B > 65535 || gamma < 1 || gamma > SPEC_MAX_GAMMA || V < 1 || V > SPEC_MAX_V || r < 0 ||
+        r > SPEC_MAX_RANK || (r % 16) != 0 || top_k < 1 || top_k > SPEC_MAX_TOP_K)
+        return SPEC_ERR_SHAPE;
+    if (!(top_p > 0.0 && top_p <= 1.0)) return SPEC_ERR_INVALID_ARG;
+    if (!draft_logits || !anchor || !seeds || !tokens_out || !conf_out) return SPEC_ERR_INVALID_ARG;
+    if (r > 0 && (!U || !Wt)) return SPEC_ERR_INVALID_ARG;
+    if (!aligned16(draft_logits) || (r > 0 && (!aligned16(U) || !aligned16(Wt)))) return SPEC_ERR_ALIGN;
+    if (!workspace || workspace_bytes < draft_topk_workspace_bytes(B)) return SPEC_ERR_WORKSPACE;
+    DraftTopkLaunch d;
+    memset(&d, 0, sizeof(d));
+    d.logits = draft_logits;
+    d.ldt = logits_dtype;
+    d.anchor = anchor;
+    d.U = r > 0 ? U : nullptr;
+    d.Wt = r > 0 ? Wt : nullptr;
+    d.r = r;
+    d.B = B;
+    d.gamma = gamma;
+    d.V = V;
+    d.k = top_k;
+    d.top_p = top_p;
+    d.seeds = seeds;
+    d.tokens_out = tokens_out;
+    d.conf_out = conf_out;
+    d.qtok_out = qtok_out;
+    return cuda_status(draft_topk_launch(d, workspace, (cudaStream_t)stream));
 }
 
 spec_status spec_tree_select(const int32_t* parent, const float* conf, int n_trees, int n_nodes, int m,

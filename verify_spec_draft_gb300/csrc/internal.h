@@ -140,6 +140,23 @@ struct TopkParams {
 size_t verify_topk_workspace_bytes(int B, int gamma);
 cudaError_t verify_topk_launch(TopkParams& p, void* ws, cudaStream_t stream);
 
+// spec_draft_block_topk: the T=1 chain with filtered draws, position by position.
+struct DraftTopkLaunch {
+    const void* logits;        // [B, gamma, V]
+    int ldt;
+    const int32_t* anchor;     // [B]
+    const void* U;             // bf16 [V, r] (r = 0: no bias)
+    const void* Wt;            // bf16 [V, r]
+    int r, B, gamma, V, k;
+    double top_p;
+    const uint64_t* seeds;     // [B]
+    int32_t* tokens_out;       // [B, gamma]
+    float* conf_out;           // [B, gamma]
+    float* qtok_out;           // [B, gamma] (nullable)
+};
+size_t draft_topk_workspace_bytes(int B);
+cudaError_t draft_topk_launch(const DraftTopkLaunch& a, void* ws, cudaStream_t stream);
+
 struct BranchPlanParams {
     const int32_t* trunk;      // [n_refs, Lmax] token ids
     const int32_t* lengths;    // [n_refs]
