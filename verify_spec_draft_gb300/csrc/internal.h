@@ -136,7 +136,11 @@ struct TopkParams {
     unsigned* status;
     unsigned long long* keys;  // [B*(2*gamma+1)][kTopkMax] each row's largest keys
     unsigned* bad;             // [B*(2*gamma+1)] NaN or +inf in the row
+    unsigned long long* part;  // [rows][kTopkPieces][kTopkMax] the pieces' largest keys
+    unsigned* part_bad;        // [rows][kTopkPieces]
+    unsigned* row_done;        // [rows] pieces finished (returned to 0 by the merge)
 };
+constexpr int kTopkPieces = 8;   // most CTAs that share one row of spec_verify_topk
 size_t verify_topk_workspace_bytes(int B, int gamma);
 cudaError_t verify_topk_launch(TopkParams& p, void* ws, cudaStream_t stream);
 

@@ -16,11 +16,13 @@
 // lower index.
 //
 // Verification (T=0): HBM-bound.  A persistent grid streams the root row and every kept
-// node's row in 8192-entry items with register double-buffered 16-byte loads, folding
-// each row's argmax into a 64-bit key (value, lowest index) with one atomicMax per CTA
-// and item.  The last CTA to finish then marks, for every node in parallel, whether its
-// token is the argmax of its parent's row (keeping the lowest such child per parent),
-// and one thread per tree follows those marks from the root.
+// node's row in 8192-entry items (the items of dropped nodes are compacted away, 256 at
+// a time), two items of 16-byte loads in flight per thread.  Each warp folds its
+// 1024-entry segment of an item into the row's 64-bit argmax key (value, lowest index)
+// with one atomicMax, so warps never wait for one another.  The last CTA to finish then
+// marks, for every node in parallel, whether its token is the argmax of its parent's row
+// (keeping the lowest such child per parent), and one thread per tree follows those
+// marks from the root.
 #include "spec_device.cuh"
 #include "internal.h"
 #include "chunk_rows.cuh"
@@ -169,7 +171,8 @@ __global__ void __launch_bounds__(kTvThreads) tree_verify_kernel(TreeVerifyParam
     constexpr int NW = Words<TT>::N;
     constexpr int D = TvDepth<TT>::D;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    __shared__ long s_it[kTvThreads];   // the CTA's kept items of the current batch
+    __shared__ int s_row[kTvThreads];   // the CTA's kept items of the current batch: row
+    __shared__ int s_c[kTvThreads];     // and chunk
     __shared__ int s_wc[kTvWarps];
     const long mine = items > (long)blockIdx.x ? (items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
 
@@ -194,19 +197,21 @@ __global__ void __launch_bounds__(kTvThreads) tree_verify_kernel(TreeVerifyParam
                 off += w < warp ? v : 0;
                 cnt += v;
             }
-            if (kept) s_it[off + __popc(bal & ((1u << lane) - 1u))] = it;
+            if (kept) {
+                const int at = off + __popc(bal & ((1u << lane) - 1u));
+                s_row[at] = (int)row;
+                s_c[at] = c;
+            }
             __syncthreads();
         }
         // stream the batch with D items of loads in flight per thread
         uint4 buf[D][NW];
-        long rows[D];
-        int cs[D];
+        int rows[D], cs[D];
 #pragma unroll
         for (int d = 0; d < D - 1; ++d)
             if (d < cnt) {
-                const long it = s_it[d];
-                rows[d] = it / (long)nch;
-                cs[d] = (int)(it - rows[d] * (long)nch);
+                rows[d] = s_row[d];
+                cs[d] = s_c[d];
                 load_words_il<TT, NW>(buf[d], target + (size_t)rows[d] * V, V, il_seg(cs[d]), vec);
             }
         for (int j0 = 0; j0 < cnt; j0 += D) {
@@ -215,15 +220,14 @@ __global__ void __launch_bounds__(kTvThreads) tree_verify_kernel(TreeVerifyParam
                 const int j = j0 + d;
                 const int jn = j + D - 1, dn = (d + D - 1) % D;
                 if (jn < cnt) {
-                    const long it = s_it[jn];
-                    rows[dn] = it / (long)nch;
-                    cs[dn] = (int)(it - rows[dn] * (long)nch);
+                    rows[dn] = s_row[jn];
+                    cs[dn] = s_c[jn];
                     load_words_il<TT, NW>(buf[dn], target + (size_t)rows[dn] * V, V, il_seg(cs[dn]), vec);
                 }
                 if (j < cnt) tv_fold<TT, NW>(p, buf[d], rows[d], cs[d]);
             }
         }
-        __syncthreads();   // s_it is rewritten by the next batch
+        __syncthreads();   // s_row and s_c are rewritten by the next batch
     }
 
     if (!last_block_done(&p.done[0], gridDim.x)) return;

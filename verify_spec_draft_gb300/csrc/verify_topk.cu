@@ -38,66 +38,112 @@ namespace spec {
 constexpr int kTopkThreads = 256;
 constexpr int kTopkWarps = kTopkThreads / 32;
 
-// Candidates a warp found in one item, waiting for insertion into its list.
-constexpr int kCandCap = 128;
+// Resident CTAs per SM the row kernel is built for: 4 with bf16 rows (two 64-byte item
+// buffers per thread fit in 64 registers), 2 when either row type is float32.
+template <typename TT, typename DT> struct TopkOcc {
+    static constexpr int N = sizeof(TT) == 2 && sizeof(DT) == 2 ? 4 : 2;
+};
 
-// Entry q (in decode_words order) of a thread's words, decoded on its own.
+// The CTA whose item range [c*I/G, (c+1)*I/G) holds item i.
+__device__ __forceinline__ long topk_cta_of(long i, long I, long G) { return ((i + 1) * G - 1) / I; }
+
+// Lane `e` (< 8) of the warp: entry e of lane L's 8-entry group j of the current item.
 template <typename T, int NW>
-__device__ __forceinline__ float word_entry(const uint4 (&w)[NW], int q) {
+__device__ __forceinline__ float group_entry(const uint4 (&w)[NW], int j, int L, int e) {
     if constexpr (sizeof(T) == 2) {
-        const uint4 v = w[q >> 3];
-        const int h = (q & 7) >> 1;
-        const uint32_t a = h == 0 ? v.x : (h == 1 ? v.y : (h == 2 ? v.z : v.w));
-        return (q & 1) ? __uint_as_float(a & 0xffff0000u) : __uint_as_float(a << 16);
+        const unsigned a0 = __shfl_sync(0xffffffffu, w[j].x, L), a1 = __shfl_sync(0xffffffffu, w[j].y, L);
+        const unsigned a2 = __shfl_sync(0xffffffffu, w[j].z, L), a3 = __shfl_sync(0xffffffffu, w[j].w, L);
+        const int h = (e >> 1) & 3;
+        const unsigned a = h == 0 ? a0 : (h == 1 ? a1 : (h == 2 ? a2 : a3));
+        return (e & 1) ? __uint_as_float(a & 0xffff0000u) : __uint_as_float(a << 16);
     } else {
-        const uint4 v = w[q >> 2];
-        const int h = q & 3;
-        return __uint_as_float(h == 0 ? v.x : (h == 1 ? v.y : (h == 2 ? v.z : v.w)));
+        const uint4 lo = w[2 * j], hi = w[2 * j + 1];
+        const unsigned b0 = __shfl_sync(0xffffffffu, lo.x, L), b1 = __shfl_sync(0xffffffffu, lo.y, L);
+        const unsigned b2 = __shfl_sync(0xffffffffu, lo.z, L), b3 = __shfl_sync(0xffffffffu, lo.w, L);
+        const unsigned b4 = __shfl_sync(0xffffffffu, hi.x, L), b5 = __shfl_sync(0xffffffffu, hi.y, L);
+        const unsigned b6 = __shfl_sync(0xffffffffu, hi.z, L), b7 = __shfl_sync(0xffffffffu, hi.w, L);
+        const int h = e & 7;
+        const unsigned a = h < 4 ? (h == 0 ? b0 : (h == 1 ? b1 : (h == 2 ? b2 : b3)))
+                                 : (h == 4 ? b4 : (h == 5 ? b5 : (h == 6 ? b6 : b7)));
+        return __uint_as_float(a);
     }
 }
 
-// The row at `rowp` (V entries); its k largest keys go to keys[row * kTopkMax + i] in
-// descending order (0 where the row has fewer entries), its bad flag to bad_out[row].
+// Keys of the descending list a[0..n) (distinct, 0 = empty) greater than `key`.
+__device__ __forceinline__ int count_above(const unsigned long long* a, int n, unsigned long long key) {
+    int lo = 0, hi = n;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (a[mid] > key) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo;
+}
+
+// Chunks [c0, c1) of the row at `rowp` (global row `row`), streamed by the CTA: each warp
+// takes its 1024-entry segment of every chunk and keeps the k largest keys it has seen
+// as a sorted list over its lanes.  The piece's k largest go to slot `slot` of the row;
+// the CTA that finishes the row's last piece (of `npieces`) merges them into keys[row].
 template <typename T>
-__device__ __forceinline__ void topk_row(const T* rowp, long V, int k, bool vec, int row, unsigned long long* keys,
-                                         unsigned* bad_out) {
+__device__ __forceinline__ void topk_piece(const TopkParams& p, const T* rowp, long V, bool vec, int c0, int c1,
+                                           long row, int slot, int npieces) {
     constexpr int NW = Words<T>::N;
-    __shared__ unsigned long long s_thr;                       // best k-th key a warp has published
-    __shared__ unsigned long long s_all[kTopkThreads];         // the warps' lists, for the final ranking
-    __shared__ unsigned long long s_cand[kTopkWarps][kCandCap];
-    __shared__ int s_bad;
+    __shared__ unsigned long long s_thr;                 // a key at or below the piece's k-th largest
+    __shared__ unsigned long long s_mth[kTopkWarps];     // each warp's m-th largest key so far
+    __shared__ float s_seed[kTopkWarps];                 // each warp's m-th largest lane maximum
+    __shared__ unsigned long long s_all[kTopkThreads];   // the warps' lists, then the pieces' lists
+    __shared__ int s_bad, s_last;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int nch = (int)((V + kVerifyChunk - 1) / kVerifyChunk);
+    const int k = p.k;
+    const int m = (k + kTopkWarps - 1) / kTopkWarps;   // m keys from each of the 8 warps make k
+    __syncthreads();   // the previous piece's readers of s_thr and s_all are done
     if (threadIdx.x == 0) { s_thr = 0ull; s_bad = 0; }
-    __syncthreads();
+    if (threadIdx.x < kTopkWarps) s_mth[threadIdx.x] = 0ull;
 
     unsigned long long mine = 0ull;   // this lane's slot of the warp's sorted list
     unsigned long long kth = 0ull;    // the warp's k-th key (0 while the list is short)
     unsigned long long thr = 0ull;    // the key to beat: the larger of kth and the CTA's best
     float thr_v = -INFINITY;          // value threshold: entries below it are skipped
     int bad = 0;
+    const int vi = (int)V;            // V < 2^31
     uint4 cur[NW], nxt[NW];
-    load_words_il<T, NW>(cur, rowp, V, il_seg(0), vec);
-    for (int c = 0; c < nch; ++c) {
-        if (c + 1 < nch) load_words_il<T, NW>(nxt, rowp, V, il_seg(c + 1), vec);
-        if (c == 0) {
+    load_words_il<T, NW>(cur, rowp, V, il_seg(c0), vec);
+    unsigned long long mth = 0ull;   // the warp's m-th key, as last published
+    for (int c = c0; c < c1; ++c) {
+        if (c + 1 < c1) load_words_il<T, NW>(nxt, rowp, V, il_seg(c + 1), vec);
+        float g[4];   // the maxima of this lane's four 8-entry groups (NaN if any is NaN)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if constexpr (sizeof(T) == 2) g[j] = u4_max_nan<2>(cur[j]);
+            else g[j] = f_max_nan(u4_max_nan<4>(cur[2 * j]), u4_max_nan<4>(cur[2 * j + 1]));
+        }
+        float lm = f_max_nan(f_max_nan(g[0], g[1]), f_max_nan(g[2], g[3]));
+        if (isnan(lm) || lm == INFINITY) bad = 1;
+        if (c == c0) {
             // seed: the k-th largest of the 32 lane maxima (each an entry of this item)
-            float lm = chunk_max_nan<T, NW>(cur);
-            if (isnan(lm) || lm == INFINITY) bad = 1;
+            float sm = lm;
 #pragma unroll
             for (int kk = 2; kk <= 32; kk <<= 1)   // bitonic sort of the lane maxima, ascending
 #pragma unroll
                 for (int j = kk >> 1; j > 0; j >>= 1) {
-                    const float o = __shfl_xor_sync(0xffffffffu, lm, j);
+                    const float o = __shfl_xor_sync(0xffffffffu, sm, j);
                     const bool take_max = ((lane & kk) == 0) != ((lane & j) == 0);
-                    lm = take_max ? fmaxf(lm, o) : fminf(lm, o);
+                    sm = take_max ? fmaxf(sm, o) : fminf(sm, o);
                 }
-            const float seed = __shfl_sync(0xffffffffu, lm, 32 - k);   // the k-th largest
+            // a value with k entries of the item at or above it: this warp's k-th largest
+            // lane maximum, or the smallest of the warps' m-th largest (m from each warp)
+            const float own = __shfl_sync(0xffffffffu, sm, 32 - k);
+            const float mw = __shfl_sync(0xffffffffu, sm, 32 - m);
+            if (lane == 0) s_seed[warp] = mw;
+            __syncthreads();
+            float cta = s_seed[0];
+#pragma unroll
+            for (int w = 1; w < kTopkWarps; ++w) cta = fminf(cta, s_seed[w]);
+            const float seed = fmaxf(own, cta);
             thr_v = isnan(seed) ? -INFINITY : seed;
         }
-        // the CTA's best k-th key, read once and broadcast: every lane of the warp must see
-        // the same threshold (the insertions below are warp-collective), and other warps
-        // raise s_thr concurrently
+        // the CTA's best k-th key, read once and broadcast: every lane must see the same
+        // threshold (the insertions below are warp-collective)
         unsigned long long st_l = 0ull;
         if (lane == 0) st_l = *(volatile unsigned long long*)&s_thr;
         const unsigned long long shared_thr = shfl_u64(st_l, 0);
@@ -105,102 +151,133 @@ __device__ __forceinline__ void topk_row(const T* rowp, long V, int k, bool vec,
             thr = shared_thr;
             thr_v = fmaxf(thr_v, key_value(shared_thr));
         }
-        // this lane's entries at or above the threshold (their keys), counted first; entry
-        // q of the lane is vocabulary index ebase + (q / 8) * 256 + q % 8 (V < 2^31)
-        const int ebase = (int)il_seg(c) + lane * 8;
-        const int vi = (int)V;
-        int ncand = 0;
-        float gmax[4];
+        if (__any_sync(0xffffffffu, !bad && lm >= thr_v)) {
+            const int seg = (int)il_seg(c);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            if constexpr (sizeof(T) == 2) gmax[j] = u4_max_nan<2>(cur[j]);
-            else gmax[j] = f_max_nan(u4_max_nan<4>(cur[2 * j]), u4_max_nan<4>(cur[2 * j + 1]));
-            if (isnan(gmax[j]) || gmax[j] == INFINITY) bad = 1;
-        }
-        const bool any_hot = !bad && (gmax[0] >= thr_v || gmax[1] >= thr_v || gmax[2] >= thr_v || gmax[3] >= thr_v);
-        if (__any_sync(0xffffffffu, any_hot)) {
-            const float cut = thr_v;   // the entries taken this item: fixed while they are buffered
-            if (any_hot) {
-#pragma unroll
-                for (int q = 0; q < kEPT; ++q)
-                    ncand += (word_entry<T, NW>(cur, q) >= cut && ebase + (q >> 3) * 256 + (q & 7) < vi) ? 1 : 0;
-            }
-            // write them to the warp's buffer (an exclusive prefix over lanes); rounds of at
-            // most kCandCap, each followed by the insertions
-            int before = 0, total = 0;
-            {
-                int incl = ncand;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += y;
-                }
-                before = incl - ncand;
-                total = __shfl_sync(0xffffffffu, incl, 31);
-            }
-            for (int r0 = 0; r0 < total; r0 += kCandCap) {
-                int pos = before - r0;
-                if (any_hot && ncand > 0) {
-#pragma unroll
-                    for (int q = 0; q < kEPT; ++q) {
-                        const int e = ebase + (q >> 3) * 256 + (q & 7);
-                        const float xq = word_entry<T, NW>(cur, q);
-                        if (xq >= cut && e < vi) {
-                            if (pos >= 0 && pos < kCandCap) s_cand[warp][pos] = argmax_key(xq, (uint32_t)e);
-                            ++pos;
+            for (int j = 0; j < 4; ++j) {
+                // the lanes whose group j reaches the threshold, one group at a time: lanes
+                // 0..7 take its entries, and the keys above the threshold are inserted
+                unsigned hm = __ballot_sync(0xffffffffu, !bad && g[j] >= thr_v);
+                while (hm) {
+                    const int L = __ffs(hm) - 1;
+                    hm &= hm - 1u;
+                    const float x = group_entry<T, NW>(cur, j, L, lane);
+                    const int e = seg + (j * 32 + L) * 8 + (lane & 7);
+                    const unsigned long long key = argmax_key(x, (uint32_t)e);
+                    unsigned cm = __ballot_sync(0xffffffffu, lane < 8 && e < vi && x >= thr_v && key > thr);
+                    while (cm) {   // warp-uniform
+                        const int s = __ffs(cm) - 1;
+                        cm &= cm - 1u;
+                        const unsigned long long ks = shfl_u64(key, s);
+                        if (ks > thr) {
+                            list_insert(mine, ks, k, kth);
+                            if (kth > thr) {
+                                thr = kth;
+                                thr_v = fmaxf(thr_v, key_value(kth));
+                            }
                         }
                     }
                 }
-                __syncwarp();
-                const int nr = min(kCandCap, total - r0);
-                for (int i = 0; i < nr; ++i) {   // warp-uniform
-                    const unsigned long long key = s_cand[warp][i];
-                    if (key > thr) {
-                        list_insert(mine, key, k, kth);
-                        if (kth > thr) {
-                            thr = kth;
-                            thr_v = fmaxf(thr_v, key_value(kth));
-                        }
-                    }
-                }
-                __syncwarp();
             }
-            // publish the warp's k-th key
-            if (lane == 0 && kth > *(volatile unsigned long long*)&s_thr) atomicMax(&s_thr, kth);
+            // publish the warp's k-th key, and its m-th: the smallest of the warps' m-th
+            // keys has at least k keys at or above it (each value stays valid: a list's
+            // j-th key never falls)
+            const unsigned long long mt = shfl_u64(mine, m - 1);
+            if (lane == 0) {
+                unsigned long long bound = kth;
+                if (mt != mth) {
+                    *(volatile unsigned long long*)&s_mth[warp] = mt;
+                    unsigned long long lo = mt;
+#pragma unroll
+                    for (int w = 0; w < kTopkWarps; ++w) {
+                        const unsigned long long v = *(volatile unsigned long long*)&s_mth[w];
+                        lo = v < lo ? v : lo;
+                    }
+                    bound = lo > bound ? lo : bound;
+                }
+                if (bound > *(volatile unsigned long long*)&s_thr) atomicMax(&s_thr, bound);
+            }
+            mth = mt;
         }
 #pragma unroll
         for (int i = 0; i < NW; ++i) cur[i] = nxt[i];
     }
     if (bad) s_bad = 1;
-    __syncthreads();
-    bad = s_bad;
-    // the row's k largest: only a warp's first k keys can be among them; rank each of
+    // the piece's k largest: only a warp's first k keys can be among them; rank each of
     // those among all of them (keys are distinct, the index being part of them, except
     // the empty key 0)
     const bool lane_k = lane < k;
     s_all[threadIdx.x] = lane_k ? mine : 0ull;
     __syncthreads();
-    unsigned long long* out = keys + (size_t)row * kTopkMax;
+    const size_t ps = (size_t)row * kTopkPieces + slot;
+    unsigned long long* out = p.part + ps * kTopkMax;
     if (threadIdx.x < kTopkMax) out[threadIdx.x] = 0ull;
     __syncthreads();
-    if (!bad && lane_k && mine != 0ull) {
-        int rank = 0;
+    if (!s_bad && lane_k && mine != 0ull) {
+        int rank = lane;   // the keys of this warp's list above this one
         for (int w = 0; w < kTopkWarps; ++w)
-            for (int i = 0; i < k; ++i) rank += s_all[w * 32 + i] > mine ? 1 : 0;
+            if (w != warp) rank += count_above(s_all + w * 32, k, mine);
         if (rank < k) out[rank] = mine;
     }
-    if (threadIdx.x == 0) bad_out[row] = bad ? 1u : 0u;
+    if (threadIdx.x == 0) p.part_bad[ps] = s_bad ? 1u : 0u;
+
+    // the last piece of the row to finish merges the pieces' lists
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        s_last = atomicAdd(&p.row_done[row], 1u) == (unsigned)npieces - 1u ? 1 : 0;
+        if (s_last) __threadfence();
+    }
+    __syncthreads();
+    if (!s_last) return;
+    unsigned long long* kout = p.keys + (size_t)row * kTopkMax;
+    const int q = threadIdx.x;   // kTopkThreads == kTopkPieces * kTopkMax
+    const unsigned long long key =
+        q / kTopkMax < npieces && q % kTopkMax < k ? __ldcg(&p.part[(size_t)row * kTopkPieces * kTopkMax + q]) : 0ull;
+    const int pbad = q < npieces ? (int)__ldcg(&p.part_bad[(size_t)row * kTopkPieces + q]) : 0;
+    s_all[q] = key;
+    if (q < kTopkMax) kout[q] = 0ull;
+    const int rowbad = __syncthreads_or(pbad);
+    if (!rowbad && key != 0ull) {
+        int rank = q % kTopkMax;   // the keys of this piece's list above this one
+        for (int w = 0; w < npieces; ++w)
+            if (w != q / kTopkMax) rank += count_above(s_all + w * kTopkMax, k, key);
+        if (rank < k) kout[rank] = key;
+    }
+    if (q == 0) {
+        p.bad[row] = rowbad ? 1u : 0u;
+        p.row_done[row] = 0u;
+    }
 }
 
-// All rows of a request batch in one grid: target rows 0 .. nT-1, then draft rows.
+// Items (row, chunk of 8192 entries) of the target rows 0 .. nT-1, then of the draft
+// rows; CTA c streams items [c*I/G, (c+1)*I/G), at least a quarter of a row, so that a
+// row is split over at most 6 CTAs.
+template <typename T>
+__device__ __forceinline__ void topk_range(const TopkParams& p, const T* base, bool vec, long a, long b, long row0,
+                                           long nch, long I) {
+    const long G = gridDim.x;
+    for (long it = a; it < b;) {
+        const long row = it / nch;
+        const long end = b < (row + 1) * nch ? b : (row + 1) * nch;
+        const long cf = topk_cta_of(row * nch, I, G), cl = topk_cta_of((row + 1) * nch - 1, I, G);
+        topk_piece<T>(p, base + (size_t)(row - row0) * p.V, p.V, vec, (int)(it - row * nch), (int)(end - row * nch),
+                      row, (int)(blockIdx.x - cf), (int)(cl - cf + 1));
+        it = end;
+    }
+}
+
 template <typename TT, typename DT>
-__global__ void __launch_bounds__(kTopkThreads) topk_rows_kernel(TopkParams p, bool vt, bool vd) {
-    const int row = blockIdx.x;
-    const int nT = p.B * (p.gamma + 1);
-    if (row < nT)
-        topk_row<TT>(static_cast<const TT*>(p.target) + (size_t)row * p.V, p.V, p.k, vt, row, p.keys, p.bad);
-    else
-        topk_row<DT>(static_cast<const DT*>(p.draft) + (size_t)(row - nT) * p.V, p.V, p.k, vd, row, p.keys, p.bad);
+__global__ void __launch_bounds__(kTopkThreads, TopkOcc<TT, DT>::N) topk_rows_kernel(TopkParams p, bool vt, bool vd) {
+    static_assert(kTopkThreads == kTopkPieces * kTopkMax, "merge layout");
+    const long nch = ((long)p.V + kVerifyChunk - 1) / kVerifyChunk;
+    const long nT = (long)p.B * (p.gamma + 1);
+    const long I = (long)p.B * (2 * p.gamma + 1) * nch;
+    const long G = gridDim.x;
+    const long i0 = (long)blockIdx.x * I / G, i1 = ((long)blockIdx.x + 1) * I / G;
+    const long tend = nT * nch;
+    if (i0 < tend) topk_range<TT>(p, static_cast<const TT*>(p.target), vt, i0, i1 < tend ? i1 : tend, 0, nch, I);
+    if (i1 > tend) topk_range<DT>(p, static_cast<const DT*>(p.draft), vd, i0 > tend ? i0 : tend, i1, nT, nch, I);
 }
 
 // ----------------------------------------------------------------------------------
@@ -284,15 +361,30 @@ __global__ void __launch_bounds__(kTopkThreads) topk_accept_kernel(TopkParams p)
     }
 }
 
+static size_t topk_align(size_t x) { return (x + 255) / 256 * 256; }
+
 size_t verify_topk_workspace_bytes(int B, int gamma) {
     const size_t rows = (size_t)B * (2 * gamma + 1);
-    return kWsHeaderBytes + rows * kTopkMax * sizeof(unsigned long long) + rows * sizeof(unsigned);
+    size_t off = kWsHeaderBytes;
+    off = topk_align(off + rows * kTopkMax * sizeof(unsigned long long));                 // keys
+    off = topk_align(off + rows * sizeof(unsigned));                                      // bad
+    off = topk_align(off + rows * kTopkPieces * kTopkMax * sizeof(unsigned long long));   // part
+    off = topk_align(off + rows * kTopkPieces * sizeof(unsigned));                        // part_bad
+    return topk_align(off + rows * sizeof(unsigned));                                     // row_done
 }
 
 template <typename TT, typename DT>
 static cudaError_t launch_rows(const TopkParams& p, bool vt, bool vd, cudaStream_t stream) {
-    const long rows = (long)p.B * (2 * p.gamma + 1);
-    topk_rows_kernel<TT, DT><<<(unsigned)rows, kTopkThreads, 0, stream>>>(p, vt, vd);
+    void (*k)(TopkParams, bool, bool) = topk_rows_kernel<TT, DT>;
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, kTopkThreads, 0) != cudaSuccess || occ < 1) occ = 1;
+    const long nch = ((long)p.V + kVerifyChunk - 1) / kVerifyChunk;
+    const long I = (long)p.B * (2 * p.gamma + 1) * nch;
+    const long per_min = (nch + 3) / 4;   // a CTA takes at least a quarter of a row
+    long grid = (long)device_sm_count() * occ;
+    if (grid > I / per_min) grid = I / per_min;
+    if (grid < 1) grid = 1;
+    k<<<(unsigned)grid, kTopkThreads, 0, stream>>>(p, vt, vd);
     return cudaGetLastError();
 }
 
@@ -300,8 +392,16 @@ cudaError_t verify_topk_launch(TopkParams& p, void* ws, cudaStream_t stream) {
     char* w = static_cast<char*>(ws);
     p.status = &reinterpret_cast<WsHeader*>(w)->status;
     const size_t rows = (size_t)p.B * (2 * p.gamma + 1);
-    p.keys = reinterpret_cast<unsigned long long*>(w + kWsHeaderBytes);
-    p.bad = reinterpret_cast<unsigned*>(w + kWsHeaderBytes + rows * kTopkMax * sizeof(unsigned long long));
+    size_t off = kWsHeaderBytes;
+    p.keys = reinterpret_cast<unsigned long long*>(w + off);
+    off = topk_align(off + rows * kTopkMax * sizeof(unsigned long long));
+    p.bad = reinterpret_cast<unsigned*>(w + off);
+    off = topk_align(off + rows * sizeof(unsigned));
+    p.part = reinterpret_cast<unsigned long long*>(w + off);
+    off = topk_align(off + rows * kTopkPieces * kTopkMax * sizeof(unsigned long long));
+    p.part_bad = reinterpret_cast<unsigned*>(w + off);
+    off = topk_align(off + rows * kTopkPieces * sizeof(unsigned));
+    p.row_done = reinterpret_cast<unsigned*>(w + off);
     const bool vt = ((size_t)p.V * (p.tdt == SPEC_BF16 ? 2 : 4)) % 16 == 0;
     const bool vd = ((size_t)p.V * (p.ddt == SPEC_BF16 ? 2 : 4)) % 16 == 0;
     cudaError_t e;

@@ -1,6 +1,6 @@
 """Launch one operation a few times on a synthetic workload, for profiler captures.
 
-    python -m verify_spec_draft_gb300.profile_cases {draft,draft_t1,verify_t0,verify_t1,verify_topk,e2etv} [--launches N]
+    python -m verify_spec_draft_gb300.profile_cases CASE [--launches N]
 
 Nothing is timed here; the point is a short process with a handful of launches of one
 kernel, on inputs larger than L2 (129 MB) but only a few hundred MB on the device:
@@ -12,15 +12,18 @@ kernel, on inputs larger than L2 (129 MB) but only a few hundred MB on the devic
   verify_topk spec_verify_topk on the same rows, top_k 20, top_p 0.95
   e2etv      spec_e2etv on 64 branches x Wb=7 = 448 rows, V=248320 (445 MB in, 222 MB out):
              a 64-anchor slice of the 16 x 64 x 7 layout
+  tree_verify spec_tree_verify on 32 trees x 64 nodes, V=248320 (2080 rows, 1.03 GB)
+  draft_topk spec_draft_block_topk, B=32, gamma=7, V=248320, r=256, top_k 20, top_p 0.95
+             (365 MB: logits, U, Wt)
 """
 
 import argparse
 
 import torch
 
-from . import draft_block, e2etv, load, synth, verify, verify_topk
+from . import draft_block, draft_block_topk, e2etv, load, synth, tree_verify, verify, verify_topk
 
-CASES = ("draft", "draft_t1", "verify_t0", "verify_t1", "verify_topk", "e2etv")
+CASES = ("draft", "draft_t1", "verify_t0", "verify_t1", "verify_topk", "e2etv", "tree_verify", "draft_topk")
 
 
 def main(argv=None):
@@ -53,6 +56,16 @@ def main(argv=None):
         tok = synth.draft_tokens(inp["draft"], 1, seed=inp["cfg"].seed)
         ref = verify(inp["target"], inp["draft"], tok, 1, inp["seeds"])
         run = lambda: verify(inp["target"], inp["draft"], tok, 1, inp["seeds"], ws=ref["ws"], out=ref)
+    elif args.case == "tree_verify":
+        c = synth.TREE_CONFIG
+        x = synth.tree_inputs(c.B, c.gamma, c.V, c.dtype, seed=c.seed, device=dev, p_match=0.75)
+        ref = tree_verify(x["target"], x["parent"], x["token"])
+        run = lambda: tree_verify(x["target"], x["parent"], x["token"], ws=ref["ws"], out=ref)
+    elif args.case == "draft_topk":
+        inp = synth.config_inputs(4, device=dev)
+        ref = draft_block_topk(inp["draft"], inp["anchor"], inp["U"], inp["Wt"], 20, 0.95, inp["seeds"])
+        run = lambda: draft_block_topk(inp["draft"], inp["anchor"], inp["U"], inp["Wt"], 20, 0.95, inp["seeds"],
+                                       ws=ref["ws"], out=ref)
     else:
         c = synth.CONFIGS[5]
         n_branches = 64
