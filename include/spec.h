@@ -102,6 +102,7 @@ typedef enum {
 #define SPEC_MAX_DRAFT_ROWS (1 << 20)   /* spec_draft_block: B * gamma             */
 #define SPEC_MAX_TRUNK 16384   /* spec_branch_plan: tokens of one reference        */
 #define SPEC_MAX_TOP_K 32      /* spec_verify_topk: largest top_k                  */
+#define SPEC_MAX_V_DRAFT_TOPK (1 << 19)   /* spec_draft_block_topk: vocabulary size */
 #define SPEC_MAX_TREE_NODES 1024  /* spec_tree_select / spec_tree_verify: nodes per tree */
 
 /*
@@ -114,7 +115,7 @@ typedef enum {
  *          SPEC_OP_VERIFY_TOPK: B requests, gamma positions (V and r unused).
  *          SPEC_OP_TREE_VERIFY: B = trees, gamma = nodes per tree (0 allowed, up to
  *          SPEC_MAX_TREE_NODES), V, r unused.
- *          SPEC_OP_DRAFT_TOPK: B requests (gamma, V, r unused).
+ *          SPEC_OP_DRAFT_TOPK: B requests, V entries (gamma and r unused).
  *          For SPEC_OP_DRAFT the size covers one launch's slice of requests, which
  *          spec_draft_block reuses across the slices of a larger batch.
  * Returns 0 for arguments outside the supported ranges.
@@ -399,12 +400,14 @@ spec_status spec_e2etv_shard(const uint16_t *target_logits, const uint16_t *draf
  *   seeds         [B] uint64.
  *   tokens_out    [B, gamma] int32; conf_out [B, gamma] float32; qtok_out [B, gamma]
  *                 float32 (nullable).
- *   workspace     spec_workspace_bytes(SPEC_OP_DRAFT_TOPK, B, gamma, V, r).
+ *   workspace     spec_workspace_bytes(SPEC_OP_DRAFT_TOPK, B, gamma, V, r): about
+ *                 B * V * 4 bytes (each position's biased logits are kept there for the
+ *                 draw), 32 MB at B = 32, V = 248,320.
  * A request whose anchor lies outside [0, V) (flag TOKEN), or whose row j holds NaN or
  * +inf or no finite entry (flag NONFINITE), gets tokens -1 and NaN statistics from that
  * position on.  The chain is walked position by position (2 * gamma launches); the
  * weights are read once per position for every 32 requests.
- * Limits: 1 <= gamma <= SPEC_MAX_GAMMA, 1 <= V <= SPEC_MAX_V, 1 <= B <= 65535.
+ * Limits: 1 <= gamma <= SPEC_MAX_GAMMA, 1 <= V <= SPEC_MAX_V_DRAFT_TOPK, 1 <= B <= 65535.
  */
 spec_status spec_draft_block_topk(const void *draft_logits, spec_dtype logits_dtype, const int32_t *anchor,
                                   const void *U, const void *Wt, spec_dtype w_dtype, int r, int B, int gamma,

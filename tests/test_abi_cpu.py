@@ -268,3 +268,7 @@ def test_draft_block_topk_rejects_bad_arguments(lib):
     assert call(args(l=MIS)) == 4
     assert call(args(wsb=wb(vsd.OP_DRAFT_TOPK, 2, 3, 100, 16) - 1)) == 9
     assert call(args(G=65)) == 2
+    assert call(args(V=(1 << 19) + 1)) == 2       # beyond SPEC_MAX_V_DRAFT_TOPK
+    assert wb(vsd.OP_DRAFT_TOPK, 2, 3, (1 << 19) + 1, 16) == 0
+    # the workspace holds each position's biased logits: about B * V * 4 bytes
+    assert wb(vsd.OP_DRAFT_TOPK, 32, 7, 248320, 256) >= 32 * 248320 * 4

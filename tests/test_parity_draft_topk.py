@@ -74,6 +74,10 @@ def _compare(out, ref):
     (1, 7, 20, 32, 32, 1.0, torch.float32, 0.5),       # V < k: every entry a candidate
     (40, 2, 3000, 32, 20, 0.95, torch.bfloat16, 0.3),  # more than one chunk of 32 requests
     (3, 3, 7001, 48, 7, 0.5, torch.float32, 0.4),      # V % 8 != 0, small top_p
+    # tensor-core tiles kernel (r a multiple of 64, rows a multiple of 16 bytes):
+    (40, 2, 3000, 64, 20, 0.95, torch.bfloat16, 0.3),  # two chunks of requests
+    (70, 2, 2048, 128, 16, 0.9, torch.bfloat16, 0.3),  # three chunks: the U buffers are reused
+    (2, 3, 40, 64, 32, 1.0, torch.bfloat16, 0.5),      # one ragged tile, V < k
 ])
 def test_small(spec, B, G, V, r, k, top_p, ldtype, scale):
     d, U, Wt, anchor, seeds = _inputs(B, G, V, r, ldtype, scale, seed=V + k + r)

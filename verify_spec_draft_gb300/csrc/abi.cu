@@ -45,8 +45,8 @@ extern "C" {
 
 size_t spec_workspace_bytes(spec_op op, int B, int gamma, int V, int r) {
     if (op == SPEC_OP_DRAFT_TOPK) {
-        if (B < 1 || B > 65535) return 0;
-        return draft_topk_workspace_bytes(B);
+        if (B < 1 || B > 65535 || V < 1 || V > SPEC_MAX_V_DRAFT_TOPK) return 0;
+        return draft_topk_workspace_bytes(B, V);
     }
     if (op == SPEC_OP_TREE_VERIFY) {   // gamma is the number of nodes per tree
         if (B < 1 || B > 65535 || gamma < 0 || gamma > SPEC_MAX_TREE_NODES || V < 1 || V > SPEC_MAX_V) return 0;
@@ -276,14 +276,14 @@ spec_status spec_draft_block_topk(const void* draft_logits, spec_dtype logits_dt
                                   float* conf_out, float* qtok_out, void* workspace, size_t workspace_bytes,
                                   spec_stream_t stream) {
     if (!dtype_ok(logits_dtype) || (r > 0 && w_dtype != SPEC_BF16)) return SPEC_ERR_DTYPE;
-    if (B < 1 || B > 65535 || gamma < 1 || gamma > SPEC_MAX_GAMMA || V < 1 || V > SPEC_MAX_V || r < 0 ||
+    if (B < 1 || B > 65535 || gamma < 1 || gamma > SPEC_MAX_GAMMA || V < 1 || V > SPEC_MAX_V_DRAFT_TOPK || r < 0 ||
         r > SPEC_MAX_RANK || (r % 16) != 0 || top_k < 1 || top_k > SPEC_MAX_TOP_K)
         return SPEC_ERR_SHAPE;
     if (!(top_p > 0.0 && top_p <= 1.0)) return SPEC_ERR_INVALID_ARG;
     if (!draft_logits || !anchor || !seeds || !tokens_out || !conf_out) return SPEC_ERR_INVALID_ARG;
     if (r > 0 && (!U || !Wt)) return SPEC_ERR_INVALID_ARG;
     if (!aligned16(draft_logits) || (r > 0 && (!aligned16(U) || !aligned16(Wt)))) return SPEC_ERR_ALIGN;
-    if (!workspace || workspace_bytes < draft_topk_workspace_bytes(B)) return SPEC_ERR_WORKSPACE;
+    if (!workspace || workspace_bytes < draft_topk_workspace_bytes(B, V)) return SPEC_ERR_WORKSPACE;
     DraftTopkLaunch d;
     memset(&d, 0, sizeof(d));
     d.logits = draft_logits;

@@ -11,34 +11,48 @@
 //
 // A filtered draw needs the biased row's k largest entries, so the chain is walked
 // position by position: per position j, two kernels.
-//   draft_topk_tiles_kernel  CTA c owns a contiguous range of 128-entry vocabulary tiles.
-//                            For 32 requests at a time it gathers U[x_{j-1}] into shared
-//                            memory; per tile it stages the tile's Wt rows, forms the
+//   draft_topk_tiles_kernel  CTA c owns a contiguous range of 128-entry vocabulary tiles
+//                            (one CTA per SM).  The tiles' Wt rows stream through a
+//                            two-stage ring of bulk copies, so the next tile lands while
+//                            the current one is used.  For 32 requests at a time it
+//                            gathers U[x_{j-1}] into shared memory; per tile it forms the
 //                            128 x 32 bias block with bf16 tensor-core MMAs (float32
-//                            accumulate), adds the drafter logits, and folds each
-//                            request's z values into base-2 softmax statistics and a
-//                            warp-sorted list of its k largest keys (entries below the
-//                            list's threshold are skipped).  One record per (request,
-//                            CTA).
-//   draft_topk_pick_kernel   one CTA per request: merges the statistics (c_j = 1/Z),
-//                            takes the row's k largest keys from the CTAs' lists (only
-//                            keys at or above the largest CTA k-th key can qualify),
-//                            filters, draws, writes the outputs and x_j for position j+1.
-// The weights are read once per position (per 32 requests).
+//                            accumulate) and adds the drafter logits.  Each request's z
+//                            values are folded into base-2 softmax statistics (one record
+//                            per request and CTA), the tile's largest key (value, lowest
+//                            index) is recorded, and z itself is written out (float32).
+//   draft_topk_pick_kernel   one CTA per request: merges the statistics (c_j = 1/Z).  The
+//                            row's k largest entries lie in the k tiles with the largest
+//                            maxima: no other tile holds an entry at or above the k-th
+//                            largest tile maximum T, which is itself at or below the row's
+//                            k-th largest entry.  So the k largest tile maxima are selected,
+//                            those tiles' z values re-read, the entries at or above T
+//                            ranked, and the k largest filtered and drawn.  It writes the
+//                            outputs and x_j for position j+1.
+// The weights are read once per position for every 32 requests.  The tiles kernel is a
+// programmatic dependent of the previous pick: its first weight copies are issued before
+// it waits for x_{j-1}.
 #include <mma.h>
 
 #include "spec_device.cuh"
 #include "internal.h"
+#include "tc_common.cuh"
 #include "topk_common.cuh"
 
 namespace spec {
 
-constexpr int kDtThreads = 256;
-constexpr int kDtWarps = kDtThreads / 32;
-constexpr int kDtChunk = 32;        // requests per gathered U block
-constexpr int kDtTile = 128;        // vocabulary entries per tile
-constexpr int kDtMaxCtas = 512;     // CTA ranges (workspace sizing)
-constexpr int kDtCandCap = 4096;    // merge buffer of the pick kernel
+constexpr int kDtThreads = 512;               // tiles kernel: 16 warps
+constexpr int kDpThreads = 256;               // pick kernel
+constexpr int kDpWarps = kDpThreads / 32;
+constexpr int kDtChunk = 32;                  // requests per gathered U block
+constexpr int kDtTile = 128;                  // vocabulary entries per tile
+constexpr int kDtMaxCtas = 512;               // CTA ranges (workspace sizing)
+constexpr int kDtRecMax = 4 * kDtMaxCtas;     // statistics records per request (CTA, or CTA and quadrant)
+constexpr int kDtCandCap = 4096;              // candidates of the pick kernel
+constexpr int kDtLdz = kDtTile + 4;           // bias block row (floats)
+constexpr int kDpPer = kDtCandCap / kDpThreads;   // candidates per pick thread
+static_assert(SPEC_MAX_V_DRAFT_TOPK / kDtTile <= kDtCandCap, "every tile maximum fits the candidate buffer");
+static_assert(SPEC_MAX_TOP_K * kDtTile <= kDtCandCap, "the k best tiles' entries fit the candidate buffer");
 
 struct DraftTopkParams {
     const void* logits;        // [B, gamma, V]
@@ -53,12 +67,17 @@ struct DraftTopkParams {
     float* conf_out;
     float* qtok_out;           // nullable
     int nC;                    // CTA ranges of the tiles kernel
+    int nrec;                  // statistics records per request (nC, or 4 nC on the tensor-core path)
     int n_tiles;
+    long ldzb;                 // row stride of zbuf: V rounded up to a multiple of 4
+    bool vec;                  // logits rows 16-byte aligned with V % 4 == 0 (4-entry loads)
+    bool lbulk;                // logits rows a multiple of 16 bytes: tiles copied with the weights
     unsigned* status;
     int32_t* xprev;            // [B] x_{j-1} for j >= 2 (-1: the request has ended)
-    float2* stats;             // [B * kDtMaxCtas] (m2, s) per CTA range
-    unsigned* bad;             // [B * kDtMaxCtas]
-    unsigned long long* keys;  // [B * kDtMaxCtas * kTopkMax]
+    float2* stats;             // [B * kDtRecMax] (m2, s) per record
+    unsigned* bad;             // [B * kDtRecMax]
+    unsigned long long* tmax;  // [B * n_tiles] each tile's largest key (zero between positions)
+    float* zbuf;               // [B][ldzb] the biased logits z_j
 };
 
 __device__ __forceinline__ int dt_prev(const DraftTopkParams& p, int b) {
@@ -66,23 +85,88 @@ __device__ __forceinline__ int dt_prev(const DraftTopkParams& p, int b) {
     return (x >= 0 && x < p.V) ? x : -1;
 }
 
+// Four consecutive drafter logits from entry v (-inf past V).
 template <typename LT>
-__global__ void __launch_bounds__(kDtThreads) draft_topk_tiles_kernel(DraftTopkParams p) {
+__device__ __forceinline__ void load4(const LT* row, long v, int V, bool vec, float (&x)[4]) {
+    if (vec && v + 4 <= V) {
+        if constexpr (sizeof(LT) == 2) {
+            const uint2 w = __ldg(reinterpret_cast<const uint2*>(row + v));
+            x[0] = __uint_as_float(w.x << 16);
+            x[1] = __uint_as_float(w.x & 0xffff0000u);
+            x[2] = __uint_as_float(w.y << 16);
+            x[3] = __uint_as_float(w.y & 0xffff0000u);
+        } else {
+            const float4 w = __ldg(reinterpret_cast<const float4*>(row + v));
+            x[0] = w.x; x[1] = w.y; x[2] = w.z; x[3] = w.w;
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[e] = v + e < V ? load_one(row + v + e) : -INFINITY;
+    }
+}
+
+// One logit from shared memory as float.
+__device__ __forceinline__ float load_one_smem(const float* q) { return *q; }
+__device__ __forceinline__ float load_one_smem(const bf16_t* q) {
+    return __uint_as_float((uint32_t)*reinterpret_cast<const unsigned short*>(q) << 16);
+}
+
+template <typename LT>
+__global__ void __launch_bounds__(kDtThreads, 1) draft_topk_tiles_kernel(DraftTopkParams p) {
     using namespace nvcuda;
     extern __shared__ __align__(128) uint8_t dt_smem[];
+    __shared__ __align__(8) uint64_t s_full[2];
     const int r = p.r;
-    const int ldw = r + 8;                      // padded rows (bf16), a multiple of 8
-    constexpr int ldz = kDtTile + 4;            // z block [32 requests][ldz] float
-    bf16_t* s_w = reinterpret_cast<bf16_t*>(dt_smem);                        // [128][ldw]
-    bf16_t* s_u = s_w + (size_t)kDtTile * ldw;                                // [32][ldw]
-    float* s_z = reinterpret_cast<float*>(s_u + (size_t)kDtChunk * ldw);      // [32][ldz]
+    const int ldw = r + 8;   // padded Wt / U rows (bf16): 16-byte multiples, no bank conflicts
+    const bool lbulk = p.lbulk;
+    // ring stage: the tile's Wt rows [128][ldw], then the chunk's logits [32][128]
+    const size_t wbytes = r > 0 ? (size_t)kDtTile * ldw * sizeof(bf16_t) : 0;
+    const size_t stage = wbytes + (lbulk ? (size_t)kDtChunk * kDtTile * sizeof(LT) : 0);
+    bf16_t* s_u = reinterpret_cast<bf16_t*>(dt_smem + 2 * stage);                        // [32][ldw]
+    float* s_z = reinterpret_cast<float*>(s_u + (size_t)kDtChunk * ldw);                 // [2][32][kDtLdz]
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int c = blockIdx.x;
     const int tb = (int)(((long)c * p.n_tiles) / p.nC), te = (int)(((long)(c + 1) * p.n_tiles) / p.nC);
-    const int k = p.k;
+    const int nt = te - tb;
+    const int nchunks = (p.B + kDtChunk - 1) / kDtChunk;
+    const bool ring = r > 0 || lbulk;
+    const long total = ring ? (long)nchunks * nt : 0;   // ring items: (chunk, tile) in order
 
-    for (int b0 = 0; b0 < p.B; b0 += kDtChunk) {
-        const int nb = min(kDtChunk, p.B - b0);
+    // ring item i: tile tb + i % nt of chunk i / nt into stage i % 2 (issued by warp 0): the
+    // tile's Wt rows and the chunk's drafter logits over the tile
+    auto issue = [&](long i) {
+        const long v0 = (long)(tb + (int)(i % nt)) * kDtTile;
+        const int nv = (int)min((long)kDtTile, (long)p.V - v0);
+        const int b0 = (int)(i / nt) * kDtChunk, nb = min(kDtChunk, p.B - b0);
+        uint8_t* dst = dt_smem + (size_t)(i & 1) * stage;
+        const unsigned bytes = (unsigned)(r > 0 ? nv * r * 2 : 0) + (unsigned)(lbulk ? nb * nv * (int)sizeof(LT) : 0);
+        if (lane == 0) mbar_arrive_expect_tx(&s_full[i & 1], bytes);
+        __syncwarp();
+        if (r > 0)
+            for (int q = lane; q < nv; q += 32)
+                bulk_g2s(dst + (size_t)q * ldw * sizeof(bf16_t), p.Wt + (size_t)(v0 + q) * r, (unsigned)(r * 2),
+                         &s_full[i & 1]);
+        if (lbulk)
+            for (int q = lane; q < nb; q += 32)
+                bulk_g2s(dst + wbytes + (size_t)q * kDtTile * sizeof(LT),
+                         static_cast<const LT*>(p.logits) + ((size_t)(b0 + q) * p.gamma + (p.j - 1)) * p.V + v0,
+                         (unsigned)(nv * (int)sizeof(LT)), &s_full[i & 1]);
+    };
+    if (threadIdx.x == 0) {
+        mbar_init(&s_full[0], 1);
+        mbar_init(&s_full[1], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    long issued = 0;
+    if (warp == 0)
+        for (; issued < 2 && issued < total; ++issued) issue(issued);   // independent of x_{j-1}
+    pdl_wait_primary();   // x_{j-1}, and the previous position's reads of this workspace
+
+    long i = 0;           // ring items consumed
+    bool abort = false;
+    for (int ch = 0; ch < nchunks && !abort; ++ch) {
+        const int b0 = ch * kDtChunk, nb = min(kDtChunk, p.B - b0);
         // U[x_{j-1}] of the chunk's requests (zero rows for ended requests and padding)
         if (r > 0) {
             const int wpr = r / 8;   // 16-byte words per row
@@ -96,151 +180,457 @@ __global__ void __launch_bounds__(kDtThreads) draft_topk_tiles_kernel(DraftTopkP
                 *reinterpret_cast<uint4*>(s_u + (size_t)rb * ldw + w * 8) = v;
             }
         }
-        // this warp's four requests of the chunk: running statistics and top-k lists
-        unsigned long long mine[4], kth[4], thr[4];
-        float thr_v[4], m2[4], sacc[4];
-        int bad[4], live[4];
-        const LT* lrow[4];
+        // this warp's two requests of the chunk: running statistics
+        float m2[2], sacc[2];
+        int bad[2], live[2];
+        const LT* lrow[2];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int rb = warp * 4 + i, b = b0 + rb;
-            mine[i] = kth[i] = thr[i] = 0ull;
-            thr_v[i] = -INFINITY;
-            m2[i] = -INFINITY;
-            sacc[i] = 0.0f;
-            bad[i] = 0;
-            live[i] = (rb < nb && dt_prev(p, b) >= 0) ? 1 : 0;
-            lrow[i] = static_cast<const LT*>(p.logits) + ((size_t)b * p.gamma + (p.j - 1)) * p.V;
+        for (int h = 0; h < 2; ++h) {
+            const int rb = warp * 2 + h, b = b0 + rb;
+            m2[h] = -INFINITY;
+            sacc[h] = 0.0f;
+            bad[h] = 0;
+            live[h] = (rb < nb && dt_prev(p, b) >= 0) ? 1 : 0;
+            lrow[h] = static_cast<const LT*>(p.logits) + ((size_t)b * p.gamma + (p.j - 1)) * p.V;
         }
         __syncthreads();
 
         for (int t = tb; t < te; ++t) {
             const long v0 = (long)t * kDtTile;
-            if (r > 0) {
-                // the tile's Wt rows (contiguous in memory; zero past V)
-                const int wpr = r / 8;
-                const int nv = (int)min((long)kDtTile, (long)p.V - v0);
-                const uint4* src = reinterpret_cast<const uint4*>(p.Wt + (size_t)v0 * r);
-                for (int q = threadIdx.x; q < kDtTile * wpr; q += blockDim.x) {
-                    const int rv = q / wpr, w = q - rv * wpr;
-                    const uint4 v = rv < nv ? __ldg(src + (size_t)rv * wpr + w) : make_uint4(0u, 0u, 0u, 0u);
-                    *reinterpret_cast<uint4*>(s_w + (size_t)rv * ldw + w * 8) = v;
+            float* sz = s_z + (size_t)(i & 1) * kDtChunk * kDtLdz;
+            const uint8_t* st = dt_smem + (size_t)(i & 1) * stage;
+            bool ok = true;
+            if (ring) ok = mbar_wait(&s_full[i & 1], (unsigned)((i >> 1) & 1), p.status, kWaitLimitNs);
+            // this warp's two requests' logits over the tile (lane l: entries v0 + 4l .. +3),
+            // taken before the stage is released
+            float lv[2][4];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                if (!live[h]) continue;
+                if (lbulk) {
+                    const LT* sl = reinterpret_cast<const LT*>(st + wbytes) + (size_t)(warp * 2 + h) * kDtTile + 4 * lane;
+                    if constexpr (sizeof(LT) == 2) {
+                        const uint2 w = *reinterpret_cast<const uint2*>(sl);
+                        lv[h][0] = __uint_as_float(w.x << 16);
+                        lv[h][1] = __uint_as_float(w.x & 0xffff0000u);
+                        lv[h][2] = __uint_as_float(w.y << 16);
+                        lv[h][3] = __uint_as_float(w.y & 0xffff0000u);
+                    } else {
+                        const float4 w = *reinterpret_cast<const float4*>(sl);
+                        lv[h][0] = w.x; lv[h][1] = w.y; lv[h][2] = w.z; lv[h][3] = w.w;
+                    }
+                } else {
+                    load4<LT>(lrow[h], v0 + 4 * lane, p.V, p.vec, lv[h]);
                 }
-                __syncthreads();
-                // bias block: rows v of this warp's 16, columns the 32 requests
-                wmma::fragment<wmma::matrix_a, 16, 16, 16, __nv_bfloat16, wmma::row_major> fa;
-                wmma::fragment<wmma::matrix_b, 16, 16, 16, __nv_bfloat16, wmma::col_major> fb;
-                wmma::fragment<wmma::accumulator, 16, 16, 16, float> acc0, acc1;
-                wmma::fill_fragment(acc0, 0.0f);
-                wmma::fill_fragment(acc1, 0.0f);
-                const __nv_bfloat16* A = reinterpret_cast<const __nv_bfloat16*>(s_w) + (size_t)(16 * warp) * ldw;
-                const __nv_bfloat16* Bm = reinterpret_cast<const __nv_bfloat16*>(s_u);
-                for (int kk = 0; kk < r; kk += 16) {
-                    wmma::load_matrix_sync(fa, A + kk, ldw);
-                    wmma::load_matrix_sync(fb, Bm + kk, ldw);
-                    wmma::mma_sync(acc0, fa, fb, acc0);
-                    wmma::load_matrix_sync(fb, Bm + (size_t)16 * ldw + kk, ldw);
-                    wmma::mma_sync(acc1, fa, fb, acc1);
-                }
-                // element (v, b) goes to s_z[b * ldz + v]
-                wmma::store_matrix_sync(s_z + 16 * warp, acc0, ldz, wmma::mem_col_major);
-                wmma::store_matrix_sync(s_z + (size_t)16 * ldz + 16 * warp, acc1, ldz, wmma::mem_col_major);
-                __syncthreads();
             }
-            // fold the tile's z values of this warp's requests
+            if (ring) {
+                // bias block: warp w takes vocabulary rows 16 (w % 8) .. and requests 16 (w / 8) ..
+                if (ok && r > 0) {
+                    wmma::fragment<wmma::matrix_a, 16, 16, 16, __nv_bfloat16, wmma::row_major> fa;
+                    wmma::fragment<wmma::matrix_b, 16, 16, 16, __nv_bfloat16, wmma::col_major> fb;
+                    wmma::fragment<wmma::accumulator, 16, 16, 16, float> acc;
+                    wmma::fill_fragment(acc, 0.0f);
+                    const __nv_bfloat16* A = reinterpret_cast<const __nv_bfloat16*>(st) + (size_t)(16 * (warp & 7)) * ldw;
+                    const __nv_bfloat16* Bm = reinterpret_cast<const __nv_bfloat16*>(s_u) + (size_t)(16 * (warp >> 3)) * ldw;
+                    for (int kk = 0; kk < r; kk += 16) {
+                        wmma::load_matrix_sync(fa, A + kk, ldw);
+                        wmma::load_matrix_sync(fb, Bm + kk, ldw);
+                        wmma::mma_sync(acc, fa, fb, acc);
+                    }
+                    // element (v, b) goes to sz[b * kDtLdz + v]
+                    wmma::store_matrix_sync(sz + (size_t)(16 * (warp >> 3)) * kDtLdz + 16 * (warp & 7), acc, kDtLdz,
+                                            wmma::mem_col_major);
+                }
+                if (__syncthreads_or(!ok)) { abort = true; break; }
+                // stage i % 2 is free: refill it with item i + 2
+                if (warp == 0 && issued < total && issued == i + 2) {
+                    fence_proxy_async_smem();
+                    issue(issued);
+                    ++issued;
+                }
+                ++i;
+            }
+            // fold the tile for this warp's two requests: lane l holds entries v0 + 4l .. +3
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                if (!live[i]) continue;   // warp-uniform
-                const int rb = warp * 4 + i;
-                float z[4];
-                bool in[4];
-                float lmax = -INFINITY;
+            for (int h = 0; h < 2; ++h) {
+                if (!live[h]) continue;   // warp-uniform
+                const int rb = warp * 2 + h, b = b0 + rb;
+                const long vb = v0 + 4 * lane;
+                float z[4] = {lv[h][0], lv[h][1], lv[h][2], lv[h][3]};
+                if (r > 0) {
+                    const float4 bz = *reinterpret_cast<const float4*>(sz + (size_t)rb * kDtLdz + 4 * lane);
+                    z[0] += bz.x; z[1] += bz.y; z[2] += bz.z; z[3] += bz.w;
+                }
                 int lbad = 0;
+                float lmax = -INFINITY;
+                unsigned long long kmax = 0ull;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const long v = v0 + 32 * q + lane;
-                    in[q] = v < p.V;
-                    z[q] = in[q] ? load_one(lrow[i] + v) + (r > 0 ? s_z[(size_t)rb * ldz + 32 * q + lane] : 0.0f)
-                                 : -INFINITY;
-                    if (in[q] && bad_logit(z[q])) lbad = 1;
-                    lmax = fmaxf(lmax, z[q]);
-                }
-                bad[i] |= warp_or(lbad);
-                if (bad[i]) continue;
-                // statistics: per-lane running maximum (base 2) and rescaled sum
-                const float lm2 = lmax * kLog2e;
-                if (lm2 > m2[i]) {
-                    sacc[i] *= ex2(m2[i] - lm2);
-                    m2[i] = lm2;
-                }
-                if (m2[i] != -INFINITY) {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) sacc[i] += wexp(z[q], m2[i]);
-                }
-                // first tile of the range: start the threshold at the k-th largest lane maximum
-                if (t == tb) {
-                    float lm = lmax;
-#pragma unroll
-                    for (int kk2 = 2; kk2 <= 32; kk2 <<= 1)
-#pragma unroll
-                        for (int jj = kk2 >> 1; jj > 0; jj >>= 1) {
-                            const float o = __shfl_xor_sync(0xffffffffu, lm, jj);
-                            const bool take_max = ((lane & kk2) == 0) != ((lane & jj) == 0);
-                            lm = take_max ? fmaxf(lm, o) : fminf(lm, o);
-                        }
-                    const float seed = __shfl_sync(0xffffffffu, lm, 32 - k);   // ascending: the k-th largest
-                    thr_v[i] = fmaxf(thr_v[i], seed);
-                }
-                // candidates at or above the threshold, inserted one by one (warp-uniform)
-                const float cut = thr_v[i];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    unsigned hot = __ballot_sync(0xffffffffu, in[q] && z[q] >= cut);
-                    while (hot) {
-                        const int src = __ffs(hot) - 1;
-                        hot &= hot - 1;
-                        const float zv = __shfl_sync(0xffffffffu, z[q], src);
-                        const unsigned long long key = argmax_key(zv, (uint32_t)(v0 + 32 * q + src));
-                        if (key > thr[i]) {
-                            list_insert(mine[i], key, k, kth[i]);
-                            if (kth[i] > thr[i]) {
-                                thr[i] = kth[i];
-                                thr_v[i] = fmaxf(thr_v[i], key_value(kth[i]));
-                            }
-                        }
+                for (int e = 0; e < 4; ++e) {
+                    if (vb + e < p.V) {
+                        if (bad_logit(z[e])) lbad = 1;
+                        lmax = fmaxf(lmax, z[e]);
+                        const unsigned long long kk = argmax_key(z[e], (uint32_t)(vb + e));
+                        kmax = kk > kmax ? kk : kmax;
+                    } else {
+                        z[e] = -INFINITY;
                     }
                 }
+                bad[h] |= warp_or(lbad);
+                if (bad[h]) continue;
+                const float lm2 = lmax * kLog2e;
+                if (lm2 > m2[h]) {
+                    sacc[h] *= ex2(m2[h] - lm2);
+                    m2[h] = lm2;
+                }
+                if (m2[h] != -INFINITY) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sacc[h] += wexp(z[e], m2[h]);
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const unsigned long long k2 = shfl_u64(kmax, lane ^ o);
+                    kmax = k2 > kmax ? k2 : kmax;
+                }
+                if (lane == 0) p.tmax[(size_t)b * p.n_tiles + t] = kmax;
+                if (vb < p.V)
+                    *reinterpret_cast<float4*>(p.zbuf + (size_t)b * p.ldzb + vb) = make_float4(z[0], z[1], z[2], z[3]);
             }
-            if (r > 0) __syncthreads();   // s_w and s_z are rewritten for the next tile
         }
+        if (abort) break;
 
         // one record per (request, CTA)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int rb = warp * 4 + i, b = b0 + rb;
+        for (int h = 0; h < 2; ++h) {
+            const int rb = warp * 2 + h, b = b0 + rb;
             if (rb >= nb) continue;   // warp-uniform
-            const size_t rec = (size_t)b * kDtMaxCtas + c;
-            const float M = warp_max(m2[i]);
-            float s = (m2[i] != -INFINITY && M != -INFINITY) ? sacc[i] * ex2(m2[i] - M) : 0.0f;
+            const size_t rec = (size_t)b * kDtRecMax + c;
+            const float M = warp_max(m2[h]);
+            float s = (m2[h] != -INFINITY && M != -INFINITY) ? sacc[h] * ex2(m2[h] - M) : 0.0f;
             s = warp_sum(s);
             if (lane == 0) {
                 p.stats[rec] = make_float2(M, s);
-                p.bad[rec] = bad[i] ? 1u : 0u;
+                p.bad[rec] = bad[h] ? 1u : 0u;
             }
-            p.keys[rec * kTopkMax + lane] = (live[i] && !bad[i] && lane < k) ? mine[i] : 0ull;
         }
         __syncthreads();   // s_u is rewritten by the next chunk
     }
+    if (abort && threadIdx.x == 0)   // copies still in flight land before the CTA leaves (bounded)
+        for (long q = i; q < issued; ++q) mbar_wait(&s_full[q & 1], (unsigned)((q >> 1) & 1), p.status, kWaitLimitNs);
 }
 
-// One CTA per request: merge the CTA records, filter, draw x_j.
-__global__ void __launch_bounds__(kDtThreads) draft_topk_pick_kernel(DraftTopkParams p) {
+// ----------------------------------------------------------------------------------
+// The tiles kernel on the tcgen05 tensor cores (bf16 weights, r a multiple of 64, logits
+// rows a multiple of 16 bytes).  Per CTA (one per SM), 18 warps:
+//   warp 0      TMA producer: per tile, its Wt rows as r / 64 boxes [128 entries x 64 k]
+//               (128-byte swizzle) into a ring of 16 KB stages, and the chunk's drafter
+//               logits over the tile as one box [32 requests x 128 entries] into a ring
+//               of its own;
+//   warp 1      allocates TMEM and issues tcgen05.mma (M = 128 entries, N = 32 requests,
+//               K = 16, bf16 in, f32 accumulate) from one thread into two 32-column
+//               accumulators, so the next tile's MMAs run while the epilogue reads this
+//               one;
+//   warps 2-17  epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31 (one entry per
+//               thread) and 8 of the 32 request columns; per request it adds the
+//               logits, folds the softmax statistics, writes z, and folds the tile's
+//               largest key into tmax with one atomicMax per warp.
+// The B operand, U[x_{j-1}] of the chunk's 32 requests, is written by the epilogue warps
+// in the same K-major 128-byte-swizzled layout, double-buffered across chunks.  No
+// block-wide barrier runs after the set-up: every wait is a bounded mbarrier wait.
+// ----------------------------------------------------------------------------------
+constexpr int kDkK = 64;                                 // k per 128-byte swizzle block
+constexpr int kDkWBlock = kDtTile * kDkK * 2;            // 16 KB: one Wt box
+constexpr int kDkUBlock = kDtChunk * kDkK * 2;           // 4 KB: one U block
+constexpr int kDkStages = 8;                             // Wt ring
+constexpr int kDkLStages = 3;                            // logits ring
+constexpr int kDkEpi = 16;                               // epilogue warps
+constexpr int kDkThreads = 32 * (2 + kDkEpi);
+constexpr uint32_t kDkIdesc = idesc_bf16_f32(kDtTile, kDtChunk);
+constexpr uint32_t kDkTmemCols = 2 * kDtChunk;           // two accumulators of 32 columns
+
+template <typename LT>
+__global__ void __launch_bounds__(kDkThreads, 1)
+    draft_topk_tc_kernel(const __grid_constant__ DraftTopkParams p, const __grid_constant__ CUtensorMap wmap,
+                         const __grid_constant__ CUtensorMap lmap) {
+    extern __shared__ uint8_t dk_raw[];
+    uint8_t* base = dk_raw + ((1024u - (smem_u32(dk_raw) & 1023u)) & 1023u);
+    constexpr int LBYTES = kDtChunk * kDtTile * (int)sizeof(LT);
+    const int KB = p.r / kDkK;
+    uint8_t* s_w = base;                                          // [kDkStages][16 KB]
+    uint8_t* s_u = s_w + (size_t)kDkStages * kDkWBlock;           // [2][KB][4 KB]
+    uint8_t* s_l = s_u + (size_t)2 * KB * kDkUBlock;              // [kDkLStages][LBYTES]
+    __shared__ __align__(8) uint64_t s_full[kDkStages], s_empty[kDkStages];
+    __shared__ __align__(8) uint64_t s_lfull[kDkLStages], s_lempty[kDkLStages];
+    __shared__ __align__(8) uint64_t s_tfull[2], s_tempty[2], s_ufull[2], s_drain;
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_fail;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c = blockIdx.x;
+    const int tb = (int)(((long)c * p.n_tiles) / p.nC), te = (int)(((long)(c + 1) * p.n_tiles) / p.nC);
+    const int nchunks = (p.B + kDtChunk - 1) / kDtChunk;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kDkStages; ++s) { mbar_init(&s_full[s], 1); mbar_init(&s_empty[s], 1); }
+        for (int s = 0; s < kDkLStages; ++s) { mbar_init(&s_lfull[s], 1); mbar_init(&s_lempty[s], kDkEpi); }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&s_tfull[s], 1);
+            mbar_init(&s_tempty[s], kDkEpi);
+            mbar_init(&s_ufull[s], kDkEpi);
+        }
+        mbar_init(&s_drain, 1);
+        s_fail = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(&s_tmem, kDkTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    uint32_t iw = 0, il = 0;   // producer: Wt stages and logits stages issued
+
+    if (warp == 0) {
+        // neither the weights nor the logits depend on the previous kernel: no wait
+        if (lane == 0) {
+            for (int ch = 0; ch < nchunks && !*(volatile int*)&s_fail; ++ch)
+                for (int t = tb; t < te; ++t) {
+                    bool ok = true;
+                    for (int kb = 0; kb < KB && ok; ++kb) {
+                        const uint32_t s = iw % kDkStages, ph = (iw / kDkStages) & 1u;
+                        ok = mbar_wait(&s_empty[s], ph ^ 1u, p.status, kWaitLimitNs);
+                        if (!ok) break;
+                        mbar_arrive_expect_tx(&s_full[s], kDkWBlock);
+                        tma_load_2d(s_w + (size_t)s * kDkWBlock, &wmap, kb * kDkK, t * kDtTile, &s_full[s]);
+                        ++iw;
+                    }
+                    if (ok) {
+                        const uint32_t s = il % kDkLStages, ph = (il / kDkLStages) & 1u;
+                        ok = mbar_wait(&s_lempty[s], ph ^ 1u, p.status, kWaitLimitNs);
+                        if (ok) {
+                            mbar_arrive_expect_tx(&s_lfull[s], LBYTES);
+                            tma_load_2d(s_l + (size_t)s * LBYTES, &lmap, t * kDtTile, ch * kDtChunk, &s_lfull[s]);
+                            ++il;
+                        }
+                    }
+                    if (!ok) { s_fail = 1; break; }
+                }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            uint32_t im = 0, jt = 0;
+            for (int ch = 0; ch < nchunks && !*(volatile int*)&s_fail; ++ch) {
+                if (!mbar_wait(&s_ufull[ch & 1], (unsigned)((ch >> 1) & 1), p.status, kWaitLimitNs)) { s_fail = 1; break; }
+                tc_fence_after();
+                const uint32_t u0 = smem_u32(s_u + (size_t)(ch & 1) * KB * kDkUBlock);
+                bool ok = true;
+                for (int t = tb; t < te && ok; ++t) {
+                    const uint32_t buf = jt & 1u, jph = (jt >> 1) & 1u;
+                    ok = mbar_wait(&s_tempty[buf], jph ^ 1u, p.status, kWaitLimitNs);
+                    if (!ok) break;
+                    tc_fence_after();
+                    for (int kb = 0; kb < KB; ++kb) {
+                        const uint32_t s = im % kDkStages, ph = (im / kDkStages) & 1u;
+                        ok = mbar_wait(&s_full[s], ph, p.status, kWaitLimitNs);
+                        if (!ok) break;
+                        tc_fence_after();
+                        const uint32_t w0 = smem_u32(s_w + (size_t)s * kDkWBlock);
+#pragma unroll
+                        for (int kk = 0; kk < kDkK / 16; ++kk)
+                            umma_f16(tmem + buf * kDtChunk, sw128_desc(w0 + kk * 32),
+                                     sw128_desc(u0 + kb * kDkUBlock + kk * 32), kDkIdesc, (kb | kk) != 0 ? 1u : 0u);
+                        umma_commit(&s_empty[s]);
+                        ++im;
+                    }
+                    if (!ok) break;
+                    umma_commit(&s_tfull[buf]);
+                    ++jt;
+                }
+                if (!ok) { s_fail = 1; break; }
+            }
+        }
+    } else {
+        const int e = warp - 2;        // epilogue warp 0..15
+        const int q = warp & 3;        // its TMEM lane quadrant: entries 32 q .. +31 of a tile
+        const int g = e >> 2;          // its requests: 8 g .. 8 g + 7 of the chunk
+        const int CPR = p.r / 8;       // 16-byte chunks per U row
+        pdl_wait_primary();            // x_{j-1}; the previous pick's reads of z and tmax
+        uint32_t je = 0, ie = 0;       // tiles and logits stages consumed
+        for (int ch = 0; ch < nchunks; ++ch) {
+            const int b0 = ch * kDtChunk, nb = min(kDtChunk, p.B - b0);
+            // B operand: U[x_{j-1}] of the chunk's requests (zero rows for ended requests and
+            // padding), 128-byte swizzled, K-major, into buffer ch % 2 (its previous user,
+            // chunk ch - 2, finished its MMAs before this warp saw chunk ch - 1's tiles)
+            uint8_t* ub = s_u + (size_t)(ch & 1) * KB * kDkUBlock;
+            for (int idx = (int)threadIdx.x - 64; idx < kDtChunk * CPR; idx += 32 * kDkEpi) {
+                const int n = idx / CPR, kc = idx - n * CPR;
+                const int kb = kc >> 3, cc = kc & 7;
+                uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                if (n < nb) {
+                    const int x = dt_prev(p, b0 + n);
+                    if (x >= 0) v = __ldg(reinterpret_cast<const uint4*>(p.U + (size_t)x * p.r) + kc);
+                }
+                *reinterpret_cast<uint4*>(ub + (size_t)kb * kDkUBlock + n * 128 + ((cc ^ (n & 7)) << 4)) = v;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive1(&s_ufull[ch & 1]);
+
+            // this warp's 8 requests: warp-uniform running maximum (base 2), per-lane sums
+            float m2[8], sl[8];
+            unsigned live = 0u, badm = 0u;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                m2[i] = -INFINITY;
+                sl[i] = 0.0f;
+                const int rb = 8 * g + i;
+                if (rb < nb && dt_prev(p, b0 + rb) >= 0) live |= 1u << i;
+            }
+            bool ok = true;
+            for (int t = tb; t < te; ++t) {
+                const uint32_t buf = je & 1u, jph = (je >> 1) & 1u;
+                ok = __all_sync(0xffffffffu, mbar_wait(&s_tfull[buf], jph, p.status, kWaitLimitNs));
+                if (!ok) break;
+                tc_fence_after();
+                float bias[8];
+                tmem_ld8(tmem + ((uint32_t)(32 * q) << 16) + buf * kDtChunk + 8 * g, bias);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive1(&s_tempty[buf]);
+                ++je;
+                const uint32_t ls = ie % kDkLStages, lph = (ie / kDkLStages) & 1u;
+                ok = __all_sync(0xffffffffu, mbar_wait(&s_lfull[ls], lph, p.status, kWaitLimitNs));
+                if (!ok) break;
+                const LT* lt = reinterpret_cast<const LT*>(s_l + (size_t)ls * LBYTES);
+                const int vl = 32 * q + lane;   // this thread's entry of the tile
+                float z[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) z[i] = load_one_smem(lt + (8 * g + i) * kDtTile + vl) + bias[i];
+                __syncwarp();
+                if (lane == 0) mbar_arrive1(&s_lempty[ls]);
+                ++ie;
+                const long v = (long)t * kDtTile + vl;
+                const bool in = v < p.V;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (!((live >> i) & 1u) || ((badm >> i) & 1u)) continue;   // warp-uniform
+                    const int b = b0 + 8 * g + i;
+                    const float zi = in ? z[i] : -INFINITY;
+                    if (__any_sync(0xffffffffu, in && bad_logit(zi))) { badm |= 1u << i; continue; }
+                    // the quadrant's largest entry and its lowest index: the tile's key
+                    const float m = warp_max(zi);
+                    const unsigned hit = __ballot_sync(0xffffffffu, in && zi == m);
+                    if (lane == 0 && hit)
+                        atomicMax(&p.tmax[(size_t)b * p.n_tiles + t],
+                                  argmax_key(m, (uint32_t)((long)t * kDtTile + 32 * q + __ffs(hit) - 1)));
+                    const float tm2 = m * kLog2e;
+                    if (tm2 > m2[i]) {
+                        sl[i] *= ex2(m2[i] - tm2);
+                        m2[i] = tm2;
+                    }
+                    if (in) {
+                        if (m2[i] != -INFINITY) sl[i] += wexp(zi, m2[i]);
+                        p.zbuf[(size_t)b * p.ldzb + v] = zi;
+                    }
+                }
+            }
+            if (!ok) { s_fail = 1; break; }
+            // one record per (request, CTA, quadrant)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int rb = 8 * g + i;
+                if (rb >= nb) continue;   // warp-uniform
+                const float S = warp_sum(sl[i]);
+                if (lane == 0) {
+                    const size_t rec = (size_t)(b0 + rb) * kDtRecMax + (size_t)c * 4 + q;
+                    p.stats[rec] = make_float2(m2[i], S);
+                    p.bad[rec] = ((badm >> i) & 1u) ? 1u : 0u;
+                }
+            }
+        }
+    }
+
+    // every MMA has completed before TMEM is released, and no copy still writes this
+    // CTA's shared memory when it exits (stages requested and never consumed, after an
+    // error)
+    __syncthreads();
+    if (threadIdx.x == 32) {
+        umma_commit(&s_drain);
+        mbar_wait(&s_drain, 0u, p.status, kWaitLimitNs);
+    }
+    if (threadIdx.x == 0) {
+        const uint32_t nw = iw < (uint32_t)kDkStages ? iw : (uint32_t)kDkStages;
+        for (uint32_t i = iw - nw; i < iw; ++i) mbar_wait(&s_full[i % kDkStages], (i / kDkStages) & 1u, p.status, kWaitLimitNs);
+        const uint32_t nl = il < (uint32_t)kDkLStages ? il : (uint32_t)kDkLStages;
+        for (uint32_t i = il - nl; i < il; ++i) mbar_wait(&s_lfull[i % kDkLStages], (i / kDkLStages) & 1u, p.status, kWaitLimitNs);
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kDkTmemCols);
+    }
+}
+
+// The CTA's k-th largest of the keys held one per thread (k <= 32), by a per-warp sort
+// and a rank across the warps' sorted lists; 0 if the CTA holds fewer than k non-zero keys.
+// Every thread returns the same value.
+__device__ unsigned long long dp_block_kth(unsigned long long key, int k, unsigned long long* s_buf) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    // bitonic sort of the warp's keys, descending
+#pragma unroll
+    for (int kk = 2; kk <= 32; kk <<= 1)
+#pragma unroll
+        for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+            const unsigned long long o = shfl_u64(key, lane ^ jj);
+            const bool take_max = ((lane & kk) == 0) == ((lane & jj) == 0);
+            key = take_max ? (o > key ? o : key) : (o < key ? o : key);
+        }
+    s_buf[threadIdx.x] = key;
+    __syncthreads();
+    __shared__ unsigned long long s_kth;
+    if (threadIdx.x == 0) s_kth = 0ull;
+    __syncthreads();
+    if (lane < k && key != 0ull) {
+        int rank = lane;
+        for (int w = 0; w < kDpWarps; ++w) {
+            if (w == warp) continue;
+            const unsigned long long* a = s_buf + w * 32;
+            int lo = 0, hi = k;
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (a[mid] > key) lo = mid + 1;
+                else hi = mid;
+            }
+            rank += lo;
+        }
+        if (rank == k - 1) s_kth = key;
+    }
+    __syncthreads();
+    const unsigned long long r = s_kth;
+    __syncthreads();   // s_buf and s_kth may be reused
+    return r;
+}
+
+// The n keys of s_c ranked: those among the k largest go to s_top[rank] (s_top zeroed
+// first, so fewer than k keys leave zeros).  Keys are distinct.
+__device__ void dp_top_k(const unsigned long long* s_c, int n, int k, unsigned long long* s_top) {
+    if (threadIdx.x < kTopkMax) s_top[threadIdx.x] = 0ull;
+    __syncthreads();
+    for (int q = threadIdx.x; q < n; q += blockDim.x) {
+        const unsigned long long key = s_c[q];
+        int rank = 0;
+        for (int i = 0; i < n && rank < k; ++i) rank += s_c[i] > key ? 1 : 0;
+        if (rank < k) s_top[rank] = key;
+    }
+    __syncthreads();
+}
+
+// One CTA per request: merge the CTA records, select, filter, draw x_j.
+__global__ void __launch_bounds__(kDpThreads) draft_topk_pick_kernel(DraftTopkParams p) {
     __shared__ unsigned long long s_cand[kDtCandCap];
     __shared__ unsigned long long s_top[kTopkMax];
+    __shared__ unsigned long long s_sort[kDpThreads];
     __shared__ FRow s_row;
-    __shared__ float s_red[kDtWarps];
-    __shared__ unsigned long long s_red64[kDtWarps];
+    __shared__ float s_red[kDpWarps];
     __shared__ int s_cnt, s_bad;
+    pdl_launch_dependents();   // the next position's tiles kernel may start its weight copies
     const int b = blockIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const size_t out = (size_t)b * p.gamma + (p.j - 1);
@@ -254,6 +644,22 @@ __global__ void __launch_bounds__(kDtThreads) draft_topk_pick_kernel(DraftTopkPa
             if (flag) atomicOr(p.status, flag);
         }
     };
+    // this request's tile maxima, held in registers (one wave of loads), then returned to
+    // zero for the next position, whose tensor-core tiles kernel folds them by atomicMax
+    unsigned long long* tm = p.tmax + (size_t)b * p.n_tiles;
+    unsigned long long kr[kDpPer];
+    unsigned long long lmax = 0ull;
+#pragma unroll
+    for (int u = 0; u < kDpPer; ++u) {
+        const int t = (int)threadIdx.x + u * kDpThreads;
+        kr[u] = t < p.n_tiles ? __ldcg(&tm[t]) : 0ull;
+        lmax = kr[u] > lmax ? kr[u] : lmax;
+    }
+#pragma unroll
+    for (int u = 0; u < kDpPer; ++u) {
+        const int t = (int)threadIdx.x + u * kDpThreads;
+        if (t < p.n_tiles) tm[t] = 0ull;
+    }
     const int xp = dt_prev(p, b);
     if (xp < 0) {   // ended earlier (or the anchor is out of range)
         end_request((p.j == 1 && (p.anchor[b] < 0 || p.anchor[b] >= p.V)) ? SPEC_DEV_TOKEN : 0u);
@@ -263,77 +669,71 @@ __global__ void __launch_bounds__(kDtThreads) draft_topk_pick_kernel(DraftTopkPa
     if (threadIdx.x == 0) { s_cnt = 0; s_bad = 0; }
     __syncthreads();
     float M = -INFINITY;
-    unsigned long long T = 0ull;
-    for (int c = threadIdx.x; c < p.nC; c += blockDim.x) {
-        const size_t rec = (size_t)b * kDtMaxCtas + c;
+    for (int c = threadIdx.x; c < p.nrec; c += blockDim.x) {
+        const size_t rec = (size_t)b * kDtRecMax + c;
         const float2 st = __ldcg(&p.stats[rec]);
         if (__ldcg(&p.bad[rec]) || isnan(st.x)) s_bad = 1;
         M = fmaxf(M, st.x);
-        const unsigned long long kk = __ldcg(&p.keys[rec * kTopkMax + (k - 1)]);
-        T = kk > T ? kk : T;
     }
     M = warp_max(M);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const unsigned long long t2 = shfl_u64(T, lane ^ o);
-        T = t2 > T ? t2 : T;
-    }
-    if (lane == 0) { s_red[warp] = M; s_red64[warp] = T; }
+    if (lane == 0) s_red[warp] = M;
     __syncthreads();
     M = -INFINITY;
-    T = 0ull;
-    for (int w = 0; w < kDtWarps; ++w) {
-        M = fmaxf(M, s_red[w]);
-        T = s_red64[w] > T ? s_red64[w] : T;
-    }
+    for (int w = 0; w < kDpWarps; ++w) M = fmaxf(M, s_red[w]);
     __syncthreads();
     if (s_bad || M == -INFINITY) {
         end_request(SPEC_DEV_NONFINITE);
         return;
     }
     float S = 0.0f;
-    for (int c = threadIdx.x; c < p.nC; c += blockDim.x) {
-        const float2 st = __ldcg(&p.stats[(size_t)b * kDtMaxCtas + c]);
+    for (int c = threadIdx.x; c < p.nrec; c += blockDim.x) {
+        const float2 st = __ldcg(&p.stats[(size_t)b * kDtRecMax + c]);
         if (st.x != -INFINITY) S += st.y * ex2(st.x - M);
     }
     S = warp_sum(S);
     if (lane == 0) s_red[warp] = S;
-    // candidates: keys at or above the largest CTA k-th key (every CTA list is sorted)
-    for (int c = threadIdx.x; c < p.nC; c += blockDim.x) {
-        const unsigned long long* kl = p.keys + ((size_t)b * kDtMaxCtas + c) * kTopkMax;
-        for (int i = 0; i < k; ++i) {
-            const unsigned long long kv = __ldcg(&kl[i]);
-            if (kv == 0ull || kv < T) break;
-            const int pos = atomicAdd(&s_cnt, 1);
-            if (pos < kDtCandCap) s_cand[pos] = kv;
+    __syncthreads();
+    S = 0.0f;
+    for (int w = 0; w < kDpWarps; ++w) S += s_red[w];
+
+    // 1. a bound at or below the k-th largest tile maximum: the k-th largest of the
+    //    threads' maxima (distinct tile maxima)
+    const unsigned long long t_lo = dp_block_kth(lmax, k, s_sort);
+    // 2. the tile maxima at or above it (at most n_tiles <= kDtCandCap), and the k largest
+#pragma unroll
+    for (int u = 0; u < kDpPer; ++u)
+        if (kr[u] != 0ull && kr[u] >= t_lo) s_cand[atomicAdd(&s_cnt, 1)] = kr[u];
+    __syncthreads();
+    dp_top_k(s_cand, s_cnt, k, s_top);
+    // 3. the entries of those tiles at or above the smallest of them, T
+    unsigned long long T = 0ull;
+    int ntop = 0;
+    for (int q = 0; q < k; ++q)
+        if (s_top[q] != 0ull) { T = s_top[q]; ntop = q + 1; }
+    if (ntop < k) T = 0ull;   // fewer than k tiles: every entry of them
+    __syncthreads();
+    if (threadIdx.x == 0) s_cnt = 0;
+    __syncthreads();
+    const float* zr = p.zbuf + (size_t)b * p.ldzb;
+    float zv[kDpPer];
+#pragma unroll
+    for (int u = 0; u < kDpPer; ++u) {   // one wave of loads
+        const int q = (int)threadIdx.x + u * kDpThreads;
+        const long v = q < ntop * kDtTile ? (long)(key_index(s_top[q / kDtTile]) / kDtTile) * kDtTile + (q % kDtTile) : p.V;
+        zv[u] = v < p.V ? __ldcg(&zr[v]) : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < kDpPer; ++u) {
+        const int q = (int)threadIdx.x + u * kDpThreads;
+        const long v = q < ntop * kDtTile ? (long)(key_index(s_top[q / kDtTile]) / kDtTile) * kDtTile + (q % kDtTile) : p.V;
+        if (v < p.V) {
+            const unsigned long long kv = argmax_key(zv[u], (uint32_t)v);
+            if (kv >= T) s_cand[atomicAdd(&s_cnt, 1)] = kv;
         }
     }
     __syncthreads();
-    S = 0.0f;
-    for (int w = 0; w < kDtWarps; ++w) S += s_red[w];
-    const int cnt = min(s_cnt, kDtCandCap);
+    dp_top_k(s_cand, s_cnt, k, s_top);
     if (warp != 0) return;
-    // the k largest candidates (k rounds of a warp maximum), descending
-    unsigned long long prev_best = ~0ull;
-    for (int rr = 0; rr < k; ++rr) {
-        unsigned long long best = 0ull;
-        for (int i = lane; i < cnt; i += 32) {
-            const unsigned long long kv = s_cand[i];
-            if (kv < prev_best && kv > best) best = kv;
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const unsigned long long t2 = shfl_u64(best, lane ^ o);
-            best = t2 > best ? t2 : best;
-        }
-        if (lane == 0) s_top[rr] = best;
-        prev_best = best;
-        if (best == 0ull) {
-            for (int q = rr + 1 + lane; q < k; q += 32) s_top[q] = 0ull;
-            break;
-        }
-    }
-    __syncwarp();
     filter_row(s_top, k, p.top_p, s_row);
     __syncwarp();
     if (s_row.n == 0) {   // no finite entry
@@ -358,13 +758,79 @@ __global__ void __launch_bounds__(kDtThreads) draft_topk_pick_kernel(DraftTopkPa
 // ----------------------------------------------------------------------------------
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-size_t draft_topk_workspace_bytes(int B) {
-    const size_t n = (size_t)B * kDtMaxCtas;
+static size_t dt_ldzb(int V) { return ((size_t)V + 3) / 4 * 4; }
+
+// The tensor-core tiles kernel and the picks, position by position.  The weights' map is
+// [V rows][r] (boxes of 128 rows x 64 k, 128-byte swizzle); the logits' map for position
+// j is [B rows][V] with a row stride of gamma * V entries (boxes of 32 rows x 128
+// entries), so one copy brings a chunk's logits over a tile.
+template <typename LT>
+static cudaError_t launch_topk_tc(DraftTopkParams p, const DraftTopkLaunch& a, cudaStream_t stream) {
+    const int KB = p.r / kDkK;
+    const size_t lbytes = (size_t)kDtChunk * kDtTile * sizeof(LT);
+    const size_t smem = 1024 + (size_t)kDkStages * kDkWBlock + (size_t)2 * KB * kDkUBlock + (size_t)kDkLStages * lbytes;
+    auto kern = draft_topk_tc_kernel<LT>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int grid = device_sm_count();   // one CTA per SM (TMEM and shared memory sized for it)
+    if (grid > kDtMaxCtas) grid = kDtMaxCtas;
+    if (grid > p.n_tiles) grid = p.n_tiles;
+    p.nC = grid;
+    p.nrec = 4 * grid;
+
+    CUtensorMap wmap;
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)p.r, (cuuint64_t)p.V};
+        const cuuint64_t strides[1] = {(cuuint64_t)p.r * 2};
+        const cuuint32_t box[2] = {(cuuint32_t)kDkK, (cuuint32_t)kDtTile};
+        const cuuint32_t estr[2] = {1, 1};
+        if (encode_tiled()(&wmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<bf16_t*>(p.Wt), dims, strides, box,
+                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    for (int j = 1; j <= a.gamma; ++j) {
+        p.j = j;
+        CUtensorMap lmap;
+        const cuuint64_t dims[2] = {(cuuint64_t)p.V, (cuuint64_t)p.B};
+        const cuuint64_t strides[1] = {(cuuint64_t)p.gamma * p.V * sizeof(LT)};
+        const cuuint32_t box[2] = {(cuuint32_t)kDtTile, (cuuint32_t)kDtChunk};
+        const cuuint32_t estr[2] = {1, 1};
+        void* lbase = const_cast<LT*>(static_cast<const LT*>(p.logits) + (size_t)(j - 1) * p.V);
+        if (encode_tiled()(&lmap, sizeof(LT) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                           lbase, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+        // the tiles kernel as a programmatic dependent of the previous pick (its copies
+        // and MMAs need nothing from it; its epilogue waits)
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3(kDkThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kern, p, wmap, lmap);
+        if (e != cudaSuccess) return e;
+        draft_topk_pick_kernel<<<a.B, kDpThreads, 0, stream>>>(p);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+size_t draft_topk_workspace_bytes(int B, int V) {
+    const size_t n = (size_t)B * kDtRecMax;
+    const size_t n_tiles = ((size_t)V + kDtTile - 1) / kDtTile;
     size_t off = kWsHeaderBytes;
-    off = align_up(off + sizeof(int32_t) * (size_t)B, 256);
-    off = align_up(off + sizeof(float2) * n, 256);
-    off = align_up(off + sizeof(unsigned) * n, 256);
-    off = align_up(off + sizeof(unsigned long long) * n * kTopkMax, 256);
+    off = align_up(off + sizeof(int32_t) * (size_t)B, 256);                    // xprev
+    off = align_up(off + sizeof(float2) * n, 256);                             // stats
+    off = align_up(off + sizeof(unsigned) * n, 256);                           // bad
+    off = align_up(off + sizeof(unsigned long long) * (size_t)B * n_tiles, 256);   // tmax
+    off = align_up(off + sizeof(float) * (size_t)B * dt_ldzb(V), 256);        // zbuf
     return off;
 }
 
@@ -386,9 +852,14 @@ cudaError_t draft_topk_launch(const DraftTopkLaunch& a, void* ws, cudaStream_t s
     p.tokens_out = a.tokens_out;
     p.conf_out = a.conf_out;
     p.qtok_out = a.qtok_out;
+    p.n_tiles = (a.V + kDtTile - 1) / kDtTile;
+    p.ldzb = (long)dt_ldzb(a.V);
+    p.vec = a.V % 4 == 0 && (reinterpret_cast<uintptr_t>(a.logits) & 15u) == 0;
+    const size_t esize = a.ldt == SPEC_BF16 ? 2 : 4;
+    p.lbulk = ((size_t)a.V * esize) % 16 == 0 && (reinterpret_cast<uintptr_t>(a.logits) & 15u) == 0;
     char* w = static_cast<char*>(ws);
     p.status = &reinterpret_cast<WsHeader*>(w)->status;
-    const size_t n = (size_t)a.B * kDtMaxCtas;
+    const size_t n = (size_t)a.B * kDtRecMax;
     size_t off = kWsHeaderBytes;
     p.xprev = reinterpret_cast<int32_t*>(w + off);
     off = align_up(off + sizeof(int32_t) * (size_t)a.B, 256);
@@ -396,26 +867,44 @@ cudaError_t draft_topk_launch(const DraftTopkLaunch& a, void* ws, cudaStream_t s
     off = align_up(off + sizeof(float2) * n, 256);
     p.bad = reinterpret_cast<unsigned*>(w + off);
     off = align_up(off + sizeof(unsigned) * n, 256);
-    p.keys = reinterpret_cast<unsigned long long*>(w + off);
+    p.tmax = reinterpret_cast<unsigned long long*>(w + off);
+    off = align_up(off + sizeof(unsigned long long) * (size_t)a.B * p.n_tiles, 256);
+    p.zbuf = reinterpret_cast<float*>(w + off);
 
-    p.n_tiles = (a.V + kDtTile - 1) / kDtTile;
-    int nC = 2 * device_sm_count();
-    if (nC > kDtMaxCtas) nC = kDtMaxCtas;
-    if (nC > p.n_tiles) nC = p.n_tiles;
-    p.nC = nC;
+    if (a.r >= kDkK && a.r % kDkK == 0 && a.r <= 256 && p.lbulk && encode_tiled() != nullptr)
+        return a.ldt == SPEC_BF16 ? launch_topk_tc<bf16_t>(p, a, stream) : launch_topk_tc<float>(p, a, stream);
+
     const int ldw = a.r + 8;
-    const size_t smem = a.r > 0 ? (size_t)(kDtTile + kDtChunk) * ldw * sizeof(bf16_t) +
-                                      (size_t)kDtChunk * (kDtTile + 4) * sizeof(float)
-                                : 0;
+    const size_t stage = (a.r > 0 ? (size_t)kDtTile * ldw * sizeof(bf16_t) : 0) +
+                         (p.lbulk ? (size_t)kDtChunk * kDtTile * esize : 0);
+    const size_t smem = 2 * stage + (size_t)kDtChunk * ldw * sizeof(bf16_t) + (size_t)2 * kDtChunk * kDtLdz * sizeof(float);
     void (*kt)(DraftTopkParams) = a.ldt == SPEC_BF16 ? draft_topk_tiles_kernel<bf16_t> : draft_topk_tiles_kernel<float>;
     cudaError_t e = cudaFuncSetAttribute(kt, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kt, kDtThreads, smem) != cudaSuccess || occ < 1) occ = 1;
+    int nC = device_sm_count() * occ;
+    if (nC > kDtMaxCtas) nC = kDtMaxCtas;
+    if (nC > p.n_tiles) nC = p.n_tiles;
+    p.nC = nC;
+    p.nrec = nC;
     for (int j = 1; j <= a.gamma; ++j) {
         p.j = j;
-        kt<<<nC, kDtThreads, smem, stream>>>(p);
-        e = cudaGetLastError();
+        // the tiles kernel as a programmatic dependent of the previous pick (its weight
+        // copies are issued before it waits)
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)nC);
+        cfg.blockDim = dim3(kDtThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kt, p);
         if (e != cudaSuccess) return e;
-        draft_topk_pick_kernel<<<a.B, kDtThreads, 0, stream>>>(p);
+        draft_topk_pick_kernel<<<a.B, kDpThreads, 0, stream>>>(p);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

@@ -158,7 +158,7 @@ struct DraftTopkLaunch {
     float* conf_out;           // [B, gamma]
     float* qtok_out;           // [B, gamma] (nullable)
 };
-size_t draft_topk_workspace_bytes(int B);
+size_t draft_topk_workspace_bytes(int B, int V);
 cudaError_t draft_topk_launch(const DraftTopkLaunch& a, void* ws, cudaStream_t stream);
 
 struct BranchPlanParams {
