@@ -51,6 +51,7 @@ constexpr int kDtRecMax = 4 * kDtMaxCtas;     // statistics records per request 
 constexpr int kDtCandCap = 4096;              // candidates of the pick kernel
 constexpr int kDtLdz = kDtTile + 4;           // bias block row (floats)
 constexpr int kDpPer = kDtCandCap / kDpThreads;   // candidates per pick thread
+constexpr int kDpRecPer = kDtRecMax / kDpThreads;  // statistics records per pick thread
 static_assert(SPEC_MAX_V_DRAFT_TOPK / kDtTile <= kDtCandCap, "every tile maximum fits the candidate buffer");
 static_assert(SPEC_MAX_TOP_K * kDtTile <= kDtCandCap, "the k best tiles' entries fit the candidate buffer");
 
@@ -340,7 +341,9 @@ __global__ void __launch_bounds__(kDtThreads, 1) draft_topk_tiles_kernel(DraftTo
 constexpr int kDkK = 64;                                 // k per 128-byte swizzle block
 constexpr int kDkWBlock = kDtTile * kDkK * 2;            // 16 KB: one Wt box
 constexpr int kDkUBlock = kDtChunk * kDkK * 2;           // 4 KB: one U block
-constexpr int kDkStages = 8;                             // Wt ring
+// Wt ring stages of 16 KB (two tiles at r = 256; 9 or 10 stages streamed slower: the
+// extra copies only queue behind the first ones)
+template <typename LT> struct DkStages { static constexpr int N = 8; };
 constexpr int kDkLStages = 3;                            // logits ring
 constexpr int kDkEpi = 16;                               // epilogue warps
 constexpr int kDkThreads = 32 * (2 + kDkEpi);
@@ -353,6 +356,7 @@ __global__ void __launch_bounds__(kDkThreads, 1)
                          const __grid_constant__ CUtensorMap lmap) {
     extern __shared__ uint8_t dk_raw[];
     uint8_t* base = dk_raw + ((1024u - (smem_u32(dk_raw) & 1023u)) & 1023u);
+    constexpr int kDkStages = DkStages<LT>::N;
     constexpr int LBYTES = kDtChunk * kDtTile * (int)sizeof(LT);
     const int KB = p.r / kDkK;
     uint8_t* s_w = base;                                          // [kDkStages][16 KB]
@@ -626,10 +630,11 @@ __device__ void dp_top_k(const unsigned long long* s_c, int n, int k, unsigned l
 __global__ void __launch_bounds__(kDpThreads) draft_topk_pick_kernel(DraftTopkParams p) {
     __shared__ unsigned long long s_cand[kDtCandCap];
     __shared__ unsigned long long s_top[kTopkMax];
-    __shared__ unsigned long long s_sort[kDpThreads];
     __shared__ FRow s_row;
     __shared__ float s_red[kDpWarps];
-    __shared__ int s_cnt, s_bad;
+    __shared__ int s_badw[kDpWarps];
+    __shared__ unsigned long long s_sort[kDpThreads];
+    __shared__ int s_cnt;
     pdl_launch_dependents();   // the next position's tiles kernel may start its weight copies
     const int b = blockIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -644,8 +649,9 @@ __global__ void __launch_bounds__(kDpThreads) draft_topk_pick_kernel(DraftTopkPa
             if (flag) atomicOr(p.status, flag);
         }
     };
-    // this request's tile maxima, held in registers (one wave of loads), then returned to
-    // zero for the next position, whose tensor-core tiles kernel folds them by atomicMax
+    // one wave of loads: this request's tile maxima (returned to zero for the next
+    // position, whose tensor-core tiles kernel folds them by atomicMax), its statistics
+    // records and its previous token, all held in registers
     unsigned long long* tm = p.tmax + (size_t)b * p.n_tiles;
     unsigned long long kr[kDpPer];
     unsigned long long lmax = 0ull;
@@ -653,49 +659,59 @@ __global__ void __launch_bounds__(kDpThreads) draft_topk_pick_kernel(DraftTopkPa
     for (int u = 0; u < kDpPer; ++u) {
         const int t = (int)threadIdx.x + u * kDpThreads;
         kr[u] = t < p.n_tiles ? __ldcg(&tm[t]) : 0ull;
-        lmax = kr[u] > lmax ? kr[u] : lmax;
     }
+    float2 st[kDpRecPer];
+    unsigned bd = 0u;
+#pragma unroll
+    for (int u = 0; u < kDpRecPer; ++u) {
+        const int c = (int)threadIdx.x + u * kDpThreads;
+        const size_t rec = (size_t)b * kDtRecMax + c;
+        st[u] = c < p.nrec ? __ldcg(&p.stats[rec]) : make_float2(-INFINITY, 0.0f);
+        bd |= c < p.nrec ? __ldcg(&p.bad[rec]) : 0u;
+    }
+    const int xp = dt_prev(p, b);
+    // the draw's uniform depends on no data: warp 0 takes it while the loads are in flight
+    const float u_draw = warp == 0 ? philox_uniform(p.seeds[b], (uint64_t)b, (uint64_t)p.j, 0) : 0.0f;
 #pragma unroll
     for (int u = 0; u < kDpPer; ++u) {
         const int t = (int)threadIdx.x + u * kDpThreads;
+        lmax = kr[u] > lmax ? kr[u] : lmax;
         if (t < p.n_tiles) tm[t] = 0ull;
     }
-    const int xp = dt_prev(p, b);
     if (xp < 0) {   // ended earlier (or the anchor is out of range)
         end_request((p.j == 1 && (p.anchor[b] < 0 || p.anchor[b] >= p.V)) ? SPEC_DEV_TOKEN : 0u);
         return;
     }
     // statistics: the maximum (NaN or a bad record ends the row), then the rescaled sums
-    if (threadIdx.x == 0) { s_cnt = 0; s_bad = 0; }
-    __syncthreads();
     float M = -INFINITY;
-    for (int c = threadIdx.x; c < p.nrec; c += blockDim.x) {
-        const size_t rec = (size_t)b * kDtRecMax + c;
-        const float2 st = __ldcg(&p.stats[rec]);
-        if (__ldcg(&p.bad[rec]) || isnan(st.x)) s_bad = 1;
-        M = fmaxf(M, st.x);
+    int lbad = bd != 0u ? 1 : 0;
+#pragma unroll
+    for (int u = 0; u < kDpRecPer; ++u) {
+        if (isnan(st[u].x)) lbad = 1;
+        M = fmaxf(M, st[u].x);
     }
     M = warp_max(M);
-    if (lane == 0) s_red[warp] = M;
+    lbad = warp_or(lbad);
+    if (lane == 0) { s_red[warp] = M; s_badw[warp] = lbad; }
+    if (threadIdx.x == 0) s_cnt = 0;
     __syncthreads();
     M = -INFINITY;
-    for (int w = 0; w < kDpWarps; ++w) M = fmaxf(M, s_red[w]);
-    __syncthreads();
-    if (s_bad || M == -INFINITY) {
+    int bad_row = 0;
+    for (int w = 0; w < kDpWarps; ++w) {
+        M = fmaxf(M, s_red[w]);
+        bad_row |= s_badw[w];
+    }
+    if (bad_row || M == -INFINITY) {
         end_request(SPEC_DEV_NONFINITE);
         return;
     }
     float S = 0.0f;
-    for (int c = threadIdx.x; c < p.nrec; c += blockDim.x) {
-        const float2 st = __ldcg(&p.stats[(size_t)b * kDtRecMax + c]);
-        if (st.x != -INFINITY) S += st.y * ex2(st.x - M);
-    }
+#pragma unroll
+    for (int u = 0; u < kDpRecPer; ++u)
+        if (st[u].x != -INFINITY) S += st[u].y * ex2(st[u].x - M);
     S = warp_sum(S);
+    __syncthreads();   // s_red is rewritten
     if (lane == 0) s_red[warp] = S;
-    __syncthreads();
-    S = 0.0f;
-    for (int w = 0; w < kDpWarps; ++w) S += s_red[w];
-
     // 1. a bound at or below the k-th largest tile maximum: the k-th largest of the
     //    threads' maxima (distinct tile maxima)
     const unsigned long long t_lo = dp_block_kth(lmax, k, s_sort);
@@ -740,16 +756,20 @@ __global__ void __launch_bounds__(kDpThreads) draft_topk_pick_kernel(DraftTopkPa
         end_request(SPEC_DEV_NONFINITE);
         return;
     }
-    const float u = philox_uniform(p.seeds[b], (uint64_t)b, (uint64_t)p.j, 0);
+    float Z = 0.0f;   // the unfiltered row's normaliser (base-2 sums against M)
+    for (int w = 0; w < kDpWarps; ++w) Z += s_red[w];
+    const float u = u_draw;
     int near = 0;
     const int il = lane < s_row.n ? s_row.idx[lane] : -1;
     const int x = warp_draw(il, lane < s_row.n ? s_row.pf[lane] : 0.0f, u, near);
     const float qx = frow_prob(s_row, x);
     if (lane == 0) {
         p.tokens_out[out] = x;
-        p.conf_out[out] = 1.0f / S;
+        p.conf_out[out] = 1.0f / Z;
         if (p.qtok_out) p.qtok_out[out] = qx;
         p.xprev[b] = x;
+        // the next position gathers U[x_j]: bring the row into L2 now
+        if (p.r > 0 && p.j < p.gamma && x >= 0) bulk_prefetch_l2(p.U + (size_t)x * p.r, (unsigned)(p.r * 2));
     }
 }
 
@@ -768,7 +788,7 @@ template <typename LT>
 static cudaError_t launch_topk_tc(DraftTopkParams p, const DraftTopkLaunch& a, cudaStream_t stream) {
     const int KB = p.r / kDkK;
     const size_t lbytes = (size_t)kDtChunk * kDtTile * sizeof(LT);
-    const size_t smem = 1024 + (size_t)kDkStages * kDkWBlock + (size_t)2 * KB * kDkUBlock + (size_t)kDkLStages * lbytes;
+    const size_t smem = 1024 + (size_t)DkStages<LT>::N * kDkWBlock + (size_t)2 * KB * kDkUBlock + (size_t)kDkLStages * lbytes;
     auto kern = draft_topk_tc_kernel<LT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
