@@ -155,3 +155,24 @@ def test_batched_draft_invalid_requests_across_slices(spec):
         assert flags & vsd.DEV_NONFINITE and flags & vsd.DEV_TOKEN
         rows = [0, 3, 35, 36, 38, 39]
         assert _draft_check(out, L, anchor, U, Wt, T, seeds, rows) >= 4 * G - 2 * G
+
+
+@pytest.mark.parametrize("T", [0, 1])
+def test_batched_draft_position_path_two_slices(spec, T):
+    """1100 requests x 3 = 3300 rows with bf16 logits and weights, r = 64: the
+    position-by-position path in two slices of requests (1024 + 76); sampled requests on
+    both sides of the cut against the oracle, and the Philox request index of the second
+    slice is the request's index in the whole batch."""
+    B, G, V, r = 1100, 3, 1000, 64
+    L, _ = synth.target_and_draft(B, G - 1, V, "zipf", 0.0, torch.bfloat16, seed=24)
+    L = L[:, :G].contiguous()
+    U, Wt = synth.markov_weights(V, r, torch.bfloat16, seed=24, scale=0.5)
+    anchor = synth.anchors(B, V, seed=24)
+    seeds = synth.seeds_for(B, 9)
+    dev = torch.device("cuda")
+    out = vsd.draft_block(L.to(dev), anchor.to(dev), U.to(dev), Wt.to(dev), T, seeds.to(dev))
+    torch.cuda.synchronize()
+    assert vsd.device_status(out["ws"]) == 0
+    assert int(out["passes"].item()) == G   # the weights are read once per position
+    rows = [0, 127, 128, 511, 1023, 1024, 1025, 1099]
+    assert _draft_check(out, L, anchor, U, Wt, T, seeds, rows) >= len(rows) * G - 2 * G

@@ -57,7 +57,12 @@ size_t spec_workspace_bytes(spec_op op, int B, int gamma, int V, int r) {
         case SPEC_OP_DRAFT:
             // one launch's slice of requests at most (see spec_draft_block)
             if (r < 0 || r > SPEC_MAX_RANK || (long)B * gamma > SPEC_MAX_DRAFT_ROWS) return 0;
-            return draft_workspace_bytes(B < kDraftMaxRows / gamma ? B : kDraftMaxRows / gamma, gamma, V, r);
+            {
+                const size_t fp = draft_workspace_bytes(B < kDraftMaxRows / gamma ? B : kDraftMaxRows / gamma, gamma, V, r);
+                // a batch of more than 256 rows may take the position-by-position path
+                const size_t pos = (long)B * gamma > 256 ? draft_pos_workspace_bytes(B, V, r) : 0;
+                return fp > pos ? fp : pos;
+            }
         case SPEC_OP_VERIFY:
             if (B > 65535) return 0;
             return verify_workspace_bytes(B, gamma, V);
@@ -155,8 +160,15 @@ spec_status spec_draft_block(const void* draft_logits, spec_dtype logits_dtype, 
     p.passes_out = passes_out;
     p.vec_l = ((size_t)V * dtype_size(logits_dtype)) % 16 == 0;
     p.vec_w = r > 0 && ((size_t)r * dtype_size(w_dtype)) % 16 == 0;
-    // a batch larger than one launch runs as consecutive launches over slices of
-    // requests, each with the workspace of one slice
+    // a batch of more than 256 rows with bf16 logits and weights and r a multiple of 64
+    // walks the chain position by position, reading each row and the weights once per
+    // position
+    if (draft_pos_supported(p)) {
+        if (!workspace || workspace_bytes < draft_pos_workspace_bytes(B, V, r)) return SPEC_ERR_WORKSPACE;
+        return cuda_status(draft_pos_launch(p, workspace, (cudaStream_t)stream));
+    }
+    // otherwise a batch larger than one launch runs as consecutive launches over slices
+    // of requests, each with the workspace of one slice
     const int per = draft_requests_per_launch(p);
     const size_t need = draft_workspace_bytes(per, gamma, V, r);
     if (!workspace || workspace_bytes < need) return SPEC_ERR_WORKSPACE;

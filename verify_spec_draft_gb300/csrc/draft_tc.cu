@@ -44,78 +44,6 @@ __device__ __forceinline__ void umma_bf16(uint32_t d, uint64_t a, uint64_t b, ui
     umma_f16(d, a, b, kTcIdesc, accumulate);
 }
 
-__device__ __forceinline__ float fmax_nan_f(float a, float b) {
-    float r;
-    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
-    return r;
-}
-
-// Drafter logits of 32 consecutive entries (v0 a multiple of 32, rows 16-byte aligned,
-// V a multiple of the vector width): LW 16-byte words, -inf past V.
-template <typename LT> struct LWords { static constexpr int N = 32 * (int)sizeof(LT) / 16; };
-
-template <typename LT>
-__device__ __forceinline__ void load_l32(const LT* row, long v0, long V, uint4 (&w)[LWords<LT>::N]) {
-    constexpr int N = LWords<LT>::N, EPV = 32 / N;
-    const uint32_t ninf = sizeof(LT) == 2 ? 0xff80ff80u : 0xff800000u;
-#pragma unroll
-    for (int i = 0; i < N; ++i) {
-        const long v = v0 + EPV * i;
-        w[i] = (v + EPV <= V) ? __ldg(reinterpret_cast<const uint4*>(row + v)) : make_uint4(ninf, ninf, ninf, ninf);
-    }
-}
-// z[e] += logit e, in place
-template <typename LT>
-__device__ __forceinline__ void add_l32(const uint4 (&w)[LWords<LT>::N], float (&z)[32]) {
-    if (sizeof(LT) == 2) {
-#pragma unroll
-        for (int i = 0; i < LWords<LT>::N; ++i) {
-            const uint32_t a[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                z[(8 * i + 2 * k) & 31] += __uint_as_float(a[k] << 16);
-                z[(8 * i + 2 * k + 1) & 31] += __uint_as_float(a[k] & 0xffff0000u);
-            }
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < LWords<LT>::N; ++i) {
-            z[(4 * i) & 31] += __uint_as_float(w[i].x);
-            z[(4 * i + 1) & 31] += __uint_as_float(w[i].y);
-            z[(4 * i + 2) & 31] += __uint_as_float(w[i].z);
-            z[(4 * i + 3) & 31] += __uint_as_float(w[i].w);
-        }
-    }
-}
-
-// Record of 32 consecutive entries of one row held by one thread.  The lowest index
-// of the maximum is needed only when this chunk raises the running maximum `run_mx`
-// (entries are visited in increasing order, so on a tie the earlier index stands);
-// `want_idx` is false when no argmax is used (T=1).
-__device__ __forceinline__ RowAcc record32(const float (&z)[32], int v0, float run_mx, bool want_idx) {
-    float m = z[0];
-#pragma unroll
-    for (int e = 1; e < 32; ++e) m = fmax_nan_f(m, z[e]);
-    RowAcc r;
-    r.bad = (isnan(m) || m == INFINITY) ? 1 : 0;
-    r.mx = r.bad ? -INFINITY : m;
-    r.s = 0.0f;
-    r.idx = 0x7fffffff;
-    if (!r.bad && m != -INFINITY) {
-        const float m2 = m * kLog2e;
-        float s0 = 0.0f, s1 = 0.0f;
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) { s0 += wexp(z[e], m2); s1 += wexp(z[e + 1], m2); }
-        r.s = s0 + s1;
-        if (want_idx && m > run_mx) {
-#pragma unroll
-            for (int e = 31; e >= 0; --e)
-                if (z[e] == m) r.idx = v0 + e;
-        }
-    }
-    return r;
-}
-
 // Rows are spread over the TMEM lane quadrants so that every epilogue group has rows
 // when there are few: row n sits at MMA row 128*mt + 32*q + l with (mt, q) = the
 // quadrant slot n mod (4*MT) and lane l = n / (4*MT).

@@ -86,6 +86,11 @@ cudaError_t draft_launch(const DraftParams& p, cudaStream_t stream);
 // slices of that many requests (workspace bound for one slice)
 int draft_requests_per_launch(const DraftParams& p);
 cudaError_t draft_launch_batched(const DraftParams& p, cudaStream_t stream);
+// a batch larger than one fixed-point launch, walked position by position on the
+// tensor cores (bf16 logits and weights, r a multiple of 64): its own workspace layout
+bool draft_pos_supported(const DraftParams& p);
+size_t draft_pos_workspace_bytes(int B, int V, int r);
+cudaError_t draft_pos_launch(const DraftParams& p, void* ws, cudaStream_t stream);
 constexpr int kDraftMaxRows = 4096;   // rows (requests x gamma) of one launch
 
 // spec_draft_verify: [draft workspace | verify workspace]

@@ -15,6 +15,10 @@ kernel, on inputs larger than L2 (129 MB) but only a few hundred MB on the devic
   tree_verify spec_tree_verify on 32 trees x 64 nodes, V=248320 (2080 rows, 1.03 GB)
   draft_topk spec_draft_block_topk, B=32, gamma=7, V=248320, r=256, top_k 20, top_p 0.95
              (365 MB: logits, U, Wt)
+  draft_pos  spec_draft_block at T=1 on 512 requests x gamma=2, V=248320, r=256: the
+             position-by-position path for batches over 256 rows (509 MB of logits)
+  sampler    spec_draft_block at T=1 on the anchor-branch workload, 1024 branches x W=7
+             (3.56 GB of logits): for launch lists only (one metric, one pass)
 """
 
 import argparse
@@ -23,7 +27,8 @@ import torch
 
 from . import draft_block, draft_block_topk, e2etv, load, synth, tree_verify, verify, verify_topk
 
-CASES = ("draft", "draft_t1", "verify_t0", "verify_t1", "verify_topk", "e2etv", "tree_verify", "draft_topk")
+CASES = ("draft", "draft_t1", "verify_t0", "verify_t1", "verify_topk", "e2etv", "tree_verify", "draft_topk",
+         "draft_pos", "sampler")
 
 
 def main(argv=None):
@@ -61,6 +66,23 @@ def main(argv=None):
         x = synth.tree_inputs(c.B, c.gamma, c.V, c.dtype, seed=c.seed, device=dev, p_match=0.75)
         ref = tree_verify(x["target"], x["parent"], x["token"])
         run = lambda: tree_verify(x["target"], x["parent"], x["token"], ws=ref["ws"], out=ref)
+    elif args.case in ("draft_pos", "sampler"):
+        V, r = 248320, 256
+        if args.case == "sampler":
+            c = synth.BRANCH_CONFIG
+            x = c.extra
+            B = x["n_refs"] * x["n_anchors"]
+            inp = synth.branch_inputs(x["n_refs"], x["n_anchors"], c.gamma, c.V, c.r, x["Lmax"], c.dtype, c.seed, dev)
+            L, U, Wt, seeds = inp["logits"], inp["U"], inp["Wt"], inp["seeds"]
+        else:
+            B, G = 512, 2
+            L, _ = synth.target_and_draft(B, G - 1, V, "zipf", 0.0, torch.bfloat16, seed=1011, device=dev)
+            L = L[:, :G].contiguous()
+            U, Wt = synth.markov_weights(V, r, torch.bfloat16, seed=1011, device=dev)
+            seeds = synth.seeds_for(B, 1011).to(dev)
+        anchor = synth.anchors(B, V, seed=1011).to(dev)
+        ref = draft_block(L, anchor, U, Wt, 1, seeds)
+        run = lambda: draft_block(L, anchor, U, Wt, 1, seeds, ws=ref["ws"], out=ref)
     elif args.case == "draft_topk":
         inp = synth.config_inputs(4, device=dev)
         ref = draft_block_topk(inp["draft"], inp["anchor"], inp["U"], inp["Wt"], 20, 0.95, inp["seeds"])
