@@ -303,84 +303,28 @@ __global__ void draft_pos_gather_kernel(const __grid_constant__ DraftParams p, c
     for (int w = lane; w < p.r / 8; w += 32) dst[w] = ok ? __ldg(src + w) : make_uint4(0u, 0u, 0u, 0u);
 }
 
-// The T=1 draw's first two levels for request b (one warp; every lane gets the
-// result): the CTA range where the row's CDF (each CTA's two half records' weights, in
-// index order) crosses thr, then the 128-entry tile of that range, and what is left of
-// thr at that tile's start (INFINITY when rounding leaves no crossing, with the last
-// tile of weight).
-__device__ void pos_locate(const DraftParams& p, const PosExtra& e, int b, float M2, float thr, int& tile_out,
-                           float& tl_out) {
-    const int lane = threadIdx.x & 31;
-    const float4* recs = p.cta_rec + (size_t)b * e.nC * 2;
-    auto weight = [&](float4 v) {
-        const RowAcc r = rowacc_unpack(v);
-        return r.mx == -INFINITY ? 0.0f : r.s * ex2(r.mx * kLog2e - M2);
-    };
-    // level 1: CTA ranges, contiguous segments per lane
-    const int Kc = (e.nC + 31) / 32;
-    const int c0 = lane * Kc, c1 = min(e.nC, c0 + Kc);
-    float seg = 0.0f;
-    for (int c = c0; c < c1; ++c) seg += weight(__ldcg(&recs[2 * c])) + weight(__ldcg(&recs[2 * c + 1]));
-    const float incl = warp_inclusive_scan(seg);
-    const unsigned cross = __ballot_sync(0xffffffffu, incl > thr);
-    int cta = -1;
-    float tl = INFINITY;
-    if (cross) {
-        const int Lc = __ffs(cross) - 1;
-        if (lane == Lc) {
-            float run = incl - seg;
-            for (int c = c0; c < c1; ++c) {
-                const float w = weight(__ldcg(&recs[2 * c])) + weight(__ldcg(&recs[2 * c + 1]));
-                if (run + w > thr) { cta = c; tl = thr - run; break; }
-                run += w;
-            }
-            if (cta < 0) cta = c1 - 1;
-        }
-        cta = __shfl_sync(0xffffffffu, cta, Lc);
-        tl = __shfl_sync(0xffffffffu, tl, Lc);
-    } else {
-        int last = -1;
-        for (int c = c0; c < c1; ++c)
-            if (weight(__ldcg(&recs[2 * c])) + weight(__ldcg(&recs[2 * c + 1])) > 0.0f) last = c;
-        const unsigned has = __ballot_sync(0xffffffffu, last >= 0);
-        cta = has ? __shfl_sync(0xffffffffu, last, 31 - __clz(has)) : 0;
-    }
-    cta = max(0, min(cta, e.nC - 1));
-    // level 2: the CTA's 128-entry tiles
-    const int tb = 2 * pos_t2_begin(cta, e.nC, e.n_t2);
-    const int te = min(2 * pos_t2_begin(cta + 1, e.nC, e.n_t2), p.n_tiles);
-    int tile = -1, last_tile = te - 1;
-    float carry = 0.0f;
-    for (int t0 = tb; t0 < te && tile < 0; t0 += 32) {
-        const int t = t0 + lane;
-        const float w = t < te ? weight(__ldcg(&p.tile_rec[(size_t)b * p.n_tiles + t])) : 0.0f;
-        const float inc = warp_inclusive_scan(w) + carry;
-        const unsigned hit = __ballot_sync(0xffffffffu, t < te && inc > tl);
-        if (hit) {
-            const int Lt = __ffs(hit) - 1;
-            tile = t0 + Lt;
-            tl -= __shfl_sync(0xffffffffu, inc - w, Lt);
-        }
-        const unsigned pos = __ballot_sync(0xffffffffu, t < te && w > 0.0f);
-        if (pos) last_tile = t0 + 31 - __clz(pos);
-        carry = __shfl_sync(0xffffffffu, inc, 31);
-    }
-    if (tile < 0) { tile = last_tile; tl = INFINITY; }
-    tile_out = max(0, min(tile, p.n_tiles - 1));
-    tl_out = tl;
-}
+// One CTA of 8 warps per request: x_j and its outputs; x_j and U[x_j] for the next
+// position.  One wave of loads brings CTA c's two half records to thread c; a block merge
+// gives the row's maximum and sum.  At T=1 a block scan of the CTAs' weights (in index
+// order) finds the CTA range where the CDF crosses u * Z; every warp then finds the
+// 128-entry tile within that range from the tile records (the same loads, so the same
+// decision), computes 16 of its biased logits on CUDA cores (lane l takes the rank slice
+// [8l, 8l + 8) of each entry), and warp 0 scans them.
+constexpr int kPosDrawThreads = 32 * kDrawWarps;
+static_assert(kPosMaxCtas <= kPosDrawThreads, "a CTA record pair per thread");
 
-// One CTA of kDrawWarps warps per request: x_j and its outputs, x_j and U[x_j] for the
-// next position.
 template <int TT>
-__global__ void __launch_bounds__(32 * kDrawWarps)
+__global__ void __launch_bounds__(kPosDrawThreads, 4)
     draft_pos_draw_kernel(const __grid_constant__ DraftParams p, const __grid_constant__ PosExtra e) {
     constexpr int EPW = kDraftTile / kDrawWarps;   // entries of the tile per warp
     __shared__ float s_z[kDraftTile];
-    __shared__ int s_x;
+    __shared__ float4 s_red[kDrawWarps];
+    __shared__ float s_wsum[kDrawWarps];
+    __shared__ int s_first, s_last, s_x;
+    __shared__ float s_tl;
     pdl_launch_dependents();   // the next position's tiles kernel may request its weights
     const int b = blockIdx.x;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const size_t out = (size_t)b * p.gamma + (e.j - 1);
     const int xp = __ldcg(&e.xprev[b]);
     const bf16_t* U = static_cast<const bf16_t*>(p.U);
@@ -394,16 +338,32 @@ __global__ void __launch_bounds__(32 * kDrawWarps)
         if (e.j == p.gamma && b == 0 && p.passes_out) atomicMax(p.passes_out, p.gamma);
     };
     if (xp < 0) {   // the anchor is out of range (position 1), or the request ended earlier
-        if (threadIdx.x == 0) finish(-1, NAN, NAN, e.j == 1 ? SPEC_DEV_TOKEN : 0u);
+        if (tid == 0) finish(-1, NAN, NAN, e.j == 1 ? SPEC_DEV_TOKEN : 0u);
         return;
     }
-    // the row's records: each CTA's two halves
+    // one wave of loads: CTA tid's two half records, the U row of x_{j-1}
     const float4* recs = p.cta_rec + (size_t)b * e.nC * 2;
+    RowAcc r0 = rowacc_empty(), r1 = rowacc_empty();
+    if (tid < e.nC) {
+        r0 = rowacc_unpack(__ldcg(&recs[2 * tid]));
+        r1 = rowacc_unpack(__ldcg(&recs[2 * tid + 1]));
+    }
+    const bool has = lane < (p.r >> 3);
+    uint4 uw = make_uint4(0u, 0u, 0u, 0u);
+    if (TT == 1 && has) uw = __ldg(reinterpret_cast<const uint4*>(U + (size_t)xp * p.r) + lane);
+    const float u = TT == 1 ? philox_uniform(p.seeds[b], (uint64_t)(p.b_base + b), (uint64_t)e.j, 0) : 0.0f;
+    // the row's record
+    {
+        const RowAcc w = warp_rowacc(rowacc_merge(r0, r1));
+        if (lane == 0) s_red[warp] = rowacc_pack(w);
+    }
+    if (tid == 0) { s_first = e.nC; s_last = -1; }
+    __syncthreads();
     RowAcc acc = rowacc_empty();
-    for (int c = lane; c < 2 * e.nC; c += 32) acc = rowacc_merge(acc, rowacc_unpack(__ldcg(&recs[c])));
-    acc = warp_rowacc(acc);
+#pragma unroll
+    for (int w = 0; w < kDrawWarps; ++w) acc = rowacc_merge(acc, rowacc_unpack(s_red[w]));
     if (acc.bad || acc.mx == -INFINITY) {   // no distribution: the request ends here
-        if (threadIdx.x == 0) finish(-1, NAN, NAN, SPEC_DEV_NONFINITE);
+        if (tid == 0) finish(-1, NAN, NAN, SPEC_DEV_NONFINITE);
         return;
     }
     const float M2 = acc.mx * kLog2e;
@@ -412,17 +372,47 @@ __global__ void __launch_bounds__(32 * kDrawWarps)
     int x = acc.idx;
     float qx = conf;
     if constexpr (TT == 1) {
-        // every warp locates the tile itself (the same loads, so the same decisions),
-        // then computes EPW of its biased logits: lane l takes the rank slice [8l, 8l+8)
-        const float u = philox_uniform(p.seeds[b], (uint64_t)(p.b_base + b), (uint64_t)e.j, 0);
-        int tile = 0;
-        float tl = INFINITY;
-        pos_locate(p, e, b, M2, u * S, tile, tl);
-        const bool has = lane < (p.r >> 3);
+        const float thr = u * S;
+        auto weight = [&](const RowAcc& r) { return r.mx == -INFINITY ? 0.0f : r.s * ex2(r.mx * kLog2e - M2); };
+        // level 1: the CTA ranges' weights in index order, a block scan
+        const float w = tid < e.nC ? weight(r0) + weight(r1) : 0.0f;
+        float incl = warp_inclusive_scan(w);
+        if (lane == 31) s_wsum[warp] = incl;
+        __syncthreads();
+        for (int w2 = 0; w2 < warp; ++w2) incl += s_wsum[w2];
+        if (tid < e.nC && incl > thr) atomicMin(&s_first, tid);
+        if (tid < e.nC && w > 0.0f) atomicMax(&s_last, tid);
+        __syncthreads();
+        const int first = s_first;
+        if (tid == first) s_tl = thr - (incl - w);
+        __syncthreads();
+        const bool crossed = first < e.nC;
+        const int cta = crossed ? first : max(0, s_last);
+        float tl = crossed ? s_tl : INFINITY;
+        // level 2: the CTA's 128-entry tiles (every warp alike)
+        const int tb = 2 * pos_t2_begin(cta, e.nC, e.n_t2);
+        const int te = min(2 * pos_t2_begin(cta + 1, e.nC, e.n_t2), p.n_tiles);
+        int tile = -1, last_tile = te - 1;
+        float carry = 0.0f;
+        for (int t0 = tb; t0 < te && tile < 0; t0 += 32) {
+            const int t = t0 + lane;
+            const float wt = t < te ? weight(rowacc_unpack(__ldcg(&p.tile_rec[(size_t)b * p.n_tiles + t]))) : 0.0f;
+            const float inc = warp_inclusive_scan(wt) + carry;
+            const unsigned hit = __ballot_sync(0xffffffffu, t < te && inc > tl);
+            if (hit) {
+                const int Lt = __ffs(hit) - 1;
+                tile = t0 + Lt;
+                tl -= __shfl_sync(0xffffffffu, inc - wt, Lt);
+            }
+            const unsigned pos = __ballot_sync(0xffffffffu, t < te && wt > 0.0f);
+            if (pos) last_tile = t0 + 31 - __clz(pos);
+            carry = __shfl_sync(0xffffffffu, inc, 31);
+        }
+        if (tile < 0) { tile = last_tile; tl = INFINITY; }
+        tile = max(0, min(tile, p.n_tiles - 1));
+        // level 3: this warp's EPW biased logits of the tile, its Wt rows requested at once
         float uu[8];
         {
-            uint4 uw = make_uint4(0u, 0u, 0u, 0u);
-            if (has) uw = __ldg(reinterpret_cast<const uint4*>(U + (size_t)xp * p.r) + lane);
             const uint32_t a[4] = {uw.x, uw.y, uw.z, uw.w};
 #pragma unroll
             for (int k2 = 0; k2 < 4; ++k2) {
@@ -432,19 +422,21 @@ __global__ void __launch_bounds__(32 * kDrawWarps)
         }
         const bf16_t* lrow = static_cast<const bf16_t*>(p.logits) + out * p.V;
         const long e0 = (long)tile * kDraftTile + warp * EPW;
-#pragma unroll 1
-        for (int hb = 0; hb < EPW / kZBatch; ++hb) {
-            const long base = e0 + hb * kZBatch;
-            uint4 w[kZBatch];
+        const float zl = (lane < EPW && e0 + lane < p.V) ? load_one(lrow + e0 + lane) : 0.0f;
+        uint4 wr[2][kZBatch];   // two batches of Wt rows in flight
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb)
 #pragma unroll
             for (int qq = 0; qq < kZBatch; ++qq) {
-                w[qq] = make_uint4(0u, 0u, 0u, 0u);
-                if (has && base + qq < p.V) w[qq] = __ldg(reinterpret_cast<const uint4*>(Wt + (size_t)(base + qq) * p.r) + lane);
+                const long v = e0 + hb * kZBatch + qq;
+                wr[hb][qq] = make_uint4(0u, 0u, 0u, 0u);
+                if (has && v < p.V) wr[hb][qq] = __ldg(reinterpret_cast<const uint4*>(Wt + (size_t)v * p.r) + lane);
             }
-            const float zl = (lane < kZBatch && base + lane < p.V) ? load_one(lrow + base + lane) : 0.0f;
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb)
 #pragma unroll
             for (int qq = 0; qq < kZBatch; ++qq) {
-                const uint32_t a[4] = {w[qq].x, w[qq].y, w[qq].z, w[qq].w};
+                const uint32_t a[4] = {wr[hb][qq].x, wr[hb][qq].y, wr[hb][qq].z, wr[hb][qq].w};
                 float part = 0.0f;
 #pragma unroll
                 for (int k2 = 0; k2 < 4; ++k2) {
@@ -452,10 +444,10 @@ __global__ void __launch_bounds__(32 * kDrawWarps)
                     part = fmaf(uu[2 * k2 + 1], __uint_as_float(a[k2] & 0xffff0000u), part);
                 }
                 part = warp_sum(part);
-                const float zq = __shfl_sync(0xffffffffu, zl, qq);
-                if (lane == 0) s_z[warp * EPW + hb * kZBatch + qq] = base + qq < p.V ? zq + part : -INFINITY;
+                const int qi = hb * kZBatch + qq;
+                const float zq = __shfl_sync(0xffffffffu, zl, qi);
+                if (lane == 0) s_z[warp * EPW + qi] = e0 + qi < p.V ? zq + part : -INFINITY;
             }
-        }
         __syncthreads();
         if (warp == 0) {
             float z[4];
@@ -475,7 +467,7 @@ __global__ void __launch_bounds__(32 * kDrawWarps)
         __syncthreads();
         x = s_x;
     }
-    if (threadIdx.x == 0) finish(x, conf, qx, x < 0 ? SPEC_DEV_NONFINITE : 0u);
+    if (tid == 0) finish(x, conf, qx, x < 0 ? SPEC_DEV_NONFINITE : 0u);
     // the next position's A row
     if (warp == 0 && e.j < p.gamma) {
         const uint4* src = reinterpret_cast<const uint4*>(U + (size_t)(x >= 0 ? x : 0) * p.r);
@@ -566,7 +558,7 @@ static cudaError_t pos_launch_slice(const DraftParams& q, PosExtra e, cudaStream
         cfg.numAttrs = 1;
         err = cudaLaunchKernelEx(&cfg, tiles, q, e, wmap, umap, lmap);
         if (err != cudaSuccess) return err;
-        draft_pos_draw_kernel<TT><<<q.B, 32 * kDrawWarps, 0, stream>>>(q, e);
+        draft_pos_draw_kernel<TT><<<q.B, kPosDrawThreads, 0, stream>>>(q, e);
         err = cudaGetLastError();
         if (err != cudaSuccess) return err;
     }
