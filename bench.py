@@ -619,7 +619,7 @@ def secondary(args, torch, vsd, synth, dev, hbm, hbm_kind, sampler, rank=0, worl
 
     # the SpecOPD anchor-branch sampler: 16 references x 64 anchors, W = 7, V = 248320,
     # r = 256, T = 1: the plan, then the draft block over the 1024 branches (3.56 GB of
-    # drafter rows, more than L2), several tcgen05 launches of 36 branches each
+    # drafter rows, more than L2), walked position by position on the tensor cores
     c = synth.BRANCH_CONFIG
     x = c.extra
     inp = synth.branch_inputs(x["n_refs"], x["n_anchors"], c.gamma, c.V, c.r, x["Lmax"], c.dtype, c.seed, dev)
@@ -643,20 +643,22 @@ def secondary(args, torch, vsd, synth, dev, hbm, hbm_kind, sampler, rank=0, worl
     sampler.active = False
     ms = sum(total) / len(total)
     passes = int(ob["passes"].item())
-    per_launch = 256 // c.gamma
-    launches = 1 + (nb + per_launch - 1) // per_launch
-    # algorithmic: the drafter rows once, W once per biased pass, the outputs
+    # more than 256 rows take the position-by-position path: per slice of at most 1024
+    # branches a gather, then a tiles kernel and a draw per position (passes = gamma:
+    # W read once per position)
+    launches = 1 + ((nb + 1023) // 1024) * (1 + 2 * c.gamma)
+    # algorithmic: the drafter rows once, W once per pass over the positions, the outputs
     byts = nb * c.gamma * c.V * 2 + passes * c.V * c.r * 2
     ach = byts / (ms * 1e-3) / 1e9
     out["anchor_branches"] = {
         "workload": "SpecOPD anchor-branch sampler: 16 refs x 4096 tokens, 64 anchors each, W=7, V=248320, "
                     "r=256 bf16, T=1 (plan + draft block over 1024 branches)",
         "value": nb / (ms * 1e-3), "unit": "branches/s", "ms_per_step": ms, "cuda_graphs": graphed,
-        "passes": passes, "draft_launches_per_step": launches - 1,
+        "passes": passes, "draft_launches_per_step": launches - 1, "path": "position by position (tcgen05)",
         "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm, "peak_kind": hbm_kind, "unit": "GB/s",
                      "frac": ach / hbm, "frac_of_nominal_8tbs": ach / NOMINAL_HBM_GBS,
                      "algorithmic_bytes_per_launch": byts,
-                     "note": "per step; W is read by each of the draft launches, counted once per pass"},
+                     "note": "per step: the drafter rows once and W once per position"},
         "gpu_launches": launches * steps6,
     }
     del inp, ob, wsd
