@@ -172,14 +172,18 @@ const char *spec_last_cuda_error_string(void);
  *   qtok_out      [B, gamma] float32, q_j(x_j) (nullable).
  *   qlogits_out   [B, gamma, V] float32, the biased logits z_j the draws used
  *                 (nullable; pass it to spec_verify as the T=1 draft rows).
- *   passes_out    [1] int32, fixed-point passes over W used (nullable).
+ *   passes_out    [1] int32, passes over W used (nullable): fixed-point passes, or
+ *                 gamma when the chain is walked position by position.
  * A request whose anchor lies outside [0, V), or whose row j is invalid, gets
  * tokens -1 and NaN statistics from that position on (flags TOKEN / NONFINITE).
- * A batch larger than one launch takes (256 rows on the tensor-core path: bf16
- * weights with r a multiple of 64; 4096 rows otherwise) runs as consecutive launches
- * over slices of requests on `stream`; results are those of one call (the Philox
- * request index b is the request's index in the whole batch), and passes_out is the
- * largest over the slices.
+ * More than 256 rows with bf16 logits and weights, r a multiple of 64, V a multiple
+ * of 8 and no qlogits_out: the chain is walked position by position on the tensor
+ * cores, each position reading its rows and W once, in slices of up to 1024
+ * requests.  Otherwise a batch larger than one launch takes (256 rows on the
+ * tensor-core path: bf16 weights with r a multiple of 64; 4096 rows otherwise) runs
+ * as consecutive launches over slices of requests on `stream`, and passes_out is the
+ * largest over the slices.  Either way the results are those of one call (the Philox
+ * request index b is the request's index in the whole batch).
  * Limits: 1 <= gamma <= SPEC_MAX_GAMMA, 0 <= r <= SPEC_MAX_RANK, 1 <= V <= SPEC_MAX_V,
  * 1 <= B*gamma <= SPEC_MAX_DRAFT_ROWS.
  */
