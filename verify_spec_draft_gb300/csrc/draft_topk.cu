@@ -29,9 +29,9 @@
 //                            those tiles' z values re-read, the entries at or above T
 //                            ranked, and the k largest filtered and drawn.  It writes the
 //                            outputs and x_j for position j+1.
-// The weights are read once per position for every 32 requests.  The tiles kernel is a
-// programmatic dependent of the previous pick: its first weight copies are issued before
-// it waits for x_{j-1}.
+// The weights are read once per position for every 32 requests.  From position 2 on, the
+// tiles kernel is a programmatic dependent of the previous pick: its first weight copies
+// are issued before it waits for x_{j-1}.
 #include <mma.h>
 
 #include "spec_device.cuh"
@@ -821,8 +821,8 @@ static cudaError_t launch_topk_tc(DraftTopkParams p, const DraftTopkLaunch& a, c
                            lbase, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
-        // the tiles kernel as a programmatic dependent of the previous pick (its copies
-        // and MMAs need nothing from it; its epilogue waits)
+        // from position 2 on, the tiles kernel is a programmatic dependent of the previous
+        // pick (its copies and MMAs need nothing from it; its epilogue waits)
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)grid);
         cfg.blockDim = dim3(kDkThreads);
@@ -832,7 +832,10 @@ static cudaError_t launch_topk_tc(DraftTopkParams p, const DraftTopkLaunch& a, c
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        // position 1 follows the caller's work on the stream (which may write the logits
+        // or the weights), so it starts only once that work has finished; later positions
+        // follow this library's own pick kernel
+        cfg.numAttrs = j > 1 ? 1 : 0;
         e = cudaLaunchKernelEx(&cfg, kern, p, wmap, lmap);
         if (e != cudaSuccess) return e;
         draft_topk_pick_kernel<<<a.B, kDpThreads, 0, stream>>>(p);
@@ -910,8 +913,8 @@ cudaError_t draft_topk_launch(const DraftTopkLaunch& a, void* ws, cudaStream_t s
     p.nrec = nC;
     for (int j = 1; j <= a.gamma; ++j) {
         p.j = j;
-        // the tiles kernel as a programmatic dependent of the previous pick (its weight
-        // copies are issued before it waits)
+        // from position 2 on, the tiles kernel is a programmatic dependent of the previous
+        // pick (its weight copies are issued before it waits)
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)nC);
         cfg.blockDim = dim3(kDtThreads);
@@ -921,7 +924,10 @@ cudaError_t draft_topk_launch(const DraftTopkLaunch& a, void* ws, cudaStream_t s
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        // position 1 follows the caller's work on the stream (which may write the logits
+        // or the weights), so it starts only once that work has finished; later positions
+        // follow this library's own pick kernel
+        cfg.numAttrs = j > 1 ? 1 : 0;
         e = cudaLaunchKernelEx(&cfg, kt, p);
         if (e != cudaSuccess) return e;
         draft_topk_pick_kernel<<<a.B, kDpThreads, 0, stream>>>(p);
