@@ -176,3 +176,24 @@ def test_batched_draft_position_path_two_slices(spec, T):
     assert int(out["passes"].item()) == G   # the weights are read once per position
     rows = [0, 127, 128, 511, 1023, 1024, 1025, 1099]
     assert _draft_check(out, L, anchor, U, Wt, T, seeds, rows) >= len(rows) * G - 2 * G
+
+
+@pytest.mark.parametrize("B,G,V,r,T", [
+    (300, 3, 40000, 192, 0),    # r = 192 (three k blocks), a ragged last M tile (300 = 2 x 128 + 44)
+    (130, 2, 7000, 128, 1),     # just over 256 rows; an odd count of 128-entry tiles
+    (600, 5, 3000, 256, 1),     # five M tiles: both epilogue groups hold several
+])
+def test_batched_draft_position_path_shapes(spec, B, G, V, r, T):
+    """The position-by-position path on other ranks, M tiles and vocabularies."""
+    L, _ = synth.target_and_draft(B, G - 1, V, "zipf", 0.0, torch.bfloat16, seed=B + V)
+    L = L[:, :G].contiguous()
+    U, Wt = synth.markov_weights(V, r, torch.bfloat16, seed=B + V, scale=0.3)
+    anchor = synth.anchors(B, V, seed=B + V)
+    seeds = synth.seeds_for(B, 3)
+    dev = torch.device("cuda")
+    out = vsd.draft_block(L.to(dev), anchor.to(dev), U.to(dev), Wt.to(dev), T, seeds.to(dev))
+    torch.cuda.synchronize()
+    assert vsd.device_status(out["ws"]) == 0
+    assert int(out["passes"].item()) == G
+    rows = [0, 1, 127, 128, B // 2, B - 2, B - 1]
+    assert _draft_check(out, L, anchor, U, Wt, T, seeds, rows) >= len(rows) * G - 2 * G
