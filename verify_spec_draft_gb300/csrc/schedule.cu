@@ -49,6 +49,8 @@ __global__ void __launch_bounds__(kSchedThreads) verify_budget_kernel(const floa
     __shared__ double s_bobj[kSchedThreads / 32];
     __shared__ int s_bk[kSchedThreads / 32];
     __shared__ int s_kstar;
+    __shared__ unsigned long long s_xk[2][kSchedThreads];   // the register sort's exchange buffers
+    __shared__ int s_xi[2][kSchedThreads];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nt = blockDim.x;
 
@@ -72,21 +74,57 @@ __global__ void __launch_bounds__(kSchedThreads) verify_budget_kernel(const floa
     __syncthreads();
 
     // bitonic sort into candidate order (P descending, index ascending)
-    for (int size = 2; size <= M; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int i = tid; i < M; i += nt) {
-                const int l = i ^ stride;
-                if (l > i) {
-                    const bool up = (i & size) == 0;
-                    const unsigned long long pi_ = sb[i], pl = sb[l];
-                    const int ii = si[i], il = si[l];
-                    const bool swap = up ? sched_precedes(pl, il, pi_, ii) : sched_precedes(pi_, ii, pl, il);
-                    if (swap) { sb[i] = pl; sb[l] = pi_; si[i] = il; si[l] = ii; }
+    if (M <= nt) {
+        // one candidate per thread, in registers: partners closer than a warp are reached
+        // by shuffles, farther ones through a shared array (two buffers, so one barrier a
+        // step)
+        unsigned long long pk = tid < M ? sb[tid] : 0ull;
+        int ik = tid < M ? si[tid] : INT_MAX;
+        int buf = 0;
+        for (int size = 2; size <= M; size <<= 1) {
+            for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                unsigned long long po;
+                int io;
+                if (stride < 32) {
+                    po = ((unsigned long long)__shfl_xor_sync(0xffffffffu, (unsigned)(pk >> 32), stride) << 32) |
+                         (unsigned)__shfl_xor_sync(0xffffffffu, (unsigned)pk, stride);
+                    io = __shfl_xor_sync(0xffffffffu, ik, stride);
+                } else {
+                    s_xk[buf][tid] = pk;
+                    s_xi[buf][tid] = ik;
+                    __syncthreads();
+                    po = s_xk[buf][tid ^ stride];
+                    io = s_xi[buf][tid ^ stride];
+                    buf ^= 1;
                 }
+                // the lower position of a pair keeps the preceding candidate in an ascending
+                // run (up), the other one in a descending run
+                const bool up = (tid & size) == 0;
+                const bool lower = (tid & stride) == 0;
+                const bool other_first = sched_precedes(po, io, pk, ik);
+                if (tid < M && (lower == up ? other_first : !other_first)) { pk = po; ik = io; }
             }
-            __syncthreads();
+        }
+        __syncthreads();   // every read of the shared exchange buffers and of sb / si is done
+        if (tid < M) { sb[tid] = pk; si[tid] = ik; }
+    } else {
+        for (int size = 2; size <= M; size <<= 1) {
+            for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                for (int i = tid; i < M; i += nt) {
+                    const int l = i ^ stride;
+                    if (l > i) {
+                        const bool up = (i & size) == 0;
+                        const unsigned long long pi_ = sb[i], pl = sb[l];
+                        const int ii = si[i], il = si[l];
+                        const bool swap = up ? sched_precedes(pl, il, pi_, ii) : sched_precedes(pi_, ii, pl, il);
+                        if (swap) { sb[i] = pl; sb[l] = pi_; si[i] = il; si[l] = ii; }
+                    }
+                }
+                __syncthreads();
+            }
         }
     }
+    __syncthreads();
 
     // inclusive prefix sums of the sorted P over the first N (each thread a run of R)
     const int R = (M + nt - 1) / nt;

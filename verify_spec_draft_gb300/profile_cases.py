@@ -19,16 +19,17 @@ kernel, on inputs larger than L2 (129 MB) but only a few hundred MB on the devic
              position-by-position path for batches over 256 rows (509 MB of logits)
   sampler    spec_draft_block at T=1 on the anchor-branch workload, 1024 branches x W=7
              (3.56 GB of logits): for launch lists only (one metric, one pass)
+  budget     spec_verify_budget, B=32, gamma=16, budget 256, a linear cost curve (2 KB)
 """
 
 import argparse
 
 import torch
 
-from . import draft_block, draft_block_topk, e2etv, load, synth, tree_verify, verify, verify_topk
+from . import draft_block, draft_block_topk, e2etv, load, synth, tree_verify, verify, verify_budget, verify_topk
 
 CASES = ("draft", "draft_t1", "verify_t0", "verify_t1", "verify_topk", "e2etv", "tree_verify", "draft_topk",
-         "draft_pos", "sampler")
+         "draft_pos", "sampler", "budget")
 
 
 def main(argv=None):
@@ -83,6 +84,13 @@ def main(argv=None):
         anchor = synth.anchors(B, V, seed=1011).to(dev)
         ref = draft_block(L, anchor, U, Wt, 1, seeds)
         run = lambda: draft_block(L, anchor, U, Wt, 1, seeds, ws=ref["ws"], out=ref)
+    elif args.case == "budget":
+        g = torch.Generator(device=dev)
+        g.manual_seed(1006)
+        conf = (0.4 + 0.6 * torch.rand((32, 16), generator=g, device=dev)).contiguous()
+        cost = (40.0 + 0.1 * torch.arange(257, device=dev, dtype=torch.float32)).contiguous()
+        ref = verify_budget(conf, 256, cost)
+        run = lambda: verify_budget(conf, 256, cost, out=ref)
     elif args.case == "draft_topk":
         inp = synth.config_inputs(4, device=dev)
         ref = draft_block_topk(inp["draft"], inp["anchor"], inp["U"], inp["Wt"], 20, 0.95, inp["seeds"])
