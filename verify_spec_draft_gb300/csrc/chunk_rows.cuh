@@ -143,6 +143,43 @@ __device__ __forceinline__ float chunk_max_nan(const uint4 (&w)[NW]) {
                      fmax_nan(__uint_as_float(w[i].z), __uint_as_float(w[i].w)));
     return m;
 }
+// The decode-order position (0..31) of the first of this thread's entries equal to m,
+// or -1: the first 8-entry group whose maximum is m, then the first entry of that group
+// (decode order is index order within a thread's group and across its groups, in both
+// the contiguous and the group-interleaved layout).  For a lane whose entries hold the
+// warp's maximum, this replaces decoding and comparing all 32 entries.
+template <typename T, int NW>
+__device__ __forceinline__ int first_equal(const uint4 (&w)[NW], float m) {
+    constexpr int WPG = NW / 4;   // 16-byte words per 8-entry group: 1 (bf16) or 2 (float32)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float gm;
+        if constexpr (sizeof(T) == 2) gm = u4_max_nan<2>(w[j]);
+        else gm = f_max_nan(u4_max_nan<4>(w[WPG * j]), u4_max_nan<4>(w[WPG * j + 1]));
+        if (gm == m) {
+            float x[8];
+            if constexpr (sizeof(T) == 2) {
+                const uint32_t a[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    x[2 * k] = __uint_as_float(a[k] << 16);
+                    x[2 * k + 1] = __uint_as_float(a[k] & 0xffff0000u);
+                }
+            } else {
+                const uint4 lo = w[WPG * j], hi = w[WPG * j + 1];
+                x[0] = __uint_as_float(lo.x); x[1] = __uint_as_float(lo.y);
+                x[2] = __uint_as_float(lo.z); x[3] = __uint_as_float(lo.w);
+                x[4] = __uint_as_float(hi.x); x[5] = __uint_as_float(hi.y);
+                x[6] = __uint_as_float(hi.z); x[7] = __uint_as_float(hi.w);
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                if (x[e] == m) return 8 * j + e;
+        }
+    }
+    return -1;
+}
+
 __device__ __forceinline__ float warp_max_nan(float m) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmax_nan(m, __shfl_xor_sync(0xffffffffu, m, o));

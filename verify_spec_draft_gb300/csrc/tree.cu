@@ -142,12 +142,8 @@ __device__ __forceinline__ void tv_fold(const TreeVerifyParams& p, const uint4 (
     const int bad = (isnan(m) || m == INFINITY) ? 1 : 0;
     int idx = 0x7fffffff;
     if (!bad && lm == m) {
-        float x[kEPT];
-        decode_words<TT, NW>(w, x);
-        const long seg = il_seg(c);
-#pragma unroll
-        for (int k = kEPT - 1; k >= 0; --k)
-            if (x[k] == m) idx = (int)il_entry(seg, k);
+        const int k = first_equal<TT, NW>(w, m);
+        if (k >= 0) idx = (int)il_entry(il_seg(c), k);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) idx = min(idx, __shfl_xor_sync(0xffffffffu, idx, o));

@@ -83,17 +83,13 @@ __global__ void __launch_bounds__(kT0Threads) verify_t0_kernel(VerifyParams p) {
         split(it, row, c);
         // NaN-propagating max of the 32 entries (-inf pads the row end), then the
         // warp max; only lanes holding it look for their lowest index
-        float m = chunk_max_nan<TT, NW>(cur);
-        m = warp_max_nan(m);
+        const float lm = chunk_max_nan<TT, NW>(cur);
+        const float m = warp_max_nan(lm);
         const int bad = (isnan(m) || m == INFINITY) ? 1 : 0;
         int idx = 0x7fffffff;
-        if (!bad) {
-            float x[kEPT];
-            decode_words<TT, NW>(cur, x);
-            const long base = t0_base(c);
-#pragma unroll
-            for (int e = kEPT - 1; e >= 0; --e)
-                if (x[e] == m) idx = (int)(base + e);
+        if (!bad && lm == m) {
+            const int k = first_equal<TT, NW>(cur, m);
+            if (k >= 0) idx = (int)(t0_base(c) + k);
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) idx = min(idx, __shfl_xor_sync(0xffffffffu, idx, o));
