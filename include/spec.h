@@ -172,8 +172,11 @@ const char *spec_last_cuda_error_string(void);
  *   qtok_out      [B, gamma] float32, q_j(x_j) (nullable).
  *   qlogits_out   [B, gamma, V] float32, the biased logits z_j the draws used
  *                 (nullable; pass it to spec_verify as the T=1 draft rows).
- *   passes_out    [1] int32, passes over W used (nullable): fixed-point passes, or
- *                 gamma when the chain is walked position by position.
+ *   passes_out    [1] int32 (nullable): biased fixed-point passes, up to the first
+ *                 that changes no token, at most gamma (at T=1 a pass recomputes only
+ *                 the rows whose predecessor changed in the pass before, and a pass
+ *                 with no such row is counted without being run); gamma when the
+ *                 chain is walked position by position.
  * A request whose anchor lies outside [0, V), or whose row j is invalid, gets
  * tokens -1 and NaN statistics from that position on (flags TOKEN / NONFINITE).
  * More than 256 rows with bf16 logits and weights, r a multiple of 64, V a multiple

@@ -363,7 +363,6 @@ __device__ __forceinline__ void draw_locate(const DraftParams& p, const float4* 
 // entry of positive weight, and its z.
 __device__ __forceinline__ void draw_scan_tile(const float (&z)[4], const long (&v)[4], long V, float M2, float tl,
                                                int tile, int& found_out, float& zf_out) {
-    const int lane = threadIdx.x & 31;
     float car = 0.0f, zf = 0.0f, zl = 0.0f;
     int found = -1, last_pos = -1;
 #pragma unroll
@@ -467,7 +466,7 @@ __device__ __forceinline__ void draw_group_sync(int grp) {
 
 template <typename LT>
 __device__ void finalize_rows_t1g(const DraftParams& p, int pass, const int32_t* prev, int32_t* cur, int nblk_tile,
-                                  float* s_z) {
+                                  float* s_z, const uint8_t* act = nullptr) {
     constexpr int EPW = kDraftTile / kDrawWarps;   // entries of the tile per warp
     const int R = p.B * p.gamma;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -479,6 +478,11 @@ __device__ void finalize_rows_t1g(const DraftParams& p, int pass, const int32_t*
     const bf16_t* Wt = static_cast<const bf16_t*>(p.Wt);
     const bool has = lane < (p.r >> 3);
     for (int row = grp * gridDim.x + blockIdx.x; row < R; row += gridDim.x * ngrp) {
+        if (act != nullptr && !act[row]) {
+            // the row's predecessor kept its token: so does the row (its outputs stand)
+            if (gw == 0 && lane == 0) cur[row] = __ldcg(&prev[row]);
+            continue;
+        }
         const int b = row / p.gamma, j = row % p.gamma;
         const float4* recs = p.cta_rec + (size_t)row * nblk_tile;
         const LT* lrow = static_cast<const LT*>(p.logits) + (size_t)row * p.V;

@@ -58,9 +58,10 @@ constexpr int kTcWarps = 18;                 // producer, MMA, 16 epilogue warps
 // of the epilogue (4 with one 128-row M tile, 2 with two)
 template <int MT> struct TcBufs { static constexpr int N = MT == 1 ? 4 : 2; };
 // Wt ring stages of 16 KB: a compile-time count, so the single-thread producer and MMA
-// loops index the ring without integer division (deeper rings did not stream faster:
-// the extra copies only queue behind the first ones)
-template <int MT> struct TcStages { static constexpr int N = MT == 1 ? 6 : 3; };
+// loops index the ring without integer division (deeper rings did not stream faster
+// with one M tile: the extra copies only queue behind the first ones).  With two M
+// tiles at T=1 the ring holds one whole tile (4 stages at r = 256).
+template <int MT, int TT> struct TcStages { static constexpr int N = MT == 1 ? 6 : (TT == 1 ? 4 : 3); };
 constexpr int kTcThreads = 32 * kTcWarps;
 
 struct TcShared {
@@ -80,7 +81,8 @@ struct TcShared {
 template <int MT, typename LT, int TT>
 __device__ bool tc_tile_phase(const DraftParams& p, const CUtensorMap* tmap, const int32_t* prev, const int32_t* anc,
                               float4* rec_out, const TcShared& sh, uint32_t tmem, uint32_t& it_p, uint32_t& it_m,
-                              uint32_t& jt_m, uint32_t& jt_e, uint32_t& pre_issued, unsigned long long* keys) {
+                              uint32_t& jt_m, uint32_t& jt_e, uint32_t& pre_issued, unsigned long long* keys,
+                              const uint8_t* act) {
     constexpr int NB = TcBufs<MT>::N;
     constexpr int EW = 4 / MT;                 // column slices per quadrant and M tile
     constexpr int CPW = kTcN / EW;             // columns per epilogue warp (32 * MT)
@@ -92,15 +94,50 @@ __device__ bool tc_tile_phase(const DraftParams& p, const CUtensorMap* tmap, con
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const bf16_t* U = static_cast<const bf16_t*>(p.U);
     __shared__ int s_fail;
+    // T=1 from the second biased pass on: only the rows flagged in act are recomputed
+    auto live = [&](int n) { return TT == 1 && act != nullptr ? act[n] != 0 : true; };
 
     // gather A = U[x_prev(n)] for the padded rows, 128-byte swizzled, K-major
     if (threadIdx.x == 0) s_fail = 0;
+    __shared__ int s_xp[TT == 1 ? 256 : 1];   // T=1: x_prev of every row (R <= 256)
+    if constexpr (TT == 1) {
+        // the rows' previous tokens come from global memory: read them all at once,
+        // then keep GU of a thread's 16-byte U words in flight
+        for (int n = threadIdx.x; n < R; n += blockDim.x) s_xp[n] = live(n) ? prev_token(p, prev, n, anc) : -1;
+        __syncthreads();
+        constexpr int GU = 8;
+        const int total = MT * 128 * CPR;
+        for (int i0 = threadIdx.x; i0 < total; i0 += GU * blockDim.x) {
+            uint4 v[GU];
+#pragma unroll
+            for (int u = 0; u < GU; ++u) {
+                const int idx = i0 + u * (int)blockDim.x;
+                v[u] = make_uint4(0u, 0u, 0u, 0u);
+                if (idx < total) {
+                    const int n = idx / CPR, kc = idx - n * CPR;
+                    const int x = n < R ? s_xp[n] : -1;
+                    if (x >= 0 && x < p.V) v[u] = __ldg(reinterpret_cast<const uint4*>(U + (size_t)x * p.r) + kc);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < GU; ++u) {
+                const int idx = i0 + u * (int)blockDim.x;
+                if (idx < total) {
+                    const int n = idx / CPR, kc = idx - n * CPR;
+                    const int pos = mma_row(n, MT);
+                    const int kb = kc >> 3, c = kc & 7, mt = pos >> 7, nl = pos & 127;
+                    *reinterpret_cast<uint4*>(sh.a + (size_t)(mt * KB + kb) * kTcBlock + nl * 128 + ((c ^ (nl & 7)) << 4)) =
+                        v[u];
+                }
+            }
+        }
+    } else
     for (int idx = threadIdx.x; idx < MT * 128 * CPR; idx += blockDim.x) {
         const int n = idx / CPR, kc = idx - n * CPR;
         const int pos = mma_row(n, MT);
         const int kb = kc >> 3, c = kc & 7, mt = pos >> 7, nl = pos & 127;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (n < R) {
+        if (n < R && live(n)) {
             const int x = prev_token(p, prev, n, anc);
             if (x >= 0 && x < p.V) v = __ldg(reinterpret_cast<const uint4*>(U + (size_t)x * p.r) + kc);
         }
@@ -110,7 +147,7 @@ __device__ bool tc_tile_phase(const DraftParams& p, const CUtensorMap* tmap, con
     __syncthreads();
 
     const int tb = tile_begin(blockIdx.x, gridDim.x, p.n_tiles), te = tile_begin(blockIdx.x + 1, gridDim.x, p.n_tiles);
-    constexpr int S = TcStages<MT>::N;
+    constexpr int S = TcStages<MT, TT>::N;
     if (warp == 0) {
         if (lane == 0) {
             uint32_t skip = pre_issued;   // stages of this pass already in flight
@@ -160,10 +197,10 @@ __device__ bool tc_tile_phase(const DraftParams& p, const CUtensorMap* tmap, con
         const int mt = g4 / EW, cs = g4 % EW;
         const int g = row_of(mt, q, lane, MT);
         const bool group_rows = row_of(mt, q, 0, MT) < R;
-        const bool mine = g < R;
+        const bool mine = g < R && live(g);
         int prev_ok = 1;
         if (mine) {
-            const int x = prev_token(p, prev, g, anc);
+            const int x = TT == 1 ? s_xp[g] : prev_token(p, prev, g, anc);
             prev_ok = (x >= 0 && x < p.V) ? 1 : 0;
         }
         const LT* lrow = static_cast<const LT*>(p.logits) + (size_t)(mine ? g : 0) * p.V;
@@ -241,7 +278,7 @@ __device__ bool tc_tile_phase(const DraftParams& p, const CUtensorMap* tmap, con
         const int q = warp & 3, g4 = (warp - 2) >> 2;
         const int mt = g4 / EW, cs = g4 % EW;
         const int g = row_of(mt, q, lane, MT);
-        if (cs == 0 && g < R) {
+        if (cs == 0 && g < R && live(g)) {
             RowAcc m = rowacc_empty();
             for (int k = 0; k < EW; ++k)
                 m = rowacc_merge(m, rowacc_unpack(sh.slice_rec[(size_t)((mt * EW + k) * 4 + q) * 32 + lane]));
@@ -261,17 +298,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int KB = p.r / kTcK;
     const int nw = blockDim.x >> 5;
     // shared layout: A | Wt ring (S stages) | slice records | [T=1: tile records |
-    // per-warp U rows] | mbarriers | TMEM address | tokens | anchors.  T=0 needs neither
-    // T=1 region, so the launch gives its room to more ring stages.
+    // the draw groups' tile logits] | mbarriers | TMEM address | tokens | anchors.  T=0
+    // needs neither T=1 region.
     TcShared sh;
-    constexpr int S = TcStages<MT>::N;
+    constexpr int S = TcStages<MT, TT>::N;
     sh.a = base;
     sh.b = base + (size_t)MT * KB * kTcBlock;
     sh.slice_rec = reinterpret_cast<float4*>(sh.b + (size_t)S * kTcBlock);
     constexpr bool t1 = TT == 1;
     sh.tile_rec = t1 ? sh.slice_rec + 16 * 32 : nullptr;
     float* s_uw_all = reinterpret_cast<float*>(sh.slice_rec + (t1 ? 3 : 1) * 16 * 32);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(s_uw_all + (t1 ? (size_t)nw * p.r : 0));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s_uw_all + (t1 ? (size_t)kDraftTile * (nw / kDrawWarps) : 0));
     sh.full = bars;
     sh.empty = bars + S;
     constexpr int NB = TcBufs<MT>::N;
@@ -284,7 +321,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int32_t* s_anc = s_tok + 2 * R;                             // [B] anchors
     float* s_mx = reinterpret_cast<float*>(s_anc + p.B);        // [B*gamma] row maxima (T=0)
     const int warp = threadIdx.x >> 5;
-    float* s_uw = s_uw_all + (size_t)warp * p.r;
     constexpr uint32_t tmem_cols = 512u;
 
     pdl_launch_dependents();   // a following verify may stream its target rows meanwhile
@@ -348,7 +384,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int r = threadIdx.x; r < R; r += blockDim.x) key_buf(pass + 1)[(size_t)r * kKeyStride] = 0ull;
             float4* rec = (pass & 1) ? p.cta_rec2 : p.cta_rec;
             if (!tc_tile_phase<MT, LT, TT>(p, &tmap, tok[(pass + 1) & 1], s_anc, rec, sh, tmem, it_p, it_m, jt_m, jt_e,
-                                       pre_issued, key_buf(pass))) {
+                                       pre_issued, key_buf(pass), nullptr)) {
                 ok = false;
                 break;
             }
@@ -364,14 +400,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
         }
     } else {
+        // Row j of pass k draws from the fixed uniform of its position given x_{j-1} of
+        // pass k-1 alone, so from pass 2 on a row whose predecessor kept its token keeps
+        // its own token, confidence and probability: only the rows whose predecessor
+        // changed in the last pass are recomputed (s_act, one flag per row, in the room
+        // T=0 keeps its tokens in).  Every CTA reads the same two token buffers, which
+        // no CTA writes before the next grid barrier, so all take the same flags.
+        uint8_t* s_act = reinterpret_cast<uint8_t*>(s_tok);
         for (;; ++pass) {
             const bool use_bias = pass > 0;
             const int32_t* prev = p.tokbuf + ((pass + 1) & 1) * (size_t)R;
             int32_t* cur = p.tokbuf + (pass & 1) * (size_t)R;
             if (blockIdx.x == 0 && threadIdx.x == 0) p.changed[pass + 1] = 0u;
+            const uint8_t* act = nullptr;
+            if (pass >= 2) {
+                int n_act = 0;
+                for (int r0 = 0; r0 < R; r0 += blockDim.x) {
+                    const int row = r0 + threadIdx.x;
+                    bool a = false;
+                    if (row < R && row % p.gamma != 0) a = __ldcg(&prev[row - 1]) != __ldcg(&cur[row - 1]);
+                    if (row < R) s_act[row] = a ? 1 : 0;
+                    n_act += __syncthreads_count(a);
+                }
+                if (n_act == 0) break;   // the pass would change no row: the chain is final
+                act = s_act;
+            }
             if (use_bias) {
                 if (!tc_tile_phase<MT, LT, TT>(p, &tmap, prev, s_anc, p.cta_rec, sh, tmem, it_p, it_m, jt_m, jt_e,
-                                           pre_issued, nullptr)) {
+                                           pre_issued, nullptr, act)) {
                     ok = false;
                     break;
                 }
@@ -380,8 +436,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             if (!grid_barrier(gb, nb, p.status)) { ok = false; break; }
             if (pass == 0 && threadIdx.x == 0) { pre_issued = s_pre; it_p = s_pre; }
-            if (use_bias) finalize_rows_t1g<LT>(p, pass, prev, cur, gridDim.x, s_uw_all);
-            else finalize_rows<LT, bf16_t>(p, pass, use_bias, prev, cur, gridDim.x, s_uw);
+            if (use_bias) finalize_rows_t1g<LT>(p, pass, prev, cur, gridDim.x, s_uw_all, act);
+            else finalize_rows<LT, bf16_t>(p, pass, use_bias, prev, cur, gridDim.x, nullptr);   // no bias: no U row
             if (!grid_barrier(gb, nb, p.status)) { ok = false; break; }
             if (pass >= 1 && __ldcg(&p.changed[pass]) == 0u) break;
             if (pass == p.gamma) break;
@@ -435,9 +491,10 @@ static cudaError_t launch_tc(const DraftParams& p, cudaStream_t stream) {
     const int threads = kTcThreads;
     const int KB = p.r / kTcK;
     constexpr bool t1 = TT == 1;
-    constexpr int S = TcStages<MT>::N;
+    constexpr int S = TcStages<MT, TT>::N;
     const size_t smem = 1024 + (size_t)MT * KB * kTcBlock + (size_t)S * kTcBlock +
-                        sizeof(float4) * (t1 ? 3 : 1) * 16 * 32 + (t1 ? sizeof(float) * kTcWarps * p.r : 0) +
+                        sizeof(float4) * (t1 ? 3 : 1) * 16 * 32 +
+                        (t1 ? sizeof(float) * kDraftTile * (kTcWarps / kDrawWarps) : 0) +
                         sizeof(uint64_t) * (2 * S + 2 * TcBufs<MT>::N + 1) + 16 +
                         sizeof(int32_t) * (2 * (size_t)p.B * p.gamma + p.B) + sizeof(float) * (size_t)p.B * p.gamma;
     if (smem > kTcSmemBudget) return cudaErrorInvalidConfiguration;
