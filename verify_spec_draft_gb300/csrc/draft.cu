@@ -41,7 +41,7 @@ __global__ void __launch_bounds__(kThreads) draft_kernel(DraftParams p) {
         if (blockIdx.x == 0 && threadIdx.x == 0) p.changed[pass + 1] = 0u;
         if (!use_bias && p.vec_l && p.temperature == 0) tile_phase_stream0_t0<LT>(p, p.cta_rec, !biased, nullptr);
         else if (!use_bias && p.vec_l) {
-            if (!tile_phase_stream0_t1<LT>(p)) tile_phase_stream0<LT>(p);
+            tile_phase_stream0_t1<LT>(p);
         }
         else tile_phase_cc<LT, WT>(p, use_bias, prev, s_uw);
         if (!grid_barrier(gb, nb, p.status)) return;

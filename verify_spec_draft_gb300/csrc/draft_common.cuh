@@ -614,56 +614,6 @@ __device__ void tile_phase_cc(const DraftParams& p, bool use_bias, const int32_t
     }
 }
 
-// Unbiased tile phase (pass 0) on rows whose bytes are 16-byte aligned: one warp per
-// row, each lane one 16-byte word per unit of 32 words (a unit is one tile of f32 or
-// two tiles of bf16), with the next eight units' loads in flight (register ring,
-// statically indexed).  Tile records are reduced over the lanes of each tile.
-template <typename LT>
-__device__ __forceinline__ void unit_record(const uint4& w, long e0, long V, int lanes_per_tile, RowAcc& out) {
-    constexpr int EPL = 16 / (int)sizeof(LT);
-    float x[EPL];
-    if (sizeof(LT) == 2) {
-        const uint32_t a[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            x[(2 * k) % EPL] = __uint_as_float(a[k] << 16);
-            x[(2 * k + 1) % EPL] = __uint_as_float(a[k] & 0xffff0000u);
-        }
-    } else {
-        x[0] = __uint_as_float(w.x);
-        x[1 % EPL] = __uint_as_float(w.y);
-        x[2 % EPL] = __uint_as_float(w.z);
-        x[3 % EPL] = __uint_as_float(w.w);
-    }
-    float m = -INFINITY;
-    int bad = 0;
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) {
-        if (e0 + e < V) { bad |= bad_logit(x[e]) ? 1 : 0; m = fmaxf(m, x[e]); }
-    }
-    for (int o = lanes_per_tile >> 1; o > 0; o >>= 1) {
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        bad |= __shfl_xor_sync(0xffffffffu, bad, o);
-    }
-    float s = 0.0f;
-    int idx = 0x7fffffff;
-    if (m != -INFINITY && !bad) {
-        const float m2 = m * kLog2e;
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) {
-            if (e0 + e < V) {
-                s += wexp(x[e], m2);
-                if (x[e] == m) idx = min(idx, (int)(e0 + e));
-            }
-        }
-    }
-    for (int o = lanes_per_tile >> 1; o > 0; o >>= 1) {
-        s += __shfl_xor_sync(0xffffffffu, s, o);
-        idx = min(idx, __shfl_xor_sync(0xffffffffu, idx, o));
-    }
-    out = RowAcc{bad ? -INFINITY : m, s, idx, bad};
-}
-
 // Pass 0 at T=0: only the argmax of the unbiased rows is used when a biased pass
 // follows (need_s false), so each lane keeps a running (max, lowest index) and, if
 // need_s, a running sum rescaled when the max grows; one warp reduction per row.
@@ -766,13 +716,7 @@ __device__ void tile_phase_stream0_t0(const DraftParams& p, float4* rec_out, boo
     }
 }
 
-// Pass 0 at T=1 (unbiased rows): the per-(row, tile) records of the draw and one
-// record per (row, CTA).  A warp holds one row's slice of this CTA's tile range in
-// registers (at most kS1Units units of 32 x EPL entries), takes the slice maximum
-// with one warp reduction, then each tile's sum against it, so a tile costs only a
-// sum reduction over its lanes.  Records carry the slice maximum as their reference
-// (s = sum 2^(z log2e - fl(mx log2e))); no argmax is kept, since T=1 draws.  Returns
-// false (nothing done) when the slice is longer than kS1Units units.
+// The entries of one 16-byte word of logits as float32.
 template <typename LT>
 __device__ __forceinline__ void unpack_word(const uint4& w, float (&x)[16 / sizeof(LT)]) {
     if constexpr (sizeof(LT) == 2) {
@@ -790,10 +734,19 @@ __device__ __forceinline__ void unpack_word(const uint4& w, float (&x)[16 / size
     }
 }
 
+// Pass 0 at T=1 (unbiased rows) on rows of whole 16-byte words: the per-(row, tile)
+// records of the draw and one record per (row, CTA); no argmax is kept, since T=1
+// draws.  A warp holds one row's slice of this CTA's tile range in registers (at most
+// kS1Units units of 32 words, one word per lane: 256 bf16 or 128 float32 entries).  The
+// slice maximum takes a packed NaN-propagating maximum per word (a NaN or +inf entry
+// shows as a NaN or +inf maximum) and one warp reduction; each tile's sum against it
+// takes the exponent arguments and sums two entries at a time (float32x2), then a
+// reduction over the tile's lanes.  Records carry the slice maximum as their reference.
+// Each warp requests its rows' slices into L2 kS1Ahead rows ahead of their loads.
 constexpr int kS1Units = 8;
 constexpr int kS1Ahead = 3;
 template <typename LT>
-__device__ bool tile_phase_stream0_t1(const DraftParams& p) {
+__device__ bool stream0_t1_rows(const DraftParams& p) {
     constexpr int EPL = 16 / (int)sizeof(LT);          // entries per lane per unit
     constexpr int UNIT = 32 * EPL;                     // entries per unit
     constexpr int TPU = UNIT / kDraftTile;             // tiles per unit (1 or 2)
@@ -807,20 +760,18 @@ __device__ bool tile_phase_stream0_t1(const DraftParams& p) {
     if (upr > kS1Units) return false;
     const uint4 ninf = sizeof(LT) == 2 ? make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u)
                                        : make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
-    // each warp's row slices are requested into L2 kS1Ahead rows ahead of their loads,
-    // so a warp's rows stream from DRAM while it works through them one round trip at a
-    // time (a slice is contiguous: 16-byte aligned, whole 16-byte words)
+    const LT* L = static_cast<const LT*>(p.logits);
     const long e_stop = e_end < p.V ? e_end : p.V;
     const unsigned slice_bytes = e_stop > e_begin ? (unsigned)((e_stop - e_begin) * (long)sizeof(LT)) : 0u;
     auto prefetch_row = [&](int r) {
-        if (lane == 0 && r < R && slice_bytes > 0)
-            bulk_prefetch_l2(static_cast<const LT*>(p.logits) + (size_t)r * p.V + e_begin, slice_bytes);
+        if (lane == 0 && r < R && slice_bytes > 0) bulk_prefetch_l2(L + (size_t)r * p.V + e_begin, slice_bytes);
     };
 #pragma unroll
     for (int a = 0; a < kS1Ahead; ++a) prefetch_row((int)(threadIdx.x >> 5) + a * nw);
+    const f2x k2 = f2_pack(kLog2e, kLog2e);
     for (int row = (int)(threadIdx.x >> 5); row < R; row += nw) {
         prefetch_row(row + kS1Ahead * nw);
-        const LT* lrow = static_cast<const LT*>(p.logits) + (size_t)row * p.V;
+        const LT* lrow = L + (size_t)row * p.V;
         uint4 w[kS1Units];
 #pragma unroll
         for (int u = 0; u < kS1Units; ++u) {
@@ -828,38 +779,40 @@ __device__ bool tile_phase_stream0_t1(const DraftParams& p) {
             w[u] = ninf;
             if (u < upr && e0 < e_end && e0 + EPL <= p.V) w[u] = __ldg(reinterpret_cast<const uint4*>(lrow + e0));
         }
-        float m = -INFINITY;
-        int bad = 0;
+        float m = u4_max_nan<sizeof(LT)>(w[0]);
 #pragma unroll
-        for (int u = 0; u < kS1Units; ++u) {
-            float x[EPL];
-            unpack_word<LT>(w[u], x);
+        for (int u = 1; u < kS1Units; ++u) m = f_max_nan(m, u4_max_nan<sizeof(LT)>(w[u]));
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) {
-                bad |= bad_logit(x[e]) ? 1 : 0;
-                m = fmaxf(m, x[e]);
-            }
-        }
-        m = warp_max(m);
-        bad = warp_or(bad);
+        for (int o = 16; o > 0; o >>= 1) m = f_max_nan(m, __shfl_xor_sync(0xffffffffu, m, o));
+        const int bad = bad_logit(m) ? 1 : 0;
         const bool live = !bad && m != -INFINITY;
         const float m2 = m * kLog2e;
+        const f2x nm2 = f2_pack(-m2, -m2);
         float tot = 0.0f;
 #pragma unroll
         for (int u = 0; u < kS1Units; ++u) {
             if (u >= upr) break;
             float sum = 0.0f;
-            if (live) {
-                float x[EPL];
-                unpack_word<LT>(w[u], x);
+            if (live) {   // -inf entries add 0
+                const uint32_t a[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+                f2x acc = f2_pack(0.0f, 0.0f);
+                if constexpr (sizeof(LT) == 2) {
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) sum += wexp(x[e], m2);   // -inf entries add 0
+                    for (int q = 0; q < 4; ++q) acc = f2_add(acc, f2_ex2(f2_fma(bf2_widen(a[q]), k2, nm2)));
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 2; ++q)
+                        acc = f2_add(acc, f2_ex2(f2_fma(f2_pack(__uint_as_float(a[2 * q]), __uint_as_float(a[2 * q + 1])),
+                                                        k2, nm2)));
+                }
+                const float2 s2 = f2_unpack(acc);
+                sum = s2.x + s2.y;
             }
 #pragma unroll
             for (int o = LPT >> 1; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
             tot += sum;
             if ((lane & (LPT - 1)) == 0) {
-                const int t = (int)((e_begin + (long)u * UNIT) / kDraftTile) + lane / LPT;
+                const int t = tb + u * TPU + lane / LPT;
                 if (t < te)
                     p.tile_rec[(size_t)row * p.n_tiles + t] =
                         rowacc_pack(RowAcc{live ? m : -INFINITY, live ? sum : 0.0f, 0x7fffffff, bad});
@@ -873,8 +826,15 @@ __device__ bool tile_phase_stream0_t1(const DraftParams& p) {
     return true;
 }
 
+// Pass 0 at T=1 for slices longer than kS1Units units: each warp streams its rows'
+// slices of the CTA's tile range as one flat sequence of units (32 words, one per lane: 256 bf16 or 128 float32 entries, so two
+// tiles or one), with D units' loads in flight per lane in a register ring that runs
+// across row boundaries.  A unit folds on its own: each tile's maximum comes from its
+// own lanes (a NaN or +inf entry shows as a NaN or +inf maximum), then the tile's sum
+// against it.  The tile's first lane writes the tile record and merges it into the
+// row's slice record.  Rows are also requested into L2 a few rows ahead.
 template <typename LT>
-__device__ void tile_phase_stream0(const DraftParams& p) {
+__device__ void stream0_t1_ring(const DraftParams& p) {
     constexpr int EPL = 16 / (int)sizeof(LT);          // entries per lane per unit
     constexpr int UNIT = 32 * EPL;                     // entries per unit
     constexpr int TPU = UNIT / kDraftTile;             // tiles per unit (1 or 2)
@@ -883,69 +843,97 @@ __device__ void tile_phase_stream0(const DraftParams& p) {
     const int R = p.B * p.gamma;
     const int lane = threadIdx.x & 31;
     const int nw = blockDim.x >> 5;
+    const int w0 = (int)(threadIdx.x >> 5);
     const int tb = tile_begin(blockIdx.x, gridDim.x, p.n_tiles), te = tile_begin(blockIdx.x + 1, gridDim.x, p.n_tiles);
     const long e_begin = (long)tb * kDraftTile, e_end = (long)te * kDraftTile;
     const int upr = (int)((e_end - e_begin + UNIT - 1) / UNIT);   // units per row
-    const int my_rows = (R - (int)(threadIdx.x >> 5) + nw - 1) / nw;
+    if (upr == 0) {   // an empty tile range: empty records
+        if (lane == 0)
+            for (int row = w0; row < R; row += nw)
+                p.cta_rec[(size_t)row * gridDim.x + blockIdx.x] = rowacc_pack(rowacc_empty());
+        return;
+    }
+    const LT* L = static_cast<const LT*>(p.logits);
+    const long e_stop = e_end < p.V ? e_end : p.V;
+    const unsigned slice_bytes = e_stop > e_begin ? (unsigned)((e_stop - e_begin) * (long)sizeof(LT)) : 0u;
+    auto prefetch_row = [&](int r) {
+        if (lane == 0 && r < R && slice_bytes > 0) bulk_prefetch_l2(L + (size_t)r * p.V + e_begin, slice_bytes);
+    };
+#pragma unroll
+    for (int a = 0; a < kS1Ahead; ++a) prefetch_row(w0 + a * nw);
+    const uint4 ninf = sizeof(LT) == 2 ? make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u)
+                                       : make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
+    // load cursor (row, unit); rows past R load nothing
+    int lrow = w0, lu = 0;
+    auto load_next = [&]() -> uint4 {
+        uint4 v = ninf;
+        const long e0 = e_begin + (long)lu * UNIT + (long)lane * EPL;
+        if (lrow < R && e0 < e_end && e0 + EPL <= p.V)
+            v = __ldg(reinterpret_cast<const uint4*>(L + (size_t)lrow * p.V + e0));
+        if (++lu == upr) {
+            lu = 0;
+            lrow += nw;
+            prefetch_row(lrow + (kS1Ahead - 1) * nw);
+        }
+        return v;
+    };
+    const int my_rows = w0 < R ? (R - w0 + nw - 1) / nw : 0;
     const int Nu = my_rows * upr;
-    const bool keep_tiles = p.temperature == 1;
-    auto unit_ptr = [&](int u, long& e0) -> const uint4* {
-        const int row = (int)(threadIdx.x >> 5) + (u / upr) * nw;
-        e0 = e_begin + (long)(u % upr) * UNIT + (long)lane * EPL;
-        return reinterpret_cast<const uint4*>(static_cast<const LT*>(p.logits) + (size_t)row * p.V + e0);
-    };
-    auto load_unit = [&](int u) -> uint4 {
-        long e0;
-        const uint4* ptr = unit_ptr(u, e0);
-        if (e0 + EPL <= p.V && e0 < e_end) return __ldg(ptr);
-        return sizeof(LT) == 2 ? make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u)
-                               : make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
-    };
     uint4 ring[D];
 #pragma unroll
-    for (int s = 0; s < D; ++s)
-        if (s < Nu) ring[s] = load_unit(s);
+    for (int s = 0; s < D; ++s) ring[s] = load_next();
+    int crow = w0, cu = 0;   // consume cursor
     RowAcc acc = rowacc_empty();
     for (int u0 = 0; u0 < Nu; u0 += D) {
 #pragma unroll
         for (int s = 0; s < D; ++s) {
-            const int u = u0 + s;
-            if (u < Nu) {
+            if (u0 + s < Nu) {
                 const uint4 w = ring[s];
-                if (u + D < Nu) ring[s] = load_unit(u + D);
-                long e0;
-                unit_ptr(u, e0);
-                RowAcc tr;
-                unit_record<LT>(w, e0, p.V, LPT, tr);
-                const int row = (int)(threadIdx.x >> 5) + (u / upr) * nw;
-                const int t0 = (int)((e0 - lane * EPL) / kDraftTile);   // first tile of the unit
-                // lanes 0..LPT-1 hold the first tile's record, LPT.. the second's
-                RowAcc t1;
-                t1.mx = __shfl_sync(0xffffffffu, tr.mx, LPT % 32);
-                t1.s = __shfl_sync(0xffffffffu, tr.s, LPT % 32);
-                t1.idx = __shfl_sync(0xffffffffu, tr.idx, LPT % 32);
-                t1.bad = __shfl_sync(0xffffffffu, tr.bad, LPT % 32);
-                if (lane == 0) {
-                    if (t0 < te) {
-                        if (keep_tiles) p.tile_rec[(size_t)row * p.n_tiles + t0] = rowacc_pack(tr);
-                        acc = rowacc_merge(acc, tr);
+                ring[s] = load_next();
+                float m = u4_max_nan<sizeof(LT)>(w);
+#pragma unroll
+                for (int o = LPT >> 1; o > 0; o >>= 1) m = f_max_nan(m, __shfl_xor_sync(0xffffffffu, m, o));
+                const bool bad = bad_logit(m);
+                const bool live = !bad && m != -INFINITY;
+                float sum = 0.0f;
+                if (live) {
+                    float x[EPL];
+                    unpack_word<LT>(w, x);
+                    const float m2 = m * kLog2e;
+#pragma unroll
+                    for (int e = 0; e < EPL; ++e) sum += wexp(x[e], m2);   // -inf entries add 0
+                }
+#pragma unroll
+                for (int o = LPT >> 1; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+                const int t = tb + cu * TPU + lane / LPT;
+                if ((lane & (LPT - 1)) == 0 && t < te) {
+                    const RowAcc tr{live ? m : -INFINITY, live ? sum : 0.0f, 0x7fffffff, bad ? 1 : 0};
+                    p.tile_rec[(size_t)crow * p.n_tiles + t] = rowacc_pack(tr);
+                    acc = rowacc_merge(acc, tr);
+                }
+                if (++cu == upr) {
+                    if (TPU == 2) {   // the second tile's lanes hold the odd tiles' part
+                        RowAcc o;
+                        o.mx = __shfl_sync(0xffffffffu, acc.mx, LPT % 32);
+                        o.s = __shfl_sync(0xffffffffu, acc.s, LPT % 32);
+                        o.idx = 0x7fffffff;
+                        o.bad = __shfl_sync(0xffffffffu, acc.bad, LPT % 32);
+                        acc = rowacc_merge(acc, o);
                     }
-                    if (TPU == 2 && t0 + 1 < te) {
-                        if (keep_tiles) p.tile_rec[(size_t)row * p.n_tiles + t0 + 1] = rowacc_pack(t1);
-                        acc = rowacc_merge(acc, t1);
-                    }
-                    if ((u % upr) == upr - 1) {
-                        p.cta_rec[(size_t)row * gridDim.x + blockIdx.x] = rowacc_pack(acc);
-                        acc = rowacc_empty();
-                    }
+                    if (lane == 0) p.cta_rec[(size_t)crow * gridDim.x + blockIdx.x] = rowacc_pack(acc);
+                    acc = rowacc_empty();
+                    cu = 0;
+                    crow += nw;
                 }
             }
         }
     }
-    // rows without units (an empty tile range) still get an empty record
-    if (upr == 0 && lane == 0)
-        for (int row = threadIdx.x >> 5; row < R; row += nw)
-            p.cta_rec[(size_t)row * gridDim.x + blockIdx.x] = rowacc_pack(rowacc_empty());
+}
+
+// Pass 0 at T=1: the per-row form where a slice fits the registers, else the ring.
+template <typename LT>
+__device__ void tile_phase_stream0_t1(const DraftParams& p) {
+    if (!stream0_t1_rows<LT>(p)) stream0_t1_ring<LT>(p);
 }
 
 // T=0 tokens from the folded argmax keys, in every CTA (one load per row): into the

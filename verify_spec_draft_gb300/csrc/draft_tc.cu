@@ -431,8 +431,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     ok = false;
                     break;
                 }
-            } else if (!tile_phase_stream0_t1<LT>(p)) {
-                tile_phase_stream0<LT>(p);
+            } else {
+                tile_phase_stream0_t1<LT>(p);
             }
             if (!grid_barrier(gb, nb, p.status)) { ok = false; break; }
             if (pass == 0 && threadIdx.x == 0) { pre_issued = s_pre; it_p = s_pre; }

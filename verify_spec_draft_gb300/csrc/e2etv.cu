@@ -103,44 +103,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return r;
 }
 
-// Pairs of floats held as one 64-bit register pair, and this architecture's float32x2
-// arithmetic: one instruction rounds both halves exactly as the scalar instruction would.
-typedef unsigned long long f2x;
-__device__ __forceinline__ f2x f2_pack(float lo, float hi) {
-    f2x r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ float2 f2_unpack(f2x v) {
-    float2 r;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
-    return r;
-}
-__device__ __forceinline__ f2x f2_fma(f2x a, f2x b, f2x c) {
-    f2x r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-    return r;
-}
-__device__ __forceinline__ f2x f2_add(f2x a, f2x b) {
-    f2x r;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ f2x f2_mul(f2x a, f2x b) {
-    f2x r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-// The two bf16 values of a 32-bit word, widened (exactly) into a pair.
-__device__ __forceinline__ f2x bf2_widen(uint32_t w) {
-    return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-}
-// (2^x, 2^y) of a pair
-__device__ __forceinline__ f2x f2_ex2(f2x v) {
-    const float2 a = f2_unpack(v);
-    return f2_pack(ex2(a.x), ex2(a.y));
-}
-
 // Rows of one branch: staged in shared memory (stride cols) or read from global.
 struct Rows {
     const bf16_t* tgt;
