@@ -341,19 +341,25 @@ __device__ __forceinline__ void draw_locate(const DraftParams& p, const float4* 
     int cta = -1;
     float tl = INFINITY;
     if (cross) {
+        // lane L's segment (Kc <= 32 records), one record per lane, scanned in one go
         const int L = __ffs(cross) - 1;
-        if (lane == L) {
-            float run = incl - seg;
-            for (int c = c0; c < c1; ++c) {
-                const RowAcc r = rowacc_unpack(__ldcg(&recs[c]));
-                const float w = (r.mx == -INFINITY) ? 0.0f : r.s * ex2(r.mx * kLog2e - M2);
-                if (run + w > thr) { cta = c; tl = thr - run; break; }
-                run += w;
-            }
-            if (cta < 0) cta = c1 - 1;
+        const float before = __shfl_sync(0xffffffffu, incl - seg, L);
+        const int s0 = L * Kc, s1 = min(nblk_tile, s0 + Kc);
+        const int c = s0 + lane;
+        float w = 0.0f;
+        if (c < s1) {
+            const RowAcc r = rowacc_unpack(__ldcg(&recs[c]));
+            if (r.mx != -INFINITY) w = r.s * ex2(r.mx * kLog2e - M2);
         }
-        cta = __shfl_sync(0xffffffffu, cta, L);
-        tl = __shfl_sync(0xffffffffu, tl, L);
+        const float inc = warp_inclusive_scan(w) + before;
+        const unsigned hit = __ballot_sync(0xffffffffu, c < s1 && w > 0.0f && inc > thr);
+        if (hit) {
+            const int H = __ffs(hit) - 1;
+            cta = s0 + H;
+            tl = thr - __shfl_sync(0xffffffffu, inc - w, H);
+        } else {
+            cta = s1 - 1;
+        }
     } else {
         int last = -1;
         for (int c = c0; c < c1; ++c) {
@@ -521,6 +527,12 @@ __device__ void finalize_rows_t1g(const DraftParams& p, int pass, const int32_t*
         const int b = row / p.gamma, j = row % p.gamma;
         const float4* recs = p.cta_rec + (size_t)row * nblk_tile;
         const LT* lrow = static_cast<const LT*>(p.logits) + (size_t)row * p.V;
+        // x_{j-1}'s U row is requested first: its two dependent loads overlap the record
+        // merge and the search
+        const int xp = prev_token(p, prev, row);
+        uint4 uw = make_uint4(0u, 0u, 0u, 0u);
+        if (has && xp >= 0 && xp < p.V)   // a valid row always has a valid previous token
+            uw = __ldg(reinterpret_cast<const uint4*>(U + (size_t)xp * p.r) + lane);
         RowAcc acc = rowacc_empty();
 #pragma unroll 4
         for (int c = lane; c < nblk_tile; c += 32) acc = rowacc_merge(acc, rowacc_unpack(__ldcg(&recs[c])));
@@ -536,14 +548,8 @@ __device__ void finalize_rows_t1g(const DraftParams& p, int pass, const int32_t*
             const long e0 = (long)tile * kDraftTile + gw * EPW;
             const long e1 = e0 + EPW < p.V ? e0 + EPW : p.V;
             if (lane == 0 && e1 > e0) bulk_prefetch_l2(Wt + (size_t)e0 * p.r, (unsigned)((e1 - e0) * p.r * 2));
-            const int xp = prev_token(p, prev, row);
             float uu[8];
             {
-                uint4 uw = make_uint4(0u, 0u, 0u, 0u);
-                if (has && xp >= 0 && xp < p.V)   // a valid row always has a valid previous token
-                    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
-                                 : "=r"(uw.x), "=r"(uw.y), "=r"(uw.z), "=r"(uw.w)
-                                 : "l"(U + (size_t)xp * p.r + lane * 8));
                 const uint32_t a[4] = {uw.x, uw.y, uw.z, uw.w};
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
