@@ -197,3 +197,27 @@ def test_batched_draft_position_path_shapes(spec, B, G, V, r, T):
     assert int(out["passes"].item()) == G
     rows = [0, 1, 127, 128, B // 2, B - 2, B - 1]
     assert _draft_check(out, L, anchor, U, Wt, T, seeds, rows) >= len(rows) * G - 2 * G
+
+
+@pytest.mark.parametrize("T", [0, 1])
+def test_batched_draft_position_path_offset_rows(spec, T):
+    """Drafter rows that start 16 bytes past a 32-byte boundary (a view into a larger
+    buffer), with a vocabulary of whole 32-byte rows: the position path takes its
+    16-byte loads there, and the results are the chain's."""
+    B, G, V, r = 260, 2, 4096, 64
+    L, _ = synth.target_and_draft(B, G - 1, V, "zipf", 0.0, torch.bfloat16, seed=31)
+    L = L[:, :G].contiguous()
+    U, Wt = synth.markov_weights(V, r, torch.bfloat16, seed=31, scale=0.3)
+    anchor = synth.anchors(B, V, seed=31)
+    seeds = synth.seeds_for(B, 5)
+    dev = torch.device("cuda")
+    big = torch.empty(L.numel() + 8, dtype=torch.bfloat16, device=dev)
+    Ld = big[8:].view(B, G, V)
+    Ld.copy_(L.to(dev))
+    assert Ld.data_ptr() % 32 == 16
+    out = vsd.draft_block(Ld, anchor.to(dev), U.to(dev), Wt.to(dev), T, seeds.to(dev))
+    torch.cuda.synchronize()
+    assert vsd.device_status(out["ws"]) == 0
+    assert int(out["passes"].item()) == G
+    rows = [0, 1, 127, 128, 255, 258, 259]
+    assert _draft_check(out, L, anchor, U, Wt, T, seeds, rows) >= len(rows) * G - 2 * G

@@ -54,14 +54,32 @@ __device__ __forceinline__ float fmax_nan_f(float a, float b) {
 // V a multiple of the vector width): LW 16-byte words, -inf past V.
 template <typename LT> struct LWords { static constexpr int N = 32 * (int)sizeof(LT) / 16; };
 
-template <typename LT>
+// L32: the row's bytes are 32-byte aligned and V is a multiple of 32 bytes' worth of
+// entries, so the words come two at a time, one 32-byte load (a whole sector) each.
+template <typename LT, bool L32 = false>
 __device__ __forceinline__ void load_l32(const LT* row, long v0, long V, uint4 (&w)[LWords<LT>::N]) {
     constexpr int N = LWords<LT>::N, EPV = 32 / N;
     const uint32_t ninf = sizeof(LT) == 2 ? 0xff80ff80u : 0xff800000u;
+    if constexpr (L32) {
 #pragma unroll
-    for (int i = 0; i < N; ++i) {
-        const long v = v0 + EPV * i;
-        w[i] = (v + EPV <= V) ? __ldg(reinterpret_cast<const uint4*>(row + v)) : make_uint4(ninf, ninf, ninf, ninf);
+        for (int i = 0; i < N; i += 2) {
+            const long v = v0 + EPV * i;
+            if (v + 2 * EPV <= V) {
+                asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                             : "=r"(w[i].x), "=r"(w[i].y), "=r"(w[i].z), "=r"(w[i].w), "=r"(w[i + 1].x),
+                               "=r"(w[i + 1].y), "=r"(w[i + 1].z), "=r"(w[i + 1].w)
+                             : "l"(row + v));
+            } else {
+                w[i] = make_uint4(ninf, ninf, ninf, ninf);
+                w[i + 1] = w[i];
+            }
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            const long v = v0 + EPV * i;
+            w[i] = (v + EPV <= V) ? __ldg(reinterpret_cast<const uint4*>(row + v)) : make_uint4(ninf, ninf, ninf, ninf);
+        }
     }
 }
 // z[e] += logit e, in place.  PACKED: two entries per float32x2 add (each half rounds

@@ -17,12 +17,15 @@
 //              (128-byte swizzle) into a ring of 32 KB stages, resident while every
 //              M tile of 128 requests passes; per (tile, M tile) the M tile's gathered
 //              U rows (the A operand, r/64 boxes [128 requests x 64 k]) into a ring of
-//              16 KB stages, and an L2 prefetch of its drafter logits over the tile;
+//              16 KB stages (and, for logits rows not 32-byte aligned, an L2 prefetch of
+//              its drafter logits over the tile);
 //     warp 1   tcgen05.mma (M = 128 requests, N = 256 entries, K = 16, bf16 in, f32
 //              accumulate) into two 256-column TMEM accumulators, one per epilogue group;
 //     warps 2-17  epilogue, two groups of 8 warps; group g takes the M tiles mt = g
 //              (mod 2); warp w of a group reads TMEM lane quadrant w % 4 and one 128-entry
-//              half of the tile.  A thread owns one request's row: it adds the logits,
+//              half of the tile.  A thread owns one request's row: it loads the
+//              logits two 32-entry chunks ahead (a 32-byte sector per load when the
+//              rows are 32-byte aligned), adds them,
 //              folds the half-tile's 128 biased logits into the row's record for that
 //              128-entry tile, and into its running record over the CTA's tiles.
 //   draft_pos_draw_kernel   a group of 8 warps per request merges the records and takes
@@ -67,7 +70,8 @@ __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, i
                  : "memory");
 }
 
-template <int TT>
+// L32: the logits rows are 32-byte aligned (loaded a sector at a time)
+template <int TT, bool L32>
 __global__ void __launch_bounds__(kPosThreads, 1)
     draft_pos_tiles_kernel(const __grid_constant__ DraftParams p, const __grid_constant__ PosExtra e,
                            const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap umap,
@@ -124,9 +128,12 @@ __global__ void __launch_bounds__(kPosThreads, 1)
                         ++iw;
                     }
                 for (int mt = 0; mt < nM && ok; ++mt) {
-                    // the epilogue reads this M tile's logits over the tile from L2
-                    tma_prefetch_2d(&lmap, T * kPosN, mt * 128);
-                    tma_prefetch_2d(&lmap, T * kPosN + 128, mt * 128);
+                    // with 16-byte loads the epilogue reads this M tile's logits over the
+                    // tile from L2; its 32-byte loads ran faster without the prefetch
+                    if constexpr (!L32) {
+                        tma_prefetch_2d(&lmap, T * kPosN, mt * 128);
+                        tma_prefetch_2d(&lmap, T * kPosN + 128, mt * 128);
+                    }
                     for (int kb = 0; kb < KB && ok; ++kb) {
                         const uint32_t s = ia % kPosAStages, ph = (ia / kPosAStages) & 1u;
                         ok = mbar_wait(&s_aempty[s], ph ^ 1u, p.status, kWaitLimitNs);
@@ -204,8 +211,8 @@ __global__ void __launch_bounds__(kPosThreads, 1)
         };
         // the first pair's first two chunks
         if (tb < te && ((live & 1u) != 0u) && 2 * tb + h < p.n_tiles) {
-            load_l32<bf16_t>(pair_lrow(0), (long)(2 * tb + h) * kDraftTile, p.V, w0);
-            load_l32<bf16_t>(pair_lrow(0), (long)(2 * tb + h) * kDraftTile + 32, p.V, w1);
+            load_l32<bf16_t, L32>(pair_lrow(0), (long)(2 * tb + h) * kDraftTile, p.V, w0);
+            load_l32<bf16_t, L32>(pair_lrow(0), (long)(2 * tb + h) * kDraftTile + 32, p.V, w1);
         }
         for (int T = tb; T < te && ok; ++T) {
             const int t = 2 * T + h;      // the 128-entry tile of this half
@@ -236,11 +243,11 @@ __global__ void __launch_bounds__(kPosThreads, 1)
                     if (lv) {
                         if (ch & 1) add_l32<bf16_t, false>(w1, z);
                         else add_l32<bf16_t, false>(w0, z);
-                        if (ch == 0) load_l32<bf16_t>(lrow, v0 + 64, p.V, w0);
-                        if (ch == 1) load_l32<bf16_t>(lrow, v0 + 96, p.V, w1);
+                        if (ch == 0) load_l32<bf16_t, L32>(lrow, v0 + 64, p.V, w0);
+                        if (ch == 1) load_l32<bf16_t, L32>(lrow, v0 + 96, p.V, w1);
                     }
-                    if (ch == 2 && nlv) load_l32<bf16_t>(nlrow, nv0, p.V, w0);
-                    if (ch == 3 && nlv) load_l32<bf16_t>(nlrow, nv0 + 32, p.V, w1);
+                    if (ch == 2 && nlv) load_l32<bf16_t, L32>(nlrow, nv0, p.V, w0);
+                    if (ch == 3 && nlv) load_l32<bf16_t, L32>(nlrow, nv0 + 32, p.V, w1);
                     if (lv) {
                         const float run_mx = fmaxf(run[i].mx, rec.mx);
                         rec = rowacc_merge(rec, record32<false>(z, (int)(v0 + 32 * ch), run_mx, TT == 0));
@@ -503,7 +510,9 @@ static cudaError_t pos_launch_slice(const DraftParams& q, PosExtra e, cudaStream
     const int KB = q.r / kPosK;
     (void)KB;
     const size_t smem = 1024 + (size_t)kPosWStages * kPosWBlock + (size_t)kPosAStages * kPosABlock;
-    auto tiles = draft_pos_tiles_kernel<TT>;
+    // 32-byte loads of the logits when every row of every position starts on 32 bytes
+    const bool l32 = (reinterpret_cast<uintptr_t>(q.logits) & 31u) == 0 && ((size_t)q.V * 2) % 32 == 0;
+    auto tiles = l32 ? draft_pos_tiles_kernel<TT, true> : draft_pos_tiles_kernel<TT, false>;
     cudaError_t err = cudaFuncSetAttribute(tiles, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     CUtensorMap wmap, umap;
