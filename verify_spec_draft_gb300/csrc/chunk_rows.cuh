@@ -33,6 +33,13 @@ __device__ __forceinline__ uint4 partial_words(const bf16_t* row, long e0, long 
     return make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
 }
 
+// Two 16-byte words at p (32-byte aligned) in one load: a whole 32-byte sector.
+__device__ __forceinline__ void ld_sector(const void* p, uint4& a, uint4& b) {
+    asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+                 : "l"(p));
+}
+
 template <typename T, int NW>
 __device__ __forceinline__ void load_words(uint4 (&w)[NW], const T* row, long V, long base, bool vec_ok) {
     constexpr int EPV = 16 / (int)sizeof(T);
@@ -68,6 +75,32 @@ __device__ __forceinline__ void load_words_il(uint4 (&w)[NW], const T* row, long
             const long e0 = il_entry(seg, 8 * j) + h * EPV;
             if (vec_ok && e0 + EPV <= V) w[j * WPG + h] = __ldg(reinterpret_cast<const uint4*>(row + e0));
             else w[j * WPG + h] = partial_words(row, e0, V);
+        }
+    }
+}
+
+// The sector-interleaved layout, for rows that start on 32 bytes: lane l of warp w holds
+// the 32-byte groups j * 32 + l (j < NW / 2) of the warp's 1024-entry segment, 16 bf16
+// or 8 float32 entries each, one load per group, so each load instruction of a warp
+// reads 1 KB contiguous.  Decoded entry k is entry seg + ((k / E) * 32 + l) * E + k % E
+// with E = 32 / sizeof(T); for float32 rows this is the group-interleaved layout.
+template <typename T>
+__device__ __forceinline__ long il32_entry(long seg, int k) {
+    constexpr int E = 32 / (int)sizeof(T);
+    return seg + (long)((k / E) * 32 + (int)(threadIdx.x & 31)) * E + (k % E);
+}
+template <typename T, int NW>
+__device__ __forceinline__ void load_words_il32(uint4 (&w)[NW], const T* row, long V, long seg) {
+    constexpr int E = 32 / (int)sizeof(T);
+    const uint32_t ninf = sizeof(T) == 2 ? 0xff80ff80u : 0xff800000u;
+#pragma unroll
+    for (int j = 0; j < NW / 2; ++j) {
+        const long e0 = il32_entry<T>(seg, j * E);
+        if (e0 + E <= V) {
+            ld_sector(row + e0, w[2 * j], w[2 * j + 1]);
+        } else {   // the row's last group: whole words up to V (V is a multiple of E here)
+            w[2 * j] = make_uint4(ninf, ninf, ninf, ninf);
+            w[2 * j + 1] = w[2 * j];
         }
     }
 }

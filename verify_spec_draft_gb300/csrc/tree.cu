@@ -17,7 +17,8 @@
 //
 // Verification (T=0): HBM-bound.  A persistent grid streams the root row and every kept
 // node's row in 8192-entry items (the items of dropped nodes are compacted away, 256 at
-// a time), two items of 16-byte loads in flight per thread.  Each warp folds its
+// a time), two items of loads in flight per thread (32-byte loads where the rows start
+// on 32 bytes, 16-byte ones otherwise).  Each warp folds its
 // 1024-entry segment of an item into the row's 64-bit argmax key (value, lowest index)
 // with one atomicMax, so warps never wait for one another.  The last CTA to finish then
 // marks, for every node in parallel, whether its token is the argmax of its parent's row
@@ -132,10 +133,10 @@ __device__ __forceinline__ bool tv_item(const TreeVerifyParams& p, long it, unsi
     return node < 0 || !p.keep || p.keep[(size_t)t * p.n_nodes + node] != 0;
 }
 
-// One warp's 1024 entries of an item (group-interleaved): fold them into the row's
+// One warp's 1024 entries of an item (group- or sector-interleaved): fold them into the row's
 // argmax key (or its bad flag) with one atomic per warp, so warps never wait for one
 // another.  Only the lanes holding the maximum look for its lowest index.
-template <typename TT, int NW>
+template <typename TT, int NW, bool L32>
 __device__ __forceinline__ void tv_fold(const TreeVerifyParams& p, const uint4 (&w)[NW], long row, int c) {
     const float lm = chunk_max_nan<TT, NW>(w);
     const float m = warp_max_nan(lm);
@@ -143,7 +144,7 @@ __device__ __forceinline__ void tv_fold(const TreeVerifyParams& p, const uint4 (
     int idx = 0x7fffffff;
     if (!bad && lm == m) {
         const int k = first_equal<TT, NW>(w, m);
-        if (k >= 0) idx = (int)il_entry(il_seg(c), k);
+        if (k >= 0) idx = (int)(L32 ? il32_entry<TT>(il_seg(c), k) : il_entry(il_seg(c), k));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) idx = min(idx, __shfl_xor_sync(0xffffffffu, idx, o));
@@ -156,7 +157,9 @@ __device__ __forceinline__ void tv_fold(const TreeVerifyParams& p, const uint4 (
 // D items of loads in flight per thread (the one being reduced included).
 template <typename TT> struct TvDepth { static constexpr int D = sizeof(TT) == 2 ? TV_DEPTH_BF16 : 2; };
 
-template <typename TT>
+// L32: the target rows start on 32 bytes and hold whole 32-byte groups, so the chunks
+// are read in the sector-interleaved layout, one 32-byte load per group.
+template <typename TT, bool L32>
 __global__ void __launch_bounds__(kTvThreads) tree_verify_kernel(TreeVerifyParams p) {
     const TT* target = static_cast<const TT*>(p.target);
     const long V = p.V;
@@ -208,7 +211,8 @@ __global__ void __launch_bounds__(kTvThreads) tree_verify_kernel(TreeVerifyParam
             if (d < cnt) {
                 rows[d] = s_row[d];
                 cs[d] = s_c[d];
-                load_words_il<TT, NW>(buf[d], target + (size_t)rows[d] * V, V, il_seg(cs[d]), vec);
+                if constexpr (L32) load_words_il32<TT, NW>(buf[d], target + (size_t)rows[d] * V, V, il_seg(cs[d]));
+                else load_words_il<TT, NW>(buf[d], target + (size_t)rows[d] * V, V, il_seg(cs[d]), vec);
             }
         for (int j0 = 0; j0 < cnt; j0 += D) {
 #pragma unroll
@@ -218,9 +222,11 @@ __global__ void __launch_bounds__(kTvThreads) tree_verify_kernel(TreeVerifyParam
                 if (jn < cnt) {
                     rows[dn] = s_row[jn];
                     cs[dn] = s_c[jn];
-                    load_words_il<TT, NW>(buf[dn], target + (size_t)rows[dn] * V, V, il_seg(cs[dn]), vec);
+                    if constexpr (L32)
+                        load_words_il32<TT, NW>(buf[dn], target + (size_t)rows[dn] * V, V, il_seg(cs[dn]));
+                    else load_words_il<TT, NW>(buf[dn], target + (size_t)rows[dn] * V, V, il_seg(cs[dn]), vec);
                 }
-                if (j < cnt) tv_fold<TT, NW>(p, buf[d], rows[d], cs[d]);
+                if (j < cnt) tv_fold<TT, NW, L32>(p, buf[d], rows[d], cs[d]);
             }
         }
         __syncthreads();   // s_row and s_c are rewritten by the next batch
@@ -319,7 +325,12 @@ cudaError_t tree_verify_launch(TreeVerifyParams& p, void* ws, cudaStream_t strea
     off = align_up(off + sizeof(unsigned) * rows, 256);
     p.treebad = reinterpret_cast<unsigned*>(w + off);
 
-    void (*k)(TreeVerifyParams) = p.tdt == SPEC_BF16 ? tree_verify_kernel<bf16_t> : tree_verify_kernel<float>;
+    // rows that start on 32 bytes and hold whole 32-byte groups: the sector layout
+    const size_t esize = p.tdt == SPEC_BF16 ? 2 : 4;
+    const bool l32 = p.vec_t && (reinterpret_cast<uintptr_t>(p.target) & 31u) == 0 && ((size_t)p.V * esize) % 32 == 0;
+    void (*k)(TreeVerifyParams) =
+        p.tdt == SPEC_BF16 ? (l32 ? tree_verify_kernel<bf16_t, true> : tree_verify_kernel<bf16_t, false>)
+                           : (l32 ? tree_verify_kernel<float, true> : tree_verify_kernel<float, false>);
     int occ = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, kTvThreads, 0) != cudaSuccess || occ < 1) occ = 1;
     const long nch = ((long)p.V + kTvChunk - 1) / kTvChunk;
