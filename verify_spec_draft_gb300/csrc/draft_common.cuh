@@ -82,35 +82,27 @@ __device__ __forceinline__ void load_l32(const LT* row, long v0, long V, uint4 (
         }
     }
 }
-// z[e] += logit e, in place.  PACKED: two entries per float32x2 add (each half rounds
-// as the scalar add would); the same results either way, and each kernel takes the
-// form that measured faster in it.
-template <bool PACKED>
+// z[e] += logit e, in place, two entries per float32x2 add (each half rounds as the
+// scalar add would)
 __device__ __forceinline__ void add_pair(float& z0, float& z1, f2x l) {
-    if constexpr (PACKED) {
-        const float2 r = f2_unpack(f2_add(f2_pack(z0, z1), l));
-        z0 = r.x;
-        z1 = r.y;
-    } else {
-        const float2 a = f2_unpack(l);
-        z0 += a.x;
-        z1 += a.y;
-    }
+    const float2 r = f2_unpack(f2_add(f2_pack(z0, z1), l));
+    z0 = r.x;
+    z1 = r.y;
 }
-template <typename LT, bool PACKED = true>
+template <typename LT>
 __device__ __forceinline__ void add_l32(const uint4 (&w)[LWords<LT>::N], float (&z)[32]) {
     if (sizeof(LT) == 2) {
 #pragma unroll
         for (int i = 0; i < LWords<LT>::N; ++i) {
             const uint32_t a[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
 #pragma unroll
-            for (int k = 0; k < 4; ++k) add_pair<PACKED>(z[(8 * i + 2 * k) & 31], z[(8 * i + 2 * k + 1) & 31], bf2_widen(a[k]));
+            for (int k = 0; k < 4; ++k) add_pair(z[(8 * i + 2 * k) & 31], z[(8 * i + 2 * k + 1) & 31], bf2_widen(a[k]));
         }
     } else {
 #pragma unroll
         for (int i = 0; i < LWords<LT>::N; ++i) {
-            add_pair<PACKED>(z[(4 * i) & 31], z[(4 * i + 1) & 31], f2_pack(__uint_as_float(w[i].x), __uint_as_float(w[i].y)));
-            add_pair<PACKED>(z[(4 * i + 2) & 31], z[(4 * i + 3) & 31], f2_pack(__uint_as_float(w[i].z), __uint_as_float(w[i].w)));
+            add_pair(z[(4 * i) & 31], z[(4 * i + 1) & 31], f2_pack(__uint_as_float(w[i].x), __uint_as_float(w[i].y)));
+            add_pair(z[(4 * i + 2) & 31], z[(4 * i + 3) & 31], f2_pack(__uint_as_float(w[i].z), __uint_as_float(w[i].w)));
         }
     }
 }
@@ -119,27 +111,18 @@ __device__ __forceinline__ void add_l32(const uint4 (&w)[LWords<LT>::N], float (
 // of the maximum is needed only when this chunk raises the running maximum `run_mx`
 // (entries are visited in increasing order, so on a tie the earlier index stands);
 // `want_idx` is false when no argmax is used (T=1).
-// The sum keeps the even and the odd entries apart, each in increasing order, and adds
-// the two at the end.  PACKED: the maximum is a tree of NaN-propagating maxima (exact in
-// any order) and the two sums are the halves of a float32x2 accumulator; the results
-// are the same either way.
-template <bool PACKED = true>
+// The maximum is a tree of NaN-propagating maxima (exact in any order); the sum keeps
+// the even and the odd entries in the two halves of a float32x2 accumulator, each in
+// increasing order, and adds the halves at the end.
 __device__ __forceinline__ RowAcc record32(const float (&z)[32], int v0, float run_mx, bool want_idx) {
-    float m;
-    if constexpr (PACKED) {
-        float t[16];
+    float t[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) t[e] = fmax_nan_f(z[2 * e], z[2 * e + 1]);
+    for (int e = 0; e < 16; ++e) t[e] = fmax_nan_f(z[2 * e], z[2 * e + 1]);
 #pragma unroll
-        for (int w = 8; w > 0; w >>= 1)
+    for (int w = 8; w > 0; w >>= 1)
 #pragma unroll
-            for (int e = 0; e < w; ++e) t[e] = fmax_nan_f(t[e], t[e + w]);
-        m = t[0];
-    } else {
-        m = z[0];
-#pragma unroll
-        for (int e = 1; e < 32; ++e) m = fmax_nan_f(m, z[e]);
-    }
+        for (int e = 0; e < w; ++e) t[e] = fmax_nan_f(t[e], t[e + w]);
+    const float m = t[0];
     RowAcc r;
     r.bad = (isnan(m) || m == INFINITY) ? 1 : 0;
     r.mx = r.bad ? -INFINITY : m;
@@ -147,19 +130,12 @@ __device__ __forceinline__ RowAcc record32(const float (&z)[32], int v0, float r
     r.idx = 0x7fffffff;
     if (!r.bad && m != -INFINITY) {
         const float m2 = m * kLog2e;
-        if constexpr (PACKED) {
-            const f2x k2 = f2_pack(kLog2e, kLog2e), nm2 = f2_pack(-m2, -m2);
-            f2x acc = f2_pack(0.0f, 0.0f);
+        const f2x k2 = f2_pack(kLog2e, kLog2e), nm2 = f2_pack(-m2, -m2);
+        f2x acc = f2_pack(0.0f, 0.0f);
 #pragma unroll
-            for (int e = 0; e < 32; e += 2) acc = f2_add(acc, f2_ex2(f2_fma(f2_pack(z[e], z[e + 1]), k2, nm2)));
-            const float2 s2 = f2_unpack(acc);
-            r.s = s2.x + s2.y;
-        } else {
-            float s0 = 0.0f, s1 = 0.0f;
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) { s0 += wexp(z[e], m2); s1 += wexp(z[e + 1], m2); }
-            r.s = s0 + s1;
-        }
+        for (int e = 0; e < 32; e += 2) acc = f2_add(acc, f2_ex2(f2_fma(f2_pack(z[e], z[e + 1]), k2, nm2)));
+        const float2 s2 = f2_unpack(acc);
+        r.s = s2.x + s2.y;
         if (want_idx && m > run_mx) {
 #pragma unroll
             for (int e = 31; e >= 0; --e)

@@ -241,8 +241,8 @@ __global__ void __launch_bounds__(kPosThreads, 1)
                 for (int ch = 0; ch < 4; ++ch) {
                     tmem_ld32(ta + 32 * ch, z);
                     if (lv) {
-                        if (ch & 1) add_l32<bf16_t, false>(w1, z);
-                        else add_l32<bf16_t, false>(w0, z);
+                        if (ch & 1) add_l32<bf16_t>(w1, z);
+                        else add_l32<bf16_t>(w0, z);
                         if (ch == 0) load_l32<bf16_t, L32>(lrow, v0 + 64, p.V, w0);
                         if (ch == 1) load_l32<bf16_t, L32>(lrow, v0 + 96, p.V, w1);
                     }
@@ -250,7 +250,7 @@ __global__ void __launch_bounds__(kPosThreads, 1)
                     if (ch == 3 && nlv) load_l32<bf16_t, L32>(nlrow, nv0 + 32, p.V, w1);
                     if (lv) {
                         const float run_mx = fmaxf(run[i].mx, rec.mx);
-                        rec = rowacc_merge(rec, record32<false>(z, (int)(v0 + 32 * ch), run_mx, TT == 0));
+                        rec = rowacc_merge(rec, record32(z, (int)(v0 + 32 * ch), run_mx, TT == 0));
                     }
                 }
                 tc_fence_before();
