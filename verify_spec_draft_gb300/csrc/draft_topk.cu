@@ -512,28 +512,65 @@ __global__ void __launch_bounds__(kDkThreads, 1)
                 ++ie;
                 const long v = (long)t * kDtTile + vl;
                 const bool in = v < p.V;
+                if (!in) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) z[i] = -INFINITY;
+                }
+                // a NaN or +inf entry ends its request (one OR over the warp for all 8)
+                unsigned bl = 0u;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) bl |= bad_logit(z[i]) ? 1u << i : 0u;
+                badm |= __reduce_or_sync(0xffffffffu, bl) & live;
+                // the quadrant's 8 maxima at once: at the xor-16, -8 and -4 steps each lane
+                // keeps half of its values, so lanes 4r .. 4r+3 end with request r's
+                float h4[4], h2[2], h1;
+                {
+                    const bool up = (lane & 16) != 0;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float give = up ? z[j] : z[j + 4], keep = up ? z[j + 4] : z[j];
+                        h4[j] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, give, 16));
+                    }
+                }
+                {
+                    const bool up = (lane & 8) != 0;
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const float give = up ? h4[j] : h4[j + 2], keep = up ? h4[j + 2] : h4[j];
+                        h2[j] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, give, 8));
+                    }
+                }
+                {
+                    const bool up = (lane & 4) != 0;
+                    const float give = up ? h2[0] : h2[1], keep = up ? h2[1] : h2[0];
+                    h1 = fmaxf(keep, __shfl_xor_sync(0xffffffffu, give, 4));
+                }
+                h1 = fmaxf(h1, __shfl_xor_sync(0xffffffffu, h1, 2));
+                h1 = fmaxf(h1, __shfl_xor_sync(0xffffffffu, h1, 1));
+                const int ri = lane >> 2;   // the request whose maximum this lane holds
+                unsigned my_hit = 0u;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     if (!((live >> i) & 1u) || ((badm >> i) & 1u)) continue;   // warp-uniform
                     const int b = b0 + 8 * g + i;
-                    const float zi = in ? z[i] : -INFINITY;
-                    if (__any_sync(0xffffffffu, in && bad_logit(zi))) { badm |= 1u << i; continue; }
-                    // the quadrant's largest entry and its lowest index: the tile's key
-                    const float m = warp_max(zi);
-                    const unsigned hit = __ballot_sync(0xffffffffu, in && zi == m);
-                    if (lane == 0 && hit)
-                        atomicMax(&p.tmax[(size_t)b * p.n_tiles + t],
-                                  argmax_key(m, (uint32_t)((long)t * kDtTile + 32 * q + __ffs(hit) - 1)));
+                    const float m = __shfl_sync(0xffffffffu, h1, 4 * i);
+                    // the lowest index of the maximum: the tile's key, folded below by lane 4i
+                    const unsigned hit = __ballot_sync(0xffffffffu, in && z[i] == m);
+                    if (ri == i) my_hit = hit;
                     const float tm2 = m * kLog2e;
                     if (tm2 > m2[i]) {
                         sl[i] *= ex2(m2[i] - tm2);
                         m2[i] = tm2;
                     }
                     if (in) {
-                        if (m2[i] != -INFINITY) sl[i] += wexp(zi, m2[i]);
-                        p.zbuf[(size_t)b * p.ldzb + v] = zi;
+                        if (m2[i] != -INFINITY) sl[i] += wexp(z[i], m2[i]);
+                        p.zbuf[(size_t)b * p.ldzb + v] = z[i];
                     }
                 }
+                // the tile keys of the live requests: one atomic instruction, lanes 4i
+                if ((lane & 3) == 0 && my_hit != 0u && ((live >> ri) & 1u) && !((badm >> ri) & 1u))
+                    atomicMax(&p.tmax[(size_t)(b0 + 8 * g + ri) * p.n_tiles + t],
+                              argmax_key(h1, (uint32_t)((long)t * kDtTile + 32 * q + __ffs(my_hit) - 1)));
             }
             if (!ok) { s_fail = 1; break; }
             // one record per (request, CTA, quadrant)
