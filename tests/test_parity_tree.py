@@ -51,6 +51,7 @@ def _compare_verify(out, ref):
 @pytest.mark.parametrize("T,n,V,dtype,shape", [
     (4, 12, 1000, torch.float32, "bushy"),
     (6, 40, 20001, torch.bfloat16, "bushy"),     # V % 8 != 0: scalar loads, ragged chunk
+    (4, 12, 1000, torch.bfloat16, "bushy"),      # rows of 16-byte words but not 32-byte ones
     (3, 30, 9000, torch.float32, "chain"),
     (2, 1024, 64, torch.bfloat16, "bushy"),      # the most nodes per tree
     (5, 1, 8192, torch.bfloat16, "chain"),       # one node, exactly one chunk
