@@ -108,11 +108,12 @@ __global__ void __launch_bounds__(kPosThreads, 1)
 
     if (warp == 0) {
         if (lane == 0) {
+            const uint64_t pol = l2_evict_first_policy();   // Wt is streamed once per position
             // the first tile's weights depend on nothing: requested before the wait for
             // the previous position's draw, which writes the U rows
             for (int kb = 0; kb < KB; ++kb) {
                 mbar_arrive_expect_tx(&s_wfull[kb], kPosWBlock);
-                tma_load_2d(s_w + (size_t)kb * kPosWBlock, &wmap, kb * kPosK, tb * kPosN, &s_wfull[kb]);
+                tma_load_2d_hint(s_w + (size_t)kb * kPosWBlock, &wmap, kb * kPosK, tb * kPosN, &s_wfull[kb], pol);
             }
             iw = (uint32_t)KB;
             pdl_wait_primary();
@@ -124,7 +125,7 @@ __global__ void __launch_bounds__(kPosThreads, 1)
                         ok = mbar_wait(&s_wempty[s], ph ^ 1u, p.status, kWaitLimitNs);
                         if (!ok) break;
                         mbar_arrive_expect_tx(&s_wfull[s], kPosWBlock);
-                        tma_load_2d(s_w + (size_t)s * kPosWBlock, &wmap, kb * kPosK, T * kPosN, &s_wfull[s]);
+                        tma_load_2d_hint(s_w + (size_t)s * kPosWBlock, &wmap, kb * kPosK, T * kPosN, &s_wfull[s], pol);
                         ++iw;
                     }
                 for (int mt = 0; mt < nM && ok; ++mt) {

@@ -150,6 +150,7 @@ __device__ bool tc_tile_phase(const DraftParams& p, const CUtensorMap* tmap, con
     constexpr int S = TcStages<MT, TT>::N;
     if (warp == 0) {
         if (lane == 0) {
+            const uint64_t pol = l2_evict_first_policy();   // Wt is streamed once per pass
             uint32_t skip = pre_issued;   // stages of this pass already in flight
             pre_issued = 0;
             for (int t = tb; t < te && !*(volatile int*)&s_fail; ++t) {
@@ -158,7 +159,7 @@ __device__ bool tc_tile_phase(const DraftParams& p, const CUtensorMap* tmap, con
                     const uint32_t s = it_p % S, ph = (it_p / S) & 1u;
                     if (!mbar_wait(&sh.empty[s], ph ^ 1u, p.status, kWaitLimitNs)) { s_fail = 1; break; }
                     mbar_arrive_expect_tx(&sh.full[s], kTcBlock);
-                    tma_load_2d(sh.b + (size_t)s * kTcBlock, tmap, kb * kTcK, t * kTcN, &sh.full[s]);
+                    tma_load_2d_hint(sh.b + (size_t)s * kTcBlock, tmap, kb * kTcK, t * kTcN, &sh.full[s], pol);
                     ++it_p;
                 }
             }
@@ -349,10 +350,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int te = tile_begin(blockIdx.x + 1, gridDim.x, p.n_tiles);
             const uint32_t total = (uint32_t)(te - tb) * (uint32_t)KB;
             const uint32_t n = total < (uint32_t)S ? total : (uint32_t)S;
+            const uint64_t pol = l2_evict_first_policy();
             for (uint32_t i = 0; i < n; ++i) {
                 mbar_arrive_expect_tx(&sh.full[i], kTcBlock);
-                tma_load_2d(sh.b + (size_t)i * kTcBlock, &tmap, (int)(i % KB) * kTcK, (tb + (int)(i / KB)) * kTcN,
-                            &sh.full[i]);
+                tma_load_2d_hint(sh.b + (size_t)i * kTcBlock, &tmap, (int)(i % KB) * kTcK, (tb + (int)(i / KB)) * kTcN,
+                                 &sh.full[i], pol);
             }
             s_pre = n;
         }

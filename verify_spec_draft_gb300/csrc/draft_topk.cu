@@ -394,6 +394,7 @@ __global__ void __launch_bounds__(kDkThreads, 1)
     if (warp == 0) {
         // neither the weights nor the logits depend on the previous kernel: no wait
         if (lane == 0) {
+            const uint64_t pol = l2_evict_first_policy();   // Wt and the logits are streamed once
             for (int ch = 0; ch < nchunks && !*(volatile int*)&s_fail; ++ch)
                 for (int t = tb; t < te; ++t) {
                     bool ok = true;
@@ -402,7 +403,7 @@ __global__ void __launch_bounds__(kDkThreads, 1)
                         ok = mbar_wait(&s_empty[s], ph ^ 1u, p.status, kWaitLimitNs);
                         if (!ok) break;
                         mbar_arrive_expect_tx(&s_full[s], kDkWBlock);
-                        tma_load_2d(s_w + (size_t)s * kDkWBlock, &wmap, kb * kDkK, t * kDtTile, &s_full[s]);
+                        tma_load_2d_hint(s_w + (size_t)s * kDkWBlock, &wmap, kb * kDkK, t * kDtTile, &s_full[s], pol);
                         ++iw;
                     }
                     if (ok) {
@@ -410,7 +411,7 @@ __global__ void __launch_bounds__(kDkThreads, 1)
                         ok = mbar_wait(&s_lempty[s], ph ^ 1u, p.status, kWaitLimitNs);
                         if (ok) {
                             mbar_arrive_expect_tx(&s_lfull[s], LBYTES);
-                            tma_load_2d(s_l + (size_t)s * LBYTES, &lmap, t * kDtTile, ch * kDtChunk, &s_lfull[s]);
+                            tma_load_2d_hint(s_l + (size_t)s * LBYTES, &lmap, t * kDtTile, ch * kDtChunk, &s_lfull[s], pol);
                             ++il;
                         }
                     }

@@ -259,7 +259,7 @@ static_assert(2 * 8 * kV1StagesBf16 + 16 * kV1StagesBf16 <= kV1RingOffset, "ring
 
 template <typename TT, typename DT>
 __device__ __forceinline__ void issue_item1(const VerifyParams& p, long it, uint8_t* dst, uint64_t* bar,
-                                            int4* slot) {
+                                            int4* slot, uint64_t pol) {
     const Item1 q = item1(p, it);
     const int G = p.gamma;
     const long e0 = (long)q.c * kVerifyChunk;
@@ -275,7 +275,7 @@ __device__ __forceinline__ void issue_item1(const VerifyParams& p, long it, uint
     }
     *slot = make_int4(q.b, q.lr, q.c, (int)n);   // published to the consumers by the barrier phase
     mbar_arrive_expect_tx(bar, bytes);
-    bulk_g2s(dst, src, bytes, bar);
+    bulk_g2s_hint(dst, src, bytes, bar, pol);   // each chunk is read once here
 }
 
 // This warp's 1024-entry segment of a staged chunk as 32 entries per lane (lane-
@@ -301,9 +301,11 @@ __device__ __forceinline__ void phase_stats_staged(const VerifyParams& p, uint8_
     const long items = (long)(2 * p.gamma + 1) * p.nchunk * p.B;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long mine = items > (long)blockIdx.x ? (items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const uint64_t pol = l2_evict_first_policy();
     if (threadIdx.x == 0)
         for (long k = 0; k < S && k < mine; ++k)
-            issue_item1<TT, DT>(p, blockIdx.x + k * gridDim.x, ring + (size_t)k * stage_bytes, &full[k], &s_item[k]);
+            issue_item1<TT, DT>(p, blockIdx.x + k * gridDim.x, ring + (size_t)k * stage_bytes, &full[k], &s_item[k],
+                                pol);
     for (long k = 0; k < mine; ++k) {
         const int s = (int)(k % S);
         if (threadIdx.x == 0 && k >= 1 && k - 1 + S < mine) {
@@ -312,7 +314,7 @@ __device__ __forceinline__ void phase_stats_staged(const VerifyParams& p, uint8_
             mbar_wait(&empty[sp], (unsigned)(((k - 1) / S) & 1), p.status, kV1WaitNs);
             fence_proxy_async_smem();
             issue_item1<TT, DT>(p, blockIdx.x + (k - 1 + S) * gridDim.x, ring + (size_t)sp * stage_bytes, &full[sp],
-                                &s_item[sp]);
+                                &s_item[sp], pol);
         }
         const uint8_t* stage = ring + (size_t)s * stage_bytes;
         mbar_wait(&full[s], (unsigned)((k / S) & 1), p.status, kV1WaitNs);
