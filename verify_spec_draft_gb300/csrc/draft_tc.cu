@@ -97,6 +97,19 @@ __device__ bool tc_tile_phase(const DraftParams& p, const CUtensorMap* tmap, con
     // T=1 from the second biased pass on: only the rows flagged in act are recomputed
     auto live = [&](int n) { return TT == 1 && act != nullptr ? act[n] != 0 : true; };
 
+    const int tb = tile_begin(blockIdx.x, gridDim.x, p.n_tiles), te = tile_begin(blockIdx.x + 1, gridDim.x, p.n_tiles);
+    // the epilogue's first tile of logits depends on no token: requested before the gather,
+    // so the two round trips overlap
+    uint4 lw[NCH][LW];
+    if (warp >= 2) {
+        const int q = warp & 3, g4 = (warp - 2) >> 2;
+        const int g = row_of(g4 / EW, q, lane, MT);
+        if (g < R && live(g) && tb < te) {
+            const LT* lrow = static_cast<const LT*>(p.logits) + (size_t)g * p.V;
+#pragma unroll
+            for (int c = 0; c < NCH; ++c) load_l32<LT>(lrow, (long)tb * kTcN + (g4 % EW) * CPW + 32 * c, p.V, lw[c]);
+        }
+    }
     // gather A = U[x_prev(n)] for the padded rows, 128-byte swizzled, K-major
     if (threadIdx.x == 0) s_fail = 0;
     __shared__ int s_xp[TT == 1 ? 256 : 1];   // T=1: x_prev of every row (R <= 256)
@@ -146,7 +159,6 @@ __device__ bool tc_tile_phase(const DraftParams& p, const CUtensorMap* tmap, con
     fence_proxy_async_smem();
     __syncthreads();
 
-    const int tb = tile_begin(blockIdx.x, gridDim.x, p.n_tiles), te = tile_begin(blockIdx.x + 1, gridDim.x, p.n_tiles);
     constexpr int S = TcStages<MT, TT>::N;
     if (warp == 0) {
         if (lane == 0) {
@@ -212,11 +224,6 @@ __device__ bool tc_tile_phase(const DraftParams& p, const CUtensorMap* tmap, con
         RowAcc run = rowacc_empty();
         // logits of this warp's columns of tile t, chunk c of tile t+1 requested as soon
         // as chunk c of tile t is consumed
-        uint4 lw[NCH][LW];
-        if (mine && tb < te) {
-#pragma unroll
-            for (int c = 0; c < NCH; ++c) load_l32<LT>(lrow, (long)tb * kTcN + col0 + 32 * c, p.V, lw[c]);
-        }
         for (int t = tb; t < te; ++t) {
             const uint32_t buf = jt_e % NB, jph = (jt_e / NB) & 1u;
             const long v0 = (long)t * kTcN + col0;
