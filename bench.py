@@ -40,7 +40,7 @@ L2_FLUSH_BYTES = 512 << 20
 # DRAM bytes (read + written) per launch of draft_tc_kernel<1, bf16> on the headline
 # workload, from an ncu capture (ncu --set full, one launch); None once the kernel
 # changes, until it is captured again
-DRAFT_TC_TRAFFIC_BYTES = 142_572_032
+DRAFT_TC_TRAFFIC_BYTES = 138_496_512
 
 
 def parse():
