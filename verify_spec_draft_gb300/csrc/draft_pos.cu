@@ -311,23 +311,26 @@ __global__ void draft_pos_gather_kernel(const __grid_constant__ DraftParams p, c
     for (int w = lane; w < p.r / 8; w += 32) dst[w] = ok ? __ldg(src + w) : make_uint4(0u, 0u, 0u, 0u);
 }
 
-// One CTA of 8 warps per request: x_j and its outputs; x_j and U[x_j] for the next
-// position.  One wave of loads brings CTA c's two half records to thread c; a block merge
-// gives the row's maximum and sum.  At T=1 a block scan of the CTAs' weights (in index
-// order) finds the CTA range where the CDF crosses u * Z; every warp then finds the
-// 128-entry tile within that range from the tile records (the same loads, so the same
-// decision), computes 16 of its biased logits on CUDA cores (lane l takes the rank slice
-// [8l, 8l + 8) of each entry), and warp 0 scans them.
-constexpr int kPosDrawThreads = 32 * kDrawWarps;
-static_assert(kPosMaxCtas <= kPosDrawThreads, "a CTA record pair per thread");
+// One CTA of 4 warps per request: x_j and its outputs; x_j and U[x_j] for the next
+// position.  128-thread CTAs let 8 or more fit on an SM, so a batch of 1024 requests runs
+// in one wave.  One wave of loads brings CTA c's two half records to thread c % 128 (two
+// CTAs per thread); a block merge gives the row's maximum and sum.  At T=1 a block scan of
+// the CTAs' weights (in index order, the first 128 CTAs then the rest) finds the CTA
+// range where the CDF crosses u * Z; every warp then finds the 128-entry tile within that
+// range from the tile records (the same loads, so the same decision), computes 32 of its
+// biased logits on CUDA cores (lane l takes the rank slice [8l, 8l + 8) of each entry),
+// and warp 0 scans them.
+constexpr int kPosDrawWarps = 4;
+constexpr int kPosDrawThreads = 32 * kPosDrawWarps;
+static_assert(kPosMaxCtas <= 2 * kPosDrawThreads, "two CTA record pairs per thread");
 
 template <int TT>
-__global__ void __launch_bounds__(kPosDrawThreads, 4)
+__global__ void __launch_bounds__(kPosDrawThreads, 8)
     draft_pos_draw_kernel(const __grid_constant__ DraftParams p, const __grid_constant__ PosExtra e) {
-    constexpr int EPW = kDraftTile / kDrawWarps;   // entries of the tile per warp
+    constexpr int EPW = kDraftTile / kPosDrawWarps;   // entries of the tile per warp
     __shared__ float s_z[kDraftTile];
-    __shared__ float4 s_red[kDrawWarps];
-    __shared__ float s_wsum[kDrawWarps];
+    __shared__ float4 s_red[kPosDrawWarps];
+    __shared__ float s_wsum[kPosDrawWarps];
     __shared__ int s_first, s_last, s_x;
     __shared__ float s_tl;
     pdl_launch_dependents();   // the next position's tiles kernel may request its weights
@@ -349,12 +352,17 @@ __global__ void __launch_bounds__(kPosDrawThreads, 4)
         if (tid == 0) finish(-1, NAN, NAN, e.j == 1 ? SPEC_DEV_TOKEN : 0u);
         return;
     }
-    // one wave of loads: CTA tid's two half records, the U row of x_{j-1}
+    // one wave of loads: CTAs tid and tid + 128's two half records, the U row of x_{j-1}
     const float4* recs = p.cta_rec + (size_t)b * e.nC * 2;
-    RowAcc r0 = rowacc_empty(), r1 = rowacc_empty();
-    if (tid < e.nC) {
-        r0 = rowacc_unpack(__ldcg(&recs[2 * tid]));
-        r1 = rowacc_unpack(__ldcg(&recs[2 * tid + 1]));
+    const int ca = tid, cb = tid + kPosDrawThreads;
+    RowAcc ra0 = rowacc_empty(), ra1 = rowacc_empty(), rb0 = rowacc_empty(), rb1 = rowacc_empty();
+    if (ca < e.nC) {
+        ra0 = rowacc_unpack(__ldcg(&recs[2 * ca]));
+        ra1 = rowacc_unpack(__ldcg(&recs[2 * ca + 1]));
+    }
+    if (cb < e.nC) {
+        rb0 = rowacc_unpack(__ldcg(&recs[2 * cb]));
+        rb1 = rowacc_unpack(__ldcg(&recs[2 * cb + 1]));
     }
     const bool has = lane < (p.r >> 3);
     uint4 uw = make_uint4(0u, 0u, 0u, 0u);
@@ -362,14 +370,14 @@ __global__ void __launch_bounds__(kPosDrawThreads, 4)
     const float u = TT == 1 ? philox_uniform(p.seeds[b], (uint64_t)(p.b_base + b), (uint64_t)e.j, 0) : 0.0f;
     // the row's record
     {
-        const RowAcc w = warp_rowacc(rowacc_merge(r0, r1));
+        const RowAcc w = warp_rowacc(rowacc_merge(rowacc_merge(ra0, ra1), rowacc_merge(rb0, rb1)));
         if (lane == 0) s_red[warp] = rowacc_pack(w);
     }
     if (tid == 0) { s_first = e.nC; s_last = -1; }
     __syncthreads();
     RowAcc acc = rowacc_empty();
 #pragma unroll
-    for (int w = 0; w < kDrawWarps; ++w) acc = rowacc_merge(acc, rowacc_unpack(s_red[w]));
+    for (int w = 0; w < kPosDrawWarps; ++w) acc = rowacc_merge(acc, rowacc_unpack(s_red[w]));
     if (acc.bad || acc.mx == -INFINITY) {   // no distribution: the request ends here
         if (tid == 0) finish(-1, NAN, NAN, SPEC_DEV_NONFINITE);
         return;
@@ -382,17 +390,33 @@ __global__ void __launch_bounds__(kPosDrawThreads, 4)
     if constexpr (TT == 1) {
         const float thr = u * S;
         auto weight = [&](const RowAcc& r) { return r.mx == -INFINITY ? 0.0f : r.s * ex2(r.mx * kLog2e - M2); };
-        // level 1: the CTA ranges' weights in index order, a block scan
-        const float w = tid < e.nC ? weight(r0) + weight(r1) : 0.0f;
-        float incl = warp_inclusive_scan(w);
-        if (lane == 31) s_wsum[warp] = incl;
+        // level 1: the CTA ranges' weights in index order, a block scan over the first 128
+        // CTAs, then over the rest on top of their total
+        const float wa = ca < e.nC ? weight(ra0) + weight(ra1) : 0.0f;
+        const float wb = cb < e.nC ? weight(rb0) + weight(rb1) : 0.0f;
+        float ia = warp_inclusive_scan(wa), ib = warp_inclusive_scan(wb);
+        if (lane == 31) s_wsum[warp] = ia;
         __syncthreads();
-        for (int w2 = 0; w2 < warp; ++w2) incl += s_wsum[w2];
-        if (tid < e.nC && incl > thr) atomicMin(&s_first, tid);
-        if (tid < e.nC && w > 0.0f) atomicMax(&s_last, tid);
+        float tot_a = 0.0f;
+#pragma unroll
+        for (int w2 = 0; w2 < kPosDrawWarps; ++w2) {
+            const float v = s_wsum[w2];
+            if (w2 < warp) ia += v;
+            tot_a += v;
+        }
+        __syncthreads();   // s_wsum is rewritten
+        if (lane == 31) s_wsum[warp] = ib;
+        __syncthreads();
+        ib += tot_a;
+        for (int w2 = 0; w2 < warp; ++w2) ib += s_wsum[w2];
+        if (ca < e.nC && ia > thr) atomicMin(&s_first, ca);
+        if (cb < e.nC && ib > thr) atomicMin(&s_first, cb);
+        if (ca < e.nC && wa > 0.0f) atomicMax(&s_last, ca);
+        if (cb < e.nC && wb > 0.0f) atomicMax(&s_last, cb);
         __syncthreads();
         const int first = s_first;
-        if (tid == first) s_tl = thr - (incl - w);
+        if (ca == first) s_tl = thr - (ia - wa);
+        if (cb == first) s_tl = thr - (ib - wb);
         __syncthreads();
         const bool crossed = first < e.nC;
         const int cta = crossed ? first : max(0, s_last);
@@ -418,7 +442,8 @@ __global__ void __launch_bounds__(kPosDrawThreads, 4)
         }
         if (tile < 0) { tile = last_tile; tl = INFINITY; }
         tile = max(0, min(tile, p.n_tiles - 1));
-        // level 3: this warp's EPW biased logits of the tile, its Wt rows requested at once
+        // level 3: this warp's EPW biased logits of the tile: its Wt rows (contiguous)
+        // requested into L2 at once, then taken kZBatch at a time
         float uu[8];
         {
             const uint32_t a[4] = {uw.x, uw.y, uw.z, uw.w};
@@ -430,21 +455,21 @@ __global__ void __launch_bounds__(kPosDrawThreads, 4)
         }
         const bf16_t* lrow = static_cast<const bf16_t*>(p.logits) + out * p.V;
         const long e0 = (long)tile * kDraftTile + warp * EPW;
+        const long e1 = e0 + EPW < p.V ? e0 + EPW : p.V;
+        if (lane == 0 && e1 > e0) bulk_prefetch_l2(Wt + (size_t)e0 * p.r, (unsigned)((e1 - e0) * p.r * 2));
         const float zl = (lane < EPW && e0 + lane < p.V) ? load_one(lrow + e0 + lane) : 0.0f;
-        uint4 wr[2][kZBatch];   // two batches of Wt rows in flight
-#pragma unroll
-        for (int hb = 0; hb < 2; ++hb)
+#pragma unroll 1
+        for (int hb = 0; hb < EPW / kZBatch; ++hb) {
+            uint4 wr[kZBatch];
 #pragma unroll
             for (int qq = 0; qq < kZBatch; ++qq) {
                 const long v = e0 + hb * kZBatch + qq;
-                wr[hb][qq] = make_uint4(0u, 0u, 0u, 0u);
-                if (has && v < p.V) wr[hb][qq] = __ldg(reinterpret_cast<const uint4*>(Wt + (size_t)v * p.r) + lane);
+                wr[qq] = make_uint4(0u, 0u, 0u, 0u);
+                if (has && v < p.V) wr[qq] = __ldg(reinterpret_cast<const uint4*>(Wt + (size_t)v * p.r) + lane);
             }
 #pragma unroll
-        for (int hb = 0; hb < 2; ++hb)
-#pragma unroll
             for (int qq = 0; qq < kZBatch; ++qq) {
-                const uint32_t a[4] = {wr[hb][qq].x, wr[hb][qq].y, wr[hb][qq].z, wr[hb][qq].w};
+                const uint32_t a[4] = {wr[qq].x, wr[qq].y, wr[qq].z, wr[qq].w};
                 float part = 0.0f;
 #pragma unroll
                 for (int k2 = 0; k2 < 4; ++k2) {
@@ -456,6 +481,7 @@ __global__ void __launch_bounds__(kPosDrawThreads, 4)
                 const float zq = __shfl_sync(0xffffffffu, zl, qi);
                 if (lane == 0) s_z[warp * EPW + qi] = e0 + qi < p.V ? zq + part : -INFINITY;
             }
+        }
         __syncthreads();
         if (warp == 0) {
             float z[4];
