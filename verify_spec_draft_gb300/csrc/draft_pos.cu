@@ -28,7 +28,7 @@
 //              rows are 32-byte aligned), adds them,
 //              folds the half-tile's 128 biased logits into the row's record for that
 //              128-entry tile, and into its running record over the CTA's tiles.
-//   draft_pos_draw_kernel   a group of 8 warps per request merges the records and takes
+//   draft_pos_draw_kernel   a CTA of 4 warps per request merges the records and takes
 //     x_j: the argmax, or the T=1 draw (the CTA range, then the 128-entry tile, then
 //     that tile's biased logits recomputed on CUDA cores and scanned), writes the
 //     outputs and U[x_j], the next position's A row.
