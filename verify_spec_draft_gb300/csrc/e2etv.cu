@@ -186,10 +186,15 @@ __device__ __forceinline__ void slice_stats(const bf16_t* row, int ncol, Stat2& 
     int lbad = 0;
     for (int k0 = lane * 8; k0 < ncol; k0 += 256 * B) {
         uint4 w[B];
+        if ((k0 - lane * 8) + 256 * B <= ncol) {   // the warp's whole batch lies in the slice
 #pragma unroll
-        for (int g = 0; g < B; ++g) {
-            const int k = k0 + 256 * g;
-            w[g] = k < ncol ? ld16p<STAGED>(row + k, pol) : make_uint4(ninf, ninf, ninf, ninf);
+            for (int g = 0; g < B; ++g) w[g] = ld16p<STAGED>(row + k0 + 256 * g, pol);
+        } else {
+#pragma unroll
+            for (int g = 0; g < B; ++g) {
+                const int k = k0 + 256 * g;
+                w[g] = k < ncol ? ld16p<STAGED>(row + k, pol) : make_uint4(ninf, ninf, ninf, ninf);
+            }
         }
         uint32_t mx2 = ninf;
 #pragma unroll
@@ -234,12 +239,21 @@ __device__ __forceinline__ void slice_overlap(const bf16_t* tr, const bf16_t* dr
     const f2x cl = f2_pack(kLog2e, kLog2e), cp = f2_pack(-lse_p, -lse_p), cq = f2_pack(-lse_q, -lse_q);
     for (int k0 = lane * 8; k0 < ncol; k0 += 256 * B) {
         uint4 wl[B], wd[B];
+        const bool full = (k0 - lane * 8) + 256 * B <= ncol;   // the warp's whole batch lies in the slice
+        if (full) {
 #pragma unroll
-        for (int g = 0; g < B; ++g) {
-            const int k = k0 + 256 * g;
-            const bool in = k < ncol;
-            wl[g] = in ? ld16p<STAGED>(tr + k, pol_t) : make_uint4(ninf, ninf, ninf, ninf);
-            wd[g] = in ? ld16p<STAGED>(dr + k, pol_d) : make_uint4(ninf, ninf, ninf, ninf);
+            for (int g = 0; g < B; ++g) {
+                wl[g] = ld16p<STAGED>(tr + k0 + 256 * g, pol_t);
+                wd[g] = ld16p<STAGED>(dr + k0 + 256 * g, pol_d);
+            }
+        } else {
+#pragma unroll
+            for (int g = 0; g < B; ++g) {
+                const int k = k0 + 256 * g;
+                const bool in = k < ncol;
+                wl[g] = in ? ld16p<STAGED>(tr + k, pol_t) : make_uint4(ninf, ninf, ninf, ninf);
+                wd[g] = in ? ld16p<STAGED>(dr + k, pol_d) : make_uint4(ninf, ninf, ninf, ninf);
+            }
         }
 #pragma unroll
         for (int g = 0; g < B; ++g) {
@@ -258,7 +272,7 @@ __device__ __forceinline__ void slice_overlap(const bf16_t* tr, const bf16_t* dr
                 bits |= (b1 ? 2u : 0u) << (2 * h);
             }
             const int k = k0 + 256 * g;
-            if (k < ncol) mask[k >> 3] = (uint8_t)bits;
+            if (full || k < ncol) mask[k >> 3] = (uint8_t)bits;
         }
     }
     const float2 A = f2_unpack(sa), Sx = f2_unpack(ss);
@@ -472,46 +486,53 @@ __global__ void __launch_bounds__(kThreads, STAGED ? 2 : 4) e2etv_kernel(E2etvPa
             p.branch_sum[n] = NAN;
         }
 
-        // sweep 3: gradient w.r.t. the draft logits, rounded once to bf16; rows read from
-        // global memory keep U of a thread's 16-byte words in flight.  Item idx is group
-        // gi of row i (idx = i * ng + gi); each of a thread's U items advances by a fixed
-        // stride, so its (row, group) is stepped forward instead of divided out.
+        // sweep 3: gradient w.r.t. the draft logits, rounded once to bf16.  A warp item is
+        // 32*U consecutive 8-entry groups of one row (a lane takes U of them, 32 groups
+        // apart, with all their loads in flight); the warps step through the items of the
+        // slice's Wb rows, so a row's constants and addresses are set once per item.
         {
-            const int ng = (ncol + 7) / 8;
-            const int total = Wb * ng;
             constexpr int U = (!STAGED && VEC) ? 4 : 1;
-            const int step = (int)blockDim.x * U;
-            int ri[U], gi[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int idx = (int)threadIdx.x + u * (int)blockDim.x;
-                ri[u] = ng > 0 ? idx / ng : 0;
-                gi[u] = idx - ri[u] * ng;
-            }
+            const int ng = (ncol + 7) / 8;
+            const int parts = (ng + 32 * U - 1) / (32 * U);
+            const int total = Wb * parts;
             const f2x cl = f2_pack(kLog2e, kLog2e);
-            for (int idx0 = threadIdx.x; idx0 < total; idx0 += step) {
+            int i = 0, pt = warp;
+            if (parts > 0)
+                while (pt >= parts) { pt -= parts; ++i; }
+            for (int item = warp; item < total; item += kWarps) {
+                const bf16_t* src = rw.drf + (size_t)i * rw.stride;
+                uint16_t* dst = p.grad_out + ((size_t)n * Wb + i) * V + c0;
+                const int g0 = pt * 32 * U + lane;
                 uint4 wdu[U];
+                const bool full = (pt + 1) * 32 * U <= ng;   // the whole item lies in the slice
+                if (full && !bad_branch) {
 #pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int idx = idx0 + u * (int)blockDim.x;
-                    wdu[u] = make_uint4(0u, 0u, 0u, 0u);
-                    if (idx < total && !bad_branch) {
-                        const int i = ri[u], k = gi[u] * 8;
-                        wdu[u] = VEC ? ld16p<STAGED>(rw.drf + (size_t)i * rw.stride + k, pol_last)
-                                     : group8<STAGED, VEC>(rw.drf + (size_t)i * rw.stride, k, ncol);
+                    for (int u = 0; u < U; ++u) {
+                        const int gq = g0 + 32 * u;
+                        wdu[u] = VEC ? ld16p<STAGED>(src + (size_t)gq * 8, pol_last) : group8<STAGED, VEC>(src, gq * 8, ncol);
+                    }
+                } else {
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const int gq = g0 + 32 * u;
+                        wdu[u] = make_uint4(0u, 0u, 0u, 0u);
+                        if (gq < ng && !bad_branch)
+                            wdu[u] = VEC ? ld16p<STAGED>(src + (size_t)gq * 8, pol_last) : group8<STAGED, VEC>(src, gq * 8, ncol);
                     }
                 }
+                const uint8_t* mrow = s_mask + (size_t)i * ngroups8;
+                const f2x* ctab = s_ctab[i];
+                const float nl = -s_lse[Wb + i];
+                const f2x cq = f2_pack(nl, nl);
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
-                    const int idx = idx0 + u * (int)blockDim.x;
-                    if (idx < total) {
-                        const int i = ri[u], k = gi[u] * 8;
+                    const int gq = g0 + 32 * u;
+                    if (full || gq < ng) {
+                        const int k = gq * 8;
                         uint4 out = make_uint4(0u, 0u, 0u, 0u);
                         if (!bad_branch) {
                             const uint4 wd = wdu[u];
-                            const uint32_t bits = s_mask[(size_t)i * ngroups8 + (k >> 3)];
-                            const f2x cq = f2_pack(-s_lse[Wb + i], -s_lse[Wb + i]);
-                            const f2x* ctab = s_ctab[i];
+                            const uint32_t bits = mrow[gq];
                             const uint32_t d4[4] = {wd.x, wd.y, wd.z, wd.w};
                             uint32_t o4[4];
 #pragma unroll
@@ -523,21 +544,20 @@ __global__ void __launch_bounds__(kThreads, STAGED ? 2 : 4) e2etv_kernel(E2etvPa
                             }
                             out = make_uint4(o4[0], o4[1], o4[2], o4[3]);
                         }
-                        uint16_t* dst = p.grad_out + ((size_t)n * Wb + i) * V + c0 + k;
+                        uint16_t* d = dst + k;
                         if (VEC) {
                             asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};"
-                                         :: "l"(dst), "r"(out.x), "r"(out.y), "r"(out.z), "r"(out.w) : "memory");
+                                         :: "l"(d), "r"(out.x), "r"(out.y), "r"(out.z), "r"(out.w) : "memory");
                         } else {
                             const uint32_t o4[4] = {out.x, out.y, out.z, out.w};
 #pragma unroll
                             for (int e = 0; e < 8; ++e)
-                                if (k + e < ncol) dst[e] = (uint16_t)((o4[e >> 1] >> (16 * (e & 1))) & 0xffffu);
+                                if (k + e < ncol) d[e] = (uint16_t)((o4[e >> 1] >> (16 * (e & 1))) & 0xffffu);
                         }
                     }
-                    // the next item of slot u: step groups forward, wrapping into later rows
-                    gi[u] += step;
-                    while (gi[u] >= ng) { gi[u] -= ng; ++ri[u]; }
                 }
+                pt += kWarps;
+                while (pt >= parts) { pt -= parts; ++i; }
             }
         }
         __syncthreads();                                   // draft rows no longer read
