@@ -33,11 +33,17 @@ __device__ __forceinline__ uint4 partial_words(const bf16_t* row, long e0, long 
     return make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
 }
 
-// Two 16-byte words at p (32-byte aligned) in one load: a whole 32-byte sector.
+// Two 16-byte words at p (32-byte aligned) in one load: a whole 32-byte sector.  The
+// rows read this way are read once, so their lines are the first L2 evicts
+// (evict_first): the stream then replaces its own clean lines instead of writing back
+// whatever dirty lines L2 held before it.  The policy asm has no side effects, so the
+// compiler creates it once per loop, not per load.
 __device__ __forceinline__ void ld_sector(const void* p, uint4& a, uint4& b) {
-    asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+    uint64_t pol;
+    asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    asm volatile("ld.global.nc.L2::cache_hint.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], %9;"
                  : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
-                 : "l"(p));
+                 : "l"(p), "l"(pol));
 }
 
 template <typename T, int NW>
