@@ -55,7 +55,9 @@ __device__ __forceinline__ float fmax_nan_f(float a, float b) {
 template <typename LT> struct LWords { static constexpr int N = 32 * (int)sizeof(LT) / 16; };
 
 // L32: the row's bytes are 32-byte aligned and V is a multiple of 32 bytes' worth of
-// entries, so the words come two at a time, one 32-byte load (a whole sector) each.
+// entries, so the words come two at a time, one 32-byte load (a whole sector) each.  A
+// thread reads along its own row, so an L2 miss fetches the row's whole 256-byte block
+// (`L2::256B`), which the thread's next loads then find in L2.
 template <typename LT, bool L32 = false>
 __device__ __forceinline__ void load_l32(const LT* row, long v0, long V, uint4 (&w)[LWords<LT>::N]) {
     constexpr int N = LWords<LT>::N, EPV = 32 / N;
@@ -65,7 +67,7 @@ __device__ __forceinline__ void load_l32(const LT* row, long v0, long V, uint4 (
         for (int i = 0; i < N; i += 2) {
             const long v = v0 + EPV * i;
             if (v + 2 * EPV <= V) {
-                asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                asm volatile("ld.global.nc.L2::256B.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                              : "=r"(w[i].x), "=r"(w[i].y), "=r"(w[i].z), "=r"(w[i].w), "=r"(w[i + 1].x),
                                "=r"(w[i + 1].y), "=r"(w[i + 1].z), "=r"(w[i + 1].w)
                              : "l"(row + v));
