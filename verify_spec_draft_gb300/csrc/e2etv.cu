@@ -15,8 +15,8 @@
 // one bit per entry, so the target rows are free after it.
 //
 // Two plans.  Rows 16-byte aligned, many branches: the sweeps read the rows from
-// global memory, sweep 1 from DRAM and sweeps 2 and 3 mostly from L2, each lane
-// keeping several 16-byte words in flight; about 18 groups of a few dozen CTAs (four
+// global memory, sweep 1 from DRAM and sweeps 2 and 3 about half from L2, each lane
+// keeping several 16-byte words in flight; about two dozen groups of a few dozen CTAs (four
 // per SM) keep that many branches in flight, so one group's barrier waits overlap
 // other groups' sweeps.  Otherwise: each CTA stages its slice of all 2*Wb rows in
 // shared memory with TMA bulk copies (the next branch's target rows are fetched while
@@ -646,7 +646,7 @@ cudaError_t e2etv_launch(E2etvParams& p, void* ws, cudaStream_t stream) {
 
     const int sms = device_sm_count();
     // Rows 16-byte aligned: rows read from global memory (sweep 1 from DRAM, sweeps 2
-    // and 3 mostly from L2), kE2InFlightBytes of branches in flight (a branch is 2*Wb
+    // and 3 about half from L2), kE2InFlightBytes of branches in flight (a branch is 2*Wb
     // rows of V bf16 values), each on a group of CTAs, as many CTAs per SM as fit (up
     // to kE2MaxPerSm).  With fewer than eight such groups the plan below is used.
     if (p.vec_ok) {
