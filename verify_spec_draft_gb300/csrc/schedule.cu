@@ -126,50 +126,77 @@ __global__ void __launch_bounds__(kSchedThreads) verify_budget_kernel(const floa
     }
     __syncthreads();
 
-    // inclusive prefix sums of the sorted P over the first N (each thread a run of R)
+    // inclusive prefix sums of the sorted P over the first N (each thread a run of R).
+    // This GPU's float64 pipe is slow, so only warps holding candidates add, and the
+    // warps' offsets come from one shuffle scan of their totals by warp 0.
     const int R = (M + nt - 1) / nt;
     const int r0 = tid * R, r1 = min(N, r0 + R);
-    double local = 0.0;
-    for (int i = r0; i < r1; ++i) local += sp[i];
-    double inc = local;   // thread-level inclusive scan of the run totals
+    const bool wlive = warp * 32 * R < N;   // this warp's runs hold candidates
+    double local = 0.0, excl = 0.0;
+    if (wlive) {
+        for (int i = r0; i < r1; ++i) local += sp[i];
+        double inc = local;   // thread-level inclusive scan of the run totals
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const double y = __shfl_up_sync(0xffffffffu, inc, o);
-        if (lane >= o) inc += y;
+        for (int o = 1; o < 32; o <<= 1) {
+            const double y = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += y;
+        }
+        excl = __shfl_up_sync(0xffffffffu, inc, 1);
+        if (lane == 0) excl = 0.0;
+        if (lane == 31) s_part[warp] = inc;
+    } else if (lane == 0) {
+        s_part[warp] = 0.0;
     }
-    if (lane == 31) s_part[warp] = inc;
     __syncthreads();
-    double off = 0.0;
-    for (int w = 0; w < warp; ++w) off += s_part[w];
-    double run = off + inc - local;   // exclusive prefix of this thread's run
-    for (int i = r0; i < r1; ++i) { run += sp[i]; sp[i] = run; }
+    if (warp == 0) {   // exclusive scan of the warp totals
+        const double tot = lane < nt / 32 ? s_part[lane] : 0.0;
+        double inc = tot;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const double y = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += y;
+        }
+        double ex = __shfl_up_sync(0xffffffffu, inc, 1);
+        if (lane == 0) ex = 0.0;
+        __syncwarp();
+        if (lane < nt / 32) s_part[lane] = ex;
+    }
+    __syncthreads();
+    if (wlive) {
+        double run = s_part[warp] + excl;   // exclusive prefix of this thread's run
+        for (int i = r0; i < r1; ++i) { run += sp[i]; sp[i] = run; }
+    }
     __syncthreads();
 
     // k*: the best E(k) / t[k] over k = 0..K (smallest k on ties), or K
     if (cost == nullptr) {
         if (tid == 0) s_kstar = K;
     } else {
-        double best = -DBL_MAX;
-        int bk = INT_MAX;
-        for (int k = tid; k <= K; k += nt) {
-            const float t = cost[k];
-            if (!(t > 0.0f) || isinf(t)) continue;
-            const double E = (double)B + (k > 0 ? sp[k - 1] : 0.0);
-            const double obj = E / (double)t;
-            if (obj > best || (obj == best && k < bk)) { best = obj; bk = k; }
-        }
+        // only the warps that hold some k take part (k = tid, tid + nt, ...)
+        const int nwk = min(nt / 32, K / 32 + 1);
+        if (warp < nwk) {
+            double best = -DBL_MAX;
+            int bk = INT_MAX;
+            for (int k = tid; k <= K; k += nt) {
+                const float t = cost[k];
+                if (!(t > 0.0f) || isinf(t)) continue;
+                const double E = (double)B + (k > 0 ? sp[k - 1] : 0.0);
+                const double obj = E / (double)t;
+                if (obj > best || (obj == best && k < bk)) { best = obj; bk = k; }
+            }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const double ob = __shfl_xor_sync(0xffffffffu, best, o);
-            const int kb = __shfl_xor_sync(0xffffffffu, bk, o);
-            if (ob > best || (ob == best && kb < bk)) { best = ob; bk = kb; }
+            for (int o = 16; o > 0; o >>= 1) {
+                const double ob = __shfl_xor_sync(0xffffffffu, best, o);
+                const int kb = __shfl_xor_sync(0xffffffffu, bk, o);
+                if (ob > best || (ob == best && kb < bk)) { best = ob; bk = kb; }
+            }
+            if (lane == 0) { s_bobj[warp] = best; s_bk[warp] = bk; }
         }
-        if (lane == 0) { s_bobj[warp] = best; s_bk[warp] = bk; }
         __syncthreads();
         if (tid == 0) {
             double b0 = -DBL_MAX;
             int k0 = INT_MAX;
-            for (int w = 0; w < nt / 32; ++w)
+            for (int w = 0; w < nwk; ++w)
                 if (s_bobj[w] > b0 || (s_bobj[w] == b0 && s_bk[w] < k0)) { b0 = s_bobj[w]; k0 = s_bk[w]; }
             s_kstar = k0 == INT_MAX ? 0 : k0;   // no usable cost entry: verify nothing
         }
