@@ -144,6 +144,7 @@ struct TopkParams {
     unsigned long long* part;  // [rows][kTopkPieces][kTopkMax] the pieces' largest keys
     unsigned* part_bad;        // [rows][kTopkPieces]
     unsigned* row_done;        // [rows] pieces finished (returned to 0 by the merge)
+    unsigned long long* row_thr;   // [rows] the best bound any piece has published (0 after the merge)
 };
 constexpr int kTopkPieces = 8;   // most CTAs that share one row of spec_verify_topk
 size_t verify_topk_workspace_bytes(int B, int gamma);

@@ -11,14 +11,16 @@
 // prefix, in descending order, whose running sum reaches top_p; renormalised again.  Only
 // a row's top k entries matter, so no row-wide softmax is needed:
 //
-//   topk_rows_kernel   one CTA per row (target and draft rows in one grid) streams it
-//                      (HBM-bound).  Each warp keeps the 32 largest 64-bit keys it has
+//   topk_rows_kernel   persistent CTAs stream the rows (target and draft rows in one
+//                      grid), each row in at most 6 pieces on consecutive CTAs; the CTA
+//                      that finishes a row's last piece merges the pieces.  Each warp keeps the 32 largest 64-bit keys it has
 //                      seen (ordered value high, inverted index low: a larger key is a
 //                      larger value or, on a tie, a lower index) as a sorted list spread
 //                      over its lanes.  A lane looks inside its 8-entry groups only when a
-//                      group's packed maximum reaches the threshold, the larger of the
-//                      warp's k-th key and the CTA's best published k-th key (no entry
-//                      below it can be among the row's k largest); the threshold starts
+//                      group's packed maximum reaches the threshold, the largest of the
+//                      warp's k-th key, the CTA's best published bound and the best bound
+//                      any CTA sharing the row has published through global memory (no
+//                      entry below it can be among the row's k largest); the threshold starts
 //                      at the k-th largest lane maximum of the first item.  The entries
 //                      above it go to a per-warp buffer (one prefix over the lanes) and are
 //                      inserted one by one.  NaN or +inf marks the row bad (it has no
@@ -43,6 +45,13 @@ constexpr int kTopkWarps = kTopkThreads / 32;
 template <typename TT, typename DT> struct TopkOcc {
     static constexpr int N = sizeof(TT) == 2 && sizeof(DT) == 2 ? 4 : 2;
 };
+
+// A relaxed load of the row's published bound (other CTAs raise it with atomicMax).
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
 
 // The CTA whose item range [c*I/G, (c+1)*I/G) holds item i.
 __device__ __forceinline__ long topk_cta_of(long i, long I, long G) { return ((i + 1) * G - 1) / I; }
@@ -109,6 +118,9 @@ __device__ __forceinline__ void topk_piece(const TopkParams& p, const T* rowp, l
     uint4 cur[NW], nxt[NW];
     load_words_il<T, NW>(cur, rowp, V, il_seg(c0), vec);
     unsigned long long mth = 0ull;   // the warp's m-th key, as last published
+    // the row's bound from every piece (lane 0): requested one chunk ahead of its use,
+    // and raised by this warp when its own bound passes it
+    unsigned long long gthr = lane == 0 ? ld_relaxed_u64(&p.row_thr[row]) : 0ull;
     for (int c = c0; c < c1; ++c) {
         if (c + 1 < c1) load_words_il<T, NW>(nxt, rowp, V, il_seg(c + 1), vec);
         float g[4];   // the maxima of this lane's four 8-entry groups (NaN if any is NaN)
@@ -145,7 +157,11 @@ __device__ __forceinline__ void topk_piece(const TopkParams& p, const T* rowp, l
         // the CTA's best k-th key, read once and broadcast: every lane must see the same
         // threshold (the insertions below are warp-collective)
         unsigned long long st_l = 0ull;
-        if (lane == 0) st_l = *(volatile unsigned long long*)&s_thr;
+        if (lane == 0) {
+            st_l = *(volatile unsigned long long*)&s_thr;
+            st_l = gthr > st_l ? gthr : st_l;
+            gthr = ld_relaxed_u64(&p.row_thr[row]);   // for the next chunk
+        }
         const unsigned long long shared_thr = shfl_u64(st_l, 0);
         if (shared_thr > thr) {
             thr = shared_thr;
@@ -196,6 +212,7 @@ __device__ __forceinline__ void topk_piece(const TopkParams& p, const T* rowp, l
                     bound = lo > bound ? lo : bound;
                 }
                 if (bound > *(volatile unsigned long long*)&s_thr) atomicMax(&s_thr, bound);
+                if (bound > gthr) atomicMax(&p.row_thr[row], bound);   // every piece of the row may use it
             }
             mth = mt;
         }
@@ -247,6 +264,7 @@ __device__ __forceinline__ void topk_piece(const TopkParams& p, const T* rowp, l
     if (q == 0) {
         p.bad[row] = rowbad ? 1u : 0u;
         p.row_done[row] = 0u;
+        p.row_thr[row] = 0ull;   // every other piece of the row has finished reading it
     }
 }
 
@@ -370,7 +388,8 @@ size_t verify_topk_workspace_bytes(int B, int gamma) {
     off = topk_align(off + rows * sizeof(unsigned));                                      // bad
     off = topk_align(off + rows * kTopkPieces * kTopkMax * sizeof(unsigned long long));   // part
     off = topk_align(off + rows * kTopkPieces * sizeof(unsigned));                        // part_bad
-    return topk_align(off + rows * sizeof(unsigned));                                     // row_done
+    off = topk_align(off + rows * sizeof(unsigned));                                      // row_done
+    return topk_align(off + rows * sizeof(unsigned long long));                           // row_thr
 }
 
 template <typename TT, typename DT>
@@ -402,6 +421,8 @@ cudaError_t verify_topk_launch(TopkParams& p, void* ws, cudaStream_t stream) {
     p.part_bad = reinterpret_cast<unsigned*>(w + off);
     off = topk_align(off + rows * kTopkPieces * sizeof(unsigned));
     p.row_done = reinterpret_cast<unsigned*>(w + off);
+    off = topk_align(off + rows * sizeof(unsigned));
+    p.row_thr = reinterpret_cast<unsigned long long*>(w + off);
     const bool vt = ((size_t)p.V * (p.tdt == SPEC_BF16 ? 2 : 4)) % 16 == 0;
     const bool vd = ((size_t)p.V * (p.ddt == SPEC_BF16 ? 2 : 4)) % 16 == 0;
     cudaError_t e;
