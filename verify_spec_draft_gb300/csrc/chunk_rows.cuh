@@ -85,6 +85,18 @@ __device__ __forceinline__ void load_words_il(uint4 (&w)[NW], const T* row, long
     }
 }
 
+// The same for a segment that lies wholly in the row (vec_ok, seg + 1024 <= V).
+template <typename T, int NW>
+__device__ __forceinline__ void load_words_il_full(uint4 (&w)[NW], const T* row, long seg) {
+    constexpr int EPV = 16 / (int)sizeof(T);
+    constexpr int WPG = 8 / EPV;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int h = 0; h < WPG; ++h)
+            w[j * WPG + h] = __ldg(reinterpret_cast<const uint4*>(row + il_entry(seg, 8 * j) + h * EPV));
+}
+
 // The sector-interleaved layout, for rows that start on 32 bytes: lane l of warp w holds
 // the 32-byte groups j * 32 + l (j < NW / 2) of the warp's 1024-entry segment, 16 bf16
 // or 8 float32 entries each, one load per group, so each load instruction of a warp

@@ -122,7 +122,11 @@ __device__ __forceinline__ void topk_piece(const TopkParams& p, const T* rowp, l
     // and raised by this warp when its own bound passes it
     unsigned long long gthr = lane == 0 ? ld_relaxed_u64(&p.row_thr[row]) : 0ull;
     for (int c = c0; c < c1; ++c) {
-        if (c + 1 < c1) load_words_il<T, NW>(nxt, rowp, V, il_seg(c + 1), vec);
+        if (c + 1 < c1) {
+            const long sg = il_seg(c + 1);
+            if (vec && sg + 1024 <= V) load_words_il_full<T, NW>(nxt, rowp, sg);   // the whole segment in the row
+            else load_words_il<T, NW>(nxt, rowp, V, sg, vec);
+        }
         float g[4];   // the maxima of this lane's four 8-entry groups (NaN if any is NaN)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
