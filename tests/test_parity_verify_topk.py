@@ -96,3 +96,31 @@ def test_config4_full_size(spec):
     same = _compare(out, ref, max_near=B * G // 64)
     assert same >= B - B * G // 64
     assert vsd.device_status(out["ws"]) == 0
+
+
+def test_workspace_reuse_rows_in_pieces(spec):
+    """Rows long enough to be split over several CTAs, whose pieces share a bound through
+    the workspace.  A second call with the same workspace, on rows whose logits all lie
+    lower, must start from no bound: a bound left from the first call would lie above
+    every key of the second and empty its lists.  Both calls against the oracle, and the
+    second against a call with a fresh workspace."""
+    B, G, V, k, top_p = 4, 3, 200_000, 20, 0.95
+    dev = torch.device("cuda")
+    seeds = synth.seeds_for(B, 9)
+    ws = None
+    for shift in (0.0, -5.0):
+        t, d = synth.target_and_draft(B, G, V, "zipf", 0.7, torch.float32, seed=321)
+        t, d = (t + shift).to(torch.bfloat16), (d + shift).to(torch.bfloat16)
+        tok = synth.draft_tokens(d.float(), 1, seed=17)
+        args = (t.to(dev), d.to(dev), tok.to(dev).contiguous(), k, top_p, seeds.to(dev))
+        out = vsd.verify_topk(*args, ws=ws)
+        torch.cuda.synchronize()
+        ref = ot.verify_filtered(t.double().numpy(), d.double().numpy(), tok.numpy(), seeds.numpy(), k, top_p)
+        _compare(out, ref)
+        assert vsd.device_status(out["ws"]) == 0
+        if ws is not None:
+            fresh = vsd.verify_topk(*args)
+            torch.cuda.synchronize()
+            for key in ("n", "committed", "bonus"):
+                assert torch.equal(out[key], fresh[key])
+        ws = out["ws"]
